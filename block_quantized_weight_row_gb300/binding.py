@@ -1,0 +1,190 @@
+"""Thin Python binding over libbq.so (the C ABI in include/bq.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. Tensors must be CUDA tensors; the binding passes their device
+pointers, the torch current stream and a torch-allocated workspace to the
+library, and raises BQError on a nonzero status. There is no CPU fallback: if
+libbq.so is missing or fails to load, every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+Q4_0 = 2
+Q8_0 = 8
+QK = 32
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libbq.so"
+
+_STATUS = {0: "BQ_OK", -1: "BQ_ERR_INVALID_ARG", -2: "BQ_ERR_SHAPE", -3: "BQ_ERR_UNSUPPORTED",
+           -4: "BQ_ERR_ALIGN", -5: "BQ_ERR_CUDA", -6: "BQ_ERR_TIMEOUT", -7: "BQ_ERR_WORKSPACE"}
+
+
+class BQError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+_lib = None
+_ws = {}  # device index -> torch.uint8 workspace tensor
+
+
+def lib():
+    """Load libbq.so (built in-tree by build.py); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run __graft_entry__.build() "
+                          "(the CUDA path has no fallback)")
+    L = ctypes.CDLL(path)
+    i, i64, vp, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    sig = {
+        "bq_quantize_rows": ([i, vp, vp, i64, i64], i),
+        "bq_dequantize_rows": ([i, vp, vp, i64, i64], i),
+        "bq_gemv": ([i, vp, vp, vp, i64, i64], i),
+        "bq_gemm": ([i, vp, vp, vp, i64, i64, i64], i),
+        "bq_kv_quantize": ([i, vp, vp, vp, i64, i64, i64], i),
+        "bq_block_dots": ([i, vp, vp, vp, i64, i64], i),
+        "bq_set_stream": ([vp], i),
+        "bq_get_stream": ([], vp),
+        "bq_set_workspace": ([vp, sz], i),
+        "bq_workspace_size": ([i, i64, i64, i64], sz),
+        "bq_last_error": ([], ctypes.c_char_p),
+        "bq_block_bytes": ([i], i),
+        "bq_device_status": ([], i),
+        "bq_version": ([], i),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes, f.restype = args, res
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = lib().bq_last_error()
+        raise BQError(status, f"{what}: {msg.decode() if msg else ''}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _prep(device):
+    """Point the library at torch's current stream on `device`."""
+    L = lib()
+    s = torch.cuda.current_stream(device)
+    _check(L.bq_set_stream(ctypes.c_void_p(s.cuda_stream)), "bq_set_stream")
+    return L
+
+
+def _workspace(device, nbytes: int):
+    """Grow (never shrink) a torch-owned workspace and hand it to the library."""
+    idx = torch.device(device).index or 0
+    ws = _ws.get(idx)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws[idx] = ws
+    _check(lib().bq_set_workspace(_ptr(ws), ws.numel()), "bq_set_workspace")
+    return ws
+
+
+def _cuda(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def block_bytes(t: int) -> int:
+    return int(lib().bq_block_bytes(t))
+
+
+def quantize_rows(t: int, src: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32 (rows, cols) -> uint8 (rows, cols/32*block_bytes)."""
+    _cuda(src, "src")
+    if src.dtype != torch.float32:
+        raise TypeError("src must be float32")
+    x = src.reshape(-1, src.shape[-1]) if src.dim() != 2 else src
+    R, C = x.shape
+    if out is None:
+        out = torch.empty((R, (C // QK) * max(block_bytes(t), 1)), dtype=torch.uint8, device=src.device)
+    L = _prep(src.device)
+    _check(L.bq_quantize_rows(t, _ptr(x), _ptr(out), R, C), "bq_quantize_rows")
+    return out
+
+
+def dequantize_rows(t: int, blocks: torch.Tensor, cols: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    _cuda(blocks, "blocks")
+    nbr = (cols // QK) * block_bytes(t)
+    R = blocks.numel() // nbr if nbr else 0
+    if out is None:
+        out = torch.empty((R, cols), dtype=torch.float32, device=blocks.device)
+    L = _prep(blocks.device)
+    _check(L.bq_dequantize_rows(t, _ptr(blocks), _ptr(out), R, cols), "bq_dequantize_rows")
+    return out
+
+
+def gemv(t: int, w_blocks: torch.Tensor, x: torch.Tensor, M: int, K: int,
+         out: torch.Tensor | None = None) -> torch.Tensor:
+    """y[M] = W (M x K, blocks of type t) . x[K] (fp32, quantized to Q8_0 in-kernel)."""
+    _cuda(w_blocks, "w_blocks")
+    _cuda(x, "x")
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=x.device)
+    L = _prep(x.device)
+    _check(L.bq_gemv(t, _ptr(w_blocks), _ptr(x), _ptr(out), M, K), "bq_gemv")
+    return out
+
+
+def gemm(t: int, w_blocks: torch.Tensor, X: torch.Tensor, M: int, N: int, K: int,
+         out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y (N x M) = X (N x K fp32, quantized to Q8_0) . W^T (W: M x K blocks)."""
+    _cuda(w_blocks, "w_blocks")
+    _cuda(X, "X")
+    if out is None:
+        out = torch.empty((N, M), dtype=torch.float32, device=X.device)
+    L = _prep(X.device)
+    _workspace(X.device, int(L.bq_workspace_size(t, M, N, K)))
+    _check(L.bq_gemm(t, _ptr(w_blocks), _ptr(X), _ptr(out), M, N, K), "bq_gemm")
+    return out
+
+
+def kv_quantize(t: int, rows: torch.Tensor, bias: torch.Tensor | None,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """rows: (n_tokens, n_kv_heads, head_dim) fp32; bias: (n_kv_heads, head_dim) or None."""
+    _cuda(rows, "rows")
+    if bias is not None:
+        _cuda(bias, "bias")
+    T, H, D = rows.shape
+    if out is None:
+        out = torch.empty((T, H, (D // QK) * max(block_bytes(t), 1)), dtype=torch.uint8, device=rows.device)
+    L = _prep(rows.device)
+    _check(L.bq_kv_quantize(t, _ptr(rows), _ptr(bias), _ptr(out), T, H, D), "bq_kv_quantize")
+    return out
+
+
+def block_dots(t: int, w_blocks: torch.Tensor, xq_blocks: torch.Tensor, M: int, K: int) -> torch.Tensor:
+    """Test export: int32 (M, K/32) per-block integer dots of W against Q8_0 blocks xq."""
+    _cuda(w_blocks, "w_blocks")
+    _cuda(xq_blocks, "xq_blocks")
+    out = torch.empty((M, K // QK), dtype=torch.int32, device=w_blocks.device)
+    L = _prep(w_blocks.device)
+    _check(L.bq_block_dots(t, _ptr(w_blocks), _ptr(xq_blocks), _ptr(out), M, K), "bq_block_dots")
+    return out
+
+
+def device_status() -> int:
+    """Synchronize the current stream and return (and clear) the device error word."""
+    return int(lib().bq_device_status())

@@ -1,0 +1,337 @@
+/*
+ * bq_oracle.c — plain, slow, scalar CPU oracle for block-quantized weight rows.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg; never by the product path. It shares no code
+ * with the CUDA library (no headers, helpers, tables or constants).
+ *
+ * Build: plain C11, no SIMD intrinsics, no fast-math, no FP contraction
+ * (see oracle/build.py), so every float operation below is one IEEE
+ * binary32 (or binary64 where stated) operation in program order.
+ *
+ * Sources (pages on llama.cpp; citations give page title and section):
+ *   [FMT4] llama.cpp 原理：如何在普通硬件跑本地大模型, §量化：内存真正去哪了 —
+ *          Q4_0: groups of 32 weights, one FP16 scale, each weight a 4-bit
+ *          integer; 18 bytes per 32 weights, 4.5 bits per weight.
+ *   [FMT8] 05. llama.cpp：从 GGUF 文件到本地推理服务, §量化类型：Q4_K_M 到底是什么,
+ *          format table — legacy types: one FP16 scale per 32 weights; Q8_0
+ *          about 8.5 bits per weight.
+ *   [SYM]  lpnh.cn KV-cache article, §kv-mean-center 进阶技巧 / §问题 — Q4_0 is a
+ *          symmetric block format, value ≈ scale × q, with no zero point.
+ *   [ROOF] 05. llama.cpp…, §性能直觉：带宽决定 Decode，算力决定 Prefill — decode
+ *          reads every weight once per token (GEMV); prefill reuses weights
+ *          across many tokens (GEMM).
+ *   [KVMC] lpnh.cn KV-cache article, §解法 and §适用边界 — a per-(kv-head,
+ *          channel) bias is subtracted from K before Q4_0 quantization; any
+ *          other K type is rejected.
+ *   [DEQ]  xdnf.cn/news/348240, §2.2 — names dequantize_row_q4_0.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   R1 scale first, little-endian fp16, then the codes;
+ *   R2 Q4_0 nibble order: low nibbles hold elements 0..15, high nibbles 16..31,
+ *      stored unsigned as q + 8;
+ *   R3 scale d = amax / 7 (Q4_0) or amax / 127 (Q8_0), fp32 IEEE division,
+ *      rounded to fp16 ties-to-even;
+ *   R4 codes q = clamp(round_half_even(x / d16), -8, 7) (Q4_0) or
+ *      clamp(..., -127, 127) (Q8_0), dividing by the *stored* fp16 scale;
+ *      d16 == 0 gives all codes 0;
+ *   R5 activations are quantized to Q8_0 with R3/R4 before the integer dot;
+ *   R6 float results are the fp64 sum of exact per-block terms, rounded once
+ *      to fp32.
+ *
+ * Parity pins (tests/test_oracle_pins.py): block sizes; hand-worked blocks
+ * (tests/golden/); fp16 conversion against numpy's binary16; ties; the
+ * round-trip bound |x - x_hat| <= d16/2 (1 + 2^-18); brute-force fp64 dot
+ * products of dequantized operands; integer block dots against an int64 loop;
+ * bias subtraction against numpy subtraction; softmax shift invariance.
+ */
+#include "bq_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QK 32
+
+int64_t oracle_block_bytes(int type)
+{
+    /* [FMT4] 18 bytes per 32 Q4_0 weights; [FMT8] 2-byte scale + 32 int8. */
+    if (type == ORACLE_TYPE_Q4_0) return 2 + QK / 2;
+    if (type == ORACLE_TYPE_Q8_0) return 2 + QK;
+    return 0;
+}
+
+/* ---- IEEE binary16 conversion, written from the format definition ---- */
+
+uint16_t oracle_f32_to_f16(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ex = (x >> 23) & 0xFFu;
+    uint32_t man = x & 0x7FFFFFu;
+
+    if (ex == 0xFFu) /* inf stays inf, NaN stays a quiet NaN */
+        return (uint16_t)(sign | 0x7C00u | (man ? 0x0200u : 0u));
+    if (ex == 0u) /* binary32 subnormals are below half the smallest binary16 subnormal */
+        return sign;
+
+    /* value = sig * 2^(ex - 150), sig has 24 significant bits */
+    uint32_t sig = man | 0x800000u;
+    int32_t e16 = (int32_t)ex - 127 + 15; /* biased binary16 exponent if normal */
+    if (e16 >= 31)
+        return (uint16_t)(sign | 0x7C00u);
+
+    /* normal: keep 11 significant bits; subnormal: value / 2^-24 */
+    uint32_t shift = (e16 >= 1) ? 13u : (uint32_t)(13 + 1 - e16);
+    if (shift >= 25u) /* below half of 2^-24 (ties included, they go to even 0) */
+        return sign;
+
+    uint32_t q = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1u);
+    if (rem > half || (rem == half && (q & 1u)))
+        q++;
+
+    if (e16 >= 1) {
+        uint32_t e = (uint32_t)e16;
+        if (q == 0x800u) { /* rounding carried into the next binade */
+            q = 0x400u;
+            e++;
+        }
+        if (e >= 31u)
+            return (uint16_t)(sign | 0x7C00u);
+        return (uint16_t)(sign | (e << 10) | (q & 0x3FFu));
+    }
+    /* subnormal result; q == 0x400 is exactly the smallest normal, encoded as is */
+    return (uint16_t)(sign | q);
+}
+
+float oracle_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = ((uint32_t)h & 0x8000u) << 16;
+    uint32_t e = ((uint32_t)h >> 10) & 0x1Fu;
+    uint32_t m = (uint32_t)h & 0x3FFu;
+    uint32_t x;
+    if (e == 0u) {
+        /* subnormal (or zero): m * 2^-24, exact in binary32 */
+        float v = (float)m * 5.9604644775390625e-08f;
+        return sign ? -v : v;
+    }
+    if (e == 31u)
+        x = sign | 0x7F800000u | (m << 13);
+    else
+        x = sign | ((e + 112u) << 23) | (m << 13);
+    float f;
+    memcpy(&f, &x, sizeof f);
+    return f;
+}
+
+float oracle_round_half_even(float v)
+{
+    /* nearbyintf rounds in the current mode, which is the default
+     * round-to-nearest-even: 0.5 -> 0, 1.5 -> 2, 2.5 -> 2, -0.5 -> -0. */
+    return nearbyintf(v);
+}
+
+/* ---- one block: R3 + R4 ---- */
+
+static void quantize_block(int type, const float *x, uint8_t *out)
+{
+    const int qmax = (type == ORACLE_TYPE_Q4_0) ? 7 : 127;
+    const int qmin = (type == ORACLE_TYPE_Q4_0) ? -8 : -127;
+
+    float amax = 0.0f;
+    for (int j = 0; j < QK; j++) {
+        float a = fabsf(x[j]);
+        if (a > amax)
+            amax = a;
+    }
+    float d = amax / (float)qmax;           /* R3: one IEEE binary32 division */
+    uint16_t d16 = oracle_f32_to_f16(d);    /* R3: stored scale */
+    float ds = oracle_f16_to_f32(d16);      /* R4: quantize with the stored scale */
+
+    int q[QK];
+    for (int j = 0; j < QK; j++) {
+        if (ds == 0.0f) {
+            q[j] = 0;
+            continue;
+        }
+        float r = oracle_round_half_even(x[j] / ds);
+        int v = (int)r;
+        if (v > qmax) v = qmax;
+        if (v < qmin) v = qmin;
+        q[j] = v;
+    }
+
+    out[0] = (uint8_t)(d16 & 0xFFu); /* R1: little-endian scale first */
+    out[1] = (uint8_t)(d16 >> 8);
+    if (type == ORACLE_TYPE_Q4_0) {
+        for (int j = 0; j < QK / 2; j++) /* R2 */
+            out[2 + j] = (uint8_t)((unsigned)(q[j] + 8) | ((unsigned)(q[j + QK / 2] + 8) << 4));
+    } else {
+        for (int j = 0; j < QK; j++)
+            out[2 + j] = (uint8_t)(int8_t)q[j];
+    }
+}
+
+static float block_scale(const uint8_t *blk)
+{
+    uint16_t d16 = (uint16_t)(blk[0] | ((uint16_t)blk[1] << 8));
+    return oracle_f16_to_f32(d16);
+}
+
+/* codes of one block as plain ints, R2 inverted */
+static void block_codes(int type, const uint8_t *blk, int *q)
+{
+    if (type == ORACLE_TYPE_Q4_0) {
+        for (int j = 0; j < QK / 2; j++) {
+            q[j] = (int)(blk[2 + j] & 0x0Fu) - 8;
+            q[j + QK / 2] = (int)(blk[2 + j] >> 4) - 8;
+        }
+    } else {
+        for (int j = 0; j < QK; j++)
+            q[j] = (int)(int8_t)blk[2 + j];
+    }
+}
+
+int oracle_quantize_rows(int type, const float *src, uint8_t *dst,
+                         int64_t n_rows, int64_t n_cols)
+{
+    int64_t bb = oracle_block_bytes(type);
+    if (bb == 0 || n_cols % QK != 0 || n_rows < 0 || n_cols < 0)
+        return -1;
+    int64_t nb = n_cols / QK;
+    for (int64_t r = 0; r < n_rows; r++)
+        for (int64_t b = 0; b < nb; b++)
+            quantize_block(type, src + r * n_cols + b * QK, dst + (r * nb + b) * bb);
+    return 0;
+}
+
+int oracle_dequantize_rows(int type, const uint8_t *blocks, float *dst,
+                           int64_t n_rows, int64_t n_cols)
+{
+    int64_t bb = oracle_block_bytes(type);
+    if (bb == 0 || n_cols % QK != 0 || n_rows < 0 || n_cols < 0)
+        return -1;
+    int64_t nb = n_cols / QK;
+    int q[QK];
+    for (int64_t r = 0; r < n_rows; r++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *blk = blocks + (r * nb + b) * bb;
+            float d = block_scale(blk);
+            block_codes(type, blk, q);
+            for (int j = 0; j < QK; j++)
+                dst[r * n_cols + b * QK + j] = d * (float)q[j]; /* [SYM] value = scale * q */
+        }
+    return 0;
+}
+
+static int32_t block_dot(int w_type, const uint8_t *wblk, const uint8_t *xblk)
+{
+    int qw[QK], qx[QK];
+    block_codes(w_type, wblk, qw);
+    block_codes(ORACLE_TYPE_Q8_0, xblk, qx);
+    int32_t s = 0;
+    for (int j = 0; j < QK; j++)
+        s += qw[j] * qx[j];
+    return s;
+}
+
+int oracle_block_dots(int w_type, const uint8_t *w_blocks, const uint8_t *xq_blocks,
+                      int32_t *out, int64_t M, int64_t K)
+{
+    int64_t bw = oracle_block_bytes(w_type);
+    int64_t bx = oracle_block_bytes(ORACLE_TYPE_Q8_0);
+    if (bw == 0 || K % QK != 0 || M < 0 || K < 0)
+        return -1;
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t b = 0; b < nb; b++)
+            out[m * nb + b] = block_dot(w_type, w_blocks + (m * nb + b) * bw, xq_blocks + b * bx);
+    return 0;
+}
+
+/* one output: R6 (fp64 sum of exact terms, one rounding to fp32) */
+static void dot_row(int w_type, const uint8_t *wrow, const uint8_t *xrow, int64_t nb,
+                    float *y, double *mag)
+{
+    int64_t bw = oracle_block_bytes(w_type);
+    int64_t bx = oracle_block_bytes(ORACLE_TYPE_Q8_0);
+    double acc = 0.0, macc = 0.0;
+    for (int64_t b = 0; b < nb; b++) {
+        const uint8_t *wb = wrow + b * bw;
+        const uint8_t *xb = xrow + b * bx;
+        int32_t sumi = block_dot(w_type, wb, xb);
+        double term = (double)block_scale(wb) * (double)block_scale(xb) * (double)sumi;
+        acc += term;
+        macc += fabs(term);
+    }
+    *y = (float)acc;
+    if (mag)
+        *mag = macc;
+}
+
+int oracle_gemv(int w_type, const uint8_t *w_blocks, const float *x, float *y,
+                double *mag, int64_t M, int64_t K)
+{
+    int64_t bw = oracle_block_bytes(w_type);
+    if (bw == 0 || K % QK != 0 || M < 0 || K < 0)
+        return -1;
+    int64_t nb = K / QK;
+    uint8_t *xq = (uint8_t *)malloc((size_t)(nb * oracle_block_bytes(ORACLE_TYPE_Q8_0)) + 1);
+    if (!xq)
+        return -3;
+    oracle_quantize_rows(ORACLE_TYPE_Q8_0, x, xq, 1, K); /* R5 */
+    for (int64_t m = 0; m < M; m++)
+        dot_row(w_type, w_blocks + m * nb * bw, xq, nb, y + m, mag ? mag + m : NULL);
+    free(xq);
+    return 0;
+}
+
+int oracle_gemm(int w_type, const uint8_t *w_blocks, const float *X, float *Y,
+                double *mag, int64_t M, int64_t N, int64_t K)
+{
+    int64_t bw = oracle_block_bytes(w_type);
+    int64_t bx = oracle_block_bytes(ORACLE_TYPE_Q8_0);
+    if (bw == 0 || K % QK != 0 || M < 0 || N < 0 || K < 0)
+        return -1;
+    int64_t nb = K / QK;
+    uint8_t *xq = (uint8_t *)malloc((size_t)(N * nb * bx) + 1);
+    if (!xq)
+        return -3;
+    oracle_quantize_rows(ORACLE_TYPE_Q8_0, X, xq, N, K); /* R5, row by row */
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t m = 0; m < M; m++)
+            dot_row(w_type, w_blocks + m * nb * bw, xq + n * nb * bx, nb,
+                    Y + n * M + m, mag ? mag + n * M + m : NULL);
+    free(xq);
+    return 0;
+}
+
+int oracle_kv_quantize(int type, const float *rows, const float *bias, uint8_t *dst,
+                       int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim)
+{
+    int64_t bb = oracle_block_bytes(type);
+    if (bb == 0 || head_dim % QK != 0 || n_tokens < 0 || n_kv_heads < 0 || head_dim < 0)
+        return -1;
+    if (bias && type != ORACLE_TYPE_Q4_0) /* [KVMC] mean-centering needs a Q4_0 K cache */
+        return -2;
+    int64_t nb = head_dim / QK;
+    float tmp[QK];
+    for (int64_t t = 0; t < n_tokens; t++)
+        for (int64_t h = 0; h < n_kv_heads; h++) {
+            const float *src = rows + (t * n_kv_heads + h) * head_dim;
+            uint8_t *out = dst + (t * n_kv_heads + h) * nb * bb;
+            for (int64_t b = 0; b < nb; b++) {
+                for (int j = 0; j < QK; j++) {
+                    float v = src[b * QK + j];
+                    if (bias) /* [KVMC] K' = K - bias[h][c], one fp32 subtraction */
+                        v = v - bias[h * head_dim + b * QK + j];
+                    tmp[j] = v;
+                }
+                quantize_block(type, tmp, out + b * bb);
+            }
+        }
+    return 0;
+}

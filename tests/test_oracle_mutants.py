@@ -1,0 +1,75 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of oracle/bq_oracle.c (on the CPU, in a
+temporary folder), builds it, and runs tests/test_oracle_pins.py against the
+broken copy; the pin suite has to fail. The real oracle is never modified.
+"""
+import concurrent.futures as cf
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "bq_oracle.c")
+
+# (name, exact text in bq_oracle.c, replacement)
+MUTANTS = [
+    ("scale_divisor_8", "float d = amax / (float)qmax;", "float d = amax / (float)(qmax + 1);"),
+    ("divide_by_unrounded_scale", "oracle_round_half_even(x[j] / ds)", "oracle_round_half_even(x[j] / d)"),
+    ("round_half_away", "return nearbyintf(v);", "return roundf(v);"),
+    ("amax_without_abs", "float a = fabsf(x[j]);", "float a = x[j];"),
+    ("interleaved_nibbles", "((unsigned)(q[j + QK / 2] + 8) << 4)", "((unsigned)(q[j ^ 1] + 8) << 4)"),
+    ("decode_missing_offset", "q[j] = (int)(blk[2 + j] & 0x0Fu) - 8;", "q[j] = (int)(blk[2 + j] & 0x0Fu);"),
+    ("fp16_truncates", "if (rem > half || (rem == half && (q & 1u)))", "if (0)"),
+    ("fp16_ties_up", "if (rem > half || (rem == half && (q & 1u)))", "if (rem >= half)"),
+    ("scale_big_endian", "out[0] = (uint8_t)(d16 & 0xFFu);", "out[0] = (uint8_t)(d16 >> 8); out[1] = (uint8_t)(d16 & 0xFFu); if (0)"),
+    ("dot_uses_weight_scale_twice", "(double)block_scale(wb) * (double)block_scale(xb)", "(double)block_scale(wb) * (double)block_scale(wb)"),
+    ("dot_drops_last_block", "for (int64_t b = 0; b < nb; b++) {\n        const uint8_t *wb", "for (int64_t b = 0; b + 1 < nb; b++) {\n        const uint8_t *wb"),
+    ("gemm_output_transposed", "Y + n * M + m, mag ? mag + n * M + m : NULL", "Y + m * N + n, mag ? mag + m * N + n : NULL"),
+    ("kv_bias_added", "v = v - bias[h * head_dim + b * QK + j];", "v = v + bias[h * head_dim + b * QK + j];"),
+    ("kv_bias_ignores_head", "v = v - bias[h * head_dim + b * QK + j];", "v = v - bias[b * QK + j];"),
+    ("q8_clamp_narrow", "const int qmin = (type == ORACLE_TYPE_Q4_0) ? -8 : -127;", "const int qmin = (type == ORACLE_TYPE_Q4_0) ? -8 : -126;"),
+]
+
+
+def _build_mutant(tmp, name, old, new):
+    src = open(SRC, encoding="utf-8").read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    src = src.replace(old, new)
+    d = os.path.join(tmp, name)
+    os.makedirs(d, exist_ok=True)
+    with open(os.path.join(d, "bq_oracle.c"), "w", encoding="utf-8") as f:
+        f.write(src)
+    with open(os.path.join(ROOT, "oracle", "bq_oracle.h"), encoding="utf-8") as f:
+        hdr = f.read()
+    with open(os.path.join(d, "bq_oracle.h"), "w", encoding="utf-8") as f:
+        f.write(hdr)
+    lib = os.path.join(d, "libmut.so")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC",
+                    "-shared", "-o", lib, os.path.join(d, "bq_oracle.c"), "-lm"], check=True)
+    return lib
+
+
+def _pins_fail(lib):
+    env = dict(os.environ, BQ_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode != 0, r.stdout[-400:]
+
+
+def test_pins_catch_every_mutant(tmp_path):
+    libs = {name: _build_mutant(str(tmp_path), name, old, new) for name, old, new in MUTANTS}
+    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+        res = dict(zip(libs, ex.map(_pins_fail, libs.values())))
+    survived = [n for n, (failed, _) in res.items() if not failed]
+    assert not survived, f"pins did not catch: {survived}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    """Control: the same harness on an unmodified copy passes."""
+    lib = _build_mutant(str(tmp_path), "control", "#define QK 32", "#define QK 32")
+    failed, out = _pins_fail(lib)
+    assert not failed, out

@@ -1,0 +1,314 @@
+"""Pins of the CPU oracle to facts outside itself (runs without a GPU).
+
+Each test checks the oracle against something it does not compute itself:
+sizes printed by the pages, blocks worked out by hand, numpy's IEEE binary16
+and rint, the round-trip bound that the symmetric block rule implies, brute
+force fp64 products of dequantized operands, integer dots recomputed in int64
+from dequantized values, numpy's fp32 subtraction for the mean-centering bias,
+and the softmax shift identity the KV-cache article relies on.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from tests import golden
+
+Q4, Q8 = 2, 8
+TYPES = {"Q4_0": Q4, "Q8_0": Q8}
+
+
+# ---------------------------------------------------------------- sizes ----
+
+def test_block_sizes_match_pages(orc):
+    s = golden.sizes()
+    assert orc.block_bytes(Q4) == s["q4_0_bytes_per_32"] == 18
+    assert orc.block_bytes(Q4) * 8 / 32 == s["q4_0_bits_per_weight"]
+    assert orc.block_bytes(Q8) * 8 / 32 == s["q8_0_bits_per_weight"]
+    assert round(32 * 2 / orc.block_bytes(Q4), 1) == s["q4_0_vs_fp16"]
+    assert round(32 * 4 / orc.block_bytes(Q4), 1) == s["q4_0_vs_fp32"]
+    assert round(orc.block_bytes(Q4) / 32, 2) == s["kv_q4_0_bytes_per_elem"]
+    assert round(orc.block_bytes(Q8) / 32, 2) == s["kv_q8_0_bytes_per_elem"]
+    # KV cache of the pages' 0.6B model: 16384 cells x 28 layers x 8 heads x 128, K and V
+    elems = 16384 * 28 * 8 * 128 * 2
+    assert elems * 2 / 2**20 == s["kv_f16_mib"]
+    assert elems // 32 * orc.block_bytes(Q8) / 2**20 == s["kv_q8_0_mib"]
+    # 7B-shaped Q4_0 projections are most of the "about 3.8 GB" file
+    proj = 32 * (4 * 4096 * 4096 + 3 * 4096 * 11008) // 32 * orc.block_bytes(Q4)
+    assert 0.94 * s["q4_0_7b_gb"] * 1e9 < proj < s["q4_0_7b_gb"] * 1e9
+
+
+def test_output_sizes(orc):
+    x = np.zeros((3, 96), np.float32)
+    assert orc.quantize_rows(Q4, x).shape == (3, 3 * 18)
+    assert orc.quantize_rows(Q8, x).shape == (3, 3 * 34)
+
+
+# ---------------------------------------------------- hand-worked blocks ----
+
+@pytest.mark.parametrize("case", golden.hand_blocks(), ids=lambda c: f"{c[0]}-{c[1]}")
+def test_hand_worked_blocks(orc, case):
+    tname, _name, vals, expected = case
+    x = np.zeros((1, 32), np.float32)
+    for i, v in vals.items():
+        x[0, i] = v
+    got = orc.quantize_rows(TYPES[tname], x).tobytes()
+    assert got.hex() == expected.hex()
+
+
+def test_hand_worked_dequantize(orc):
+    # scale 1.0 blocks dequantize to their codes exactly
+    blk = bytes.fromhex("003c5f888a8a" + "88" * 12)
+    xh = orc.dequantize_rows(Q4, np.frombuffer(blk, np.uint8), 32)[0]
+    exp = np.zeros(32, np.float32)
+    exp[0], exp[2], exp[3], exp[16] = 7, 2, 2, -3
+    np.testing.assert_array_equal(xh, exp)
+    blk8 = bytes.fromhex("003c" + "81" + "40" * 2 + "00" * 29)
+    xh8 = orc.dequantize_rows(Q8, np.frombuffer(blk8, np.uint8), 32)[0]
+    exp8 = np.zeros(32, np.float32)
+    exp8[0], exp8[1], exp8[2] = -127, 64, 64
+    np.testing.assert_array_equal(xh8, exp8)
+
+
+# ------------------------------------------------ IEEE binary16, rounding ----
+
+def test_f32_to_f16_matches_numpy(orc):
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * np.float32(10.0) ** rng.integers(-9, 6, 4000),
+        np.array([0.0, -0.0, 1.0, 65504.0, 65519.0, 65520.0, 7e5, -7e5, 6.1035156e-05,
+                  6.0975552e-05, 5.9604645e-08, 2.9802322e-08, 2.9802326e-08, 8.940697e-08,
+                  1.0004, 1.0006, 1.00048828125, 1.00146484375, 2049.0, 2051.0, 1e-30,
+                  np.inf, -np.inf], np.float32),
+    ])
+    # halfway cases between consecutive binary16 values, in every binade
+    h = np.arange(0, 0x7BFF, 37, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mids = ((lo + hi) / 2).astype(np.float32)
+    vals = np.concatenate([vals, mids, -mids])
+    for v in vals:
+        assert orc.f32_to_f16_bits(v) == int(np.float32(v).astype(np.float16).view(np.uint16)), v
+
+
+def test_f16_to_f32_matches_numpy_all_codes(orc):
+    for h in range(0, 1 << 16):
+        ref = np.uint16(h).view(np.float16).astype(np.float32)
+        got = np.float32(orc.f16_bits_to_f32(h))
+        if np.isnan(ref):
+            assert np.isnan(got)
+        else:
+            assert got.view(np.uint32) == ref.view(np.uint32), hex(h)
+
+
+def test_round_half_even_matches_rint(orc):
+    vals = np.array([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 7.5, 126.5, 127.5, 0.49999997,
+                     2.5000002, 1e8 + 0.5, 3.3, -3.7], np.float32)
+    for v in vals:
+        assert orc.round_half_even(v) == np.rint(v), v
+
+
+# -------------------------------------------------------- round trip -------
+
+def _blocks(rng, n):
+    """Random blocks over many magnitudes, plus heavy-tailed and signed cases."""
+    scale = np.float32(10.0) ** rng.uniform(-3.5, 4, (n, 1)).astype(np.float32)
+    x = rng.standard_normal((n, 32)).astype(np.float32) * scale
+    x[::7] = rng.standard_cauchy((len(x[::7]), 32)).astype(np.float32)
+    x[::11] = np.abs(x[::11])
+    return x
+
+
+@pytest.mark.parametrize("tname", ["Q4_0", "Q8_0"])
+def test_round_trip_bound(orc, tname):
+    """|x - x_hat| <= d16/2 (1 + 2^-18) whenever the fp16 scale is normal."""
+    t = TYPES[tname]
+    qmax = 7 if t == Q4 else 127
+    rng = np.random.default_rng(2)
+    x = _blocks(rng, 4000)
+    x = x[np.abs(x).max(axis=1) < 60000 * qmax / 8]          # stay inside fp16 range
+    q = orc.quantize_rows(t, x.reshape(-1, 32))
+    xh = orc.dequantize_rows(t, q, 32)
+    bb = orc.block_bytes(t)
+    d16 = q.reshape(-1, bb)[:, :2].copy().view(np.uint16).reshape(-1)
+    d = d16.view(np.float16).astype(np.float64)
+    normal = d >= 2.0 ** -14
+    assert normal.sum() > 3000
+    err = np.abs(x.astype(np.float64) - xh.astype(np.float64))
+    bound = d[:, None] / 2 * (1 + 2.0 ** -18)
+    assert np.all(err[normal] <= bound[normal])
+    # the element of largest magnitude gets code +-qmax (no clamping loss)
+    codes = np.rint(xh.astype(np.float64)[normal] / d[normal, None])
+    amax_idx = np.abs(x[normal]).argmax(axis=1)
+    top = codes[np.arange(len(codes)), amax_idx]
+    assert np.all(np.abs(top) == qmax)
+    assert np.all(np.sign(top) == np.sign(x[normal][np.arange(len(codes)), amax_idx]))
+    # the fp16 scale is the ties-to-even rounding of amax/qmax (numpy's binary16)
+    amax = np.abs(x).max(axis=1)
+    ref = (amax / np.float32(qmax)).astype(np.float32).astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(d16, ref)
+
+
+@pytest.mark.parametrize("tname", ["Q4_0", "Q8_0"])
+def test_codes_in_range_and_zero_blocks(orc, tname):
+    t = TYPES[tname]
+    import torch
+    from block_quantized_weight_row_gb300 import inputs
+    x = inputs.adversarial_blocks().numpy()
+    q = orc.quantize_rows(t, x)
+    xh = orc.dequantize_rows(t, q, 32)
+    d = q.reshape(-1, orc.block_bytes(t))[:, :2].copy().view(np.uint16).view(np.float16).astype(np.float64).reshape(-1)
+    lo, hi = (-8, 7) if t == Q4 else (-127, 127)
+    nz = d > 0
+    codes = xh.astype(np.float64)[nz] / d[nz, None]
+    assert np.all(codes == np.rint(codes))
+    assert codes.min() >= lo and codes.max() <= hi
+    assert np.all(xh[~nz] == 0)
+    del torch
+
+
+# ------------------------------------------------------- integer dots ------
+
+@pytest.mark.parametrize("tname", ["Q4_0", "Q8_0"])
+def test_block_dots_vs_int64(orc, tname):
+    t = TYPES[tname]
+    rng = np.random.default_rng(3)
+    M, K = 7, 160
+    W = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    W[0, :32] = 0
+    x = rng.standard_normal(K).astype(np.float32)
+    wq = orc.quantize_rows(t, W)
+    xq = orc.quantize_rows(Q8, x)
+    got = orc.block_dots(t, wq, xq, M, K)
+    # recompute codes from the dequantized values (x_hat / scale is exact)
+    def codes(blocks, tt, rows):
+        xh = orc.dequantize_rows(tt, blocks, K).astype(np.float64).reshape(rows, K // 32, 32)
+        d = blocks.reshape(rows, K // 32, -1)[:, :, :2].copy().view(np.uint16)
+        d = d.view(np.float16).astype(np.float64).reshape(rows, K // 32, 1)
+        return np.where(d > 0, xh / np.where(d > 0, d, 1), 0).astype(np.int64)
+    cw = codes(wq, t, M)
+    cx = codes(xq, Q8, 1)[0]
+    ref = np.einsum("mbj,bj->mb", cw, cx)
+    np.testing.assert_array_equal(got, ref)
+    # bounds quoted in the design: |sumi| <= 32*8*127 (Q4_0) or 32*127*127 (Q8_0)
+    assert np.abs(got).max() <= (32 * 8 * 127 if t == Q4 else 32 * 127 * 127)
+
+
+# ------------------------------------------------ GEMV / GEMM, brute force --
+
+def _bruteforce(orc, t, wq, X, M, K):
+    """fp64 product of the dequantized operands (no blocking)."""
+    Wh = orc.dequantize_rows(t, wq, K).astype(np.float64).reshape(M, K)
+    Xq = orc.quantize_rows(Q8, X.reshape(-1, K))
+    Xh = orc.dequantize_rows(Q8, Xq, K).astype(np.float64)
+    return Xh @ Wh.T
+
+
+@pytest.mark.parametrize("tname", ["Q4_0", "Q8_0"])
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 64), (8, 128), (5, 96)])
+def test_gemv_matches_bruteforce(orc, tname, M, K):
+    t = TYPES[tname]
+    rng = np.random.default_rng(M * 1000 + K)
+    W = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    x = rng.standard_normal(K).astype(np.float32)
+    wq = orc.quantize_rows(t, W)
+    y, mag = orc.gemv(t, wq, x, M, K, with_mag=True)
+    ref = _bruteforce(orc, t, wq, x, M, K)[0]
+    # the oracle rounds an (essentially exact) fp64 sum once to fp32
+    assert np.all(np.abs(y.astype(np.float64) - ref) <= np.abs(ref) * 2.0 ** -24 + 1e-30)
+    assert np.all(mag >= np.abs(ref) * (1 - 1e-12))
+
+
+@pytest.mark.parametrize("tname", ["Q4_0", "Q8_0"])
+def test_gemm_matches_bruteforce_and_gemv(orc, tname):
+    t = TYPES[tname]
+    rng = np.random.default_rng(5)
+    M, N, K = 6, 5, 128
+    W = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    X = rng.standard_normal((N, K)).astype(np.float32)
+    wq = orc.quantize_rows(t, W)
+    Y = orc.gemm(t, wq, X, M, N, K)
+    ref = _bruteforce(orc, t, wq, X, M, K)
+    assert Y.shape == (N, M)
+    assert np.all(np.abs(Y.astype(np.float64) - ref) <= np.abs(ref) * 2.0 ** -24 + 1e-30)
+    for n in range(N):
+        np.testing.assert_array_equal(Y[n], orc.gemv(t, wq, X[n], M, K))
+
+
+def test_gemv_detects_transposed_operands(orc):
+    """A non-square case where reading W as K x M would give a different answer."""
+    rng = np.random.default_rng(6)
+    M, K = 2, 64
+    W = (rng.standard_normal((M, K)) * 0.02).astype(np.float32)
+    x = rng.standard_normal(K).astype(np.float32)
+    wq = orc.quantize_rows(Q4, W)
+    y = orc.gemv(Q4, wq, x, M, K)
+    Wh = orc.dequantize_rows(Q4, wq, K).astype(np.float64)
+    xh = orc.dequantize_rows(Q8, orc.quantize_rows(Q8, x), K)[0].astype(np.float64)
+    np.testing.assert_allclose(y, Wh @ xh, rtol=1e-6)
+
+
+# ------------------------------------------------------------ KV write -----
+
+def test_kv_bias_matches_numpy_subtraction(orc):
+    rng = np.random.default_rng(7)
+    T, H, D = 9, 3, 64
+    K = rng.standard_normal((T, H, D)).astype(np.float32) + 1.5
+    b = rng.uniform(-2, 2, (H, D)).astype(np.float32)
+    got = orc.kv_quantize(Q4, K, b, T, H, D)
+    centered = (K - b[None]).astype(np.float32)           # numpy IEEE fp32 subtraction
+    ref = orc.quantize_rows(Q4, centered.reshape(-1, D)).reshape(T, H, -1)
+    np.testing.assert_array_equal(got, ref)
+    # without a bias the KV write is the plain row quantizer, for both types
+    for t in (Q4, Q8):
+        np.testing.assert_array_equal(orc.kv_quantize(t, K, None, T, H, D),
+                                      orc.quantize_rows(t, K.reshape(-1, D)).reshape(T, H, -1))
+
+
+def test_kv_bias_rejected_for_q8_0(orc):
+    K = np.zeros((1, 1, 32), np.float32)
+    with pytest.raises(ValueError):
+        orc.kv_quantize(Q8, K, np.zeros((1, 32), np.float32), 1, 1, 32)
+
+
+def _softmax(z):
+    z = z - z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def test_softmax_shift_invariance_fp32():
+    """q.k_i = q.(k_i - kbar) + q.kbar; the last term is the same for every key
+    of a query row, and softmax(z + c) = softmax(z) (lpnh.cn KV-cache article,
+    §解法). Unquantized fp32 K, as the article's F32-cache test does."""
+    import torch
+    from block_quantized_weight_row_gb300 import inputs
+    L = inputs.kv_layer(0, tokens=512, kv_heads=2, head_dim=128, calib_tokens=256)
+    bias = L.K_calib.double().mean(dim=0).float().numpy()
+    K = L.K.numpy()
+    q = inputs.normal((16, 2, 128), 1.0, 99).numpy()
+    for h in range(2):
+        z0 = (q[:, h] @ K[:, h].T).astype(np.float32) / np.float32(math.sqrt(128))
+        z1 = (q[:, h] @ (K[:, h] - bias[h]).T).astype(np.float32) / np.float32(math.sqrt(128))
+        assert np.abs(_softmax(z0) - _softmax(z1)).max() <= 1e-6
+    del torch
+
+
+def test_mean_centering_lowers_q4_0_attention_error(orc):
+    """Expected, not proved (parity-unpinned magnitude): centering K before
+    Q4_0 lowers the attention KL against the fp32 cache."""
+    from block_quantized_weight_row_gb300 import inputs
+    T, H, D = 1024, 4, 128
+    L = inputs.kv_layer(1, tokens=T, kv_heads=H, head_dim=D, calib_tokens=512)
+    K = L.K.numpy()
+    bias = L.K_calib.double().mean(dim=0).float().numpy()
+    q = inputs.normal((32, H, D), 1.0, 98).numpy()
+    Kq_plain = orc.dequantize_rows(Q4, orc.kv_quantize(Q4, K, None, T, H, D), D).reshape(T, H, D)
+    Kq_cent = orc.dequantize_rows(Q4, orc.kv_quantize(Q4, K, bias, T, H, D), D).reshape(T, H, D)
+    kl = {"plain": 0.0, "cent": 0.0}
+    for h in range(H):
+        p = _softmax(q[:, h].astype(np.float64) @ K[:, h].T.astype(np.float64) / math.sqrt(D))
+        for name, Kq in (("plain", Kq_plain), ("cent", Kq_cent)):
+            r = _softmax(q[:, h].astype(np.float64) @ Kq[:, h].T.astype(np.float64) / math.sqrt(D))
+            kl[name] += float(np.sum(p * (np.log(p) - np.log(r))) / len(p))
+    assert kl["cent"] < kl["plain"]
