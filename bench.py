@@ -1,0 +1,569 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-quantized weight-row hot path on GB300.
+
+Headline (one JSON line on rank 0): Q4_0 decode GEMV weight GB/s over the
+7B-shaped decode step (32 layers x {q,k,v,o 4096x4096, gate/up 11008x4096,
+down 4096x11008}, batch 1, 224 GEMVs, 3.643 GB of Q4_0 weights), inputs
+resident in HBM, the step replayed as one CUDA graph. A "step" is one decode
+token: every weight read once, each activation quantized to Q8_0 inside the
+GEMV kernel. The step's weights are far larger than L2 (3.6 GB vs 129 MB), so
+no flush is needed between steps.
+
+Also measured in the same run (keys of the JSON line):
+  roofline      the dominant kernel (Q4_0 GEMV) timed alone over back-to-back
+                launches on distinct 11008x4096 matrices, against the measured
+                HBM copy bandwidth;
+  e2e           the same metric through the C ABI with host buffers: per step
+                the activations are copied from pinned host memory, the 224
+                GEMVs are issued as direct C-ABI calls, and all outputs are read
+                back to the host, then the host waits;
+  secondary     the prefill GEMM (512 tokens, Q8_0, TOPS), the KV-cache write
+                (28 layers x 32768 tokens x 8 x 128, K to Q4_0 with the
+                mean-centering bias and V to Q8_0, GB/s) and the Qwen3-0.6B-shaped
+                decode step (GB/s, L2 flushed between steps);
+  cpu_baseline  the plain-C oracle's GEMV timed on this host's cores over a
+                bounded sample of the same workload.
+
+--impl reference times the oracle itself as the reference arm.
+Under torchrun (N > 1) every rank runs an independent replica (the path has
+no data exchange); time is the max over ranks and value sums all ranks' bytes.
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Q4_0/Q8_0 decode GEMV weight GB/s (% of HBM peak); prefill GEMM int8 TOPS"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(value: float, dist) -> float:
+    """Max of a float over all ranks (the slowest rank sets the time)."""
+    if dist is None:
+        return value
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() and \
+        dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(bytes_per_rank_step: float, world: int, max_seconds_per_step: float) -> float:
+    """Whole-job rate: all ranks' units over the slowest rank's time."""
+    return bytes_per_rank_step * world / max_seconds_per_step
+
+
+# ------------------------------------------------------------------ peaks --
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path, encoding="utf-8") as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_traffic(key: str):
+    """DRAM bytes per launch from a committed ncu capture, or None if the
+    kernel source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path, encoding="utf-8") as f:
+            rec = json.load(f).get(key)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", []):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("sha256"):
+        return None
+    return float(rec["bytes_per_launch"])
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms or finer) kept only inside [t0, t1]."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.first = threading.Event()
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+        self.first.wait(timeout=10)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+            self.first.set()
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+
+    def close(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.t0 is None or self.t1 is None:
+            return {"samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for t, line in self.rows:
+            if not (self.t0 <= t <= self.t1 + 0.05):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- workloads --
+
+def build_decode_step(workload, dev, bq, inputs, pool_x=True):
+    """Resident Q4_0 weights of every matrix of the step, one fp32 input per
+    distinct activation (in one contiguous buffer) and one output per matrix
+    (in one contiguous buffer)."""
+    import torch
+    plan = inputs.decode_plan(workload)
+    keys = []
+    for e in plan:
+        if e.x_key not in keys:
+            keys.append(e.x_key)
+    x_len = {e.x_key: e.K for e in plan}
+    x_off, off = {}, 0
+    for k in keys:
+        x_off[k] = off
+        off += (x_len[k] + 3) // 4 * 4  # keep every x 16-byte aligned
+    x_all = torch.empty(off, dtype=torch.float32, device=dev)
+    filled = set()
+    for e in plan:
+        if e.x_key not in filled:
+            o = x_off[e.x_key]
+            x_all[o:o + e.K].copy_(inputs.activation(e.K, e.x_seed, device=dev))
+            filled.add(e.x_key)
+    y_off, off = [], 0
+    for e in plan:
+        y_off.append(off)
+        off += (e.M + 3) // 4 * 4
+    y_all = torch.empty(off, dtype=torch.float32, device=dev)
+    mats = []
+    for i, e in enumerate(plan):
+        W = inputs.weight(e.M, e.K, e.w_seed, device=dev)
+        wq = bq.quantize_rows(bq.Q4_0, W)
+        del W
+        o = x_off[e.x_key]
+        mats.append((wq, x_all[o:o + e.K], y_all[y_off[i]:y_off[i] + e.M], e.M, e.K))
+    torch.cuda.synchronize(dev)
+    wbytes = sum(e.M * (e.K // 32) * 18 for e in plan)
+    return {"plan": plan, "mats": mats, "x_all": x_all, "y_all": y_all, "weight_bytes": wbytes}
+
+
+def run_step(step, bq):
+    for wq, x, y, M, K in step["mats"]:
+        bq.gemv(bq.Q4_0, wq, x, M, K, out=y)
+
+
+def capture(fn, stream):
+    import torch
+    with torch.cuda.stream(stream):
+        fn()  # uncaptured first call: kernel attributes, device info
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, stream, steps, warmup, dist=None, clocks=None, between=None):
+    """Per-step device time (ms): events on the launching stream around each
+    replay; `between` (e.g. an L2 flush) runs outside the timed spans."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+            if between:
+                between()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    if between is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        total = e0.elapsed_time(e1)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                between()
+        torch.cuda.synchronize()
+        total = sum(a.elapsed_time(b) for a, b in evs)
+    if clocks:
+        clocks.stop()
+    torch.cuda.synchronize()
+    barrier(dist)
+    return total / steps
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+def oracle_decode_sample(seconds: float, workload="7b-decode"):
+    """The oracle GEMV over layer 0 of the decode step, repeated until at
+    least `seconds` of oracle time; returns (GB/s, description)."""
+    import oracle
+    from block_quantized_weight_row_gb300 import inputs
+    plan = [e for e in inputs.decode_plan(workload) if e.layer == 0]
+    mats = []
+    for e in plan:
+        W = inputs.weight(e.M, e.K, e.w_seed).numpy()
+        mats.append((oracle.quantize_rows(oracle.Q4_0, W), inputs.activation(e.K, e.x_seed).numpy(), e.M, e.K))
+        del W
+    done_bytes, spent, passes = 0, 0.0, 0
+    while spent < seconds:
+        for wq, x, M, K in mats:
+            t = time.perf_counter()
+            oracle.gemv(oracle.Q4_0, wq, x, M, K)
+            spent += time.perf_counter() - t
+            done_bytes += wq.nbytes
+        passes += 1
+    mb = sum(m[0].nbytes for m in mats) / 1e6
+    return done_bytes / spent / 1e9, (f"oracle GEMV (single thread) over layer 0 of the {workload} step "
+                                      f"(7 matrices, {mb:.1f} MB Q4_0), {passes} passes, {spent:.1f} s")
+
+
+# ------------------------------------------------------------------ main ---
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    import block_quantized_weight_row_gb300 as bq
+    from block_quantized_weight_row_gb300 import binding, inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+
+    # ---- headline: 7B decode step
+    step = build_decode_step("7b-decode", dev, bq, inputs)
+    g = capture(lambda: run_step(step, bq), stream)
+    clocks = ClockSampler(local) if rank == 0 else None
+    ms = time_graph(g, stream, args.steps, args.warmup, dist, clocks)
+    if clocks:
+        clocks.close()
+    ms_max = max_over_ranks(ms, dist)
+    value = aggregate_rate(step["weight_bytes"], world, ms_max * 1e-3) / 1e9
+    launches = len(step["mats"]) * args.steps
+
+    # ---- roofline: the dominant kernel alone on distinct 11008 x 4096 matrices
+    gate_up = [m for m, e in zip(step["mats"], step["plan"]) if e.name in ("gate", "up")]
+    rg = capture(lambda: [bq.gemv(bq.Q4_0, wq, x, M, K, out=y) for wq, x, y, M, K in gate_up], stream)
+    r_ms = time_graph(rg, stream, 20, 3) / len(gate_up)
+    M_, K_ = 11008, 4096
+    alg_bytes = M_ * (K_ // 32) * 18 + K_ * 4 + M_ * 4
+    achieved = alg_bytes / (r_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "k_gemv_tma<Q4_0> 11008x4096", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": kernel_traffic("gemv_q4_0_11008x4096"), "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_us": round(r_ms * 1e3, 3)}
+
+    # ---- e2e: direct C-ABI calls, host buffers, copies inside the timed region
+    e2e = e2e_decode(step, stream, dev, args, dist, world)
+
+    secondary = {}
+    if not args.no_secondary:
+        secondary = secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        v, desc = oracle_decode_sample(args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "q4_0xq8_0->f32",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
+            "config": {"workload": "7b-decode: 32 layers x {q,k,v,o 4096x4096, gate/up 11008x4096, "
+                                   "down 4096x11008}, batch 1, Q4_0 weights, 224 GEMVs per step",
+                       "weight_bytes_per_step": step["weight_bytes"],
+                       "l2": "inputs larger than L2 (3.64 GB of weights per step)",
+                       "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step"},
+            "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
+            "tokens_per_s_equiv": round(1e3 / ms_max, 1),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks.summary() if clocks else None,
+            "cpu_baseline": cpu, "secondary": secondary,
+        }
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def e2e_decode(step, stream, dev, args, dist, world):
+    """Per step: pinned host -> device copy of every activation, the 224
+    GEMVs as direct C-ABI calls, device -> pinned host copy of every output,
+    and a host wait on the stream."""
+    import torch
+    from block_quantized_weight_row_gb300 import binding
+    L = binding.lib()
+    x_host = step["x_all"].cpu().pin_memory()
+    y_host = torch.empty(step["y_all"].numel(), dtype=torch.float32).pin_memory()
+    calls = [(ctypes.c_void_p(wq.data_ptr()), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
+              M, K) for wq, x, y, M, K in step["mats"]]
+    f = L.bq_gemv
+
+    def one():
+        step["x_all"].copy_(x_host, non_blocking=True)
+        for w, x, y, M, K in calls:
+            rc = f(2, w, x, y, M, K)
+            if rc:
+                raise binding.BQError(rc, L.bq_last_error().decode())
+        y_host.copy_(step["y_all"], non_blocking=True)
+        stream.synchronize()
+
+    n = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        assert L.bq_set_stream(ctypes.c_void_p(stream.cuda_stream)) == 0
+        for _ in range(args.warmup):
+            one()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, dist)
+    return {"value": round(aggregate_rate(step["weight_bytes"], world, ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(step["x_all"].numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4),
+            "ms_per_step": round(ms, 4), "steps": n, "path": "direct C-ABI calls (no graph)"}
+
+
+def l2_flusher(dev):
+    import torch
+    buf = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        buf.fill_(1)
+    return flush
+
+
+def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
+    import torch
+    out = {}
+    flush = l2_flusher(dev)
+
+    # prefill GEMM, 512 tokens, Q8_0 weights
+    cfg = inputs.WORKLOADS["prefill-q8_0"]
+    N = cfg["tokens"]
+    rows = []
+    for i, (M, K) in enumerate(cfg["shapes"]):
+        W = inputs.weight(M, K, inputs.seed_of("prefill-q8_0", 0, i), device=dev)
+        wq = bq.quantize_rows(bq.Q8_0, W)
+        del W
+        X = inputs.activation(K, inputs.seed_of("prefill-q8_0", 1, i), device=dev, rows=N)
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+        g = capture(lambda: bq.gemm(bq.Q8_0, wq, X, M, N, K, out=Y), stream)
+        ms = max_over_ranks(time_graph(g, stream, 20, 3, between=flush), dist)
+        ops = 2.0 * N * M * K
+        tops = ops / (ms * 1e-3) / 1e12
+        rows.append({"M": M, "K": K, "N": N, "ms": round(ms, 4), "tops": round(tops, 1)})
+    tot_ops = sum(2.0 * r["N"] * r["M"] * r["K"] for r in rows)
+    tot_ms = sum(r["ms"] for r in rows)
+    tops = tot_ops / (tot_ms * 1e-3) / 1e12 * world
+    out["prefill_gemm"] = {"metric": "prefill GEMM int8-equivalent TOPS (2*N*M*K per GEMM, X quantize included)",
+                           "value": round(tops, 1), "unit": "TOPS", "shapes": rows,
+                           "kernel": "k_gemm_q8_mma (mma.sync m16n8k32 s8)",
+                           "l2": "flushed between iterations"}
+
+    # KV-cache write: 28 layers x (K -> Q4_0 with bias, V -> Q8_0)
+    kv = inputs.WORKLOADS["kv-write"]
+    T, H, D = kv["tokens"], kv["kv_heads"], kv["head_dim"]
+    layers = []
+    for layer in range(kv["layers"]):
+        Lr = inputs.kv_layer(layer, T, H, D, kv["calib_tokens"], device=dev)
+        bias = Lr.K_calib.double().mean(dim=0).float().contiguous()
+        kq = torch.empty((T, H, D // 32 * 18), dtype=torch.uint8, device=dev)
+        vq = torch.empty((T, H, D // 32 * 34), dtype=torch.uint8, device=dev)
+        layers.append((Lr.K, Lr.V, bias, kq, vq))
+        del Lr
+
+    def kv_step():
+        for K_, V_, b, kq, vq in layers:
+            bq.kv_quantize(bq.Q4_0, K_, b, out=kq)
+            bq.kv_quantize(bq.Q8_0, V_, None, out=vq)
+    g = capture(kv_step, stream)
+    ms = max_over_ranks(time_graph(g, stream, 10, 3), dist)
+    kv_bytes = kv["layers"] * (2 * T * H * D * 4 + H * D * 4 + T * H * (D // 32) * (18 + 34))
+    out["kv_write"] = {"metric": "KV-cache write GB/s (fp32 K,V read + Q4_0 K / Q8_0 V written)",
+                       "value": round(aggregate_rate(kv_bytes, world, ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                       "ms_per_step": round(ms, 4), "bytes_per_step": kv_bytes,
+                       "hbm_frac_of_measured": round(kv_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                       "l2": "inputs larger than L2 (7.5 GB read per step)"}
+    del layers, g
+    torch.cuda.empty_cache()
+
+    # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps
+    q = build_decode_step("qwen3-0.6b-decode", dev, bq, inputs)
+    g = capture(lambda: run_step(q, bq), stream)
+    ms = max_over_ranks(time_graph(g, stream, 50, 5, between=flush), dist)
+    out["qwen3_0_6b_decode"] = {"metric": "Q4_0 decode GEMV weight GB/s", "unit": "GB/s",
+                                "value": round(aggregate_rate(q["weight_bytes"], world, ms * 1e-3) / 1e9, 1),
+                                "ms_per_step": round(ms, 4), "weight_bytes_per_step": q["weight_bytes"],
+                                "gemvs_per_step": len(q["mats"]), "l2": "flushed between steps"}
+    return out
+
+
+def reference_arm(args, world, rank):
+    """The CPU oracle as the reference arm, on the host cores: each step is
+    the oracle GEMV over a fixed slice of rows of every matrix of layer 0 of
+    the 7B decode step, the slice sized so that warm-up plus timed steps take
+    about a minute of oracle time."""
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    from block_quantized_weight_row_gb300 import inputs
+    plan = [e for e in inputs.decode_plan("7b-decode") if e.layer == 0]
+    mats = []
+    for e in plan:
+        W = inputs.weight(e.M, e.K, e.w_seed).numpy()
+        mats.append((oracle.quantize_rows(oracle.Q4_0, W), inputs.activation(e.K, e.x_seed).numpy(), e.M, e.K))
+        del W
+    # calibrate: oracle seconds per weight byte on one full matrix
+    wq, x, M, K = mats[0]
+    t = time.perf_counter()
+    oracle.gemv(oracle.Q4_0, wq, x, M, K)
+    s_per_byte = (time.perf_counter() - t) / wq.nbytes
+    layer_bytes = sum(m[0].nbytes for m in mats)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    frac = min(1.0, budget / (s_per_byte * layer_bytes))
+    sample = [(wq[:max(1, int(M * frac))], x, max(1, int(M * frac)), K) for wq, x, M, K in mats]
+    step_bytes = sum(m[0].nbytes for m in sample)
+
+    def one():
+        for wq_, x_, M_, K_ in sample:
+            oracle.gemv(oracle.Q4_0, wq_, x_, M_, K_)
+
+    for _ in range(args.warmup):
+        one()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    spent = time.perf_counter() - t
+    ms = spent / args.steps * 1e3
+    value = step_bytes / (ms * 1e-3) / 1e9
+    desc = (f"oracle GEMV (single thread) per step over the first {frac:.2%} of the rows of each of the "
+            f"7 matrices of layer 0 of the 7b-decode step ({step_bytes / 1e6:.2f} MB Q4_0 per step)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "q4_0xq8_0->f64", "data": "synthetic",
+        "config": {"workload": "7b-decode (layer-0 row sample per step), oracle on host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    main()

@@ -62,6 +62,7 @@ def lib():
         "bq_block_bytes": ([i], i),
         "bq_device_status": ([], i),
         "bq_version": ([], i),
+        "bq_set_spin_limit": ([i64], i),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)

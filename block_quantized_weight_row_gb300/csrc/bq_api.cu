@@ -1,0 +1,305 @@
+// bq_api.cu — the C ABI of libbq.so (declared in include/bq.h): argument
+// validation, per-thread stream / workspace / error state, per-device info,
+// and the device error word that bounded in-kernel waits report through.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "bq.h"
+#include "bq_device.cuh"
+#include "bq_internal.h"
+
+namespace bq {
+
+// Set by kernels whose bounded waits ran out; read and cleared by bq_device_status.
+static __device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint32_t kDefaultSpinLimit = 1u << 22;
+
+thread_local cudaStream_t t_stream = nullptr;
+thread_local void *t_ws = nullptr;
+thread_local size_t t_ws_bytes = 0;
+thread_local std::string t_error = "no error";
+
+std::mutex g_info_mutex;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ready[kMaxDevices] = {};
+uint32_t g_spin_limit = kDefaultSpinLimit;
+
+int fail(int status, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+  return fail(BQ_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int block_bytes(int type) {
+  if (type == BQ_TYPE_Q4_0) return Fmt<kTypeQ4_0>::kBytes;
+  if (type == BQ_TYPE_Q8_0) return Fmt<kTypeQ8_0>::kBytes;
+  return 0;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// n_rows * n_cols within int64 and both non-negative
+bool sizes_ok(int64_t a, int64_t b) {
+  if (a < 0 || b < 0) return false;
+  return b == 0 || a <= (int64_t(1) << 62) / b;
+}
+
+int ok() {
+  t_error = "no error";
+  return BQ_OK;
+}
+
+}  // namespace
+
+const DeviceInfo *device_info(cudaError_t *err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_info_mutex);
+  if (!g_info_ready[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess ||
+        (e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err_word), g_error_word)) != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    g_info[dev] = d;
+    g_info_ready[dev] = true;
+  }
+  *err = cudaSuccess;
+  return &g_info[dev];
+}
+
+uint32_t spin_limit() { return g_spin_limit; }
+
+namespace {
+struct SmemEntry {
+  int device;
+  const void *func;
+  int bytes;
+};
+std::mutex g_smem_mutex;
+SmemEntry g_smem[256];
+int g_smem_n = 0;
+}  // namespace
+
+cudaError_t ensure_smem(const void *func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_smem_mutex);
+  for (int i = 0; i < g_smem_n; ++i)
+    if (g_smem[i].device == dev && g_smem[i].func == func) {
+      if (g_smem[i].bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) g_smem[i].bytes = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && g_smem_n < 256) g_smem[g_smem_n++] = SmemEntry{dev, func, bytes};
+  return e;
+}
+
+}  // namespace bq
+
+using namespace bq;
+
+extern "C" {
+
+int bq_version(void) { return (0 << 16) | 1; }
+
+int bq_block_bytes(int type) { return block_bytes(type); }
+
+const char *bq_last_error(void) { return t_error.c_str(); }
+
+int bq_set_stream(void *cuda_stream) {
+  t_stream = static_cast<cudaStream_t>(cuda_stream);
+  return ok();
+}
+
+void *bq_get_stream(void) { return t_stream; }
+
+int bq_set_workspace(void *dev_ptr, size_t bytes) {
+  if ((dev_ptr == nullptr) != (bytes == 0))
+    return fail(BQ_ERR_INVALID_ARG, "bq_set_workspace: pointer and size must be both set or both empty");
+  if (dev_ptr && !aligned(dev_ptr, 256)) return fail(BQ_ERR_ALIGN, "bq_set_workspace: pointer must be 256-byte aligned");
+  t_ws = dev_ptr;
+  t_ws_bytes = bytes;
+  return ok();
+}
+
+size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K) {
+  (void)M;
+  if (type != BQ_TYPE_Q8_0 || N <= 0 || K <= 0 || K % kQK) return 0;
+  const size_t bytes = size_t(N) * size_t(K / kQK) * Fmt<kTypeQ8_0>::kBytes;
+  return (bytes + 255) / 256 * 256;
+}
+
+int bq_set_spin_limit(int64_t polls) {
+  g_spin_limit = polls < 0 ? kDefaultSpinLimit : uint32_t(polls > 0xffffffffll ? 0xffffffffll : polls);
+  return ok();
+}
+
+int bq_device_status(void) {
+  cudaError_t e = cudaStreamSynchronize(t_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bq_device_status: stream synchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "bq_device_status: read error word");
+  if (word) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "bq_device_status: clear error word");
+    if (word & kErrTimeout) return fail(BQ_ERR_TIMEOUT, "a bounded in-kernel wait ran out (error word 0x%x)", word);
+  }
+  return ok();
+}
+
+int bq_quantize_rows(int type, const float *src, void *dst, int64_t n_rows, int64_t n_cols) {
+  const int bb = block_bytes(type);
+  if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_quantize_rows: unknown type %d", type);
+  if (!sizes_ok(n_rows, n_cols)) return fail(BQ_ERR_INVALID_ARG, "bq_quantize_rows: bad sizes %lld x %lld", (long long)n_rows, (long long)n_cols);
+  if (n_cols % kQK) return fail(BQ_ERR_SHAPE, "bq_quantize_rows: n_cols %lld is not a multiple of 32", (long long)n_cols);
+  const int64_t n_blocks = n_rows * (n_cols / kQK);
+  if (n_blocks == 0) return ok();
+  if (!src || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_quantize_rows: null pointer");
+  if (!aligned(src, 16) || !aligned(dst, 16)) return fail(BQ_ERR_ALIGN, "bq_quantize_rows: src and dst must be 16-byte aligned");
+  if (overlap(src, size_t(n_blocks) * 128, dst, size_t(n_blocks) * bb))
+    return fail(BQ_ERR_INVALID_ARG, "bq_quantize_rows: src and dst overlap");
+  cudaError_t e = launch_quantize_rows(type, src, static_cast<uint8_t *>(dst), n_blocks, n_cols / kQK, nullptr, 1, t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_quantize_rows launch");
+}
+
+int bq_dequantize_rows(int type, const void *blocks, float *dst, int64_t n_rows, int64_t n_cols) {
+  const int bb = block_bytes(type);
+  if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_dequantize_rows: unknown type %d", type);
+  if (!sizes_ok(n_rows, n_cols)) return fail(BQ_ERR_INVALID_ARG, "bq_dequantize_rows: bad sizes");
+  if (n_cols % kQK) return fail(BQ_ERR_SHAPE, "bq_dequantize_rows: n_cols %lld is not a multiple of 32", (long long)n_cols);
+  const int64_t n_blocks = n_rows * (n_cols / kQK);
+  if (n_blocks == 0) return ok();
+  if (!blocks || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_dequantize_rows: null pointer");
+  if (!aligned(blocks, 16) || !aligned(dst, 16)) return fail(BQ_ERR_ALIGN, "bq_dequantize_rows: pointers must be 16-byte aligned");
+  if (overlap(blocks, size_t(n_blocks) * bb, dst, size_t(n_blocks) * 128))
+    return fail(BQ_ERR_INVALID_ARG, "bq_dequantize_rows: blocks and dst overlap");
+  cudaError_t e = launch_dequantize_rows(type, static_cast<const uint8_t *>(blocks), dst, n_blocks, t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_dequantize_rows launch");
+}
+
+int bq_gemv(int type, const void *W, const float *x, float *y, int64_t M, int64_t K) {
+  const int bb = block_bytes(type);
+  if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_gemv: unknown type %d", type);
+  if (!sizes_ok(M, K)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: bad sizes");
+  if (K % kQK) return fail(BQ_ERR_SHAPE, "bq_gemv: K %lld is not a multiple of 32", (long long)K);
+  if (K > BQ_GEMV_MAX_K) return fail(BQ_ERR_SHAPE, "bq_gemv: K %lld exceeds %d", (long long)K, BQ_GEMV_MAX_K);
+  if (M > 0x7fffffffll) return fail(BQ_ERR_SHAPE, "bq_gemv: M %lld exceeds 2^31-1", (long long)M);
+  if (M == 0) return ok();
+  if (!y || (K > 0 && (!W || !x))) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: null pointer");
+  if (!aligned(y, 4) || (K > 0 && (!aligned(W, 16) || !aligned(x, 16))))
+    return fail(BQ_ERR_ALIGN, "bq_gemv: W and x must be 16-byte aligned, y 4-byte aligned");
+  const size_t wbytes = size_t(M) * size_t(K / kQK) * bb;
+  if (overlap(y, size_t(M) * 4, W, wbytes) || overlap(y, size_t(M) * 4, x, size_t(K) * 4))
+    return fail(BQ_ERR_INVALID_ARG, "bq_gemv: y overlaps an input");
+  cudaError_t e;
+  if (K == 0)
+    e = cudaMemsetAsync(y, 0, size_t(M) * 4, t_stream);
+  else
+    e = launch_gemv(type, static_cast<const uint8_t *>(W), x, y, M, K, t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemv launch");
+}
+
+int bq_gemm(int type, const void *W, const float *X, float *Y, int64_t M, int64_t N, int64_t K) {
+  const int bb = block_bytes(type);
+  if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_gemm: unknown type %d", type);
+  if (type != BQ_TYPE_Q8_0) return fail(BQ_ERR_UNSUPPORTED, "bq_gemm: only Q8_0 weights are supported");
+  if (!sizes_ok(M, K) || !sizes_ok(N, K) || !sizes_ok(M, N)) return fail(BQ_ERR_INVALID_ARG, "bq_gemm: bad sizes");
+  if (K % kQK) return fail(BQ_ERR_SHAPE, "bq_gemm: K %lld is not a multiple of 32", (long long)K);
+  if (M > 0x7fffffffll || N > 0x7fffffffll) return fail(BQ_ERR_SHAPE, "bq_gemm: M and N must be below 2^31");
+  if (M == 0 || N == 0) return ok();
+  if (!Y || (K > 0 && (!W || !X))) return fail(BQ_ERR_INVALID_ARG, "bq_gemm: null pointer");
+  if (!aligned(Y, 4) || (K > 0 && (!aligned(W, 16) || !aligned(X, 16))))
+    return fail(BQ_ERR_ALIGN, "bq_gemm: W and X must be 16-byte aligned, Y 4-byte aligned");
+  const size_t ybytes = size_t(M) * size_t(N) * 4;
+  if (overlap(Y, ybytes, W, size_t(M) * size_t(K / kQK) * bb) || overlap(Y, ybytes, X, size_t(N) * size_t(K) * 4))
+    return fail(BQ_ERR_INVALID_ARG, "bq_gemm: Y overlaps an input");
+  if (K == 0) {
+    cudaError_t e = cudaMemsetAsync(Y, 0, ybytes, t_stream);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemm memset");
+  }
+  const size_t need = bq_workspace_size(type, M, N, K);
+  if (!t_ws || t_ws_bytes < need)
+    return fail(BQ_ERR_WORKSPACE, "bq_gemm: needs %zu workspace bytes, %zu set", need, t_ws_bytes);
+  if (overlap(t_ws, need, Y, ybytes) || overlap(t_ws, need, X, size_t(N) * size_t(K) * 4) ||
+      overlap(t_ws, need, W, size_t(M) * size_t(K / kQK) * bb))
+    return fail(BQ_ERR_INVALID_ARG, "bq_gemm: workspace overlaps an argument");
+  uint8_t *xq = static_cast<uint8_t *>(t_ws);
+  cudaError_t e = launch_quantize_rows(BQ_TYPE_Q8_0, X, xq, N * (K / kQK), K / kQK, nullptr, 1, t_stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bq_gemm: activation quantize launch");
+  e = launch_gemm(type, static_cast<const uint8_t *>(W), xq, Y, M, N, K, t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemm launch");
+}
+
+int bq_kv_quantize(int type, const float *rows, const float *bias, void *dst, int64_t n_tokens,
+                   int64_t n_kv_heads, int64_t head_dim) {
+  const int bb = block_bytes(type);
+  if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: unknown type %d", type);
+  if (bias && type != BQ_TYPE_Q4_0)
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: a mean-centering bias requires the Q4_0 type");
+  if (!sizes_ok(n_tokens, n_kv_heads) || !sizes_ok(n_tokens * n_kv_heads, head_dim))
+    return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: bad sizes");
+  if (head_dim % kQK) return fail(BQ_ERR_SHAPE, "bq_kv_quantize: head_dim %lld is not a multiple of 32", (long long)head_dim);
+  const int64_t n_blocks = n_tokens * n_kv_heads * (head_dim / kQK);
+  if (n_blocks == 0) return ok();
+  if (!rows || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: null pointer");
+  if (!aligned(rows, 16) || !aligned(dst, 16) || (bias && !aligned(bias, 16)))
+    return fail(BQ_ERR_ALIGN, "bq_kv_quantize: rows, bias and dst must be 16-byte aligned");
+  if (overlap(rows, size_t(n_blocks) * 128, dst, size_t(n_blocks) * bb) ||
+      overlap(bias, size_t(n_kv_heads * head_dim) * 4, dst, size_t(n_blocks) * bb))
+    return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: dst overlaps an input");
+  cudaError_t e = launch_quantize_rows(type, rows, static_cast<uint8_t *>(dst), n_blocks, head_dim / kQK, bias,
+                                       n_kv_heads * (head_dim / kQK), t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_kv_quantize launch");
+}
+
+int bq_block_dots(int type, const void *W, const void *xq, int32_t *out, int64_t M, int64_t K) {
+  const int bb = block_bytes(type);
+  if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_block_dots: unknown type %d", type);
+  if (!sizes_ok(M, K)) return fail(BQ_ERR_INVALID_ARG, "bq_block_dots: bad sizes");
+  if (K % kQK) return fail(BQ_ERR_SHAPE, "bq_block_dots: K %lld is not a multiple of 32", (long long)K);
+  if (M == 0 || K == 0) return ok();
+  if (!W || !xq || !out) return fail(BQ_ERR_INVALID_ARG, "bq_block_dots: null pointer");
+  if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(out, 4)) return fail(BQ_ERR_ALIGN, "bq_block_dots: alignment");
+  cudaError_t e = launch_block_dots(type, static_cast<const uint8_t *>(W), static_cast<const uint8_t *>(xq), out, M, K,
+                                    t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_block_dots launch");
+}
+
+}  // extern "C"

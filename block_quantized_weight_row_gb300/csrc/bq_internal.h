@@ -1,0 +1,44 @@
+// bq_internal.h — host-side interfaces between the C-ABI layer (bq_api.cu)
+// and the kernel translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bq {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int max_smem_optin = 0;      // bytes of dynamic shared memory a CTA may opt into
+  int smem_per_sm = 0;         // bytes of shared memory per SM
+  unsigned *err_word = nullptr;  // device address of the error word (bit kErrTimeout, ...)
+};
+
+// Info of the current device (cached after the first call on each device).
+// Returns nullptr and sets *err on failure.
+const DeviceInfo *device_info(cudaError_t *err);
+
+// Poll budget of the bounded mbarrier waits inside kernels.
+uint32_t spin_limit();
+
+// Raise the dynamic shared memory limit of `func` on the current device to
+// `bytes` unless an earlier call already did (so that launches recorded in a
+// stream capture make no attribute calls after the first, uncaptured one).
+cudaError_t ensure_smem(const void *func, int bytes);
+
+// Launchers; each returns the launch status. Sizes were validated by the ABI layer.
+cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64_t n_blocks,
+                                 int64_t blocks_per_row, const float *bias, int64_t bias_period,
+                                 cudaStream_t stream);
+cudaError_t launch_dequantize_rows(int type, const uint8_t *blocks, float *dst, int64_t n_blocks,
+                                   cudaStream_t stream);
+cudaError_t launch_gemv(int type, const uint8_t *W, const float *x, float *y, int64_t M,
+                        int64_t K, cudaStream_t stream);
+cudaError_t launch_gemm(int type, const uint8_t *W, const uint8_t *Xq, float *Y, int64_t M,
+                        int64_t N, int64_t K, cudaStream_t stream);
+cudaError_t launch_block_dots(int type, const uint8_t *W, const uint8_t *xq, int32_t *out,
+                              int64_t M, int64_t K, cudaStream_t stream);
+
+}  // namespace bq

@@ -125,3 +125,31 @@ def adversarial_blocks(device="cpu") -> torch.Tensor:
     r = torch.zeros(32); r[7] = -8.0; rows.append(r)         # negative amax
     r = torch.tensor([(-1.0) ** i * (i + 1) for i in range(32)]); rows.append(r)
     return torch.stack(rows).to(device)
+
+
+INPUT_ORDER = ("attn_in", "attn_out", "ffn_in", "ffn_hidden")
+
+
+@dataclass
+class PlanEntry:
+    layer: int
+    name: str
+    M: int
+    K: int
+    w_seed: int
+    x_key: tuple   # (layer, input name); matrices with the same key share one x
+    x_seed: int
+
+
+def decode_plan(workload: str) -> list:
+    """Matrices of one decode step in execution order, with their seeds.
+    Weight seeds: workload*1000 + layer*10 + matrix index; activation seeds:
+    workload*1000 + 500 + layer*10 + input index."""
+    cfg = WORKLOADS[workload]
+    plan = []
+    for layer in range(cfg["layers"]):
+        for mi, (name, M, K) in enumerate(cfg["layer"]):
+            inp = LAYER_INPUT[name]
+            plan.append(PlanEntry(layer, name, M, K, seed_of(workload, layer, mi), (layer, inp),
+                                  cfg["index"] * 1000 + 500 + layer * 10 + INPUT_ORDER.index(inp)))
+    return plan

@@ -1,0 +1,154 @@
+/*
+ * bq.h — C ABI of libbq.so: block-quantized weight rows on one GB300 GPU.
+ *
+ * Formats (sizes fixed by the pages; byte and nibble order are this
+ * library's stated layout):
+ *   Q4_0 block, 18 bytes: 32 weights share one FP16 scale, each weight is a
+ *     4-bit integer, 4.5 bits per weight ("llama.cpp 原理：如何在普通硬件跑本地
+ *     大模型", §量化：内存真正去哪了); symmetric, value = scale * q with no zero
+ *     point (lpnh.cn KV-cache article, §kv-mean-center 进阶技巧 / §问题).
+ *     Layout: bytes 0-1 the scale (IEEE binary16, little endian), bytes 2-17
+ *     qs[j] = (q[j] + 8) | ((q[j + 16] + 8) << 4), q in [-8, 7].
+ *   Q8_0 block, 34 bytes: one FP16 scale per 32 weights, about 8.5 bits per
+ *     weight ("05. llama.cpp：从 GGUF 文件到本地推理服务", §量化类型, format
+ *     table). Layout: bytes 0-1 the scale, bytes 2-33 int8 q[j] in [-127, 127].
+ *   Quantization of a 32-value block: amax = max |x|; d = amax / 7 (Q4_0) or
+ *     amax / 127 (Q8_0) in fp32 IEEE division; the stored scale is d rounded
+ *     to binary16 (ties to even); q = clamp(round_half_even(x / scale), ...)
+ *     with an IEEE division by the stored scale; a zero scale gives q = 0.
+ *
+ * Conventions for every entry point:
+ *   - Status: 0 (BQ_OK) on success, a negative BQ_ERR_* code otherwise; the
+ *     message for the last failure on the calling thread is bq_last_error().
+ *     ("nonzero means failure", as the quantize tool's library entry reports
+ *     it: "采样、量化与部署 — 代码走读", §tools/quantize/.)
+ *   - Data pointers are DEVICE pointers owned by the caller. Inputs and
+ *     outputs must not alias. Nothing is allocated by the library: entry
+ *     points that need scratch use the caller-provided workspace.
+ *   - Calls are asynchronous on the calling thread's current stream
+ *     (bq_set_stream; NULL = the legacy default stream). Argument errors and
+ *     launch errors are returned at once; faults inside a kernel surface at
+ *     the caller's next synchronization. Bounded waits inside kernels that run
+ *     out set a device error word that bq_device_status() reports.
+ *   - A call whose sizes make the output empty is a successful no-op.
+ *   - Block pointers (weights, quantized outputs) must be 16-byte aligned and
+ *     fp32 pointers 16-byte aligned, else BQ_ERR_ALIGN.
+ *   - Sizes are int64; a row length (n_cols, K, head_dim) must be a multiple
+ *     of 32, else BQ_ERR_SHAPE.
+ */
+#ifndef BQ_H
+#define BQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BQ_TYPE_Q4_0 2
+#define BQ_TYPE_Q8_0 8
+
+#define BQ_OK 0
+#define BQ_ERR_INVALID_ARG (-1) /* null pointer, negative size, aliasing */
+#define BQ_ERR_SHAPE (-2)       /* row length not a multiple of 32, or above a stated limit */
+#define BQ_ERR_UNSUPPORTED (-3) /* unknown type, or a type this entry point does not take */
+#define BQ_ERR_ALIGN (-4)       /* pointer alignment */
+#define BQ_ERR_CUDA (-5)        /* a CUDA runtime call failed (message has the CUDA error) */
+#define BQ_ERR_TIMEOUT (-6)     /* a bounded in-kernel wait ran out (see bq_device_status) */
+#define BQ_ERR_WORKSPACE (-7)   /* workspace missing or smaller than bq_workspace_size() */
+
+/* Largest K taken by bq_gemv (the quantized activation lives in shared memory). */
+#define BQ_GEMV_MAX_K 65536
+
+/* Quantize rows (row quantize for Q4_0 and Q8_0).
+ * Pages: Q4_0 and Q8_0 block rules above ("llama.cpp 原理…", §量化：内存真正去哪了;
+ * "05. llama.cpp…", §量化类型).
+ * src: n_rows x n_cols fp32, row-major, 16-byte aligned.
+ * dst_blocks: n_rows x (n_cols/32) blocks of `type`, contiguous, 16-byte aligned,
+ *   n_rows * n_cols / 32 * bq_block_bytes(type) bytes.
+ * Errors: BQ_ERR_UNSUPPORTED (type), BQ_ERR_SHAPE (n_cols % 32), BQ_ERR_ALIGN,
+ *   BQ_ERR_INVALID_ARG (null pointers with a nonzero size, negative sizes). */
+int bq_quantize_rows(int type, const float *src_f32, void *dst_blocks, int64_t n_rows,
+                     int64_t n_cols);
+
+/* Dequantize rows: x_hat = scale * q, exact in fp32 (the pages name
+ * dequantize_row_q4_0: xdnf.cn/news/348240, §2.2).
+ * blocks: n_rows x (n_cols/32) blocks; dst: n_rows x n_cols fp32. */
+int bq_dequantize_rows(int type, const void *blocks, float *dst, int64_t n_rows, int64_t n_cols);
+
+/* Decode GEMV: y = W . x for one token. Decode reads every weight once per
+ * token, so it is bound by memory bandwidth ("05. llama.cpp…", §性能直觉：带宽决定
+ * Decode，算力决定 Prefill).
+ * W_blocks: M rows of K/32 blocks of `type` (Q4_0 or Q8_0), row-major, 16-byte aligned.
+ * x: K fp32 (quantized to Q8_0 inside the kernel with the block rule above).
+ * y: M fp32. y[m] = sum_b scale_w[m][b] * scale_x[b] * sumi[m][b] where sumi is
+ *   the exact int32 dot of the block codes; accumulated in fp32 (partial sums
+ *   per lane, then a tree), relative error well under 1e-5 of sum_b |term|.
+ * Limits: K <= BQ_GEMV_MAX_K. Needs no workspace. */
+int bq_gemv(int type, const void *W_blocks, const float *x, float *y, int64_t M, int64_t K);
+
+/* Prefill GEMM: Y = X . W^T for N tokens; prefill reuses each weight across
+ * many tokens and is compute-bound ("05. llama.cpp…", §性能直觉).
+ * type: Q8_0 weights. W_blocks: M x K/32 blocks. X: N x K fp32 (each row
+ *   quantized to Q8_0 into the workspace first). Y: N x M fp32 (row-major,
+ *   Y[n][m]), same per-element sum as bq_gemv, fp32 accumulation.
+ * Needs a workspace of bq_workspace_size(type, M, N, K) bytes set with
+ *   bq_set_workspace, else BQ_ERR_WORKSPACE. */
+int bq_gemm(int type, const void *W_blocks, const float *X, float *Y, int64_t M, int64_t N,
+            int64_t K);
+
+/* KV-cache write, one tensor per call (K or V). rows: n_tokens x n_kv_heads x
+ * head_dim fp32. bias: NULL or n_kv_heads x head_dim fp32; when given, each row
+ * of head h becomes rows - bias[h] (one fp32 subtraction) before quantization
+ * ("kv-mean-center": lpnh.cn KV-cache article, §解法; the bias is one fp32 tensor
+ * per layer indexed by (kv-head, channel), §适用边界).
+ * A bias with a type other than Q4_0 is rejected with BQ_ERR_UNSUPPORTED (the
+ * article: mean-centering requires a q4_0 K cache and errors out otherwise,
+ * §三步上手). dst: n_tokens x n_kv_heads x head_dim/32 blocks of `type`. */
+int bq_kv_quantize(int type, const float *K_rows, const float *bias, void *dst, int64_t n_tokens,
+                   int64_t n_kv_heads, int64_t head_dim);
+
+/* Test export: out[m][b] = int32 dot of W block (m, b) (type Q4_0 or Q8_0)
+ * with the Q8_0 block b of xq, computed by the same device code as bq_gemv's
+ * inner loop. out: M x K/32 int32. */
+int bq_block_dots(int type, const void *W_blocks, const void *xq_blocks, int32_t *out, int64_t M,
+                  int64_t K);
+
+/* Stream used by the calling thread's subsequent calls (a cudaStream_t);
+ * NULL selects the legacy default stream. */
+int bq_set_stream(void *cuda_stream);
+void *bq_get_stream(void);
+
+/* Caller-owned device workspace for the calling thread (NULL, 0 clears it). */
+int bq_set_workspace(void *dev_ptr, size_t bytes);
+/* Bytes of workspace an entry point needs for these sizes (0 if none). */
+size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K);
+
+/* Thread-local message of the last failure (never NULL). */
+const char *bq_last_error(void);
+
+/* Bytes per block: 18 (Q4_0), 34 (Q8_0), 0 otherwise. */
+int bq_block_bytes(int type);
+
+/* Synchronize the calling thread's stream, then read and clear the device
+ * error word: BQ_OK, BQ_ERR_TIMEOUT if a bounded wait ran out, BQ_ERR_CUDA if
+ * the synchronization itself failed. */
+int bq_device_status(void);
+
+/* Poll budget of the bounded waits inside kernels (each poll of an mbarrier
+ * may suspend for a short, hardware-chosen time). polls < 0 restores the
+ * default (2^22); 0 makes every bounded wait give up at once, so that the
+ * timeout path can be exercised: the kernel then drains its own copies in
+ * flight, returns, and bq_device_status() reports BQ_ERR_TIMEOUT. Global to
+ * the process. */
+int bq_set_spin_limit(int64_t polls);
+
+/* Library version, (major << 16) | minor. */
+int bq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BQ_H */

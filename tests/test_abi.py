@@ -1,0 +1,174 @@
+"""The C-ABI library loads, exports every symbol include/bq.h declares, and
+rejects bad arguments on the host (no GPU needed: none of these calls reaches
+a CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, SHAPE, UNSUPPORTED, ALIGN, CUDA, TIMEOUT, WORKSPACE = 0, -1, -2, -3, -4, -5, -6, -7
+Q4, Q8 = 2, 8
+FAKE = 0x7f0000000000  # a 256-byte aligned, never dereferenced address
+
+
+def declared_functions():
+    hdr = open(os.path.join(ROOT, "include", "bq.h"), encoding="utf-8").read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(bq_[a-z_0-9]+)\s*\(", hdr)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from block_quantized_weight_row_gb300 import binding
+    if not os.path.exists(binding.library_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return binding.lib()
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_signatures_use_no_torch_types():
+    hdr = open(os.path.join(ROOT, "include", "bq.h"), encoding="utf-8").read()
+    assert "torch" not in hdr.lower().replace("no torch", "")
+    assert "at::" not in hdr and "Tensor" not in hdr
+
+
+def test_block_bytes_and_version(L):
+    assert L.bq_block_bytes(Q4) == 18
+    assert L.bq_block_bytes(Q8) == 34
+    assert L.bq_block_bytes(5) == 0
+    assert L.bq_version() >= 1
+
+
+def test_workspace_size(L):
+    assert L.bq_workspace_size(Q8, 4096, 512, 4096) == 512 * 128 * 34
+    assert L.bq_workspace_size(Q8, 1, 3, 96) == 512  # 3 x 3 x 34 = 306, rounded up to 256 bytes
+    assert L.bq_workspace_size(Q4, 1, 3, 96) == 0
+    assert L.bq_workspace_size(Q8, 1, 0, 96) == 0
+
+
+def _err(L):
+    return L.bq_last_error().decode()
+
+
+def test_unknown_type_is_unsupported(L):
+    assert L.bq_quantize_rows(3, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4096), 1, 32) == UNSUPPORTED
+    assert "unknown type" in _err(L)
+    assert L.bq_gemv(7, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 32) == UNSUPPORTED
+    assert L.bq_kv_quantize(0, ctypes.c_void_p(FAKE), None, ctypes.c_void_p(FAKE + 4096), 1, 1, 32) == UNSUPPORTED
+    assert L.bq_block_dots(1, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 32) == UNSUPPORTED
+
+
+def test_row_length_must_be_multiple_of_32(L):
+    p = ctypes.c_void_p
+    assert L.bq_quantize_rows(Q4, p(FAKE), p(FAKE + (1 << 20)), 2, 33) == SHAPE
+    assert L.bq_dequantize_rows(Q8, p(FAKE), p(FAKE + (1 << 20)), 2, 48) == SHAPE
+    assert L.bq_gemv(Q4, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 100) == SHAPE
+    assert L.bq_gemm(Q8, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 4, 100) == SHAPE
+    assert L.bq_kv_quantize(Q4, p(FAKE), None, p(FAKE + (1 << 20)), 2, 2, 40) == SHAPE
+
+
+def test_gemv_k_limit(L):
+    p = ctypes.c_void_p
+    assert L.bq_gemv(Q4, p(FAKE), p(FAKE + (1 << 30)), p(FAKE + (2 << 30)), 1, 65536 + 32) == SHAPE
+
+
+def test_null_pointers_and_negative_sizes(L):
+    p = ctypes.c_void_p
+    assert L.bq_quantize_rows(Q4, None, p(FAKE), 1, 32) == INVALID
+    assert L.bq_quantize_rows(Q4, p(FAKE), None, 1, 32) == INVALID
+    assert L.bq_quantize_rows(Q4, p(FAKE), p(FAKE + 4096), -1, 32) == INVALID
+    assert L.bq_gemv(Q4, None, p(FAKE), p(FAKE + 4096), 1, 32) == INVALID
+    assert L.bq_gemm(Q8, p(FAKE), None, p(FAKE + 4096), 1, 1, 32) == INVALID
+    assert L.bq_kv_quantize(Q4, None, None, p(FAKE), 1, 1, 32) == INVALID
+
+
+def test_alignment(L):
+    p = ctypes.c_void_p
+    assert L.bq_quantize_rows(Q4, p(FAKE + 4), p(FAKE + 4096), 1, 32) == ALIGN
+    assert L.bq_quantize_rows(Q4, p(FAKE), p(FAKE + 4098), 1, 32) == ALIGN
+    assert L.bq_gemv(Q4, p(FAKE + 2), p(FAKE + 4096), p(FAKE + 8192), 1, 32) == ALIGN
+    assert L.bq_gemv(Q4, p(FAKE), p(FAKE + 4100), p(FAKE + 8192), 1, 32) == ALIGN
+    assert L.bq_kv_quantize(Q4, p(FAKE), p(FAKE + 8), p(FAKE + 8192), 1, 1, 32) == ALIGN
+
+
+def test_aliasing_rejected(L):
+    p = ctypes.c_void_p
+    # dst inside src
+    assert L.bq_quantize_rows(Q4, p(FAKE), p(FAKE + 64), 1, 64) == INVALID
+    # y overlapping x
+    assert L.bq_gemv(Q4, p(FAKE), p(FAKE + 4096), p(FAKE + 4096), 4, 32) == INVALID
+
+
+def test_mean_centering_bias_requires_q4_0(L):
+    p = ctypes.c_void_p
+    rc = L.bq_kv_quantize(Q8, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 2, 64)
+    assert rc == UNSUPPORTED
+    assert "Q4_0" in _err(L)
+
+
+def test_gemm_takes_q8_0_only_and_needs_workspace(L):
+    p = ctypes.c_void_p
+    assert L.bq_gemm(Q4, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 4, 64) == UNSUPPORTED
+    assert L.bq_set_workspace(None, 0) == OK
+    assert L.bq_gemm(Q8, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 4, 64) == WORKSPACE
+    assert "workspace" in _err(L)
+    assert L.bq_set_workspace(p(FAKE + 8), 1024) == ALIGN
+    assert L.bq_set_workspace(p(FAKE), 0) == INVALID
+
+
+def test_empty_calls_are_noops(L):
+    p = ctypes.c_void_p
+    assert L.bq_quantize_rows(Q4, None, None, 0, 32) == OK
+    assert L.bq_quantize_rows(Q8, None, None, 5, 0) == OK
+    assert L.bq_gemv(Q4, None, None, None, 0, 4096) == OK
+    assert L.bq_gemm(Q8, None, None, None, 0, 512, 4096) == OK
+    assert L.bq_kv_quantize(Q4, None, None, None, 0, 8, 128) == OK
+    assert L.bq_block_dots(Q4, None, None, None, 0, 64) == OK
+    assert L.bq_dequantize_rows(Q4, None, None, 0, 64) == OK
+    assert _err(L) == "no error"
+    del p
+
+
+def test_stream_is_thread_local(L):
+    import threading
+    assert L.bq_set_stream(ctypes.c_void_p(0x1234)) == OK
+    seen = {}
+
+    def other():
+        seen["s"] = L.bq_get_stream()
+
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    assert L.bq_get_stream() == 0x1234
+    assert seen["s"] is None
+    assert L.bq_set_stream(None) == OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import block_quantized_weight_row_gb300 as bq
+    with pytest.raises(TypeError):
+        bq.quantize_rows(bq.Q4_0, torch.zeros(2, 32))
+    with pytest.raises(TypeError):
+        bq.gemv(bq.Q4_0, torch.zeros(18, dtype=torch.uint8), torch.zeros(32), 1, 32)
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "block_quantized_weight_row_gb300")
+    for dirpath, _dirs, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "bq_oracle" not in src, f

@@ -1,0 +1,295 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Bars: quantized bytes and integer block dots bit-exact; float outputs within
+1e-5 of sum_b |scale_w scale_x sumi_b| per element (normwise: a plain relative
+bound is ill-posed where the sum cancels to ~0). Every input is seeded and
+synthetic (block_quantized_weight_row_gb300.inputs); the oracle never sees a
+value produced by the CUDA path.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from block_quantized_weight_row_gb300.inputs import LLAMA_7B_LAYER, QWEN3_0_6B_LAYER
+
+pytestmark = pytest.mark.gpu
+
+Q4, Q8 = 2, 8
+TOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def bq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_quantized_weight_row_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return torch.device("cuda:0")
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _check_float(y, y_ref, mag, what=""):
+    y = np.asarray(y, np.float64).reshape(-1)
+    y_ref = np.asarray(y_ref, np.float64).reshape(-1)
+    mag = np.asarray(mag, np.float64).reshape(-1)
+    err = np.abs(y - y_ref)
+    bad = err > TOL * mag
+    assert not bad.any(), (f"{what}: {int(bad.sum())} outputs off; worst normwise "
+                           f"{float((err / np.maximum(mag, 1e-300)).max()):.3g}")
+    big = np.abs(y_ref) > 1e-3 * mag
+    if big.any():  # element-wise relative error where it is meaningful
+        assert float((err[big] / np.abs(y_ref[big])).max()) < 1e-3, what
+
+
+# ------------------------------------------------------------ quantize ----
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+@pytest.mark.parametrize("shape,std", [((1, 32), 1.0), ((3, 96), 0.02), ((257, 64), 1.0),
+                                       ((64, 4096), 0.02), ((7, 11008), 1.0), ((1000, 1024), 0.02),
+                                       ((1, 8192 + 32), 3.0)])
+def test_quantize_rows_bit_exact(bq, orc, dev, t, shape, std):
+    from block_quantized_weight_row_gb300 import inputs
+    x = inputs.normal(shape, std, seed=shape[0] * 7 + shape[1])
+    got = _np(bq.quantize_rows(t, x.to(dev)))
+    ref = orc.quantize_rows(t, x.numpy())
+    assert got.shape == ref.shape
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} bytes differ"
+
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+def test_quantize_adversarial_blocks(bq, orc, dev, t):
+    from block_quantized_weight_row_gb300 import inputs
+    x = inputs.adversarial_blocks()
+    x = torch.cat([x, -x, x * 1e-4, x * 3e3]).contiguous()
+    got = _np(bq.quantize_rows(t, x.to(dev)))
+    assert np.array_equal(got, orc.quantize_rows(t, x.numpy()))
+
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+def test_dequantize_bit_exact(bq, orc, dev, t):
+    from block_quantized_weight_row_gb300 import inputs
+    x = inputs.normal((37, 160), 0.5, seed=11)
+    q = orc.quantize_rows(t, x.numpy())
+    got = _np(bq.dequantize_rows(t, torch.from_numpy(q).to(dev), 160))
+    ref = orc.dequantize_rows(t, q, 160)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# --------------------------------------------------------- block dots -----
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+@pytest.mark.parametrize("M,K", [(1, 32), (5, 96), (64, 4096), (3, 11008)])
+def test_block_dots_bit_exact(bq, orc, dev, t, M, K):
+    from block_quantized_weight_row_gb300 import inputs
+    W = inputs.weight(M, K, seed=M + K)
+    x = inputs.activation(K, seed=M + K + 1)
+    wq = orc.quantize_rows(t, W.numpy())
+    xq = orc.quantize_rows(Q8, x.numpy())
+    got = _np(bq.block_dots(t, torch.from_numpy(wq).to(dev), torch.from_numpy(xq).to(dev), M, K))
+    assert np.array_equal(got, orc.block_dots(t, wq, xq, M, K))
+
+
+# ---------------------------------------------------------------- GEMV ----
+
+def _gemv_case(bq, orc, dev, t, M, K, seed, std=0.02):
+    from block_quantized_weight_row_gb300 import inputs
+    W = inputs.normal((M, K), std, seed)
+    x = inputs.activation(K, seed + 1)
+    wq = orc.quantize_rows(t, W.numpy())
+    y = _np(bq.gemv(t, torch.from_numpy(wq).to(dev), x.to(dev), M, K))
+    y_ref, mag = orc.gemv(t, wq, x.numpy(), M, K, with_mag=True)
+    _check_float(y, y_ref, mag, f"gemv t={t} M={M} K={K}")
+
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 64), (17, 96), (64, 160), (333, 288),     # ragged K
+                                 (1, 256), (3, 512), (17, 768), (64, 1280), (100, 2304),  # 1..9 groups
+                                 (1, 4096), (3, 4096), (129, 4096), (257, 11008), (5, 16384)])
+def test_gemv_shapes(bq, orc, dev, t, M, K):
+    _gemv_case(bq, orc, dev, t, M, K, seed=M * 131 + K)
+
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+def test_gemv_tiny_config(bq, orc, dev, t):
+    """1024 x 1024 ~ N(0, 0.02), x ~ N(0, 1), seed 0, both weight types."""
+    from block_quantized_weight_row_gb300 import inputs
+    W, x = inputs.tiny()
+    wq_dev = bq.quantize_rows(t, W.to(dev))
+    wq = orc.quantize_rows(t, W.numpy())
+    assert np.array_equal(_np(wq_dev), wq)
+    y = _np(bq.gemv(t, wq_dev, x.to(dev), 1024, 1024))
+    y_ref, mag = orc.gemv(t, wq, x.numpy(), 1024, 1024, with_mag=True)
+    _check_float(y, y_ref, mag, "tiny")
+
+
+@pytest.mark.parametrize("M,K", sorted({(m, k) for _n, m, k in QWEN3_0_6B_LAYER + LLAMA_7B_LAYER}))
+def test_gemv_model_shapes_full(bq, orc, dev, M, K):
+    """Every distinct matrix shape of the 0.6B and 7B decode steps, whole
+    matrix, Q4_0; also checks the GPU row quantizer on the full matrix."""
+    from block_quantized_weight_row_gb300 import inputs
+    W = inputs.weight(M, K, seed=M + 3 * K)
+    x = inputs.activation(K, seed=M + 3 * K + 1)
+    wq_dev = bq.quantize_rows(Q4, W.to(dev))
+    wq = orc.quantize_rows(Q4, W.numpy())
+    assert np.array_equal(_np(wq_dev), wq)
+    y = _np(bq.gemv(Q4, wq_dev, x.to(dev), M, K))
+    y_ref, mag = orc.gemv(Q4, wq, x.numpy(), M, K, with_mag=True)
+    _check_float(y, y_ref, mag, f"model shape {M}x{K}")
+
+
+def test_gemv_on_side_stream(bq, orc, dev):
+    """Quantize then GEMV enqueued on a non-default stream, no sync in between."""
+    from block_quantized_weight_row_gb300 import inputs
+    W = inputs.weight(512, 4096, seed=5)
+    x = inputs.activation(4096, seed=6)
+    s = torch.cuda.Stream(dev)
+    Wd, xd = W.to(dev), x.to(dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        wq = bq.quantize_rows(Q4, Wd)
+        y = bq.gemv(Q4, wq, xd, 512, 4096)
+    s.synchronize()
+    wq_ref = orc.quantize_rows(Q4, W.numpy())
+    y_ref, mag = orc.gemv(Q4, wq_ref, x.numpy(), 512, 4096, with_mag=True)
+    _check_float(_np(y), y_ref, mag, "side stream")
+
+
+def test_gemv_k_zero_gives_zeros(bq, dev):
+    y = torch.full((7,), 5.0, device=dev)
+    bq.gemv(Q4, torch.empty(16, dtype=torch.uint8, device=dev), torch.empty(4, device=dev), 0, 0)
+    bq.gemv(Q4, torch.empty(16, dtype=torch.uint8, device=dev), torch.empty(4, device=dev), 7, 0, out=y)
+    assert torch.all(y == 0)
+
+
+def test_gemv_timeout_path_returns_error(bq, orc, dev):
+    """With a poll budget of 0 every bounded wait gives up at once: the kernel
+    drains its own copies, returns, and the status reports the timeout; the
+    next call with the default budget is correct again."""
+    from block_quantized_weight_row_gb300 import binding, inputs
+    L = binding.lib()
+    W = inputs.weight(256, 4096, seed=9)
+    x = inputs.activation(4096, seed=10)
+    wq = bq.quantize_rows(Q4, W.to(dev))
+    assert binding.device_status() == 0
+    try:
+        assert L.bq_set_spin_limit(0) == 0
+        bq.gemv(Q4, wq, x.to(dev), 256, 4096)
+        assert binding.device_status() == -6
+    finally:
+        L.bq_set_spin_limit(-1)
+    y = bq.gemv(Q4, wq, x.to(dev), 256, 4096)
+    assert binding.device_status() == 0
+    y_ref, mag = orc.gemv(Q4, orc.quantize_rows(Q4, W.numpy()), x.numpy(), 256, 4096, with_mag=True)
+    _check_float(_np(y), y_ref, mag, "after timeout")
+
+
+# ---------------------------------------------------------------- GEMM ----
+
+@pytest.mark.parametrize("M,N,K", [(64, 16, 256), (130, 70, 512), (33, 5, 96), (256, 128, 4096),
+                                   (200, 65, 2304), (1, 1, 32), (128, 64, 11008)])
+def test_gemm_shapes(bq, orc, dev, M, N, K):
+    from block_quantized_weight_row_gb300 import inputs
+    W = inputs.weight(M, K, seed=M * 7 + K)
+    X = inputs.activation(K, seed=N * 3 + K, rows=N)
+    wq = orc.quantize_rows(Q8, W.numpy())
+    Y = _np(bq.gemm(Q8, torch.from_numpy(wq).to(dev), X.to(dev), M, N, K))
+    Y_ref, mag = orc.gemm(Q8, wq, X.numpy(), M, N, K, with_mag=True)
+    _check_float(Y, Y_ref, mag, f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,K", [(4096, 4096), (11008, 4096), (4096, 11008)])
+def test_gemm_prefill_config_sampled(bq, orc, dev, M, K):
+    """512 tokens at full size; 48 sampled tokens x 96 sampled weight rows
+    are recomputed by the oracle (each output depends on one row of each)."""
+    from block_quantized_weight_row_gb300 import inputs
+    N = 512
+    W = inputs.weight(M, K, seed=inputs.seed_of("prefill-q8_0", 0, M // 1000 + K // 1000), device=dev)
+    X = inputs.activation(K, seed=inputs.seed_of("prefill-q8_0", 1, K // 1000), device=dev, rows=N)
+    wq = bq.quantize_rows(Q8, W)
+    Y = _np(bq.gemm(Q8, wq, X, M, N, K))
+    rng = np.random.default_rng(M + K)
+    ns = np.sort(rng.choice(N, 48, replace=False))
+    ms = np.sort(rng.choice(M, 96, replace=False))
+    W_s = _np(W[torch.from_numpy(ms).to(dev)])
+    X_s = _np(X[torch.from_numpy(ns).to(dev)])
+    wq_s = orc.quantize_rows(Q8, W_s)
+    assert np.array_equal(_np(wq[torch.from_numpy(ms).to(dev)]), wq_s)
+    Y_ref, mag = orc.gemm(Q8, wq_s, X_s, len(ms), len(ns), K, with_mag=True)
+    _check_float(Y[np.ix_(ns, ms)], Y_ref, mag, f"prefill {M}x{K}")
+
+
+def test_gemm_errors(bq, dev):
+    from block_quantized_weight_row_gb300 import binding
+    wq = torch.zeros(64 * 34, dtype=torch.uint8, device=dev)
+    with pytest.raises(binding.BQError) as e:
+        bq.gemm(Q4, wq, torch.zeros(2, 64, device=dev), 2, 2, 64)
+    assert e.value.status == -3
+
+
+# ----------------------------------------------------------- KV write -----
+
+@pytest.mark.parametrize("tokens", [1, 37, 1024])
+def test_kv_write_bit_exact(bq, orc, dev, tokens):
+    from block_quantized_weight_row_gb300 import inputs
+    L = inputs.kv_layer(2, tokens=tokens, kv_heads=8, head_dim=128, calib_tokens=64)
+    bias = L.K_calib.double().mean(dim=0).float()
+    kq = _np(bq.kv_quantize(Q4, L.K.to(dev), bias.to(dev)))
+    assert np.array_equal(kq, orc.kv_quantize(Q4, L.K.numpy(), bias.numpy(), tokens, 8, 128))
+    vq = _np(bq.kv_quantize(Q8, L.V.to(dev), None))
+    assert np.array_equal(vq, orc.kv_quantize(Q8, L.V.numpy(), None, tokens, 8, 128))
+    k_plain = _np(bq.kv_quantize(Q4, L.K.to(dev), None))
+    assert np.array_equal(k_plain, orc.kv_quantize(Q4, L.K.numpy(), None, tokens, 8, 128))
+
+
+def test_kv_write_full_layer(bq, orc, dev):
+    """One layer of the KV-write workload at full size: 32768 tokens x 8 kv
+    heads x 128, K with the calibrated bias to Q4_0 and V to Q8_0."""
+    from block_quantized_weight_row_gb300 import inputs
+    cfg = inputs.WORKLOADS["kv-write"]
+    L = inputs.kv_layer(0, cfg["tokens"], cfg["kv_heads"], cfg["head_dim"], cfg["calib_tokens"], device=dev)
+    bias = L.K_calib.double().mean(dim=0).float()
+    kq = _np(bq.kv_quantize(Q4, L.K, bias))
+    vq = _np(bq.kv_quantize(Q8, L.V, None))
+    T, H, D = L.K.shape
+    assert np.array_equal(kq, orc.kv_quantize(Q4, _np(L.K), _np(bias), T, H, D))
+    assert np.array_equal(vq, orc.kv_quantize(Q8, _np(L.V), None, T, H, D))
+
+
+def test_kv_mean_centering_keeps_softmax_and_helps(bq, dev):
+    """GPU-written cache: adding the bias back after dequantization recovers K
+    within half a scale step, and centering lowers the attention KL against
+    the fp32 cache (softmax(z + c) = softmax(z) makes the bias free)."""
+    from block_quantized_weight_row_gb300 import inputs
+    T, H, D = 2048, 8, 128
+    L = inputs.kv_layer(3, tokens=T, kv_heads=H, head_dim=D, calib_tokens=512, device=dev)
+    bias = L.K_calib.double().mean(dim=0).float()
+    kc = bq.kv_quantize(Q4, L.K, bias)
+    kp = bq.kv_quantize(Q4, L.K, None)
+    Kc = bq.dequantize_rows(Q4, kc, D).view(T, H, D) + bias
+    Kp = bq.dequantize_rows(Q4, kp, D).view(T, H, D)
+    d = kc.view(T * H * D // 32, 18)[:, :2].contiguous().view(torch.float16).float().view(T, H, D // 32, 1)
+    err = (Kc - L.K).view(T, H, D // 32, 32).abs()
+    assert bool(torch.all(err <= d / 2 * (1 + 2.0 ** -18) + 1e-6))
+    q = inputs.normal((64, H, D), 1.0, 97, device=dev).double()
+    ref = torch.softmax(torch.einsum("qhd,thd->hqt", q, L.K.double()) / math.sqrt(D), dim=-1)
+    kl = {}
+    for name, Kq in (("centered", Kc), ("plain", Kp)):
+        p = torch.softmax(torch.einsum("qhd,thd->hqt", q, Kq.double()) / math.sqrt(D), dim=-1)
+        kl[name] = float((ref * (ref.log() - p.log())).sum(-1).mean())
+    assert kl["centered"] < kl["plain"]
+
+
+def test_kv_bias_with_q8_0_rejected(bq, dev):
+    from block_quantized_weight_row_gb300 import binding
+    with pytest.raises(binding.BQError) as e:
+        bq.kv_quantize(Q8, torch.zeros(2, 2, 64, device=dev), torch.zeros(2, 64, device=dev))
+    assert e.value.status == -3
