@@ -101,6 +101,18 @@ const DeviceInfo *device_info(cudaError_t *err) {
 
 uint32_t spin_limit() { return g_spin_limit; }
 
+int report_error(int status, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_error = buf;
+  return status;
+}
+
+int report_ok() { return ok(); }
+
 namespace {
 struct SmemEntry {
   int device;

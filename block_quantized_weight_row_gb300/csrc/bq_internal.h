@@ -28,6 +28,11 @@ uint32_t spin_limit();
 // stream capture make no attribute calls after the first, uncaptured one).
 cudaError_t ensure_smem(const void *func, int bytes);
 
+// Record a failure message for bq_last_error() on the calling thread and
+// return `status`; report_ok() records "no error" and returns BQ_OK.
+int report_error(int status, const char *fmt, ...);
+int report_ok();
+
 // Launchers; each returns the launch status. Sizes were validated by the ABI layer.
 cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64_t n_blocks,
                                  int64_t blocks_per_row, const float *bias, int64_t bias_period,

@@ -115,6 +115,27 @@ int bq_kv_quantize(int type, const float *K_rows, const float *bias, void *dst, 
 int bq_block_dots(int type, const void *W_blocks, const void *xq_blocks, int32_t *out, int64_t M,
                   int64_t K);
 
+/* Bytes of the static scratch array that bq_gemm_noalloc uses (8 MiB). */
+#define BQ_GEMM_NOALLOC_SCRATCH_BYTES (8 << 20)
+
+/* Prefill GEMM that allocates nothing and needs no workspace. The pages have
+ * no counterpart: this entry point exists for callers that cannot allocate
+ * device memory when they call (a plugin hook that must not call cudaMalloc
+ * while it runs, a process whose device memory is fixed after start-up) and
+ * have no workspace of their own to lend.
+ * Same arguments, layouts and result as bq_gemm (Q8_0 weights only). The
+ * Q8_0 activations go to a file-scope device array of
+ * BQ_GEMM_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits; N * (K/32) * 34 bytes beyond it are rejected with
+ * BQ_ERR_WORKSPACE. The call makes no cudaMalloc, cudaFree or other allocating
+ * call. Its first call on a device looks up the array's device address with
+ * that device current; make that first call before any stream capture. All
+ * calls share the one array (every call overwrites the part it uses before
+ * reading it), so calls that overlap on the GPU race: issue them on one
+ * stream, or order them. */
+int bq_gemm_noalloc(int type, const void *W_blocks, const float *X, float *Y, int64_t M, int64_t N,
+                    int64_t K);
+
 /* Stream used by the calling thread's subsequent calls (a cudaStream_t);
  * NULL selects the legacy default stream. */
 int bq_set_stream(void *cuda_stream);
