@@ -225,14 +225,31 @@ def build_decode_step(workload, dev, bq, inputs, pool_x=True):
         del W
         o = x_off[e.x_key]
         mats.append((wq, x_all[o:o + e.K], y_all[y_off[i]:y_off[i] + e.M], e.M, e.K))
+    # matrices that read the same activation (q/k/v, gate/up) form one launch
+    groups = []
+    for (wq, x, y, M, K), e in zip(mats, plan):
+        if groups and groups[-1]["key"] == e.x_key:
+            g = groups[-1]
+        else:
+            g = {"key": e.x_key, "x": x, "K": K, "w": [], "y": [], "M": []}
+            groups.append(g)
+        g["w"].append(wq)
+        g["y"].append(y)
+        g["M"].append(M)
     torch.cuda.synchronize(dev)
     wbytes = sum(e.M * (e.K // 32) * 18 for e in plan)
-    return {"plan": plan, "mats": mats, "x_all": x_all, "y_all": y_all, "weight_bytes": wbytes}
+    return {"plan": plan, "mats": mats, "groups": groups, "x_all": x_all, "y_all": y_all, "weight_bytes": wbytes}
 
 
-def run_step(step, bq):
-    for wq, x, y, M, K in step["mats"]:
-        bq.gemv(bq.Q4_0, wq, x, M, K, out=y)
+def run_step(step, bq, batched=True):
+    """One decode token: every matrix once, in layer order. batched: one
+    launch per group of matrices sharing an input; else one per matrix."""
+    if batched:
+        for g in step["groups"]:
+            bq.gemv_multi(bq.Q4_0, g["w"], g["x"], g["M"], g["K"], outs=g["y"])
+    else:
+        for wq, x, y, M, K in step["mats"]:
+            bq.gemv(bq.Q4_0, wq, x, M, K, out=y)
 
 
 def capture(fn, stream):
@@ -323,8 +340,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-prefetch", action="store_true",
+                    help="launch each GEMV only after the previous kernel completed")
+    ap.add_argument("--no-batch", action="store_true",
+                    help="one launch per matrix instead of one per group of matrices sharing an input")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "gemm", "kv"), default=None,
+                    help="run one kernel case a few times and exit (for profiler captures)")
+    ap.add_argument("--case-launches", type=int, default=16)
     args = ap.parse_args()
+    if args.kernel_case:
+        return kernel_case(args.kernel_case, args.case_launches)
     if args.warmup < 3:
         args.warmup = 3
 
@@ -342,16 +368,20 @@ def main():
     peaks = load_peaks()
     stream = torch.cuda.Stream(dev)
 
-    # ---- headline: 7B decode step
+    # ---- headline: 7B decode step. Model weights are written once, before
+    # the step, so every GEMV may stream its weights while the previous
+    # kernel on the stream finishes (programmatic dependent launch).
     step = build_decode_step("7b-decode", dev, bq, inputs)
-    g = capture(lambda: run_step(step, bq), stream)
+    binding.set_weight_prefetch(not args.no_prefetch)
+    batched = not args.no_batch
+    g = capture(lambda: run_step(step, bq, batched), stream)
     clocks = ClockSampler(local) if rank == 0 else None
     ms = time_graph(g, stream, args.steps, args.warmup, dist, clocks)
     if clocks:
         clocks.close()
     ms_max = max_over_ranks(ms, dist)
     value = aggregate_rate(step["weight_bytes"], world, ms_max * 1e-3) / 1e9
-    launches = len(step["mats"]) * args.steps
+    launches = (len(step["groups"]) if batched else len(step["mats"])) * args.steps
 
     # ---- roofline: the dominant kernel alone on distinct 11008 x 4096 matrices
     gate_up = [m for m, e in zip(step["mats"], step["plan"]) if e.name in ("gate", "up")]
@@ -387,7 +417,11 @@ def main():
                                    "down 4096x11008}, batch 1, Q4_0 weights, 224 GEMVs per step",
                        "weight_bytes_per_step": step["weight_bytes"],
                        "l2": "inputs larger than L2 (3.64 GB of weights per step)",
-                       "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step"},
+                       "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step",
+                       "weight_prefetch": not args.no_prefetch,
+                       "launches_per_step": len(step["groups"]) if batched else len(step["mats"]),
+                       "batching": "q/k/v and gate/up share one launch each (one x)" if batched
+                                   else "one launch per matrix"},
             "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
             "tokens_per_s_equiv": round(1e3 / ms_max, 1),
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
@@ -408,14 +442,14 @@ def e2e_decode(step, stream, dev, args, dist, world):
     L = binding.lib()
     x_host = step["x_all"].cpu().pin_memory()
     y_host = torch.empty(step["y_all"].numel(), dtype=torch.float32).pin_memory()
-    calls = [(ctypes.c_void_p(wq.data_ptr()), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
-              M, K) for wq, x, y, M, K in step["mats"]]
-    f = L.bq_gemv
+    calls = [(*binding.gemv_multi_args(g["w"], g["y"], g["M"]), ctypes.c_void_p(g["x"].data_ptr()), g["K"])
+             for g in step["groups"]]
+    f = L.bq_gemv_multi
 
     def one():
         step["x_all"].copy_(x_host, non_blocking=True)
-        for w, x, y, M, K in calls:
-            rc = f(2, w, x, y, M, K)
+        for n_, W_, Y_, M_, x_, K_ in calls:
+            rc = f(2, n_, W_, Y_, M_, x_, K_)
             if rc:
                 raise binding.BQError(rc, L.bq_last_error().decode())
         y_host.copy_(step["y_all"], non_blocking=True)
@@ -437,7 +471,7 @@ def e2e_decode(step, stream, dev, args, dist, world):
     ms = max_over_ranks(e0.elapsed_time(e1) / n, dist)
     return {"value": round(aggregate_rate(step["weight_bytes"], world, ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(step["x_all"].numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4),
-            "ms_per_step": round(ms, 4), "steps": n, "path": "direct C-ABI calls (no graph)"}
+            "ms_per_step": round(ms, 4), "steps": n, "path": "direct bq_gemv_multi C-ABI calls (no graph)"}
 
 
 def l2_flusher(dev):
@@ -506,13 +540,51 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
 
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps
     q = build_decode_step("qwen3-0.6b-decode", dev, bq, inputs)
-    g = capture(lambda: run_step(q, bq), stream)
+    g = capture(lambda: run_step(q, bq, True), stream)
     ms = max_over_ranks(time_graph(g, stream, 50, 5, between=flush), dist)
     out["qwen3_0_6b_decode"] = {"metric": "Q4_0 decode GEMV weight GB/s", "unit": "GB/s",
                                 "value": round(aggregate_rate(q["weight_bytes"], world, ms * 1e-3) / 1e9, 1),
                                 "ms_per_step": round(ms, 4), "weight_bytes_per_step": q["weight_bytes"],
-                                "gemvs_per_step": len(q["mats"]), "l2": "flushed between steps"}
+                                "gemvs_per_step": len(q["mats"]), "launches_per_step": len(q["groups"]),
+                                "l2": "flushed between steps"}
     return out
+
+
+def kernel_case(name, launches):
+    """A small, self-contained case of one kernel for profiler captures:
+    inputs larger than L2 (rotated over distinct buffers) but well under a
+    few GB on the device."""
+    import torch
+    import block_quantized_weight_row_gb300 as bq
+    from block_quantized_weight_row_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if name in ("gemv", "gemv-q8"):
+        t = bq.Q4_0 if name == "gemv" else bq.Q8_0
+        M, K = 11008, 4096
+        mats = []
+        for i in range(8):  # 8 x 25.4 MB (Q4_0) or 48 MB (Q8_0): beyond L2
+            mats.append(bq.quantize_rows(t, inputs.weight(M, K, 7000 + i, device=dev)))
+        x = inputs.activation(K, 7100, device=dev)
+        y = torch.empty(M, device=dev)
+        for i in range(launches):
+            bq.gemv(t, mats[i % len(mats)], x, M, K, out=y)
+    elif name == "gemm":
+        M, N, K = 4096, 512, 4096
+        wq = bq.quantize_rows(bq.Q8_0, inputs.weight(M, K, 7200, device=dev))
+        X = inputs.activation(K, 7201, device=dev, rows=N)
+        Y = torch.empty((N, M), device=dev)
+        for _ in range(launches):
+            bq.gemm(bq.Q8_0, wq, X, M, N, K, out=Y)
+    elif name == "kv":
+        kv = inputs.WORKLOADS["kv-write"]
+        L_ = inputs.kv_layer(0, kv["tokens"], kv["kv_heads"], kv["head_dim"], kv["calib_tokens"], device=dev)
+        bias = L_.K_calib.double().mean(dim=0).float().contiguous()
+        for _ in range(launches):
+            bq.kv_quantize(bq.Q4_0, L_.K, bias)
+            bq.kv_quantize(bq.Q8_0, L_.V, None)
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel_case": name, "launches": launches, "ok": True}))
 
 
 def reference_arm(args, world, rank):

@@ -51,6 +51,7 @@ def lib():
         "bq_quantize_rows": ([i, vp, vp, i64, i64], i),
         "bq_dequantize_rows": ([i, vp, vp, i64, i64], i),
         "bq_gemv": ([i, vp, vp, vp, i64, i64], i),
+        "bq_gemv_multi": ([i, i, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64), vp, i64], i),
         "bq_gemm": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_kv_quantize": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_block_dots": ([i, vp, vp, vp, i64, i64], i),
@@ -58,11 +59,13 @@ def lib():
         "bq_get_stream": ([], vp),
         "bq_set_workspace": ([vp, sz], i),
         "bq_workspace_size": ([i, i64, i64, i64], sz),
+        "bq_gemv_workspace_size": ([i, i64], sz),
         "bq_last_error": ([], ctypes.c_char_p),
         "bq_block_bytes": ([i], i),
         "bq_device_status": ([], i),
         "bq_version": ([], i),
         "bq_set_spin_limit": ([i64], i),
+        "bq_set_weight_prefetch": ([i], i),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -87,6 +90,11 @@ def _prep(device):
     s = torch.cuda.current_stream(device)
     _check(L.bq_set_stream(ctypes.c_void_p(s.cuda_stream)), "bq_set_stream")
     return L
+
+
+def clear_workspace() -> None:
+    """Detach the calling thread's workspace (GEMVs then quantize x in-kernel)."""
+    _check(lib().bq_set_workspace(None, 0), "bq_set_workspace")
 
 
 def _workspace(device, nbytes: int):
@@ -145,8 +153,32 @@ def gemv(t: int, w_blocks: torch.Tensor, x: torch.Tensor, M: int, K: int,
     if out is None:
         out = torch.empty(M, dtype=torch.float32, device=x.device)
     L = _prep(x.device)
+    _workspace(x.device, int(L.bq_gemv_workspace_size(t, K)))
     _check(L.bq_gemv(t, _ptr(w_blocks), _ptr(x), _ptr(out), M, K), "bq_gemv")
     return out
+
+
+def gemv_multi_args(w_list, y_list, M_list):
+    """ctypes arrays (W pointers, y pointers, row counts) for bq_gemv_multi."""
+    n = len(w_list)
+    W = (ctypes.c_void_p * n)(*[w.data_ptr() for w in w_list])
+    Y = (ctypes.c_void_p * n)(*[y.data_ptr() for y in y_list])
+    M = (ctypes.c_int64 * n)(*M_list)
+    return n, W, Y, M
+
+
+def gemv_multi(t: int, w_list, x: torch.Tensor, M_list, K: int, outs=None):
+    """y_i = W_i . x for matrices sharing one input x, in one launch."""
+    for w in w_list:
+        _cuda(w, "w_blocks")
+    _cuda(x, "x")
+    if outs is None:
+        outs = [torch.empty(m, dtype=torch.float32, device=x.device) for m in M_list]
+    n, W, Y, M = gemv_multi_args(w_list, outs, M_list)
+    L = _prep(x.device)
+    _workspace(x.device, int(L.bq_gemv_workspace_size(t, K)))
+    _check(L.bq_gemv_multi(t, n, W, Y, M, _ptr(x), K), "bq_gemv_multi")
+    return outs
 
 
 def gemm(t: int, w_blocks: torch.Tensor, X: torch.Tensor, M: int, N: int, K: int,
@@ -184,6 +216,13 @@ def block_dots(t: int, w_blocks: torch.Tensor, xq_blocks: torch.Tensor, M: int, 
     L = _prep(w_blocks.device)
     _check(L.bq_block_dots(t, _ptr(w_blocks), _ptr(xq_blocks), _ptr(out), M, K), "bq_block_dots")
     return out
+
+
+def set_weight_prefetch(enable: bool) -> None:
+    """Let the calling thread's GEMVs stream weights before the previous
+    kernel on the stream has completed (only for weights no running kernel
+    writes)."""
+    _check(lib().bq_set_weight_prefetch(1 if enable else 0), "bq_set_weight_prefetch")
 
 
 def device_status() -> int:

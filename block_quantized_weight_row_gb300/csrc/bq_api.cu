@@ -3,6 +3,7 @@
 // and the device error word that bounded in-kernel waits report through.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -22,6 +23,7 @@ constexpr int kMaxDevices = 64;
 constexpr uint32_t kDefaultSpinLimit = 1u << 22;
 
 thread_local cudaStream_t t_stream = nullptr;
+thread_local bool t_weight_prefetch = false;
 thread_local void *t_ws = nullptr;
 thread_local size_t t_ws_bytes = 0;
 thread_local std::string t_error = "no error";
@@ -101,6 +103,13 @@ const DeviceInfo *device_info(cudaError_t *err) {
 
 uint32_t spin_limit() { return g_spin_limit; }
 
+bool weight_prefetch() { return t_weight_prefetch; }
+
+int tuning_value(const char *name) {
+  const char *v = getenv(name);
+  return v ? atoi(v) : 0;
+}
+
 int report_error(int status, const char *fmt, ...) {
   char buf[512];
   va_list ap;
@@ -160,6 +169,11 @@ int bq_set_stream(void *cuda_stream) {
 
 void *bq_get_stream(void) { return t_stream; }
 
+int bq_set_weight_prefetch(int enable) {
+  t_weight_prefetch = enable != 0;
+  return ok();
+}
+
 int bq_set_workspace(void *dev_ptr, size_t bytes) {
   if ((dev_ptr == nullptr) != (bytes == 0))
     return fail(BQ_ERR_INVALID_ARG, "bq_set_workspace: pointer and size must be both set or both empty");
@@ -174,6 +188,11 @@ size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K) {
   if (type != BQ_TYPE_Q8_0 || N <= 0 || K <= 0 || K % kQK) return 0;
   const size_t bytes = size_t(N) * size_t(K / kQK) * Fmt<kTypeQ8_0>::kBytes;
   return (bytes + 255) / 256 * 256;
+}
+
+size_t bq_gemv_workspace_size(int type, int64_t K) {
+  if (!block_bytes(type)) return 0;
+  return gemv_workspace_bytes(K);
 }
 
 int bq_set_spin_limit(int64_t polls) {
@@ -226,26 +245,58 @@ int bq_dequantize_rows(int type, const void *blocks, float *dst, int64_t n_rows,
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_dequantize_rows launch");
 }
 
-int bq_gemv(int type, const void *W, const float *x, float *y, int64_t M, int64_t K) {
+int bq_gemv_multi(int type, int n, const void *const *W, float *const *y, const int64_t *M, const float *x,
+                  int64_t K) {
   const int bb = block_bytes(type);
   if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_gemv: unknown type %d", type);
-  if (!sizes_ok(M, K)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: bad sizes");
+  if (n < 1 || n > BQ_GEMV_MAX_MATS) return fail(BQ_ERR_SHAPE, "bq_gemv_multi: n %d not in 1..%d", n, BQ_GEMV_MAX_MATS);
+  if (!W || !y || !M) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_multi: null array");
+  if (K < 0) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: negative K");
   if (K % kQK) return fail(BQ_ERR_SHAPE, "bq_gemv: K %lld is not a multiple of 32", (long long)K);
   if (K > BQ_GEMV_MAX_K) return fail(BQ_ERR_SHAPE, "bq_gemv: K %lld exceeds %d", (long long)K, BQ_GEMV_MAX_K);
-  if (M > 0x7fffffffll) return fail(BQ_ERR_SHAPE, "bq_gemv: M %lld exceeds 2^31-1", (long long)M);
-  if (M == 0) return ok();
-  if (!y || (K > 0 && (!W || !x))) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: null pointer");
-  if (!aligned(y, 4) || (K > 0 && (!aligned(W, 16) || !aligned(x, 16))))
-    return fail(BQ_ERR_ALIGN, "bq_gemv: W and x must be 16-byte aligned, y 4-byte aligned");
-  const size_t wbytes = size_t(M) * size_t(K / kQK) * bb;
-  if (overlap(y, size_t(M) * 4, W, wbytes) || overlap(y, size_t(M) * 4, x, size_t(K) * 4))
-    return fail(BQ_ERR_INVALID_ARG, "bq_gemv: y overlaps an input");
-  cudaError_t e;
-  if (K == 0)
-    e = cudaMemsetAsync(y, 0, size_t(M) * 4, t_stream);
-  else
-    e = launch_gemv(type, static_cast<const uint8_t *>(W), x, y, M, K, t_stream);
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    if (M[i] < 0) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: negative M");
+    total += M[i];
+    if (total > 0x7fffffffll) return fail(BQ_ERR_SHAPE, "bq_gemv: rows exceed 2^31-1");
+  }
+  if (total == 0) return ok();
+  for (int i = 0; i < n; ++i) {
+    if (M[i] == 0) continue;
+    if (!y[i] || (K > 0 && (!W[i] || !x))) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: null pointer");
+    if (!aligned(y[i], 4) || (K > 0 && (!aligned(W[i], 16) || !aligned(x, 16))))
+      return fail(BQ_ERR_ALIGN, "bq_gemv: W and x must be 16-byte aligned, y 4-byte aligned");
+    const size_t ybytes = size_t(M[i]) * 4;
+    if (overlap(y[i], ybytes, x, size_t(K) * 4)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: y overlaps x");
+    for (int j = 0; j < n; ++j) {
+      if (M[j] == 0) continue;
+      if (overlap(y[i], ybytes, W[j], size_t(M[j]) * size_t(K / kQK) * bb))
+        return fail(BQ_ERR_INVALID_ARG, "bq_gemv: y overlaps a weight matrix");
+      if (j != i && overlap(y[i], ybytes, y[j], size_t(M[j]) * 4))
+        return fail(BQ_ERR_INVALID_ARG, "bq_gemv_multi: outputs overlap");
+    }
+  }
+  cudaError_t e = cudaSuccess;
+  if (K == 0) {
+    for (int i = 0; i < n && e == cudaSuccess; ++i)
+      if (M[i] > 0) e = cudaMemsetAsync(y[i], 0, size_t(M[i]) * 4, t_stream);
+  } else {
+    // with a large enough workspace, x is quantized once by a prep kernel that
+    // also prefetches the weights into L2; otherwise every CTA quantizes x
+    const size_t need = gemv_workspace_bytes(K);
+    uint32_t *rec = (need && t_ws && t_ws_bytes >= need) ? static_cast<uint32_t *>(t_ws) : nullptr;
+    if (rec && (overlap(rec, need, x, size_t(K) * 4)))
+      return fail(BQ_ERR_INVALID_ARG, "bq_gemv: workspace overlaps x");
+    for (int i = 0; rec && i < n; ++i)
+      if (M[i] > 0 && overlap(rec, need, y[i], size_t(M[i]) * 4))
+        return fail(BQ_ERR_INVALID_ARG, "bq_gemv: workspace overlaps y");
+    e = launch_gemv(type, n, reinterpret_cast<const uint8_t *const *>(W), y, M, x, K, rec, t_stream);
+  }
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemv launch");
+}
+
+int bq_gemv(int type, const void *W, const float *x, float *y, int64_t M, int64_t K) {
+  return bq_gemv_multi(type, 1, &W, &y, &M, x, K);
 }
 
 int bq_gemm(int type, const void *W, const float *X, float *Y, int64_t M, int64_t N, int64_t K) {

@@ -59,11 +59,21 @@ __device__ __forceinline__ void block_scale(float amax, uint16_t &bits, float &d
   ds = __half2float(h);
 }
 
-// code of one value: round-half-even of x / stored scale (IEEE division), clamped
+// code of one value: round-half-even of the IEEE fp32 quotient x / ds, clamped.
+//
+// The quotient is formed as r = x * rn(1/ds) (one correctly rounded
+// reciprocal per block, one multiply per value). r is within 2 ulp of the
+// correctly rounded quotient q = rn(x / ds), so rint(r) == rint(q) unless a
+// half-integer lies within that distance of r; values whose distance to the
+// nearest integer is that close to 0.5 (a band of 4e-5 * max(|r|, 1), far
+// wider than 2 ulp) take the exact IEEE division instead. The result is
+// bit-identical to rint(rn(x / ds)) for every input; only the cost differs.
 template <int TYPE>
-__device__ __forceinline__ int code_of(float x, float ds) {
-  if (ds == 0.0f) return 0;
-  const int q = __float2int_rn(__fdiv_rn(x, ds));
+__device__ __forceinline__ int code_of(float x, float ds, float inv) {
+  float r = __fmul_rn(x, inv);
+  float n = rintf(r);
+  if (fabsf(__fsub_rn(r, n)) > 0.5f - 4e-5f * fmaxf(fabsf(r), 1.0f)) n = rintf(__fdiv_rn(x, ds));
+  const int q = __float2int_rz(n);  // n is integral
   return min(max(q, Fmt<TYPE>::kQmin), Fmt<TYPE>::kQmax);
 }
 
@@ -87,8 +97,14 @@ __device__ __forceinline__ BlockCodes<TYPE> quantize_block8(float4 v) {
   BlockCodes<TYPE> r;
   float ds;
   block_scale<TYPE>(group8_max(amax4(v)), r.scale, ds);
-  const int q0 = code_of<TYPE>(v.x, ds), q1 = code_of<TYPE>(v.y, ds);
-  const int q2 = code_of<TYPE>(v.z, ds), q3 = code_of<TYPE>(v.w, ds);
+  int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+  if (ds != 0.0f) {  // a zero scale (all-zero or underflowing block) gives all codes 0
+    const float inv = __frcp_rn(ds);
+    q0 = code_of<TYPE>(v.x, ds, inv);
+    q1 = code_of<TYPE>(v.y, ds, inv);
+    q2 = code_of<TYPE>(v.z, ds, inv);
+    q3 = code_of<TYPE>(v.w, ds, inv);
+  }
   if (TYPE == kTypeQ4_0) {
     r.bytes4 = uint32_t(q0 + 8) | (uint32_t(q1 + 8) << 8) | (uint32_t(q2 + 8) << 16) |
                (uint32_t(q3 + 8) << 24);
@@ -125,15 +141,18 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
 
 // Integer dot of one Q4_0 block (qs as 4 words) with one Q8_0 block (codes as
 // 8 words, xsum = sum of its 32 codes): sum_j (nib_j - 8) * qx_j, computed as
-// sum_j nib_j * qx_j - 8 * xsum. Exact in int32.
+// sum_j nib_j * qx_j - 8 * xsum. The high nibbles are used in place (bytes
+// 16 * nib, no shift): their dot is 16 times the wanted one, so it is shifted
+// right by 4 at the end, which is exact because every term is a multiple of
+// 16. All of it is exact in int32.
 __device__ __forceinline__ int sumi_q4_q8(const uint32_t qs[4], const uint32_t xw[8], int xsum) {
-  int s = 0;
+  int lo = 0, hi = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    s = dp4a_us(qs[i] & 0x0f0f0f0fu, xw[i], s);          // elements 4i..4i+3
-    s = dp4a_us((qs[i] >> 4) & 0x0f0f0f0fu, xw[4 + i], s);  // elements 16+4i..
+    lo = dp4a_us(qs[i] & 0x0f0f0f0fu, xw[i], lo);      // elements 4i..4i+3
+    hi = dp4a_us(qs[i] & 0xf0f0f0f0u, xw[4 + i], hi);  // 16 x elements 16+4i..
   }
-  return s - 8 * xsum;
+  return lo + (hi >> 4) - 8 * xsum;
 }
 
 // Integer dot of one Q8_0 block with another.
@@ -207,6 +226,20 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start, and
+// wait until the previous one has completed and its writes are visible. Both
+// are no-ops when the launch did not opt in.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Ask L2 to fetch [src, src + bytes) from memory; no completion, no data
+// returned (src and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "bq.h"
+
 namespace bq {
 
 struct DeviceInfo {
@@ -23,6 +25,14 @@ const DeviceInfo *device_info(cudaError_t *err);
 // Poll budget of the bounded mbarrier waits inside kernels.
 uint32_t spin_limit();
 
+// Whether bq_gemv may stream weights before the previous kernel on the stream
+// has completed (calling thread's setting, see bq_set_weight_prefetch).
+bool weight_prefetch();
+
+// Integer launch-tuning override from the environment (0 when unset); read
+// once per name. Used to compare launch shapes, never to skip work.
+int tuning_value(const char *name);
+
 // Raise the dynamic shared memory limit of `func` on the current device to
 // `bytes` unless an earlier call already did (so that launches recorded in a
 // stream capture make no attribute calls after the first, uncaptured one).
@@ -39,8 +49,13 @@ cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64
                                  cudaStream_t stream);
 cudaError_t launch_dequantize_rows(int type, const uint8_t *blocks, float *dst, int64_t n_blocks,
                                    cudaStream_t stream);
-cudaError_t launch_gemv(int type, const uint8_t *W, const float *x, float *y, int64_t M,
-                        int64_t K, cudaStream_t stream);
+// n matrices (n <= BQ_GEMV_MAX_MATS) sharing one input x; matrix i has M[i] rows.
+// rec_ws: optional workspace of gemv_workspace_bytes(K) for x's quantized
+// records (then a prep kernel quantizes x once and prefetches the weights
+// into L2); null: every GEMV CTA quantizes x itself.
+cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *y, const int64_t *M,
+                        const float *x, int64_t K, uint32_t *rec_ws, cudaStream_t stream);
+size_t gemv_workspace_bytes(int64_t K);
 cudaError_t launch_gemm(int type, const uint8_t *W, const uint8_t *Xq, float *Y, int64_t M,
                         int64_t N, int64_t K, cudaStream_t stream);
 cudaError_t launch_block_dots(int type, const uint8_t *W, const uint8_t *xq, int32_t *out,

@@ -25,6 +25,8 @@
 //     tree. At most 16 sequential terms per lane plus 5 tree levels.
 //   - Rows with K % 256 != 0 (row bytes not a multiple of 16) take a plain
 //     warp-per-row kernel with 2-byte loads.
+#include <algorithm>
+
 #include "bq_device.cuh"
 #include "bq_internal.h"
 
@@ -32,47 +34,80 @@ namespace bq {
 namespace {
 
 constexpr int kConsumerWarps = 8;
+constexpr int kMaxMats = BQ_GEMV_MAX_MATS;
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kXRecWords = 84;          // per group of 8 blocks: 64 code words, 8 scales, 8 sums, 4 pad
 constexpr int kXRecBytes = kXRecWords * 4;
 constexpr uint32_t kDrainLimit = 1u << 26;
+constexpr int kMaxStageBytes = 64 * 1024;
 
 struct GemvArgs {
-  const uint8_t *W;
+  const uint8_t *W[kMaxMats];  // matrix i: rows [row_start[i], row_start[i+1]) of the batch
+  float *y[kMaxMats];
+  int row_start[kMaxMats + 1];
+  int n_mats;
   const float *x;
-  float *y;
-  int M;
+  int M;               // total rows of the batch
   int K;
   int groups;          // K / 256
   int lanes_per_row;   // power of two <= 32
-  int rows_per_task;   // 32 / lanes_per_row
+  int rows_per_warp;   // 32 / lanes_per_row: rows one warp covers per pass
   int row_bytes;
-  int n_tasks;         // ceil(M / rows_per_task)
+  int stage_rows;      // at most this many rows per stage (one bulk copy)
   int stages;
-  int stage_bytes;     // rows_per_task * row_bytes
+  int stage_bytes;     // stage_rows * row_bytes
   int xrec_bytes;      // groups * kXRecBytes rounded up to 128
+  const uint32_t *rec;  // x's records written by k_gemv_prep, or null: quantize x here
   unsigned *err;
   uint32_t spin_limit;
 };
 
+// The CTA's rows are cut into stages of at most stage_rows rows that never
+// straddle two matrices; producer and consumers walk the same sequence.
+struct StageCursor {
+  int row;  // global row of the batch where the next stage starts
+  __device__ __forceinline__ void next(const GemvArgs &a, int r1, int &mat, int &nrows) const {
+    mat = 0;
+    while (row >= a.row_start[mat + 1]) ++mat;
+    nrows = min(min(a.stage_rows, r1 - row), a.row_start[mat + 1] - row);
+  }
+};
+
 // Quantize x (K fp32, 16-byte aligned) into the per-group records:
 // word [g*84 + 8*jb + i] = codes 4i..4i+3 of block 8g+jb, [g*84 + 64 + jb] =
-// fp32 scale, [g*84 + 72 + jb] = code sum. Called by `nthreads` threads.
+// fp32 scale, [g*84 + 72 + jb] = code sum. 8 lanes per block; `nthreads`
+// threads (a multiple of 32) cover nthreads/8 blocks per pass. Up to
+// kXPassBatch passes are loaded at once (one memory round trip for a whole
+// activation of up to 12288 values at 256 threads) and then quantized with
+// their shuffle and division chains interleaved; every thread runs the same
+// iterations, keeping the 8-lane shuffles converged.
+constexpr int kXPassBatch = 12;
 __device__ __forceinline__ void quantize_x_records(const float *__restrict__ x, int nb,
                                                    uint32_t *rec, int tid, int nthreads) {
   const int j = tid & 7;
-  for (int b0 = tid >> 3; b0 - (tid >> 3) < nb; b0 += nthreads >> 3) {
-    const int b = b0;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (b < nb) v = __ldg(reinterpret_cast<const float4 *>(x + b * kQK + j * 4));
-    const BlockCodes<kTypeQ8_0> c = quantize_block8<kTypeQ8_0>(v);
-    if (b < nb) {
-      uint32_t *r = rec + (b >> 3) * kXRecWords;
-      const int jb = b & 7;
-      r[8 * jb + j] = c.bytes4;
-      if (j == 0) {
-        r[64 + jb] = __float_as_uint(half_bits_to_float(c.scale));
-        r[72 + jb] = uint32_t(c.sum);
+  const int stride = nthreads >> 3;  // blocks per pass
+  const int passes = (nb + stride - 1) / stride;
+  for (int p0 = 0; p0 < passes; p0 += kXPassBatch) {
+    float4 v[kXPassBatch];
+#pragma unroll
+    for (int u = 0; u < kXPassBatch; ++u) {
+      const int b = (tid >> 3) + (p0 + u) * stride;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b < nb) v[u] = __ldcg(reinterpret_cast<const float4 *>(x + b * kQK + j * 4));
+    }
+#pragma unroll
+    for (int u = 0; u < kXPassBatch; ++u) {
+      if (p0 + u >= passes) break;  // uniform: every thread has the same trip count
+      const int b = (tid >> 3) + (p0 + u) * stride;
+      const BlockCodes<kTypeQ8_0> c = quantize_block8<kTypeQ8_0>(v[u]);
+      if (b < nb) {
+        uint32_t *r = rec + (b >> 3) * kXRecWords;
+        const int jb = b & 7;
+        r[8 * jb + j] = c.bytes4;
+        if (j == 0) {
+          r[64 + jb] = __float_as_uint(half_bits_to_float(c.scale));
+          r[72 + jb] = uint32_t(c.sum);
+        }
       }
     }
   }
@@ -148,37 +183,42 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int t0 = int(int64_t(a.n_tasks) * blockIdx.x / gridDim.x);
-  const int t1 = int(int64_t(a.n_tasks) * (blockIdx.x + 1) / gridDim.x);
-  const int ntask = t1 - t0;
+  // contiguous, balanced row range of this CTA, streamed in stages
+  const int r0 = int(int64_t(a.M) * blockIdx.x / gridDim.x);
+  const int r1 = int(int64_t(a.M) * (blockIdx.x + 1) / gridDim.x);
   const int S = a.stages;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);  // every consumer warp releases every stage
     }
     fence_mbar_init();
   }
   __syncthreads();
+  // The next kernel on the stream may start as soon as every CTA got here
+  // (only when it was launched with programmatic dependent launch).
+  pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < ntask; ++i) {
-        const int s = i % S;
-        if (i >= S && !mbar_wait_bounded(&empty[s], uint32_t((i / S - 1) & 1), a.spin_limit)) {
+      StageCursor cur{r0};
+      for (int j = 0; cur.row < r1; ++j) {
+        const int s = j % S;
+        if (j >= S && !mbar_wait_bounded(&empty[s], uint32_t((j / S - 1) & 1), a.spin_limit)) {
           atomicOr(a.err, kErrTimeout);
           break;
         }
-        const int row0 = (t0 + i) * a.rows_per_task;
-        const int nrows = min(a.rows_per_task, a.M - row0);
+        int mat, nrows;
+        cur.next(a, r1, mat, nrows);
         const uint32_t bytes = uint32_t(nrows) * uint32_t(a.row_bytes);
         mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(stage_base + size_t(s) * a.stage_bytes, a.W + int64_t(row0) * a.row_bytes, bytes,
-                 &full[s]);
-        issued = i + 1;
+        bulk_g2s(stage_base + size_t(s) * a.stage_bytes,
+                 a.W[mat] + int64_t(cur.row - a.row_start[mat]) * a.row_bytes, bytes, &full[s]);
+        cur.row += nrows;
+        issued = j + 1;
       }
       // Never leave with a copy in flight: wait for the last use of each slot.
       for (int s = 0; s < min(S, issued); ++s) {
@@ -189,44 +229,118 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
     }
   } else {
     // --------------------------------------------------------- consumers --
-    quantize_x_records(a.x, a.K / kQK, xrec, threadIdx.x, kConsumerWarps * 32);
+    // W is already streaming; x and y may belong to the previous kernel on
+    // the stream, so wait for it to complete before touching them.
+    pdl_wait();
+    if (a.rec) {
+      // records of x, ready in L2 (read past L1: they were written after this CTA started)
+      const int n16 = a.groups * (kXRecBytes / 16);
+      for (int i = threadIdx.x; i < n16; i += kConsumerWarps * 32)
+        reinterpret_cast<uint4 *>(xrec)[i] = __ldcg(reinterpret_cast<const uint4 *>(a.rec) + i);
+    } else {
+      quantize_x_records(a.x, a.K / kQK, xrec, threadIdx.x, kConsumerWarps * 32);
+    }
     named_bar_sync(1, kConsumerWarps * 32);
 
     const int L = a.lanes_per_row;
-    const int rr = lane / L;  // row of the task handled by this lane
+    const int rr = lane / L;  // row (within the warp's pass) handled by this lane
     const int gl = lane % L;  // first group of that row handled by this lane
-    for (int i = warp; i < ntask; i += kConsumerWarps) {
-      const int s = i % S;
-      if (!mbar_wait_bounded(&full[s], uint32_t((i / S) & 1), a.spin_limit)) {
+    StageCursor cur{r0};
+    for (int j = 0; cur.row < r1; ++j) {
+      const int s = j % S;
+      // every warp consumes every stage in order, so a parity wait is never
+      // more than one phase ahead of the barrier
+      if (!mbar_wait_bounded(&full[s], uint32_t((j / S) & 1), a.spin_limit)) {
         atomicOr(a.err, kErrTimeout);
         break;
       }
-      const int row0 = (t0 + i) * a.rows_per_task;
-      const int nrows = min(a.rows_per_task, a.M - row0);
-      float acc = 0.0f;
-      if (rr < nrows) {
-        const uint8_t *row = stage_base + size_t(s) * a.stage_bytes + size_t(rr) * a.row_bytes;
-        for (int g = gl; g < a.groups; g += L) {
-          uint32_t w[GW];
-          const uint4 *src = reinterpret_cast<const uint4 *>(row + size_t(g) * GW * 4);
+      int mat, nrows;
+      cur.next(a, r1, mat, nrows);
+      float *yp = a.y[mat] + (cur.row - a.row_start[mat]);
+      const uint8_t *stage = stage_base + size_t(s) * a.stage_bytes;
+      for (int pr = warp * a.rows_per_warp; pr < nrows; pr += kConsumerWarps * a.rows_per_warp) {
+        const int row = pr + rr;
+        float acc = 0.0f;
+        if (row < nrows) {
+          const uint8_t *rowp = stage + size_t(row) * a.row_bytes;
+          for (int g = gl; g < a.groups; g += L) {
+            uint32_t w[GW];
+            const uint4 *src = reinterpret_cast<const uint4 *>(rowp + size_t(g) * GW * 4);
 #pragma unroll
-          for (int k = 0; k < GW / 4; ++k) {
-            const uint4 u = src[k];
-            w[4 * k] = u.x;
-            w[4 * k + 1] = u.y;
-            w[4 * k + 2] = u.z;
-            w[4 * k + 3] = u.w;
+            for (int k = 0; k < GW / 4; ++k) {
+              const uint4 u = src[k];
+              w[4 * k] = u.x;
+              w[4 * k + 1] = u.y;
+              w[4 * k + 2] = u.z;
+              w[4 * k + 3] = u.w;
+            }
+            acc = group_terms<TYPE>(w, xrec + g * kXRecWords, acc);
           }
-          acc = group_terms<TYPE>(w, xrec + g * kXRecWords, acc);
         }
+        for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+        if (gl == 0 && row < nrows) yp[row] = acc;
       }
-      for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-      if (gl == 0 && rr < nrows) a.y[row0 + rr] = acc;
+      cur.row += nrows;
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
   __syncthreads();
+}
+
+// ------------------------------------------------------------ prep kernel --
+
+// Runs before k_gemv_tma in the same stream:
+//   1. asks L2 to fetch every weight byte of the launch (no dependency on
+//      earlier kernels, so with programmatic dependent launch this overlaps
+//      the previous kernel and keeps HBM busy through the launch boundary);
+//   2. after the previous kernel completed, quantizes x once into records in
+//      global memory (16 blocks per CTA, 8 lanes per block), which every GEMV
+//      CTA then copies instead of quantizing x itself.
+constexpr int kPrepThreads = 128;
+constexpr int kPrepBlocksPerCta = kPrepThreads / 8;
+constexpr uint32_t kPrepChunk = 64 * 1024;
+
+struct PrepArgs {
+  const uint8_t *W[kMaxMats];
+  int64_t bytes[kMaxMats];     // weight bytes of matrix i
+  int64_t chunk_start[kMaxMats + 1];  // first L2-prefetch chunk of matrix i
+  int n_mats;
+  const float *x;
+  int nb;                      // K / 32
+  uint32_t *rec;               // groups * kXRecWords words
+  int quant_ctas;
+};
+
+__global__ void __launch_bounds__(kPrepThreads) k_gemv_prep(const PrepArgs p) {
+  if (threadIdx.x == 0) {
+    for (int64_t c = blockIdx.x; c < p.chunk_start[p.n_mats]; c += gridDim.x) {
+      int m = 0;
+      while (c >= p.chunk_start[m + 1]) ++m;
+      const int64_t off = (c - p.chunk_start[m]) * int64_t(kPrepChunk);
+      const uint32_t n = uint32_t(min(int64_t(kPrepChunk), p.bytes[m] - off));
+      prefetch_l2(p.W[m] + off, n);
+    }
+  }
+  pdl_launch_dependents();
+  // x may be written by the previous kernel, which may also still read the
+  // records of its own x: touch neither before it has completed
+  pdl_wait();
+  if (int(blockIdx.x) >= p.quant_ctas) return;  // whole CTA: the shuffles below stay converged
+  const int j = threadIdx.x & 7;
+  const int b = blockIdx.x * kPrepBlocksPerCta + (threadIdx.x >> 3);
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (b < p.nb) v = __ldcg(reinterpret_cast<const float4 *>(p.x + b * kQK + j * 4));
+  const BlockCodes<kTypeQ8_0> c = quantize_block8<kTypeQ8_0>(v);
+  if (b < p.nb) {
+    uint32_t *r = p.rec + (b >> 3) * kXRecWords;
+    const int jb = b & 7;
+    r[8 * jb + j] = c.bytes4;
+    if (j == 0) {
+      r[64 + jb] = __float_as_uint(half_bits_to_float(c.scale));
+      r[72 + jb] = uint32_t(c.sum);
+    }
+  }
 }
 
 // ------------------------------------------------------ generic fallback --
@@ -244,7 +358,7 @@ __global__ void __launch_bounds__(256)
     const int j = threadIdx.x & 7;
     for (int b0 = threadIdx.x >> 3; b0 - int(threadIdx.x >> 3) < nb; b0 += 32) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b0 < nb) v = __ldg(reinterpret_cast<const float4 *>(x + b0 * kQK + j * 4));
+      if (b0 < nb) v = __ldcg(reinterpret_cast<const float4 *>(x + b0 * kQK + j * 4));
       const BlockCodes<kTypeQ8_0> c = quantize_block8<kTypeQ8_0>(v);
       if (b0 < nb) {
         xs[8 * b0 + j] = c.bytes4;
@@ -288,73 +402,140 @@ int next_pow2(int v) {
 }
 
 template <int TYPE>
-cudaError_t launch_typed(const uint8_t *W, const float *x, float *y, int64_t M, int64_t K,
-                         cudaStream_t stream) {
+cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const int64_t *M, const float *x,
+                         int64_t K, uint32_t *rec_ws, cudaStream_t stream) {
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
   constexpr int BB = Fmt<TYPE>::kBytes;
   const int nb = int(K / kQK);
   const int row_bytes = nb * BB;
+  int64_t M_total = 0;
+  for (int i = 0; i < n; ++i) M_total += M[i];
+  if (M_total == 0) return cudaSuccess;
 
   if (K % 256 == 0) {
     GemvArgs a{};
-    a.W = W;
+    int acc_rows = 0;
+    a.n_mats = 0;
+    for (int i = 0; i < n; ++i) {  // empty matrices are dropped from the batch
+      if (M[i] == 0) continue;
+      a.W[a.n_mats] = W[i];
+      a.y[a.n_mats] = y[i];
+      a.row_start[a.n_mats++] = acc_rows;
+      acc_rows += int(M[i]);
+    }
+    for (int i = a.n_mats; i <= kMaxMats; ++i) a.row_start[i] = acc_rows;
     a.x = x;
-    a.y = y;
-    a.M = int(M);
+    a.M = acc_rows;
     a.K = int(K);
     a.groups = nb / 8;
     a.lanes_per_row = min(32, next_pow2(a.groups));
-    a.rows_per_task = 32 / a.lanes_per_row;
+    a.rows_per_warp = 32 / a.lanes_per_row;
     a.row_bytes = row_bytes;
-    a.n_tasks = int((M + a.rows_per_task - 1) / a.rows_per_task);
-    a.stage_bytes = a.rows_per_task * row_bytes;
     a.xrec_bytes = (a.groups * kXRecBytes + 127) / 128 * 128;
     a.err = di->err_word;
     a.spin_limit = spin_limit();
-    // The ring holds a multiple of kConsumerWarps stages: consumer warp w
-    // takes tasks w, w+8, ..., so the previous user of its slot is itself and
-    // a parity wait can never be two phases ahead of the barrier.
-    // Two CTAs per SM when the ring gets >= 16 stages, else one CTA.
+    a.rec = rec_ws;
+    // Stages are large (one bulk copy of tens of KB): the copy engine's cost
+    // is per copy, and small copies cap the stream far below HBM bandwidth.
+    // A stage holds one pass of all consumer warps (8 x rows_per_warp rows),
+    // cut to kMaxStageBytes for long rows.
     const int reserve = 1024;  // per-CTA system reservation
-    const int per_cta2 = min(di->smem_per_sm / 2 - reserve, di->max_smem_optin);
-    const int per_cta1 = min(di->smem_per_sm - reserve, di->max_smem_optin);
+    const int half_sm = min(di->smem_per_sm / 2 - reserve, di->max_smem_optin);
+    const int whole_sm = min(di->smem_per_sm - reserve, di->max_smem_optin);
+    const int forced_rows = tuning_value("BQ_GEMV_STAGE_ROWS");
+    int stage_rows = forced_rows > 0 ? forced_rows : kConsumerWarps * a.rows_per_warp;
+    stage_rows = min(stage_rows, max(1, kMaxStageBytes / row_bytes));
+    stage_rows = int(std::min<int64_t>(stage_rows, a.M));
+    a.stage_rows = stage_rows;
+    a.stage_bytes = stage_rows * row_bytes;
+    const int max_stages = tuning_value("BQ_GEMV_STAGES") > 0 ? tuning_value("BQ_GEMV_STAGES") : 4;
     auto ring = [&](int budget) {
-      const int s = (budget - a.xrec_bytes - 16 * 32) / a.stage_bytes;
-      return min(s, 32) / kConsumerWarps * kConsumerWarps;
+      return min(max_stages, (budget - a.xrec_bytes - 16 * max_stages) / a.stage_bytes);
     };
+    // Two CTAs per SM (16 consumer warps) when each fits in half an SM: the
+    // consumers' shared-memory reads and dp4a work need that many warps to
+    // keep up with the stream; rows too long for that take one CTA per SM.
     int ctas_per_sm = 2;
-    int stages = ring(per_cta2);
-    if (stages < 2 * kConsumerWarps) {
+    int stages = ring(half_sm);
+    if (stages < 2) {
       ctas_per_sm = 1;
-      stages = ring(per_cta1);
+      stages = ring(whole_sm);
     }
-    if (stages >= kConsumerWarps) {
+    if (const int forced = tuning_value("BQ_GEMV_CTAS_PER_SM")) ctas_per_sm = forced;
+    if (stages >= 2) {
       a.stages = stages;
+      const bool pdl = weight_prefetch();
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      if (rec_ws) {
+        PrepArgs p{};
+        p.n_mats = a.n_mats;
+        p.chunk_start[0] = 0;
+        for (int i = 0; i < a.n_mats; ++i) {
+          p.W[i] = a.W[i];
+          p.bytes[i] = int64_t(a.row_start[i + 1] - a.row_start[i]) * row_bytes;
+          p.chunk_start[i + 1] = p.chunk_start[i] + (p.bytes[i] + kPrepChunk - 1) / kPrepChunk;
+        }
+        for (int i = a.n_mats; i < kMaxMats; ++i) p.chunk_start[i + 1] = p.chunk_start[i];
+        p.x = x;
+        p.nb = nb;
+        p.rec = rec_ws;
+        p.quant_ctas = (nb + kPrepBlocksPerCta - 1) / kPrepBlocksPerCta;
+        const int64_t pgrid = std::max<int64_t>(p.quant_ctas, std::min<int64_t>(di->sm_count, p.chunk_start[a.n_mats]));
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3(unsigned(pgrid));
+        pc.blockDim = dim3(kPrepThreads);
+        pc.dynamicSmemBytes = 0;
+        pc.stream = stream;
+        pc.attrs = attr;
+        pc.numAttrs = pdl ? 1 : 0;
+        cudaError_t e = cudaLaunchKernelEx(&pc, k_gemv_prep, p);
+        if (e != cudaSuccess) return e;
+      }
       const size_t smem = size_t(a.xrec_bytes) + size_t(stages) * a.stage_bytes + 2 * 8 * size_t(stages);
       cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_tma<TYPE>), int(smem));
       if (e != cudaSuccess) return e;
-      const int64_t grid = min(int64_t(a.n_tasks), int64_t(di->sm_count) * ctas_per_sm);
-      k_gemv_tma<TYPE><<<unsigned(grid), kGemvThreads, smem, stream>>>(a);
-      return cudaGetLastError();
+      // at least half a stage of rows per CTA, at most ctas_per_sm CTAs per SM
+      const int64_t half_stage = std::max(1, stage_rows / 2);
+      const int64_t grid = std::min((int64_t(a.M) + half_stage - 1) / half_stage,
+                                    int64_t(di->sm_count) * ctas_per_sm);
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(unsigned(grid));
+      cfg.blockDim = dim3(kGemvThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cfg.attrs = attr;
+      cfg.numAttrs = pdl ? 1 : 0;
+      return cudaLaunchKernelEx(&cfg, k_gemv_tma<TYPE>, a);
     }
   }
+  // any K % 32 == 0 (or rows too long for two stages): one plain launch per matrix
   const size_t smem = size_t(nb) * 40;  // 32 code bytes + scale + sum per block
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_generic<TYPE>), int(smem));
   if (e != cudaSuccess) return e;
-  const int64_t grid = min((M + 7) / 8, int64_t(di->sm_count) * 4);
-  k_gemv_generic<TYPE><<<unsigned(grid), 256, smem, stream>>>(W, x, y, int(M), int(K));
-  return cudaGetLastError();
+  for (int i = 0; i < n; ++i) {
+    if (M[i] == 0) continue;
+    const int64_t grid = std::min((M[i] + 7) / 8, int64_t(di->sm_count) * 4);
+    k_gemv_generic<TYPE><<<unsigned(grid), 256, smem, stream>>>(W[i], x, y[i], int(M[i]), int(K));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(int type, const uint8_t *W, const float *x, float *y, int64_t M, int64_t K,
-                        cudaStream_t stream) {
-  if (M == 0) return cudaSuccess;
-  if (type == kTypeQ4_0) return launch_typed<kTypeQ4_0>(W, x, y, M, K, stream);
-  return launch_typed<kTypeQ8_0>(W, x, y, M, K, stream);
+cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *y, const int64_t *M,
+                        const float *x, int64_t K, uint32_t *rec_ws, cudaStream_t stream) {
+  if (type == kTypeQ4_0) return launch_typed<kTypeQ4_0>(n, W, y, M, x, K, rec_ws, stream);
+  return launch_typed<kTypeQ8_0>(n, W, y, M, x, K, rec_ws, stream);
+}
+
+size_t gemv_workspace_bytes(int64_t K) {
+  if (K <= 0 || K % 256) return 0;
+  return (size_t(K / 256) * kXRecBytes + 255) / 256 * 256;
 }
 
 // ------------------------------------------------------------ block dots --

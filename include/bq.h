@@ -85,8 +85,21 @@ int bq_dequantize_rows(int type, const void *blocks, float *dst, int64_t n_rows,
  * y: M fp32. y[m] = sum_b scale_w[m][b] * scale_x[b] * sumi[m][b] where sumi is
  *   the exact int32 dot of the block codes; accumulated in fp32 (partial sums
  *   per lane, then a tree), relative error well under 1e-5 of sum_b |term|.
- * Limits: K <= BQ_GEMV_MAX_K. Needs no workspace. */
+ * Limits: K <= BQ_GEMV_MAX_K. A workspace is optional (bq_gemv_workspace_size). */
 int bq_gemv(int type, const void *W_blocks, const float *x, float *y, int64_t M, int64_t K);
+
+/* Largest number of matrices one bq_gemv_multi call takes. */
+#define BQ_GEMV_MAX_MATS 8
+
+/* Decode GEMV over n matrices that read the same input x (e.g. the q, k and
+ * v projections, or gate and up): y_i = W_i . x for i < n, in one launch, with
+ * x quantized once. Same per-element result as n calls of bq_gemv.
+ * W_blocks, y and M are HOST arrays of n entries; W_blocks[i] (16-byte
+ * aligned) and y[i] are device pointers, M[i] >= 0 rows; all share type and K.
+ * n in 1..BQ_GEMV_MAX_MATS and sum(M) < 2^31, else BQ_ERR_SHAPE. No y[i] may
+ * overlap x, a weight matrix or another y[j]. */
+int bq_gemv_multi(int type, int n, const void *const *W_blocks, float *const *y, const int64_t *M,
+                  const float *x, int64_t K);
 
 /* Prefill GEMM: Y = X . W^T for N tokens; prefill reuses each weight across
  * many tokens and is compute-bound ("05. llama.cpp…", §性能直觉).
@@ -141,10 +154,28 @@ int bq_gemm_noalloc(int type, const void *W_blocks, const float *X, float *Y, in
 int bq_set_stream(void *cuda_stream);
 void *bq_get_stream(void);
 
+/* Weight prefetch across kernel boundaries for the calling thread's bq_gemv
+ * calls (default off). When enabled, a GEMV is launched with programmatic
+ * dependent launch: it may start, and stream W_blocks into shared memory,
+ * while the previous kernel on the stream is still running; it reads x and
+ * writes y only after that kernel has completed. Enable it only when no
+ * kernel that may still be running on the stream writes W_blocks (model
+ * weights loaded ahead of time); x and y carry no such restriction. */
+int bq_set_weight_prefetch(int enable);
+
 /* Caller-owned device workspace for the calling thread (NULL, 0 clears it). */
 int bq_set_workspace(void *dev_ptr, size_t bytes);
 /* Bytes of workspace an entry point needs for these sizes (0 if none). */
 size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K);
+
+/* Workspace bytes that let bq_gemv / bq_gemv_multi quantize x once per call
+ * (0 when K % 256 != 0, where x is always quantized inside the GEMV kernel).
+ * With a workspace of at least this size set by bq_set_workspace, a call
+ * launches a small prep kernel, which first asks L2 to fetch the call's
+ * weights and then writes x's Q8_0 codes, scales and code sums to the
+ * workspace, and then the GEMV kernel, which copies them. Without one, every
+ * GEMV CTA quantizes x itself. Both give bit-identical results. */
+size_t bq_gemv_workspace_size(int type, int64_t K);
 
 /* Thread-local message of the last failure (never NULL). */
 const char *bq_last_error(void);

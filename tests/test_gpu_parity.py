@@ -293,3 +293,107 @@ def test_kv_bias_with_q8_0_rejected(bq, dev):
     with pytest.raises(binding.BQError) as e:
         bq.kv_quantize(Q8, torch.zeros(2, 2, 64, device=dev), torch.zeros(2, 64, device=dev))
     assert e.value.status == -3
+
+
+# ------------------------------------------- weight prefetch across kernels --
+
+def test_gemv_prefetch_chain_respects_war_and_raw(bq, orc, dev):
+    """With weight prefetch on, a GEMV starts streaming W before the previous
+    GEMV has finished. Chain: g1 reads A and writes B; g2 reads C and writes A
+    (g2 must not overwrite A before g1 read it); g3 reads B (g1's output) and
+    writes D (it must see g1's finished y). g1 and g2 are checked against the
+    oracle on the generator's inputs; g3 against the same chain without
+    prefetch."""
+    from block_quantized_weight_row_gb300 import binding, inputs
+    K = 4096
+    Ws = [inputs.weight(K, K, seed=1300 + i) for i in range(3)]
+    wq = [orc.quantize_rows(Q4, W.numpy()) for W in Ws]
+    wq_d = [torch.from_numpy(w).to(dev) for w in wq]
+    A0 = inputs.activation(K, seed=1310)
+    C0 = inputs.activation(K, seed=1311)
+
+    def chain(prefetch):
+        A, C = A0.to(dev), C0.to(dev)
+        B, D = torch.empty(K, device=dev), torch.empty(K, device=dev)
+        torch.cuda.synchronize()
+        binding.set_weight_prefetch(prefetch)
+        try:
+            for _ in range(3):  # repeat so the three launches overlap in steady state
+                A.copy_(A0.to(dev, non_blocking=True))
+                bq.gemv(Q4, wq_d[0], A, K, K, out=B)
+                bq.gemv(Q4, wq_d[1], C, K, K, out=A)
+                bq.gemv(Q4, wq_d[2], B, K, K, out=D)
+        finally:
+            binding.set_weight_prefetch(False)
+        torch.cuda.synchronize()
+        return _np(B), _np(A), _np(D)
+
+    B1, A1, D1 = chain(True)
+    y_ref, mag = orc.gemv(Q4, wq[0], A0.numpy(), K, K, with_mag=True)
+    _check_float(B1, y_ref, mag, "g1 (reads A before g2 overwrites it)")
+    y_ref, mag = orc.gemv(Q4, wq[1], C0.numpy(), K, K, with_mag=True)
+    _check_float(A1, y_ref, mag, "g2")
+    _B0, _A0, D0 = chain(False)
+    assert np.array_equal(D1, D0), "g3 differs when it may start before g1 finished"
+
+
+# ------------------------------------------------------ batched GEMV ---------
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+@pytest.mark.parametrize("Ms,K", [([4096, 1024, 1024], 4096), ([11008, 11008], 4096), ([5, 0, 17, 1, 3, 64, 2, 9], 4096),
+                                  ([33, 7], 96), ([1], 256), ([300, 200, 100], 2304)])
+def test_gemv_multi_matches_oracle(bq, orc, dev, t, Ms, K):
+    from block_quantized_weight_row_gb300 import inputs
+    x = inputs.activation(K, seed=K + 77)
+    wq = [orc.quantize_rows(t, inputs.weight(m, K, seed=1000 + 17 * i + m).numpy()) if m else
+          np.zeros((0, K // 32 * (18 if t == Q4 else 34)), np.uint8) for i, m in enumerate(Ms)]
+    w_dev = [torch.from_numpy(w).to(dev) if w.size else torch.empty(16, dtype=torch.uint8, device=dev) for w in wq]
+    outs = bq.gemv_multi(t, w_dev, x.to(dev), Ms, K)
+    for i, (m, w) in enumerate(zip(Ms, wq)):
+        if m == 0:
+            continue
+        y_ref, mag = orc.gemv(t, w, x.numpy(), m, K, with_mag=True)
+        _check_float(_np(outs[i]), y_ref, mag, f"matrix {i} of the batch")
+
+
+def test_gemv_multi_rejects_bad_batches(bq, dev):
+    from block_quantized_weight_row_gb300 import binding
+    w = torch.zeros(64 * 18, dtype=torch.uint8, device=dev)
+    x = torch.zeros(64, device=dev)
+    with pytest.raises(binding.BQError) as e:
+        bq.gemv_multi(Q4, [w] * 9, x, [1] * 9, 64)
+    assert e.value.status == -2
+    y = torch.zeros(8, device=dev)
+    with pytest.raises(binding.BQError) as e:  # two outputs on the same buffer
+        bq.gemv_multi(Q4, [w, w], x, [4, 4], 64, outs=[y, y])
+    assert e.value.status == -1
+
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+@pytest.mark.parametrize("with_ws", [True, False])
+@pytest.mark.parametrize("Ms,K", [([4096, 1024], 4096), ([3, 700], 11008), ([257], 2304)])
+def test_gemv_both_activation_paths(bq, orc, dev, t, with_ws, Ms, K):
+    """x quantized once by the prep kernel into the workspace, or by every
+    GEMV CTA: both must match the oracle (and hence each other)."""
+    import ctypes
+    from block_quantized_weight_row_gb300 import binding, inputs
+    L = binding.lib()
+    x = inputs.activation(K, seed=K + 5)
+    wq = [orc.quantize_rows(t, inputs.weight(m, K, seed=2000 + 3 * i + m).numpy()) for i, m in enumerate(Ms)]
+    w_dev = [torch.from_numpy(w).to(dev) for w in wq]
+    outs = [torch.full((m,), float("nan"), device=dev) for m in Ms]
+    xd = x.to(dev)
+    ws = torch.empty(max(1, int(L.bq_gemv_workspace_size(t, K))), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    assert L.bq_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+    if with_ws:
+        assert L.bq_set_workspace(ctypes.c_void_p(ws.data_ptr()), ws.numel()) == 0
+    else:
+        assert L.bq_set_workspace(None, 0) == 0
+    n, W, Y, M = binding.gemv_multi_args(w_dev, outs, Ms)
+    assert L.bq_gemv_multi(t, n, W, Y, M, ctypes.c_void_p(xd.data_ptr()), K) == 0, L.bq_last_error()
+    torch.cuda.synchronize()
+    L.bq_set_workspace(None, 0)
+    for i, (m, w) in enumerate(zip(Ms, wq)):
+        y_ref, mag = orc.gemv(t, w, x.numpy(), m, K, with_mag=True)
+        _check_float(_np(outs[i]), y_ref, mag, f"matrix {i}, workspace={with_ws}")
