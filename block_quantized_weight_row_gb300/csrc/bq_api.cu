@@ -285,8 +285,7 @@ int bq_gemv_multi(int type, int n, const void *const *W, float *const *y, const 
     // also prefetches the weights into L2; otherwise every CTA quantizes x
     const size_t need = gemv_workspace_bytes(K);
     uint32_t *rec = (need && t_ws && t_ws_bytes >= need) ? static_cast<uint32_t *>(t_ws) : nullptr;
-    if (rec && (overlap(rec, need, x, size_t(K) * 4)))
-      return fail(BQ_ERR_INVALID_ARG, "bq_gemv: workspace overlaps x");
+    if (rec && overlap(rec, need, x, size_t(K) * 4)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: workspace overlaps x");
     for (int i = 0; rec && i < n; ++i)
       if (M[i] > 0 && overlap(rec, need, y[i], size_t(M[i]) * 4))
         return fail(BQ_ERR_INVALID_ARG, "bq_gemv: workspace overlaps y");

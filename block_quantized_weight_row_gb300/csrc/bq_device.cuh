@@ -34,21 +34,6 @@ template <> struct Fmt<kTypeQ8_0> {
 
 // ---------------------------------------------------------------- quantize --
 
-// max over the 8 lanes (aligned groups of 8) that hold one 32-value block
-__device__ __forceinline__ float group8_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 2));
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
-  return v;
-}
-
-__device__ __forceinline__ int group8_sum(int v) {
-  v += __shfl_xor_sync(kFull, v, 1);
-  v += __shfl_xor_sync(kFull, v, 2);
-  v += __shfl_xor_sync(kFull, v, 4);
-  return v;
-}
-
 // scale of a block: d = amax / qmax (IEEE fp32 division), stored as binary16
 // rounded to nearest even; `ds` is the stored scale read back as fp32.
 template <int TYPE>
@@ -59,69 +44,123 @@ __device__ __forceinline__ void block_scale(float amax, uint16_t &bits, float &d
   ds = __half2float(h);
 }
 
-// code of one value: round-half-even of the IEEE fp32 quotient x / ds, clamped.
-//
-// The quotient is formed as r = x * rn(1/ds) (one correctly rounded
-// reciprocal per block, one multiply per value). r is within 2 ulp of the
-// correctly rounded quotient q = rn(x / ds), so rint(r) == rint(q) unless a
-// half-integer lies within that distance of r; values whose distance to the
-// nearest integer is that close to 0.5 (a band of 4e-5 * max(|r|, 1), far
-// wider than 2 ulp) take the exact IEEE division instead. The result is
-// bit-identical to rint(rn(x / ds)) for every input; only the cost differs.
-template <int TYPE>
-__device__ __forceinline__ int code_of(float x, float ds, float inv) {
-  float r = __fmul_rn(x, inv);
-  float n = rintf(r);
-  if (fabsf(__fsub_rn(r, n)) > 0.5f - 4e-5f * fmaxf(fabsf(r), 1.0f)) n = rintf(__fdiv_rn(x, ds));
-  const int q = __float2int_rz(n);  // n is integral
-  return min(max(q, Fmt<TYPE>::kQmin), Fmt<TYPE>::kQmax);
-}
-
-__device__ __forceinline__ float amax4(float4 v) {
-  return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-}
-
-// One block held by 8 lanes (lane j of the group holds elements 4j..4j+3).
-// Produces, for lane j, the 4 code bytes of elements 4j..4j+3 packed
-// little-endian as int8 (Q8_0) or as unsigned nibbles q + 8 (Q4_0, one nibble
-// per byte), the scale bits, and the code sum of the whole block.
-template <int TYPE>
-struct BlockCodes {
-  uint32_t bytes4;   // 4 codes, one per byte
-  uint16_t scale;    // binary16 bits of the stored scale
-  int sum;           // sum of the 32 signed codes (over the 8-lane group)
-};
-
-template <int TYPE>
-__device__ __forceinline__ BlockCodes<TYPE> quantize_block8(float4 v) {
-  BlockCodes<TYPE> r;
-  float ds;
-  block_scale<TYPE>(group8_max(amax4(v)), r.scale, ds);
-  int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-  if (ds != 0.0f) {  // a zero scale (all-zero or underflowing block) gives all codes 0
-    const float inv = __frcp_rn(ds);
-    q0 = code_of<TYPE>(v.x, ds, inv);
-    q1 = code_of<TYPE>(v.y, ds, inv);
-    q2 = code_of<TYPE>(v.z, ds, inv);
-    q3 = code_of<TYPE>(v.w, ds, inv);
-  }
-  if (TYPE == kTypeQ4_0) {
-    r.bytes4 = uint32_t(q0 + 8) | (uint32_t(q1 + 8) << 8) | (uint32_t(q2 + 8) << 16) |
-               (uint32_t(q3 + 8) << 24);
-  } else {
-    r.bytes4 = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) |
-               ((uint32_t(q2) & 0xffu) << 16) | ((uint32_t(q3) & 0xffu) << 24);
-  }
-  r.sum = group8_sum(q0 + q1 + q2 + q3);
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
-// Q4_0 packing across the 8-lane group: byte i of qs holds element i in its
-// low nibble and element i+16 in its high nibble. Lane j < 4 returns qs bytes
-// 4j..4j+3 (lanes 4..7 hold the high-nibble halves and return garbage).
-__device__ __forceinline__ uint32_t pack_q4_nibbles(uint32_t nib4) {
-  const uint32_t hi = __shfl_down_sync(kFull, nib4, 4);
-  return nib4 | (hi << 4);
+// Code of one value: round-half-even of the IEEE fp32 quotient x / ds,
+// clamped to the type's range. ds > 0 with inv ~ 1/ds, or ds = 0 with
+// inv = 0, which gives code 0 (the exact path is never taken then).
+//
+// r = x * inv with inv within 1 ulp of 1/ds is within 3 ulp of the correctly
+// rounded quotient q = rn(x / ds); |r| < 256 for every block (|x| <= amax and
+// ds ~ amax / qmax), so 3 ulp < 1e-4. Adding 1.5 * 2^23 rounds r to an integer
+// (ties to even, the add is correctly rounded) and leaves that integer in the
+// low bits of the sum. When r is farther than 0.4999 from its integer (a tie
+// may lie between r and q), the value takes the exact division instead; in all
+// other cases rint(r) == rint(q). The result is bit-identical to
+// clamp(rint(rn(x / ds))) for every input; only the cost differs.
+template <int TYPE>
+__device__ __forceinline__ int code_of(float x, float ds, float inv) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const float r = __fmul_rn(x, inv);
+  const float t = __fadd_rn(r, kMagic);
+  int q = __float_as_int(t) - 0x4B400000;
+  if (fabsf(__fsub_rn(r, __fsub_rn(t, kMagic))) > 0.4999f) q = __float2int_rn(__fdiv_rn(x, ds));
+  return min(max(q, Fmt<TYPE>::kQmin), Fmt<TYPE>::kQmax);
+}
+
+__device__ __forceinline__ uint32_t pack_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  // byte 0 of each argument, in order (two's complement low byte for codes)
+  return __byte_perm(__byte_perm(b0, b1, 0x3340), __byte_perm(b2, b3, 0x3340), 0x5410);
+}
+
+// One lane quantizes one whole 32-value block v[0..31]: the scale bits, the
+// block's code bytes as words (Q4_0: 4 words, byte i = (q[i]+8) | (q[i+16]+8)
+// << 4; Q8_0: 8 words of int8 codes) and, when asked, the sum of the codes.
+template <int TYPE, bool SUM>
+__device__ __forceinline__ void quantize_block_lane(const float (&v)[32], uint16_t &scale, uint32_t *words,
+                                                    int &sum) {
+  // max of |v| as a 5-level tree (exact in any order)
+  float m[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 16]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+  const float amax = m[0];
+  float ds;
+  block_scale<TYPE>(amax, scale, ds);
+  // a zero scale (all-zero block, or a scale that underflows binary16) gives
+  // inv = 0 and so every code 0, without a branch
+  const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
+  int q[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) q[j] = code_of<TYPE>(v[j], ds, inv);
+  if (SUM) {  // integer tree sum (exact)
+    int t[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = q[j] + q[j + 16];
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w; ++j) t[j] += t[j + w];
+    sum = t[0];
+  }
+  if (TYPE == kTypeQ4_0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) b[k] = uint32_t(q[4 * i + k] + 8) | (uint32_t(q[16 + 4 * i + k] + 8) << 4);
+      words[i] = pack_bytes(b[0], b[1], b[2], b[3]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      words[i] = pack_bytes(uint32_t(q[4 * i]), uint32_t(q[4 * i + 1]), uint32_t(q[4 * i + 2]), uint32_t(q[4 * i + 3]));
+  }
+}
+
+// One Q8_0 block held by 8 lanes (lane j of an aligned group of 8 holds
+// elements 4j..4j+3): the scale bits, the lane's 4 codes as one word of int8
+// and the block's code sum, every lane of the group getting scale and sum.
+// Straight-line code apart from the rare exact-division path of code_of.
+__device__ __forceinline__ void quantize_block_8lanes(float4 v, uint16_t &scale, uint32_t &word, int &sum) {
+  float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+  float ds;
+  block_scale<kTypeQ8_0>(m, scale, ds);
+  // a zero scale (all-zero block, or a scale that underflows binary16) gives
+  // inv = 0 and so every code 0, without a branch
+  const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
+  const int q0 = code_of<kTypeQ8_0>(v.x, ds, inv), q1 = code_of<kTypeQ8_0>(v.y, ds, inv);
+  const int q2 = code_of<kTypeQ8_0>(v.z, ds, inv), q3 = code_of<kTypeQ8_0>(v.w, ds, inv);
+  word = pack_bytes(uint32_t(q0), uint32_t(q1), uint32_t(q2), uint32_t(q3));
+  int s = q0 + q1 + q2 + q3;
+  s += __shfl_xor_sync(kFull, s, 1);
+  s += __shfl_xor_sync(kFull, s, 2);
+  s += __shfl_xor_sync(kFull, s, 4);
+  sum = s;
+}
+
+// Load one 32-value fp32 block (16-byte aligned) as 8 vectors.
+template <bool STREAM>
+__device__ __forceinline__ void load_block(const float *p, float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 f = STREAM ? __ldcs(reinterpret_cast<const float4 *>(p) + c)
+                            : __ldcg(reinterpret_cast<const float4 *>(p) + c);
+    v[4 * c] = f.x;
+    v[4 * c + 1] = f.y;
+    v[4 * c + 2] = f.z;
+    v[4 * c + 3] = f.w;
+  }
 }
 
 // ------------------------------------------------------------- block dots --
@@ -240,6 +279,24 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // returned (src and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// L2 policy for data read once (streamed weights): evicted before other lines,
+// so the stream does not push activations or prefetched lines out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// bulk_g2s with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {

@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kMaxMats = BQ_GEMV_MAX_MATS;
+
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kXRecWords = 84;          // per group of 8 blocks: 64 code words, 8 scales, 8 sums, 4 pad
 constexpr int kXRecBytes = kXRecWords * 4;
@@ -73,40 +74,50 @@ struct StageCursor {
   }
 };
 
-// Quantize x (K fp32, 16-byte aligned) into the per-group records:
-// word [g*84 + 8*jb + i] = codes 4i..4i+3 of block 8g+jb, [g*84 + 64 + jb] =
-// fp32 scale, [g*84 + 72 + jb] = code sum. 8 lanes per block; `nthreads`
-// threads (a multiple of 32) cover nthreads/8 blocks per pass. Up to
-// kXPassBatch passes are loaded at once (one memory round trip for a whole
-// activation of up to 12288 values at 256 threads) and then quantized with
-// their shuffle and division chains interleaved; every thread runs the same
-// iterations, keeping the 8-lane shuffles converged.
-constexpr int kXPassBatch = 12;
-__device__ __forceinline__ void quantize_x_records(const float *__restrict__ x, int nb,
-                                                   uint32_t *rec, int tid, int nthreads) {
+// Quantize x (K fp32, 16-byte aligned) into the per-group records: words
+// [g*84 + 8*jb + i] = codes 4i..4i+3 of block b = 8g+jb, [g*84 + 64 + jb] =
+// the scale as fp32, [g*84 + 72 + jb] = the code sum. 8 lanes per block
+// (coalesced loads, short dependency chains); `nthreads` (a multiple of 32)
+// threads cover nthreads/8 blocks per pass. The loads of up to 12 passes are
+// issued before any arithmetic and passes are quantized 4 at a time in
+// straight-line code. Every thread runs every pass (the guards are uniform),
+// keeping the 8-lane shuffles converged. Passes start at block `rot` so that
+// CTAs reading the same x spread their requests over L2.
+__device__ __forceinline__ void quantize_x_records(const float *__restrict__ x, int nb, uint32_t *rec, int tid,
+                                                   int nthreads, int rot) {
+  constexpr int kBatch = 12;
   const int j = tid & 7;
-  const int stride = nthreads >> 3;  // blocks per pass
+  const int stride = nthreads >> 3;
   const int passes = (nb + stride - 1) / stride;
-  for (int p0 = 0; p0 < passes; p0 += kXPassBatch) {
-    float4 v[kXPassBatch];
+  const int span = passes * stride;
+  for (int p0 = 0; p0 < passes; p0 += kBatch) {
+    float4 v[kBatch];
+    int b[kBatch];
 #pragma unroll
-    for (int u = 0; u < kXPassBatch; ++u) {
-      const int b = (tid >> 3) + (p0 + u) * stride;
+    for (int u = 0; u < kBatch; ++u) {
+      b[u] = (p0 + u < passes) ? ((p0 + u) * stride + (tid >> 3) + rot) % span : nb;
       v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b < nb) v[u] = __ldcg(reinterpret_cast<const float4 *>(x + b * kQK + j * 4));
+      if (b[u] < nb) v[u] = __ldcg(reinterpret_cast<const float4 *>(x + b[u] * kQK + j * 4));  // past L1
     }
 #pragma unroll
-    for (int u = 0; u < kXPassBatch; ++u) {
-      if (p0 + u >= passes) break;  // uniform: every thread has the same trip count
-      const int b = (tid >> 3) + (p0 + u) * stride;
-      const BlockCodes<kTypeQ8_0> c = quantize_block8<kTypeQ8_0>(v[u]);
-      if (b < nb) {
-        uint32_t *r = rec + (b >> 3) * kXRecWords;
-        const int jb = b & 7;
-        r[8 * jb + j] = c.bytes4;
-        if (j == 0) {
-          r[64 + jb] = __float_as_uint(half_bits_to_float(c.scale));
-          r[72 + jb] = uint32_t(c.sum);
+    for (int u0 = 0; u0 < kBatch; u0 += 4) {
+      if (p0 + u0 < passes) {  // uniform across the CTA
+        uint16_t sc[4];
+        uint32_t wd[4];
+        int sm[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) quantize_block_8lanes(v[u0 + k], sc[k], wd[k], sm[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (b[u0 + k] < nb) {
+            uint32_t *r = rec + (b[u0 + k] >> 3) * kXRecWords;
+            const int jb = b[u0 + k] & 7;
+            r[8 * jb + j] = wd[k];
+            if (j == 0) {
+              r[64 + jb] = __float_as_uint(half_bits_to_float(sc[k]));
+              r[72 + jb] = uint32_t(sm[k]);
+            }
+          }
         }
       }
     }
@@ -204,6 +215,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       int issued = 0;
+      const uint64_t stream_policy = l2_evict_first_policy();  // W is read once
       StageCursor cur{r0};
       for (int j = 0; cur.row < r1; ++j) {
         const int s = j % S;
@@ -215,8 +227,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
         cur.next(a, r1, mat, nrows);
         const uint32_t bytes = uint32_t(nrows) * uint32_t(a.row_bytes);
         mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(stage_base + size_t(s) * a.stage_bytes,
-                 a.W[mat] + int64_t(cur.row - a.row_start[mat]) * a.row_bytes, bytes, &full[s]);
+        bulk_g2s_hint(stage_base + size_t(s) * a.stage_bytes,
+                      a.W[mat] + int64_t(cur.row - a.row_start[mat]) * a.row_bytes, bytes, &full[s],
+                      stream_policy);
         cur.row += nrows;
         issued = j + 1;
       }
@@ -233,12 +246,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
     // the stream, so wait for it to complete before touching them.
     pdl_wait();
     if (a.rec) {
-      // records of x, ready in L2 (read past L1: they were written after this CTA started)
+      // x's records, ready in L2 (read past L1: written after this CTA
+      // started); every CTA starts at a different offset to spread the
+      // requests over L2
       const int n16 = a.groups * (kXRecBytes / 16);
-      for (int i = threadIdx.x; i < n16; i += kConsumerWarps * 32)
-        reinterpret_cast<uint4 *>(xrec)[i] = __ldcg(reinterpret_cast<const uint4 *>(a.rec) + i);
+      const int rot = int((blockIdx.x * 97u) % unsigned(n16));
+      for (int i = threadIdx.x; i < n16; i += kConsumerWarps * 32) {
+        const int k = i + rot < n16 ? i + rot : i + rot - n16;
+        reinterpret_cast<uint4 *>(xrec)[k] = __ldcg(reinterpret_cast<const uint4 *>(a.rec) + k);
+      }
     } else {
-      quantize_x_records(a.x, a.K / kQK, xrec, threadIdx.x, kConsumerWarps * 32);
+      quantize_x_records(a.x, a.K / kQK, xrec, threadIdx.x, kConsumerWarps * 32, int(blockIdx.x) * 8);
     }
     named_bar_sync(1, kConsumerWarps * 32);
 
@@ -290,7 +308,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
 
 // ------------------------------------------------------------ prep kernel --
 
-// Runs before k_gemv_tma in the same stream:
+// Runs before k_gemv_tma in the same stream when a workspace is available:
 //   1. asks L2 to fetch every weight byte of the launch (no dependency on
 //      earlier kernels, so with programmatic dependent launch this overlaps
 //      the previous kernel and keeps HBM busy through the launch boundary);
@@ -303,12 +321,12 @@ constexpr uint32_t kPrepChunk = 64 * 1024;
 
 struct PrepArgs {
   const uint8_t *W[kMaxMats];
-  int64_t bytes[kMaxMats];     // weight bytes of matrix i
+  int64_t bytes[kMaxMats];            // weight bytes of matrix i
   int64_t chunk_start[kMaxMats + 1];  // first L2-prefetch chunk of matrix i
   int n_mats;
   const float *x;
-  int nb;                      // K / 32
-  uint32_t *rec;               // groups * kXRecWords words
+  int nb;         // K / 32
+  uint32_t *rec;  // groups * kXRecWords words
   int quant_ctas;
 };
 
@@ -318,8 +336,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_gemv_prep(const PrepArgs p) {
       int m = 0;
       while (c >= p.chunk_start[m + 1]) ++m;
       const int64_t off = (c - p.chunk_start[m]) * int64_t(kPrepChunk);
-      const uint32_t n = uint32_t(min(int64_t(kPrepChunk), p.bytes[m] - off));
-      prefetch_l2(p.W[m] + off, n);
+      prefetch_l2(p.W[m] + off, uint32_t(min(int64_t(kPrepChunk), p.bytes[m] - off)));
     }
   }
   pdl_launch_dependents();
@@ -327,20 +344,9 @@ __global__ void __launch_bounds__(kPrepThreads) k_gemv_prep(const PrepArgs p) {
   // records of its own x: touch neither before it has completed
   pdl_wait();
   if (int(blockIdx.x) >= p.quant_ctas) return;  // whole CTA: the shuffles below stay converged
-  const int j = threadIdx.x & 7;
-  const int b = blockIdx.x * kPrepBlocksPerCta + (threadIdx.x >> 3);
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (b < p.nb) v = __ldcg(reinterpret_cast<const float4 *>(p.x + b * kQK + j * 4));
-  const BlockCodes<kTypeQ8_0> c = quantize_block8<kTypeQ8_0>(v);
-  if (b < p.nb) {
-    uint32_t *r = p.rec + (b >> 3) * kXRecWords;
-    const int jb = b & 7;
-    r[8 * jb + j] = c.bytes4;
-    if (j == 0) {
-      r[64 + jb] = __float_as_uint(half_bits_to_float(c.scale));
-      r[72 + jb] = uint32_t(c.sum);
-    }
-  }
+  quantize_x_records(p.x + int64_t(blockIdx.x) * kPrepBlocksPerCta * kQK,
+                     min(kPrepBlocksPerCta, p.nb - int(blockIdx.x) * kPrepBlocksPerCta),
+                     p.rec + blockIdx.x * (kPrepBlocksPerCta / 8) * kXRecWords, threadIdx.x, kPrepThreads, 0);
 }
 
 // ------------------------------------------------------ generic fallback --
@@ -354,20 +360,17 @@ __global__ void __launch_bounds__(256)
   constexpr int BB = Fmt<TYPE>::kBytes;
   extern __shared__ __align__(16) uint32_t xs[];
   const int nb = K / kQK;
-  {
-    const int j = threadIdx.x & 7;
-    for (int b0 = threadIdx.x >> 3; b0 - int(threadIdx.x >> 3) < nb; b0 += 32) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b0 < nb) v = __ldcg(reinterpret_cast<const float4 *>(x + b0 * kQK + j * 4));
-      const BlockCodes<kTypeQ8_0> c = quantize_block8<kTypeQ8_0>(v);
-      if (b0 < nb) {
-        xs[8 * b0 + j] = c.bytes4;
-        if (j == 0) {
-          xs[8 * nb + b0] = __float_as_uint(half_bits_to_float(c.scale));
-          xs[9 * nb + b0] = uint32_t(c.sum);
-        }
-      }
-    }
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    float v[32];
+    load_block<false>(x + b * kQK, v);
+    uint16_t scale;
+    uint32_t w[8];
+    int sum;
+    quantize_block_lane<kTypeQ8_0, true>(v, scale, w, sum);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xs[8 * b + i] = w[i];
+    xs[8 * nb + b] = __float_as_uint(half_bits_to_float(scale));
+    xs[9 * nb + b] = uint32_t(sum);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -466,6 +469,13 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
     if (const int forced = tuning_value("BQ_GEMV_CTAS_PER_SM")) ctas_per_sm = forced;
     if (stages >= 2) {
       a.stages = stages;
+      const size_t smem = size_t(a.xrec_bytes) + size_t(stages) * a.stage_bytes + 2 * 8 * size_t(stages);
+      cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_tma<TYPE>), int(smem));
+      if (e != cudaSuccess) return e;
+      // at least half a stage of rows per CTA, at most ctas_per_sm CTAs per SM
+      const int64_t half_stage = std::max(1, stage_rows / 2);
+      const int64_t grid = std::min((int64_t(a.M) + half_stage - 1) / half_stage,
+                                    int64_t(di->sm_count) * ctas_per_sm);
       const bool pdl = weight_prefetch();
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -484,24 +494,17 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
         p.nb = nb;
         p.rec = rec_ws;
         p.quant_ctas = (nb + kPrepBlocksPerCta - 1) / kPrepBlocksPerCta;
-        const int64_t pgrid = std::max<int64_t>(p.quant_ctas, std::min<int64_t>(di->sm_count, p.chunk_start[a.n_mats]));
+        const int64_t pgrid =
+            std::max<int64_t>(p.quant_ctas, std::min<int64_t>(di->sm_count, p.chunk_start[a.n_mats]));
         cudaLaunchConfig_t pc = {};
         pc.gridDim = dim3(unsigned(pgrid));
         pc.blockDim = dim3(kPrepThreads);
-        pc.dynamicSmemBytes = 0;
         pc.stream = stream;
         pc.attrs = attr;
         pc.numAttrs = pdl ? 1 : 0;
-        cudaError_t e = cudaLaunchKernelEx(&pc, k_gemv_prep, p);
+        e = cudaLaunchKernelEx(&pc, k_gemv_prep, p);
         if (e != cudaSuccess) return e;
       }
-      const size_t smem = size_t(a.xrec_bytes) + size_t(stages) * a.stage_bytes + 2 * 8 * size_t(stages);
-      cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_tma<TYPE>), int(smem));
-      if (e != cudaSuccess) return e;
-      // at least half a stage of rows per CTA, at most ctas_per_sm CTAs per SM
-      const int64_t half_stage = std::max(1, stage_rows / 2);
-      const int64_t grid = std::min((int64_t(a.M) + half_stage - 1) / half_stage,
-                                    int64_t(di->sm_count) * ctas_per_sm);
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(unsigned(grid));
       cfg.blockDim = dim3(kGemvThreads);

@@ -7,13 +7,20 @@
 // to the cache quantized, optionally after subtracting a calibrated
 // per-(kv-head, channel) bias (lpnh.cn KV-cache article, §解法).
 //
-// Design (HBM-bound: 128 B of fp32 read per 18 or 34 B written):
-//   - a CTA owns tiles of 256 consecutive blocks (32 KB of fp32 input);
-//   - 8 lanes per block, one float4 each, so every warp load instruction
-//     reads 512 contiguous bytes; each thread keeps 8 loads in flight;
-//   - the block's amax is a 3-step shuffle max inside the 8-lane group;
-//   - codes are packed to the block layout in shared memory, and the tile's
-//     4.5 KB (Q4_0) / 8.5 KB (Q8_0) of output leaves as 16-byte stores.
+// Design (HBM-bound: 128 B of fp32 read per 18 or 34 B written; the
+// quantization arithmetic must stay well under the SMs' issue rate at that
+// byte rate, so one lane owns one whole block: no shuffles, one division per
+// block, full-rate rounding):
+//   - warp tile = 32 consecutive blocks (4 KB): read with fully coalesced
+//     128-bit loads (512 contiguous bytes per instruction), then moved through
+//     a warp-private shared-memory tile so that lane i holds block i. The tile
+//     is XOR-swizzled (16-byte chunk c of block b sits at chunk c ^ (b & 7)),
+//     which keeps both the coalesced writes and the per-block reads free of
+//     bank conflicts;
+//   - a mean-centering bias (one block per (kv-head, 32 channels), a few KB)
+//     is staged once per CTA in the same swizzled layout;
+//   - the tile's output (576 B Q4_0 / 1088 B Q8_0) is assembled in shared
+//     memory and leaves as 16-byte stores.
 #include "bq_device.cuh"
 #include "bq_internal.h"
 
@@ -21,74 +28,93 @@ namespace bq {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kTileBlocks = 256;  // blocks per CTA tile; 8 warps x 8 rounds x 4 blocks
+constexpr int kQuantWarps = kQuantThreads / 32;
+constexpr int kMaxSmemBiasBlocks = 128;  // 16 KB of bias staged per CTA
+
+// byte offset of 16-byte chunk c of block b in a swizzled tile
+__device__ __forceinline__ int swz(int b, int c) { return b * 128 + ((c ^ (b & 7)) << 4); }
 
 template <int TYPE, bool BIAS>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kQuantThreads, 3)
     k_quantize_rows(const float *__restrict__ src, uint8_t *__restrict__ dst, int64_t n_blocks,
                     const float *__restrict__ bias, int64_t bias_period) {
   constexpr int BB = Fmt<TYPE>::kBytes;
-  __shared__ __align__(16) uint8_t tile_out[kTileBlocks * BB];
-
+  constexpr int NW = TYPE == kTypeQ4_0 ? 4 : 8;  // code words per block
+  __shared__ __align__(16) uint8_t in_tile[kQuantWarps][32 * 128];
+  __shared__ __align__(16) uint8_t out_tile[kQuantWarps][32 * BB];
+  __shared__ __align__(16) uint8_t bias_tile[BIAS ? kMaxSmemBiasBlocks * 128 : 16];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int sub = lane >> 3;  // block of the 4-block round handled by this 8-lane group
-  const int j = lane & 7;     // float4 of the block held by this lane
-
-  for (int64_t tile0 = int64_t(blockIdx.x) * kTileBlocks; tile0 < n_blocks;
-       tile0 += int64_t(gridDim.x) * kTileBlocks) {
-    const int tile_n = int(min(int64_t(kTileBlocks), n_blocks - tile0));
-
-    float4 v[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int tb = warp * 32 + r * 4 + sub;
-      v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (tb < tile_n) v[r] = ld_stream_f4(src + (tile0 + tb) * kQK + j * 4);
-    }
-    if (BIAS) {
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int tb = warp * 32 + r * 4 + sub;
-        if (tb < tile_n) {
-          // block g of row (token, head) uses bias block g mod (heads * blocks per row)
-          const int64_t bblk = (tile0 + tb) % bias_period;
-          const float4 b = __ldg(reinterpret_cast<const float4 *>(bias + bblk * kQK + j * 4));
-          v[r].x = __fsub_rn(v[r].x, b.x);
-          v[r].y = __fsub_rn(v[r].y, b.y);
-          v[r].z = __fsub_rn(v[r].z, b.z);
-          v[r].w = __fsub_rn(v[r].w, b.w);
-        }
-      }
-    }
-
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int tb = warp * 32 + r * 4 + sub;
-      const BlockCodes<TYPE> c = quantize_block8<TYPE>(v[r]);
-      uint8_t *blk = tile_out + tb * BB;
-      uint32_t word = c.bytes4;
-      if (TYPE == kTypeQ4_0) word = pack_q4_nibbles(c.bytes4);
-      if (tb < tile_n) {
-        if (j == 0) *reinterpret_cast<uint16_t *>(blk) = c.scale;
-        if (TYPE == kTypeQ8_0 || j < 4) {
-          // qs bytes 4j..4j+3 live at block offset 2 + 4j: 2-byte aligned
-          uint16_t *q = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);
-          q[0] = uint16_t(word & 0xffffu);
-          q[1] = uint16_t(word >> 16);
-        }
-      }
-    }
+  uint8_t *it = in_tile[warp];
+  uint8_t *ot = out_tile[warp];
+  const bool bias_in_smem = BIAS && bias_period <= kMaxSmemBiasBlocks;
+  if (bias_in_smem) {
+    for (int i = threadIdx.x; i < int(bias_period) * 8; i += kQuantThreads)
+      *reinterpret_cast<float4 *>(bias_tile + swz(i >> 3, i & 7)) = __ldg(reinterpret_cast<const float4 *>(bias) + i);
     __syncthreads();
-
-    uint8_t *out = dst + tile0 * BB;  // 16-byte aligned: tile0 is a multiple of 256
-    const int nbytes = tile_n * BB;
+  }
+  const int64_t total_warps = int64_t(gridDim.x) * kQuantWarps;
+  for (int64_t tile = int64_t(blockIdx.x) * kQuantWarps + warp; tile * 32 < n_blocks; tile += total_warps) {
+    const int nblk = int(min(int64_t(32), n_blocks - tile * 32));
+    const float4 *gsrc = reinterpret_cast<const float4 *>(src + tile * 32 * kQK);
+    // coalesced: vector i = lane + 32c is chunk (i & 7) of block (i >> 3)
+    float4 ld[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int i = lane + 32 * c;
+      ld[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if ((i >> 3) < nblk) ld[c] = __ldcs(gsrc + i);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int i = lane + 32 * c;
+      *reinterpret_cast<float4 *>(it + swz(i >> 3, i & 7)) = ld[c];
+    }
+    __syncwarp();
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 f = *reinterpret_cast<const float4 *>(it + swz(lane, c));
+      v[4 * c] = f.x;
+      v[4 * c + 1] = f.y;
+      v[4 * c + 2] = f.z;
+      v[4 * c + 3] = f.w;
+    }
+    const int64_t b = tile * 32 + lane;
+    if (BIAS && b < n_blocks) {
+      // block b of row (token, head) uses bias block b mod (heads * blocks per row)
+      const int64_t bb = b % bias_period;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 f = bias_in_smem ? *reinterpret_cast<const float4 *>(bias_tile + swz(int(bb), c))
+                                      : __ldg(reinterpret_cast<const float4 *>(bias + bb * kQK) + c);
+        v[4 * c] = __fsub_rn(v[4 * c], f.x);
+        v[4 * c + 1] = __fsub_rn(v[4 * c + 1], f.y);
+        v[4 * c + 2] = __fsub_rn(v[4 * c + 2], f.z);
+        v[4 * c + 3] = __fsub_rn(v[4 * c + 3], f.w);
+      }
+    }
+    uint16_t scale;
+    uint32_t w[NW];
+    int unused;
+    quantize_block_lane<TYPE, false>(v, scale, w, unused);
+    // block `lane` of the tile at byte lane*BB (2-byte aligned)
+    uint16_t *o = reinterpret_cast<uint16_t *>(ot + lane * BB);
+    o[0] = scale;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      o[1 + 2 * i] = uint16_t(w[i] & 0xffffu);
+      o[2 + 2 * i] = uint16_t(w[i] >> 16);
+    }
+    __syncwarp();
+    const int nbytes = nblk * BB;
+    uint8_t *out = dst + tile * 32 * BB;  // 16-byte aligned: 32 * BB is a multiple of 16
     const int n16 = nbytes / 16;
-    for (int i = threadIdx.x; i < n16; i += kQuantThreads)
-      reinterpret_cast<uint4 *>(out)[i] = reinterpret_cast<const uint4 *>(tile_out)[i];
-    for (int i = n16 * 8 + threadIdx.x; i < nbytes / 2; i += kQuantThreads)
-      reinterpret_cast<uint16_t *>(out)[i] = reinterpret_cast<const uint16_t *>(tile_out)[i];
-    __syncthreads();
+    for (int i = lane; i < n16; i += 32)
+      reinterpret_cast<uint4 *>(out)[i] = reinterpret_cast<const uint4 *>(ot)[i];
+    for (int i = n16 * 8 + lane; i < nbytes / 2; i += 32)
+      reinterpret_cast<uint16_t *>(out)[i] = reinterpret_cast<const uint16_t *>(ot)[i];
+    __syncwarp();
   }
 }
 
@@ -125,13 +151,14 @@ __global__ void __launch_bounds__(256)
 }
 
 template <int TYPE, bool BIAS>
-cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias,
-                     int64_t bias_period, cudaStream_t stream) {
+cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
+                     cudaStream_t stream) {
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
-  const int64_t tiles = (n_blocks + kTileBlocks - 1) / kTileBlocks;
-  const int64_t grid = min(tiles, int64_t(di->sm_count) * 8);
+  const int64_t tiles = (n_blocks + 31) / 32;
+  const int64_t ctas = (tiles + kQuantWarps - 1) / kQuantWarps;
+  const int64_t grid = min(ctas, int64_t(di->sm_count) * 8);
   k_quantize_rows<TYPE, BIAS><<<unsigned(grid), kQuantThreads, 0, stream>>>(src, dst, n_blocks, bias,
                                                                            bias_period);
   return cudaGetLastError();

@@ -174,7 +174,8 @@ size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K);
  * launches a small prep kernel, which first asks L2 to fetch the call's
  * weights and then writes x's Q8_0 codes, scales and code sums to the
  * workspace, and then the GEMV kernel, which copies them. Without one, every
- * GEMV CTA quantizes x itself. Both give bit-identical results. */
+ * GEMV CTA quantizes x itself. Both give bit-identical results. The
+ * workspace must not be in use by another call that may run concurrently. */
 size_t bq_gemv_workspace_size(int type, int64_t K);
 
 /* Thread-local message of the last failure (never NULL). */
