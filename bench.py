@@ -508,7 +508,7 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
     tops = tot_ops / (tot_ms * 1e-3) / 1e12 * world
     out["prefill_gemm"] = {"metric": "prefill GEMM int8-equivalent TOPS (2*N*M*K per GEMM, X quantize included)",
                            "value": round(tops, 1), "unit": "TOPS", "shapes": rows,
-                           "kernel": "k_gemm_q8_mma (mma.sync m16n8k32 s8)",
+                           "kernel": "k_gemm_q8_tc (tcgen05.mma kind::f16, exact integer codes) + k_quantize_x_tc",
                            "l2": "flushed between iterations"}
 
     # KV-cache write: 28 layers x (K -> Q4_0 with bias, V -> Q8_0)

@@ -2,6 +2,7 @@
 // validation, per-thread stream / workspace / error state, per-device info,
 // and the device error word that bounded in-kernel waits report through.
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -184,10 +185,11 @@ int bq_set_workspace(void *dev_ptr, size_t bytes) {
 }
 
 size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K) {
-  (void)M;
-  if (type != BQ_TYPE_Q8_0 || N <= 0 || K <= 0 || K % kQK) return 0;
-  const size_t bytes = size_t(N) * size_t(K / kQK) * Fmt<kTypeQ8_0>::kBytes;
-  return (bytes + 255) / 256 * 256;
+  if (type != BQ_TYPE_Q8_0 || M <= 0 || N <= 0 || K <= 0 || K % kQK) return 0;
+  if (!sizes_ok(N, K) || M > 0x7fffffffll || N > 0x7fffffffll) return 0;
+  size_t bytes = 0;
+  prefill_path(M, N, K, SIZE_MAX, &bytes);
+  return bytes;
 }
 
 size_t bq_gemv_workspace_size(int type, int64_t K) {
@@ -316,16 +318,14 @@ int bq_gemm(int type, const void *W, const float *X, float *Y, int64_t M, int64_
     cudaError_t e = cudaMemsetAsync(Y, 0, ybytes, t_stream);
     return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemm memset");
   }
-  const size_t need = bq_workspace_size(type, M, N, K);
+  size_t need = 0;
+  const PrefillPath path = prefill_path(M, N, K, SIZE_MAX, &need);
   if (!t_ws || t_ws_bytes < need)
     return fail(BQ_ERR_WORKSPACE, "bq_gemm: needs %zu workspace bytes, %zu set", need, t_ws_bytes);
   if (overlap(t_ws, need, Y, ybytes) || overlap(t_ws, need, X, size_t(N) * size_t(K) * 4) ||
       overlap(t_ws, need, W, size_t(M) * size_t(K / kQK) * bb))
     return fail(BQ_ERR_INVALID_ARG, "bq_gemm: workspace overlaps an argument");
-  uint8_t *xq = static_cast<uint8_t *>(t_ws);
-  cudaError_t e = launch_quantize_rows(BQ_TYPE_Q8_0, X, xq, N * (K / kQK), K / kQK, nullptr, 1, t_stream);
-  if (e != cudaSuccess) return cuda_fail(e, "bq_gemm: activation quantize launch");
-  e = launch_gemm(type, static_cast<const uint8_t *>(W), xq, Y, M, N, K, t_stream);
+  cudaError_t e = launch_prefill(path, static_cast<const uint8_t *>(W), X, Y, M, N, K, t_ws, t_stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemm launch");
 }
 

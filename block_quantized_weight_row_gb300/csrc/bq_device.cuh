@@ -149,6 +149,19 @@ __device__ __forceinline__ void quantize_block_8lanes(float4 v, uint16_t &scale,
   sum = s;
 }
 
+// Four int8 codes (one word, code 0 in the low byte) as two words of two
+// binary16 values each, exactly: the biased byte q + 128 is the low mantissa
+// byte of the binary16 number 1024 + (q + 128) (exponent byte 0x64), and
+// subtracting 1152 leaves q. Every step is exact for q in [-128, 127].
+__device__ __forceinline__ uint2 codes_to_f16x2(uint32_t w) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+  uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+  return make_uint2(lo, hi);
+}
+
 // Load one 32-value fp32 block (16-byte aligned) as 8 vectors.
 template <bool STREAM>
 __device__ __forceinline__ void load_block(const float *p, float (&v)[32]) {

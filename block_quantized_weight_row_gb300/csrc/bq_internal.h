@@ -58,6 +58,20 @@ cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *
 size_t gemv_workspace_bytes(int64_t K);
 cudaError_t launch_gemm(int type, const uint8_t *W, const uint8_t *Xq, float *Y, int64_t M,
                         int64_t N, int64_t K, cudaStream_t stream);
+// Prefill GEMM on the tcgen05 tensor cores (K a multiple of 256): quantizes X
+// into `ws` (gemm_tc_workspace_bytes(N, K) bytes) and runs the GEMM.
+bool gemm_tc_supported(int64_t M, int64_t N, int64_t K);
+size_t gemm_tc_workspace_bytes(int64_t N, int64_t K);
+cudaError_t launch_gemm_tc(const uint8_t *W, const float *X, float *Y, int64_t M, int64_t N, int64_t K, void *ws,
+                           cudaStream_t stream);
+// The prefill path bq_gemm and bq_gemm_noalloc take for these sizes, given
+// `ws_limit` bytes of scratch (SIZE_MAX: any): the tcgen05 kernel where it
+// applies and its workspace fits, else the mma.sync kernel over Q8_0
+// activations. *ws_bytes receives the scratch the chosen path needs.
+enum class PrefillPath { kTc, kMmaSync };
+PrefillPath prefill_path(int64_t M, int64_t N, int64_t K, size_t ws_limit, size_t *ws_bytes);
+cudaError_t launch_prefill(PrefillPath path, const uint8_t *W, const float *X, float *Y, int64_t M, int64_t N,
+                           int64_t K, void *ws, cudaStream_t stream);
 cudaError_t launch_block_dots(int type, const uint8_t *W, const uint8_t *xq, int32_t *out,
                               int64_t M, int64_t K, cudaStream_t stream);
 

@@ -236,3 +236,28 @@ cudaError_t launch_gemm(int type, const uint8_t *W, const uint8_t *Xq, float *Y,
 }
 
 }  // namespace bq
+
+namespace bq {
+
+PrefillPath prefill_path(int64_t M, int64_t N, int64_t K, size_t ws_limit, size_t *ws_bytes) {
+  if (gemm_tc_supported(M, N, K)) {
+    const size_t tc = (gemm_tc_workspace_bytes(N, K) + 255) / 256 * 256;
+    if (tc <= ws_limit) {
+      *ws_bytes = tc;
+      return PrefillPath::kTc;
+    }
+  }
+  *ws_bytes = (size_t(N) * size_t(K / kQK) * Fmt<kTypeQ8_0>::kBytes + 255) / 256 * 256;
+  return PrefillPath::kMmaSync;
+}
+
+cudaError_t launch_prefill(PrefillPath path, const uint8_t *W, const float *X, float *Y, int64_t M, int64_t N,
+                           int64_t K, void *ws, cudaStream_t stream) {
+  if (path == PrefillPath::kTc) return launch_gemm_tc(W, X, Y, M, N, K, ws, stream);
+  uint8_t *xq = static_cast<uint8_t *>(ws);
+  cudaError_t e = launch_quantize_rows(BQ_TYPE_Q8_0, X, xq, N * (K / kQK), K / kQK, nullptr, 1, stream);
+  if (e != cudaSuccess) return e;
+  return launch_gemm(BQ_TYPE_Q8_0, W, xq, Y, M, N, K, stream);
+}
+
+}  // namespace bq

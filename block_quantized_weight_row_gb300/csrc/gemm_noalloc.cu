@@ -6,7 +6,9 @@
 // The quantized activations, which bq_gemm keeps in the caller's workspace,
 // live here in a file-scope device array of fixed size instead. Every GPU
 // that loads the library holds that array until the process exits. The
-// kernels are the ones bq_gemm launches; only the scratch location differs.
+// kernels are the ones bq_gemm launches, except that the tcgen05 path, whose
+// binary16 activation codes take twice the bytes of Q8_0 blocks, is used only
+// where its activations fit the array; otherwise the mma.sync path runs.
 #include <mutex>
 
 #include "bq.h"
@@ -59,7 +61,8 @@ extern "C" int bq_gemm_noalloc(int type, const void *W, const float *X, float *Y
   if (M > 0x7fffffffll || N > 0x7fffffffll || K > 0x7fffffffll)
     return report_error(BQ_ERR_SHAPE, "bq_gemm_noalloc: M, N and K must be below 2^31");
   if (M == 0 || N == 0) return report_ok();
-  const size_t need = size_t(N) * size_t(K / kQK) * Fmt<kTypeQ8_0>::kBytes;
+  size_t need = 0;
+  const PrefillPath path = prefill_path(M, N, K, size_t(BQ_GEMM_NOALLOC_SCRATCH_BYTES), &need);
   if (need > size_t(BQ_GEMM_NOALLOC_SCRATCH_BYTES))
     return report_error(BQ_ERR_WORKSPACE, "bq_gemm_noalloc: N x K/32 x 34 = %zu bytes of quantized activations exceed the "
              "%d-byte static scratch; use bq_gemm with a workspace",
@@ -82,12 +85,7 @@ extern "C" int bq_gemm_noalloc(int type, const void *W, const float *X, float *Y
   } else {
     void *scratch = nullptr;
     e = scratch_address(&scratch);
-    if (e == cudaSuccess)
-      e = launch_quantize_rows(BQ_TYPE_Q8_0, X, static_cast<uint8_t *>(scratch), N * (K / kQK), K / kQK,
-                               nullptr, 1, stream);
-    if (e == cudaSuccess)
-      e = launch_gemm(type, static_cast<const uint8_t *>(W), static_cast<const uint8_t *>(scratch), Y, M, N, K,
-                      stream);
+    if (e == cudaSuccess) e = launch_prefill(path, static_cast<const uint8_t *>(W), X, Y, M, N, K, scratch, stream);
   }
   if (e != cudaSuccess)
     return report_error(BQ_ERR_CUDA, "bq_gemm_noalloc: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));

@@ -50,7 +50,11 @@ def test_block_bytes_and_version(L):
 
 
 def test_workspace_size(L):
-    assert L.bq_workspace_size(Q8, 4096, 512, 4096) == 512 * 128 * 34
+    # K a multiple of 256: binary16 codes of 128-token tiles plus one fp32 scale per block and token
+    assert L.bq_workspace_size(Q8, 4096, 512, 4096) == 4 * 128 * 4096 * 2 + 4 * 128 * 128 * 4
+    assert L.bq_workspace_size(Q8, 4096, 129, 256) == 2 * 128 * 256 * 2 + 2 * 8 * 128 * 4
+    # other K: Q8_0 blocks of the N rows
+    assert L.bq_workspace_size(Q8, 4096, 512, 4128) == 512 * 129 * 34
     assert L.bq_workspace_size(Q8, 1, 3, 96) == 512  # 3 x 3 x 34 = 306, rounded up to 256 bytes
     assert L.bq_workspace_size(Q4, 1, 3, 96) == 0
     assert L.bq_workspace_size(Q8, 1, 0, 96) == 0

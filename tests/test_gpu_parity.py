@@ -218,8 +218,15 @@ def test_gemv_timeout_path_returns_error(bq, orc, dev):
 
 # ---------------------------------------------------------------- GEMM ----
 
+# K a multiple of 256 runs the tcgen05 kernel (128 x 128 tiles, partial sums
+# folded every 16 blocks), other K the mma.sync kernel. The shapes cover M and
+# N tails inside and beyond one tile, a single token, block counts that end
+# on and between fold boundaries (8, 24, 40, 72, 256, 344 blocks) and K not a
+# multiple of 256.
 @pytest.mark.parametrize("M,N,K", [(64, 16, 256), (130, 70, 512), (33, 5, 96), (256, 128, 4096),
-                                   (200, 65, 2304), (1, 1, 32), (128, 64, 11008)])
+                                   (200, 65, 2304), (1, 1, 32), (128, 64, 11008), (129, 1, 256),
+                                   (300, 129, 768), (1000, 300, 1280), (384, 256, 8192), (257, 131, 4352),
+                                   (64, 16, 4128)])
 def test_gemm_shapes(bq, orc, dev, M, N, K):
     from block_quantized_weight_row_gb300 import inputs
     W = inputs.weight(M, K, seed=M * 7 + K)
@@ -249,6 +256,53 @@ def test_gemm_prefill_config_sampled(bq, orc, dev, M, K):
     assert np.array_equal(_np(wq[torch.from_numpy(ms).to(dev)]), wq_s)
     Y_ref, mag = orc.gemm(Q8, wq_s, X_s, len(ms), len(ns), K, with_mag=True)
     _check_float(Y[np.ix_(ns, ms)], Y_ref, mag, f"prefill {M}x{K}")
+
+
+def test_gemm_full_code_range(bq, orc, dev):
+    """Weight blocks the quantizer never writes but the format allows: every
+    int8 code including -128 and arbitrary binary16 scales; activations with
+    the adversarial blocks (zeros, spikes, ties, tiny and huge scales)."""
+    from block_quantized_weight_row_gb300 import inputs
+    M, N, K = 260, 136, 512
+    rng = np.random.default_rng(77)
+    nb = K // 32
+    blocks = np.empty((M, nb, 34), np.uint8)
+    scales = rng.uniform(1e-4, 1e-1, size=(M, nb)).astype(np.float16)
+    blocks[:, :, 0:2] = scales.view(np.uint8).reshape(M, nb, 2)
+    blocks[:, :, 2:] = rng.integers(0, 256, size=(M, nb, 32), dtype=np.uint8)
+    blocks[0, 0, 2:] = 0x80  # a block of -128 codes
+    wq = blocks.reshape(-1)
+    adv = inputs.adversarial_blocks().numpy()
+    X = np.resize(adv, (N * nb, 32)).reshape(N, K).astype(np.float32)
+    X[N // 2:] = inputs.activation(K, seed=5, rows=N - N // 2).numpy()
+    Y = _np(bq.gemm(Q8, torch.from_numpy(wq).to(dev), torch.from_numpy(X).to(dev), M, N, K))
+    Y_ref, mag = orc.gemm(Q8, wq, X, M, N, K, with_mag=True)
+    _check_float(Y, Y_ref, mag, "gemm full code range")
+
+
+def test_gemm_timeout_path_returns_error(bq, orc, dev):
+    """The tcgen05 GEMM with a poll budget of 0: every role gives up at its
+    first wait, the MMAs and copies already issued are waited for, the tensor
+    memory is freed, and the status reports the timeout; the next call with
+    the default budget is correct (it could not allocate tensor memory if the
+    failed one had kept it)."""
+    from block_quantized_weight_row_gb300 import binding, inputs
+    L = binding.lib()
+    M, N, K = 256, 130, 1024
+    W = inputs.weight(M, K, seed=19)
+    X = inputs.activation(K, seed=20, rows=N)
+    wq = torch.from_numpy(orc.quantize_rows(Q8, W.numpy())).to(dev)
+    assert binding.device_status() == 0
+    try:
+        assert L.bq_set_spin_limit(0) == 0
+        bq.gemm(Q8, wq, X.to(dev), M, N, K)
+        assert binding.device_status() == -6
+    finally:
+        L.bq_set_spin_limit(-1)
+    Y = _np(bq.gemm(Q8, wq, X.to(dev), M, N, K))
+    assert binding.device_status() == 0
+    Y_ref, mag = orc.gemm(Q8, _np(wq), X.numpy(), M, N, K, with_mag=True)
+    _check_float(Y, Y_ref, mag, "gemm after timeout")
 
 
 def test_gemm_errors(bq, dev):
