@@ -17,23 +17,24 @@
 // of fp32 roundoff of the sum of the terms' magnitudes.
 //
 // CTA tile: 128 weight rows (the MMA's M, tensor-memory lanes) x 128 tokens
-// (the MMA's N, tensor-memory columns); K in stages:
-//   - warp 0, one lane: 2-D TMA copies of the raw 34-byte weight blocks, 8
+// (the MMA's N, tensor-memory columns); K in stages. 12 warps, so that every
+// SM sub-partition runs one helper warp next to two epilogue warps:
+//   - warp 0, lane 0: 2-D TMA copies of the raw 34-byte weight blocks, 8
 //     blocks (272 bytes) of each of the 128 rows per stage, and 1-D bulk
-//     copies of the tile's activation scales;
-//   - warp 14, one lane: 1-D bulk copies of the activation operand, which the
-//     activation quantizer already wrote as binary16 codes in the MMA's
-//     128-byte-swizzled K-major layout (16 KB per 2 blocks x 128 tokens);
-//   - warps 2, 3, 12, 13: one thread per weight row turns the raw blocks into
-//     binary16 codes in the same swizzled layout, and the weight scales into
-//     fp32;
+//     copies of the tile's activation scales; lane 1: 1-D bulk copies of the
+//     activation operand, which the activation quantizer already wrote as
+//     binary16 codes in the MMA's 128-byte-swizzled K-major layout (16 KB per
+//     2 blocks x 128 tokens);
 //   - warp 1: allocates the 512 tensor-memory columns and, from one lane,
 //     issues two MMAs (K = 16 each) per block into one of three 128-column
 //     accumulators;
+//   - warps 2, 3: each thread turns two weight rows of raw blocks into
+//     binary16 codes in the same swizzled layout, and their scales into fp32;
 //   - warps 4..11: the epilogue; warp w reads lanes 32 (w mod 4) .. + 31 and
-//     64 of the 128 columns, multiplies by the scale products with packed
-//     fp32x2 FMAs, and every 16 blocks folds its partial sums into a running
-//     sum held in the last 128 tensor-memory columns.
+//     64 of the 128 columns in two chunks (the second loading while the first
+//     is scaled), multiplies by the scale products with packed fp32x2 FMAs,
+//     and every 16 blocks folds its partial sums into a running sum held in
+//     the last 128 tensor-memory columns.
 // Every wait is bounded; a wait that runs out sets the device error word and
 // a CTA-wide abort flag, after which every role leaves its loop, copies and
 // MMAs in flight are waited for, and the tensor memory is freed.
@@ -62,7 +63,10 @@ constexpr int kSBufs = 3;                       // per-block accumulators (128 c
 constexpr int kAccCol = kSBufs * kTN;           // running sums: columns 384..511
 constexpr int kTmemCols = 512;
 constexpr int kFold = 16;                       // blocks per partial sum
-constexpr int kTcThreads = 15 * 32;
+constexpr int kEpiWarps = 8;                    // 2 per SM sub-partition
+constexpr int kEpiCols = kTN / (kEpiWarps / 4); // 64 columns per epilogue warp
+constexpr int kConvWarps = 2;                   // 2 weight rows per thread
+constexpr int kTcThreads = 12 * 32;
 constexpr uint32_t kDrainPolls = 1u << 22;
 
 constexpr int kOffA = 0;
@@ -123,25 +127,32 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
                : "memory");
 }
 
-// 16 consecutive columns of this warp's 32 lanes: thread i gets lane
-// (lane base + i), columns taddr.col .. + 15. The wait is in the same asm
+// 32 consecutive columns of this warp's 32 lanes: thread i gets lane
+// (lane base + i), columns taddr.col .. + 31. The wait is in the same asm
 // statement so that no use of the registers can be scheduled before it.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
       "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
       "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 
@@ -184,27 +195,118 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
-// Bounded wait that also gives up once another thread of the CTA has given up.
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait that also gives up once another thread of the CTA has given
+// up. Polls do not suspend in the barrier unit (whose wake-up came hundreds
+// of cycles after the phase completed); between polls the thread sleeps
+// briefly, so that waiting warps leave the issue slots to working ones. The
+// abort flag is read every 64 polls.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, uint32_t limit, volatile int *abort_flag,
                                         unsigned *err) {
   for (uint32_t i = 0; i < limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
+    if (mbar_test_wait(bar, parity)) return true;
+    __nanosleep(i < 64 ? 20 : 200);
+    if ((i & 63) == 63 && *abort_flag) return false;
   }
   *abort_flag = 1;
   atomicOr(err, kErrTimeout);
   return false;
 }
-// The same for a whole warp, with a warp-uniform result.
+// The same for a whole warp: lane 0 polls, the result is broadcast, and the
+// warp synchronizes (which orders the other lanes' later accesses after lane
+// 0's observation of the phase).
 __device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity, uint32_t limit, volatile int *abort_flag,
                                              unsigned *err) {
-  const bool ok = tc_wait(bar, parity, limit, abort_flag, err);
-  return __all_sync(kFull, ok);
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, limit, abort_flag, err);
+  ok = __shfl_sync(kFull, ok, 0);
+  __syncwarp();
+  return ok != 0;
 }
 // Wait for copies or MMAs already issued (they complete on their own).
 __device__ __forceinline__ void drain(uint64_t *bar, uint32_t parity) {
   for (uint32_t i = 0; i < kDrainPolls; ++i)
     if (mbar_try_wait(bar, parity)) return;
+}
+
+// One converter thread: rows r and r + 64 of operand stage k (0..3) of the
+// raw chunk in `raw`, written as binary16 codes into the swizzled tile `a`.
+__device__ __forceinline__ void convert_stage(const uint8_t *raw, uint8_t *a, int r, int k) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rr = r + 64 * h;
+    const uint8_t *row = raw + rr * kRawPitch;
+    // bytes 68k .. 68k+67 of the row: 16-byte vectors 4k .. 4k+4, words k .. k+16 of them
+    uint32_t w[20];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (4 * k + i));
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    uint32_t code[16];  // first block: bytes 2..33 (shifted by 2 bytes); second: words 9..16
+#pragma unroll
+    for (int i = 0; i < 8; ++i) code[i] = __funnelshift_r(w[k + i], w[k + i + 1], 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) code[8 + i] = w[k + 9 + i];
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const uint2 lo = codes_to_f16x2(code[2 * cc]), hi = codes_to_f16x2(code[2 * cc + 1]);
+      *reinterpret_cast<uint4 *>(a + sw128_off(rr, cc)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+  }
+}
+
+// Issue a 32-column tensor-memory load without waiting for it.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Wait for this thread's tensor-memory loads; the registers of the last one
+// are operands so that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// part[2i], part[2i+1] += S[c] * (dw * dx[c]) for the 32 columns of one chunk
+__device__ __forceinline__ void scale_accumulate(uint64_t *part, const uint32_t (&s)[32], uint64_t dw2,
+                                                 const float4 *dx4) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 d = lds_f4_ordered(dx4 + q);
+    const uint64_t p01 = fmul2(dw2, pack2(__float_as_uint(d.x), __float_as_uint(d.y)));
+    const uint64_t p23 = fmul2(dw2, pack2(__float_as_uint(d.z), __float_as_uint(d.w)));
+    part[2 * q] = ffma2(pack2(s[4 * q], s[4 * q + 1]), p01, part[2 * q]);
+    part[2 * q + 1] = ffma2(pack2(s[4 * q + 2], s[4 * q + 3]), p23, part[2 * q + 1]);
+  }
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -224,21 +326,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
       mbar_init(&bar[kRawFull + i], 1);
-      mbar_init(&bar[kRawEmpty + i], 4);
+      mbar_init(&bar[kRawEmpty + i], kConvWarps);
     }
     for (int i = 0; i < kSubStages; ++i) {
       mbar_init(&bar[kBFull + i], 1);
-      mbar_init(&bar[kAReady + i], 4);
+      mbar_init(&bar[kAReady + i], kConvWarps);
       mbar_init(&bar[kSubEmpty + i], 1);
     }
     for (int i = 0; i < kScaleSlots; ++i) {
       mbar_init(&bar[kDxFull + i], 1);
-      mbar_init(&bar[kScaleFull + i], 4);
-      mbar_init(&bar[kScaleEmpty + i], 8);
+      mbar_init(&bar[kScaleFull + i], kConvWarps);
+      mbar_init(&bar[kScaleEmpty + i], kEpiWarps);
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bar[kTFull + i], 1);
-      mbar_init(&bar[kTEmpty + i], 8);
+      mbar_init(&bar[kTEmpty + i], kEpiWarps);
     }
     mbar_init(&bar[kDone], 1);
     *abort_flag = 0;
@@ -255,84 +357,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 && lane == 0) {
     // ---- producer: raw weight blocks (2-D TMA) and activation scales ----
-    if (lane == 0) {
-      int raw_armed = 0, dx_armed = 0;  // chunks whose copies were issued
-      for (int c = 0; c < nchunks; ++c) {
-        const int rs = c % kRawStages, ss = c % kScaleSlots;
-        if (!tc_wait(&bar[kRawEmpty + rs], ((c / kRawStages) & 1) ^ 1, spin, abort_flag, err)) break;
-        mbar_arrive_expect_tx(&bar[kRawFull + rs], kRawBytes);
-        tma_load_2d(sm + kOffRaw + rs * kRawBytes, &wmap, c * (kRawPitch / 2), m0, &bar[kRawFull + rs]);
-        raw_armed = c + 1;
-        if (!tc_wait(&bar[kScaleEmpty + ss], ((c / kScaleSlots) & 1) ^ 1, spin, abort_flag, err)) break;
-        mbar_arrive_expect_tx(&bar[kDxFull + ss], kChunkBlocks * 128 * 4);
-        bulk_g2s(sm + kOffScale + ss * kScaleSlotBytes, dxs + (int64_t(n_tile) * nb + c * kChunkBlocks) * 128,
-                 kChunkBlocks * 128 * 4, &bar[kDxFull + ss]);
-        dx_armed = c + 1;
-      }
-      // wait until every issued copy has landed: the last phase armed on each
-      // slot (chunk last = the largest chunk < armed that used the slot)
-      for (int i = 0; i < kRawStages && i < raw_armed; ++i) {
-        const int last = raw_armed - 1 - ((raw_armed - 1 - i) % kRawStages);
-        drain(&bar[kRawFull + i], (last / kRawStages) & 1);
-      }
-      for (int i = 0; i < kScaleSlots && i < dx_armed; ++i) {
-        const int last = dx_armed - 1 - ((dx_armed - 1 - i) % kScaleSlots);
-        drain(&bar[kDxFull + i], (last / kScaleSlots) & 1);
-      }
+    int raw_armed = 0, dx_armed = 0;  // chunks whose copies were issued
+    for (int c = 0; c < nchunks; ++c) {
+      const int rs = c % kRawStages, ss = c % kScaleSlots;
+      if (!tc_wait(&bar[kRawEmpty + rs], ((c / kRawStages) & 1) ^ 1, spin, abort_flag, err)) break;
+      mbar_arrive_expect_tx(&bar[kRawFull + rs], kRawBytes);
+      tma_load_2d(sm + kOffRaw + rs * kRawBytes, &wmap, c * (kRawPitch / 2), m0, &bar[kRawFull + rs]);
+      raw_armed = c + 1;
+      if (!tc_wait(&bar[kScaleEmpty + ss], ((c / kScaleSlots) & 1) ^ 1, spin, abort_flag, err)) break;
+      mbar_arrive_expect_tx(&bar[kDxFull + ss], kChunkBlocks * 128 * 4);
+      bulk_g2s(sm + kOffScale + ss * kScaleSlotBytes, dxs + (int64_t(n_tile) * nb + c * kChunkBlocks) * 128,
+               kChunkBlocks * 128 * 4, &bar[kDxFull + ss]);
+      dx_armed = c + 1;
     }
-  } else if (warp == 14) {
+    // wait until every issued copy has landed: the last phase armed on each
+    // slot (chunk last = the largest chunk < armed that used the slot)
+    for (int i = 0; i < kRawStages && i < raw_armed; ++i) {
+      const int last = raw_armed - 1 - ((raw_armed - 1 - i) % kRawStages);
+      drain(&bar[kRawFull + i], (last / kRawStages) & 1);
+    }
+    for (int i = 0; i < kScaleSlots && i < dx_armed; ++i) {
+      const int last = dx_armed - 1 - ((dx_armed - 1 - i) % kScaleSlots);
+      drain(&bar[kDxFull + i], (last / kScaleSlots) & 1);
+    }
+  } else if (warp == 0 && lane == 1) {
     // ---- producer: activation operand tiles (1-D bulk, pre-swizzled) ----
-    if (lane == 0) {
-      const uint8_t *src = xp + int64_t(n_tile) * nsub * kOpBytes;
-      int g = 0;
-      for (; g < nsub; ++g) {
-        const int as = g % kSubStages;
-        if (!tc_wait(&bar[kSubEmpty + as], ((g / kSubStages) & 1) ^ 1, spin, abort_flag, err)) break;
-        mbar_arrive_expect_tx(&bar[kBFull + as], kOpBytes);
-        bulk_g2s(sm + kOffB + as * kOpBytes, src + int64_t(g) * kOpBytes, kOpBytes, &bar[kBFull + as]);
-      }
-      for (int i = 0; i < kSubStages && i < g; ++i) {
-        const int last = g - 1 - ((g - 1 - i) % kSubStages);
-        drain(&bar[kBFull + i], (last / kSubStages) & 1);
-      }
+    const uint8_t *src = xp + int64_t(n_tile) * nsub * kOpBytes;
+    int g = 0;
+    for (; g < nsub; ++g) {
+      const int as = g % kSubStages;
+      if (!tc_wait(&bar[kSubEmpty + as], ((g / kSubStages) & 1) ^ 1, spin, abort_flag, err)) break;
+      mbar_arrive_expect_tx(&bar[kBFull + as], kOpBytes);
+      bulk_g2s(sm + kOffB + as * kOpBytes, src + int64_t(g) * kOpBytes, kOpBytes, &bar[kBFull + as]);
     }
-  } else if (warp == 1) {
+    for (int i = 0; i < kSubStages && i < g; ++i) {
+      const int last = g - 1 - ((g - 1 - i) % kSubStages);
+      drain(&bar[kBFull + i], (last / kSubStages) & 1);
+    }
+  } else if (warp == 1 && lane == 0) {
     // ---- MMA issue (one lane) ----
-    if (lane == 0) {
-      const uint32_t a0 = smem_u32(sm + kOffA), b0 = smem_u32(sm + kOffB);
-      for (int gb = 0; gb < nb; ++gb) {
-        const int g = gb >> 1, j = gb & 1, as = g % kSubStages, sb = gb % kSBufs;
-        if (j == 0) {
-          if (!tc_wait(&bar[kAReady + as], (g / kSubStages) & 1, spin, abort_flag, err)) break;
-          if (!tc_wait(&bar[kBFull + as], (g / kSubStages) & 1, spin, abort_flag, err)) break;
-        }
-        if (!tc_wait(&bar[kTEmpty + sb], ((gb / kSBufs) & 1) ^ 1, spin, abort_flag, err)) break;
-        tc_fence_after();
-        const uint64_t ad = sw128_desc(a0 + as * kOpBytes) + uint64_t(j * 4);
-        const uint64_t bd = sw128_desc(b0 + as * kOpBytes) + uint64_t(j * 4);
-        const uint32_t d = tmem + uint32_t(sb * kTN);
-        tc_mma(d, ad, bd, 0);          // k 0..15 of the block
-        tc_mma(d, ad + 2, bd + 2, 1);  // k 16..31 (32 bytes further)
-        tc_commit(&bar[kTFull + sb]);
-        if (j == 1) tc_commit(&bar[kSubEmpty + as]);
+    const uint32_t a0 = smem_u32(sm + kOffA), b0 = smem_u32(sm + kOffB);
+    for (int gb = 0; gb < nb; ++gb) {
+      const int g = gb >> 1, j = gb & 1, as = g % kSubStages, sb = gb % kSBufs;
+      if (j == 0) {
+        if (!tc_wait(&bar[kAReady + as], (g / kSubStages) & 1, spin, abort_flag, err)) break;
+        if (!tc_wait(&bar[kBFull + as], (g / kSubStages) & 1, spin, abort_flag, err)) break;
       }
-      tc_commit(&bar[kDone]);
-      drain(&bar[kDone], 0);
+      if (!tc_wait(&bar[kTEmpty + sb], ((gb / kSBufs) & 1) ^ 1, spin, abort_flag, err)) break;
+      tc_fence_after();
+      const uint64_t ad = sw128_desc(a0 + as * kOpBytes) + uint64_t(j * 4);
+      const uint64_t bd = sw128_desc(b0 + as * kOpBytes) + uint64_t(j * 4);
+      const uint32_t d = tmem + uint32_t(sb * kTN);
+      tc_mma(d, ad, bd, 0);          // k 0..15 of the block
+      tc_mma(d, ad + 2, bd + 2, 1);  // k 16..31 (32 bytes further)
+      tc_commit(&bar[kTFull + sb]);
+      if (j == 1) tc_commit(&bar[kSubEmpty + as]);
     }
-  } else if (warp == 2 || warp == 3 || warp == 12 || warp == 13) {
+    tc_commit(&bar[kDone]);
+    drain(&bar[kDone], 0);
+  } else if (warp == 2 || warp == 3) {
     // ---- converters: raw Q8_0 blocks -> binary16 codes (swizzled) + fp32 scales ----
-    const int r = (warp == 2 ? 0 : warp == 3 ? 1 : warp == 12 ? 2 : 3) * 32 + lane;
+    const int r = (warp - 2) * 32 + lane;  // rows r and r + 64
     for (int c = 0; c < nchunks; ++c) {
       const int rs = c % kRawStages, ss = c % kScaleSlots;
       if (!tc_wait_warp(&bar[kRawFull + rs], (c / kRawStages) & 1, spin, abort_flag, err)) break;
       if (!tc_wait_warp(&bar[kScaleEmpty + ss], ((c / kScaleSlots) & 1) ^ 1, spin, abort_flag, err)) break;
-      const uint8_t *row = sm + kOffRaw + rs * kRawBytes + r * kRawPitch;
+      const uint8_t *raw = sm + kOffRaw + rs * kRawBytes;
       float *dw = reinterpret_cast<float *>(sm + kOffScale + ss * kScaleSlotBytes) + kChunkBlocks * 128;
 #pragma unroll
-      for (int j = 0; j < kChunkBlocks; ++j)
-        dw[j * 128 + r] = half_bits_to_float(reinterpret_cast<const uint16_t *>(row)[17 * j]);
+      for (int j = 0; j < kChunkBlocks; ++j) {
+        dw[j * 128 + r] = half_bits_to_float(reinterpret_cast<const uint16_t *>(raw + r * kRawPitch)[17 * j]);
+        dw[j * 128 + r + 64] = half_bits_to_float(reinterpret_cast<const uint16_t *>(raw + (r + 64) * kRawPitch)[17 * j]);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kScaleFull + ss]);
       bool ok = true;
@@ -343,27 +441,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = false;
           break;
         }
-        // bytes 68k .. 68k+67 of the row: 16-byte vectors 4k .. 4k+4, words k .. k+16 of them
-        uint32_t w[20];
-#pragma unroll
-        for (int i = 0; i < 5; ++i) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * (4 * k + i));
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
-        }
-        uint32_t code[16];  // first block: bytes 2..33 (shifted by 2 bytes); second: words 9..16
-#pragma unroll
-        for (int i = 0; i < 8; ++i) code[i] = __funnelshift_r(w[k + i], w[k + i + 1], 16);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) code[8 + i] = w[k + 9 + i];
-        uint8_t *a = sm + kOffA + as * kOpBytes;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint2 lo = codes_to_f16x2(code[2 * cc]), hi = codes_to_f16x2(code[2 * cc + 1]);
-          *reinterpret_cast<uint4 *>(a + sw128_off(r, cc)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-        }
+        convert_stage(raw, sm + kOffA + as * kOpBytes, r, k);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kAReady + as]);
@@ -372,14 +450,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kRawEmpty + rs]);
     }
-  } else if (warp >= 4 && warp <= 11) {
-    // ---- epilogue ----
+  } else if (warp >= 4 && warp < 4 + kEpiWarps) {
+    // ---- epilogue: lanes 32 (warp mod 4) .., 64 columns, two 32-column chunks ----
     const int lg = warp & 3, ch = (warp - 4) >> 2;
-    const int row = lg * 32 + lane;
+    const int row = lg * 32 + lane, col0 = ch * kEpiCols;
     const uint32_t lane_addr = tmem + (uint32_t(lg * 32) << 16);
-    uint64_t part[32];  // columns 64ch + 2i, 2i + 1
+    uint64_t part[kEpiCols / 2];  // columns col0 + 2i, 2i + 1
 #pragma unroll
-    for (int i = 0; i < 32; ++i) part[i] = 0;
+    for (int i = 0; i < kEpiCols / 2; ++i) part[i] = 0;
     bool first_fold = true, ok = true;
     for (int gb = 0; gb < nb && ok; ++gb) {
       const int c = gb / kChunkBlocks, jj = gb % kChunkBlocks, ss = c % kScaleSlots, sb = gb % kSBufs;
@@ -393,70 +471,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float *slot = reinterpret_cast<const float *>(sm + kOffScale + ss * kScaleSlotBytes);
       const float dwv = slot[kChunkBlocks * 128 + jj * 128 + row];
       const uint64_t dw2 = pack2(__float_as_uint(dwv), __float_as_uint(dwv));
-      const float4 *dx4 = reinterpret_cast<const float4 *>(slot + jj * 128 + ch * 64);
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {  // 16 columns at a time
-        uint32_t s16[16];
-        tmem_ld16(lane_addr + uint32_t(sb * kTN + ch * 64 + h * 16), s16);
-        if (h == 3) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar[kTEmpty + sb]);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 d = lds_f4_ordered(dx4 + h * 4 + q);
-          const uint64_t p01 = fmul2(dw2, pack2(__float_as_uint(d.x), __float_as_uint(d.y)));
-          const uint64_t p23 = fmul2(dw2, pack2(__float_as_uint(d.z), __float_as_uint(d.w)));
-          const int i = h * 8 + 2 * q;
-          part[i] = ffma2(pack2(s16[4 * q], s16[4 * q + 1]), p01, part[i]);
-          part[i + 1] = ffma2(pack2(s16[4 * q + 2], s16[4 * q + 3]), p23, part[i + 1]);
-        }
-      }
+      const float4 *dx4 = reinterpret_cast<const float4 *>(slot + jj * 128 + col0);
+      uint32_t s0[32], s1[32];
+      tmem_ld32_issue(lane_addr + uint32_t(sb * kTN + col0), s0);
+      tmem_ld_wait(s0);
+      tmem_ld32_issue(lane_addr + uint32_t(sb * kTN + col0 + 32), s1);  // lands while chunk 0 is scaled
+      scale_accumulate(part, s0, dw2, dx4);
+      tmem_ld_wait(s1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kTEmpty + sb]);
+      scale_accumulate(part + 16, s1, dw2, dx4 + 8);
       if (jj == kChunkBlocks - 1) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kScaleEmpty + ss]);
       }
-      const bool last = gb == nb - 1;
-      if ((gb % kFold) == kFold - 1 || last) {
-        // fold the partial sums into the running sum (tensor-memory columns 384 + 64ch ..)
+      if ((gb % kFold) == kFold - 1 || gb == nb - 1) {
+        // fold the partial sums into the running sum (tensor-memory columns 384 + col0 ..)
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint32_t acc_addr = lane_addr + uint32_t(kAccCol + ch * 64 + h * 16);
-          uint32_t v[16];
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t acc_addr = lane_addr + uint32_t(kAccCol + col0 + 32 * h);
+          uint32_t v[32];
           if (first_fold) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              v[2 * i] = uint32_t(part[h * 8 + i]);
-              v[2 * i + 1] = uint32_t(part[h * 8 + i] >> 32);
+            for (int i = 0; i < 16; ++i) {
+              v[2 * i] = uint32_t(part[16 * h + i]);
+              v[2 * i + 1] = uint32_t(part[16 * h + i] >> 32);
             }
           } else {
-            tmem_ld16(acc_addr, v);
+            tmem_ld32(acc_addr, v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint64_t sum = fadd2(pack2(v[2 * i], v[2 * i + 1]), part[h * 8 + i]);
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t sum = fadd2(pack2(v[2 * i], v[2 * i + 1]), part[16 * h + i]);
               v[2 * i] = uint32_t(sum);
               v[2 * i + 1] = uint32_t(sum >> 32);
             }
           }
-          tmem_st16(acc_addr, v);
+          tmem_st32(acc_addr, v);
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) part[i] = 0;
+        for (int i = 0; i < kEpiCols / 2; ++i) part[i] = 0;
         first_fold = false;
       }
     }
     if (ok && !*abort_flag) {
       const int m = m0 + row;
-      const int nbase = n_tile * kTN + ch * 64;
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        uint32_t v[16];
-        tmem_ld16(lane_addr + uint32_t(kAccCol + ch * 64 + h * 16), v);
+      for (int h = 0; h < 2; ++h) {
+        const int nbase = n_tile * kTN + col0 + 32 * h;
+        uint32_t v[32];
+        tmem_ld32(lane_addr + uint32_t(kAccCol + col0 + 32 * h), v);
         if (m < M) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (nbase + h * 16 + i < N) Y[int64_t(nbase + h * 16 + i) * M + m] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i)
+            if (nbase + i < N) Y[int64_t(nbase + i) * M + m] = __uint_as_float(v[i]);
         }
       }
     }
