@@ -52,6 +52,9 @@ def lib():
         "bq_dequantize_rows": ([i, vp, vp, i64, i64], i),
         "bq_gemv": ([i, vp, vp, vp, i64, i64], i),
         "bq_gemv_multi": ([i, i, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64), vp, i64], i),
+        "bq_gemv_sequence": ([i, i, ctypes.POINTER(i), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64),
+                              ctypes.POINTER(vp), ctypes.POINTER(i64)], i),
+        "bq_gemv_sequence_workspace_size": ([], sz),
         "bq_gemm": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_kv_quantize": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_block_dots": ([i, vp, vp, vp, i64, i64], i),
@@ -179,6 +182,45 @@ def gemv_multi(t: int, w_list, x: torch.Tensor, M_list, K: int, outs=None):
     _workspace(x.device, int(L.bq_gemv_workspace_size(t, K)))
     _check(L.bq_gemv_multi(t, n, W, Y, M, _ptr(x), K), "bq_gemv_multi")
     return outs
+
+
+def gemv_sequence_args(groups):
+    """ctypes arrays for bq_gemv_sequence from batches (w_list, x, M_list, K, outs).
+    Building them once and passing them to gemv_sequence_call keeps the
+    per-call host work to one C call."""
+    n_groups = len(groups)
+    n_mats = (ctypes.c_int * n_groups)(*[len(g[0]) for g in groups])
+    ws = [w for g in groups for w in g[0]]
+    ys = [y for g in groups for y in g[4]]
+    ms = [m for g in groups for m in g[2]]
+    W = (ctypes.c_void_p * len(ws))(*[w.data_ptr() for w in ws])
+    Y = (ctypes.c_void_p * len(ys))(*[y.data_ptr() for y in ys])
+    M = (ctypes.c_int64 * len(ms))(*ms)
+    X = (ctypes.c_void_p * n_groups)(*[g[1].data_ptr() for g in groups])
+    K = (ctypes.c_int64 * n_groups)(*[g[3] for g in groups])
+    return (n_groups, n_mats, W, Y, M, X, K)
+
+
+def gemv_sequence_call(t: int, args, device):
+    L = _prep(device)
+    _workspace(device, int(L.bq_gemv_sequence_workspace_size()))
+    _check(L.bq_gemv_sequence(t, *args), "bq_gemv_sequence")
+
+
+def gemv_sequence(t: int, groups):
+    """Batches (w_list, x, M_list, K, outs) in one launch; batch g reads its x
+    after the outputs of batches 0..g-1 are written. outs may be None."""
+    full = []
+    for w_list, x, M_list, K, outs in groups:
+        for w in w_list:
+            _cuda(w, "w_blocks")
+        _cuda(x, "x")
+        if outs is None:
+            outs = [torch.empty(m, dtype=torch.float32, device=x.device) for m in M_list]
+        full.append((w_list, x, M_list, K, outs))
+    if full:
+        gemv_sequence_call(t, gemv_sequence_args(full), full[0][1].device)
+    return [g[4] for g in full]
 
 
 def gemm(t: int, w_blocks: torch.Tensor, X: torch.Tensor, M: int, N: int, K: int,

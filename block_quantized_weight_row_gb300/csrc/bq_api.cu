@@ -1,6 +1,7 @@
 // bq_api.cu — the C ABI of libbq.so (declared in include/bq.h): argument
 // validation, per-thread stream / workspace / error state, per-device info,
 // and the device error word that bounded in-kernel waits report through.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -8,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "bq.h"
 #include "bq_device.cuh"
@@ -298,6 +300,89 @@ int bq_gemv_multi(int type, int n, const void *const *W, float *const *y, const 
 
 int bq_gemv(int type, const void *W, const float *x, float *y, int64_t M, int64_t K) {
   return bq_gemv_multi(type, 1, &W, &y, &M, x, K);
+}
+
+size_t bq_gemv_sequence_workspace_size(void) { return 256; }
+
+int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *const *W, float *const *y,
+                     const int64_t *M, const float *const *x, const int64_t *K) {
+  const int bb = block_bytes(type);
+  if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_gemv_sequence: unknown type %d", type);
+  if (n_groups < 0) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: negative batch count");
+  if (n_groups == 0) return ok();
+  if (!n_mats || !x || !K) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: null array");
+  int64_t total = 0;
+  for (int g = 0; g < n_groups; ++g) {
+    if (n_mats[g] < 0) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: batch %d has a negative matrix count", g);
+    total += n_mats[g];
+  }
+  if (total > (int64_t(1) << 30)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: too many matrices");
+  if (total > 0 && (!W || !y || !M)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: null array");
+  struct Span {
+    uintptr_t lo, hi;
+    int g;
+  };
+  std::vector<Span> outs;
+  outs.reserve(size_t(total));
+  int64_t mi = 0;
+  for (int g = 0; g < n_groups; ++g) {
+    const int64_t Kg = K[g];
+    if (Kg <= 0 || Kg % 256 || Kg > BQ_GEMV_SEQ_MAX_K)
+      return fail(BQ_ERR_SHAPE, "bq_gemv_sequence: batch %d: K %lld is not a multiple of 256 in 256..%d", g,
+                  (long long)Kg, BQ_GEMV_SEQ_MAX_K);
+    int64_t rows = 0;
+    for (int k = 0; k < n_mats[g]; ++k, ++mi) {
+      if (M[mi] < 0) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: negative M");
+      rows += M[mi];
+      if (M[mi] == 0) continue;
+      if (!W[mi] || !y[mi]) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: null matrix or output");
+      if (!aligned(W[mi], 16) || !aligned(y[mi], 4))
+        return fail(BQ_ERR_ALIGN, "bq_gemv_sequence: W must be 16-byte and y 4-byte aligned");
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(y[mi]);
+      outs.push_back({lo, lo + uintptr_t(M[mi]) * 4, g});
+    }
+    if (rows >= (int64_t(1) << 31)) return fail(BQ_ERR_SHAPE, "bq_gemv_sequence: batch %d has 2^31 rows or more", g);
+    if (rows > 0 && (!x[g] || !aligned(x[g], 16)))
+      return fail(x[g] ? BQ_ERR_ALIGN : BQ_ERR_INVALID_ARG, "bq_gemv_sequence: x of batch %d null or not 16-byte aligned", g);
+  }
+  // outputs are pairwise disjoint; no weight matrix overlaps an output; no
+  // output overlaps its own batch's input
+  std::sort(outs.begin(), outs.end(), [](const Span &a, const Span &b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < outs.size(); ++i)
+    if (outs[i].lo < outs[i - 1].hi) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: two outputs overlap");
+  auto hits = [&](uintptr_t lo, uintptr_t hi, int only_g) {
+    // the last output starting below hi is the only one that can overlap [lo, hi)
+    auto it = std::lower_bound(outs.begin(), outs.end(), hi, [](const Span &a, uintptr_t v) { return a.lo < v; });
+    while (it != outs.begin()) {
+      --it;
+      if (it->hi <= lo) return false;
+      if (only_g < 0 || it->g == only_g) return true;
+    }
+    return false;
+  };
+  mi = 0;
+  for (int g = 0; g < n_groups; ++g) {
+    for (int k = 0; k < n_mats[g]; ++k, ++mi) {
+      if (M[mi] == 0) continue;
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(W[mi]);
+      if (hits(lo, lo + uintptr_t(M[mi]) * uintptr_t(K[g] / kQK) * uintptr_t(bb), -1))
+        return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: an output overlaps a weight matrix");
+    }
+    if (x[g]) {
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(x[g]);
+      if (hits(lo, lo + uintptr_t(K[g]) * 4, g))
+        return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: an output of batch %d overlaps its x", g);
+    }
+  }
+  if (outs.empty()) return ok();
+  const size_t need = bq_gemv_sequence_workspace_size();
+  if (!t_ws || t_ws_bytes < need)
+    return fail(BQ_ERR_WORKSPACE, "bq_gemv_sequence: needs %zu workspace bytes, %zu set", need, t_ws_bytes);
+  if (hits(reinterpret_cast<uintptr_t>(t_ws), reinterpret_cast<uintptr_t>(t_ws) + need, -1))
+    return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: the workspace overlaps an output");
+  cudaError_t e = launch_gemv_seq(type, n_groups, n_mats, reinterpret_cast<const uint8_t *const *>(W), y, M, x, K,
+                                  static_cast<unsigned *>(t_ws), t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemv_sequence launch");
 }
 
 int bq_gemm(int type, const void *W, const float *X, float *Y, int64_t M, int64_t N, int64_t K) {

@@ -56,6 +56,13 @@ cudaError_t launch_dequantize_rows(int type, const uint8_t *blocks, float *dst, 
 cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *y, const int64_t *M,
                         const float *x, int64_t K, uint32_t *rec_ws, cudaStream_t stream);
 size_t gemv_workspace_bytes(int64_t K);
+// A sequence of GEMV batches in one launch per at most 256 batches: batch g
+// (n_mats[g] matrices from the flattened W / y / M arrays, input x[g], K[g] a
+// multiple of 256) behaves as a launch_gemv issued after those of batches
+// 0..g-1. sync: 2 words of scratch (zeroed before each launch).
+cudaError_t launch_gemv_seq(int type, int n_groups, const int *n_mats, const uint8_t *const *W, float *const *y,
+                            const int64_t *M, const float *const *x, const int64_t *K, unsigned *sync,
+                            cudaStream_t stream);
 cudaError_t launch_gemm(int type, const uint8_t *W, const uint8_t *Xq, float *Y, int64_t M,
                         int64_t N, int64_t K, cudaStream_t stream);
 // Prefill GEMM on the tcgen05 tensor cores (K a multiple of 256): quantizes X

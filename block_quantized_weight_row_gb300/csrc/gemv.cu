@@ -29,16 +29,21 @@
 
 #include "bq_device.cuh"
 #include "bq_internal.h"
+#include "gemv_common.cuh"
 
 namespace bq {
 namespace {
+
+using gemv::kXRecBytes;
+using gemv::kXRecWords;
+using gemv::group_terms;
+using gemv::quantize_x_records;
+using gemv::GroupWords;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kMaxMats = BQ_GEMV_MAX_MATS;
 
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
-constexpr int kXRecWords = 84;          // per group of 8 blocks: 64 code words, 8 scales, 8 sums, 4 pad
-constexpr int kXRecBytes = kXRecWords * 4;
 constexpr uint32_t kDrainLimit = 1u << 26;
 constexpr int kMaxStageBytes = 64 * 1024;
 
@@ -73,115 +78,6 @@ struct StageCursor {
     nrows = min(min(a.stage_rows, r1 - row), a.row_start[mat + 1] - row);
   }
 };
-
-// Quantize x (K fp32, 16-byte aligned) into the per-group records: words
-// [g*84 + 8*jb + i] = codes 4i..4i+3 of block b = 8g+jb, [g*84 + 64 + jb] =
-// the scale as fp32, [g*84 + 72 + jb] = the code sum. 8 lanes per block
-// (coalesced loads, short dependency chains); `nthreads` (a multiple of 32)
-// threads cover nthreads/8 blocks per pass. The loads of up to 12 passes are
-// issued before any arithmetic and passes are quantized 4 at a time in
-// straight-line code. Every thread runs every pass (the guards are uniform),
-// keeping the 8-lane shuffles converged. Passes start at block `rot` so that
-// CTAs reading the same x spread their requests over L2.
-__device__ __forceinline__ void quantize_x_records(const float *__restrict__ x, int nb, uint32_t *rec, int tid,
-                                                   int nthreads, int rot) {
-  constexpr int kBatch = 12;
-  const int j = tid & 7;
-  const int stride = nthreads >> 3;
-  const int passes = (nb + stride - 1) / stride;
-  const int span = passes * stride;
-  for (int p0 = 0; p0 < passes; p0 += kBatch) {
-    float4 v[kBatch];
-    int b[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      b[u] = (p0 + u < passes) ? ((p0 + u) * stride + (tid >> 3) + rot) % span : nb;
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (b[u] < nb) v[u] = __ldcg(reinterpret_cast<const float4 *>(x + b[u] * kQK + j * 4));  // past L1
-    }
-#pragma unroll
-    for (int u0 = 0; u0 < kBatch; u0 += 4) {
-      if (p0 + u0 < passes) {  // uniform across the CTA
-        uint16_t sc[4];
-        uint32_t wd[4];
-        int sm[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) quantize_block_8lanes(v[u0 + k], sc[k], wd[k], sm[k]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (b[u0 + k] < nb) {
-            uint32_t *r = rec + (b[u0 + k] >> 3) * kXRecWords;
-            const int jb = b[u0 + k] & 7;
-            r[8 * jb + j] = wd[k];
-            if (j == 0) {
-              r[64 + jb] = __float_as_uint(half_bits_to_float(sc[k]));
-              r[72 + jb] = uint32_t(sm[k]);
-            }
-          }
-        }
-      }
-    }
-  }
-}
-
-template <int TYPE>
-struct GroupWords;
-template <>
-struct GroupWords<kTypeQ4_0> {
-  static constexpr int kWords = 36;  // 144 bytes
-};
-template <>
-struct GroupWords<kTypeQ8_0> {
-  static constexpr int kWords = 68;  // 272 bytes
-};
-
-// Sum of the 8 block terms of one group. w: the group's bytes as words (the
-// group starts 16-byte aligned, block jb starts at byte BB*jb).
-template <int TYPE>
-__device__ __forceinline__ float group_terms(const uint32_t *w, const uint32_t *xr, float acc) {
-  constexpr int BB = Fmt<TYPE>::kBytes;
-  const uint4 dx0 = *reinterpret_cast<const uint4 *>(xr + 64);
-  const uint4 dx1 = *reinterpret_cast<const uint4 *>(xr + 68);
-  const uint32_t dxs[8] = {dx0.x, dx0.y, dx0.z, dx0.w, dx1.x, dx1.y, dx1.z, dx1.w};
-  uint32_t sxs[8];
-  if (TYPE == kTypeQ4_0) {
-    const uint4 s0 = *reinterpret_cast<const uint4 *>(xr + 72);
-    const uint4 s1 = *reinterpret_cast<const uint4 *>(xr + 76);
-    sxs[0] = s0.x; sxs[1] = s0.y; sxs[2] = s0.z; sxs[3] = s0.w;
-    sxs[4] = s1.x; sxs[5] = s1.y; sxs[6] = s1.z; sxs[7] = s1.w;
-  }
-#pragma unroll
-  for (int jb = 0; jb < 8; ++jb) {
-    constexpr int kQW = (TYPE == kTypeQ4_0) ? 4 : 8;  // code words per block
-    uint32_t q[kQW];
-    uint32_t dbits;
-    const int byte0 = BB * jb;
-    if ((byte0 & 3) == 0) {
-      // scale in the low half of word byte0/4; codes start 2 bytes later
-      const int w0 = byte0 >> 2;
-      dbits = w[w0] & 0xffffu;
-#pragma unroll
-      for (int i = 0; i < kQW; ++i) q[i] = __funnelshift_r(w[w0 + i], w[w0 + i + 1], 16);
-    } else {
-      // scale in the high half of word (byte0-2)/4; codes are word aligned
-      const int w0 = (byte0 - 2) >> 2;
-      dbits = w[w0] >> 16;
-#pragma unroll
-      for (int i = 0; i < kQW; ++i) q[i] = w[w0 + 1 + i];
-    }
-    const uint4 xa = *reinterpret_cast<const uint4 *>(xr + 8 * jb);
-    const uint4 xb = *reinterpret_cast<const uint4 *>(xr + 8 * jb + 4);
-    const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-    int sumi;
-    if (TYPE == kTypeQ4_0)
-      sumi = sumi_q4_q8(q, xw, int(sxs[jb]));
-    else
-      sumi = sumi_q8_q8(q, xw);
-    const float s = __fmul_rn(half_bits_to_float(dbits), __uint_as_float(dxs[jb]));
-    acc = __fmaf_rn(s, float(sumi), acc);
-  }
-  return acc;
-}
 
 template <int TYPE>
 __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) {

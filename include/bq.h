@@ -101,6 +101,34 @@ int bq_gemv(int type, const void *W_blocks, const float *x, float *y, int64_t M,
 int bq_gemv_multi(int type, int n, const void *const *W_blocks, float *const *y, const int64_t *M,
                   const float *x, int64_t K);
 
+/* Largest K taken by bq_gemv_sequence. */
+#define BQ_GEMV_SEQ_MAX_K 16384
+
+/* A sequence of decode GEMV batches in one persistent launch (a decode step's
+ * matrix products, "05. llama.cpp…", §性能直觉：带宽决定 Decode). Batch g has
+ * n_mats[g] matrices that read the input x[g] and the same K[g]; its
+ * matrices are entries mat0 .. mat0 + n_mats[g] - 1 of the flattened arrays
+ * W_blocks, y and M, mat0 being the sum of the earlier n_mats. The result is
+ * that of one bq_gemv_multi call per batch, issued in order: batch g reads
+ * x[g] only after every output of batches 0..g-1 has been written, so x[g]
+ * may be (part of) such an output. Inside the launch a grid-wide barrier
+ * (bounded waits) separates the batches while the weights of later batches
+ * keep streaming into shared memory.
+ * All arrays are HOST arrays; their entries are device pointers. W_blocks
+ * (16-byte aligned): M rows of K/32 blocks of `type`; x[g] (16-byte aligned):
+ * K[g] fp32; y (4-byte aligned): M fp32.
+ * Errors: BQ_ERR_SHAPE (K[g] not a positive multiple of 256 or above
+ * BQ_GEMV_SEQ_MAX_K, a batch of 2^31 rows or more), BQ_ERR_ALIGN,
+ * BQ_ERR_INVALID_ARG (null pointers, negative sizes, an output overlapping
+ * another output, any weight matrix or its own batch's x), BQ_ERR_WORKSPACE
+ * (no workspace of bq_gemv_sequence_workspace_size() bytes set: the launch
+ * keeps its barrier counter there, so calls sharing a workspace must not run
+ * concurrently). The pages have no persistent launch; llama.cpp launches one
+ * kernel per matrix product. */
+int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *const *W_blocks, float *const *y,
+                     const int64_t *M, const float *const *x, const int64_t *K);
+size_t bq_gemv_sequence_workspace_size(void);
+
 /* Prefill GEMM: Y = X . W^T for N tokens; prefill reuses each weight across
  * many tokens and is compute-bound ("05. llama.cpp…", §性能直觉).
  * type: Q8_0 weights. W_blocks: M x K/32 blocks. X: N x K fp32 (each row

@@ -176,3 +176,38 @@ def test_product_path_never_imports_the_oracle():
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "bq_oracle" not in src, f
+
+
+def _seq(L, n_mats, W, Y, M, X, K, t=8):
+    """bq_gemv_sequence with integer stand-ins for device pointers (the calls
+    below fail validation, or find no workspace, before any device work)."""
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    g = len(n_mats)
+    return L.bq_gemv_sequence(t, g, (ctypes.c_int * g)(*n_mats), (vp * len(W))(*W), (vp * len(Y))(*Y),
+                              (i64 * len(M))(*M), (vp * g)(*X), (i64 * g)(*K))
+
+
+def test_gemv_sequence_validation(L):
+    assert L.bq_set_workspace(None, 0) == 0
+    base = 1 << 32
+    W0, W1 = base, base + (1 << 24)
+    Y0, Y1 = base + (2 << 24), base + (3 << 24)
+    X0, X1 = base + (4 << 24), base + (5 << 24)
+    ok = dict(n_mats=[1, 1], W=[W0, W1], Y=[Y0, Y1], M=[64, 64], X=[X0, X1], K=[512, 512])
+    assert L.bq_gemv_sequence_workspace_size() == 256
+    assert L.bq_gemv_sequence(8, 0, None, None, None, None, None, None) == 0
+    assert _seq(L, **ok) == -7                               # valid, but no workspace set
+    assert _seq(L, **{**ok, "K": [512, 96]}) == -2           # K not a multiple of 256
+    assert _seq(L, **{**ok, "K": [512, 32768]}) == -2        # above BQ_GEMV_SEQ_MAX_K
+    assert _seq(L, **{**ok, "M": [64, -1]}) == -1
+    assert _seq(L, **{**ok, "n_mats": [1, -1]}) == -1
+    assert _seq(L, **ok, t=5) == -3
+    assert _seq(L, **{**ok, "W": [W0 + 8, W1]}) == -4        # W not 16-byte aligned
+    assert _seq(L, **{**ok, "X": [X0 + 4, X1]}) == -4
+    assert _seq(L, **{**ok, "Y": [Y0 + 2, Y1]}) == -4
+    assert _seq(L, **{**ok, "Y": [Y0, Y0 + 128]}) == -1      # two outputs overlap
+    assert _seq(L, **{**ok, "Y": [Y0, W1 + 64]}) == -1       # an output overlaps a weight matrix
+    assert _seq(L, **{**ok, "X": [Y0 + 64, X1]}) == -1       # batch 0 reads its own output
+    # a later batch may read an earlier batch's output: only the workspace is missing
+    assert _seq(L, **{**ok, "X": [X0, Y0]}) == -7
+    assert "workspace" in L.bq_last_error().decode()

@@ -475,3 +475,135 @@ def test_gemv_both_activation_paths(bq, orc, dev, t, with_ws, Ms, K):
     for i, (m, w) in enumerate(zip(Ms, wq)):
         y_ref, mag = orc.gemv(t, w, x.numpy(), m, K, with_mag=True)
         _check_float(_np(outs[i]), y_ref, mag, f"matrix {i}, workspace={with_ws}")
+
+
+# ------------------------------------------------ GEMV sequence (one launch) --
+
+def _seq_case(t, seed, shapes):
+    """Batches of (K, [M...]) with seeded weights and inputs, quantized by the oracle."""
+    from block_quantized_weight_row_gb300 import inputs
+    batches = []
+    for g, (K, Ms) in enumerate(shapes):
+        x = inputs.activation(K, seed=seed + 100 * g)
+        mats = []
+        for i, M in enumerate(Ms):
+            W = inputs.weight(M, K, seed=seed + 100 * g + 1 + i)
+            mats.append(_orc().quantize_rows(t, W.numpy()))
+        batches.append((K, Ms, x, mats))
+    return batches
+
+
+def _orc():
+    import oracle
+    return oracle
+
+
+@pytest.mark.parametrize("t", [Q4, Q8])
+def test_gemv_sequence_matches_oracle(bq, orc, dev, t):
+    """Mixed K (one to 16 groups of 8 blocks per row, 43 for 11008), ragged
+    and empty matrices, one to three matrices per batch."""
+    shapes = [(256, [7]), (4096, [300, 0, 129]), (1024, [1]), (11008, [64, 33]), (2304, [200]),
+              (512, [1000, 17, 5])]
+    batches = _seq_case(t, 4242, shapes)
+    groups = []
+    for K, Ms, x, mats in batches:
+        outs = [torch.full((M,), float("nan"), device=dev) for M in Ms]
+        groups.append(([torch.from_numpy(w).to(dev) for w in mats], x.to(dev), Ms, K, outs))
+    bq.gemv_sequence(t, groups)
+    torch.cuda.synchronize()
+    for (K, Ms, x, mats), g in zip(batches, groups):
+        for M, w, y in zip(Ms, mats, g[4]):
+            if M == 0:
+                continue
+            y_ref, mag = orc.gemv(t, w, x.numpy(), M, K, with_mag=True)
+            _check_float(_np(y), y_ref, mag, f"sequence K={K} M={M}")
+
+
+def test_gemv_sequence_chain_reads_previous_outputs(bq, orc, dev):
+    """x of batch g+1 is the output of batch g (square matrices): the launch
+    must read it only after every CTA wrote it. The same chain run as one
+    bq_gemv_multi call per batch (same device arithmetic, launches ordered by
+    the stream) gives identical bits; the first product is also checked
+    against the oracle."""
+    from block_quantized_weight_row_gb300 import inputs
+    K, G = 2048, 12
+    ws = [bq.quantize_rows(Q4, inputs.weight(K, K, seed=700 + g, device=dev)) for g in range(G)]
+    x0 = inputs.activation(K, seed=699, device=dev)
+    ys = [torch.full((K,), float("nan"), device=dev) for _ in range(G)]
+    groups = [([ws[g]], x0 if g == 0 else ys[g - 1], [K], K, [ys[g]]) for g in range(G)]
+    bq.gemv_sequence(Q4, groups)
+    ref = [torch.full((K,), float("nan"), device=dev) for _ in range(G)]
+    for g in range(G):
+        bq.gemv_multi(Q4, [ws[g]], x0 if g == 0 else ref[g - 1], [K], K, outs=[ref[g]])
+    torch.cuda.synchronize()
+    for g in range(G):
+        assert torch.equal(ys[g], ref[g]), f"batch {g}"
+    y_ref, mag = orc.gemv(Q4, _np(ws[0]), x0.cpu().numpy(), K, K, with_mag=True)
+    _check_float(_np(ys[0]), y_ref, mag, "chain batch 0")
+
+
+def test_gemv_sequence_longer_than_one_launch(bq, orc, dev):
+    """300 batches and 600 matrices: more than one launch's worth, split on
+    the host; every output still matches the oracle."""
+    from block_quantized_weight_row_gb300 import inputs
+    K = 256
+    W = inputs.weight(48, K, seed=31)
+    wq = orc.quantize_rows(Q8, W.numpy())
+    w_dev = torch.from_numpy(wq).to(dev)
+    xs = inputs.activation(K, seed=32, rows=300)
+    groups = []
+    for g in range(300):
+        outs = [torch.full((48,), float("nan"), device=dev) for _ in range(2)]
+        groups.append(([w_dev, w_dev], xs[g].to(dev), [48, 48], K, outs))
+    bq.gemv_sequence(Q8, groups)
+    torch.cuda.synchronize()
+    for g in (0, 1, 255, 256, 299):
+        y_ref, mag = orc.gemv(Q8, wq, xs[g].numpy(), 48, K, with_mag=True)
+        for y in groups[g][4]:
+            _check_float(_np(y), y_ref, mag, f"batch {g}")
+
+
+def test_gemv_sequence_full_decode_step_matches_per_launch(bq, orc, dev):
+    """The Qwen3-0.6B-shaped decode step (28 layers, 112 batches, 196
+    matrices): identical bits to one launch per batch, and sampled rows of
+    the last layer against the oracle."""
+    from block_quantized_weight_row_gb300 import inputs
+    import bench
+    step = bench.build_decode_step("qwen3-0.6b-decode", dev, bq, inputs)
+    seq_out = []
+    groups = []
+    for g in step["groups"]:
+        outs = [torch.full_like(y, float("nan")) for y in g["y"]]
+        seq_out.append(outs)
+        groups.append((g["w"], g["x"], g["M"], g["K"], outs))
+    bq.gemv_sequence(Q4, groups)
+    bench.run_step(step, bq, True)
+    torch.cuda.synchronize()
+    for g, outs in zip(step["groups"], seq_out):
+        for y_ref, y in zip(g["y"], outs):
+            assert torch.equal(y, y_ref)
+    g = step["groups"][-1]
+    y_ref, mag = orc.gemv(Q4, _np(g["w"][0]), _np(g["x"]), g["M"][0], g["K"], with_mag=True)
+    _check_float(_np(seq_out[-1][0]), y_ref, mag, "last batch")
+
+
+def test_gemv_sequence_timeout_path_returns_error(bq, orc, dev):
+    """Poll budget 0: every wait gives up at once, the grid-wide abort flag
+    stops the other CTAs, copies in flight are drained, the status reports
+    the timeout, and the next call is correct."""
+    from block_quantized_weight_row_gb300 import binding
+    L = binding.lib()
+    batches = _seq_case(Q4, 515, [(1024, [256]), (1024, [128])])
+    groups = [([torch.from_numpy(w).to(dev) for w in mats], x.to(dev), Ms, K, None) for K, Ms, x, mats in batches]
+    assert binding.device_status() == 0
+    try:
+        assert L.bq_set_spin_limit(0) == 0
+        bq.gemv_sequence(Q4, groups)
+        assert binding.device_status() == -6
+    finally:
+        L.bq_set_spin_limit(-1)
+    outs = bq.gemv_sequence(Q4, groups)
+    assert binding.device_status() == 0
+    for (K, Ms, x, mats), ys in zip(batches, outs):
+        y_ref, mag = orc.gemv(Q4, mats[0], x.numpy(), Ms[0], K, with_mag=True)
+        _check_float(_np(ys[0]), y_ref, mag, "after timeout")
