@@ -508,6 +508,9 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
     tops = tot_ops / (tot_ms * 1e-3) / 1e12 * world
     out["prefill_gemm"] = {"metric": "prefill GEMM int8-equivalent TOPS (2*N*M*K per GEMM, X quantize included)",
                            "value": round(tops, 1), "unit": "TOPS", "shapes": rows,
+                           "tensor_frac_of_measured": round(tops / peaks["bf16_tflops"], 4),
+                           "tensor_peak_note": "integer codes run as binary16 operands, so the peak is the measured "
+                                               "dense bf16/f16 rate",
                            "kernel": "k_gemm_q8_tc (tcgen05.mma kind::f16, exact integer codes) + k_quantize_x_tc",
                            "l2": "flushed between iterations"}
 

@@ -165,9 +165,11 @@ int bq_block_dots(int type, const void *W_blocks, const void *xq_blocks, int32_t
  * while it runs, a process whose device memory is fixed after start-up) and
  * have no workspace of their own to lend.
  * Same arguments, layouts and result as bq_gemm (Q8_0 weights only). The
- * Q8_0 activations go to a file-scope device array of
+ * quantized activations go to a file-scope device array of
  * BQ_GEMM_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
- * the process exits; N * (K/32) * 34 bytes beyond it are rejected with
+ * the process exits: bq_gemm's tensor-core path when its activations (2.125
+ * bytes per value, tokens rounded up to 128) fit, else the mma.sync path over
+ * Q8_0 activations; N * (K/32) * 34 bytes beyond the array are rejected with
  * BQ_ERR_WORKSPACE. The call makes no cudaMalloc, cudaFree or other allocating
  * call. Its first call on a device looks up the array's device address with
  * that device current; make that first call before any stream capture. All
