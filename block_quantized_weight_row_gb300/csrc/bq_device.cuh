@@ -80,9 +80,38 @@ __device__ __forceinline__ uint32_t pack_bytes(uint32_t b0, uint32_t b1, uint32_
 // One lane quantizes one whole 32-value block v[0..31]: the scale bits, the
 // block's code bytes as words (Q4_0: 4 words, byte i = (q[i]+8) | (q[i+16]+8)
 // << 4; Q8_0: 8 words of int8 codes) and, when asked, the sum of the codes.
-template <int TYPE, bool SUM>
-__device__ __forceinline__ void quantize_block_lane(const float (&v)[32], uint16_t &scale, uint32_t *words,
-                                                    int &sum) {
+//
+// Common path, per value: r = x * inv, t = r + M with M = 1.5 * 2^23 (+ 8 for
+// Q4_0, the code bias): t is rint(r) + M exactly (ties to even; 8 is even, so
+// the bias does not change a tie's parity), and the low byte of t's bits is
+// already the stored code byte (q + 8 for Q4_0, q mod 256 for Q8_0). The
+// block's largest |r - rint(r)| decides, once per block, whether any value may
+// lie near a tie (> 0.4999, see code_of); then, and when the stored scale is a
+// subnormal binary16 (whose rounding can put |x / ds| above the code range),
+// the whole block takes code_of's exact, clamped path instead. With a normal
+// scale, |x / ds| <= qmax * (1 + 2^-11) + 3 ulp < qmax + 0.5, so no clamp is
+// needed. Every path gives bit-identical codes.
+// Code bytes of a block as words from the per-value bits t (low byte = the
+// stored code byte, see quantize_block_lane).
+template <int TYPE>
+__device__ __forceinline__ void pack_code_words(const uint32_t (&tb)[32], uint32_t *words) {
+  if (TYPE == kTypeQ4_0) {
+    // low byte of each t is q + 8 in 0..15: low nibbles from elements 4i..4i+3,
+    // high nibbles from elements 16+4i..16+4i+3
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = pack_bytes(tb[4 * i], tb[4 * i + 1], tb[4 * i + 2], tb[4 * i + 3]);
+      const uint32_t hi = pack_bytes(tb[16 + 4 * i], tb[16 + 4 * i + 1], tb[16 + 4 * i + 2], tb[16 + 4 * i + 3]);
+      words[i] = lo + (hi << 4);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) words[i] = pack_bytes(tb[4 * i], tb[4 * i + 1], tb[4 * i + 2], tb[4 * i + 3]);
+  }
+}
+
+template <int TYPE>
+__device__ __forceinline__ float block_amax(const float (&v)[32]) {
   // max of |v| as a 5-level tree (exact in any order)
   float m[16];
 #pragma unroll
@@ -91,38 +120,80 @@ __device__ __forceinline__ void quantize_block_lane(const float (&v)[32], uint16
   for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
     for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
-  const float amax = m[0];
+  return m[0];
+}
+
+// The common path of quantize_block_lane alone: false when the block needs the
+// exact path (a value near a tie, or a subnormal scale), and then `words` is
+// not written. Lets a caller that can fetch the block again drop v early.
+template <int TYPE>
+__device__ __forceinline__ bool quantize_block_lane_fast(const float (&v)[32], uint16_t &scale, uint32_t *words) {
   float ds;
-  block_scale<TYPE>(amax, scale, ds);
+  block_scale<TYPE>(block_amax<TYPE>(v), scale, ds);
+  const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
+  constexpr float kMagic = 12582912.0f + float(TYPE == kTypeQ4_0 ? 8 : 0);
+  uint32_t tb[32];
+  float dmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float r = __fmul_rn(v[j], inv);
+    const float t = __fadd_rn(r, kMagic);
+    tb[j] = __float_as_uint(t);
+    dmax = fmaxf(dmax, fabsf(__fsub_rn(r, __fsub_rn(t, kMagic))));
+  }
+  if (dmax > 0.4999f || (ds > 0.0f && ds < 6.103515625e-05f)) return false;
+  pack_code_words<TYPE>(tb, words);
+  return true;
+}
+
+// The exact path of quantize_block_lane alone (any block).
+template <int TYPE>
+__device__ __forceinline__ void quantize_block_lane_exact(const float (&v)[32], uint16_t &scale, uint32_t *words) {
+  float ds;
+  block_scale<TYPE>(block_amax<TYPE>(v), scale, ds);
+  const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
+  constexpr uint32_t kMagicBits = 0x4B400000u + uint32_t(TYPE == kTypeQ4_0 ? 8 : 0);
+  uint32_t tb[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) tb[j] = kMagicBits + uint32_t(code_of<TYPE>(v[j], ds, inv));
+  pack_code_words<TYPE>(tb, words);
+}
+
+template <int TYPE, bool SUM>
+__device__ __forceinline__ void quantize_block_lane(const float (&v)[32], uint16_t &scale, uint32_t *words,
+                                                    int &sum) {
+  float ds;
+  block_scale<TYPE>(block_amax<TYPE>(v), scale, ds);
   // a zero scale (all-zero block, or a scale that underflows binary16) gives
   // inv = 0 and so every code 0, without a branch
   const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
-  int q[32];
+  constexpr int kBias = (TYPE == kTypeQ4_0) ? 8 : 0;
+  constexpr float kMagic = 12582912.0f + float(kBias);
+  constexpr uint32_t kMagicBits = 0x4B400000u + uint32_t(kBias);
+  uint32_t tb[32];
+  float dmax = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) q[j] = code_of<TYPE>(v[j], ds, inv);
-  if (SUM) {  // integer tree sum (exact)
-    int t[16];
+  for (int j = 0; j < 32; ++j) {
+    const float r = __fmul_rn(v[j], inv);
+    const float t = __fadd_rn(r, kMagic);
+    tb[j] = __float_as_uint(t);
+    dmax = fmaxf(dmax, fabsf(__fsub_rn(r, __fsub_rn(t, kMagic))));
+  }
+  if (dmax > 0.4999f || (ds > 0.0f && ds < 6.103515625e-05f)) {  // rare: near a tie, or a subnormal scale
 #pragma unroll
-    for (int j = 0; j < 16; ++j) t[j] = q[j] + q[j + 16];
+    for (int j = 0; j < 32; ++j) tb[j] = kMagicBits + uint32_t(code_of<TYPE>(v[j], ds, inv));
+  }
+  if (SUM) {  // sum of the codes: sum of the bits minus 32 magic words (exact modulo 2^32)
+    uint32_t t2[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t2[j] = tb[j] + tb[j + 16];
 #pragma unroll
     for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
-      for (int j = 0; j < w; ++j) t[j] += t[j + w];
-    sum = t[0];
+      for (int j = 0; j < w; ++j) t2[j] += t2[j + w];
+    sum = int(t2[0] - 32u * kMagicBits);
   }
-  if (TYPE == kTypeQ4_0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t b[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) b[k] = uint32_t(q[4 * i + k] + 8) | (uint32_t(q[16 + 4 * i + k] + 8) << 4);
-      words[i] = pack_bytes(b[0], b[1], b[2], b[3]);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      words[i] = pack_bytes(uint32_t(q[4 * i]), uint32_t(q[4 * i + 1]), uint32_t(q[4 * i + 2]), uint32_t(q[4 * i + 3]));
-  }
+  pack_code_words<TYPE>(tb, words);
 }
 
 // One Q8_0 block held by 8 lanes (lane j of an aligned group of 8 holds

@@ -10,9 +10,11 @@
 // Design (HBM-bound: 128 B of fp32 read per 18 or 34 B written; the
 // quantization arithmetic must stay well under the SMs' issue rate at that
 // byte rate, so one lane owns one whole block: no shuffles, one division per
-// block, full-rate rounding):
+// block, full-rate rounding, one tie test per block):
 //   - warp tile = 32 consecutive blocks (4 KB): read with fully coalesced
-//     128-bit loads (512 contiguous bytes per instruction), then moved through
+//     128-bit loads (512 contiguous bytes per instruction), the next tile's
+//     loads issued before the current tile is quantized (a persistent grid of
+//     two CTAs per SM, so every warp keeps 4 KB of reads in flight), then moved through
 //     a warp-private shared-memory tile so that lane i holds block i. The tile
 //     is XOR-swizzled (16-byte chunk c of block b sits at chunk c ^ (b & 7)),
 //     which keeps both the coalesced writes and the per-block reads free of
@@ -35,7 +37,7 @@ constexpr int kMaxSmemBiasBlocks = 128;  // 16 KB of bias staged per CTA
 __device__ __forceinline__ int swz(int b, int c) { return b * 128 + ((c ^ (b & 7)) << 4); }
 
 template <int TYPE, bool BIAS>
-__global__ void __launch_bounds__(kQuantThreads, 3)
+__global__ void __launch_bounds__(kQuantThreads, 2)
     k_quantize_rows(const float *__restrict__ src, uint8_t *__restrict__ dst, int64_t n_blocks,
                     const float *__restrict__ bias, int64_t bias_period) {
   constexpr int BB = Fmt<TYPE>::kBytes;
@@ -54,23 +56,30 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     __syncthreads();
   }
   const int64_t total_warps = int64_t(gridDim.x) * kQuantWarps;
-  for (int64_t tile = int64_t(blockIdx.x) * kQuantWarps + warp; tile * 32 < n_blocks; tile += total_warps) {
-    const int nblk = int(min(int64_t(32), n_blocks - tile * 32));
-    const float4 *gsrc = reinterpret_cast<const float4 *>(src + tile * 32 * kQK);
-    // coalesced: vector i = lane + 32c is chunk (i & 7) of block (i >> 3)
-    float4 ld[8];
+  // coalesced: vector i = lane + 32c of a tile is chunk (i & 7) of block (i >> 3).
+  // The loads of a warp's next tile are in flight while it quantizes the
+  // current one, so that every warp keeps 4 KB of reads outstanding.
+  auto load_tile = [&](int64_t t, float4 (&ld)[8]) {
+    const int64_t nb = t * 32 < n_blocks ? min(int64_t(32), n_blocks - t * 32) : 0;
+    const float4 *gsrc = reinterpret_cast<const float4 *>(src + t * 32 * kQK);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int i = lane + 32 * c;
       ld[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if ((i >> 3) < nblk) ld[c] = __ldcs(gsrc + i);
+      if ((i >> 3) < nb) ld[c] = __ldcs(gsrc + i);
     }
+  };
+  float4 ld[8];
+  load_tile(int64_t(blockIdx.x) * kQuantWarps + warp, ld);
+  for (int64_t tile = int64_t(blockIdx.x) * kQuantWarps + warp; tile * 32 < n_blocks; tile += total_warps) {
+    const int nblk = int(min(int64_t(32), n_blocks - tile * 32));
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int i = lane + 32 * c;
       *reinterpret_cast<float4 *>(it + swz(i >> 3, i & 7)) = ld[c];
     }
     __syncwarp();
+    load_tile(tile + total_warps, ld);
     float v[32];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -96,8 +105,32 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     }
     uint16_t scale;
     uint32_t w[NW];
-    int unused;
-    quantize_block_lane<TYPE, false>(v, scale, w, unused);
+    if (!quantize_block_lane_fast<TYPE>(v, scale, w)) {
+      // rare (a value near a tie, or a subnormal scale): the block again from
+      // the tile, through the exact path
+      float e[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 f = *reinterpret_cast<const float4 *>(it + swz(lane, c));
+        e[4 * c] = f.x;
+        e[4 * c + 1] = f.y;
+        e[4 * c + 2] = f.z;
+        e[4 * c + 3] = f.w;
+      }
+      if (BIAS && b < n_blocks) {
+        const int64_t bb = b % bias_period;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 f = bias_in_smem ? *reinterpret_cast<const float4 *>(bias_tile + swz(int(bb), c))
+                                        : __ldg(reinterpret_cast<const float4 *>(bias + bb * kQK) + c);
+          e[4 * c] = __fsub_rn(e[4 * c], f.x);
+          e[4 * c + 1] = __fsub_rn(e[4 * c + 1], f.y);
+          e[4 * c + 2] = __fsub_rn(e[4 * c + 2], f.z);
+          e[4 * c + 3] = __fsub_rn(e[4 * c + 3], f.w);
+        }
+      }
+      quantize_block_lane_exact<TYPE>(e, scale, w);
+    }
     // block `lane` of the tile at byte lane*BB (2-byte aligned)
     uint16_t *o = reinterpret_cast<uint16_t *>(ot + lane * BB);
     o[0] = scale;
@@ -158,7 +191,7 @@ cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const flo
   if (!di) return err;
   const int64_t tiles = (n_blocks + 31) / 32;
   const int64_t ctas = (tiles + kQuantWarps - 1) / kQuantWarps;
-  const int64_t grid = min(ctas, int64_t(di->sm_count) * 8);
+  const int64_t grid = min(ctas, int64_t(di->sm_count) * 2);  // persistent: 2 resident CTAs per SM
   k_quantize_rows<TYPE, BIAS><<<unsigned(grid), kQuantThreads, 0, stream>>>(src, dst, n_blocks, bias,
                                                                            bias_period);
   return cudaGetLastError();
