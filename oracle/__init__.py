@@ -54,8 +54,9 @@ def _declare(L):
     L.oracle_gemv.argtypes = [i, vp, vp, vp, vp, i64, i64]
     L.oracle_gemm.argtypes = [i, vp, vp, vp, vp, i64, i64, i64]
     L.oracle_kv_quantize.argtypes = [i, vp, vp, vp, i64, i64, i64]
+    L.oracle_attn_decode.argtypes = [i, i, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float]
     for f in ("oracle_quantize_rows", "oracle_dequantize_rows", "oracle_block_dots",
-              "oracle_gemv", "oracle_gemm", "oracle_kv_quantize"):
+              "oracle_gemv", "oracle_gemm", "oracle_kv_quantize", "oracle_attn_decode"):
         getattr(L, f).restype = i
 
 
@@ -163,3 +164,17 @@ def kv_quantize(t, rows, bias, n_tokens, n_kv_heads, head_dim):
         raise ValueError("oracle kv_quantize: a bias requires the Q4_0 type")
     _check(rc, "kv_quantize")
     return out
+
+
+def attn_decode(k_type, v_type, q, K, V, n_tokens, n_heads, n_kv_heads, head_dim, scale, with_mag=False):
+    """Decode attention of one token: q (n_heads, head_dim) fp32; K, V the
+    quantized caches (n_tokens, n_kv_heads, head_dim/32 blocks). Returns o
+    (n_heads, head_dim), and with_mag also mag (same shape) and the largest
+    |score| per head."""
+    q, K, V = _f32(q), _u8(K), _u8(V)
+    o = np.zeros((n_heads, head_dim), dtype=np.float32)
+    mag = np.zeros((n_heads, head_dim), dtype=np.float64)
+    smax = np.zeros(n_heads, dtype=np.float64)
+    _check(lib().oracle_attn_decode(k_type, v_type, _p(q), _p(K), _p(V), _p(o), _p(mag), _p(smax),
+                                    n_tokens, n_heads, n_kv_heads, head_dim, float(scale)), "attn_decode")
+    return (o, mag, smax) if with_mag else o

@@ -25,6 +25,12 @@
  *          channel) bias is subtracted from K before Q4_0 quantization; any
  *          other K type is rejected.
  *   [DEQ]  xdnf.cn/news/348240, §2.2 — names dequantize_row_q4_0.
+ *   [FA]   05. llama.cpp…, §KV Cache 类型与 Flash Attention, and the lpnh.cn
+ *          KV-cache article, §量化 KV Cache 的一键配置方法 — K and V caches take
+ *          q8_0 / q4_0; a quantized V cache is read by flash attention, which
+ *          computes attention in one pass without the intermediate matrix.
+ *   [SHIFT] lpnh.cn KV-cache article, §解法 — q·k_i = q·(k_i − k̄) + q·k̄, and
+ *          softmax is unchanged by a constant added to a whole row.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   R1 scale first, little-endian fp16, then the codes;
@@ -37,7 +43,12 @@
  *      d16 == 0 gives all codes 0;
  *   R5 activations are quantized to Q8_0 with R3/R4 before the integer dot;
  *   R6 float results are the fp64 sum of exact per-block terms, rounded once
- *      to fp32.
+ *      to fp32;
+ *   R11 attention is scaled dot-product attention over the dequantized cache,
+ *      o_h = sum_t softmax_t(scale q_h . k_t) v_t, query head h reading kv head
+ *      h / (n_heads / n_kv_heads); the scale is the caller's;
+ *   R12 q . k_t is the block dot of R5/R6: q quantized to Q8_0 per block of
+ *      32 channels, the integer dot with K's codes times dk dq.
  *
  * Parity pins (tests/test_oracle_pins.py): block sizes; hand-worked blocks
  * (tests/golden/); fp16 conversion against numpy's binary16; ties; the
@@ -333,5 +344,71 @@ int oracle_kv_quantize(int type, const float *rows, const float *bias, uint8_t *
                 quantize_block(type, tmp, out + b * bb);
             }
         }
+    return 0;
+}
+
+/* ---- decode attention: R11, R12; [FA], [SHIFT] ---- */
+
+int oracle_attn_decode(int k_type, int v_type, const float *q, const uint8_t *K, const uint8_t *V,
+                       float *o, double *mag, double *smax, int64_t n_tokens, int64_t n_heads,
+                       int64_t n_kv_heads, int64_t head_dim, float scale)
+{
+    int64_t bk = oracle_block_bytes(k_type), bv = oracle_block_bytes(v_type);
+    if (bk == 0 || bv == 0 || head_dim <= 0 || head_dim % QK != 0 || n_tokens < 1 || n_kv_heads < 1 ||
+        n_heads < n_kv_heads || n_heads % n_kv_heads != 0)
+        return -1;
+    int64_t nb = head_dim / QK, group = n_heads / n_kv_heads;
+    int64_t bq = oracle_block_bytes(ORACLE_TYPE_Q8_0);
+    uint8_t *qq = (uint8_t *)malloc((size_t)(n_heads * nb * bq));
+    double *s = (double *)malloc((size_t)n_tokens * sizeof(double));
+    float *vrow = (float *)malloc((size_t)head_dim * sizeof(float));
+    if (!qq || !s || !vrow) {
+        free(qq); free(s); free(vrow);
+        return -3;
+    }
+    oracle_quantize_rows(ORACLE_TYPE_Q8_0, q, qq, n_heads, head_dim); /* R12: per head, per 32 channels */
+    for (int64_t h = 0; h < n_heads; h++) {
+        int64_t kvh = h / group; /* R11: grouped query heads share a kv head */
+        const uint8_t *qh = qq + h * nb * bq;
+        /* scores: scale * sum_b dk dq sumi, exact terms summed in fp64 */
+        double smx = -INFINITY, sabs = 0.0;
+        for (int64_t t = 0; t < n_tokens; t++) {
+            const uint8_t *kt = K + (t * n_kv_heads + kvh) * nb * bk;
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; b++) {
+                int32_t sumi = block_dot(k_type, kt + b * bk, qh + b * bq);
+                acc += (double)block_scale(kt + b * bk) * (double)block_scale(qh + b * bq) * (double)sumi;
+            }
+            s[t] = (double)scale * acc;
+            if (s[t] > smx) smx = s[t];
+            if (fabs(s[t]) > sabs) sabs = fabs(s[t]);
+        }
+        /* softmax over the tokens, after subtracting the row maximum ([SHIFT]) */
+        double l = 0.0;
+        for (int64_t t = 0; t < n_tokens; t++) {
+            s[t] = exp(s[t] - smx);
+            l += s[t];
+        }
+        double *acc = (double *)calloc((size_t)(2 * head_dim), sizeof(double));
+        if (!acc) {
+            free(qq); free(s); free(vrow);
+            return -3;
+        }
+        for (int64_t t = 0; t < n_tokens; t++) {
+            double w = s[t] / l;
+            oracle_dequantize_rows(v_type, V + (t * n_kv_heads + kvh) * nb * bv, vrow, 1, head_dim);
+            for (int64_t d = 0; d < head_dim; d++) {
+                acc[d] += w * (double)vrow[d];
+                acc[head_dim + d] += w * fabs((double)vrow[d]);
+            }
+        }
+        for (int64_t d = 0; d < head_dim; d++) {
+            o[h * head_dim + d] = (float)acc[d];
+            if (mag) mag[h * head_dim + d] = acc[head_dim + d];
+        }
+        if (smax) smax[h] = sabs;
+        free(acc);
+    }
+    free(qq); free(s); free(vrow);
     return 0;
 }

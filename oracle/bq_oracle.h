@@ -77,6 +77,18 @@ int oracle_gemm(int w_type, const uint8_t *w_blocks, const float *X, float *Y,
 int oracle_kv_quantize(int type, const float *rows, const float *bias, uint8_t *dst,
                        int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim);
 
+/* Decode attention of one token over a block-quantized KV cache.
+ * q: n_heads x head_dim fp32. K, V: n_tokens x n_kv_heads x (head_dim/32)
+ * blocks of k_type / v_type (the layout oracle_kv_quantize writes).
+ * Query head h reads kv head h / (n_heads / n_kv_heads). Each head of q is
+ * quantized to Q8_0; score s_t = scale * sum_b dk dq sumi (fp64);
+ * w = softmax_t(s) (fp64); o[h][d] = fp32( sum_t w_t * v_hat[t][d] ).
+ * mag (nullable, n_heads x head_dim) = sum_t w_t |v_hat[t][d]|;
+ * smax (nullable, n_heads) = max_t |s_t|. Returns 0, -1 on bad arguments. */
+int oracle_attn_decode(int k_type, int v_type, const float *q, const uint8_t *K, const uint8_t *V,
+                       float *o, double *mag, double *smax, int64_t n_tokens, int64_t n_heads,
+                       int64_t n_kv_heads, int64_t head_dim, float scale);
+
 #ifdef __cplusplus
 }
 #endif

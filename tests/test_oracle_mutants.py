@@ -31,6 +31,12 @@ MUTANTS = [
     ("kv_bias_added", "v = v - bias[h * head_dim + b * QK + j];", "v = v + bias[h * head_dim + b * QK + j];"),
     ("kv_bias_ignores_head", "v = v - bias[h * head_dim + b * QK + j];", "v = v - bias[b * QK + j];"),
     ("q8_clamp_narrow", "const int qmin = (type == ORACLE_TYPE_Q4_0) ? -8 : -127;", "const int qmin = (type == ORACLE_TYPE_Q4_0) ? -8 : -126;"),
+    ("attn_kv_head_modulo", "int64_t kvh = h / group;", "int64_t kvh = h % n_kv_heads;"),
+    ("attn_no_scale", "s[t] = (double)scale * acc;", "s[t] = acc;"),
+    ("attn_weights_unnormalized", "double w = s[t] / l;", "double w = s[t];"),
+    ("attn_v_decoded_as_k", "oracle_dequantize_rows(v_type, V +", "oracle_dequantize_rows(k_type, V +"),
+    ("attn_k_scale_twice", "(double)block_scale(kt + b * bk) * (double)block_scale(qh + b * bq)",
+     "(double)block_scale(kt + b * bk) * (double)block_scale(kt + b * bk)"),
 ]
 
 

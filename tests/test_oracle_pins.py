@@ -312,3 +312,116 @@ def test_mean_centering_lowers_q4_0_attention_error(orc):
             r = _softmax(q[:, h].astype(np.float64) @ Kq[:, h].T.astype(np.float64) / math.sqrt(D))
             kl[name] += float(np.sum(p * (np.log(p) - np.log(r))) / len(p))
     assert kl["cent"] < kl["plain"]
+
+
+# ---------------------------------------- decode attention over the cache --
+# R11 (scaled dot-product attention over the dequantized cache, grouped query
+# heads) and R12 (q . k as the Q8_0 block dot); [FA], [SHIFT].
+
+def _q4_block(scale, codes):
+    """A Q4_0 block from the format definition: fp16 scale (LE), then byte j =
+    (q[j]+8) | (q[j+16]+8) << 4."""
+    c = np.asarray(codes, np.int64) + 8
+    qs = (c[:16] | (c[16:] << 4)).astype(np.uint8)
+    return np.concatenate([np.array([scale], np.float16).view(np.uint8), qs])
+
+
+def _q8_block(scale, codes):
+    return np.concatenate([np.array([scale], np.float16).view(np.uint8),
+                           np.asarray(codes, np.int8).view(np.uint8)])
+
+
+def _rand_cache(orc, rng, T, H, D, kt, vt):
+    K = orc.kv_quantize(kt, rng.normal(size=(T, H, D)).astype(np.float32), None, T, H, D)
+    V = orc.kv_quantize(vt, rng.normal(size=(T, H, D)).astype(np.float32), None, T, H, D)
+    return K, V
+
+
+def test_attn_single_token_returns_its_value_row(orc):
+    rng = np.random.default_rng(3)
+    T, NH, NKV, D = 1, 4, 2, 64
+    K, V = _rand_cache(orc, rng, T, NKV, D, Q4, Q8)
+    q = rng.normal(size=(NH, D)).astype(np.float32)
+    o = orc.attn_decode(Q4, Q8, q, K, V, T, NH, NKV, D, 1.0 / math.sqrt(D))
+    v = orc.dequantize_rows(Q8, V.reshape(-1), D).reshape(NKV, D)
+    for h in range(NH):
+        assert np.array_equal(o[h], v[h // 2])  # weight 1, heads 0,1 -> kv 0; 2,3 -> kv 1
+
+
+def test_attn_equal_keys_give_the_mean_value(orc):
+    rng = np.random.default_rng(4)
+    T, D = 3, 32
+    K1, V = _rand_cache(orc, rng, T, 1, D, Q4, Q4)
+    K = np.repeat(K1[:1], T, axis=0)  # the same key bytes for every token
+    q = rng.normal(size=(1, D)).astype(np.float32)
+    o = orc.attn_decode(Q4, Q4, q, K, V, T, 1, 1, D, 0.3)
+    v = orc.dequantize_rows(Q4, V.reshape(-1), D).astype(np.float64)
+    assert np.allclose(o[0], v.mean(axis=0), rtol=0, atol=1e-6 * np.abs(v).max())
+
+
+def test_attn_two_tokens_closed_form(orc):
+    """Hand-built blocks: q = 1.0 everywhere quantizes to codes 127 with the
+    binary16 scale of 1/127; token 0 has K codes all +1 at scale 0.5, token 1
+    alternates +2 / -1 at scale 0.25; V is constant per token. Scores, softmax
+    and output then follow in closed form."""
+    D = 32
+    dq = float(np.float16(np.float32(1.0) / np.float32(127.0)))
+    assert round(1.0 / dq) == 127
+    K = np.stack([_q4_block(0.5, [1] * 32), _q4_block(0.25, [2, -1] * 16)]).reshape(2, 1, 18)
+    V = np.stack([_q8_block(0.5, [10] * 32), _q8_block(0.125, [-20] * 32)]).reshape(2, 1, 34)
+    scale = float(np.float32(1.0 / math.sqrt(D)))  # the scale is an fp32 argument
+    s0 = scale * 0.5 * dq * (32 * 127 * 1)
+    s1 = scale * 0.25 * dq * (16 * 127 * 2 - 16 * 127)
+    w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    expect = w0 * 5.0 + (1.0 - w0) * (-2.5)
+    q = np.ones((1, D), np.float32)
+    o, mag, smax = orc.attn_decode(Q4, Q8, q, K, V, 2, 1, 1, D, scale, with_mag=True)
+    assert np.allclose(o[0], expect, rtol=1e-6, atol=0)
+    assert np.allclose(mag[0], w0 * 5.0 + (1.0 - w0) * 2.5, rtol=1e-12)
+    assert math.isclose(smax[0], max(abs(s0), abs(s1)), rel_tol=1e-12)
+
+
+def test_attn_grouped_heads_read_their_kv_head(orc):
+    rng = np.random.default_rng(5)
+    T, NH, NKV, D = 40, 6, 3, 64
+    K, V = _rand_cache(orc, rng, T, NKV, D, Q8, Q8)
+    q = rng.normal(size=(NH, D)).astype(np.float32)
+    o = orc.attn_decode(Q8, Q8, q, K, V, T, NH, NKV, D, 0.125)
+    for h in range(NH):
+        kvh = h // 2
+        o1 = orc.attn_decode(Q8, Q8, q[h:h + 1], np.ascontiguousarray(K[:, kvh:kvh + 1]),
+                             np.ascontiguousarray(V[:, kvh:kvh + 1]), T, 1, 1, D, 0.125)
+        assert np.array_equal(o[h], o1[0])
+
+
+def test_attn_token_order_does_not_matter(orc):
+    rng = np.random.default_rng(6)
+    T, NH, NKV, D = 57, 4, 2, 128
+    K, V = _rand_cache(orc, rng, T, NKV, D, Q4, Q8)
+    q = rng.normal(size=(NH, D)).astype(np.float32)
+    o, mag, _ = orc.attn_decode(Q4, Q8, q, K, V, T, NH, NKV, D, 1 / math.sqrt(D), with_mag=True)
+    p = rng.permutation(T)
+    o2 = orc.attn_decode(Q4, Q8, q, np.ascontiguousarray(K[p]), np.ascontiguousarray(V[p]), T, NH, NKV, D,
+                         1 / math.sqrt(D))
+    assert np.all(np.abs(o2 - o) <= 1e-6 * mag + 1e-30)
+
+
+def test_attn_shift_of_all_scores_leaves_the_output(orc):
+    """[SHIFT]: a channel block whose key bytes are the same for every token
+    adds one constant to every score of a head; the other channels' output is
+    unchanged."""
+    rng = np.random.default_rng(7)
+    T, D = 33, 64
+    K, V = _rand_cache(orc, rng, T, 1, D, Q4, Q8)
+    q = rng.normal(size=(1, D)).astype(np.float32)
+    o = orc.attn_decode(Q4, Q8, q, K, V, T, 1, 1, D, 0.2)
+    extra_k = np.tile(_q4_block(0.75, [3] * 32), (T, 1, 1))
+    extra_v = np.tile(_q8_block(0.0, [0] * 32), (T, 1, 1))
+    K2 = np.concatenate([K.reshape(T, 1, -1), extra_k.reshape(T, 1, -1)], axis=2)
+    V2 = np.concatenate([V.reshape(T, 1, -1), extra_v.reshape(T, 1, -1)], axis=2)
+    q2 = np.concatenate([q, np.full((1, 32), 2.0, np.float32)], axis=1)
+    o2, _, s2 = orc.attn_decode(Q4, Q8, q2, K2, V2, T, 1, 1, D + 32, 0.2, with_mag=True)
+    _, _, s1 = orc.attn_decode(Q4, Q8, q, K, V, T, 1, 1, D, 0.2, with_mag=True)
+    assert s2[0] > s1[0] + 1.0  # the shift is real, and large
+    assert np.allclose(o2[0, :D], o[0], rtol=1e-6, atol=1e-7)
+    assert np.all(o2[0, D:] == 0.0)
