@@ -55,6 +55,8 @@ def lib():
         "bq_gemv_sequence": ([i, i, ctypes.POINTER(i), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64),
                               ctypes.POINTER(vp), ctypes.POINTER(i64)], i),
         "bq_gemv_sequence_workspace_size": ([], sz),
+        "bq_attn_decode": ([i, i, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float], i),
+        "bq_attn_workspace_size": ([i, i, i64, i64, i64, i64], sz),
         "bq_gemm": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_kv_quantize": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_block_dots": ([i, vp, vp, vp, i64, i64], i),
@@ -221,6 +223,24 @@ def gemv_sequence(t: int, groups):
     if full:
         gemv_sequence_call(t, gemv_sequence_args(full), full[0][1].device)
     return [g[4] for g in full]
+
+
+def attn_decode(k_type: int, v_type: int, q: torch.Tensor, K_cache: torch.Tensor, V_cache: torch.Tensor,
+                n_kv_heads: int, scale: float, out: torch.Tensor | None = None) -> torch.Tensor:
+    """o (n_heads, head_dim) = attention of q (n_heads, head_dim) over the
+    quantized caches (n_tokens, n_kv_heads, head_dim/32 blocks as bytes)."""
+    _cuda(q, "q")
+    _cuda(K_cache, "K_cache")
+    _cuda(V_cache, "V_cache")
+    H, D = q.shape
+    T = K_cache.shape[0]
+    if out is None:
+        out = torch.empty((H, D), dtype=torch.float32, device=q.device)
+    L = _prep(q.device)
+    _workspace(q.device, int(L.bq_attn_workspace_size(k_type, v_type, T, H, n_kv_heads, D)))
+    _check(L.bq_attn_decode(k_type, v_type, _ptr(q), _ptr(K_cache), _ptr(V_cache), _ptr(out), T, H, n_kv_heads, D,
+                            float(scale)), "bq_attn_decode")
+    return out
 
 
 def gemm(t: int, w_blocks: torch.Tensor, X: torch.Tensor, M: int, N: int, K: int,

@@ -17,7 +17,7 @@ OBJ_DIR = os.path.join(CSRC, "_build")
 LIB = os.path.join(HERE, "libbq.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["bq_api.cu", "quantize.cu", "gemv.cu", "gemv_seq.cu", "gemm.cu", "gemm_tc.cu", "gemm_noalloc.cu"]
+SOURCES = ["bq_api.cu", "quantize.cu", "gemv.cu", "gemv_seq.cu", "gemm.cu", "gemm_tc.cu", "gemm_noalloc.cu", "attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]

@@ -385,6 +385,49 @@ int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *cons
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemv_sequence launch");
 }
 
+namespace {
+int attn_check(int k_type, int v_type, int64_t T, int64_t H, int64_t n_kv, int64_t D, const char *who) {
+  if (!block_bytes(k_type) || !block_bytes(v_type)) return fail(BQ_ERR_UNSUPPORTED, "%s: unknown cache type", who);
+  if (T < 1 || H < 1 || n_kv < 1 || D < kQK || D % kQK || H % n_kv)
+    return fail(BQ_ERR_SHAPE, "%s: needs n_tokens >= 1, head_dim a multiple of 32, n_heads a multiple of n_kv_heads", who);
+  const int64_t G = H / n_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(BQ_ERR_UNSUPPORTED, "%s: %lld query heads per kv head", who, (long long)G);
+  if (H * D > 4096) return fail(BQ_ERR_SHAPE, "%s: n_heads * head_dim above 4096", who);
+  if (T > (int64_t(1) << 21)) return fail(BQ_ERR_SHAPE, "%s: n_tokens above 2^21", who);
+  return BQ_OK;
+}
+}  // namespace
+
+size_t bq_attn_workspace_size(int k_type, int v_type, int64_t n_tokens, int64_t n_heads, int64_t n_kv_heads,
+                              int64_t head_dim) {
+  if (attn_check(k_type, v_type, n_tokens, n_heads, n_kv_heads, head_dim, "bq_attn_workspace_size") != BQ_OK) return 0;
+  return attn_workspace_bytes(k_type, v_type, n_tokens, n_heads, n_kv_heads, head_dim);
+}
+
+int bq_attn_decode(int k_type, int v_type, const float *q, const void *K, const void *V, float *o, int64_t n_tokens,
+                   int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, float scale) {
+  const int st = attn_check(k_type, v_type, n_tokens, n_heads, n_kv_heads, head_dim, "bq_attn_decode");
+  if (st != BQ_OK) return st;
+  if (!q || !K || !V || !o) return fail(BQ_ERR_INVALID_ARG, "bq_attn_decode: null pointer");
+  if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(o, 4))
+    return fail(BQ_ERR_ALIGN, "bq_attn_decode: q, K and V must be 16-byte aligned, o 4-byte aligned");
+  const size_t nb = size_t(head_dim / kQK);
+  const size_t kbytes = size_t(n_tokens) * size_t(n_kv_heads) * nb * block_bytes(k_type);
+  const size_t vbytes = size_t(n_tokens) * size_t(n_kv_heads) * nb * block_bytes(v_type);
+  const size_t qbytes = size_t(n_heads) * size_t(head_dim) * 4;
+  if (overlap(o, qbytes, q, qbytes) || overlap(o, qbytes, K, kbytes) || overlap(o, qbytes, V, vbytes))
+    return fail(BQ_ERR_INVALID_ARG, "bq_attn_decode: o overlaps an input");
+  const size_t need = attn_workspace_bytes(k_type, v_type, n_tokens, n_heads, n_kv_heads, head_dim);
+  if (!t_ws || t_ws_bytes < need)
+    return fail(BQ_ERR_WORKSPACE, "bq_attn_decode: needs %zu workspace bytes, %zu set", need, t_ws_bytes);
+  if (overlap(t_ws, need, o, qbytes) || overlap(t_ws, need, q, qbytes) || overlap(t_ws, need, K, kbytes) ||
+      overlap(t_ws, need, V, vbytes))
+    return fail(BQ_ERR_INVALID_ARG, "bq_attn_decode: the workspace overlaps an argument");
+  cudaError_t e = launch_attn_decode(k_type, v_type, q, static_cast<const uint8_t *>(K), static_cast<const uint8_t *>(V),
+                                     o, n_tokens, n_heads, n_kv_heads, head_dim, scale, t_ws, t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_attn_decode launch");
+}
+
 int bq_gemm(int type, const void *W, const float *X, float *Y, int64_t M, int64_t N, int64_t K) {
   const int bb = block_bytes(type);
   if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_gemm: unknown type %d", type);

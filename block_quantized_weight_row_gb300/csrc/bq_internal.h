@@ -63,6 +63,14 @@ size_t gemv_workspace_bytes(int64_t K);
 cudaError_t launch_gemv_seq(int type, int n_groups, const int *n_mats, const uint8_t *const *W, float *const *y,
                             const int64_t *M, const float *const *x, const int64_t *K, unsigned *sync,
                             cudaStream_t stream);
+// Decode attention of one token over a block-quantized KV cache (attn.cu):
+// chunks of tokens in parallel, then a combine; `ws` holds
+// attn_workspace_bytes(...) bytes of partial results.
+size_t attn_workspace_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D);
+size_t attn_smem_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D);
+cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K, const uint8_t *V, float *o,
+                               int64_t T, int64_t H, int64_t n_kv, int64_t D, float scale, void *ws,
+                               cudaStream_t stream);
 cudaError_t launch_gemm(int type, const uint8_t *W, const uint8_t *Xq, float *Y, int64_t M,
                         int64_t N, int64_t K, cudaStream_t stream);
 // Prefill GEMM on the tcgen05 tensor cores (K a multiple of 256): quantizes X

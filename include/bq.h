@@ -129,6 +129,28 @@ int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *cons
                      const int64_t *M, const float *const *x, const int64_t *K);
 size_t bq_gemv_sequence_workspace_size(void);
 
+/* Decode attention of one token over a block-quantized KV cache (flash
+ * decoding): a quantized V cache is read by flash attention ("05.
+ * llama.cpp…", §KV Cache 类型与 Flash Attention; lpnh.cn KV-cache article,
+ * §量化 KV Cache 的一键配置方法).
+ * q: n_heads x head_dim fp32 (16-byte aligned). K_cache / V_cache: n_tokens x
+ * n_kv_heads x (head_dim/32) blocks of k_type / v_type (Q4_0 or Q8_0; the
+ * layout bq_kv_quantize writes), 16-byte aligned. o: n_heads x head_dim fp32.
+ * Query head h reads kv head h / G, G = n_heads / n_kv_heads. Each head of q
+ * is quantized to Q8_0 per 32 channels; s_t = scale * sum_b dk dq sumi (the
+ * GEMV's block dot); o_h = sum_t softmax_t(s) * v_hat_t (dequantized V).
+ * A mean-centered K cache needs no correction: softmax ignores the constant
+ * q . k_bar (lpnh.cn KV-cache article, §解法).
+ * Limits: 1 <= n_tokens <= 2^21; head_dim a multiple of 32; G in {1, 2, 4, 8};
+ * n_heads * head_dim <= 4096. Needs a workspace of bq_attn_workspace_size(...)
+ * bytes (bq_set_workspace). Errors: BQ_ERR_UNSUPPORTED (types, G),
+ * BQ_ERR_SHAPE (limits), BQ_ERR_ALIGN, BQ_ERR_INVALID_ARG (null pointers, o
+ * overlapping an input), BQ_ERR_WORKSPACE. */
+int bq_attn_decode(int k_type, int v_type, const float *q, const void *K_cache, const void *V_cache, float *o,
+                   int64_t n_tokens, int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, float scale);
+size_t bq_attn_workspace_size(int k_type, int v_type, int64_t n_tokens, int64_t n_heads, int64_t n_kv_heads,
+                              int64_t head_dim);
+
 /* Prefill GEMM: Y = X . W^T for N tokens; prefill reuses each weight across
  * many tokens and is compute-bound ("05. llama.cpp…", §性能直觉).
  * type: Q8_0 weights. W_blocks: M x K/32 blocks. X: N x K fp32 (each row

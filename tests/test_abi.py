@@ -211,3 +211,20 @@ def test_gemv_sequence_validation(L):
     # a later batch may read an earlier batch's output: only the workspace is missing
     assert _seq(L, **{**ok, "X": [X0, Y0]}) == -7
     assert "workspace" in L.bq_last_error().decode()
+
+
+def test_attn_decode_validation(L):
+    assert L.bq_set_workspace(None, 0) == 0
+    base = 1 << 32
+    q, K, V, o = base, base + (1 << 24), base + (2 << 24), base + (3 << 24)
+    f = ctypes.c_float(0.1)
+    assert L.bq_attn_decode(2, 8, q, K, V, o, 100, 16, 8, 128, f) == -7   # valid, no workspace
+    assert L.bq_attn_workspace_size(2, 8, 100, 16, 8, 128) > 0
+    assert L.bq_attn_decode(2, 8, q, K, V, o, 100, 12, 4, 128, f) == -3   # 3 query heads per kv head
+    assert L.bq_attn_decode(2, 8, q, K, V, o, 100, 16, 8, 48, f) == -2    # head_dim not a multiple of 32
+    assert L.bq_attn_decode(2, 8, q, K, V, o, 0, 16, 8, 128, f) == -2     # no tokens
+    assert L.bq_attn_decode(2, 8, q, K, V, o, 100, 64, 8, 128, f) == -2   # n_heads * head_dim above 4096
+    assert L.bq_attn_decode(5, 8, q, K, V, o, 100, 16, 8, 128, f) == -3
+    assert L.bq_attn_decode(2, 8, q + 4, K, V, o, 100, 16, 8, 128, f) == -4
+    assert L.bq_attn_decode(2, 8, q, K, V, q + 256, 100, 16, 8, 128, f) == -1  # o overlaps q
+    assert L.bq_attn_decode(2, 8, None, K, V, o, 100, 16, 8, 128, f) == -1

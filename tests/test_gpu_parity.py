@@ -607,3 +607,71 @@ def test_gemv_sequence_timeout_path_returns_error(bq, orc, dev):
     for (K, Ms, x, mats), ys in zip(batches, outs):
         y_ref, mag = orc.gemv(Q4, mats[0], x.numpy(), Ms[0], K, with_mag=True)
         _check_float(_np(ys[0]), y_ref, mag, "after timeout")
+
+
+# ------------------------------------- decode attention over the KV cache --
+
+def _attn_tol(mag, smax, D):
+    """Bound for the GPU's attention output: 1e-5 of sum_t w_t |v_t| (fp32
+    accumulation), plus the effect of fp32 score rounding: each score carries
+    at most (blocks + 2) roundings of ~|s|, taken with a factor 8 margin, and
+    moving the softmax by ds moves o by at most 2 ds sum_t w_t |v_t|."""
+    ds = 8.0 * (D // 32 + 2) * 2.0 ** -24 * (1.0 + smax)[:, None]
+    return (1e-5 + 2.0 * ds) * mag
+
+
+def _attn_case(orc, T, H, NKV, D, kt, vt, seed, centered=False):
+    rng = np.random.default_rng(seed)
+    mu = rng.uniform(-2, 2, size=(NKV, D)).astype(np.float32)
+    Kf = (mu + rng.normal(size=(T, NKV, D))).astype(np.float32)
+    Vf = rng.normal(size=(T, NKV, D)).astype(np.float32)
+    bias = Kf.astype(np.float64).mean(axis=0).astype(np.float32) if centered else None
+    K = orc.kv_quantize(kt, Kf, bias, T, NKV, D)
+    V = orc.kv_quantize(vt, Vf, None, T, NKV, D)
+    q = rng.normal(size=(H, D)).astype(np.float32)
+    return q, K, V
+
+
+@pytest.mark.parametrize("T,H,NKV,D,kt,vt", [
+    (1, 4, 2, 64, Q4, Q8), (7, 2, 1, 32, Q8, Q4), (33, 8, 8, 128, Q4, Q8), (1000, 16, 8, 128, Q4, Q8),
+    (300, 32, 4, 64, Q8, Q8), (4097, 16, 4, 128, Q4, Q4), (130, 1, 1, 256, Q8, Q8), (70000, 8, 8, 128, Q4, Q8)])
+def test_attn_decode_matches_oracle(bq, orc, dev, T, H, NKV, D, kt, vt):
+    q, K, V = _attn_case(orc, T, H, NKV, D, kt, vt, seed=T + 31 * H + D)
+    scale = 1.0 / math.sqrt(D)
+    o = _np(bq.attn_decode(kt, vt, torch.from_numpy(q).to(dev), torch.from_numpy(K).to(dev),
+                           torch.from_numpy(V).to(dev), NKV, scale))
+    o_ref, mag, smax = orc.attn_decode(kt, vt, q, K, V, T, H, NKV, D, scale, with_mag=True)
+    err = np.abs(o.astype(np.float64) - o_ref)
+    tol = _attn_tol(mag, smax, D)
+    assert np.all(err <= tol), f"worst err/tol {float((err / tol).max()):.3g}"
+
+
+def test_attn_decode_full_layer_with_mean_centered_k(bq, orc, dev):
+    """A full 32768-token layer of the KV-write workload shape (8 kv heads,
+    16 query heads, head_dim 128), K mean-centered before Q4_0."""
+    T, H, NKV, D = 32768, 16, 8, 128
+    q, K, V = _attn_case(orc, T, H, NKV, D, Q4, Q8, seed=77, centered=True)
+    scale = 1.0 / math.sqrt(D)
+    o = _np(bq.attn_decode(Q4, Q8, torch.from_numpy(q).to(dev), torch.from_numpy(K).to(dev),
+                           torch.from_numpy(V).to(dev), NKV, scale))
+    o_ref, mag, smax = orc.attn_decode(Q4, Q8, q, K, V, T, H, NKV, D, scale, with_mag=True)
+    assert np.all(np.abs(o.astype(np.float64) - o_ref) <= _attn_tol(mag, smax, D))
+
+
+def test_attn_decode_timeout_path_returns_error(bq, orc, dev):
+    from block_quantized_weight_row_gb300 import binding
+    L = binding.lib()
+    T, H, NKV, D = 2000, 8, 4, 128
+    q, K, V = _attn_case(orc, T, H, NKV, D, Q4, Q8, seed=5)
+    args = (torch.from_numpy(q).to(dev), torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev))
+    assert binding.device_status() == 0
+    try:
+        assert L.bq_set_spin_limit(0) == 0
+        bq.attn_decode(Q4, Q8, *args, NKV, 0.1)
+        assert binding.device_status() == -6
+    finally:
+        L.bq_set_spin_limit(-1)
+    o = _np(bq.attn_decode(Q4, Q8, *args, NKV, 0.1))
+    assert binding.device_status() == 0
+    o_ref, mag, smax = orc.attn_decode(Q4, Q8, q, K, V, T, H, NKV, D, 0.1, with_mag=True)
+    assert np.all(np.abs(o.astype(np.float64) - o_ref) <= _attn_tol(mag, smax, D))
