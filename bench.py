@@ -345,7 +345,7 @@ def main():
     ap.add_argument("--no-batch", action="store_true",
                     help="one launch per matrix instead of one per group of matrices sharing an input")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "gemm", "kv"), default=None,
+    ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "gemm", "kv", "attn"), default=None,
                     help="run one kernel case a few times and exit (for profiler captures)")
     ap.add_argument("--case-launches", type=int, default=16)
     args = ap.parse_args()
@@ -538,7 +538,31 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
                        "ms_per_step": round(ms, 4), "bytes_per_step": kv_bytes,
                        "hbm_frac_of_measured": round(kv_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                        "l2": "inputs larger than L2 (7.5 GB read per step)"}
-    del layers, g
+
+    # decode attention of one token over every layer's quantized cache: the
+    # caches the KV write above produced (mean-centered Q4_0 K, Q8_0 V), 16
+    # query heads over 8 kv heads
+    HQ = 2 * H
+    qs = [inputs.activation(D, inputs.seed_of("kv-write", layer, 9), device=dev, rows=HQ)
+          for layer in range(kv["layers"])]
+    outs = [torch.empty((HQ, D), dtype=torch.float32, device=dev) for _ in qs]
+    scale = 1.0 / (D ** 0.5)
+
+    def attn_step():
+        for (_K, _V, _b, kq, vq), qv, ov in zip(layers, qs, outs):
+            bq.attn_decode(bq.Q4_0, bq.Q8_0, qv, kq, vq, H, scale, out=ov)
+    g2 = capture(attn_step, stream)
+    ms2 = max_over_ranks(time_graph(g2, stream, 20, 3), dist)
+    cache_bytes = kv["layers"] * T * H * (D // 32) * (18 + 34)
+    out["attn_decode"] = {"metric": "decode attention GB/s of quantized KV cache read (one token, every layer)",
+                          "value": round(aggregate_rate(cache_bytes, world, ms2 * 1e-3) / 1e9, 1), "unit": "GB/s",
+                          "ms_per_step": round(ms2, 4), "bytes_per_step": cache_bytes,
+                          "hbm_frac_of_measured": round(cache_bytes / (ms2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                          "config": f"{kv['layers']} layers x {T} tokens x {H} kv heads x {D}, {HQ} query heads, "
+                                    "Q4_0 K (mean-centered) + Q8_0 V",
+                          "kernel": "k_attn_chunk + k_attn_combine",
+                          "l2": "inputs larger than L2 (1.5 GB of cache per step)"}
+    del layers, g, g2, qs, outs
     torch.cuda.empty_cache()
 
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps
@@ -586,6 +610,19 @@ def kernel_case(name, launches):
         for _ in range(launches):
             bq.kv_quantize(bq.Q4_0, L_.K, bias)
             bq.kv_quantize(bq.Q8_0, L_.V, None)
+    elif name == "attn":
+        kv = inputs.WORKLOADS["kv-write"]
+        T, H, D = kv["tokens"], kv["kv_heads"], kv["head_dim"]
+        caches = []
+        for layer in range(4):  # 4 x 54.5 MB of cache: beyond L2
+            L_ = inputs.kv_layer(layer, T, H, D, kv["calib_tokens"], device=dev)
+            caches.append((bq.kv_quantize(bq.Q4_0, L_.K, None), bq.kv_quantize(bq.Q8_0, L_.V, None)))
+            del L_
+        q = inputs.activation(D, 7300, device=dev, rows=2 * H)
+        o = torch.empty((2 * H, D), device=dev)
+        for i in range(launches):
+            kq, vq = caches[i % len(caches)]
+            bq.attn_decode(bq.Q4_0, bq.Q8_0, q, kq, vq, H, 1.0 / D ** 0.5, out=o)
     torch.cuda.synchronize()
     print(json.dumps({"kernel_case": name, "launches": launches, "ok": True}))
 

@@ -20,8 +20,8 @@
 //   pass 2: o[h][d] = sum_t p[h][t] * dv * qv; a thread owns one kv head's G
 //           query heads x 16/G channels (16 outputs), with partial sums per
 //           sub-tile of at most 32 tokens;
-//   the chunk writes (m, l, o) per head; k_attn_combine merges the chunks in
-//   fp64: o = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c.
+//   the chunk writes (m, l, o) per head; k_attn_combine merges the chunks:
+//   o = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c (fp32, two levels).
 #include <algorithm>
 
 #include "bq_device.cuh"
@@ -31,7 +31,11 @@ namespace bq {
 namespace {
 
 constexpr int kAttnThreads = 256;
-constexpr int kQRecWords = 12;  // per (head, block): 8 code words, scale (fp32), code sum, 2 pad
+// per (block, head): 8 code words, scale (fp32), code sum, 3 pad; stored
+// block-major with an odd stride, so that the lanes of a warp, which read
+// different heads' records of the same block, hit different banks
+constexpr int kQRecWords = 13;
+constexpr int kMaxStages = 4;
 
 // Words covering `bytes` bytes that start at an even shared-memory offset:
 // word i = bytes 4i .. 4i+3 of the block, taken from aligned words by a funnel
@@ -73,22 +77,42 @@ __device__ __forceinline__ float k_block_term(const uint8_t *kb, const uint32_t 
   return __fmul_rn(__fmul_rn(dk, dq), float(sumi));
 }
 
-// DPU dequantized codes of one V block starting at channel c0 (c0 % DPU == 0)
+// DPU dequantized codes of one V block starting at channel c0 (c0 % DPU ==
+// 0), as DPU/2 packed pairs. A code byte u (biased to 0..255 for Q8_0, the
+// nibble for Q4_0) is put in the low mantissa byte of 2^23 and the bias is
+// subtracted, two values per instruction: exact, and without integer-to-float
+// conversion instructions.
 template <int VT, int DPU>
-__device__ __forceinline__ void v_codes(const uint8_t *vb, int c0, float (&v)[DPU]) {
+__device__ __forceinline__ void v_code_pairs(const uint8_t *vb, int c0, uint64_t (&v)[DPU / 2]) {
+  uint32_t bits[DPU];
+  float bias;
   if (VT == kTypeQ8_0) {
-    const int8_t *qs = reinterpret_cast<const int8_t *>(vb + 2);
-#pragma unroll
-    for (int k = 0; k < DPU; ++k) v[k] = float(qs[c0 + k]);
-  } else {
-    const uint8_t *qs = vb + 2;
+    constexpr int NW = DPU >= 4 ? DPU / 4 : 1;
+    uint32_t w[NW];
+    lds_block_words<NW>(vb + 2 + (c0 & ~3), w);  // 2 + (c0 & ~3) is even
 #pragma unroll
     for (int k = 0; k < DPU; ++k) {
-      const int c = c0 + k;
-      const int nib = c < 16 ? (qs[c] & 0x0f) : (qs[c - 16] >> 4);
-      v[k] = float(nib - 8);
+      const int kk = (c0 & 3) + k;  // c0 & 3 != 0 only for DPU = 2
+      bits[k] = __byte_perm(w[kk >> 2] ^ 0x80808080u, 0x4B000000u, 0x7540u + uint32_t(kk & 3));
     }
+    bias = -8388736.0f;  // 2^23 + 128
+  } else {
+    // channel c: nibble c (low) of byte c, or nibble c - 16 (high) of byte c - 16
+    const int byte0 = c0 & 15;
+    constexpr int NW = DPU >= 4 ? DPU / 4 : 1;
+    uint32_t w[NW];
+    lds_block_words<NW>(vb + 2 + (byte0 & ~3), w);
+    const uint32_t sh = c0 >= 16 ? 4u : 0u;
+#pragma unroll
+    for (int k = 0; k < DPU; ++k) {
+      const int kk = (byte0 & 3) + k;
+      bits[k] = 0x4B000000u | (((w[kk >> 2] >> (8 * (kk & 3))) >> sh) & 0x0fu);
+    }
+    bias = -8388616.0f;  // 2^23 + 8
   }
+  const uint64_t b2 = pack2(__float_as_uint(bias), __float_as_uint(bias));
+#pragma unroll
+  for (int k = 0; k < DPU / 2; ++k) v[k] = fadd2(pack2(bits[2 * k], bits[2 * k + 1]), b2);
 }
 
 struct AttnArgs {
@@ -102,7 +126,8 @@ struct AttnArgs {
   int chunk_tokens;  // tokens per chunk (a multiple of sub)
   int sub;           // tokens per ring stage (8, 16 or 32)
   int stage_bytes;   // sub * max(k_tok, v_tok), a multiple of 16
-  int ring_bytes;    // >= 2 stages and >= the split reduction, a multiple of 16
+  int ring_bytes;    // >= the stages and >= the split reduction, a multiple of 16
+  int stages;        // ring stages, 2..4
   unsigned *err;
   uint32_t spin_limit;
 };
@@ -114,20 +139,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = a.nb, H = a.n_heads, CT = a.chunk_tokens;
-  // ring (2 stages, later the split reduction) | 32 B pad | q records | scores [H][CT] | (m, l) [H] | 2 barriers
+  const int SP = CT + 1;  // row stride of the scores: odd, so that 16 heads of one token hit 16 banks
+  // ring (stages, later the split reduction) | 32 B pad | q records | scores [H][CT] | (m, l) [H] | barriers
   uint8_t *ring = smem;
   uint32_t *qrec = reinterpret_cast<uint32_t *>(smem + size_t(a.ring_bytes) + 32);
   float *S = reinterpret_cast<float *>(qrec + H * nb * kQRecWords);
-  float *ML = S + size_t(H) * CT;
+  float *ML = S + size_t(H) * SP;
   uint64_t *bar = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(ML + 2 * H) + 15) & ~uintptr_t(15));
 
   const int t0 = blockIdx.x * CT;
   const int tn = min(CT, a.n_tokens - t0);
   const int ns = (tn + a.sub - 1) / a.sub;  // sub-tiles per pass
 
+  const int NS = a.stages;
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int st = 0; st < NS; ++st) mbar_init(&bar[st], 1);
     fence_mbar_init();
   }
   // q quantized to Q8_0 records, 8 lanes per block (every thread takes every
@@ -141,10 +167,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
     int sum;
     quantize_block_8lanes(v, sc, word, sum);
     if (blk < H * nb) {
-      qrec[blk * kQRecWords + j] = word;
+      uint32_t *r = qrec + ((blk % nb) * H + blk / nb) * kQRecWords;  // head blk / nb, block blk % nb
+      r[j] = word;
       if (j == 0) {
-        qrec[blk * kQRecWords + 8] = __float_as_uint(half_bits_to_float(sc));
-        qrec[blk * kQRecWords + 9] = uint32_t(sum);
+        r[8] = __float_as_uint(half_bits_to_float(sc));
+        r[9] = uint32_t(sum);
       }
     }
   }
@@ -158,13 +185,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
   };
   // full sub-tiles arrive by bulk copy (a multiple of 16 bytes); a partial one
   // (only the chunk's last) is copied by all threads when it is consumed
-  int issued[2] = {0, 0};  // copies armed per stage (thread 0)
+  int issued[kMaxStages] = {0, 0, 0, 0};  // copies armed per stage (thread 0)
   auto issue = [&](int i) {
     if (i >= 2 * ns || tile_tokens(i) != a.sub) return;
-    ++issued[i & 1];
+    const int st = i % NS;
+    ++issued[st];
     const uint32_t bytes = uint32_t(a.sub) * uint32_t(i < ns ? a.k_tok : a.v_tok);
-    mbar_arrive_expect_tx(&bar[i & 1], bytes);
-    bulk_g2s(ring + size_t(i & 1) * a.stage_bytes, tile_src(i), bytes, &bar[i & 1]);
+    mbar_arrive_expect_tx(&bar[st], bytes);
+    bulk_g2s(ring + size_t(st) * a.stage_bytes, tile_src(i), bytes, &bar[st]);
   };
 
   // pass-2 thread unit: kv head, DPU channels from d0, G query heads; S_split
@@ -175,23 +203,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
   const bool has_unit = split < splits;
   const int kvh = u / (a.D / DPU), d0 = (u % (a.D / DPU)) * DPU;
   const int vb_off = (kvh * nb + d0 / kQK) * BBv, c0 = d0 % kQK;
-  float acc[G][DPU], part[G][DPU];
+  uint64_t acc[G][DPU / 2], part[G][DPU / 2];  // channel pairs (d0 + 2k, d0 + 2k + 1)
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int k = 0; k < DPU; ++k) acc[g][k] = part[g][k] = 0.0f;
+    for (int k = 0; k < DPU / 2; ++k) acc[g][k] = part[g][k] = 0;
 
-  int armed[2] = {0, 0};
+  int armed[kMaxStages] = {0, 0, 0, 0};
   bool ok = true;
-  if (tid == 0) issue(0);
+  if (tid == 0)
+    for (int i = 0; i + 1 < NS; ++i) issue(i);
   for (int i = 0; i < 2 * ns && ok; ++i) {
-    if (tid == 0) issue(i + 1);  // the other stage was released by the barrier closing iteration i-1
+    // the stage of tile i + NS - 1 held tile i - 1, released by the barrier closing iteration i - 1
+    if (tid == 0) issue(i + NS - 1);
     const int n = tile_tokens(i);
-    const uint8_t *stage = ring + size_t(i & 1) * a.stage_bytes;
+    const int st = i % NS;
+    const uint8_t *stage = ring + size_t(st) * a.stage_bytes;
     if (n == a.sub) {
-      ok = mbar_wait_bounded(&bar[i & 1], uint32_t(armed[i & 1] & 1), a.spin_limit);
+      ok = mbar_wait_bounded(&bar[st], uint32_t(armed[st] & 1), a.spin_limit);
       if (ok)
-        ++armed[i & 1];
+        ++armed[st];
       else
         atomicOr(a.err, kErrTimeout);
       ok = __syncthreads_and(ok);
@@ -199,7 +230,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
     } else {
       const int bytes = n * (i < ns ? a.k_tok : a.v_tok);  // even
       const uint16_t *src = reinterpret_cast<const uint16_t *>(tile_src(i));
-      uint16_t *dst = reinterpret_cast<uint16_t *>(ring + size_t(i & 1) * a.stage_bytes);
+      uint16_t *dst = reinterpret_cast<uint16_t *>(ring + size_t(st) * a.stage_bytes);
       for (int k = tid; k < bytes / 2; k += kAttnThreads) dst[k] = src[k];
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stage is a bulk-copy target later
       __syncthreads();
@@ -211,21 +242,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
         const int t = p / H, h = p % H;
         const uint8_t *krow = stage + size_t(t) * a.k_tok + size_t(h / G) * nb * BBk;
         float s = 0.0f;
-        for (int b = 0; b < nb; ++b) s = __fadd_rn(s, k_block_term<KT>(krow + b * BBk, qrec + (h * nb + b) * kQRecWords));
-        S[h * CT + tt + t] = __fmul_rn(s, a.scale);
+        for (int b = 0; b < nb; ++b) s = __fadd_rn(s, k_block_term<KT>(krow + b * BBk, qrec + (b * H + h) * kQRecWords));
+        S[h * SP + tt + t] = __fmul_rn(s, a.scale);
       }
       if (i == ns - 1) {
         __syncthreads();
         // ---- softmax over the chunk, one warp per head ----
         for (int h = warp; h < H; h += kAttnThreads / 32) {
           float m = -INFINITY;
-          for (int t = lane; t < tn; t += 32) m = fmaxf(m, S[h * CT + t]);
+          for (int t = lane; t < tn; t += 32) m = fmaxf(m, S[h * SP + t]);
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
           float l = 0.0f;
           for (int t = lane; t < tn; t += 32) {
-            const float e = expf(__fsub_rn(S[h * CT + t], m));
-            S[h * CT + t] = e;
+            const float e = expf(__fsub_rn(S[h * SP + t], m));
+            S[h * SP + t] = e;
             l = __fadd_rn(l, e);
           }
 #pragma unroll
@@ -242,21 +273,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
       for (int t = split; t < n; t += splits) {
         const uint8_t *vb = stage + size_t(t) * a.v_tok + vb_off;
         const float dv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(vb));
-        float vals[DPU];
-        v_codes<VT, DPU>(vb, c0, vals);
+        uint64_t vals[DPU / 2];
+        v_code_pairs<VT, DPU>(vb, c0, vals);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float pdv = __fmul_rn(S[(kvh * G + g) * CT + tt + t], dv);
+          const uint32_t pdv = __float_as_uint(__fmul_rn(S[(kvh * G + g) * SP + tt + t], dv));
+          const uint64_t pdv2 = pack2(pdv, pdv);
 #pragma unroll
-          for (int k = 0; k < DPU; ++k) part[g][k] = __fmaf_rn(pdv, vals[k], part[g][k]);
+          for (int k = 0; k < DPU / 2; ++k) part[g][k] = ffma2(pdv2, vals[k], part[g][k]);
         }
       }
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int k = 0; k < DPU; ++k) {
-          acc[g][k] = __fadd_rn(acc[g][k], part[g][k]);
-          part[g][k] = 0.0f;
+        for (int k = 0; k < DPU / 2; ++k) {
+          acc[g][k] = fadd2(acc[g][k], part[g][k]);
+          part[g][k] = 0;
         }
     }
     __syncthreads();
@@ -264,7 +296,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
   if (!ok) {
     // a wait ran out: let the copies still in flight land before leaving
     if (tid == 0)
-      for (int st = 0; st < 2; ++st)
+      for (int st = 0; st < NS; ++st)
         for (; armed[st] < issued[st]; ++armed[st])
           if (!mbar_wait_bounded(&bar[st], uint32_t(armed[st] & 1), 1u << 26)) break;
     return;
@@ -275,7 +307,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int k = 0; k < DPU; ++k) red[((split - 1) * units + u) * 16 + g * DPU + k] = acc[g][k];
+      for (int k = 0; k < DPU / 2; ++k)
+        reinterpret_cast<uint64_t *>(red)[((split - 1) * units + u) * 8 + g * (DPU / 2) + k] = acc[g][k];
   }
   __syncthreads();
   if (has_unit && split == 0) {
@@ -283,12 +316,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int k = 0; k < DPU; ++k) acc[g][k] = __fadd_rn(acc[g][k], red[((sp - 1) * units + u) * 16 + g * DPU + k]);
+        for (int k = 0; k < DPU / 2; ++k)
+          acc[g][k] = fadd2(acc[g][k], reinterpret_cast<const uint64_t *>(red)[((sp - 1) * units + u) * 8 + g * (DPU / 2) + k]);
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int k = 0; k < DPU; ++k)
-        a.o_part[(size_t(blockIdx.x) * H + kvh * G + g) * a.D + d0 + k] = acc[g][k];
+      for (int k = 0; k < DPU / 2; ++k) {
+        float *dst = a.o_part + (size_t(blockIdx.x) * H + kvh * G + g) * a.D + d0 + 2 * k;
+        dst[0] = __uint_as_float(uint32_t(acc[g][k]));
+        dst[1] = __uint_as_float(uint32_t(acc[g][k] >> 32));
+      }
   }
   for (int h = tid; h < H; h += kAttnThreads) {
     a.ml[(size_t(blockIdx.x) * H + h) * 2] = ML[2 * h];
@@ -296,30 +333,55 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
   }
 }
 
-// o[h][d] = sum_c e^(m_c - M) o_c[h][d] / sum_c e^(m_c - M) l_c[h], in fp64
-__global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ o_part, const float *__restrict__ ml,
+// o[h][d] = sum_c e^(m_c - M) o_c[h][d] / sum_c e^(m_c - M) l_c[h]. One CTA
+// per head and 32 channels; 8 slices of the chunks per channel, each summed in
+// fp32 and then added together (two levels: at most chunks/8 + 8 roundings).
+constexpr int kCombineSlices = 8;
+__global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ o_part, const float *__restrict__ ml,
                                                       float *__restrict__ o, int chunks, int H, int D) {
-  extern __shared__ double e[];  // [chunks]
-  __shared__ double s_M, s_L;
-  const int h = blockIdx.x;
-  if (threadIdx.x == 0) {
-    double M = -INFINITY;
-    for (int c = 0; c < chunks; ++c) M = fmax(M, double(ml[(size_t(c) * H + h) * 2]));
-    s_M = M;
+  extern __shared__ float e[];  // [chunks]
+  __shared__ float red[kCombineSlices][33];
+  const int h = blockIdx.x, d = blockIdx.y * 32 + (threadIdx.x & 31), slice = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // M = max_c m_c (slices of 32 lanes, then over the slices)
+  float m = -INFINITY;
+  for (int c = threadIdx.x; c < chunks; c += blockDim.x) m = fmaxf(m, ml[(size_t(c) * H + h) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  if (lane == 0) red[slice][32] = m;
+  __syncthreads();
+  float M = red[0][32];
+#pragma unroll
+  for (int k = 1; k < kCombineSlices; ++k) M = fmaxf(M, red[k][32]);
+  __syncthreads();
+  float l = 0.0f;
+  for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+    e[c] = expf(__fsub_rn(ml[(size_t(c) * H + h) * 2], M));
+    l = __fmaf_rn(e[c], ml[(size_t(c) * H + h) * 2 + 1], l);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(kFull, l, off);
+  if (lane == 0) red[slice][32] = l;
   __syncthreads();
-  for (int c = threadIdx.x; c < chunks; c += blockDim.x) e[c] = exp(double(ml[(size_t(c) * H + h) * 2]) - s_M);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double L = 0.0;
-    for (int c = 0; c < chunks; ++c) L += e[c] * double(ml[(size_t(c) * H + h) * 2 + 1]);
-    s_L = L;
+  float L = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kCombineSlices; ++k) L += red[k][32];
+  float O0 = 0.0f, O1 = 0.0f;  // two chains, so that the loads of the unrolled loop overlap
+  if (d < D) {
+#pragma unroll 8
+    for (int c = slice; c < chunks; c += 2 * kCombineSlices) {
+      O0 = __fmaf_rn(e[c], __ldg(o_part + (size_t(c) * H + h) * D + d), O0);
+      if (c + kCombineSlices < chunks)
+        O1 = __fmaf_rn(e[c + kCombineSlices], __ldg(o_part + (size_t(c + kCombineSlices) * H + h) * D + d), O1);
+    }
   }
+  red[slice][lane] = O0 + O1;
   __syncthreads();
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    double O = 0.0;
-    for (int c = 0; c < chunks; ++c) O += e[c] * double(o_part[(size_t(c) * H + h) * D + d]);
-    o[size_t(h) * D + d] = float(O / s_L);
+  if (slice == 0 && d < D) {
+    float sum = red[0][lane];
+#pragma unroll
+    for (int k = 1; k < kCombineSlices; ++k) sum += red[k][lane];
+    o[size_t(h) * D + d] = __fdiv_rn(sum, L);
   }
 }
 
@@ -329,10 +391,10 @@ namespace {
 
 constexpr int kAttnTargetChunks = 304;  // two per SM of a 152-SM GPU
 constexpr int kAttnMaxChunkTokens = 512;
-constexpr int kAttnStageBudget = 48 * 1024;
+constexpr int kAttnRingBudget = 72 * 1024;  // two CTAs per SM
 
 struct AttnPlan {
-  int sub, chunk_tokens, chunks, stage_bytes, ring_bytes, k_tok, v_tok;
+  int sub, chunk_tokens, chunks, stage_bytes, ring_bytes, stages, k_tok, v_tok;
   size_t smem;
 };
 
@@ -342,8 +404,12 @@ AttnPlan attn_plan(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D
   p.k_tok = int(n_kv) * nb * (kt == kTypeQ4_0 ? Fmt<kTypeQ4_0>::kBytes : Fmt<kTypeQ8_0>::kBytes);
   p.v_tok = int(n_kv) * nb * (vt == kTypeQ4_0 ? Fmt<kTypeQ4_0>::kBytes : Fmt<kTypeQ8_0>::kBytes);
   const int tok = std::max(p.k_tok, p.v_tok);
-  p.sub = 32;
-  while (p.sub > 8 && p.sub * tok > kAttnStageBudget) p.sub /= 2;
+  // four stages of 16 tokens where they fit (the copies' latency is covered
+  // by three stages of compute), else two stages of at least 8 tokens
+  p.sub = 16;
+  p.stages = 4;
+  while (p.sub > 8 && p.stages * p.sub * tok > kAttnRingBudget) p.sub /= 2;
+  if (p.stages * p.sub * tok > kAttnRingBudget) p.stages = 2;
   const int64_t per = (T + kAttnTargetChunks - 1) / kAttnTargetChunks;
   const int64_t ct = std::min<int64_t>(kAttnMaxChunkTokens, (per + p.sub - 1) / p.sub * p.sub);
   p.chunk_tokens = int(ct);
@@ -351,10 +417,10 @@ AttnPlan attn_plan(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D
   p.stage_bytes = p.sub * tok;  // a multiple of 16: sub is a multiple of 8, a block 18 or 34 bytes
   const int units = int(H * D / 16);
   const int splits = kAttnThreads / units;
-  p.ring_bytes = std::max(2 * p.stage_bytes, (splits - 1) * units * 16 * 4);
+  p.ring_bytes = std::max(p.stages * p.stage_bytes, (splits - 1) * units * 16 * 4);
   p.ring_bytes = (p.ring_bytes + 15) / 16 * 16;
-  p.smem = size_t(p.ring_bytes) + 32 + size_t(H) * nb * kQRecWords * 4 + size_t(H) * p.chunk_tokens * 4 +
-           size_t(H) * 8 + 16 + 16;
+  p.smem = size_t(p.ring_bytes) + 32 + size_t(H) * nb * kQRecWords * 4 + size_t(H) * (p.chunk_tokens + 1) * 4 +
+           size_t(H) * 8 + 16 + 8 * kMaxStages;
   return p;
 }
 
@@ -415,6 +481,7 @@ cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K,
   a.sub = p.sub;
   a.stage_bytes = p.stage_bytes;
   a.ring_bytes = p.ring_bytes;
+  a.stages = p.stages;
   a.err = di->err_word;
   a.spin_limit = spin_limit();
   const int G = int(H / n_kv);
@@ -426,9 +493,10 @@ cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K,
     e = vt == kTypeQ4_0 ? launch_attn_kv<kTypeQ8_0, kTypeQ4_0>(G, a, p.chunks, p.smem, stream)
                         : launch_attn_kv<kTypeQ8_0, kTypeQ8_0>(G, a, p.chunks, p.smem, stream);
   if (e != cudaSuccess) return e;
-  const size_t csmem = size_t(p.chunks) * sizeof(double);
+  const size_t csmem = size_t(p.chunks) * sizeof(float);
   if ((e = ensure_smem(reinterpret_cast<const void *>(k_attn_combine), int(csmem))) != cudaSuccess) return e;
-  k_attn_combine<<<unsigned(H), 128, csmem, stream>>>(a.o_part, a.ml, o, p.chunks, int(H), int(D));
+  k_attn_combine<<<dim3(unsigned(H), unsigned((D + 31) / 32)), 256, csmem, stream>>>(a.o_part, a.ml, o, p.chunks,
+                                                                                  int(H), int(D));
   return cudaGetLastError();
 }
 

@@ -290,6 +290,30 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xffffu)));
 }
 
+// ------------------------------------------------------ packed fp32 pairs --
+
+// Two fp32 values in one 64-bit register pair (lo = first); the f32x2
+// operations round each half like the scalar IEEE operation.
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+  return uint64_t(lo) | (uint64_t(hi) << 32);
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+
 // ------------------------------------------------------------------ memory --
 
 __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
