@@ -31,6 +31,13 @@ namespace bq {
 namespace {
 
 constexpr int kAttnThreads = 256;
+
+// 2^x (hardware approximation, relative error about 2^-22; 0 for -inf)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // per (block, head): 8 code words, scale (fp32), code sum, 3 pad; stored
 // block-major with an odd stride, so that the lanes of a warp, which read
 // different heads' records of the same block, hit different banks
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
           for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
           float l = 0.0f;
           for (int t = lane; t < tn; t += 32) {
-            const float e = expf(__fsub_rn(S[h * SP + t], m));
+            const float e = ex2(__fsub_rn(S[h * SP + t], m));
             S[h * SP + t] = e;
             l = __fadd_rn(l, e);
           }
@@ -333,54 +340,493 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
   }
 }
 
-// o[h][d] = sum_c e^(m_c - M) o_c[h][d] / sum_c e^(m_c - M) l_c[h]. One CTA
-// per head and 32 channels; 8 slices of the chunks per channel, each summed in
-// fp32 and then added together (two levels: at most chunks/8 + 8 roundings).
-constexpr int kCombineSlices = 8;
-__global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ o_part, const float *__restrict__ ml,
-                                                      float *__restrict__ o, int chunks, int H, int D) {
-  extern __shared__ float e[];  // [chunks]
-  __shared__ float red[kCombineSlices][33];
-  const int h = blockIdx.x, d = blockIdx.y * 32 + (threadIdx.x & 31), slice = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  // M = max_c m_c (slices of 32 lanes, then over the slices)
-  float m = -INFINITY;
-  for (int c = threadIdx.x; c < chunks; c += blockDim.x) m = fmaxf(m, ml[(size_t(c) * H + h) * 2]);
+// ---------------------------------------------------------------------------
+// Warp-per-kv-head chunk kernel (n_kv in {1, 2, 4, 8}, D * G <= 1024).
+//
+// The 8 warps of a CTA are (kv head j, token slice ws): warp w takes kv head
+// w % n_kv and tokens [ws * tw, ws * tw + tw) of every tile, so each warp
+// owns its query heads' softmax state and runs without block-wide barriers:
+// tiles of `sub` tokens (K and V rows of the same tokens) arrive by bulk copy
+// into an NS-stage ring with a barrier per stage that completes on arrival, and the
+// warp keeps a running maximum m, sum l and output o per query head (online
+// softmax: when the maximum grows from m to m', l and o are multiplied by
+// e^(m - m')). The warps of a CTA merge the same way at the end.
+// Ring protocol: all NS stages are filled at the start; the last warp to
+// release a stage (a shared counter per stage) issues the copy of the tile NS
+// ahead into it, so no thread ever blocks waiting for a free stage. Waits on a
+// stage poll without suspending the thread (a suspended thread woke up
+// hundreds of cycles after the phase completed).
+//   scores:  lanes are (token, block b); the lane's Q8_0 q records for block b
+//            of its G heads stay in registers; block terms dk * dq * sumi are
+//            summed over the blocks of a token by a butterfly over its lanes;
+//   values:  lanes are (token, 32/G channels); each lane converts its codes
+//            once and adds p * dv * v for all G heads (fp32 pairs).
+constexpr int kWarpAttnWarps = 8;
+constexpr int kWarpAttnThreads = 32 * kWarpAttnWarps;
+constexpr int kQRecWords2 = 12;  // 8 code words, scale, code sum, 2 pad: 48 bytes
+constexpr int kMaxQBlocks = 128;  // H * D <= 4096
+
+struct AttnWArgs {
+  const float *q;
+  const uint8_t *K, *V;
+  float *o_part, *ml;
+  float scale;
+  int n_tokens, n_heads, n_kv, D, nb;
+  int k_tok, v_tok;
+  int lb;            // lanes per token in the score step: nb rounded up to a power of two (<= 32)
+  int chunk_tokens;  // a multiple of sub
+  int tw;            // tokens per warp and tile (<= 32)
+  int sub;           // tokens per tile: tw * 8 / n_kv, a multiple of 8
+  int stage_bytes;   // sub * (k_tok + v_tok): K rows, then V rows
+  int stages;        // 2..4
+  int ring_bytes;    // >= stages * stage_bytes and >= the merge buffer
+  unsigned *err;
+  uint32_t spin_limit;
+};
+
+// CPL codes of one V block from channel o (o % CPL == 0), as CPL/2 exact fp32
+// pairs (the byte in the low mantissa byte of 2^23, minus the bias).
+template <int VT, int CPL>
+__device__ __forceinline__ void v_pairs(const uint8_t *vb, int o, uint64_t (&v)[CPL / 2]) {
+  uint32_t bits[CPL];
+  float bias;
+  if constexpr (VT == kTypeQ8_0) {
+    uint32_t w[CPL / 4];
+    lds_block_words<CPL / 4>(vb + 2 + o, w);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-  if (lane == 0) red[slice][32] = m;
-  __syncthreads();
-  float M = red[0][32];
+    for (int i = 0; i < CPL / 4; ++i) w[i] ^= 0x80808080u;
 #pragma unroll
-  for (int k = 1; k < kCombineSlices; ++k) M = fmaxf(M, red[k][32]);
-  __syncthreads();
-  float l = 0.0f;
-  for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
-    e[c] = expf(__fsub_rn(ml[(size_t(c) * H + h) * 2], M));
-    l = __fmaf_rn(e[c], ml[(size_t(c) * H + h) * 2 + 1], l);
+    for (int k = 0; k < CPL; ++k) bits[k] = __byte_perm(w[k >> 2], 0x4B000000u, 0x7540u + uint32_t(k & 3));
+    bias = -8388736.0f;  // 2^23 + 128
+  } else if constexpr (CPL == 32) {
+    // channel c < 16: low nibble of byte c; c >= 16: high nibble of byte c - 16
+    uint32_t w[4];
+    lds_block_words<4>(vb + 2, w);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      bits[k] = __byte_perm(w[k >> 2] & 0x0f0f0f0fu, 0x4B000000u, 0x7540u + uint32_t(k & 3));
+      bits[k + 16] = __byte_perm((w[k >> 2] >> 4) & 0x0f0f0f0fu, 0x4B000000u,
+                                                     0x7540u + uint32_t(k & 3));
+    }
+    bias = -8388616.0f;  // 2^23 + 8
+  } else {
+    constexpr int NW = CPL / 4;
+    uint32_t w[NW];
+    lds_block_words<NW>(vb + 2 + (o & 15), w);
+    const uint32_t sh = o >= 16 ? 4u : 0u;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = (w[i] >> sh) & 0x0f0f0f0fu;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) bits[k] = __byte_perm(w[k >> 2], 0x4B000000u, 0x7540u + uint32_t(k & 3));
+    bias = -8388616.0f;
   }
+  const uint64_t b2 = pack2(__float_as_uint(bias), __float_as_uint(bias));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(kFull, l, off);
-  if (lane == 0) red[slice][32] = l;
-  __syncthreads();
-  float L = 0.0f;
+  for (int k = 0; k < CPL / 2; ++k) v[k] = fadd2(pack2(bits[2 * k], bits[2 * k + 1]), b2);
+}
+
+template <int KT, int VT, int G>
+__global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWArgs a) {
+  constexpr int CPL = 32 / G;  // channels per lane in the value step
+  constexpr int NP = CPL / 2;
+  constexpr int BBk = Fmt<KT>::kBytes, BBv = Fmt<VT>::kBytes;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = a.nb, H = a.n_heads, n_kv = a.n_kv, D = a.D;
+  // ring | q records [H][nb][12] | scores [8 warps][32][G] | (m, l) [8][G][2] |
+  // control words (abort flag, tiles issued, release count per stage) | barriers
+  uint8_t *ring = smem;
+  uint32_t *qrec = reinterpret_cast<uint32_t *>(smem + size_t(a.ring_bytes));
+  float *P = reinterpret_cast<float *>(qrec + size_t(H) * nb * kQRecWords2);
+  float *WML = P + kWarpAttnWarps * 32 * G;
+  int *ctl = reinterpret_cast<int *>(WML + kWarpAttnWarps * G * 2);
+  volatile int *abort_flag = ctl;
+  int *n_issued = ctl + 1, *released = ctl + 2;
+  uint64_t *full = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(ctl + 2 + kMaxStages) + 15) & ~uintptr_t(15));
+
+  const int t0 = blockIdx.x * a.chunk_tokens;
+  const int tn = min(a.chunk_tokens, a.n_tokens - t0);
+  const int nt = (tn + a.sub - 1) / a.sub;
+  const int NS = a.stages;
+  const int vpart = a.sub * a.k_tok;  // offset of the V rows in a stage (a multiple of 16)
+
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream: the K and V rows of the first NS tiles are asked into L2 at once
+  // (always safe: L2 is where writes become visible, so a line the previous
+  // kernel writes later is updated there), everything else waits until that
+  // kernel has completed. The combine may then be scheduled.
+  if (tid == 0) {
+    const uint32_t n = uint32_t(min(tn, NS * a.sub));
+    prefetch_l2(a.K + int64_t(t0) * a.k_tok, (n * uint32_t(a.k_tok)) & ~15u);
+    prefetch_l2(a.V + int64_t(t0) * a.v_tok, (n * uint32_t(a.v_tok)) & ~15u);
+  }
+
+  // tile i -> stage i % NS: full 16-byte multiples by bulk copy; the tail of
+  // a partial tile (under 16 bytes per tensor) by plain copies of this thread
+  auto issue = [&](int i) {
+    if (i >= nt) return;
+    atomicMax(n_issued, i + 1);  // tiles are issued without gaps: 0 .. n_issued - 1
+    const int st = i % NS;
+    const int n = min(a.sub, tn - i * a.sub);
+    uint8_t *dst = ring + size_t(st) * a.stage_bytes;
+    const uint8_t *ks = a.K + int64_t(t0 + i * a.sub) * a.k_tok;
+    const uint8_t *vs = a.V + int64_t(t0 + i * a.sub) * a.v_tok;
+    const uint32_t kb = uint32_t(n) * uint32_t(a.k_tok), vb = uint32_t(n) * uint32_t(a.v_tok);
+    const uint32_t kb16 = kb & ~15u, vb16 = vb & ~15u;
+    if (kb16 != kb || vb16 != vb) {
+      for (uint32_t k = kb16; k < kb; k += 2)
+        *reinterpret_cast<uint16_t *>(dst + k) = *reinterpret_cast<const uint16_t *>(ks + k);
+      for (uint32_t k = vb16; k < vb; k += 2)
+        *reinterpret_cast<uint16_t *>(dst + vpart + k) = *reinterpret_cast<const uint16_t *>(vs + k);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    mbar_arrive_expect_tx(&full[st], kb16 + vb16);
+    if (kb16) bulk_g2s(dst, ks, kb16, &full[st]);
+    if (vb16) bulk_g2s(dst + vpart, vs, vb16, &full[st]);
+  };
+
+  if (tid == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(&full[st], 1);
+      released[st] = 0;
+    }
+    *abort_flag = 0;
+    *n_issued = 0;
+    fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  // q quantized to Q8_0 records, 8 lanes per block. Every load of q is
+  // issued first (one round trip, ahead of the cache tiles in the memory
+  // queues), then the first tiles' copies, then the blocks are quantized.
+  {
+    constexpr int kRounds = kMaxQBlocks * 8 / kWarpAttnThreads;
+    float4 v[kRounds];
 #pragma unroll
-  for (int k = 0; k < kCombineSlices; ++k) L += red[k][32];
-  float O0 = 0.0f, O1 = 0.0f;  // two chains, so that the loads of the unrolled loop overlap
-  if (d < D) {
-#pragma unroll 8
-    for (int c = slice; c < chunks; c += 2 * kCombineSlices) {
-      O0 = __fmaf_rn(e[c], __ldg(o_part + (size_t(c) * H + h) * D + d), O0);
-      if (c + kCombineSlices < chunks)
-        O1 = __fmaf_rn(e[c + kCombineSlices], __ldg(o_part + (size_t(c + kCombineSlices) * H + h) * D + d), O1);
+    for (int r = 0; r < kRounds; ++r) {
+      const int blk = r * (kWarpAttnThreads / 8) + (tid >> 3);
+      v[r] = blk < H * nb ? __ldg(reinterpret_cast<const float4 *>(a.q + size_t(blk) * kQK) + (tid & 7))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid == 0)
+      for (int i = 0; i < NS; ++i) issue(i);
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int blk = r * (kWarpAttnThreads / 8) + (tid >> 3), jj = tid & 7;
+      if (r * (kWarpAttnThreads / 8) >= H * nb) break;  // uniform
+      uint16_t sc;
+      uint32_t word;
+      int sum;
+      quantize_block_8lanes(v[r], sc, word, sum);
+      if (blk < H * nb) {
+        uint32_t *rec = qrec + size_t(blk) * kQRecWords2;  // head blk / nb, block blk % nb
+        rec[jj] = word;
+        if (jj == 0) {
+          rec[8] = __float_as_uint(half_bits_to_float(sc));
+          rec[9] = uint32_t(sum);
+        }
+      }
     }
   }
-  red[slice][lane] = O0 + O1;
   __syncthreads();
-  if (slice == 0 && d < D) {
-    float sum = red[0][lane];
+
+  const int j = warp % n_kv, ws = warp / n_kv;
+  // score step: lane = (token tt1, block b1)
+  const int LB = a.lb, b1 = lane % LB, tt1 = lane / LB, tpp1 = 32 / LB;
+  const bool b1ok = b1 < nb;
+  // the lane's q records (block b1 of its G heads): in registers for G <= 4,
+  // else read from shared memory where they are used
+  constexpr bool kQRegs = G <= 4;
+  const uint32_t *qr0 = qrec + (size_t(j * G) * nb + (b1ok ? b1 : 0)) * kQRecWords2;
+  const size_t qstride = size_t(nb) * kQRecWords2;  // next head
+  uint32_t qw[G][8];
+  float qd[G];
+  int qs[G];
+  auto load_q = [&](int g) {
+    const uint32_t *r = qr0 + g * qstride;
+    const uint4 r0 = *reinterpret_cast<const uint4 *>(r), r1 = *reinterpret_cast<const uint4 *>(r + 4);
+    const uint2 r2 = *reinterpret_cast<const uint2 *>(r + 8);
+    qw[g][0] = r0.x; qw[g][1] = r0.y; qw[g][2] = r0.z; qw[g][3] = r0.w;
+    qw[g][4] = r1.x; qw[g][5] = r1.y; qw[g][6] = r1.z; qw[g][7] = r1.w;
+    qd[g] = __uint_as_float(r2.x);
+    qs[g] = int(r2.y);
+  };
+  if (kQRegs)
 #pragma unroll
-    for (int k = 1; k < kCombineSlices; ++k) sum += red[k][lane];
+    for (int g = 0; g < G; ++g) load_q(g);
+  const int kb_off = (j * nb + b1) * BBk;
+  // value step: lane = (token tt2, channel group cg)
+  const int R = D / CPL, tpp2 = 32 / R, cg = lane % R, tt2 = lane / R;
+  const bool p2 = tt2 < tpp2;
+  const int c0 = cg * CPL;
+  const int vb_off = (j * nb + c0 / kQK) * BBv, o2 = c0 % kQK;
+  uint64_t acc[G][NP];
+  float m_run[G], l_run[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_run[g] = -INFINITY;
+    l_run[g] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) acc[g][k] = 0;
+  }
+  float *Pw = P + warp * 32 * G;  // [token][G]: scores, then weights p
+
+  for (int i = 0; i < nt; ++i) {
+    const int st = i % NS;
+    // the decision to go on is the same for every lane of the warp (the
+    // shuffles below need all 32 lanes)
+    bool ok = false;
+    for (uint32_t k = 0; k < a.spin_limit; ++k) {
+      if (mbar_test_wait(&full[st], uint32_t((i / NS) & 1))) {
+        ok = true;
+        break;
+      }
+      if ((k & 63) == 63 && *abort_flag) break;
+      __nanosleep(k < 64 ? 20 : 200);
+    }
+    if (!__all_sync(kFull, ok)) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        atomicOr(a.err, kErrTimeout);
+      }
+      break;
+    }
+    const uint8_t *Ks = ring + size_t(st) * a.stage_bytes, *Vs = Ks + vpart;
+    const int n = min(a.sub, tn - i * a.sub);
+    const int w0 = ws * a.tw, wn = min(a.tw, n - w0);
+    if (wn > 0) {
+      // ---- scores s = scale * sum_b dk * dq * sumi ----
+      const uint8_t *krow = Ks + size_t(w0 + tt1) * a.k_tok + kb_off;  // the lane's block of its token
+      const size_t kstep = size_t(tpp1) * a.k_tok;
+      for (int tb = 0; tb < wn; tb += tpp1, krow += kstep) {
+        const int t = tb + tt1;
+        float part[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) part[g] = 0.0f;
+        if (t < wn && b1ok) {
+          constexpr int NW = KT == kTypeQ4_0 ? 5 : 9;
+          uint32_t w[NW];
+          lds_block_words<NW>(krow, w);
+          const float dk = half_bits_to_float(w[0] & 0xffffu);
+          if (KT == kTypeQ4_0) {
+            uint32_t c[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) c[k] = __funnelshift_rc(w[k], w[k + 1], 16);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              if (!kQRegs) load_q(g);
+              part[g] = __fmul_rn(__fmul_rn(dk, qd[g]), float(sumi_q4_q8(c, qw[g], qs[g])));
+            }
+          } else {
+            uint32_t c[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) c[k] = __funnelshift_rc(w[k], w[k + 1], 16);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              if (!kQRegs) load_q(g);
+              part[g] = __fmul_rn(__fmul_rn(dk, qd[g]), float(sumi_q8_q8(c, qw[g])));
+            }
+          }
+        }
+        for (int off = 1; off < LB; off <<= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g] = __fadd_rn(part[g], __shfl_xor_sync(kFull, part[g], off));
+        if (b1 == 0 && t < wn)
+#pragma unroll
+          for (int g = 0; g < G; ++g) Pw[t * G + g] = __fmul_rn(part[g], a.scale);
+      }
+      __syncwarp();
+      // ---- online softmax over the warp's tokens of the tile (base 2) ----
+      // two heads at a time: lanes 0-15 take head g0, lanes 16-31 head g0 + 1
+      // (token = lane & 15; a warp tile has at most 16 tokens)
+#pragma unroll
+      for (int g0 = 0; g0 < G; g0 += 2) {
+        const int hi = lane >> 4, t = lane & 15;
+        const bool live = t < wn && (G > 1 || hi == 0);
+        const float mo = (G > 1 && hi) ? m_run[G > 1 ? g0 + 1 : 0] : m_run[g0];
+        const float sc = live ? Pw[t * G + (G > 1 ? g0 + hi : 0)] : -INFINITY;
+        float mt = sc;
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, off));
+        const float mn = fmaxf(mo, mt);
+        const float p = live ? ex2(__fsub_rn(sc, mn)) : 0.0f;
+        float ls = p;
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) ls += __shfl_xor_sync(kFull, ls, off);
+        if (live) Pw[t * G + (G > 1 ? g0 + hi : 0)] = p;
+#pragma unroll
+        for (int u = 0; u < (G > 1 ? 2 : 1); ++u) {
+          const int g = g0 + u;
+          const float mg = __shfl_sync(kFull, mn, 16 * u), lg = __shfl_sync(kFull, ls, 16 * u);
+          const float alpha = ex2(__fsub_rn(m_run[g], mg));  // 0 on the first tile (m_run = -inf)
+          l_run[g] = __fmaf_rn(l_run[g], alpha, lg);
+          m_run[g] = mg;
+          if (alpha != 1.0f) {  // the same in every lane
+            const uint64_t a2 = pack2(__float_as_uint(alpha), __float_as_uint(alpha));
+#pragma unroll
+            for (int k = 0; k < NP; ++k) acc[g][k] = fmul2(acc[g][k], a2);
+          }
+        }
+      }
+      __syncwarp();
+      // ---- values: o[g][c] += p[g][t] * dv * v[c] ----
+      if (p2) {
+        const uint8_t *vb = Vs + size_t(w0 + tt2) * a.v_tok + vb_off;  // the lane's block of its token
+        const size_t vstep = size_t(tpp2) * a.v_tok;
+        const float *pw = Pw + tt2 * G;
+#pragma unroll 2
+        for (int t = tt2; t < wn; t += tpp2, vb += vstep, pw += tpp2 * G) {
+          const float dv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(vb));
+          uint64_t vals[NP];
+          v_pairs<VT, CPL>(vb, o2, vals);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const uint32_t pd = __float_as_uint(__fmul_rn(pw[g], dv));
+            const uint64_t pd2 = pack2(pd, pd);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) acc[g][k] = ffma2(pd2, vals[k], acc[g][k]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      // release the stage; the last warp to do so refills it with tile i + NS
+      __threadfence_block();
+      if (atomicAdd(&released[st], 1) == kWarpAttnWarps - 1) {
+        released[st] = 0;
+        __threadfence_block();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads above, bulk writes below
+        issue(i + NS);
+      }
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    // a wait ran out: let every copy still in flight land before leaving
+    // (the last tile issued to a stage completes after the earlier ones)
+    if (tid == 0)
+      for (int k = max(0, *n_issued - NS); k < *n_issued; ++k)
+        if (!mbar_wait_bounded(&full[k % NS], uint32_t((k / NS) & 1), 1u << 26)) break;
+    return;
+  }
+  // ---- merge: warps of a kv head and lanes of a channel group ----
+  // MB[((w * G + g) * tpp2 + tt2) * R * (CPL + 1) + cg * (CPL + 1) + c]: one
+  // padding word per channel group, so that both the writes (lanes differ in
+  // tt2 and cg) and the reads (lanes differ in the channel) hit 32 banks
+  float *MB = reinterpret_cast<float *>(ring);
+  const int RS = R * (CPL + 1);
+  if (p2) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float *dst = MB + ((warp * G + g) * tpp2 + tt2) * RS + cg * (CPL + 1);
+#pragma unroll
+      for (int k = 0; k < NP; ++k) {
+        dst[2 * k] = __uint_as_float(uint32_t(acc[g][k]));
+        dst[2 * k + 1] = __uint_as_float(uint32_t(acc[g][k] >> 32));
+      }
+    }
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      WML[(warp * G + g) * 2] = m_run[g];
+      WML[(warp * G + g) * 2 + 1] = l_run[g];
+    }
+  __syncthreads();
+  const int WS = kWarpAttnWarps / n_kv;
+  for (int h = warp; h < H; h += kWarpAttnWarps) {
+    const int jj = h / G, g = h % G;
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < WS; ++s2) M = fmaxf(M, WML[((jj + s2 * n_kv) * G + g) * 2]);
+    float L = 0.0f;
+    for (int s2 = 0; s2 < WS; ++s2) {
+      const int w = jj + s2 * n_kv;
+      L = __fmaf_rn(ex2(__fsub_rn(WML[(w * G + g) * 2], M)), WML[(w * G + g) * 2 + 1], L);
+    }
+    for (int d = lane; d < D; d += 32) {
+      const int off = (d / CPL) * (CPL + 1) + d % CPL;
+      float O = 0.0f;
+      for (int s2 = 0; s2 < WS; ++s2) {
+        const int w = jj + s2 * n_kv;
+        const float f = ex2(__fsub_rn(WML[(w * G + g) * 2], M));  // 0 for a warp that saw no token
+        const float *src = MB + (w * G + g) * tpp2 * RS + off;
+        float Ow = 0.0f;
+        for (int q2 = 0; q2 < tpp2; ++q2) Ow = __fadd_rn(Ow, src[q2 * RS]);
+        O = __fmaf_rn(f, Ow, O);
+      }
+      a.o_part[(size_t(blockIdx.x) * H + h) * D + d] = O;
+    }
+    if (lane == 0) {
+      a.ml[(size_t(blockIdx.x) * H + h) * 2] = M;
+      a.ml[(size_t(blockIdx.x) * H + h) * 2 + 1] = L;
+    }
+  }
+}
+
+// o[h][d] = sum_c e^(m_c - M) o_c[h][d] / sum_c e^(m_c - M) l_c[h]. One CTA
+// per head and 32 channels, 32 slices of the chunks per channel. A thread
+// loads every (o_c, m_c, l_c) of its slice at once (one round trip per 16
+// chunks) and keeps a running maximum with its own sums rescaled as in the
+// chunks; the slices are then merged the same way. fp32 throughout. Launched
+// as a programmatic dependent of the chunk kernel: it lets the next kernel
+// start at once and waits for the chunk kernel's writes before reading them.
+constexpr int kCombineThreads = 1024;
+constexpr int kCombineSlices = kCombineThreads / 32;
+constexpr int kCombinePer = 16;  // chunks per thread and round
+__global__ void __launch_bounds__(kCombineThreads) k_attn_combine(const float *__restrict__ o_part,
+                                                                  const float *__restrict__ ml,
+                                                                  float *__restrict__ o, int chunks, int H, int D) {
+  __shared__ float sO[kCombineSlices][33];
+  __shared__ float sM[kCombineSlices], sL[kCombineSlices];
+  const int h = blockIdx.x, lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
+  const int d = blockIdx.y * 32 + lane;
+  const bool dv = d < D;
+  pdl_launch_dependents();
+  pdl_wait();
+  float m = -INFINITY, l = 0.0f, O = 0.0f;
+  for (int base = 0; base < chunks; base += kCombineSlices * kCombinePer) {
+    float v[kCombinePer];
+    float2 p[kCombinePer];
+#pragma unroll
+    for (int k = 0; k < kCombinePer; ++k) {
+      const int c = base + slice + kCombineSlices * k;
+      const bool in = c < chunks;
+      v[k] = (in && dv) ? __ldg(o_part + (size_t(c) * H + h) * D + d) : 0.0f;
+      p[k] = in ? __ldg(reinterpret_cast<const float2 *>(ml) + size_t(c) * H + h) : make_float2(-INFINITY, 0.0f);
+    }
+    float mr = m;
+#pragma unroll
+    for (int k = 0; k < kCombinePer; ++k) mr = fmaxf(mr, p[k].x);
+    if (mr == -INFINITY) continue;  // this slice has no chunk in the round
+    const float f = ex2(__fsub_rn(m, mr));  // 0 while m = -inf
+    l = __fmul_rn(l, f);
+    O = __fmul_rn(O, f);
+#pragma unroll
+    for (int k = 0; k < kCombinePer; ++k) {
+      const float e = ex2(__fsub_rn(p[k].x, mr));  // 0 past the last chunk
+      l = __fmaf_rn(e, p[k].y, l);
+      O = __fmaf_rn(e, v[k], O);
+    }
+    m = mr;
+  }
+  sO[slice][lane] = O;
+  if (lane == 0) {
+    sM[slice] = m;
+    sL[slice] = l;
+  }
+  __syncthreads();
+  if (slice == 0 && dv) {
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int k = 0; k < kCombineSlices; ++k) M = fmaxf(M, sM[k]);
+    float sum = 0.0f, L = 0.0f;
+#pragma unroll 8
+    for (int k = 0; k < kCombineSlices; ++k) {
+      const float f = ex2(__fsub_rn(sM[k], M));  // 0 for a slice with no chunk
+      sum = __fmaf_rn(f, sO[k][lane], sum);
+      L = __fmaf_rn(f, sL[k], L);
+    }
     o[size_t(h) * D + d] = __fdiv_rn(sum, L);
   }
 }
@@ -424,6 +870,82 @@ AttnPlan attn_plan(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D
   return p;
 }
 
+// Plan of the warp-per-kv-head kernel; ok = false where it does not apply.
+constexpr int kWarpRingBudget = 96 * 1024;  // two CTAs per SM
+
+struct AttnWPlan {
+  bool ok;
+  int lb, tw, sub, chunk_tokens, chunks, stage_bytes, stages, ring_bytes, k_tok, v_tok;
+  size_t smem;
+};
+
+AttnWPlan attn_wplan(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D) {
+  AttnWPlan p{};
+  const int64_t G = H / n_kv;
+  if (!(n_kv == 1 || n_kv == 2 || n_kv == 4 || n_kv == 8) || D * G > 1024) return p;
+  const int nb = int(D / kQK);
+  p.lb = 1;
+  while (p.lb < nb) p.lb *= 2;
+  p.k_tok = int(n_kv) * nb * (kt == kTypeQ4_0 ? Fmt<kTypeQ4_0>::kBytes : Fmt<kTypeQ8_0>::kBytes);
+  p.v_tok = int(n_kv) * nb * (vt == kTypeQ4_0 ? Fmt<kTypeQ4_0>::kBytes : Fmt<kTypeQ8_0>::kBytes);
+  const int WS = kWarpAttnWarps / int(n_kv);
+  // the largest warp tile (at most 16 tokens) with three or four stages, else two
+  for (int min_stages = 3; min_stages >= 2 && !p.ok; --min_stages)
+    for (int tw = 16; tw >= 1 && !p.ok; tw /= 2) {
+      const int sub = tw * WS;
+      if (sub % 8) break;  // tiles must start on 16-byte boundaries
+      const int stage = sub * (p.k_tok + p.v_tok);
+      for (int ns = 4; ns >= min_stages && !p.ok; --ns)
+        if (ns * stage <= kWarpRingBudget) {
+          p.ok = true;
+          p.tw = tw;
+          p.sub = sub;
+          p.stages = ns;
+          p.stage_bytes = stage;
+        }
+    }
+  if (!p.ok) return p;
+  const int64_t per = (T + kAttnTargetChunks - 1) / kAttnTargetChunks;
+  const int64_t max_ct = std::max<int64_t>(p.sub, kAttnMaxChunkTokens / p.sub * p.sub);
+  p.chunk_tokens = int(std::min<int64_t>(max_ct, (per + p.sub - 1) / p.sub * p.sub));
+  p.chunks = int((T + p.chunk_tokens - 1) / p.chunk_tokens);
+  const int merge = kWarpAttnThreads * (32 + int(G)) * 4;  // G * (32 / G + 1) floats per thread
+  p.ring_bytes = (std::max(p.stages * p.stage_bytes, merge) + 15) / 16 * 16;
+  p.smem = size_t(p.ring_bytes) + size_t(H) * nb * kQRecWords2 * 4 + size_t(kWarpAttnWarps) * 32 * G * 4 +
+           size_t(kWarpAttnWarps) * G * 2 * 4 + (2 + kMaxStages) * 4 + 16 + kMaxStages * 8;
+  return p;
+}
+
+template <int KT, int VT>
+cudaError_t launch_attn_warp(int G, const AttnWArgs &a, int chunks, size_t smem, cudaStream_t stream) {
+  const void *fn = nullptr;
+  switch (G) {
+    case 1: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 1>); break;
+    case 2: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 2>); break;
+    case 4: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 4>); break;
+    case 8: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 8>); break;
+    default: return cudaErrorInvalidValue;
+  }
+  cudaError_t e = ensure_smem(fn, int(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(chunks));
+  cfg.blockDim = dim3(kWarpAttnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  switch (G) {
+    case 1: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 1>, a);
+    case 2: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 2>, a);
+    case 4: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 4>, a);
+    default: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 8>, a);
+  }
+}
+
 template <int KT, int VT>
 cudaError_t launch_attn_kv(int G, const AttnArgs &a, int chunks, size_t smem, cudaStream_t stream) {
   const void *fn = nullptr;
@@ -445,15 +967,20 @@ cudaError_t launch_attn_kv(int G, const AttnArgs &a, int chunks, size_t smem, cu
   return cudaGetLastError();
 }
 
+int attn_chunks(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D) {
+  const AttnWPlan w = attn_wplan(kt, vt, T, H, n_kv, D);
+  return w.ok ? w.chunks : attn_plan(kt, vt, T, H, n_kv, D).chunks;
+}
+
 }  // namespace
 
 size_t attn_workspace_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D) {
-  const AttnPlan p = attn_plan(kt, vt, T, H, n_kv, D);
-  return (size_t(p.chunks) * size_t(H) * size_t(D + 2) * 4 + 255) / 256 * 256;
+  return (size_t(attn_chunks(kt, vt, T, H, n_kv, D)) * size_t(H) * size_t(D + 2) * 4 + 255) / 256 * 256;
 }
 
 size_t attn_smem_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D) {
-  return attn_plan(kt, vt, T, H, n_kv, D).smem;
+  const AttnWPlan w = attn_wplan(kt, vt, T, H, n_kv, D);
+  return w.ok ? w.smem : attn_plan(kt, vt, T, H, n_kv, D).smem;
 }
 
 cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K, const uint8_t *V, float *o,
@@ -462,42 +989,88 @@ cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K,
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
-  const AttnPlan p = attn_plan(kt, vt, T, H, n_kv, D);
-  AttnArgs a{};
-  a.q = q;
-  a.K = K;
-  a.V = V;
-  a.o_part = static_cast<float *>(ws);
-  a.ml = a.o_part + size_t(p.chunks) * H * D;
-  a.scale = scale;
-  a.n_tokens = int(T);
-  a.n_heads = int(H);
-  a.n_kv = int(n_kv);
-  a.D = int(D);
-  a.nb = int(D / kQK);
-  a.k_tok = p.k_tok;
-  a.v_tok = p.v_tok;
-  a.chunk_tokens = p.chunk_tokens;
-  a.sub = p.sub;
-  a.stage_bytes = p.stage_bytes;
-  a.ring_bytes = p.ring_bytes;
-  a.stages = p.stages;
-  a.err = di->err_word;
-  a.spin_limit = spin_limit();
   const int G = int(H / n_kv);
+  // scores are kept in base-2 units, s * scale * log2(e), so that every
+  // exponential is one exp2
+  const float scale2 = float(double(scale) * 1.4426950408889634);
+  const int chunks = attn_chunks(kt, vt, T, H, n_kv, D);
+  float *o_part = static_cast<float *>(ws);
+  float *ml = o_part + size_t(chunks) * H * D;
   cudaError_t e;
-  if (kt == kTypeQ4_0)
-    e = vt == kTypeQ4_0 ? launch_attn_kv<kTypeQ4_0, kTypeQ4_0>(G, a, p.chunks, p.smem, stream)
-                        : launch_attn_kv<kTypeQ4_0, kTypeQ8_0>(G, a, p.chunks, p.smem, stream);
-  else
-    e = vt == kTypeQ4_0 ? launch_attn_kv<kTypeQ8_0, kTypeQ4_0>(G, a, p.chunks, p.smem, stream)
-                        : launch_attn_kv<kTypeQ8_0, kTypeQ8_0>(G, a, p.chunks, p.smem, stream);
+  const AttnWPlan w = attn_wplan(kt, vt, T, H, n_kv, D);
+  if (w.ok) {
+    AttnWArgs a{};
+    a.q = q;
+    a.K = K;
+    a.V = V;
+    a.o_part = o_part;
+    a.ml = ml;
+    a.scale = scale2;
+    a.n_tokens = int(T);
+    a.n_heads = int(H);
+    a.n_kv = int(n_kv);
+    a.D = int(D);
+    a.nb = int(D / kQK);
+    a.k_tok = w.k_tok;
+    a.v_tok = w.v_tok;
+    a.lb = w.lb;
+    a.chunk_tokens = w.chunk_tokens;
+    a.tw = w.tw;
+    a.sub = w.sub;
+    a.stage_bytes = w.stage_bytes;
+    a.stages = w.stages;
+    a.ring_bytes = w.ring_bytes;
+    a.err = di->err_word;
+    a.spin_limit = spin_limit();
+    if (kt == kTypeQ4_0)
+      e = vt == kTypeQ4_0 ? launch_attn_warp<kTypeQ4_0, kTypeQ4_0>(G, a, chunks, w.smem, stream)
+                          : launch_attn_warp<kTypeQ4_0, kTypeQ8_0>(G, a, chunks, w.smem, stream);
+    else
+      e = vt == kTypeQ4_0 ? launch_attn_warp<kTypeQ8_0, kTypeQ4_0>(G, a, chunks, w.smem, stream)
+                          : launch_attn_warp<kTypeQ8_0, kTypeQ8_0>(G, a, chunks, w.smem, stream);
+  } else {
+    const AttnPlan p = attn_plan(kt, vt, T, H, n_kv, D);
+    AttnArgs a{};
+    a.q = q;
+    a.K = K;
+    a.V = V;
+    a.o_part = o_part;
+    a.ml = ml;
+    a.scale = scale2;
+    a.n_tokens = int(T);
+    a.n_heads = int(H);
+    a.n_kv = int(n_kv);
+    a.D = int(D);
+    a.nb = int(D / kQK);
+    a.k_tok = p.k_tok;
+    a.v_tok = p.v_tok;
+    a.chunk_tokens = p.chunk_tokens;
+    a.sub = p.sub;
+    a.stage_bytes = p.stage_bytes;
+    a.ring_bytes = p.ring_bytes;
+    a.stages = p.stages;
+    a.err = di->err_word;
+    a.spin_limit = spin_limit();
+    if (kt == kTypeQ4_0)
+      e = vt == kTypeQ4_0 ? launch_attn_kv<kTypeQ4_0, kTypeQ4_0>(G, a, chunks, p.smem, stream)
+                          : launch_attn_kv<kTypeQ4_0, kTypeQ8_0>(G, a, chunks, p.smem, stream);
+    else
+      e = vt == kTypeQ4_0 ? launch_attn_kv<kTypeQ8_0, kTypeQ4_0>(G, a, chunks, p.smem, stream)
+                          : launch_attn_kv<kTypeQ8_0, kTypeQ8_0>(G, a, chunks, p.smem, stream);
+  }
   if (e != cudaSuccess) return e;
-  const size_t csmem = size_t(p.chunks) * sizeof(float);
-  if ((e = ensure_smem(reinterpret_cast<const void *>(k_attn_combine), int(csmem))) != cudaSuccess) return e;
-  k_attn_combine<<<dim3(unsigned(H), unsigned((D + 31) / 32)), 256, csmem, stream>>>(a.o_part, a.ml, o, p.chunks,
-                                                                                  int(H), int(D));
-  return cudaGetLastError();
+  // the combine starts while the chunk kernel drains (programmatic dependent launch)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(H), unsigned((D + 31) / 32));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attn_combine, static_cast<const float *>(o_part), static_cast<const float *>(ml),
+                            o, chunks, int(H), int(D));
 }
 
 }  // namespace bq

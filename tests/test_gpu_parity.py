@@ -634,7 +634,11 @@ def _attn_case(orc, T, H, NKV, D, kt, vt, seed, centered=False):
 
 @pytest.mark.parametrize("T,H,NKV,D,kt,vt", [
     (1, 4, 2, 64, Q4, Q8), (7, 2, 1, 32, Q8, Q4), (33, 8, 8, 128, Q4, Q8), (1000, 16, 8, 128, Q4, Q8),
-    (300, 32, 4, 64, Q8, Q8), (4097, 16, 4, 128, Q4, Q4), (130, 1, 1, 256, Q8, Q8), (70000, 8, 8, 128, Q4, Q8)])
+    (300, 32, 4, 64, Q8, Q8), (4097, 16, 4, 128, Q4, Q4), (130, 1, 1, 256, Q8, Q8), (70000, 8, 8, 128, Q4, Q8),
+    # head_dim 96: three blocks per row; a kv-head count that is not a power
+    # of two, and eight heads per kv head at head_dim 256, take the
+    # block-wide kernel
+    (333, 4, 4, 96, Q4, Q8), (517, 6, 3, 64, Q4, Q8), (300, 16, 2, 256, Q8, Q4)])
 def test_attn_decode_matches_oracle(bq, orc, dev, T, H, NKV, D, kt, vt):
     q, K, V = _attn_case(orc, T, H, NKV, D, kt, vt, seed=T + 31 * H + D)
     scale = 1.0 / math.sqrt(D)
