@@ -560,7 +560,7 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
                           "hbm_frac_of_measured": round(cache_bytes / (ms2 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                           "config": f"{kv['layers']} layers x {T} tokens x {H} kv heads x {D}, {HQ} query heads, "
                                     "Q4_0 K (mean-centered) + Q8_0 V",
-                          "kernel": "k_attn_chunk + k_attn_combine",
+                          "kernel": "k_attn_warp + k_attn_combine",
                           "l2": "inputs larger than L2 (1.5 GB of cache per step)"}
     del layers, g, g2, qs, outs
     torch.cuda.empty_cache()

@@ -12,16 +12,16 @@
 // (lpnh.cn KV-cache article, §解法).
 //
 // Split over tokens (flash decoding): the tokens are cut into chunks, about
-// two per SM; one CTA takes a chunk and every head, so each token's K and V
-// rows (contiguous over the kv heads in the cache layout) arrive with 1-D bulk
-// copies of 8-32 tokens into a two-stage shared-memory ring.
-//   pass 1: scores s[h][t] of the chunk (thread per (token, head) pair);
-//   softmax: per head, m = max_t s, p = exp(s - m), l = sum_t p;
-//   pass 2: o[h][d] = sum_t p[h][t] * dv * qv; a thread owns one kv head's G
-//           query heads x 16/G channels (16 outputs), with partial sums per
-//           sub-tile of at most 32 tokens;
-//   the chunk writes (m, l, o) per head; k_attn_combine merges the chunks:
-//   o = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c (fp32, two levels).
+// two per SM; one CTA takes a chunk and every head, and each token's K and V
+// rows (contiguous over the kv heads in the cache layout) arrive by 1-D bulk
+// copies into a shared-memory ring. Scores are kept in base-2 units
+// (s * scale * log2 e) so that every exponential is one 2^x. Two chunk kernels:
+//   k_attn_warp (n_kv in {1, 2, 4, 8}, head_dim * G <= 1024): one warp per kv
+//     head with its own online softmax, no block-wide barrier per tile;
+//   k_attn_chunk (every other shape): the block takes all heads together,
+//     scores for the chunk, one softmax per head, then the values.
+// Each chunk writes (m, l, o) per head; k_attn_combine merges the chunks:
+// o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c (fp32).
 #include <algorithm>
 
 #include "bq_device.cuh"
@@ -139,6 +139,13 @@ struct AttnArgs {
   uint32_t spin_limit;
 };
 
+// Block-wide chunk kernel: tiles of `sub` tokens (8-32) arrive in a 2-4 stage
+// ring, all K tiles of the chunk first, then all V tiles.
+//   pass 1: scores s[h][t] of the chunk (thread per (token, head) pair);
+//   softmax: per head, m = max_t s, p = 2^(s - m), l = sum_t p;
+//   pass 2: o[h][d] = sum_t p[h][t] * dv * qv; a thread owns one kv head's G
+//           query heads x 16/G channels (16 outputs), with partial sums per
+//           sub-tile of at most 32 tokens.
 template <int KT, int VT, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a) {
   constexpr int DPU = 16 / G;  // channels per thread unit; G heads x DPU channels = 16 outputs
