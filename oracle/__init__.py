@@ -55,6 +55,10 @@ def _declare(L):
     L.oracle_gemm.argtypes = [i, vp, vp, vp, vp, i64, i64, i64]
     L.oracle_kv_quantize.argtypes = [i, vp, vp, vp, i64, i64, i64]
     L.oracle_attn_decode.argtypes = [i, i, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float]
+    L.oracle_hadamard64.argtypes = [vp, i64]
+    L.oracle_kv_quantize_basis.argtypes = [i, vp, vp, i, i, vp, i64, i64, i64]
+    L.oracle_kv_bias.argtypes = [vp, i, vp, i64, i64, i64]
+    L.oracle_attn_decode_basis.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float]
     for f in ("oracle_quantize_rows", "oracle_dequantize_rows", "oracle_block_dots",
               "oracle_gemv", "oracle_gemm", "oracle_kv_quantize", "oracle_attn_decode"):
         getattr(L, f).restype = i
@@ -154,19 +158,45 @@ def gemm(w_type, w_blocks, X, M, N, K, with_mag=False):
     return (Y, mag) if with_mag else Y
 
 
-def kv_quantize(t, rows, bias, n_tokens, n_kv_heads, head_dim):
-    """rows: (n_tokens, n_kv_heads, head_dim) fp32; bias: (n_kv_heads, head_dim) or None."""
+BASIS_PLAIN, BASIS_HADAMARD64 = 0, 1
+
+
+def kv_quantize(t, rows, bias, n_tokens, n_kv_heads, head_dim, basis=BASIS_PLAIN, bias_basis=None):
+    """rows: (n_tokens, n_kv_heads, head_dim) fp32; bias: (n_kv_heads, head_dim) or None.
+    basis: the cache's basis (rows rotated first when BASIS_HADAMARD64);
+    bias_basis: the basis the bias was calibrated in (default: basis)."""
     rows = _f32(rows)
     b = None if bias is None else _f32(bias)
     out = np.zeros((n_tokens, n_kv_heads, (head_dim // QK) * block_bytes(t)), dtype=np.uint8)
-    rc = lib().oracle_kv_quantize(t, _p(rows), _p(b), _p(out), n_tokens, n_kv_heads, head_dim)
+    rc = lib().oracle_kv_quantize_basis(t, _p(rows), _p(b), basis if bias_basis is None else bias_basis, basis,
+                                        _p(out), n_tokens, n_kv_heads, head_dim)
     if rc == -2:
         raise ValueError("oracle kv_quantize: a bias requires the Q4_0 type")
+    if rc == -4:
+        raise ValueError("oracle kv_quantize: the bias was calibrated in another basis")
     _check(rc, "kv_quantize")
     return out
 
 
-def attn_decode(k_type, v_type, q, K, V, n_tokens, n_heads, n_kv_heads, head_dim, scale, with_mag=False):
+def hadamard64(x):
+    """A copy of x (fp32, size a multiple of 64) with every group of 64
+    consecutive values rotated: H64 x / 8."""
+    y = np.array(x, dtype=np.float32, copy=True, order="C")
+    _check(lib().oracle_hadamard64(_p(y), y.size), "hadamard64")
+    return y
+
+
+def kv_bias(rows, basis, n_tokens, n_kv_heads, head_dim):
+    """Mean-centering bias (n_kv_heads, head_dim) fp32 of the calibration rows
+    (n_tokens, n_kv_heads, head_dim), measured in `basis`."""
+    rows = _f32(rows)
+    out = np.zeros((n_kv_heads, head_dim), dtype=np.float32)
+    _check(lib().oracle_kv_bias(_p(rows), basis, _p(out), n_tokens, n_kv_heads, head_dim), "kv_bias")
+    return out
+
+
+def attn_decode(k_type, v_type, q, K, V, n_tokens, n_heads, n_kv_heads, head_dim, scale, with_mag=False,
+                k_basis=BASIS_PLAIN):
     """Decode attention of one token: q (n_heads, head_dim) fp32; K, V the
     quantized caches (n_tokens, n_kv_heads, head_dim/32 blocks). Returns o
     (n_heads, head_dim), and with_mag also mag (same shape) and the largest
@@ -175,6 +205,7 @@ def attn_decode(k_type, v_type, q, K, V, n_tokens, n_heads, n_kv_heads, head_dim
     o = np.zeros((n_heads, head_dim), dtype=np.float32)
     mag = np.zeros((n_heads, head_dim), dtype=np.float64)
     smax = np.zeros(n_heads, dtype=np.float64)
-    _check(lib().oracle_attn_decode(k_type, v_type, _p(q), _p(K), _p(V), _p(o), _p(mag), _p(smax),
-                                    n_tokens, n_heads, n_kv_heads, head_dim, float(scale)), "attn_decode")
+    _check(lib().oracle_attn_decode_basis(k_type, v_type, k_basis, _p(q), _p(K), _p(V), _p(o), _p(mag),
+                                          _p(smax), n_tokens, n_heads, n_kv_heads, head_dim, float(scale)),
+           "attn_decode")
     return (o, mag, smax) if with_mag else o

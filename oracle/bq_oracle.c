@@ -31,6 +31,11 @@
  *          computes attention in one pass without the intermediate matrix.
  *   [SHIFT] lpnh.cn KV-cache article, §解法 — q·k_i = q·(k_i − k̄) + q·k̄, and
  *          softmax is unchanged by a constant added to a whole row.
+ *   [ROT]  lpnh.cn KV-cache article, §三步上手 (third step) — a quantized K
+ *          cache whose head dimension is a multiple of 64 is Hadamard-rotated;
+ *          the mean-centering bias must be measured in the same basis as the
+ *          cache, the calibration records its basis, and a mismatch fails
+ *          fast instead of degrading quietly.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   R1 scale first, little-endian fp16, then the codes;
@@ -49,12 +54,26 @@
  *      h / (n_heads / n_kv_heads); the scale is the caller's;
  *   R12 q . k_t is the block dot of R5/R6: q quantized to Q8_0 per block of
  *      32 channels, the integer dot with K's codes times dk dq.
+ *   R14 the rotation is orthonormal and block diagonal: every group of 64
+ *      consecutive channels of a head is replaced by H64 x / 8, H64 the
+ *      Sylvester-ordered Walsh-Hadamard matrix, H64[i][j] = (-1)^popcount(i&j)
+ *      (the pages require head_dim % 64 == 0 and name no size or scaling).
+ *      Only K is rotated; q is rotated the same way, so q.k is unchanged.
+ *   R15 the rotated values decide integer codes, so they are computed in the
+ *      kernel's precision: the fast Walsh-Hadamard butterflies in fp32,
+ *      stages of span 1, 2, 4, 8, 16, 32, each pair (a, b) -> (a + b, a - b),
+ *      then the exact scaling by 1/8 (pinned against the fp64 matrix
+ *      product of the definition). The calibrated bias is the fp64 mean over
+ *      the tokens, in token order, of the rotated fp32 rows, stored as fp32.
  *
  * Parity pins (tests/test_oracle_pins.py): block sizes; hand-worked blocks
  * (tests/golden/); fp16 conversion against numpy's binary16; ties; the
  * round-trip bound |x - x_hat| <= d16/2 (1 + 2^-18); brute-force fp64 dot
  * products of dequantized operands; integer block dots against an int64 loop;
- * bias subtraction against numpy subtraction; softmax shift invariance.
+ * bias subtraction against numpy subtraction; softmax shift invariance; the
+ * rotation against the fp64 matrix product of H64's definition, its columns,
+ * norm preservation and self-inverse; calibration against numpy means and
+ * against the rotation of the plain mean (linearity).
  */
 #include "bq_oracle.h"
 
@@ -320,23 +339,55 @@ int oracle_gemm(int w_type, const uint8_t *w_blocks, const float *X, float *Y,
     return 0;
 }
 
-int oracle_kv_quantize(int type, const float *rows, const float *bias, uint8_t *dst,
-                       int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim)
+/* ---- Hadamard rotation: [ROT], R14, R15 ---- */
+
+int oracle_hadamard64(float *x, int64_t n)
+{
+    if (n < 0 || n % 64 != 0)
+        return -1;
+    for (int64_t g = 0; g < n; g += 64) {
+        float *v = x + g;
+        for (int h = 1; h < 64; h *= 2) /* R15: spans 1, 2, 4, 8, 16, 32 in turn */
+            for (int j = 0; j < 64; j++)
+                if ((j & h) == 0) {
+                    float a = v[j], b = v[j + h];
+                    v[j] = a + b;
+                    v[j + h] = a - b;
+                }
+        for (int j = 0; j < 64; j++)
+            v[j] = v[j] * 0.125f; /* R14: orthonormal, 1/sqrt(64); exact */
+    }
+    return 0;
+}
+
+int oracle_kv_quantize_basis(int type, const float *rows, const float *bias, int bias_basis, int basis,
+                             uint8_t *dst, int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim)
 {
     int64_t bb = oracle_block_bytes(type);
     if (bb == 0 || head_dim % QK != 0 || n_tokens < 0 || n_kv_heads < 0 || head_dim < 0)
         return -1;
+    if (basis != ORACLE_BASIS_PLAIN && basis != ORACLE_BASIS_HADAMARD64)
+        return -1;
+    if (basis == ORACLE_BASIS_HADAMARD64 && head_dim % 64 != 0) /* [ROT] head_dim a multiple of 64 */
+        return -1;
     if (bias && type != ORACLE_TYPE_Q4_0) /* [KVMC] mean-centering needs a Q4_0 K cache */
         return -2;
+    if (bias && bias_basis != basis) /* [ROT] the bias must be in the cache's basis: fail fast */
+        return -4;
     int64_t nb = head_dim / QK;
+    float *row = (float *)malloc((size_t)(head_dim > 0 ? head_dim : 1) * sizeof(float));
+    if (!row)
+        return -3;
     float tmp[QK];
     for (int64_t t = 0; t < n_tokens; t++)
         for (int64_t h = 0; h < n_kv_heads; h++) {
-            const float *src = rows + (t * n_kv_heads + h) * head_dim;
+            memcpy(row, rows + (t * n_kv_heads + h) * head_dim, (size_t)head_dim * sizeof(float));
+            if (basis == ORACLE_BASIS_HADAMARD64) /* R14: rotate first, then center */
+                oracle_hadamard64(row, head_dim);
             uint8_t *out = dst + (t * n_kv_heads + h) * nb * bb;
             for (int64_t b = 0; b < nb; b++) {
                 for (int j = 0; j < QK; j++) {
-                    float v = src[b * QK + j];
+                    float v = row[b * QK + j];
                     if (bias) /* [KVMC] K' = K - bias[h][c], one fp32 subtraction */
                         v = v - bias[h * head_dim + b * QK + j];
                     tmp[j] = v;
@@ -344,19 +395,71 @@ int oracle_kv_quantize(int type, const float *rows, const float *bias, uint8_t *
                 quantize_block(type, tmp, out + b * bb);
             }
         }
+    free(row);
+    return 0;
+}
+
+int oracle_kv_quantize(int type, const float *rows, const float *bias, uint8_t *dst,
+                       int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim)
+{
+    return oracle_kv_quantize_basis(type, rows, bias, ORACLE_BASIS_PLAIN, ORACLE_BASIS_PLAIN, dst, n_tokens,
+                                    n_kv_heads, head_dim);
+}
+
+int oracle_kv_bias(const float *rows, int basis, float *bias, int64_t n_tokens, int64_t n_kv_heads,
+                   int64_t head_dim)
+{
+    if (n_tokens < 1 || n_kv_heads < 0 || head_dim < 0 || head_dim % QK != 0)
+        return -1;
+    if (basis != ORACLE_BASIS_PLAIN && basis != ORACLE_BASIS_HADAMARD64)
+        return -1;
+    if (basis == ORACLE_BASIS_HADAMARD64 && head_dim % 64 != 0)
+        return -1;
+    int64_t n = n_kv_heads * head_dim;
+    double *sum = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    float *row = (float *)malloc((size_t)(head_dim > 0 ? head_dim : 1) * sizeof(float));
+    if (!sum || !row) {
+        free(sum); free(row);
+        return -3;
+    }
+    for (int64_t t = 0; t < n_tokens; t++) /* R15: token order, fp64 */
+        for (int64_t h = 0; h < n_kv_heads; h++) {
+            memcpy(row, rows + (t * n_kv_heads + h) * head_dim, (size_t)head_dim * sizeof(float));
+            if (basis == ORACLE_BASIS_HADAMARD64) /* [ROT] measured in the cache's basis */
+                oracle_hadamard64(row, head_dim);
+            for (int64_t c = 0; c < head_dim; c++)
+                sum[h * head_dim + c] += (double)row[c];
+        }
+    for (int64_t i = 0; i < n; i++)
+        bias[i] = (float)(sum[i] / (double)n_tokens);
+    free(sum); free(row);
     return 0;
 }
 
 /* ---- decode attention: R11, R12; [FA], [SHIFT] ---- */
 
-int oracle_attn_decode(int k_type, int v_type, const float *q, const uint8_t *K, const uint8_t *V,
-                       float *o, double *mag, double *smax, int64_t n_tokens, int64_t n_heads,
-                       int64_t n_kv_heads, int64_t head_dim, float scale)
+int oracle_attn_decode_basis(int k_type, int v_type, int k_basis, const float *q, const uint8_t *K,
+                             const uint8_t *V, float *o, double *mag, double *smax, int64_t n_tokens,
+                             int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, float scale)
 {
     int64_t bk = oracle_block_bytes(k_type), bv = oracle_block_bytes(v_type);
     if (bk == 0 || bv == 0 || head_dim <= 0 || head_dim % QK != 0 || n_tokens < 1 || n_kv_heads < 1 ||
         n_heads < n_kv_heads || n_heads % n_kv_heads != 0)
         return -1;
+    if (k_basis != ORACLE_BASIS_PLAIN && (k_basis != ORACLE_BASIS_HADAMARD64 || head_dim % 64 != 0))
+        return -1;
+    if (k_basis == ORACLE_BASIS_HADAMARD64) {
+        /* R14: q in the K cache's basis, (Hq).(Hk) = q.k */
+        float *qr = (float *)malloc((size_t)(n_heads * head_dim) * sizeof(float));
+        if (!qr)
+            return -3;
+        memcpy(qr, q, (size_t)(n_heads * head_dim) * sizeof(float));
+        oracle_hadamard64(qr, n_heads * head_dim);
+        int rc = oracle_attn_decode_basis(k_type, v_type, ORACLE_BASIS_PLAIN, qr, K, V, o, mag, smax, n_tokens,
+                                          n_heads, n_kv_heads, head_dim, scale);
+        free(qr);
+        return rc;
+    }
     int64_t nb = head_dim / QK, group = n_heads / n_kv_heads;
     int64_t bq = oracle_block_bytes(ORACLE_TYPE_Q8_0);
     uint8_t *qq = (uint8_t *)malloc((size_t)(n_heads * nb * bq));
@@ -411,4 +514,12 @@ int oracle_attn_decode(int k_type, int v_type, const float *q, const uint8_t *K,
     }
     free(qq); free(s); free(vrow);
     return 0;
+}
+
+int oracle_attn_decode(int k_type, int v_type, const float *q, const uint8_t *K, const uint8_t *V,
+                       float *o, double *mag, double *smax, int64_t n_tokens, int64_t n_heads,
+                       int64_t n_kv_heads, int64_t head_dim, float scale)
+{
+    return oracle_attn_decode_basis(k_type, v_type, ORACLE_BASIS_PLAIN, q, K, V, o, mag, smax, n_tokens, n_heads,
+                                    n_kv_heads, head_dim, scale);
 }

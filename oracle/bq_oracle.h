@@ -34,6 +34,10 @@ extern "C" {
 #define ORACLE_TYPE_Q4_0 2
 #define ORACLE_TYPE_Q8_0 8
 
+/* bases of a K cache: plain, or Hadamard-rotated per 64 channels */
+#define ORACLE_BASIS_PLAIN 0
+#define ORACLE_BASIS_HADAMARD64 1
+
 /* bytes of one 32-value block of the given type, 0 for an unknown type */
 int64_t oracle_block_bytes(int type);
 
@@ -76,6 +80,31 @@ int oracle_gemm(int w_type, const uint8_t *w_blocks, const float *X, float *Y,
  * dst: n_tokens x n_kv_heads x (head_dim/32) blocks. */
 int oracle_kv_quantize(int type, const float *rows, const float *bias, uint8_t *dst,
                        int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim);
+
+/* In place, every group of 64 consecutive values of x (n % 64 == 0):
+ * x <- H64 x / 8, H64[i][j] = (-1)^popcount(i & j), by fp32 butterflies of
+ * span 1, 2, 4, 8, 16, 32 ((a, b) -> (a + b, a - b)) then * 0.125.
+ * Returns 0, -1 when n % 64 != 0. */
+int oracle_hadamard64(float *x, int64_t n);
+
+/* KV write in a basis: with basis ORACLE_BASIS_HADAMARD64 (head_dim % 64 ==
+ * 0) each head's row is rotated by oracle_hadamard64 first; then the bias
+ * (nullable, Q4_0 only) is subtracted, then the row is quantized. A bias
+ * calibrated in another basis (bias_basis != basis) returns -4. */
+int oracle_kv_quantize_basis(int type, const float *rows, const float *bias, int bias_basis, int basis,
+                             uint8_t *dst, int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim);
+
+/* Bias calibration: bias[h][c] = fp32( sum_t r_t[h][c] / n_tokens ), the sum
+ * in fp64 in token order, r_t the row in `basis` (rotated as above or not).
+ * rows: n_tokens x n_kv_heads x head_dim fp32; bias: n_kv_heads x head_dim. */
+int oracle_kv_bias(const float *rows, int basis, float *bias, int64_t n_tokens, int64_t n_kv_heads,
+                   int64_t head_dim);
+
+/* Decode attention over a K cache in k_basis: with ORACLE_BASIS_HADAMARD64,
+ * q is rotated like K (oracle_hadamard64 per head) before everything else. */
+int oracle_attn_decode_basis(int k_type, int v_type, int k_basis, const float *q, const uint8_t *K,
+                             const uint8_t *V, float *o, double *mag, double *smax, int64_t n_tokens,
+                             int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, float scale);
 
 /* Decode attention of one token over a block-quantized KV cache.
  * q: n_heads x head_dim fp32. K, V: n_tokens x n_kv_heads x (head_dim/32)

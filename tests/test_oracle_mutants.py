@@ -37,6 +37,15 @@ MUTANTS = [
     ("attn_v_decoded_as_k", "oracle_dequantize_rows(v_type, V +", "oracle_dequantize_rows(k_type, V +"),
     ("attn_k_scale_twice", "(double)block_scale(kt + b * bk) * (double)block_scale(qh + b * bq)",
      "(double)block_scale(kt + b * bk) * (double)block_scale(kt + b * bk)"),
+    ("hadamard_scaled_by_1_64", "v[j] = v[j] * 0.125f;", "v[j] = v[j] * 0.015625f;"),
+    ("hadamard_no_minus", "v[j + h] = a - b;", "v[j + h] = a + b;"),
+    ("hadamard_32_point", "for (int h = 1; h < 64; h *= 2)", "for (int h = 1; h < 32; h *= 2)"),
+    ("hadamard_bias_basis_unchecked", "if (bias && bias_basis != basis)", "if (0)"),
+    ("hadamard_bias_measured_plain", "if (basis == ORACLE_BASIS_HADAMARD64) /* [ROT] measured in the cache's basis */",
+     "if (0)"),
+    ("hadamard_q_not_rotated", "oracle_hadamard64(qr, n_heads * head_dim);", "(void)0;"),
+    ("hadamard_kv_write_not_rotated", "if (basis == ORACLE_BASIS_HADAMARD64) /* R14: rotate first, then center */\n                oracle_hadamard64(row, head_dim);",
+     "if (0) oracle_hadamard64(row, head_dim);"),
 ]
 
 

@@ -425,3 +425,164 @@ def test_attn_shift_of_all_scores_leaves_the_output(orc):
     assert s2[0] > s1[0] + 1.0  # the shift is real, and large
     assert np.allclose(o2[0, :D], o[0], rtol=1e-6, atol=1e-7)
     assert np.all(o2[0, D:] == 0.0)
+
+
+# ------------------------------------- Hadamard rotation of K ([ROT], R14) --
+
+def _h64():
+    """H64 of the definition: (-1)^popcount(i & j), fp64, unnormalized."""
+    i = np.arange(64)
+    pc = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+def _rot_exact(x):
+    """fp64 matrix product of the definition, every group of 64 values."""
+    g = np.asarray(x, np.float64).reshape(-1, 64)
+    return (g @ _h64().T / 8.0).reshape(np.shape(x))
+
+
+def _rot_bound(x):
+    """fp32 butterflies: 6 rounded stages, each error at most 2^-24 of the
+    partial sums, which never exceed the group's sum of |x|."""
+    g = np.abs(np.asarray(x, np.float64)).reshape(-1, 64).sum(axis=1, keepdims=True)
+    return np.broadcast_to(7.0 * 2.0 ** -24 * g / 8.0, (g.shape[0], 64)).reshape(np.shape(x))
+
+
+def test_hadamard_columns_are_the_definition(orc):
+    """Each unit vector maps to its column of H64 / 8, exactly (one nonzero
+    input: no rounding), which fixes the order, the signs and the scaling."""
+    H = _h64()
+    for j in range(64):
+        e = np.zeros(64, np.float32)
+        e[j] = 1.0
+        assert np.array_equal(orc.hadamard64(e), (H[:, j] / 8.0).astype(np.float32)), j
+    assert np.array_equal(orc.hadamard64(np.ones(64, np.float32))[:2], np.array([8.0, 0.0], np.float32))
+
+
+def test_hadamard_matches_the_matrix_product(orc):
+    rng = np.random.default_rng(11)
+    for scale in (1.0, 1e-3, 1e4):
+        x = (rng.standard_t(3, size=64 * 40) * scale).astype(np.float32)
+        y = orc.hadamard64(x).astype(np.float64)
+        assert np.all(np.abs(y - _rot_exact(x)) <= _rot_bound(x))
+
+
+def test_hadamard_is_orthonormal_and_its_own_inverse(orc):
+    rng = np.random.default_rng(12)
+    x = rng.normal(size=64 * 16).astype(np.float32)
+    y = orc.hadamard64(x)
+    g = x.astype(np.float64).reshape(-1, 64)
+    assert np.allclose((y.astype(np.float64).reshape(-1, 64) ** 2).sum(1), (g ** 2).sum(1), rtol=1e-6)
+    z = orc.hadamard64(y).astype(np.float64)
+    assert np.all(np.abs(z - x) <= 2 * _rot_bound(x) + 2 * _rot_bound(y))
+
+
+def test_hadamard_groups_are_independent(orc):
+    rng = np.random.default_rng(13)
+    a, b = rng.normal(size=64).astype(np.float32), rng.normal(size=64).astype(np.float32)
+    assert np.array_equal(orc.hadamard64(np.concatenate([a, b])),
+                          np.concatenate([orc.hadamard64(a), orc.hadamard64(b)]))
+    with pytest.raises(ValueError):
+        orc.hadamard64(np.zeros(96, np.float32))
+
+
+def test_rotated_kv_write_of_rotated_codes_is_the_plain_write(orc):
+    """K = H^T C / 8 * 8 with C exactly Q8_0-representable (power-of-two
+    scales): rotating K gives C up to fp32 rounding far below half a code, so
+    the rotated cache of K equals the plain cache of C byte for byte."""
+    rng = np.random.default_rng(14)
+    T, NKV, D = 5, 2, 128
+    codes = rng.integers(-127, 128, size=(T, NKV, D))
+    codes[..., ::32] = 127  # every block's extreme is 127: scale exactly 2^-6
+    C = (codes * 2.0 ** -6).astype(np.float32)
+    K = _rot_exact(C.reshape(-1)).reshape(T, NKV, D).astype(np.float32)  # H is its own inverse (H H / 64 = I)
+    plain = orc.kv_quantize(Q8, C, None, T, NKV, D)
+    rot = orc.kv_quantize(Q8, K, None, T, NKV, D, basis=1)
+    assert np.array_equal(rot, plain)
+    assert not np.array_equal(orc.kv_quantize(Q8, K, None, T, NKV, D), plain)
+
+
+def test_rotated_kv_write_round_trip_in_the_rotated_basis(orc):
+    rng = np.random.default_rng(15)
+    T, NKV, D = 40, 2, 64
+    K = (rng.normal(size=(T, NKV, D)) * rng.uniform(0.1, 3.0, size=(1, 1, D))).astype(np.float32)
+    bias = orc.kv_bias(K, 1, T, NKV, D)
+    cache = orc.kv_quantize(Q4, K, bias, T, NKV, D, basis=1)
+    deq = orc.dequantize_rows(Q4, cache.reshape(T * NKV, -1), D).astype(np.float64).reshape(T, NKV, D)
+    target = _rot_exact(K.reshape(-1)).reshape(T, NKV, D) - bias.astype(np.float64)[None]
+    d16 = cache.reshape(-1, 18)[:, :2].copy().view(np.float16).astype(np.float64).reshape(T, NKV, D // 32)
+    tol = np.repeat(d16, 32, axis=2) / 2 * (1 + 2.0 ** -18) + _rot_bound(K.reshape(-1)).reshape(T, NKV, D) + 1e-6
+    assert np.all(np.abs(deq - target) <= tol)
+
+
+def test_bias_from_another_basis_is_rejected(orc):
+    T, NKV, D = 3, 1, 64
+    K = np.ones((T, NKV, D), np.float32)
+    with pytest.raises(ValueError):
+        orc.kv_quantize(Q4, K, np.zeros((NKV, D), np.float32), T, NKV, D, basis=1, bias_basis=0)
+    with pytest.raises(ValueError):
+        orc.kv_quantize(Q4, K, np.zeros((NKV, D), np.float32), T, NKV, D, basis=0, bias_basis=1)
+    with pytest.raises(ValueError):
+        orc.kv_quantize(Q4, np.ones((T, NKV, 96), np.float32), None, T, NKV, 96, basis=1)
+
+
+def test_plain_bias_is_the_channel_mean(orc):
+    rng = np.random.default_rng(16)
+    T, NKV, D = 300, 3, 96
+    K = (rng.normal(size=(T, NKV, D)) + rng.uniform(-2, 2, size=(NKV, D))).astype(np.float32)
+    b = orc.kv_bias(K, 0, T, NKV, D)
+    ref = K.astype(np.float64).mean(axis=0).astype(np.float32)
+    assert np.all(np.abs(b.view(np.int32) - ref.view(np.int32)) <= 1)  # within one fp32 ulp
+
+
+def test_rotated_bias_is_the_rotation_of_the_mean(orc):
+    """Linearity: the mean of the rotated rows is the rotated mean."""
+    rng = np.random.default_rng(17)
+    T, NKV, D = 200, 2, 128
+    K = (rng.normal(size=(T, NKV, D)) + rng.uniform(-2, 2, size=(NKV, D))).astype(np.float32)
+    b = orc.kv_bias(K, 1, T, NKV, D).astype(np.float64)
+    ref = _rot_exact(K.astype(np.float64).mean(axis=0).reshape(-1)).reshape(NKV, D)
+    bound = _rot_bound(np.abs(K).max(axis=0).reshape(-1)).reshape(NKV, D) + 2 * 2.0 ** -24 * np.abs(ref) + 1e-7
+    assert np.all(np.abs(b - ref) <= bound)
+
+
+def test_rotation_spreads_outlier_channels(orc):
+    """Expected, not proved (parity unpinned magnitude): with a few outlier
+    channels per head, Q4_0 after rotation loses less of K, measured back in
+    the original basis, than Q4_0 of the raw rows."""
+    rng = np.random.default_rng(18)
+    T, NKV, D = 256, 2, 128
+    K = rng.normal(size=(T, NKV, D)).astype(np.float32)
+    K[..., [3, 40, 77, 101]] *= 25.0
+    plain = orc.dequantize_rows(Q4, orc.kv_quantize(Q4, K, None, T, NKV, D).reshape(T * NKV, -1), D)
+    rot = orc.dequantize_rows(Q4, orc.kv_quantize(Q4, K, None, T, NKV, D, basis=1).reshape(T * NKV, -1), D)
+    back = _rot_exact(rot.reshape(-1)).reshape(T * NKV, D)  # H / 8 is its own inverse
+    err_plain = np.mean((plain - K.reshape(T * NKV, D)) ** 2)
+    err_rot = np.mean((back - K.reshape(T * NKV, D)) ** 2)
+    assert err_rot < 0.5 * err_plain
+
+
+def test_attn_over_a_rotated_cache_rotates_q(orc):
+    """(Hq).(Hk) = q.k: over a rotated Q8_0 cache the output stays close to
+    exact fp64 attention of the unquantized rows (quantization noise only),
+    and using q unrotated is far off."""
+    rng = np.random.default_rng(19)
+    T, NH, NKV, D = 120, 4, 2, 128
+    K = rng.normal(size=(T, NKV, D)).astype(np.float32)
+    V = rng.normal(size=(T, NKV, D)).astype(np.float32)
+    q = rng.normal(size=(NH, D)).astype(np.float32)
+    scale = 1 / math.sqrt(D)
+    Kc = orc.kv_quantize(Q8, K, None, T, NKV, D, basis=1)
+    Vc = orc.kv_quantize(Q8, V, None, T, NKV, D)
+    vhat = orc.dequantize_rows(Q8, Vc.reshape(T * NKV, -1), D).reshape(T, NKV, D).astype(np.float64)
+    exact = np.zeros((NH, D))
+    for h in range(NH):
+        s = scale * (K[:, h // 2].astype(np.float64) @ q[h].astype(np.float64))
+        w = np.exp(s - s.max())
+        exact[h] = (w / w.sum()) @ vhat[:, h // 2]
+    o = orc.attn_decode(Q8, Q8, q, Kc, Vc, T, NH, NKV, D, scale, k_basis=1)
+    o_wrong = orc.attn_decode(Q8, Q8, q, Kc, Vc, T, NH, NKV, D, scale)
+    err = np.abs(o - exact).max()
+    assert err < 0.02
+    assert np.abs(o_wrong - exact).max() > 10 * err
