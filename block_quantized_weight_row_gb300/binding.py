@@ -19,7 +19,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_NAME = "libbq.so"
 
 _STATUS = {0: "BQ_OK", -1: "BQ_ERR_INVALID_ARG", -2: "BQ_ERR_SHAPE", -3: "BQ_ERR_UNSUPPORTED",
-           -4: "BQ_ERR_ALIGN", -5: "BQ_ERR_CUDA", -6: "BQ_ERR_TIMEOUT", -7: "BQ_ERR_WORKSPACE"}
+           -4: "BQ_ERR_ALIGN", -5: "BQ_ERR_CUDA", -6: "BQ_ERR_TIMEOUT", -7: "BQ_ERR_WORKSPACE",
+           -8: "BQ_ERR_BASIS"}
+BASIS_PLAIN, BASIS_HADAMARD64 = 0, 1
 
 
 class BQError(RuntimeError):
@@ -56,6 +58,9 @@ def lib():
                               ctypes.POINTER(vp), ctypes.POINTER(i64)], i),
         "bq_gemv_sequence_workspace_size": ([], sz),
         "bq_attn_decode": ([i, i, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float], i),
+        "bq_attn_decode_basis": ([i, i, i, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float], i),
+        "bq_kv_quantize_basis": ([i, vp, vp, i, i, vp, i64, i64, i64], i),
+        "bq_kv_bias": ([vp, i, vp, i64, i64, i64], i),
         "bq_attn_workspace_size": ([i, i, i64, i64, i64, i64], sz),
         "bq_gemm": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_kv_quantize": ([i, vp, vp, vp, i64, i64, i64], i),
@@ -226,9 +231,11 @@ def gemv_sequence(t: int, groups):
 
 
 def attn_decode(k_type: int, v_type: int, q: torch.Tensor, K_cache: torch.Tensor, V_cache: torch.Tensor,
-                n_kv_heads: int, scale: float, out: torch.Tensor | None = None) -> torch.Tensor:
+                n_kv_heads: int, scale: float, out: torch.Tensor | None = None,
+                k_basis: int = BASIS_PLAIN) -> torch.Tensor:
     """o (n_heads, head_dim) = attention of q (n_heads, head_dim) over the
-    quantized caches (n_tokens, n_kv_heads, head_dim/32 blocks as bytes)."""
+    quantized caches (n_tokens, n_kv_heads, head_dim/32 blocks as bytes);
+    k_basis: the basis the K cache was written in."""
     _cuda(q, "q")
     _cuda(K_cache, "K_cache")
     _cuda(V_cache, "V_cache")
@@ -238,8 +245,8 @@ def attn_decode(k_type: int, v_type: int, q: torch.Tensor, K_cache: torch.Tensor
         out = torch.empty((H, D), dtype=torch.float32, device=q.device)
     L = _prep(q.device)
     _workspace(q.device, int(L.bq_attn_workspace_size(k_type, v_type, T, H, n_kv_heads, D)))
-    _check(L.bq_attn_decode(k_type, v_type, _ptr(q), _ptr(K_cache), _ptr(V_cache), _ptr(out), T, H, n_kv_heads, D,
-                            float(scale)), "bq_attn_decode")
+    _check(L.bq_attn_decode_basis(k_type, v_type, k_basis, _ptr(q), _ptr(K_cache), _ptr(V_cache), _ptr(out), T, H,
+                                  n_kv_heads, D, float(scale)), "bq_attn_decode_basis")
     return out
 
 
@@ -257,8 +264,11 @@ def gemm(t: int, w_blocks: torch.Tensor, X: torch.Tensor, M: int, N: int, K: int
 
 
 def kv_quantize(t: int, rows: torch.Tensor, bias: torch.Tensor | None,
-                out: torch.Tensor | None = None) -> torch.Tensor:
-    """rows: (n_tokens, n_kv_heads, head_dim) fp32; bias: (n_kv_heads, head_dim) or None."""
+                out: torch.Tensor | None = None, basis: int = BASIS_PLAIN,
+                bias_basis: int | None = None) -> torch.Tensor:
+    """rows: (n_tokens, n_kv_heads, head_dim) fp32; bias: (n_kv_heads, head_dim) or None.
+    basis: the cache's basis; bias_basis: the basis the bias was calibrated in
+    (default: the cache's)."""
     _cuda(rows, "rows")
     if bias is not None:
         _cuda(bias, "bias")
@@ -266,7 +276,20 @@ def kv_quantize(t: int, rows: torch.Tensor, bias: torch.Tensor | None,
     if out is None:
         out = torch.empty((T, H, (D // QK) * max(block_bytes(t), 1)), dtype=torch.uint8, device=rows.device)
     L = _prep(rows.device)
-    _check(L.bq_kv_quantize(t, _ptr(rows), _ptr(bias), _ptr(out), T, H, D), "bq_kv_quantize")
+    _check(L.bq_kv_quantize_basis(t, _ptr(rows), _ptr(bias), basis if bias_basis is None else bias_basis, basis,
+                                  _ptr(out), T, H, D), "bq_kv_quantize_basis")
+    return out
+
+
+def kv_bias(rows: torch.Tensor, basis: int = BASIS_PLAIN, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Mean-centering bias (n_kv_heads, head_dim) fp32 of calibration rows
+    (n_tokens, n_kv_heads, head_dim), measured in `basis`."""
+    _cuda(rows, "rows")
+    T, H, D = rows.shape
+    if out is None:
+        out = torch.empty((H, D), dtype=torch.float32, device=rows.device)
+    L = _prep(rows.device)
+    _check(L.bq_kv_bias(_ptr(rows), basis, _ptr(out), T, H, D), "bq_kv_bias")
     return out
 
 

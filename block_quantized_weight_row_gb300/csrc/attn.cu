@@ -32,6 +32,37 @@ namespace {
 
 constexpr int kAttnThreads = 256;
 
+// q in the basis of a Hadamard-rotated K cache (lpnh.cn KV-cache article,
+// §三步上手, third step): every 64 channels of a head become H64 q / 8, so
+// (Hq).(Hk) = q.k. Lanes hold 4 channels each, 8 lanes per block of 32, two
+// blocks (lanes 16g .. 16g + 15) per group of 64: element 32 * ((lane >> 3) & 1)
+// + 4 * (lane & 7) + c. Butterflies (a, b) -> (a + b, a - b) of span 1 and 2
+// inside the lane, 4, 8, 16, 32 with lane ^ 1, 2, 4, 8, then * 0.125: the same
+// steps, in the same order, as the K cache's rotation.
+__device__ __forceinline__ float4 hadamard64_8lanes(float4 v, int lane) {
+  float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int h = 1; h < 4; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = __fadd_rn(a, b);
+        x[i + h] = __fsub_rn(a, b);
+      }
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float p = __shfl_xor_sync(kFull, x[i], m);
+      x[i] = up ? __fsub_rn(p, x[i]) : __fadd_rn(x[i], p);
+    }
+  }
+  return make_float4(__fmul_rn(x[0], 0.125f), __fmul_rn(x[1], 0.125f), __fmul_rn(x[2], 0.125f),
+                     __fmul_rn(x[3], 0.125f));
+}
+
 // 2^x (hardware approximation, relative error about 2^-22; 0 for -inf)
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -135,6 +166,7 @@ struct AttnArgs {
   int stage_bytes;   // sub * max(k_tok, v_tok), a multiple of 16
   int ring_bytes;    // >= the stages and >= the split reduction, a multiple of 16
   int stages;        // ring stages, 2..4
+  int k_rot;         // K cache Hadamard-rotated: rotate q alike
   unsigned *err;
   uint32_t spin_limit;
 };
@@ -176,6 +208,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
     const int blk = base + (tid >> 3), j = tid & 7;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (blk < H * nb) v = __ldg(reinterpret_cast<const float4 *>(a.q + size_t(blk) * kQK) + j);
+    if (a.k_rot) v = hadamard64_8lanes(v, lane);  // uniform
     uint16_t sc;
     uint32_t word;
     int sum;
@@ -387,6 +420,7 @@ struct AttnWArgs {
   int stage_bytes;   // sub * (k_tok + v_tok): K rows, then V rows
   int stages;        // 2..4
   int ring_bytes;    // >= stages * stage_bytes and >= the merge buffer
+  int k_rot;         // K cache Hadamard-rotated: rotate q alike
   unsigned *err;
   uint32_t spin_limit;
 };
@@ -524,6 +558,7 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
       uint16_t sc;
       uint32_t word;
       int sum;
+      if (a.k_rot) v[r] = hadamard64_8lanes(v[r], lane);  // uniform
       quantize_block_8lanes(v[r], sc, word, sum);
       if (blk < H * nb) {
         uint32_t *rec = qrec + size_t(blk) * kQRecWords2;  // head blk / nb, block blk % nb
@@ -992,7 +1027,7 @@ size_t attn_smem_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64
 
 cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K, const uint8_t *V, float *o,
                                int64_t T, int64_t H, int64_t n_kv, int64_t D, float scale, void *ws,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool k_rot) {
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
@@ -1027,6 +1062,7 @@ cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K,
     a.stage_bytes = w.stage_bytes;
     a.stages = w.stages;
     a.ring_bytes = w.ring_bytes;
+    a.k_rot = k_rot ? 1 : 0;
     a.err = di->err_word;
     a.spin_limit = spin_limit();
     if (kt == kTypeQ4_0)
@@ -1056,6 +1092,7 @@ cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K,
     a.stage_bytes = p.stage_bytes;
     a.ring_bytes = p.ring_bytes;
     a.stages = p.stages;
+    a.k_rot = k_rot ? 1 : 0;
     a.err = di->err_word;
     a.spin_limit = spin_limit();
     if (kt == kTypeQ4_0)

@@ -406,8 +406,18 @@ size_t bq_attn_workspace_size(int k_type, int v_type, int64_t n_tokens, int64_t 
 
 int bq_attn_decode(int k_type, int v_type, const float *q, const void *K, const void *V, float *o, int64_t n_tokens,
                    int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, float scale) {
+  return bq_attn_decode_basis(k_type, v_type, BQ_BASIS_PLAIN, q, K, V, o, n_tokens, n_heads, n_kv_heads, head_dim,
+                              scale);
+}
+
+int bq_attn_decode_basis(int k_type, int v_type, int k_basis, const float *q, const void *K, const void *V, float *o,
+                         int64_t n_tokens, int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, float scale) {
   const int st = attn_check(k_type, v_type, n_tokens, n_heads, n_kv_heads, head_dim, "bq_attn_decode");
   if (st != BQ_OK) return st;
+  if (k_basis != BQ_BASIS_PLAIN && k_basis != BQ_BASIS_HADAMARD64)
+    return fail(BQ_ERR_UNSUPPORTED, "bq_attn_decode: unknown basis %d", k_basis);
+  if (k_basis == BQ_BASIS_HADAMARD64 && head_dim % 64)
+    return fail(BQ_ERR_SHAPE, "bq_attn_decode: a rotated K cache needs head_dim %% 64 == 0");
   if (!q || !K || !V || !o) return fail(BQ_ERR_INVALID_ARG, "bq_attn_decode: null pointer");
   if (!aligned(q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(o, 4))
     return fail(BQ_ERR_ALIGN, "bq_attn_decode: q, K and V must be 16-byte aligned, o 4-byte aligned");
@@ -424,7 +434,8 @@ int bq_attn_decode(int k_type, int v_type, const float *q, const void *K, const 
       overlap(t_ws, need, V, vbytes))
     return fail(BQ_ERR_INVALID_ARG, "bq_attn_decode: the workspace overlaps an argument");
   cudaError_t e = launch_attn_decode(k_type, v_type, q, static_cast<const uint8_t *>(K), static_cast<const uint8_t *>(V),
-                                     o, n_tokens, n_heads, n_kv_heads, head_dim, scale, t_ws, t_stream);
+                                     o, n_tokens, n_heads, n_kv_heads, head_dim, scale, t_ws, t_stream,
+                                     k_basis == BQ_BASIS_HADAMARD64);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_attn_decode launch");
 }
 
@@ -459,13 +470,26 @@ int bq_gemm(int type, const void *W, const float *X, float *Y, int64_t M, int64_
 
 int bq_kv_quantize(int type, const float *rows, const float *bias, void *dst, int64_t n_tokens,
                    int64_t n_kv_heads, int64_t head_dim) {
+  return bq_kv_quantize_basis(type, rows, bias, BQ_BASIS_PLAIN, BQ_BASIS_PLAIN, dst, n_tokens, n_kv_heads, head_dim);
+}
+
+int bq_kv_quantize_basis(int type, const float *rows, const float *bias, int bias_basis, int basis, void *dst,
+                         int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim) {
   const int bb = block_bytes(type);
   if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: unknown type %d", type);
+  if (basis != BQ_BASIS_PLAIN && basis != BQ_BASIS_HADAMARD64)
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: unknown basis %d", basis);
   if (bias && type != BQ_TYPE_Q4_0)
     return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: a mean-centering bias requires the Q4_0 type");
+  if (bias && bias_basis != basis)
+    return fail(BQ_ERR_BASIS, "bq_kv_quantize: the bias was calibrated in basis %d, the cache is in basis %d",
+                bias_basis, basis);
   if (!sizes_ok(n_tokens, n_kv_heads) || !sizes_ok(n_tokens * n_kv_heads, head_dim))
     return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: bad sizes");
   if (head_dim % kQK) return fail(BQ_ERR_SHAPE, "bq_kv_quantize: head_dim %lld is not a multiple of 32", (long long)head_dim);
+  if (basis == BQ_BASIS_HADAMARD64 && head_dim % 64)
+    return fail(BQ_ERR_SHAPE, "bq_kv_quantize: the rotated basis needs head_dim %% 64 == 0, got %lld",
+                (long long)head_dim);
   const int64_t n_blocks = n_tokens * n_kv_heads * (head_dim / kQK);
   if (n_blocks == 0) return ok();
   if (!rows || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: null pointer");
@@ -475,8 +499,26 @@ int bq_kv_quantize(int type, const float *rows, const float *bias, void *dst, in
       overlap(bias, size_t(n_kv_heads * head_dim) * 4, dst, size_t(n_blocks) * bb))
     return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: dst overlaps an input");
   cudaError_t e = launch_quantize_rows(type, rows, static_cast<uint8_t *>(dst), n_blocks, head_dim / kQK, bias,
-                                       n_kv_heads * (head_dim / kQK), t_stream);
+                                       n_kv_heads * (head_dim / kQK), t_stream, basis == BQ_BASIS_HADAMARD64);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_kv_quantize launch");
+}
+
+int bq_kv_bias(const float *rows, int basis, float *bias, int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim) {
+  if (basis != BQ_BASIS_PLAIN && basis != BQ_BASIS_HADAMARD64)
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_bias: unknown basis %d", basis);
+  if (!sizes_ok(n_tokens, n_kv_heads) || !sizes_ok(n_tokens * n_kv_heads, head_dim) || n_tokens < 1)
+    return fail(BQ_ERR_INVALID_ARG, "bq_kv_bias: bad sizes (n_tokens must be at least 1)");
+  if (head_dim % kQK) return fail(BQ_ERR_SHAPE, "bq_kv_bias: head_dim %lld is not a multiple of 32", (long long)head_dim);
+  if (basis == BQ_BASIS_HADAMARD64 && head_dim % 64)
+    return fail(BQ_ERR_SHAPE, "bq_kv_bias: the rotated basis needs head_dim %% 64 == 0");
+  const int64_t row_len = n_kv_heads * head_dim;
+  if (row_len == 0) return ok();
+  if (!rows || !bias) return fail(BQ_ERR_INVALID_ARG, "bq_kv_bias: null pointer");
+  if (!aligned(rows, 16) || !aligned(bias, 4)) return fail(BQ_ERR_ALIGN, "bq_kv_bias: rows 16-byte, bias 4-byte aligned");
+  if (overlap(bias, size_t(row_len) * 4, rows, size_t(n_tokens) * size_t(row_len) * 4))
+    return fail(BQ_ERR_INVALID_ARG, "bq_kv_bias: bias overlaps the rows");
+  cudaError_t e = launch_kv_bias(rows, bias, n_tokens, row_len, basis == BQ_BASIS_HADAMARD64, t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_kv_bias launch");
 }
 
 int bq_block_dots(int type, const void *W, const void *xq, int32_t *out, int64_t M, int64_t K) {

@@ -44,9 +44,15 @@ int report_error(int status, const char *fmt, ...);
 int report_ok();
 
 // Launchers; each returns the launch status. Sizes were validated by the ABI layer.
+// rotate: each group of 64 values (blocks 2m, 2m+1) is Hadamard-rotated
+// before the bias is subtracted; n_blocks must then be even.
 cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64_t n_blocks,
                                  int64_t blocks_per_row, const float *bias, int64_t bias_period,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, bool rotate = false);
+// bias[c] = fp32(sum_t rows[t][c] / n_tokens) (fp64 sum in token order), in the
+// Hadamard basis when rotate (row_len % 64 == 0).
+cudaError_t launch_kv_bias(const float *rows, float *bias, int64_t n_tokens, int64_t row_len, bool rotate,
+                           cudaStream_t stream);
 cudaError_t launch_dequantize_rows(int type, const uint8_t *blocks, float *dst, int64_t n_blocks,
                                    cudaStream_t stream);
 // n matrices (n <= BQ_GEMV_MAX_MATS) sharing one input x; matrix i has M[i] rows.
@@ -70,7 +76,7 @@ size_t attn_workspace_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, 
 size_t attn_smem_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D);
 cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K, const uint8_t *V, float *o,
                                int64_t T, int64_t H, int64_t n_kv, int64_t D, float scale, void *ws,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool k_rot = false);
 cudaError_t launch_gemm(int type, const uint8_t *W, const uint8_t *Xq, float *Y, int64_t M,
                         int64_t N, int64_t K, cudaStream_t stream);
 // Prefill GEMM on the tcgen05 tensor cores (K a multiple of 256): quantizes X

@@ -23,6 +23,14 @@
 //     is staged once per CTA in the same swizzled layout;
 //   - the tile's output (576 B Q4_0 / 1088 B Q8_0) is assembled in shared
 //     memory and leaves as 16-byte stores.
+// Hadamard-rotated K (lpnh.cn KV-cache article, §三步上手, third step: a
+// quantized K cache with head_dim a multiple of 64 is rotated, and the bias
+// must be measured in the same basis): every 64 channels of a head become
+// H64 x / 8 before the bias is subtracted. Blocks 2m and 2m+1 of a tile are
+// one group of 64, held by lanes 2m and 2m+1: the butterflies of span 1-16
+// run inside a lane, span 32 across the lane pair, then the exact 1/8.
+// The bias calibration (k_kv_bias) sums each channel over the tokens in fp64
+// in token order, in either basis.
 #include "bq_device.cuh"
 #include "bq_internal.h"
 
@@ -36,7 +44,28 @@ constexpr int kMaxSmemBiasBlocks = 128;  // 16 KB of bias staged per CTA
 // byte offset of 16-byte chunk c of block b in a swizzled tile
 __device__ __forceinline__ int swz(int b, int c) { return b * 128 + ((c ^ (b & 7)) << 4); }
 
-template <int TYPE, bool BIAS>
+// 32 values of one block (elements 32 * (lane & 1) + i of a 64-group) ->
+// H64 x / 8: butterflies (a, b) -> (a + b, a - b) of span 1, 2, 4, 8, 16 in
+// the lane, span 32 with lane ^ 1, then * 0.125. Every lane of the warp takes part.
+__device__ __forceinline__ void hadamard64_lane_pair(float (&v)[32], int lane) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+  const bool lo = (lane & 1) == 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float p = __shfl_xor_sync(kFull, v[i], 1);
+    v[i] = __fmul_rn(lo ? __fadd_rn(v[i], p) : __fsub_rn(p, v[i]), 0.125f);
+  }
+}
+
+template <int TYPE, bool BIAS, bool ROT>
 __global__ void __launch_bounds__(kQuantThreads, 2)
     k_quantize_rows(const float *__restrict__ src, uint8_t *__restrict__ dst, int64_t n_blocks,
                     const float *__restrict__ bias, int64_t bias_period) {
@@ -88,6 +117,13 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
       v[4 * c + 1] = f.y;
       v[4 * c + 2] = f.z;
       v[4 * c + 3] = f.w;
+    }
+    if (ROT) {
+      // rotate, and keep the rotated block in the tile for the exact path
+      hadamard64_lane_pair(v, lane);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4 *>(it + swz(lane, c)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     }
     const int64_t b = tile * 32 + lane;
     if (BIAS && b < n_blocks) {
@@ -183,7 +219,7 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <int TYPE, bool BIAS>
+template <int TYPE, bool BIAS, bool ROT>
 cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
                      cudaStream_t stream) {
   cudaError_t err;
@@ -192,22 +228,98 @@ cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const flo
   const int64_t tiles = (n_blocks + 31) / 32;
   const int64_t ctas = (tiles + kQuantWarps - 1) / kQuantWarps;
   const int64_t grid = min(ctas, int64_t(di->sm_count) * 2);  // persistent: 2 resident CTAs per SM
-  k_quantize_rows<TYPE, BIAS><<<unsigned(grid), kQuantThreads, 0, stream>>>(src, dst, n_blocks, bias,
-                                                                           bias_period);
+  k_quantize_rows<TYPE, BIAS, ROT><<<unsigned(grid), kQuantThreads, 0, stream>>>(src, dst, n_blocks, bias,
+                                                                                bias_period);
   return cudaGetLastError();
+}
+
+template <bool ROT>
+cudaError_t launch_q_typed(int type, const float *src, uint8_t *dst, int64_t n_blocks, const float *bias,
+                           int64_t bias_period, cudaStream_t stream) {
+  if (type == kTypeQ4_0)
+    return bias ? launch_q<kTypeQ4_0, true, ROT>(src, dst, n_blocks, bias, bias_period, stream)
+                : launch_q<kTypeQ4_0, false, ROT>(src, dst, n_blocks, nullptr, 1, stream);
+  // a bias with Q8_0 is rejected by the ABI layer
+  return launch_q<kTypeQ8_0, false, ROT>(src, dst, n_blocks, nullptr, 1, stream);
+}
+
+// bias[h][c] = fp32(sum_t r_t[h][c] / n_tokens), the sum in fp64 in token
+// order; r_t the token's row, rotated per 64 channels when ROT. One warp per
+// group of 64 channels (lane: channels lane and lane + 32) when ROT, else one
+// thread per channel. The loads of the next tokens are issued ahead.
+template <bool ROT>
+__global__ void __launch_bounds__(128) k_kv_bias(const float *__restrict__ rows, float *__restrict__ bias,
+                                                 int64_t n_tokens, int64_t row_len) {
+  constexpr int kAhead = 8;
+  if (ROT) {
+    const int64_t g = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // group of 64
+    const int lane = threadIdx.x & 31;
+    if (g * 64 >= row_len) return;  // uniform per warp
+    const float *p = rows + g * 64 + lane;
+    double s0 = 0.0, s1 = 0.0;
+    for (int64_t t0 = 0; t0 < n_tokens; t0 += kAhead) {
+      float x0[kAhead], x1[kAhead];
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k) {
+        const bool in = t0 + k < n_tokens;
+        x0[k] = in ? __ldg(p + (t0 + k) * row_len) : 0.0f;
+        x1[k] = in ? __ldg(p + (t0 + k) * row_len + 32) : 0.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k) {
+        float a0 = x0[k], a1 = x1[k];
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+          const float p0 = __shfl_xor_sync(kFull, a0, h), p1 = __shfl_xor_sync(kFull, a1, h);
+          const bool up = (lane & h) != 0;
+          a0 = up ? __fsub_rn(p0, a0) : __fadd_rn(a0, p0);
+          a1 = up ? __fsub_rn(p1, a1) : __fadd_rn(a1, p1);
+        }
+        const float b0 = __fmul_rn(__fadd_rn(a0, a1), 0.125f), b1 = __fmul_rn(__fsub_rn(a0, a1), 0.125f);
+        if (t0 + k < n_tokens) {
+          s0 = __dadd_rn(s0, double(b0));
+          s1 = __dadd_rn(s1, double(b1));
+        }
+      }
+    }
+    bias[g * 64 + lane] = float(__ddiv_rn(s0, double(n_tokens)));
+    bias[g * 64 + lane + 32] = float(__ddiv_rn(s1, double(n_tokens)));
+  } else {
+    const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= row_len) return;
+    double s = 0.0;
+    for (int64_t t0 = 0; t0 < n_tokens; t0 += kAhead) {
+      float x[kAhead];
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k) x[k] = t0 + k < n_tokens ? __ldg(rows + (t0 + k) * row_len + c) : 0.0f;
+#pragma unroll
+      for (int k = 0; k < kAhead; ++k)
+        if (t0 + k < n_tokens) s = __dadd_rn(s, double(x[k]));
+    }
+    bias[c] = float(__ddiv_rn(s, double(n_tokens)));
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64_t n_blocks,
                                  int64_t /*blocks_per_row*/, const float *bias, int64_t bias_period,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool rotate) {
   if (n_blocks == 0) return cudaSuccess;
-  if (type == kTypeQ4_0)
-    return bias ? launch_q<kTypeQ4_0, true>(src, dst, n_blocks, bias, bias_period, stream)
-                : launch_q<kTypeQ4_0, false>(src, dst, n_blocks, nullptr, 1, stream);
-  // a bias with Q8_0 is rejected by the ABI layer
-  return launch_q<kTypeQ8_0, false>(src, dst, n_blocks, nullptr, 1, stream);
+  return rotate ? launch_q_typed<true>(type, src, dst, n_blocks, bias, bias_period, stream)
+                : launch_q_typed<false>(type, src, dst, n_blocks, bias, bias_period, stream);
+}
+
+cudaError_t launch_kv_bias(const float *rows, float *bias, int64_t n_tokens, int64_t row_len, bool rotate,
+                           cudaStream_t stream) {
+  if (row_len == 0) return cudaSuccess;
+  const int64_t threads = rotate ? row_len / 64 * 32 : row_len;
+  const unsigned grid = unsigned((threads + 127) / 128);
+  if (rotate)
+    k_kv_bias<true><<<grid, 128, 0, stream>>>(rows, bias, n_tokens, row_len);
+  else
+    k_kv_bias<false><<<grid, 128, 0, stream>>>(rows, bias, n_tokens, row_len);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dequantize_rows(int type, const uint8_t *blocks, float *dst, int64_t n_blocks,

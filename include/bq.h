@@ -57,6 +57,7 @@ extern "C" {
 #define BQ_ERR_CUDA (-5)        /* a CUDA runtime call failed (message has the CUDA error) */
 #define BQ_ERR_TIMEOUT (-6)     /* a bounded in-kernel wait ran out (see bq_device_status) */
 #define BQ_ERR_WORKSPACE (-7)   /* workspace missing or smaller than bq_workspace_size() */
+#define BQ_ERR_BASIS (-8)       /* a mean-centering bias calibrated in another basis than the K cache */
 
 /* Largest K taken by bq_gemv (the quantized activation lives in shared memory). */
 #define BQ_GEMV_MAX_K 65536
@@ -146,6 +147,13 @@ size_t bq_gemv_sequence_workspace_size(void);
  * bytes (bq_set_workspace). Errors: BQ_ERR_UNSUPPORTED (types, G),
  * BQ_ERR_SHAPE (limits), BQ_ERR_ALIGN, BQ_ERR_INVALID_ARG (null pointers, o
  * overlapping an input), BQ_ERR_WORKSPACE. */
+/* As bq_attn_decode over a K cache written in k_basis (bq_kv_quantize_basis):
+ * with BQ_BASIS_HADAMARD64 each head of q is rotated like K before it is
+ * quantized, so that the scores are unchanged ((Hq).(Hk) = q.k); head_dim
+ * must then be a multiple of 64 (else BQ_ERR_SHAPE). */
+int bq_attn_decode_basis(int k_type, int v_type, int k_basis, const float *q, const void *K_cache,
+                         const void *V_cache, float *o, int64_t n_tokens, int64_t n_heads, int64_t n_kv_heads,
+                         int64_t head_dim, float scale);
 int bq_attn_decode(int k_type, int v_type, const float *q, const void *K_cache, const void *V_cache, float *o,
                    int64_t n_tokens, int64_t n_heads, int64_t n_kv_heads, int64_t head_dim, float scale);
 size_t bq_attn_workspace_size(int k_type, int v_type, int64_t n_tokens, int64_t n_heads, int64_t n_kv_heads,
@@ -171,6 +179,38 @@ int bq_gemm(int type, const void *W_blocks, const float *X, float *Y, int64_t M,
  * §三步上手). dst: n_tokens x n_kv_heads x head_dim/32 blocks of `type`. */
 int bq_kv_quantize(int type, const float *K_rows, const float *bias, void *dst, int64_t n_tokens,
                    int64_t n_kv_heads, int64_t head_dim);
+
+/* Bases of a K cache. A quantized K cache whose head dimension is a multiple
+ * of 64 may be Hadamard-rotated; the mean-centering bias must then be measured
+ * in the rotated basis, the calibration records its basis, and a mismatch
+ * fails fast (lpnh.cn KV-cache article, §三步上手, third step). The pages name
+ * neither the size nor the scaling of the rotation; here it is orthonormal and
+ * block diagonal: every 64 channels of a head become H64 x / 8, H64[i][j] =
+ * (-1)^popcount(i & j), computed by fp32 butterflies of span 1, 2, 4, ..., 32
+ * ((a, b) -> (a + b, a - b)) followed by the exact scaling by 1/8. */
+#define BQ_BASIS_PLAIN 0
+#define BQ_BASIS_HADAMARD64 1
+
+/* KV-cache write in a basis: with basis BQ_BASIS_HADAMARD64 each head's row is
+ * rotated first (head_dim % 64 == 0, else BQ_ERR_SHAPE), then the bias (NULL
+ * or Q4_0 only, as in bq_kv_quantize) is subtracted, then the row quantized.
+ * bias_basis: the basis the bias was calibrated in (bq_kv_bias); a bias from
+ * another basis is rejected with BQ_ERR_BASIS before anything runs. Other
+ * arguments, layouts and errors as bq_kv_quantize; an unknown basis gives
+ * BQ_ERR_UNSUPPORTED. */
+int bq_kv_quantize_basis(int type, const float *K_rows, const float *bias, int bias_basis, int basis, void *dst,
+                         int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim);
+
+/* Mean-centering bias calibration (lpnh.cn KV-cache article, §三步上手: the
+ * channel mean of K over a calibration run): bias[h][c] = fp32(sum_t
+ * r_t[h][c] / n_tokens), the sum in fp64 in token order, r_t the token's row
+ * in `basis`. K_rows: n_tokens x n_kv_heads x head_dim fp32 (16-byte
+ * aligned); bias: n_kv_heads x head_dim fp32 (4-byte aligned), written.
+ * Errors: BQ_ERR_SHAPE (head_dim not a multiple of 32, or of 64 for the
+ * rotated basis), BQ_ERR_UNSUPPORTED (basis), BQ_ERR_INVALID_ARG (null
+ * pointers, n_tokens < 1, bias overlapping K_rows), BQ_ERR_ALIGN. */
+int bq_kv_bias(const float *K_rows, int basis, float *bias, int64_t n_tokens, int64_t n_kv_heads,
+               int64_t head_dim);
 
 /* Test export: out[m][b] = int32 dot of W block (m, b) (type Q4_0 or Q8_0)
  * with the Q8_0 block b of xq, computed by the same device code as bq_gemv's

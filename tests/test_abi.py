@@ -228,3 +228,33 @@ def test_attn_decode_validation(L):
     assert L.bq_attn_decode(2, 8, q + 4, K, V, o, 100, 16, 8, 128, f) == -4
     assert L.bq_attn_decode(2, 8, q, K, V, q + 256, 100, 16, 8, 128, f) == -1  # o overlaps q
     assert L.bq_attn_decode(2, 8, None, K, V, o, 100, 16, 8, 128, f) == -1
+
+
+def test_rotated_kv_and_bias_validation(L):
+    """The basis arguments are checked on the host before anything runs; a
+    bias from another basis fails fast with BQ_ERR_BASIS (-8)."""
+    base = 1 << 32
+    K, bias, dst = base, base + (1 << 24), base + (2 << 24)
+    # kv write
+    assert L.bq_kv_quantize_basis(2, K, bias, 0, 1, dst, 10, 2, 128) == -8   # plain bias, rotated cache
+    assert L.bq_kv_quantize_basis(2, K, bias, 1, 0, dst, 10, 2, 128) == -8   # rotated bias, plain cache
+    assert L.bq_kv_quantize_basis(2, K, None, 0, 1, dst, 10, 2, 96) == -2    # rotation needs head_dim % 64
+    assert L.bq_kv_quantize_basis(2, K, None, 0, 2, dst, 10, 2, 128) == -3   # unknown basis
+    assert L.bq_kv_quantize_basis(8, K, bias, 1, 1, dst, 10, 2, 128) == -3   # bias with Q8_0
+    assert L.bq_kv_quantize_basis(8, K, None, 0, 1, dst, 0, 2, 128) == 0     # empty: a no-op
+    assert L.bq_kv_quantize_basis(2, K + 4, None, 0, 1, dst, 10, 2, 128) == -4
+    # calibration
+    assert L.bq_kv_bias(K, 2, bias, 10, 2, 128) == -3
+    assert L.bq_kv_bias(K, 1, bias, 10, 2, 96) == -2
+    assert L.bq_kv_bias(K, 0, bias, 10, 2, 48) == -2
+    assert L.bq_kv_bias(K, 0, bias, 0, 2, 128) == -1                          # no calibration tokens
+    assert L.bq_kv_bias(None, 0, bias, 10, 2, 128) == -1
+    assert L.bq_kv_bias(K + 4, 0, bias, 10, 2, 128) == -4
+    assert L.bq_kv_bias(K, 0, K + 1024, 10, 2, 128) == -1                     # bias inside the rows
+    # attention over a rotated cache
+    assert L.bq_set_workspace(None, 0) == 0
+    q, o, V = base + (3 << 24), base + (4 << 24), base + (5 << 24)
+    f = ctypes.c_float(0.1)
+    assert L.bq_attn_decode_basis(2, 8, 1, q, K, V, o, 100, 16, 8, 128, f) == -7  # valid, no workspace
+    assert L.bq_attn_decode_basis(2, 8, 1, q, K, V, o, 100, 8, 8, 96, f) == -2    # rotated, head_dim 96
+    assert L.bq_attn_decode_basis(2, 8, 3, q, K, V, o, 100, 16, 8, 128, f) == -3  # unknown basis

@@ -679,3 +679,85 @@ def test_attn_decode_timeout_path_returns_error(bq, orc, dev):
     assert binding.device_status() == 0
     o_ref, mag, smax = orc.attn_decode(Q4, Q8, q, K, V, T, H, NKV, D, 0.1, with_mag=True)
     assert np.all(np.abs(o.astype(np.float64) - o_ref) <= _attn_tol(mag, smax, D))
+
+
+# ------------------------------- Hadamard-rotated K cache and calibration --
+
+ROT = 1
+
+
+def _outlier_rows(rng, T, NKV, D):
+    """K rows with per-channel means and a few outlier channels (where the
+    rotation matters), plus near-tie values after scaling."""
+    K = rng.normal(size=(T, NKV, D)) + rng.uniform(-2, 2, size=(NKV, D))
+    K[..., rng.choice(D, size=max(1, D // 32), replace=False)] *= 20.0
+    return K.astype(np.float32)
+
+
+@pytest.mark.parametrize("T,NKV,D", [(1, 1, 64), (33, 2, 64), (1000, 8, 128), (7, 1, 256), (130, 3, 192)])
+def test_kv_write_rotated_bit_exact(bq, orc, dev, T, NKV, D):
+    rng = np.random.default_rng(T * 7 + D)
+    K = _outlier_rows(rng, T, NKV, D)
+    calib = _outlier_rows(rng, 64, NKV, D)
+    bias = orc.kv_bias(calib, ROT, 64, NKV, D)
+    Kd = torch.from_numpy(K).to(dev)
+    got = _np(bq.kv_quantize(Q4, Kd, torch.from_numpy(bias).to(dev), basis=ROT))
+    assert np.array_equal(got, orc.kv_quantize(Q4, K, bias, T, NKV, D, basis=ROT))
+    assert np.array_equal(_np(bq.kv_quantize(Q4, Kd, None, basis=ROT)), orc.kv_quantize(Q4, K, None, T, NKV, D, basis=ROT))
+    assert np.array_equal(_np(bq.kv_quantize(Q8, Kd, None, basis=ROT)), orc.kv_quantize(Q8, K, None, T, NKV, D, basis=ROT))
+
+
+def test_kv_write_rotated_full_layer(bq, orc, dev):
+    """A full 32768-token layer of the KV-write workload, K rotated and
+    mean-centered with a bias calibrated in the rotated basis."""
+    from block_quantized_weight_row_gb300 import inputs
+    cfg = inputs.WORKLOADS["kv-write"]
+    L = inputs.kv_layer(0, cfg["tokens"], cfg["kv_heads"], cfg["head_dim"], cfg["calib_tokens"], device=dev)
+    bias = bq.kv_bias(L.K_calib, ROT)
+    assert np.array_equal(_np(bias), orc.kv_bias(_np(L.K_calib), ROT, *L.K_calib.shape))
+    got = _np(bq.kv_quantize(Q4, L.K, bias, basis=ROT))
+    assert np.array_equal(got, orc.kv_quantize(Q4, _np(L.K), _np(bias), *L.K.shape, basis=ROT))
+
+
+@pytest.mark.parametrize("T,NKV,D,basis", [(4096, 8, 128, 0), (4096, 8, 128, 1), (37, 3, 64, 1), (5, 1, 96, 0),
+                                           (1, 2, 256, 1)])
+def test_kv_bias_bit_exact(bq, orc, dev, T, NKV, D, basis):
+    rng = np.random.default_rng(T + D + basis)
+    rows = _outlier_rows(rng, T, NKV, D)
+    got = _np(bq.kv_bias(torch.from_numpy(rows).to(dev), basis))
+    assert np.array_equal(got, orc.kv_bias(rows, basis, T, NKV, D))
+
+
+def test_kv_bias_from_another_basis_fails_fast(bq, dev):
+    from block_quantized_weight_row_gb300 import binding
+    K = torch.ones(4, 2, 64, device=dev)
+    out = torch.full((4, 2, 36), 7, dtype=torch.uint8, device=dev)
+    for basis, bias_basis in ((1, 0), (0, 1)):
+        with pytest.raises(binding.BQError) as e:
+            bq.kv_quantize(Q4, K, torch.zeros(2, 64, device=dev), out=out, basis=basis, bias_basis=bias_basis)
+        assert e.value.status == -8
+    torch.cuda.synchronize()
+    assert bool((out == 7).all())  # nothing was written
+
+
+@pytest.mark.parametrize("T,H,NKV,D,kt,vt", [
+    (1000, 16, 8, 128, Q4, Q8), (300, 8, 2, 64, Q8, Q8), (4097, 16, 4, 128, Q4, Q4), (130, 1, 1, 256, Q8, Q8),
+    (517, 6, 3, 64, Q4, Q8), (300, 16, 2, 256, Q8, Q4)])
+def test_attn_decode_rotated_matches_oracle(bq, orc, dev, T, H, NKV, D, kt, vt):
+    """Attention over a rotated (and, for Q4_0, mean-centered) K cache: q is
+    rotated alike by both kernels (the last two shapes take the block-wide
+    kernel)."""
+    rng = np.random.default_rng(T + 3 * H + D)
+    Kf = _outlier_rows(rng, T, NKV, D)
+    Vf = rng.normal(size=(T, NKV, D)).astype(np.float32)
+    bias = orc.kv_bias(Kf, ROT, T, NKV, D) if kt == Q4 else None
+    K = orc.kv_quantize(kt, Kf, bias, T, NKV, D, basis=ROT)
+    V = orc.kv_quantize(vt, Vf, None, T, NKV, D)
+    q = rng.normal(size=(H, D)).astype(np.float32)
+    scale = 1.0 / math.sqrt(D)
+    o = _np(bq.attn_decode(kt, vt, torch.from_numpy(q).to(dev), torch.from_numpy(K).to(dev),
+                           torch.from_numpy(V).to(dev), NKV, scale, k_basis=ROT))
+    o_ref, mag, smax = orc.attn_decode(kt, vt, q, K, V, T, H, NKV, D, scale, with_mag=True, k_basis=ROT)
+    err = np.abs(o.astype(np.float64) - o_ref)
+    tol = _attn_tol(mag, smax, D)
+    assert np.all(err <= tol), f"worst err/tol {float((err / tol).max()):.3g}"
