@@ -562,7 +562,35 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
                                     "Q4_0 K (mean-centered) + Q8_0 V",
                           "kernel": "k_attn_warp + k_attn_combine",
                           "l2": "inputs larger than L2 (1.5 GB of cache per step)"}
-    del layers, g, g2, qs, outs
+    # the same write and attention with K Hadamard-rotated per 64 channels and
+    # the bias calibrated in the rotated basis (bq_kv_bias)
+    for i, (K_, V_, b, kq, vq) in enumerate(layers):
+        layers[i] = (K_, V_, bq.kv_bias(inputs.kv_layer(i, 1, H, D, kv["calib_tokens"], device=dev).K_calib,
+                                        bq.BASIS_HADAMARD64), kq, vq)
+
+    def kv_step_rot():
+        for K_, V_, b, kq, vq in layers:
+            bq.kv_quantize(bq.Q4_0, K_, b, out=kq, basis=bq.BASIS_HADAMARD64)
+            bq.kv_quantize(bq.Q8_0, V_, None, out=vq)
+    g3 = capture(kv_step_rot, stream)
+    ms3 = max_over_ranks(time_graph(g3, stream, 10, 3), dist)
+    out["kv_write_rotated"] = {"metric": "KV-cache write GB/s, K Hadamard-rotated per 64 channels",
+                               "value": round(aggregate_rate(kv_bytes, world, ms3 * 1e-3) / 1e9, 1), "unit": "GB/s",
+                               "ms_per_step": round(ms3, 4), "bytes_per_step": kv_bytes,
+                               "hbm_frac_of_measured": round(kv_bytes / (ms3 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                               "l2": "inputs larger than L2 (7.5 GB read per step)"}
+
+    def attn_step_rot():
+        for (_K, _V, _b, kq, vq), qv, ov in zip(layers, qs, outs):
+            bq.attn_decode(bq.Q4_0, bq.Q8_0, qv, kq, vq, H, scale, out=ov, k_basis=bq.BASIS_HADAMARD64)
+    g4 = capture(attn_step_rot, stream)
+    ms4 = max_over_ranks(time_graph(g4, stream, 20, 3), dist)
+    out["attn_decode_rotated"] = {"metric": "decode attention GB/s over the rotated K cache (q rotated alike)",
+                                  "value": round(aggregate_rate(cache_bytes, world, ms4 * 1e-3) / 1e9, 1),
+                                  "unit": "GB/s", "ms_per_step": round(ms4, 4), "bytes_per_step": cache_bytes,
+                                  "hbm_frac_of_measured": round(cache_bytes / (ms4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                  "l2": "inputs larger than L2 (1.5 GB of cache per step)"}
+    del layers, g, g2, g3, g4, qs, outs
     torch.cuda.empty_cache()
 
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps
