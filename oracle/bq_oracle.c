@@ -31,6 +31,10 @@
  *          computes attention in one pass without the intermediate matrix.
  *   [SHIFT] lpnh.cn KV-cache article, §解法 — q·k_i = q·(k_i − k̄) + q·k̄, and
  *          softmax is unchanged by a constant added to a whole row.
+ *   [LEG]  05. llama.cpp…, §量化类型, format table — legacy formats (Q4_0,
+ *          Q5_1, Q8_0) group 32 weights with one FP16 scale, and the "_1"
+ *          types add a minimum; §KV Cache 类型与 Flash Attention lists q4_1,
+ *          q5_0 and q5_1 among the K/V cache types.
  *   [ROT]  lpnh.cn KV-cache article, §三步上手 (third step) — a quantized K
  *          cache whose head dimension is a multiple of 64 is Hadamard-rotated;
  *          the mean-centering bias must be measured in the same basis as the
@@ -59,6 +63,21 @@
  *      Sylvester-ordered Walsh-Hadamard matrix, H64[i][j] = (-1)^popcount(i&j)
  *      (the pages require head_dim % 64 == 0 and name no size or scaling).
  *      Only K is rotated; q is rotated the same way, so q.k is unchanged.
+ *   R16 legacy layouts (the pages give none): Q4_1 = {fp16 d, fp16 m,
+ *      16 nibble bytes} (20 bytes), Q5_0 = {fp16 d, 32-bit qh, 16 nibble
+ *      bytes} (22), Q5_1 = {fp16 d, fp16 m, qh, 16 nibble bytes} (24); all
+ *      little endian; the low 4 bits of code j sit as in R2 (byte j % 16,
+ *      low nibble for j < 16), bit 4 of code j is bit j of qh; codes are
+ *      stored unsigned u (Q5_0: u = q + 16).
+ *   R17 Q5_0 is symmetric like Q4_0: d = amax / 15, q = clamp(round_half_even
+ *      (x / d16), -16, 15); value d16 * q.
+ *   R18 the "_1" types are affine: m = min_j x_j, d = (max_j x_j - m) /
+ *      (2^bits - 1) in fp32, both stored as fp16; u = clamp(round_half_even(
+ *      (x - m16) / d16), 0, 2^bits - 1) with one fp32 subtraction and one
+ *      fp32 division by the stored values; d16 == 0 gives u = 0; value
+ *      d16 * u + m16 (fp32 product, then fp32 sum).
+ *   R19 the dot of an affine weight block with a Q8_0 block is
+ *      d_w d_x sum_j u_j qx_j + m_w d_x sum_j qx_j, summed in fp64 (R6).
  *   R15 the rotated values decide integer codes, so they are computed in the
  *      kernel's precision: the fast Walsh-Hadamard butterflies in fp32,
  *      stages of span 1, 2, 4, 8, 16, 32, each pair (a, b) -> (a + b, a - b),
@@ -88,6 +107,10 @@ int64_t oracle_block_bytes(int type)
     /* [FMT4] 18 bytes per 32 Q4_0 weights; [FMT8] 2-byte scale + 32 int8. */
     if (type == ORACLE_TYPE_Q4_0) return 2 + QK / 2;
     if (type == ORACLE_TYPE_Q8_0) return 2 + QK;
+    /* [LEG] + R16: scale, (minimum,) (high bits,) nibbles */
+    if (type == ORACLE_TYPE_Q4_1) return 2 + 2 + QK / 2;
+    if (type == ORACLE_TYPE_Q5_0) return 2 + 4 + QK / 2;
+    if (type == ORACLE_TYPE_Q5_1) return 2 + 2 + 4 + QK / 2;
     return 0;
 }
 
@@ -164,10 +187,86 @@ float oracle_round_half_even(float v)
     return nearbyintf(v);
 }
 
+/* ---- one block of a legacy type: R16, R17, R18 ---- */
+
+static int legacy_bits(int type) { return type == ORACLE_TYPE_Q4_1 ? 4 : 5; }
+static int legacy_affine(int type) { return type != ORACLE_TYPE_Q5_0; }
+static int is_legacy(int type)
+{
+    return type == ORACLE_TYPE_Q4_1 || type == ORACLE_TYPE_Q5_0 || type == ORACLE_TYPE_Q5_1;
+}
+
+static void put_u16(uint8_t *p, uint16_t v)
+{
+    p[0] = (uint8_t)(v & 0xFFu);
+    p[1] = (uint8_t)(v >> 8);
+}
+
+static void quantize_block_legacy(int type, const float *x, uint8_t *out)
+{
+    const int umax = (1 << legacy_bits(type)) - 1;
+    int u[QK];
+    uint16_t d16, m16 = 0;
+    if (legacy_affine(type)) {
+        float mn = x[0], mx = x[0];
+        for (int j = 1; j < QK; j++) {
+            if (x[j] < mn) mn = x[j];
+            if (x[j] > mx) mx = x[j];
+        }
+        float d = (mx - mn) / (float)umax; /* R18 */
+        d16 = oracle_f32_to_f16(d);
+        m16 = oracle_f32_to_f16(mn);
+        float ds = oracle_f16_to_f32(d16), ms = oracle_f16_to_f32(m16);
+        for (int j = 0; j < QK; j++) {
+            int v = 0;
+            if (ds != 0.0f)
+                v = (int)oracle_round_half_even((x[j] - ms) / ds);
+            if (v > umax) v = umax;
+            if (v < 0) v = 0;
+            u[j] = v;
+        }
+    } else {
+        float amax = 0.0f;
+        for (int j = 0; j < QK; j++)
+            if (fabsf(x[j]) > amax) amax = fabsf(x[j]);
+        float d = amax / 15.0f; /* R17 */
+        d16 = oracle_f32_to_f16(d);
+        float ds = oracle_f16_to_f32(d16);
+        for (int j = 0; j < QK; j++) {
+            int v = 0;
+            if (ds != 0.0f)
+                v = (int)oracle_round_half_even(x[j] / ds);
+            if (v > 15) v = 15;
+            if (v < -16) v = -16;
+            u[j] = v + 16;
+        }
+    }
+    int o = 2;
+    put_u16(out, d16);
+    if (legacy_affine(type)) {
+        put_u16(out + 2, m16);
+        o = 4;
+    }
+    if (legacy_bits(type) == 5) {
+        uint32_t qh = 0;
+        for (int j = 0; j < QK; j++)
+            qh |= (uint32_t)((u[j] >> 4) & 1) << j;
+        for (int k = 0; k < 4; k++)
+            out[o + k] = (uint8_t)(qh >> (8 * k));
+        o += 4;
+    }
+    for (int j = 0; j < QK / 2; j++)
+        out[o + j] = (uint8_t)((unsigned)(u[j] & 15) | ((unsigned)(u[j + QK / 2] & 15) << 4));
+}
+
 /* ---- one block: R3 + R4 ---- */
 
 static void quantize_block(int type, const float *x, uint8_t *out)
 {
+    if (is_legacy(type)) {
+        quantize_block_legacy(type, x, out);
+        return;
+    }
     const int qmax = (type == ORACLE_TYPE_Q4_0) ? 7 : 127;
     const int qmin = (type == ORACLE_TYPE_Q4_0) ? -8 : -127;
 
@@ -211,9 +310,33 @@ static float block_scale(const uint8_t *blk)
     return oracle_f16_to_f32(d16);
 }
 
-/* codes of one block as plain ints, R2 inverted */
+/* the stored minimum of an affine block (R18), 0 for the symmetric types */
+static float block_min(int type, const uint8_t *blk)
+{
+    if (!is_legacy(type) || !legacy_affine(type))
+        return 0.0f;
+    return oracle_f16_to_f32((uint16_t)(blk[2] | ((uint16_t)blk[3] << 8)));
+}
+
+/* codes of one block as plain ints, R2 inverted; affine types give u,
+ * Q5_0 gives u - 16 (R16-R18) */
 static void block_codes(int type, const uint8_t *blk, int *q)
 {
+    if (is_legacy(type)) {
+        int o = legacy_affine(type) ? 4 : 2;
+        uint32_t qh = 0;
+        if (legacy_bits(type) == 5) {
+            qh = (uint32_t)blk[o] | ((uint32_t)blk[o + 1] << 8) | ((uint32_t)blk[o + 2] << 16) |
+                 ((uint32_t)blk[o + 3] << 24);
+            o += 4;
+        }
+        for (int j = 0; j < QK; j++) {
+            unsigned lo = (j < QK / 2) ? (blk[o + j] & 0x0Fu) : (unsigned)(blk[o + j - QK / 2] >> 4);
+            int u = (int)(lo | (((qh >> j) & 1u) << 4));
+            q[j] = legacy_affine(type) ? u : u - 16;
+        }
+        return;
+    }
     if (type == ORACLE_TYPE_Q4_0) {
         for (int j = 0; j < QK / 2; j++) {
             q[j] = (int)(blk[2 + j] & 0x0Fu) - 8;
@@ -249,10 +372,14 @@ int oracle_dequantize_rows(int type, const uint8_t *blocks, float *dst,
     for (int64_t r = 0; r < n_rows; r++)
         for (int64_t b = 0; b < nb; b++) {
             const uint8_t *blk = blocks + (r * nb + b) * bb;
-            float d = block_scale(blk);
+            float d = block_scale(blk), mn = block_min(type, blk);
             block_codes(type, blk, q);
-            for (int j = 0; j < QK; j++)
-                dst[r * n_cols + b * QK + j] = d * (float)q[j]; /* [SYM] value = scale * q */
+            for (int j = 0; j < QK; j++) {
+                float v = d * (float)q[j]; /* [SYM] value = scale * q */
+                if (is_legacy(type) && legacy_affine(type))
+                    v = v + mn; /* R18: then the minimum, a second fp32 operation */
+                dst[r * n_cols + b * QK + j] = v;
+            }
         }
     return 0;
 }
@@ -296,6 +423,16 @@ static void dot_row(int w_type, const uint8_t *wrow, const uint8_t *xrow, int64_
         double term = (double)block_scale(wb) * (double)block_scale(xb) * (double)sumi;
         acc += term;
         macc += fabs(term);
+        if (is_legacy(w_type) && legacy_affine(w_type)) { /* R19: the minimum times the x block's code sum */
+            int qx[QK];
+            block_codes(ORACLE_TYPE_Q8_0, xb, qx);
+            int32_t xs = 0;
+            for (int j = 0; j < QK; j++)
+                xs += qx[j];
+            double mterm = (double)block_min(w_type, wb) * (double)block_scale(xb) * (double)xs;
+            acc += mterm;
+            macc += fabs(mterm);
+        }
     }
     *y = (float)acc;
     if (mag)
@@ -445,6 +582,8 @@ int oracle_attn_decode_basis(int k_type, int v_type, int k_basis, const float *q
     int64_t bk = oracle_block_bytes(k_type), bv = oracle_block_bytes(v_type);
     if (bk == 0 || bv == 0 || head_dim <= 0 || head_dim % QK != 0 || n_tokens < 1 || n_kv_heads < 1 ||
         n_heads < n_kv_heads || n_heads % n_kv_heads != 0)
+        return -1;
+    if (is_legacy(k_type) || is_legacy(v_type)) /* attention reads Q4_0 / Q8_0 caches */
         return -1;
     if (k_basis != ORACLE_BASIS_PLAIN && (k_basis != ORACLE_BASIS_HADAMARD64 || head_dim % 64 != 0))
         return -1;

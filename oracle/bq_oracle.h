@@ -33,6 +33,17 @@ extern "C" {
 
 #define ORACLE_TYPE_Q4_0 2
 #define ORACLE_TYPE_Q8_0 8
+/* legacy types with a 5th bit and/or a minimum ("_1 adds a minimum";
+ * 05. llama.cpp…, §量化类型). Layouts, this project's reading:
+ *   Q4_1: 20 bytes = { fp16 d, fp16 m, 16 nibble bytes }
+ *   Q5_0: 22 bytes = { fp16 d, uint32 qh, 16 nibble bytes }
+ *   Q5_1: 24 bytes = { fp16 d, fp16 m, uint32 qh, 16 nibble bytes }
+ * nibbles as Q4_0 (element j: low nibble of byte j for j < 16, high nibble of
+ * byte j - 16), bit 4 of element j = bit j of qh; codes unsigned u, value
+ * d * u + m (Q4_1, Q5_1) or d * (u - 16) (Q5_0). */
+#define ORACLE_TYPE_Q4_1 3
+#define ORACLE_TYPE_Q5_0 6
+#define ORACLE_TYPE_Q5_1 7
 
 /* bases of a K cache: plain, or Hadamard-rotated per 64 channels */
 #define ORACLE_BASIS_PLAIN 0

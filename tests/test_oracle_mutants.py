@@ -37,6 +37,13 @@ MUTANTS = [
     ("attn_v_decoded_as_k", "oracle_dequantize_rows(v_type, V +", "oracle_dequantize_rows(k_type, V +"),
     ("attn_k_scale_twice", "(double)block_scale(kt + b * bk) * (double)block_scale(qh + b * bq)",
      "(double)block_scale(kt + b * bk) * (double)block_scale(kt + b * bk)"),
+    ("legacy_min_not_added", "v = v + mn; /* R18: then the minimum, a second fp32 operation */", "(void)mn;"),
+    ("legacy_qh_reversed", "qh |= (uint32_t)((u[j] >> 4) & 1) << j;", "qh |= (uint32_t)((u[j] >> 4) & 1) << (31 - j);"),
+    ("legacy_q5_0_divisor_16", "float d = amax / 15.0f; /* R17 */", "float d = amax / 16.0f; /* R17 */"),
+    ("legacy_min_term_dropped", "acc += mterm;", "(void)mterm;"),
+    ("legacy_5bit_range_15", "const int umax = (1 << legacy_bits(type)) - 1;", "const int umax = 15;"),
+    ("legacy_unrounded_min", "float ds = oracle_f16_to_f32(d16), ms = oracle_f16_to_f32(m16);",
+     "float ds = oracle_f16_to_f32(d16), ms = mn;"),
     ("hadamard_scaled_by_1_64", "v[j] = v[j] * 0.125f;", "v[j] = v[j] * 0.015625f;"),
     ("hadamard_no_minus", "v[j + h] = a - b;", "v[j + h] = a + b;"),
     ("hadamard_32_point", "for (int h = 1; h < 64; h *= 2)", "for (int h = 1; h < 32; h *= 2)"),

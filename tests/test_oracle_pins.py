@@ -586,3 +586,142 @@ def test_attn_over_a_rotated_cache_rotates_q(orc):
     err = np.abs(o - exact).max()
     assert err < 0.02
     assert np.abs(o_wrong - exact).max() > 10 * err
+
+
+# ---------------------------------------------- legacy types ([LEG], R16-R19) --
+
+Q4_1, Q5_0, Q5_1 = 3, 6, 7
+LEGACY = {"Q4_1": Q4_1, "Q5_0": Q5_0, "Q5_1": Q5_1}
+
+
+def _parse_legacy(t, blocks):
+    """The test's own reading of R16: (d16, m16, u[32]) per block, as numpy."""
+    b = np.asarray(blocks, np.uint8).reshape(-1, {Q4_1: 20, Q5_0: 22, Q5_1: 24}[t])
+    d = b[:, 0:2].copy().view(np.float16).astype(np.float64)[:, 0]
+    o = 2
+    m = np.zeros_like(d)
+    if t != Q5_0:
+        m = b[:, 2:4].copy().view(np.float16).astype(np.float64)[:, 0]
+        o = 4
+    qh = np.zeros(len(b), np.uint64)
+    if t != Q4_1:
+        qh = b[:, o:o + 4].copy().view(np.uint32)[:, 0].astype(np.uint64)
+        o += 4
+    nib = b[:, o:o + 16].astype(np.int64)
+    lo = np.concatenate([nib & 15, nib >> 4], axis=1)
+    hi = ((qh[:, None] >> np.arange(32, dtype=np.uint64)[None, :]) & np.uint64(1)).astype(np.int64)
+    return d, m, lo | (hi << 4)
+
+
+def test_legacy_block_sizes(orc):
+    # the "_1" types add one fp16 minimum to the scale (R16); 5-bit types add 32 high bits
+    assert orc.block_bytes(Q4_1) == orc.block_bytes(Q4) + 2 == 20
+    assert orc.block_bytes(Q5_0) == 2 + 4 + 16 == 22
+    assert orc.block_bytes(Q5_1) == orc.block_bytes(Q5_0) + 2 == 24
+    assert [orc.block_bytes(t) * 8 / 32 for t in (Q4_1, Q5_0, Q5_1)] == [5.0, 5.5, 6.0]
+
+
+def test_legacy_hand_blocks(orc):
+    # Q4_1: x = -1, 0.5, 1.5, 14, rest 0 -> m = -1, d = 15/15 = 1 (0x3C00);
+    # (x - m) = 0, 1.5, 2.5, 15, 1 -> u = 0, 2 (half-even), 2 (half-even), 15, 1
+    x = np.zeros((1, 32), np.float32)
+    x[0, :4] = [-1.0, 0.5, 1.5, 14.0]
+    b = orc.quantize_rows(Q4_1, x)[0]
+    assert b[:4].tolist() == [0x00, 0x3C, 0x00, 0xBC]          # d = 1.0, m = -1.0 (0xBC00)
+    assert b[4:8].tolist() == [0x10, 0x12, 0x12, 0x1F]          # low nibble u[j], high nibble u[j+16] = 1
+    assert b[8:].tolist() == [0x11] * 12
+    # Q5_0: x0 = 15, x1 = -15, rest 0 -> d = 1, q = 15, -15, 0 -> u = 31, 1, 16
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0], x[0, 1] = 15.0, -15.0
+    b = orc.quantize_rows(Q5_0, x)[0]
+    assert b[:2].tolist() == [0x00, 0x3C]
+    qh = int.from_bytes(bytes(b[2:6]), "little")
+    assert qh == 0xFFFFFFFF & ~0b10                              # bit 1 clear: u1 = 1 < 16
+    assert b[6:8].tolist() == [0x0F, 0x01] and b[8:].tolist() == [0x00] * 14
+    # Q5_1: a constant block -> d = 0, m = 3.25 (0x4280), every u = 0, value 3.25 exactly
+    x = np.full((1, 32), 3.25, np.float32)
+    b = orc.quantize_rows(Q5_1, x)[0]
+    assert b.tolist() == [0x00, 0x00, 0x80, 0x42] + [0] * 20
+    assert np.all(orc.dequantize_rows(Q5_1, b[None], 32) == 3.25)
+
+
+def _legacy_rows(rng, n):
+    rows = [rng.normal(size=(n, 32)), rng.standard_t(2, size=(n, 32)) * 10, rng.uniform(3, 9, size=(n, 32)),
+            rng.normal(size=(n, 32)) * 1e-4 - 50.0]
+    return np.concatenate(rows).astype(np.float32)
+
+
+@pytest.mark.parametrize("name", list(LEGACY))
+def test_legacy_codes_are_the_rounded_quotients(orc, name):
+    """Codes stored = clamp(round_half_even((x - m16) / d16)) computed by numpy
+    in fp32 from the stored scale and minimum (R17/R18)."""
+    t = LEGACY[name]
+    x = _legacy_rows(np.random.default_rng(21), 500)
+    d, m, u = _parse_legacy(t, orc.quantize_rows(t, x))
+    d32, m32 = d.astype(np.float32)[:, None], m.astype(np.float32)[:, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        if t == Q5_0:
+            q = np.rint(x / d32)
+            ref = np.where(d32 == 0, 16, np.clip(q, -16, 15) + 16)
+        else:
+            q = np.rint((x - m32) / d32)
+            ref = np.where(d32 == 0, 0, np.clip(q, 0, 15 if t == Q4_1 else 31))
+    assert np.array_equal(u, ref.astype(np.int64))
+    # and the scales: symmetric amax / 15, affine (max - min) / qmax and min, as binary16
+    if t == Q5_0:
+        assert np.array_equal(d.astype(np.float16), (np.abs(x).max(1) / np.float32(15)).astype(np.float16))
+    else:
+        qmax = np.float32(15 if t == Q4_1 else 31)
+        assert np.array_equal(d.astype(np.float16), ((x.max(1) - x.min(1)) / qmax).astype(np.float16))
+        assert np.array_equal(m.astype(np.float16), x.min(1).astype(np.float16))
+
+
+@pytest.mark.parametrize("name", list(LEGACY))
+def test_legacy_round_trip_bound(orc, name):
+    t = LEGACY[name]
+    x = _legacy_rows(np.random.default_rng(22), 800)
+    blocks = orc.quantize_rows(t, x)
+    xh = orc.dequantize_rows(t, blocks, 32).astype(np.float64)
+    d, m, _ = _parse_legacy(t, blocks)
+    xd = x.astype(np.float64)
+    ulp = 4 * np.abs(xd).max(1) * 2.0 ** -23
+    if t == Q5_0:
+        bound = d / 2 * (1 + 2.0 ** -18) + ulp
+    else:
+        qmax = 15 if t == Q4_1 else 31
+        dt, mt = (xd.max(1) - xd.min(1)) / qmax, xd.min(1)
+        bound = d / 2 * (1 + 2.0 ** -18) + qmax * np.abs(d - dt) + np.abs(m - mt) + ulp
+    assert np.all(np.abs(xh - xd) <= bound[:, None])
+
+
+@pytest.mark.parametrize("name", list(LEGACY))
+def test_legacy_gemv_is_the_brute_force_product(orc, name):
+    """R19: y = sum over blocks of (d_w u + m_w) . (d_x qx), in fp64 from the
+    test's own parse of both operands."""
+    t = LEGACY[name]
+    rng = np.random.default_rng(23)
+    M, K = 7, 160
+    W = (rng.normal(size=(M, K)) + rng.uniform(-1, 1, size=(M, 1))).astype(np.float32)
+    x = rng.normal(size=K).astype(np.float32)
+    wb = orc.quantize_rows(t, W)
+    y, mag = orc.gemv(t, wb, x, M, K, with_mag=True)
+    dw, mw, uw = _parse_legacy(t, wb)
+    xq = orc.quantize_rows(Q8, x[None])[0].reshape(-1, 34)
+    dx = xq[:, 0:2].copy().view(np.float16).astype(np.float64)[:, 0]
+    qx = xq[:, 2:].view(np.int8).astype(np.float64)
+    vw = (dw[:, None] * (uw - (16 if t == Q5_0 else 0)) + mw[:, None]).reshape(M, K // 32, 32)
+    vx = (dx[:, None] * qx)[None]
+    ref = (vw * vx).sum(axis=(1, 2))
+    assert np.allclose(y.astype(np.float64), ref, rtol=1e-6, atol=1e-9 * mag.max())
+
+
+@pytest.mark.parametrize("name", list(LEGACY))
+def test_legacy_kv_write_is_the_row_quantizer(orc, name):
+    t = LEGACY[name]
+    rng = np.random.default_rng(24)
+    T, NKV, D = 9, 3, 64
+    K = rng.normal(size=(T, NKV, D)).astype(np.float32)
+    assert np.array_equal(orc.kv_quantize(t, K, None, T, NKV, D).reshape(-1),
+                          orc.quantize_rows(t, K.reshape(-1, D)).reshape(-1))
+    with pytest.raises(ValueError):
+        orc.kv_quantize(t, K, np.zeros((NKV, D), np.float32), T, NKV, D)  # bias: Q4_0 only
