@@ -13,6 +13,7 @@ import torch
 
 Q4_0 = 2
 Q8_0 = 8
+Q4_1, Q5_0, Q5_1 = 3, 6, 7
 QK = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

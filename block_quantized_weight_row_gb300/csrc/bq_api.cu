@@ -53,8 +53,14 @@ int cuda_fail(cudaError_t e, const char *where) {
 int block_bytes(int type) {
   if (type == BQ_TYPE_Q4_0) return Fmt<kTypeQ4_0>::kBytes;
   if (type == BQ_TYPE_Q8_0) return Fmt<kTypeQ8_0>::kBytes;
+  if (type == BQ_TYPE_Q4_1) return Fmt<kTypeQ4_1>::kBytes;
+  if (type == BQ_TYPE_Q5_0) return Fmt<kTypeQ5_0>::kBytes;
+  if (type == BQ_TYPE_Q5_1) return Fmt<kTypeQ5_1>::kBytes;
   return 0;
 }
+
+// Q4_0 / Q8_0: the types every entry point takes
+bool core_type(int type) { return type == BQ_TYPE_Q4_0 || type == BQ_TYPE_Q8_0; }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -195,7 +201,7 @@ size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K) {
 }
 
 size_t bq_gemv_workspace_size(int type, int64_t K) {
-  if (!block_bytes(type)) return 0;
+  if (!core_type(type)) return 0;  // legacy types quantize x inside the GEMV
   return gemv_workspace_bytes(K);
 }
 
@@ -308,6 +314,7 @@ int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *cons
                      const int64_t *M, const float *const *x, const int64_t *K) {
   const int bb = block_bytes(type);
   if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_gemv_sequence: unknown type %d", type);
+  if (!core_type(type)) return fail(BQ_ERR_UNSUPPORTED, "bq_gemv_sequence: Q4_0 or Q8_0 weights only");
   if (n_groups < 0) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: negative batch count");
   if (n_groups == 0) return ok();
   if (!n_mats || !x || !K) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: null array");
@@ -387,7 +394,7 @@ int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *cons
 
 namespace {
 int attn_check(int k_type, int v_type, int64_t T, int64_t H, int64_t n_kv, int64_t D, const char *who) {
-  if (!block_bytes(k_type) || !block_bytes(v_type)) return fail(BQ_ERR_UNSUPPORTED, "%s: unknown cache type", who);
+  if (!core_type(k_type) || !core_type(v_type)) return fail(BQ_ERR_UNSUPPORTED, "%s: caches are Q4_0 or Q8_0", who);
   if (T < 1 || H < 1 || n_kv < 1 || D < kQK || D % kQK || H % n_kv)
     return fail(BQ_ERR_SHAPE, "%s: needs n_tokens >= 1, head_dim a multiple of 32, n_heads a multiple of n_kv_heads", who);
   const int64_t G = H / n_kv;
@@ -490,6 +497,8 @@ int bq_kv_quantize_basis(int type, const float *rows, const float *bias, int bia
   if (basis == BQ_BASIS_HADAMARD64 && head_dim % 64)
     return fail(BQ_ERR_SHAPE, "bq_kv_quantize: the rotated basis needs head_dim %% 64 == 0, got %lld",
                 (long long)head_dim);
+  if (basis == BQ_BASIS_HADAMARD64 && !core_type(type))
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: the rotated basis takes Q4_0 or Q8_0");
   const int64_t n_blocks = n_tokens * n_kv_heads * (head_dim / kQK);
   if (n_blocks == 0) return ok();
   if (!rows || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: null pointer");
@@ -524,6 +533,7 @@ int bq_kv_bias(const float *rows, int basis, float *bias, int64_t n_tokens, int6
 int bq_block_dots(int type, const void *W, const void *xq, int32_t *out, int64_t M, int64_t K) {
   const int bb = block_bytes(type);
   if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_block_dots: unknown type %d", type);
+  if (!core_type(type)) return fail(BQ_ERR_UNSUPPORTED, "bq_block_dots: Q4_0 or Q8_0 weights only");
   if (!sizes_ok(M, K)) return fail(BQ_ERR_INVALID_ARG, "bq_block_dots: bad sizes");
   if (K % kQK) return fail(BQ_ERR_SHAPE, "bq_block_dots: K %lld is not a multiple of 32", (long long)K);
   if (M == 0 || K == 0) return ok();

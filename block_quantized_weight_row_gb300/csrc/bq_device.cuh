@@ -15,6 +15,10 @@ namespace bq {
 constexpr int kQK = 32;
 constexpr int kTypeQ4_0 = 2;
 constexpr int kTypeQ8_0 = 8;
+// legacy types with a fifth bit and/or a minimum (below)
+constexpr int kTypeQ4_1 = 3;
+constexpr int kTypeQ5_0 = 6;
+constexpr int kTypeQ5_1 = 7;
 constexpr unsigned kFull = 0xffffffffu;
 
 // error bits of the device error word
@@ -30,6 +34,29 @@ template <> struct Fmt<kTypeQ8_0> {
   static constexpr int kBytes = 34;   // 2-byte scale + 32 int8
   static constexpr int kQmax = 127;
   static constexpr int kQmin = -127;
+};
+template <> struct Fmt<kTypeQ4_1> { static constexpr int kBytes = 20; };  // d, m, 16 nibble bytes
+template <> struct Fmt<kTypeQ5_0> { static constexpr int kBytes = 22; };  // d, qh, 16 nibble bytes
+template <> struct Fmt<kTypeQ5_1> { static constexpr int kBytes = 24; };  // d, m, qh, 16 nibble bytes
+
+// Legacy types ("05. llama.cpp：从 GGUF 文件到本地推理服务", §量化类型: legacy
+// formats keep one FP16 scale per 32 weights, and "_1" adds a minimum). The
+// layouts are this library's reading: scale first, then the minimum (_1),
+// then bit 4 of every code as one little-endian 32-bit word (5-bit types),
+// then the low 4 bits in Q4_0's nibble order. Codes are unsigned u; the value
+// is d * u + m (_1) or d * (u - 16) (Q5_0).
+template <int TYPE> struct Legacy { static constexpr bool kIs = false; };
+template <> struct Legacy<kTypeQ4_1> {
+  static constexpr bool kIs = true, kAffine = true;
+  static constexpr int kUmax = 15, kQh = -1, kQs = 4;  // byte offsets of qh and the nibbles
+};
+template <> struct Legacy<kTypeQ5_0> {
+  static constexpr bool kIs = true, kAffine = false;
+  static constexpr int kUmax = 31, kQh = 2, kQs = 6;
+};
+template <> struct Legacy<kTypeQ5_1> {
+  static constexpr bool kIs = true, kAffine = true;
+  static constexpr int kUmax = 31, kQh = 4, kQs = 8;
 };
 
 // ---------------------------------------------------------------- quantize --
@@ -288,6 +315,92 @@ __device__ __forceinline__ int sumi_q8_q8(const uint32_t qw[8], const uint32_t x
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xffffu)));
+}
+
+// ---------------------------------------------------------- legacy types --
+
+// One block of a legacy type, by a single lane, exactly: symmetric Q5_0
+// d = amax / 15, u = clamp(rn(x / d16), -16, 15) + 16; affine "_1" types
+// m = min x, d = (max x - m) / umax, u = clamp(rn((x - m16) / d16), 0, umax),
+// every step one IEEE fp32 operation on the stored binary16 values. `out` is
+// the block, 2-byte aligned.
+template <int TYPE>
+__device__ __forceinline__ void legacy_quantize_block(const float (&v)[32], uint16_t *out) {
+  using L = Legacy<TYPE>;
+  uint32_t u[32];
+  uint16_t d16, m16 = 0;
+  if (L::kAffine) {
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {  // strict comparisons: the first of equal extremes is kept
+      if (v[j] < mn) mn = v[j];
+      if (v[j] > mx) mx = v[j];
+    }
+    const __half hd = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), float(L::kUmax)));
+    const __half hm = __float2half_rn(mn);
+    d16 = __half_as_ushort(hd);
+    m16 = __half_as_ushort(hm);
+    const float ds = __half2float(hd), ms = __half2float(hm);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      int q = 0;
+      if (ds != 0.0f) q = int(rintf(__fdiv_rn(__fsub_rn(v[j], ms), ds)));
+      u[j] = uint32_t(min(max(q, 0), L::kUmax));
+    }
+  } else {
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    const __half hd = __float2half_rn(__fdiv_rn(amax, 15.0f));
+    d16 = __half_as_ushort(hd);
+    const float ds = __half2float(hd);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      int q = 0;
+      if (ds != 0.0f) q = int(rintf(__fdiv_rn(v[j], ds)));
+      u[j] = uint32_t(min(max(q, -16), 15) + 16);
+    }
+  }
+  int o = 0;
+  out[o++] = d16;
+  if (L::kAffine) out[o++] = m16;
+  if (L::kQh >= 0) {
+    uint32_t qh = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) qh |= ((u[j] >> 4) & 1u) << j;
+    out[o++] = uint16_t(qh & 0xffffu);
+    out[o++] = uint16_t(qh >> 16);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t b0 = (u[2 * k] & 15u) | ((u[2 * k + 16] & 15u) << 4);
+    const uint32_t b1 = (u[2 * k + 1] & 15u) | ((u[2 * k + 17] & 15u) << 4);
+    out[o + k] = uint16_t(b0 | (b1 << 8));
+  }
+}
+
+// Bit 4 of codes 4i..4i+3 (bits 4i.. of qh) moved to bit 4 of each byte.
+__device__ __forceinline__ uint32_t qh_nibble_bits(uint32_t qh, int i) {
+  return (((qh >> (4 * i)) & 0xfu) * 0x00204081u & 0x01010101u) << 4;
+}
+
+// Integer dot of a legacy block's unsigned codes u with a Q8_0 block's
+// codes: sum_j u_j * qx_j. qs: the 4 nibble words (bytes 4i..4i+3 each);
+// qh: the high-bit word (0 for Q4_1).
+template <int TYPE>
+__device__ __forceinline__ int legacy_sumu(const uint32_t (&qs)[4], uint32_t qh, const uint32_t *xw) {
+  int lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t a = qs[i] & 0x0f0f0f0fu, b = (qs[i] >> 4) & 0x0f0f0f0fu;
+    if (Legacy<TYPE>::kQh >= 0) {
+      a |= qh_nibble_bits(qh, i);
+      b |= qh_nibble_bits(qh, 4 + i);
+    }
+    lo = dp4a_us(a, xw[i], lo);      // codes 4i..4i+3
+    hi = dp4a_us(b, xw[4 + i], hi);  // codes 16+4i..
+  }
+  return lo + hi;
 }
 
 // ------------------------------------------------------ packed fp32 pairs --

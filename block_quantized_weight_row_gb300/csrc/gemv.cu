@@ -275,6 +275,21 @@ __global__ void __launch_bounds__(256)
     float acc = 0.0f;
     for (int b = lane; b < nb; b += 32) {
       const uint16_t *blk = reinterpret_cast<const uint16_t *>(W + m * row_bytes + int64_t(b) * BB);
+      if constexpr (Legacy<TYPE>::kIs) {
+        // d_w d_x sum_j u_j qx_j (- 16 d_w d_x sum qx for Q5_0) + m_w d_x sum qx
+        using L = Legacy<TYPE>;
+        uint32_t qs[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qs[i] = uint32_t(blk[L::kQs / 2 + 2 * i]) | (uint32_t(blk[L::kQs / 2 + 2 * i + 1]) << 16);
+        const uint32_t qh = L::kQh >= 0 ? (uint32_t(blk[L::kQh / 2]) | (uint32_t(blk[L::kQh / 2 + 1]) << 16)) : 0u;
+        const int xsum = int(xs[9 * nb + b]);
+        int sumi = legacy_sumu<TYPE>(qs, qh, xs + 8 * b);
+        if (!L::kAffine) sumi -= 16 * xsum;
+        const float dx = __uint_as_float(xs[8 * nb + b]);
+        acc = __fmaf_rn(__fmul_rn(half_bits_to_float(blk[0]), dx), float(sumi), acc);
+        if (L::kAffine) acc = __fmaf_rn(__fmul_rn(half_bits_to_float(blk[1]), dx), float(xsum), acc);
+        continue;
+      }
       constexpr int kQW = (TYPE == kTypeQ4_0) ? 4 : 8;
       uint32_t q[kQW];
 #pragma unroll
@@ -424,10 +439,34 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
   return cudaSuccess;
 }
 
+// Legacy weight types: the generic kernel, one launch per matrix (every CTA
+// quantizes x into shared memory).
+template <int TYPE>
+cudaError_t launch_legacy(int n, const uint8_t *const *W, float *const *y, const int64_t *M, const float *x,
+                          int64_t K, cudaStream_t stream) {
+  cudaError_t err;
+  const DeviceInfo *di = device_info(&err);
+  if (!di) return err;
+  const int nb = int(K / kQK);
+  const size_t smem = size_t(nb) * 40;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_generic<TYPE>), int(smem));
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i) {
+    if (M[i] == 0) continue;
+    const int64_t grid = std::min((M[i] + 7) / 8, int64_t(di->sm_count) * 4);
+    k_gemv_generic<TYPE><<<unsigned(grid), 256, smem, stream>>>(W[i], x, y[i], int(M[i]), int(K));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *y, const int64_t *M,
                         const float *x, int64_t K, uint32_t *rec_ws, cudaStream_t stream) {
+  if (type == kTypeQ4_1) return launch_legacy<kTypeQ4_1>(n, W, y, M, x, K, stream);
+  if (type == kTypeQ5_0) return launch_legacy<kTypeQ5_0>(n, W, y, M, x, K, stream);
+  if (type == kTypeQ5_1) return launch_legacy<kTypeQ5_1>(n, W, y, M, x, K, stream);
   if (type == kTypeQ4_0) return launch_typed<kTypeQ4_0>(n, W, y, M, x, K, rec_ws, stream);
   return launch_typed<kTypeQ8_0>(n, W, y, M, x, K, rec_ws, stream);
 }

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     k_quantize_rows(const float *__restrict__ src, uint8_t *__restrict__ dst, int64_t n_blocks,
                     const float *__restrict__ bias, int64_t bias_period) {
   constexpr int BB = Fmt<TYPE>::kBytes;
-  constexpr int NW = TYPE == kTypeQ4_0 ? 4 : 8;  // code words per block
+  constexpr int NW = TYPE == kTypeQ4_0 ? 4 : 8;  // code words per block (Q4_0 / Q8_0)
   __shared__ __align__(16) uint8_t in_tile[kQuantWarps][32 * 128];
   __shared__ __align__(16) uint8_t out_tile[kQuantWarps][32 * BB];
   __shared__ __align__(16) uint8_t bias_tile[BIAS ? kMaxSmemBiasBlocks * 128 : 16];
@@ -139,6 +139,10 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
         v[4 * c + 3] = __fsub_rn(v[4 * c + 3], f.w);
       }
     }
+    if constexpr (Legacy<TYPE>::kIs) {
+      // legacy types: the exact rule for every block
+      legacy_quantize_block<TYPE>(v, reinterpret_cast<uint16_t *>(ot + lane * BB));
+    } else {
     uint16_t scale;
     uint32_t w[NW];
     if (!quantize_block_lane_fast<TYPE>(v, scale, w)) {
@@ -175,6 +179,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
       o[1 + 2 * i] = uint16_t(w[i] & 0xffffu);
       o[2 + 2 * i] = uint16_t(w[i] >> 16);
     }
+    }
     __syncwarp();
     const int nbytes = nblk * BB;
     uint8_t *out = dst + tile * 32 * BB;  // 16-byte aligned: 32 * BB is a multiple of 16
@@ -199,23 +204,40 @@ __global__ void __launch_bounds__(256)
     const int j = int(i & 7);  // elements 4j..4j+3
     const uint8_t *blk = blocks + g * BB;
     const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
-    int q[4];
+    if constexpr (Legacy<TYPE>::kIs) {
+      using L = Legacy<TYPE>;
+      const uint16_t *h = reinterpret_cast<const uint16_t *>(blk);  // 2-byte aligned
+      const float mn = L::kAffine ? half_bits_to_float(h[1]) : 0.0f;
+      const uint32_t qh = L::kQh >= 0 ? (uint32_t(h[L::kQh / 2]) | (uint32_t(h[L::kQh / 2 + 1]) << 16)) : 0u;
+      float r[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (TYPE == kTypeQ4_0) {
+      for (int e = 0; e < 4; ++e) {
         const int el = 4 * j + e;
-        const uint8_t b = blk[2 + (el & 15)];
-        q[e] = int(el < 16 ? (b & 0x0f) : (b >> 4)) - 8;
-      } else {
-        q[e] = int(static_cast<int8_t>(blk[2 + 4 * j + e]));
+        const uint8_t b = blk[L::kQs + (el & 15)];
+        const int uu = int((el < 16 ? (b & 0x0f) : (b >> 4)) | (((qh >> el) & 1u) << 4));
+        // value d * u + m (two fp32 operations) or d * (u - 16)
+        r[e] = L::kAffine ? __fadd_rn(__fmul_rn(d, float(uu)), mn) : __fmul_rn(d, float(uu - 16));
       }
+      reinterpret_cast<float4 *>(dst)[i] = make_float4(r[0], r[1], r[2], r[3]);
+    } else {
+      int q[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (TYPE == kTypeQ4_0) {
+          const int el = 4 * j + e;
+          const uint8_t b = blk[2 + (el & 15)];
+          q[e] = int(el < 16 ? (b & 0x0f) : (b >> 4)) - 8;
+        } else {
+          q[e] = int(static_cast<int8_t>(blk[2 + 4 * j + e]));
+        }
+      }
+      float4 o;
+      o.x = __fmul_rn(d, float(q[0]));
+      o.y = __fmul_rn(d, float(q[1]));
+      o.z = __fmul_rn(d, float(q[2]));
+      o.w = __fmul_rn(d, float(q[3]));
+      reinterpret_cast<float4 *>(dst)[i] = o;
     }
-    float4 o;
-    o.x = __fmul_rn(d, float(q[0]));
-    o.y = __fmul_rn(d, float(q[1]));
-    o.z = __fmul_rn(d, float(q[2]));
-    o.w = __fmul_rn(d, float(q[3]));
-    reinterpret_cast<float4 *>(dst)[i] = o;
   }
 }
 
@@ -236,6 +258,10 @@ cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const flo
 template <bool ROT>
 cudaError_t launch_q_typed(int type, const float *src, uint8_t *dst, int64_t n_blocks, const float *bias,
                            int64_t bias_period, cudaStream_t stream) {
+  // legacy types: no bias and no rotation (rejected by the ABI layer)
+  if (type == kTypeQ4_1) return launch_q<kTypeQ4_1, false, false>(src, dst, n_blocks, nullptr, 1, stream);
+  if (type == kTypeQ5_0) return launch_q<kTypeQ5_0, false, false>(src, dst, n_blocks, nullptr, 1, stream);
+  if (type == kTypeQ5_1) return launch_q<kTypeQ5_1, false, false>(src, dst, n_blocks, nullptr, 1, stream);
   if (type == kTypeQ4_0)
     return bias ? launch_q<kTypeQ4_0, true, ROT>(src, dst, n_blocks, bias, bias_period, stream)
                 : launch_q<kTypeQ4_0, false, ROT>(src, dst, n_blocks, nullptr, 1, stream);
@@ -329,10 +355,13 @@ cudaError_t launch_dequantize_rows(int type, const uint8_t *blocks, float *dst, 
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
   const int64_t grid = min((n_blocks * 8 + 255) / 256, int64_t(di->sm_count) * 8);
-  if (type == kTypeQ4_0)
-    k_dequantize_rows<kTypeQ4_0><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks);
-  else
-    k_dequantize_rows<kTypeQ8_0><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks);
+  switch (type) {
+    case kTypeQ4_0: k_dequantize_rows<kTypeQ4_0><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks); break;
+    case kTypeQ4_1: k_dequantize_rows<kTypeQ4_1><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks); break;
+    case kTypeQ5_0: k_dequantize_rows<kTypeQ5_0><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks); break;
+    case kTypeQ5_1: k_dequantize_rows<kTypeQ5_1><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks); break;
+    default: k_dequantize_rows<kTypeQ8_0><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks); break;
+  }
   return cudaGetLastError();
 }
 

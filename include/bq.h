@@ -48,6 +48,26 @@ extern "C" {
 
 #define BQ_TYPE_Q4_0 2
 #define BQ_TYPE_Q8_0 8
+/* Legacy types with a fifth bit and/or a minimum: one FP16 scale per 32
+ * weights, and "_1" adds a minimum ("05. llama.cpp…", §量化类型; q4_1, q5_0
+ * and q5_1 are also K/V cache types, §KV Cache 类型与 Flash Attention). The
+ * pages give no layout; this library's reading (little endian):
+ *   Q4_1: 20 bytes = { fp16 d, fp16 m, 16 nibble bytes }        5.0 bits/weight
+ *   Q5_0: 22 bytes = { fp16 d, u32 qh, 16 nibble bytes }        5.5
+ *   Q5_1: 24 bytes = { fp16 d, fp16 m, u32 qh, 16 nibble bytes } 6.0
+ * The low 4 bits of code j sit as in Q4_0 (low nibble of byte j for j < 16,
+ * high nibble of byte j - 16), bit 4 of code j is bit j of qh; codes are
+ * unsigned u. Q5_0: d = amax / 15, u = clamp(rn(x / d), -16, 15) + 16, value
+ * d * (u - 16). Q4_1 / Q5_1: m = min x, d = (max x - m) / (2^bits - 1),
+ * u = clamp(rn((x - m) / d), 0, 2^bits - 1) with the stored fp16 d and m,
+ * value d * u + m (fp32 product, then fp32 sum); a block whose scale or
+ * minimum overflows binary16 is outside the supported range. Taken by bq_quantize_rows,
+ * bq_dequantize_rows, bq_gemv / bq_gemv_multi (the minimum adds
+ * m_w * d_x * sum(qx) per block) and bq_kv_quantize (without a bias or a
+ * rotation); the other entry points answer BQ_ERR_UNSUPPORTED. */
+#define BQ_TYPE_Q4_1 3
+#define BQ_TYPE_Q5_0 6
+#define BQ_TYPE_Q5_1 7
 
 #define BQ_OK 0
 #define BQ_ERR_INVALID_ARG (-1) /* null pointer, negative size, aliasing */

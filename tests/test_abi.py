@@ -65,11 +65,27 @@ def _err(L):
 
 
 def test_unknown_type_is_unsupported(L):
-    assert L.bq_quantize_rows(3, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4096), 1, 32) == UNSUPPORTED
+    assert L.bq_quantize_rows(4, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4096), 1, 32) == UNSUPPORTED
     assert "unknown type" in _err(L)
-    assert L.bq_gemv(7, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 32) == UNSUPPORTED
+    assert L.bq_gemv(5, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 32) == UNSUPPORTED
     assert L.bq_kv_quantize(0, ctypes.c_void_p(FAKE), None, ctypes.c_void_p(FAKE + 4096), 1, 1, 32) == UNSUPPORTED
     assert L.bq_block_dots(1, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1, 32) == UNSUPPORTED
+
+
+def test_legacy_types_where_they_are_not_taken(L):
+    """Q4_1 (3), Q5_0 (6), Q5_1 (7) have block sizes and go through the row
+    quantizer, the GEMV and the KV write; the other entry points refuse them."""
+    p = ctypes.c_void_p
+    assert [L.bq_block_bytes(t) for t in (3, 6, 7)] == [20, 22, 24]
+    for t in (3, 6, 7):
+        assert L.bq_block_dots(t, p(FAKE), p(FAKE), p(FAKE), 1, 32) == UNSUPPORTED
+        assert L.bq_gemm(t, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 4, 64) == UNSUPPORTED
+        assert L.bq_gemv_workspace_size(t, 4096) == 0
+        assert L.bq_kv_quantize(t, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 2, 2, 64) == UNSUPPORTED  # bias
+        assert L.bq_kv_quantize_basis(t, p(FAKE), None, 1, 1, p(FAKE + (2 << 20)), 2, 2, 64) == UNSUPPORTED  # rotation
+        assert L.bq_attn_decode(t, 8, p(FAKE), p(FAKE), p(FAKE), p(FAKE + (1 << 24)), 10, 8, 8, 64,
+                                ctypes.c_float(0.1)) == UNSUPPORTED
+        assert L.bq_quantize_rows(t, p(FAKE), p(FAKE + 4096), 2, 33) == SHAPE  # taken: a shape error, not a type error
 
 
 def test_row_length_must_be_multiple_of_32(L):

@@ -761,3 +761,64 @@ def test_attn_decode_rotated_matches_oracle(bq, orc, dev, T, H, NKV, D, kt, vt):
     err = np.abs(o.astype(np.float64) - o_ref)
     tol = _attn_tol(mag, smax, D)
     assert np.all(err <= tol), f"worst err/tol {float((err / tol).max()):.3g}"
+
+
+# ---------------------------------------------- legacy types Q4_1, Q5_0, Q5_1 --
+
+LEGACY_TYPES = [3, 6, 7]
+
+
+def _legacy_input(rng, rows, cols):
+    """Normal, heavy-tailed, offset, constant and near-tie blocks, with the
+    quantizer's adversarial blocks and their negations and rescalings."""
+    from block_quantized_weight_row_gb300 import inputs
+    x = np.concatenate([rng.normal(size=(rows, cols)), rng.standard_t(2, size=(rows, cols)) * 10,
+                        rng.normal(size=(rows, cols)) * 1e-3 + 40.0]).astype(np.float32)
+    adv = inputs.adversarial_blocks().numpy()
+    adv = np.concatenate([adv, -adv, adv * 1e-4 + 1.0, adv * 3e3, np.full_like(adv, 2.5)]).reshape(-1)
+    pad = (-adv.size) % cols
+    adv = np.concatenate([adv, np.zeros(pad, np.float32)]).reshape(-1, cols)
+    # near ties: x = m + (k + 0.5) d for scales d exactly representable in binary16
+    k = rng.integers(0, 15, size=(rows, cols)).astype(np.float32)
+    d = np.float32(2.0) ** rng.integers(-8, 4, size=(rows, 1)).astype(np.float32)
+    ties = (k + np.float32(0.5)) * d - np.float32(3.0) * d
+    ties[:, ::32] = np.float32(-3.0) * d[:, :1]   # every block's minimum ...
+    ties[:, 1::32] = np.float32(12.0) * d[:, :1]  # ... and maximum: Q4_1's scale is d exactly, ties exact
+    return np.concatenate([x, adv.astype(np.float32), ties.astype(np.float32)])
+
+
+@pytest.mark.parametrize("t", LEGACY_TYPES)
+def test_legacy_quantize_and_dequantize_bit_exact(bq, orc, dev, t):
+    x = _legacy_input(np.random.default_rng(t), 200, 256)
+    got = _np(bq.quantize_rows(t, torch.from_numpy(x).to(dev)))
+    ref = orc.quantize_rows(t, x)
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} bytes differ"
+    deq = _np(bq.dequantize_rows(t, torch.from_numpy(ref).to(dev), 256))
+    dref = orc.dequantize_rows(t, ref, 256)
+    # bit for bit, except that NaN payloads (a block whose scale overflowed
+    # binary16: outside the supported range) only need to be NaN on both sides
+    bad = np.argwhere((deq.view(np.uint32) != dref.view(np.uint32)) & ~(np.isnan(deq) & np.isnan(dref)))
+    assert len(bad) == 0, (f"{len(bad)} values differ; first {bad[:3].tolist()}: gpu {deq[tuple(bad[0])]!r} "
+                           f"oracle {dref[tuple(bad[0])]!r}, block bytes "
+                           f"{ref[bad[0][0], (bad[0][1] // 32) * ref.shape[1] // 8:][:ref.shape[1] // 8].tolist()}")
+
+
+@pytest.mark.parametrize("t", LEGACY_TYPES)
+@pytest.mark.parametrize("M,K", [(1, 32), (37, 96), (4096, 4096), (11008, 4096), (300, 11008)])
+def test_legacy_gemv_matches_oracle(bq, orc, dev, t, M, K):
+    rng = np.random.default_rng(M + K + t)
+    W = (rng.normal(size=(M, K)) * 0.02 + rng.uniform(-0.01, 0.01, size=(M, 1))).astype(np.float32)
+    x = rng.normal(size=K).astype(np.float32)
+    wb = orc.quantize_rows(t, W)
+    y = _np(bq.gemv(t, torch.from_numpy(wb).to(dev), torch.from_numpy(x).to(dev), M, K))
+    y_ref, mag = orc.gemv(t, wb, x, M, K, with_mag=True)
+    _check_float(y, y_ref, mag, f"type {t}")
+
+
+@pytest.mark.parametrize("t", LEGACY_TYPES)
+def test_legacy_kv_write_bit_exact(bq, orc, dev, t):
+    rng = np.random.default_rng(30 + t)
+    T, NKV, D = 1000, 8, 128
+    K = (rng.normal(size=(T, NKV, D)) + rng.uniform(-2, 2, size=(NKV, D))).astype(np.float32)
+    got = _np(bq.kv_quantize(t, torch.from_numpy(K).to(dev), None))
+    assert np.array_equal(got, orc.kv_quantize(t, K, None, T, NKV, D))
