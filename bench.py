@@ -593,6 +593,32 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
     del layers, g, g2, g3, g4, qs, outs
     torch.cuda.empty_cache()
 
+    # legacy weight types: GEMV on 11008 x 4096 matrices, 8 distinct matrices
+    # per type (beyond L2) launched back to back in one graph
+    M_, K_ = 11008, 4096
+    x_ = inputs.activation(K_, inputs.seed_of("legacy-gemv", 0, 0), device=dev)
+    y_ = torch.empty(M_, dtype=torch.float32, device=dev)
+    leg = {}
+    for name, t in (("Q4_0", bq.Q4_0), ("Q4_1", bq.Q4_1), ("Q5_0", bq.Q5_0), ("Q5_1", bq.Q5_1)):
+        mats = [bq.quantize_rows(t, inputs.weight(M_, K_, inputs.seed_of("legacy-gemv", 1, i), device=dev))
+                for i in range(8)]
+
+        def leg_step():
+            for w in mats:
+                bq.gemv(t, w, x_, M_, K_, out=y_)
+        gl = capture(leg_step, stream)
+        msl = max_over_ranks(time_graph(gl, stream, 20, 3), dist)
+        byts = 8 * mats[0].numel()
+        leg[name] = {"GB/s": round(aggregate_rate(byts, world, msl * 1e-3) / 1e9, 1),
+                     "us_per_launch": round(msl * 1e3 / 8, 2),
+                     "hbm_frac_of_measured": round(byts / (msl * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        del mats, gl
+    out["gemv_legacy_types"] = {"metric": "decode GEMV GB/s of weights per type (11008 x 4096, back to back)",
+                                "value": leg["Q5_0"]["GB/s"], "unit": "GB/s", "per_type": leg,
+                                "kernel": "k_gemv_tma (+ k_gemv_prep) for every type: Q4_0 for comparison",
+                                "l2": "8 distinct matrices per type, 203-282 MB: beyond L2"}
+    torch.cuda.empty_cache()
+
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps
     q = build_decode_step("qwen3-0.6b-decode", dev, bq, inputs)
     g = capture(lambda: run_step(q, bq, True), stream)

@@ -201,7 +201,7 @@ size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K) {
 }
 
 size_t bq_gemv_workspace_size(int type, int64_t K) {
-  if (!core_type(type)) return 0;  // legacy types quantize x inside the GEMV
+  if (!block_bytes(type)) return 0;
   return gemv_workspace_bytes(K);
 }
 

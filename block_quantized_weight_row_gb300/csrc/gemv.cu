@@ -439,34 +439,14 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
   return cudaSuccess;
 }
 
-// Legacy weight types: the generic kernel, one launch per matrix (every CTA
-// quantizes x into shared memory).
-template <int TYPE>
-cudaError_t launch_legacy(int n, const uint8_t *const *W, float *const *y, const int64_t *M, const float *x,
-                          int64_t K, cudaStream_t stream) {
-  cudaError_t err;
-  const DeviceInfo *di = device_info(&err);
-  if (!di) return err;
-  const int nb = int(K / kQK);
-  const size_t smem = size_t(nb) * 40;
-  cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_generic<TYPE>), int(smem));
-  if (e != cudaSuccess) return e;
-  for (int i = 0; i < n; ++i) {
-    if (M[i] == 0) continue;
-    const int64_t grid = std::min((M[i] + 7) / 8, int64_t(di->sm_count) * 4);
-    k_gemv_generic<TYPE><<<unsigned(grid), 256, smem, stream>>>(W[i], x, y[i], int(M[i]), int(K));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
 
 }  // namespace
 
 cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *y, const int64_t *M,
                         const float *x, int64_t K, uint32_t *rec_ws, cudaStream_t stream) {
-  if (type == kTypeQ4_1) return launch_legacy<kTypeQ4_1>(n, W, y, M, x, K, stream);
-  if (type == kTypeQ5_0) return launch_legacy<kTypeQ5_0>(n, W, y, M, x, K, stream);
-  if (type == kTypeQ5_1) return launch_legacy<kTypeQ5_1>(n, W, y, M, x, K, stream);
+  if (type == kTypeQ4_1) return launch_typed<kTypeQ4_1>(n, W, y, M, x, K, rec_ws, stream);
+  if (type == kTypeQ5_0) return launch_typed<kTypeQ5_0>(n, W, y, M, x, K, rec_ws, stream);
+  if (type == kTypeQ5_1) return launch_typed<kTypeQ5_1>(n, W, y, M, x, K, rec_ws, stream);
   if (type == kTypeQ4_0) return launch_typed<kTypeQ4_0>(n, W, y, M, x, K, rec_ws, stream);
   return launch_typed<kTypeQ8_0>(n, W, y, M, x, K, rec_ws, stream);
 }

@@ -72,6 +72,55 @@ template <>
 struct GroupWords<kTypeQ8_0> {
   static constexpr int kWords = 68;  // 272 bytes
 };
+template <>
+struct GroupWords<kTypeQ4_1> {
+  static constexpr int kWords = 40;  // 160 bytes
+};
+template <>
+struct GroupWords<kTypeQ5_0> {
+  static constexpr int kWords = 44;  // 176 bytes
+};
+template <>
+struct GroupWords<kTypeQ5_1> {
+  static constexpr int kWords = 48;  // 192 bytes
+};
+
+// One legacy block's term, block jb of a group (its bytes start at 4-byte
+// word w0, plus 2 bytes when `odd`): d_w d_x sum_j u_j qx_j (minus 16 d_w d_x
+// sum qx for Q5_0) plus, for the "_1" types, m_w d_x sum qx.
+template <int TYPE>
+__device__ __forceinline__ float legacy_group_block(const uint32_t *w, int w0, bool odd, const uint32_t *xw,
+                                                    float dx, int xsum, float acc) {
+  using L = Legacy<TYPE>;
+  uint32_t dbits, mbits = 0, qh = 0, qs[4];
+  if (!odd) {
+    // Q4_1 / Q5_1: d, m in word w0, then qh (Q5_1) and the nibbles word aligned;
+    // Q5_0: d in the low half of w0, qh and the nibbles 2 bytes off
+    dbits = w[w0] & 0xffffu;
+    if (L::kAffine) {
+      mbits = w[w0] >> 16;
+      const int q0 = w0 + (L::kQh >= 0 ? 2 : 1);
+      if (L::kQh >= 0) qh = w[w0 + 1];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qs[i] = w[q0 + i];
+    } else {
+      qh = __funnelshift_r(w[w0], w[w0 + 1], 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qs[i] = __funnelshift_r(w[w0 + 1 + i], w[w0 + 2 + i], 16);
+    }
+  } else {
+    // Q5_0 at 2 mod 4: d in the high half of w0, qh and the nibbles word aligned
+    dbits = w[w0] >> 16;
+    qh = w[w0 + 1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) qs[i] = w[w0 + 2 + i];
+  }
+  int sumi = legacy_sumu<TYPE>(qs, qh, xw);
+  if (!L::kAffine) sumi -= 16 * xsum;
+  acc = __fmaf_rn(__fmul_rn(half_bits_to_float(dbits), dx), float(sumi), acc);
+  if (L::kAffine) acc = __fmaf_rn(__fmul_rn(half_bits_to_float(mbits), dx), float(xsum), acc);
+  return acc;
+}
 
 // Sum of the 8 block terms of one group. w: the group's bytes as words (the
 // group starts 16-byte aligned, block jb starts at byte BB*jb).
@@ -82,7 +131,7 @@ __device__ __forceinline__ float group_terms(const uint32_t *w, const uint32_t *
   const uint4 dx1 = *reinterpret_cast<const uint4 *>(xr + 68);
   const uint32_t dxs[8] = {dx0.x, dx0.y, dx0.z, dx0.w, dx1.x, dx1.y, dx1.z, dx1.w};
   uint32_t sxs[8];
-  if (TYPE == kTypeQ4_0) {
+  if (TYPE == kTypeQ4_0 || Legacy<TYPE>::kIs) {
     const uint4 s0 = *reinterpret_cast<const uint4 *>(xr + 72);
     const uint4 s1 = *reinterpret_cast<const uint4 *>(xr + 76);
     sxs[0] = s0.x; sxs[1] = s0.y; sxs[2] = s0.z; sxs[3] = s0.w;
@@ -90,6 +139,15 @@ __device__ __forceinline__ float group_terms(const uint32_t *w, const uint32_t *
   }
 #pragma unroll
   for (int jb = 0; jb < 8; ++jb) {
+    if constexpr (Legacy<TYPE>::kIs) {
+      const uint4 xa = *reinterpret_cast<const uint4 *>(xr + 8 * jb);
+      const uint4 xb = *reinterpret_cast<const uint4 *>(xr + 8 * jb + 4);
+      const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      const int byte0 = BB * jb;
+      acc = legacy_group_block<TYPE>(w, byte0 >> 2, (byte0 & 3) != 0, xw, __uint_as_float(dxs[jb]), int(sxs[jb]),
+                                     acc);
+      continue;
+    }
     constexpr int kQW = (TYPE == kTypeQ4_0) ? 4 : 8;  // code words per block
     uint32_t q[kQW];
     uint32_t dbits;

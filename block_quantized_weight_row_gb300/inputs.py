@@ -17,6 +17,8 @@ Workloads (shapes and distributions of the pages' models):
   kv         per layer K, V [32768][8][128]; K = mu + N(0, 1) with
              mu[h][c] ~ U(-2, 2) per layer, V ~ N(0, 1); a separate 4096-token
              calibration draw of K gives the bias; 28 layers
+  legacy     W 11008 x 4096 ~ N(0, 0.02) (8 draws), x ~ N(0, 1): the GEMV in
+             Q4_1, Q5_0, Q5_1 (and Q4_0 for comparison)
 Seeds: workload index * 1000 + layer * 10 + matrix index.
 """
 from dataclasses import dataclass
@@ -43,6 +45,8 @@ WORKLOADS = {
     "7b-decode": dict(index=2, layers=32, layer=LLAMA_7B_LAYER),
     "prefill-q8_0": dict(index=3, tokens=512, shapes=((4096, 4096), (11008, 4096), (4096, 11008))),
     "kv-write": dict(index=4, layers=28, tokens=32768, kv_heads=8, head_dim=128, calib_tokens=4096),
+    # the 7B gate/up shape in every legacy weight type
+    "legacy-gemv": dict(index=5, shape=(11008, 4096)),
 }
 
 
