@@ -41,6 +41,8 @@ def lib():
 def _declare(L):
     i64, vp, i = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     L.oracle_block_bytes.argtypes = [i]
+    L.oracle_block_values.argtypes = [i]
+    L.oracle_block_values.restype = i64
     L.oracle_block_bytes.restype = i64
     L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
     L.oracle_f32_to_f16.restype = ctypes.c_uint16
@@ -103,6 +105,11 @@ def block_bytes(t):
     return int(lib().oracle_block_bytes(t))
 
 
+def block_values(t):
+    """values per block: 32, or 256 for the k-quant super-blocks"""
+    return int(lib().oracle_block_values(t))
+
+
 def f32_to_f16_bits(v: float) -> int:
     return int(lib().oracle_f32_to_f16(float(v)))
 
@@ -121,14 +128,14 @@ def quantize_rows(t, x):
     if x.ndim == 1:
         x = x.reshape(1, -1)
     R, C = x.shape
-    out = np.zeros((R, (C // QK) * block_bytes(t)), dtype=np.uint8)
+    out = np.zeros((R, (C // block_values(t)) * block_bytes(t)), dtype=np.uint8)
     _check(lib().oracle_quantize_rows(t, _p(x), _p(out), R, C), "quantize_rows")
     return out
 
 
 def dequantize_rows(t, blocks, cols):
     blocks = _u8(blocks)
-    R = blocks.size // ((cols // QK) * block_bytes(t)) if cols else 0
+    R = blocks.size // ((cols // block_values(t)) * block_bytes(t)) if cols else 0
     out = np.zeros((R, cols), dtype=np.float32)
     _check(lib().oracle_dequantize_rows(t, _p(blocks), _p(out), R, cols), "dequantize_rows")
     return out

@@ -35,6 +35,10 @@
  *          Q5_1, Q8_0) group 32 weights with one FP16 scale, and the "_1"
  *          types add a minimum; §KV Cache 类型与 Flash Attention lists q4_1,
  *          q5_0 and q5_1 among the K/V cache types.
+ *   [KQ]   05. llama.cpp…, §量化类型, format table — k-quants use super-blocks
+ *          of 256 weights holding 8 sub-blocks of 32, whose scales are
+ *          themselves quantized with 6 bits; the Llama-3-8B table prints Q8_0
+ *          7.96 GiB and Q6_K 6.14 GiB for the same model.
  *   [ROT]  lpnh.cn KV-cache article, §三步上手 (third step) — a quantized K
  *          cache whose head dimension is a multiple of 64 is Hadamard-rotated;
  *          the mean-centering bias must be measured in the same basis as the
@@ -78,6 +82,32 @@
  *      d16 * u + m16 (fp32 product, then fp32 sum).
  *   R19 the dot of an affine weight block with a Q8_0 block is
  *      d_w d_x sum_j u_j qx_j + m_w d_x sum_j qx_j, summed in fp64 (R6).
+ *   R20 Q4_K layout (PARITY UNPINNED beyond its size): 144 bytes per 256
+ *      weights = { fp16 d, fp16 dmin, 12 bytes holding 6-bit sub-block
+ *      scales sc[0..7] then 6-bit sub-block minimums mn[0..7] as one
+ *      little-endian 96-bit stream (value k at bits 6k..6k+5), 128 bytes of
+ *      4-bit codes: sub-block j in bytes 16j..16j+15, Q4_0's nibble order };
+ *      value (d sc_j) u - (dmin mn_j), the two sub-block factors rounded to
+ *      fp32, then the fp32 product and the fp32 difference.
+ *   R21 Q4_K quantizer (PARITY UNPINNED; the pages give no algorithm): per
+ *      sub-block m_j = max(0, -min x), s_j = (max x + m_j) / 15; d = max_j s_j
+ *      / 63, dmin = max_j m_j / 63 (fp32, stored fp16); sc_j = clamp(rn(s_j
+ *      / d16), 0, 63), mn_j = clamp(rn(m_j / dmin16), 0, 63); S_j = fp32(d16
+ *      sc_j), M_j = fp32(dmin16 mn_j); u = clamp(rn((x + M_j) / S_j), 0,
+ *      15), one fp32 sum and one fp32 division (S_j = 0 gives u = 0).
+ *   R22 Q6_K layout (size pinned by the Llama-3-8B table): 210 bytes per
+ *      256 weights = { 128 bytes ql: byte i holds the low 4 bits of code i
+ *      (low nibble) and of code i + 128 (high nibble); 64 bytes qh: byte i
+ *      holds the top 2 bits of codes i, i+64, i+128, i+192 at bits 0-1, 2-3,
+ *      4-5, 6-7; int8 scales sc[0..15] of the 16 sub-blocks of 16; fp16 d };
+ *      value fp32(d sc_k) * (u - 32), u in 0..63.
+ *   R23 Q6_K quantizer (PARITY UNPINNED): per sub-block of 16 s_k = amax /
+ *      31; d = max_k s_k / 127; sc_k = clamp(rn(s_k / d16), -128, 127);
+ *      S_k = fp32(d16 sc_k); u = clamp(rn(x / S_k), -32, 31) + 32.
+ *   R24 k-quant GEMV: x quantized to Q8_0 as always (R5); a super-block
+ *      meets the 8 x blocks under it; the terms d_x S sum(u qx) (and
+ *      - d_x M sum(qx) for Q4_K; Q6_K: S per half of an x block, codes u - 32)
+ *      are exact and summed in fp64 (R6).
  *   R15 the rotated values decide integer codes, so they are computed in the
  *      kernel's precision: the fast Walsh-Hadamard butterflies in fp32,
  *      stages of span 1, 2, 4, 8, 16, 32, each pair (a, b) -> (a + b, a - b),
@@ -102,8 +132,18 @@
 
 #define QK 32
 
+static int is_kquant(int type) { return type == ORACLE_TYPE_Q4_K || type == ORACLE_TYPE_Q6_K; }
+
+int64_t oracle_block_values(int type)
+{
+    if (is_kquant(type)) return 256; /* [KQ] super-blocks of 256 weights */
+    return oracle_block_bytes(type) ? QK : 0;
+}
+
 int64_t oracle_block_bytes(int type)
 {
+    if (type == ORACLE_TYPE_Q4_K) return 2 + 2 + 12 + 128; /* R20 */
+    if (type == ORACLE_TYPE_Q6_K) return 128 + 64 + 16 + 2; /* R22 */
     /* [FMT4] 18 bytes per 32 Q4_0 weights; [FMT8] 2-byte scale + 32 int8. */
     if (type == ORACLE_TYPE_Q4_0) return 2 + QK / 2;
     if (type == ORACLE_TYPE_Q8_0) return 2 + QK;
@@ -348,10 +388,209 @@ static void block_codes(int type, const uint8_t *blk, int *q)
     }
 }
 
+/* ---- k-quant super-blocks: R20-R24 ---- */
+
+static int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+static void q4k_get(const uint8_t *blk, int *sc, int *mn)
+{
+    uint64_t lo = 0, hi = 0; /* the 96-bit stream in bytes 4..15 */
+    for (int k = 0; k < 8; k++) lo |= (uint64_t)blk[4 + k] << (8 * k);
+    for (int k = 0; k < 4; k++) hi |= (uint64_t)blk[12 + k] << (8 * k);
+    for (int k = 0; k < 16; k++) {
+        int bit = 6 * k, v;
+        if (bit + 6 <= 64) v = (int)((lo >> bit) & 63u);
+        else if (bit >= 64) v = (int)((hi >> (bit - 64)) & 63u);
+        else v = (int)(((lo >> bit) | (hi << (64 - bit))) & 63u);
+        if (k < 8) sc[k] = v; else mn[k - 8] = v;
+    }
+}
+
+static void q4k_put(uint8_t *blk, const int *sc, const int *mn)
+{
+    uint64_t lo = 0, hi = 0;
+    for (int k = 0; k < 16; k++) {
+        uint64_t v = (uint64_t)(k < 8 ? sc[k] : mn[k - 8]);
+        int bit = 6 * k;
+        if (bit + 6 <= 64) lo |= v << bit;
+        else if (bit >= 64) hi |= v << (bit - 64);
+        else { lo |= v << bit; hi |= v >> (64 - bit); }
+    }
+    for (int k = 0; k < 8; k++) blk[4 + k] = (uint8_t)(lo >> (8 * k));
+    for (int k = 0; k < 4; k++) blk[12 + k] = (uint8_t)(hi >> (8 * k));
+}
+
+/* sub-block factors of a Q4_K super-block, as the fp32 values R20 uses */
+static void q4k_factors(const uint8_t *blk, float *S, float *M)
+{
+    int sc[8], mn[8];
+    q4k_get(blk, sc, mn);
+    float d = oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+    float dm = oracle_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
+    for (int j = 0; j < 8; j++) {
+        S[j] = d * (float)sc[j];
+        M[j] = dm * (float)mn[j];
+    }
+}
+
+static void quantize_q4k(const float *x, uint8_t *out)
+{
+    float s[8], m[8], smax = 0.0f, mmax = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        float lo = x[32 * j], hi = x[32 * j];
+        for (int i = 1; i < 32; i++) {
+            if (x[32 * j + i] < lo) lo = x[32 * j + i];
+            if (x[32 * j + i] > hi) hi = x[32 * j + i];
+        }
+        m[j] = lo < 0.0f ? -lo : 0.0f;
+        s[j] = (hi + m[j]) / 15.0f;
+        if (s[j] > smax) smax = s[j];
+        if (m[j] > mmax) mmax = m[j];
+    }
+    uint16_t d16 = oracle_f32_to_f16(smax / 63.0f), dm16 = oracle_f32_to_f16(mmax / 63.0f);
+    float d = oracle_f16_to_f32(d16), dm = oracle_f16_to_f32(dm16);
+    int sc[8], mn[8];
+    for (int j = 0; j < 8; j++) {
+        sc[j] = d == 0.0f ? 0 : clampi((int)oracle_round_half_even(s[j] / d), 0, 63);
+        mn[j] = dm == 0.0f ? 0 : clampi((int)oracle_round_half_even(m[j] / dm), 0, 63);
+    }
+    put_u16(out, d16);
+    put_u16(out + 2, dm16);
+    q4k_put(out, sc, mn);
+    for (int j = 0; j < 8; j++) {
+        float S = d * (float)sc[j], M = dm * (float)mn[j];
+        int u[32];
+        for (int i = 0; i < 32; i++)
+            u[i] = S == 0.0f ? 0 : clampi((int)oracle_round_half_even((x[32 * j + i] + M) / S), 0, 15);
+        for (int i = 0; i < 16; i++)
+            out[16 + 16 * j + i] = (uint8_t)((unsigned)u[i] | ((unsigned)u[i + 16] << 4));
+    }
+}
+
+static void q4k_codes(const uint8_t *blk, int *u) /* 256 codes, R20 */
+{
+    for (int j = 0; j < 8; j++)
+        for (int i = 0; i < 16; i++) {
+            u[32 * j + i] = blk[16 + 16 * j + i] & 15;
+            u[32 * j + i + 16] = blk[16 + 16 * j + i] >> 4;
+        }
+}
+
+static float q6k_scale(const uint8_t *blk) { return oracle_f16_to_f32((uint16_t)(blk[208] | (blk[209] << 8))); }
+
+static void q6k_codes(const uint8_t *blk, int *u) /* 256 codes 0..63, R22 */
+{
+    for (int i = 0; i < 256; i++) {
+        int lo = (i < 128) ? (blk[i] & 15) : (blk[i - 128] >> 4);
+        int hi = (blk[128 + (i & 63)] >> (2 * (i >> 6))) & 3;
+        u[i] = lo | (hi << 4);
+    }
+}
+
+static void quantize_q6k(const float *x, uint8_t *out)
+{
+    float s[16], smax = 0.0f;
+    for (int k = 0; k < 16; k++) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; i++)
+            if (fabsf(x[16 * k + i]) > amax) amax = fabsf(x[16 * k + i]);
+        s[k] = amax / 31.0f;
+        if (s[k] > smax) smax = s[k];
+    }
+    uint16_t d16 = oracle_f32_to_f16(smax / 127.0f);
+    float d = oracle_f16_to_f32(d16);
+    int u[256];
+    memset(out, 0, 210);
+    for (int k = 0; k < 16; k++) {
+        int sc = d == 0.0f ? 0 : clampi((int)oracle_round_half_even(s[k] / d), -128, 127);
+        out[192 + k] = (uint8_t)(int8_t)sc;
+        float S = d * (float)sc;
+        for (int i = 0; i < 16; i++)
+            u[16 * k + i] = (S == 0.0f ? 0 : clampi((int)oracle_round_half_even(x[16 * k + i] / S), -32, 31)) + 32;
+    }
+    for (int i = 0; i < 128; i++)
+        out[i] = (uint8_t)((unsigned)(u[i] & 15) | ((unsigned)(u[i + 128] & 15) << 4));
+    for (int i = 0; i < 256; i++)
+        out[128 + (i & 63)] |= (uint8_t)(((unsigned)u[i] >> 4) << (2 * (i >> 6)));
+    put_u16(out + 208, d16);
+}
+
+static void dequantize_kquant(int type, const uint8_t *blk, float *dst)
+{
+    int u[256];
+    if (type == ORACLE_TYPE_Q4_K) {
+        float S[8], M[8];
+        q4k_factors(blk, S, M);
+        q4k_codes(blk, u);
+        for (int i = 0; i < 256; i++)
+            dst[i] = S[i / 32] * (float)u[i] - M[i / 32]; /* R20: fp32 product, then difference */
+    } else {
+        float d = q6k_scale(blk);
+        q6k_codes(blk, u);
+        for (int i = 0; i < 256; i++)
+            dst[i] = (d * (float)(int8_t)blk[192 + i / 16]) * (float)(u[i] - 32); /* R22 */
+    }
+}
+
+/* R24: one super-block against the 8 Q8_0 blocks of x under it */
+static void kquant_dot(int type, const uint8_t *wb, const uint8_t *xb8, double *acc, double *macc)
+{
+    int u[256], qx[QK];
+    int64_t bx = oracle_block_bytes(ORACLE_TYPE_Q8_0);
+    if (type == ORACLE_TYPE_Q4_K) {
+        float S[8], M[8];
+        q4k_factors(wb, S, M);
+        q4k_codes(wb, u);
+        for (int j = 0; j < 8; j++) {
+            const uint8_t *xb = xb8 + j * bx;
+            block_codes(ORACLE_TYPE_Q8_0, xb, qx);
+            int64_t su = 0, sx = 0;
+            for (int i = 0; i < 32; i++) {
+                su += (int64_t)u[32 * j + i] * qx[i];
+                sx += qx[i];
+            }
+            double dx = (double)block_scale(xb);
+            double t1 = dx * (double)S[j] * (double)su, t2 = -dx * (double)M[j] * (double)sx;
+            *acc += t1 + t2;
+            *macc += fabs(t1) + fabs(t2);
+        }
+    } else {
+        float d = q6k_scale(wb);
+        q6k_codes(wb, u);
+        for (int j = 0; j < 8; j++) {
+            const uint8_t *xb = xb8 + j * bx;
+            block_codes(ORACLE_TYPE_Q8_0, xb, qx);
+            double dx = (double)block_scale(xb);
+            for (int h = 0; h < 2; h++) {
+                int k = 2 * j + h;
+                int64_t si = 0;
+                for (int i = 0; i < 16; i++)
+                    si += (int64_t)(u[16 * k + i] - 32) * qx[16 * h + i];
+                double t = dx * (double)(d * (float)(int8_t)wb[192 + k]) * (double)si;
+                *acc += t;
+                *macc += fabs(t);
+            }
+        }
+    }
+}
+
 int oracle_quantize_rows(int type, const float *src, uint8_t *dst,
                          int64_t n_rows, int64_t n_cols)
 {
     int64_t bb = oracle_block_bytes(type);
+    if (is_kquant(type)) {
+        if (n_cols % 256 != 0 || n_rows < 0 || n_cols < 0)
+            return -1;
+        int64_t ns = n_cols / 256;
+        for (int64_t r = 0; r < n_rows; r++)
+            for (int64_t b = 0; b < ns; b++) {
+                if (type == ORACLE_TYPE_Q4_K)
+                    quantize_q4k(src + r * n_cols + b * 256, dst + (r * ns + b) * bb);
+                else
+                    quantize_q6k(src + r * n_cols + b * 256, dst + (r * ns + b) * bb);
+            }
+        return 0;
+    }
     if (bb == 0 || n_cols % QK != 0 || n_rows < 0 || n_cols < 0)
         return -1;
     int64_t nb = n_cols / QK;
@@ -365,6 +604,15 @@ int oracle_dequantize_rows(int type, const uint8_t *blocks, float *dst,
                            int64_t n_rows, int64_t n_cols)
 {
     int64_t bb = oracle_block_bytes(type);
+    if (is_kquant(type)) {
+        if (n_cols % 256 != 0 || n_rows < 0 || n_cols < 0)
+            return -1;
+        int64_t ns = n_cols / 256;
+        for (int64_t r = 0; r < n_rows; r++)
+            for (int64_t b = 0; b < ns; b++)
+                dequantize_kquant(type, blocks + (r * ns + b) * bb, dst + r * n_cols + b * 256);
+        return 0;
+    }
     if (bb == 0 || n_cols % QK != 0 || n_rows < 0 || n_cols < 0)
         return -1;
     int64_t nb = n_cols / QK;
@@ -400,7 +648,7 @@ int oracle_block_dots(int w_type, const uint8_t *w_blocks, const uint8_t *xq_blo
 {
     int64_t bw = oracle_block_bytes(w_type);
     int64_t bx = oracle_block_bytes(ORACLE_TYPE_Q8_0);
-    if (bw == 0 || K % QK != 0 || M < 0 || K < 0)
+    if (bw == 0 || is_kquant(w_type) || K % QK != 0 || M < 0 || K < 0)
         return -1;
     int64_t nb = K / QK;
     for (int64_t m = 0; m < M; m++)
@@ -416,6 +664,14 @@ static void dot_row(int w_type, const uint8_t *wrow, const uint8_t *xrow, int64_
     int64_t bw = oracle_block_bytes(w_type);
     int64_t bx = oracle_block_bytes(ORACLE_TYPE_Q8_0);
     double acc = 0.0, macc = 0.0;
+    if (is_kquant(w_type)) { /* nb counts 32-blocks of x; a super-block spans 8 */
+        for (int64_t b = 0; b < nb / 8; b++)
+            kquant_dot(w_type, wrow + b * bw, xrow + 8 * b * bx, &acc, &macc);
+        *y = (float)acc;
+        if (mag)
+            *mag = macc;
+        return;
+    }
     for (int64_t b = 0; b < nb; b++) {
         const uint8_t *wb = wrow + b * bw;
         const uint8_t *xb = xrow + b * bx;
@@ -442,16 +698,16 @@ static void dot_row(int w_type, const uint8_t *wrow, const uint8_t *xrow, int64_
 int oracle_gemv(int w_type, const uint8_t *w_blocks, const float *x, float *y,
                 double *mag, int64_t M, int64_t K)
 {
-    int64_t bw = oracle_block_bytes(w_type);
-    if (bw == 0 || K % QK != 0 || M < 0 || K < 0)
+    int64_t bw = oracle_block_bytes(w_type), bv = oracle_block_values(w_type);
+    if (bw == 0 || K % bv != 0 || M < 0 || K < 0)
         return -1;
-    int64_t nb = K / QK;
+    int64_t nb = K / QK, row_bytes = K / bv * bw;
     uint8_t *xq = (uint8_t *)malloc((size_t)(nb * oracle_block_bytes(ORACLE_TYPE_Q8_0)) + 1);
     if (!xq)
         return -3;
     oracle_quantize_rows(ORACLE_TYPE_Q8_0, x, xq, 1, K); /* R5 */
     for (int64_t m = 0; m < M; m++)
-        dot_row(w_type, w_blocks + m * nb * bw, xq, nb, y + m, mag ? mag + m : NULL);
+        dot_row(w_type, w_blocks + m * row_bytes, xq, nb, y + m, mag ? mag + m : NULL);
     free(xq);
     return 0;
 }
@@ -459,18 +715,18 @@ int oracle_gemv(int w_type, const uint8_t *w_blocks, const float *x, float *y,
 int oracle_gemm(int w_type, const uint8_t *w_blocks, const float *X, float *Y,
                 double *mag, int64_t M, int64_t N, int64_t K)
 {
-    int64_t bw = oracle_block_bytes(w_type);
+    int64_t bw = oracle_block_bytes(w_type), bv = oracle_block_values(w_type);
     int64_t bx = oracle_block_bytes(ORACLE_TYPE_Q8_0);
-    if (bw == 0 || K % QK != 0 || M < 0 || N < 0 || K < 0)
+    if (bw == 0 || K % bv != 0 || M < 0 || N < 0 || K < 0)
         return -1;
-    int64_t nb = K / QK;
+    int64_t nb = K / QK, row_bytes = K / bv * bw;
     uint8_t *xq = (uint8_t *)malloc((size_t)(N * nb * bx) + 1);
     if (!xq)
         return -3;
     oracle_quantize_rows(ORACLE_TYPE_Q8_0, X, xq, N, K); /* R5, row by row */
     for (int64_t n = 0; n < N; n++)
         for (int64_t m = 0; m < M; m++)
-            dot_row(w_type, w_blocks + m * nb * bw, xq + n * nb * bx, nb,
+            dot_row(w_type, w_blocks + m * row_bytes, xq + n * nb * bx, nb,
                     Y + n * M + m, mag ? mag + n * M + m : NULL);
     free(xq);
     return 0;
@@ -501,7 +757,7 @@ int oracle_kv_quantize_basis(int type, const float *rows, const float *bias, int
                              uint8_t *dst, int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim)
 {
     int64_t bb = oracle_block_bytes(type);
-    if (bb == 0 || head_dim % QK != 0 || n_tokens < 0 || n_kv_heads < 0 || head_dim < 0)
+    if (bb == 0 || is_kquant(type) || head_dim % QK != 0 || n_tokens < 0 || n_kv_heads < 0 || head_dim < 0)
         return -1;
     if (basis != ORACLE_BASIS_PLAIN && basis != ORACLE_BASIS_HADAMARD64)
         return -1;
@@ -583,7 +839,7 @@ int oracle_attn_decode_basis(int k_type, int v_type, int k_basis, const float *q
     if (bk == 0 || bv == 0 || head_dim <= 0 || head_dim % QK != 0 || n_tokens < 1 || n_kv_heads < 1 ||
         n_heads < n_kv_heads || n_heads % n_kv_heads != 0)
         return -1;
-    if (is_legacy(k_type) || is_legacy(v_type)) /* attention reads Q4_0 / Q8_0 caches */
+    if (is_legacy(k_type) || is_legacy(v_type) || is_kquant(k_type) || is_kquant(v_type)) /* Q4_0 / Q8_0 caches */
         return -1;
     if (k_basis != ORACLE_BASIS_PLAIN && (k_basis != ORACLE_BASIS_HADAMARD64 || head_dim % 64 != 0))
         return -1;

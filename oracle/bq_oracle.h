@@ -44,13 +44,20 @@ extern "C" {
 #define ORACLE_TYPE_Q4_1 3
 #define ORACLE_TYPE_Q5_0 6
 #define ORACLE_TYPE_Q5_1 7
+/* k-quants: super-blocks of 256 weights (05. llama.cpp…, §量化类型); layouts
+ * in bq_oracle.c (R20-R23); rows must hold a multiple of 256 values. Taken
+ * by quantize/dequantize and the GEMV/GEMM dots only. */
+#define ORACLE_TYPE_Q4_K 12
+#define ORACLE_TYPE_Q6_K 14
 
 /* bases of a K cache: plain, or Hadamard-rotated per 64 channels */
 #define ORACLE_BASIS_PLAIN 0
 #define ORACLE_BASIS_HADAMARD64 1
 
-/* bytes of one 32-value block of the given type, 0 for an unknown type */
+/* bytes of one block of the given type, 0 for an unknown type; a block is
+ * oracle_block_values(type) values: 32, or 256 for the k-quants */
 int64_t oracle_block_bytes(int type);
+int64_t oracle_block_values(int type);
 
 /* IEEE binary16 <-> binary32 (round to nearest, ties to even). */
 uint16_t oracle_f32_to_f16(float f);

@@ -44,6 +44,16 @@ MUTANTS = [
     ("legacy_5bit_range_15", "const int umax = (1 << legacy_bits(type)) - 1;", "const int umax = 15;"),
     ("legacy_unrounded_min", "float ds = oracle_f16_to_f32(d16), ms = oracle_f16_to_f32(m16);",
      "float ds = oracle_f16_to_f32(d16), ms = mn;"),
+    ("q4k_min_added", "dst[i] = S[i / 32] * (float)u[i] - M[i / 32];", "dst[i] = S[i / 32] * (float)u[i] + M[i / 32];"),
+    ("q4k_scale_stream_shifted", "int bit = 6 * k, v;", "int bit = 6 * k + 1, v;"),
+    ("q6k_offset_31", "dst[i] = (d * (float)(int8_t)blk[192 + i / 16]) * (float)(u[i] - 32);",
+     "dst[i] = (d * (float)(int8_t)blk[192 + i / 16]) * (float)(u[i] - 31);"),
+    ("q6k_high_bits_order", "int hi = (blk[128 + (i & 63)] >> (2 * (i >> 6))) & 3;",
+     "int hi = (blk[128 + (i >> 2)] >> (2 * (i & 3))) & 3;"),
+    ("kquant_gemv_min_term_dropped", "double t1 = dx * (double)S[j] * (double)su, t2 = -dx * (double)M[j] * (double)sx;",
+     "double t1 = dx * (double)S[j] * (double)su, t2 = 0.0 * (double)M[j] * (double)sx;"),
+    ("kquant_row_stride", "int64_t nb = K / QK, row_bytes = K / bv * bw;\n    uint8_t *xq = (uint8_t *)malloc((size_t)(nb * oracle_block_bytes(ORACLE_TYPE_Q8_0)) + 1);",
+     "int64_t nb = K / QK, row_bytes = nb * bw;\n    uint8_t *xq = (uint8_t *)malloc((size_t)(nb * oracle_block_bytes(ORACLE_TYPE_Q8_0)) + 1);"),
     ("hadamard_scaled_by_1_64", "v[j] = v[j] * 0.125f;", "v[j] = v[j] * 0.015625f;"),
     ("hadamard_no_minus", "v[j + h] = a - b;", "v[j + h] = a + b;"),
     ("hadamard_32_point", "for (int h = 1; h < 64; h *= 2)", "for (int h = 1; h < 32; h *= 2)"),

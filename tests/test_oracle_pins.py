@@ -725,3 +725,109 @@ def test_legacy_kv_write_is_the_row_quantizer(orc, name):
                           orc.quantize_rows(t, K.reshape(-1, D)).reshape(-1))
     with pytest.raises(ValueError):
         orc.kv_quantize(t, K, np.zeros((NKV, D), np.float32), T, NKV, D)  # bias: Q4_0 only
+
+
+# ------------------------------------------------ k-quants ([KQ], R20-R24) --
+
+Q4_K, Q6_K = 12, 14
+
+
+def _parse_q4k(blocks):
+    """The test's own reading of R20: d, dmin, sc[8], mn[8], u[256] per super-block."""
+    b = np.asarray(blocks, np.uint8).reshape(-1, 144)
+    d = b[:, 0:2].copy().view(np.float16).astype(np.float32)[:, 0]
+    dm = b[:, 2:4].copy().view(np.float16).astype(np.float32)[:, 0]
+    bits = np.unpackbits(b[:, 4:16], axis=1, bitorder="little")  # 96 bits, value k at 6k..6k+5
+    vals = (bits.reshape(-1, 16, 6) * (1 << np.arange(6))).sum(axis=2)
+    nib = b[:, 16:].reshape(-1, 8, 16).astype(np.int64)
+    u = np.concatenate([nib & 15, nib >> 4], axis=2).reshape(-1, 256)
+    return d, dm, vals[:, :8], vals[:, 8:], u
+
+
+def _parse_q6k(blocks):
+    """The test's own reading of R22: d, sc[16] (int8), u[256] (0..63)."""
+    b = np.asarray(blocks, np.uint8).reshape(-1, 210)
+    ql, qh = b[:, :128].astype(np.int64), b[:, 128:192].astype(np.int64)
+    lo = np.concatenate([ql & 15, ql >> 4], axis=1)
+    hi = np.concatenate([(qh >> (2 * k)) & 3 for k in range(4)], axis=1)
+    sc = b[:, 192:208].view(np.int8).astype(np.int64)
+    d = b[:, 208:210].copy().view(np.float16).astype(np.float32)[:, 0]
+    return d, sc, lo | (hi << 4)
+
+
+def test_kquant_sizes(orc):
+    s = golden.sizes()
+    # Q4_K: 256 4-bit codes + 8 sub-blocks x (6-bit scale + 6-bit minimum) + two fp16 super-scales
+    assert orc.block_bytes(Q4_K) == 256 * 4 // 8 + 8 * 12 // 8 + 4 == 144 and orc.block_values(Q4_K) == 256
+    # Q6_K: 210 bytes per 256 is the layout whose size ratio to Q8_0 matches the pages'
+    # Llama-3-8B file sizes; 8 sub-blocks with 6-bit scales (200 bytes) would not
+    ratio = s["llama3_8b_q6_k_gib"] / s["llama3_8b_q8_0_gib"]
+    bpw = lambda t: orc.block_bytes(t) * 8 / orc.block_values(t)
+    assert abs(bpw(Q6_K) / bpw(Q8) - ratio) < 0.005 * ratio
+    assert abs((200 * 8 / 256) / bpw(Q8) - ratio) > 0.03 * ratio
+
+
+@pytest.mark.parametrize("t", [Q4_K, Q6_K])
+def test_kquant_values_from_an_independent_parse(orc, t):
+    rng = np.random.default_rng(40 + t)
+    x = np.concatenate([rng.normal(size=(20, 512)), rng.standard_t(3, size=(20, 512)) * 5,
+                        rng.uniform(0.5, 3.0, size=(20, 512))]).astype(np.float32)
+    q = orc.quantize_rows(t, x)
+    deq = orc.dequantize_rows(t, q, 512).reshape(-1, 256)
+    if t == Q4_K:
+        d, dm, sc, mn, u = _parse_q4k(q)
+        S = (d[:, None] * sc.astype(np.float32)).astype(np.float32)
+        M = (dm[:, None] * mn.astype(np.float32)).astype(np.float32)
+        ref = np.repeat(S, 32, axis=1) * u.astype(np.float32) - np.repeat(M, 32, axis=1)
+        assert sc.max() <= 63 and mn.max() <= 63
+    else:
+        d, sc, u = _parse_q6k(q)
+        S = (d[:, None] * sc.astype(np.float32)).astype(np.float32)
+        ref = np.repeat(S, 16, axis=1) * (u - 32).astype(np.float32)
+    assert np.array_equal(deq.view(np.uint32), ref.astype(np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("t", [Q4_K, Q6_K])
+def test_kquant_round_trip_bound(orc, t):
+    """Half a sub-block step, plus what quantizing the sub-block factors to
+    6 (Q4_K) or 8 (Q6_K) bits against fp16 super-scales can cost."""
+    rng = np.random.default_rng(50 + t)
+    x = np.concatenate([rng.normal(size=(40, 256)), rng.standard_t(2, size=(40, 256)),
+                        rng.normal(size=(40, 256)) * 0.01 + 2.0]).astype(np.float32)
+    q = orc.quantize_rows(t, x)
+    err = np.abs(orc.dequantize_rows(t, q, 256).astype(np.float64) - x)
+    ulp = 4 * np.abs(x).max(1, keepdims=True) * 2.0 ** -23
+    if t == Q4_K:
+        d, dm, sc, mn, u = _parse_q4k(q)
+        S = np.repeat(d[:, None].astype(np.float64) * sc, 32, axis=1)
+        bound = S / 2 + 15 * np.repeat(d[:, None], 256, 1) / 2 * 1.001 + np.repeat(dm[:, None], 256, 1) / 2 * 1.001
+    else:
+        d, sc, u = _parse_q6k(q)
+        S = np.repeat(d[:, None].astype(np.float64) * sc, 16, axis=1)
+        bound = S / 2 + 31 * np.repeat(d[:, None], 256, 1) / 2 * 1.001
+    assert np.all(err <= bound + ulp)
+
+
+@pytest.mark.parametrize("t", [Q4_K, Q6_K])
+def test_kquant_gemv_is_the_brute_force_product(orc, t):
+    rng = np.random.default_rng(60 + t)
+    M, K = 5, 768
+    W = (rng.normal(size=(M, K)) * 0.02).astype(np.float32)
+    x = rng.normal(size=K).astype(np.float32)
+    wb = orc.quantize_rows(t, W)
+    y, mag = orc.gemv(t, wb, x, M, K, with_mag=True)
+    if t == Q4_K:
+        d, dm, sc, mn, u = _parse_q4k(wb)
+        S = (d[:, None] * sc.astype(np.float32)).astype(np.float64)
+        Mn = (dm[:, None] * mn.astype(np.float32)).astype(np.float64)
+        vw = np.repeat(S, 32, axis=1) * u - np.repeat(Mn, 32, axis=1)
+    else:
+        d, sc, u = _parse_q6k(wb)
+        S = (d[:, None] * sc.astype(np.float32)).astype(np.float64)
+        vw = np.repeat(S, 16, axis=1) * (u - 32)
+    xq = orc.quantize_rows(Q8, x[None])[0].reshape(-1, 34)
+    vx = (xq[:, 0:2].copy().view(np.float16).astype(np.float64) * xq[:, 2:].view(np.int8)).reshape(-1)
+    ref = vw.reshape(M, K) @ vx
+    assert np.allclose(y.astype(np.float64), ref, rtol=1e-6, atol=1e-9 * mag.max())
+    with pytest.raises(ValueError):
+        orc.gemv(t, wb, x[:640], M, 640)  # a row must hold whole super-blocks
