@@ -599,7 +599,8 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
     x_ = inputs.activation(K_, inputs.seed_of("legacy-gemv", 0, 0), device=dev)
     y_ = torch.empty(M_, dtype=torch.float32, device=dev)
     leg = {}
-    for name, t in (("Q4_0", bq.Q4_0), ("Q4_1", bq.Q4_1), ("Q5_0", bq.Q5_0), ("Q5_1", bq.Q5_1)):
+    for name, t in (("Q4_0", bq.Q4_0), ("Q4_1", bq.Q4_1), ("Q5_0", bq.Q5_0), ("Q5_1", bq.Q5_1),
+                    ("Q4_K", bq.Q4_K), ("Q6_K", bq.Q6_K)):
         mats = [bq.quantize_rows(t, inputs.weight(M_, K_, inputs.seed_of("legacy-gemv", 1, i), device=dev))
                 for i in range(8)]
 
@@ -615,8 +616,9 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
         del mats, gl
     out["gemv_legacy_types"] = {"metric": "decode GEMV GB/s of weights per type (11008 x 4096, back to back)",
                                 "value": leg["Q5_0"]["GB/s"], "unit": "GB/s", "per_type": leg,
-                                "kernel": "k_gemv_tma (+ k_gemv_prep) for every type: Q4_0 for comparison",
-                                "l2": "8 distinct matrices per type, 203-282 MB: beyond L2"}
+                                "kernel": "k_gemv_tma (+ k_gemv_prep) for every type but Q6_K (k_gemv_generic); "
+                                          "Q4_0 for comparison",
+                                "l2": "8 distinct matrices per type, 203-370 MB: beyond L2"}
     torch.cuda.empty_cache()
 
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps

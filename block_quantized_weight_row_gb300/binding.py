@@ -14,6 +14,7 @@ import torch
 Q4_0 = 2
 Q8_0 = 8
 Q4_1, Q5_0, Q5_1 = 3, 6, 7
+Q4_K, Q6_K = 12, 14
 QK = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +74,7 @@ def lib():
         "bq_gemv_workspace_size": ([i, i64], sz),
         "bq_last_error": ([], ctypes.c_char_p),
         "bq_block_bytes": ([i], i),
+        "bq_block_values": ([i], i),
         "bq_device_status": ([], i),
         "bq_version": ([], i),
         "bq_set_spin_limit": ([i64], i),
@@ -131,6 +133,10 @@ def block_bytes(t: int) -> int:
     return int(lib().bq_block_bytes(t))
 
 
+def block_values(t: int) -> int:
+    return int(lib().bq_block_values(t))
+
+
 def quantize_rows(t: int, src: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
     """fp32 (rows, cols) -> uint8 (rows, cols/32*block_bytes)."""
     _cuda(src, "src")
@@ -139,7 +145,8 @@ def quantize_rows(t: int, src: torch.Tensor, out: torch.Tensor | None = None) ->
     x = src.reshape(-1, src.shape[-1]) if src.dim() != 2 else src
     R, C = x.shape
     if out is None:
-        out = torch.empty((R, (C // QK) * max(block_bytes(t), 1)), dtype=torch.uint8, device=src.device)
+        out = torch.empty((R, (C // max(block_values(t), 1)) * max(block_bytes(t), 1)), dtype=torch.uint8,
+                          device=src.device)
     L = _prep(src.device)
     _check(L.bq_quantize_rows(t, _ptr(x), _ptr(out), R, C), "bq_quantize_rows")
     return out
@@ -147,7 +154,7 @@ def quantize_rows(t: int, src: torch.Tensor, out: torch.Tensor | None = None) ->
 
 def dequantize_rows(t: int, blocks: torch.Tensor, cols: int, out: torch.Tensor | None = None) -> torch.Tensor:
     _cuda(blocks, "blocks")
-    nbr = (cols // QK) * block_bytes(t)
+    nbr = (cols // max(block_values(t), 1)) * block_bytes(t)
     R = blocks.numel() // nbr if nbr else 0
     if out is None:
         out = torch.empty((R, cols), dtype=torch.float32, device=blocks.device)

@@ -56,8 +56,13 @@ int block_bytes(int type) {
   if (type == BQ_TYPE_Q4_1) return Fmt<kTypeQ4_1>::kBytes;
   if (type == BQ_TYPE_Q5_0) return Fmt<kTypeQ5_0>::kBytes;
   if (type == BQ_TYPE_Q5_1) return Fmt<kTypeQ5_1>::kBytes;
+  if (type == BQ_TYPE_Q4_K) return Fmt<kTypeQ4_K>::kBytes;
+  if (type == BQ_TYPE_Q6_K) return Fmt<kTypeQ6_K>::kBytes;
   return 0;
 }
+
+// values per block: 256 for the k-quant super-blocks, else 32
+int block_values(int type) { return (type == BQ_TYPE_Q4_K || type == BQ_TYPE_Q6_K) ? kQK_K : kQK; }
 
 // Q4_0 / Q8_0: the types every entry point takes
 bool core_type(int type) { return type == BQ_TYPE_Q4_0 || type == BQ_TYPE_Q8_0; }
@@ -168,6 +173,7 @@ extern "C" {
 int bq_version(void) { return (0 << 16) | 1; }
 
 int bq_block_bytes(int type) { return block_bytes(type); }
+int bq_block_values(int type) { return block_bytes(type) ? block_values(type) : 0; }
 
 const char *bq_last_error(void) { return t_error.c_str(); }
 
@@ -229,14 +235,15 @@ int bq_quantize_rows(int type, const float *src, void *dst, int64_t n_rows, int6
   const int bb = block_bytes(type);
   if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_quantize_rows: unknown type %d", type);
   if (!sizes_ok(n_rows, n_cols)) return fail(BQ_ERR_INVALID_ARG, "bq_quantize_rows: bad sizes %lld x %lld", (long long)n_rows, (long long)n_cols);
-  if (n_cols % kQK) return fail(BQ_ERR_SHAPE, "bq_quantize_rows: n_cols %lld is not a multiple of 32", (long long)n_cols);
-  const int64_t n_blocks = n_rows * (n_cols / kQK);
+  const int bv = block_values(type);
+  if (n_cols % bv) return fail(BQ_ERR_SHAPE, "bq_quantize_rows: n_cols %lld is not a multiple of %d", (long long)n_cols, bv);
+  const int64_t n_blocks = n_rows * (n_cols / bv);
   if (n_blocks == 0) return ok();
   if (!src || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_quantize_rows: null pointer");
   if (!aligned(src, 16) || !aligned(dst, 16)) return fail(BQ_ERR_ALIGN, "bq_quantize_rows: src and dst must be 16-byte aligned");
-  if (overlap(src, size_t(n_blocks) * 128, dst, size_t(n_blocks) * bb))
+  if (overlap(src, size_t(n_blocks) * bv * 4, dst, size_t(n_blocks) * bb))
     return fail(BQ_ERR_INVALID_ARG, "bq_quantize_rows: src and dst overlap");
-  cudaError_t e = launch_quantize_rows(type, src, static_cast<uint8_t *>(dst), n_blocks, n_cols / kQK, nullptr, 1, t_stream);
+  cudaError_t e = launch_quantize_rows(type, src, static_cast<uint8_t *>(dst), n_blocks, n_cols / bv, nullptr, 1, t_stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_quantize_rows launch");
 }
 
@@ -244,12 +251,13 @@ int bq_dequantize_rows(int type, const void *blocks, float *dst, int64_t n_rows,
   const int bb = block_bytes(type);
   if (!bb) return fail(BQ_ERR_UNSUPPORTED, "bq_dequantize_rows: unknown type %d", type);
   if (!sizes_ok(n_rows, n_cols)) return fail(BQ_ERR_INVALID_ARG, "bq_dequantize_rows: bad sizes");
-  if (n_cols % kQK) return fail(BQ_ERR_SHAPE, "bq_dequantize_rows: n_cols %lld is not a multiple of 32", (long long)n_cols);
-  const int64_t n_blocks = n_rows * (n_cols / kQK);
+  const int bv = block_values(type);
+  if (n_cols % bv) return fail(BQ_ERR_SHAPE, "bq_dequantize_rows: n_cols %lld is not a multiple of %d", (long long)n_cols, bv);
+  const int64_t n_blocks = n_rows * (n_cols / bv);
   if (n_blocks == 0) return ok();
   if (!blocks || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_dequantize_rows: null pointer");
   if (!aligned(blocks, 16) || !aligned(dst, 16)) return fail(BQ_ERR_ALIGN, "bq_dequantize_rows: pointers must be 16-byte aligned");
-  if (overlap(blocks, size_t(n_blocks) * bb, dst, size_t(n_blocks) * 128))
+  if (overlap(blocks, size_t(n_blocks) * bb, dst, size_t(n_blocks) * bv * 4))
     return fail(BQ_ERR_INVALID_ARG, "bq_dequantize_rows: blocks and dst overlap");
   cudaError_t e = launch_dequantize_rows(type, static_cast<const uint8_t *>(blocks), dst, n_blocks, t_stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_dequantize_rows launch");
@@ -262,7 +270,8 @@ int bq_gemv_multi(int type, int n, const void *const *W, float *const *y, const 
   if (n < 1 || n > BQ_GEMV_MAX_MATS) return fail(BQ_ERR_SHAPE, "bq_gemv_multi: n %d not in 1..%d", n, BQ_GEMV_MAX_MATS);
   if (!W || !y || !M) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_multi: null array");
   if (K < 0) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: negative K");
-  if (K % kQK) return fail(BQ_ERR_SHAPE, "bq_gemv: K %lld is not a multiple of 32", (long long)K);
+  const int bv = block_values(type);
+  if (K % bv) return fail(BQ_ERR_SHAPE, "bq_gemv: K %lld is not a multiple of %d", (long long)K, bv);
   if (K > BQ_GEMV_MAX_K) return fail(BQ_ERR_SHAPE, "bq_gemv: K %lld exceeds %d", (long long)K, BQ_GEMV_MAX_K);
   int64_t total = 0;
   for (int i = 0; i < n; ++i) {
@@ -280,7 +289,7 @@ int bq_gemv_multi(int type, int n, const void *const *W, float *const *y, const 
     if (overlap(y[i], ybytes, x, size_t(K) * 4)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv: y overlaps x");
     for (int j = 0; j < n; ++j) {
       if (M[j] == 0) continue;
-      if (overlap(y[i], ybytes, W[j], size_t(M[j]) * size_t(K / kQK) * bb))
+      if (overlap(y[i], ybytes, W[j], size_t(M[j]) * size_t(K / bv) * bb))
         return fail(BQ_ERR_INVALID_ARG, "bq_gemv: y overlaps a weight matrix");
       if (j != i && overlap(y[i], ybytes, y[j], size_t(M[j]) * 4))
         return fail(BQ_ERR_INVALID_ARG, "bq_gemv_multi: outputs overlap");
@@ -499,6 +508,8 @@ int bq_kv_quantize_basis(int type, const float *rows, const float *bias, int bia
                 (long long)head_dim);
   if (basis == BQ_BASIS_HADAMARD64 && !core_type(type))
     return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: the rotated basis takes Q4_0 or Q8_0");
+  if (block_values(type) != kQK)
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_quantize: k-quants are weight types, not cache types");
   const int64_t n_blocks = n_tokens * n_kv_heads * (head_dim / kQK);
   if (n_blocks == 0) return ok();
   if (!rows || !dst) return fail(BQ_ERR_INVALID_ARG, "bq_kv_quantize: null pointer");

@@ -19,6 +19,10 @@ constexpr int kTypeQ8_0 = 8;
 constexpr int kTypeQ4_1 = 3;
 constexpr int kTypeQ5_0 = 6;
 constexpr int kTypeQ5_1 = 7;
+// k-quants: super-blocks of 256 weights (below)
+constexpr int kTypeQ4_K = 12;
+constexpr int kTypeQ6_K = 14;
+constexpr int kQK_K = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
 // error bits of the device error word
@@ -38,6 +42,11 @@ template <> struct Fmt<kTypeQ8_0> {
 template <> struct Fmt<kTypeQ4_1> { static constexpr int kBytes = 20; };  // d, m, 16 nibble bytes
 template <> struct Fmt<kTypeQ5_0> { static constexpr int kBytes = 22; };  // d, qh, 16 nibble bytes
 template <> struct Fmt<kTypeQ5_1> { static constexpr int kBytes = 24; };  // d, m, qh, 16 nibble bytes
+template <> struct Fmt<kTypeQ4_K> { static constexpr int kBytes = 144; };  // per 256: d, dmin, 12 scale bytes, 128 code bytes
+template <> struct Fmt<kTypeQ6_K> { static constexpr int kBytes = 210; };  // per 256: ql 128, qh 64, 16 int8 scales, d
+template <int TYPE> struct IsKQuant { static constexpr bool kV = false; };
+template <> struct IsKQuant<kTypeQ4_K> { static constexpr bool kV = true; };
+template <> struct IsKQuant<kTypeQ6_K> { static constexpr bool kV = true; };
 
 // Legacy types ("05. llama.cpp：从 GGUF 文件到本地推理服务", §量化类型: legacy
 // formats keep one FP16 scale per 32 weights, and "_1" adds a minimum). The
@@ -401,6 +410,30 @@ __device__ __forceinline__ int legacy_sumu(const uint32_t (&qs)[4], uint32_t qh,
     hi = dp4a_us(b, xw[4 + i], hi);  // codes 16+4i..
   }
   return lo + hi;
+}
+
+// --------------------------------------------------------------- k-quants --
+// Super-blocks of 256 weights with 8 sub-blocks of 32 whose scales are
+// quantized to 6 bits ("05. llama.cpp：从 GGUF 文件到本地推理服务", §量化类型).
+// Layouts (this library's reading):
+//   Q4_K, 144 bytes: fp16 d, fp16 dmin, 12 bytes = sub-block scales sc[0..7]
+//     then minimums mn[0..7] as 6-bit values of a little-endian 96-bit
+//     stream (value k at bits 6k..6k+5), then 128 bytes: sub-block j's 32
+//     4-bit codes in bytes 16j..16j+15 (low nibble code i, high nibble
+//     code i + 16); value fp32(d sc_j) * u - fp32(dmin mn_j).
+//   Q6_K, 210 bytes: 128 bytes ql (byte i: low 4 bits of code i, then of
+//     code i + 128), 64 bytes qh (byte i: top 2 bits of codes i, i+64,
+//     i+128, i+192 at bits 0-1, 2-3, 4-5, 6-7), 16 int8 scales of the
+//     sub-blocks of 16, fp16 d; value fp32(d sc_k) * (u - 32).
+
+// 6-bit value k (0..15) of the Q4_K scale stream held in words w1..w3
+// (stream bits 0..95 = w1 | w2 << 32 | w3 << 64).
+__device__ __forceinline__ int q4k_stream(uint32_t w1, uint32_t w2, uint32_t w3, int k) {
+  const int bit = 6 * k;
+  const uint64_t lo = uint64_t(w1) | (uint64_t(w2) << 32);
+  if (bit + 6 <= 64) return int((lo >> bit) & 63u);
+  if (bit >= 64) return int((w3 >> (bit - 64)) & 63u);
+  return int(((lo >> bit) | (uint64_t(w3) << (64 - bit))) & 63u);
 }
 
 // ------------------------------------------------------ packed fp32 pairs --

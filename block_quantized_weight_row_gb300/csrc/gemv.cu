@@ -270,10 +270,54 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row_bytes = int64_t(nb) * BB;
+  // k-quants: BB bytes per super-block of 8 x blocks
+  const int64_t row_bytes = IsKQuant<TYPE>::kV ? int64_t(nb / 8) * BB : int64_t(nb) * BB;
   for (int64_t m = int64_t(blockIdx.x) * 8 + warp; m < M; m += int64_t(gridDim.x) * 8) {
     float acc = 0.0f;
     for (int b = lane; b < nb; b += 32) {
+      if constexpr (IsKQuant<TYPE>::kV) {
+        // x block b meets sub-block(s) of super-block b / 8
+        const uint8_t *sbp = W + m * row_bytes + int64_t(b >> 3) * BB;
+        const int j = b & 7;
+        const uint32_t *xw = xs + 8 * b;
+        const float dx = __uint_as_float(xs[8 * nb + b]);
+        const int xsum = int(xs[9 * nb + b]);
+        if constexpr (TYPE == kTypeQ4_K) {
+          const uint4 h = *reinterpret_cast<const uint4 *>(sbp);
+          const float S = __fmul_rn(half_bits_to_float(h.x & 0xffffu), float(q4k_stream(h.y, h.z, h.w, j)));
+          const float Mn = __fmul_rn(half_bits_to_float(h.x >> 16), float(q4k_stream(h.y, h.z, h.w, 8 + j)));
+          const uint4 c = *reinterpret_cast<const uint4 *>(sbp + 16 + 16 * j);
+          const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+          int su = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            su = dp4a_us(cw[i] & 0x0f0f0f0fu, xw[i], su);
+            su = dp4a_us((cw[i] >> 4) & 0x0f0f0f0fu, xw[4 + i], su);
+          }
+          acc = __fmaf_rn(__fmul_rn(S, dx), float(su), acc);
+          acc = __fmaf_rn(__fmul_rn(Mn, dx), float(-xsum), acc);
+        } else {
+          const uint16_t *b16 = reinterpret_cast<const uint16_t *>(sbp);  // 2-byte aligned
+          const float d = half_bits_to_float(b16[104]);
+          const int lo_off = (32 * j) & 127, hi_off = 128 + ((32 * j) & 63);
+          const uint32_t lsh = j < 4 ? 0u : 4u, hsh = 2u * uint32_t(j >> 1);
+          int su[2] = {0, 0}, sx[2] = {0, 0};
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            const uint32_t ql = uint32_t(b16[lo_off / 2 + 2 * w]) | (uint32_t(b16[lo_off / 2 + 2 * w + 1]) << 16);
+            const uint32_t qh = uint32_t(b16[hi_off / 2 + 2 * w]) | (uint32_t(b16[hi_off / 2 + 2 * w + 1]) << 16);
+            const uint32_t u = ((ql >> lsh) & 0x0f0f0f0fu) | (((qh >> hsh) & 0x03030303u) << 4);
+            su[w >> 2] = dp4a_us(u, xw[w], su[w >> 2]);
+            sx[w >> 2] = dp4a_ss(0x01010101u, xw[w], sx[w >> 2]);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float S = __fmul_rn(d, float(int8_t(sbp[192 + 2 * j + h])));
+            acc = __fmaf_rn(__fmul_rn(S, dx), float(su[h] - 32 * sx[h]), acc);
+          }
+        }
+        continue;
+      }
       const uint16_t *blk = reinterpret_cast<const uint16_t *>(W + m * row_bytes + int64_t(b) * BB);
       if constexpr (Legacy<TYPE>::kIs) {
         // d_w d_x sum_j u_j qx_j (- 16 d_w d_x sum qx for Q5_0) + m_w d_x sum qx
@@ -323,11 +367,12 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
   if (!di) return err;
   constexpr int BB = Fmt<TYPE>::kBytes;
   const int nb = int(K / kQK);
-  const int row_bytes = nb * BB;
+  const int row_bytes = IsKQuant<TYPE>::kV ? (nb / 8) * BB : nb * BB;  // k-quants: BB per 8 x blocks
   int64_t M_total = 0;
   for (int i = 0; i < n; ++i) M_total += M[i];
   if (M_total == 0) return cudaSuccess;
 
+  if constexpr (TYPE != kTypeQ6_K) {  // Q6_K: 210-byte super-blocks, generic kernel only
   if (K % 256 == 0) {
     GemvArgs a{};
     int acc_rows = 0;
@@ -426,6 +471,7 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
       return cudaLaunchKernelEx(&cfg, k_gemv_tma<TYPE>, a);
     }
   }
+  }
   // any K % 32 == 0 (or rows too long for two stages): one plain launch per matrix
   const size_t smem = size_t(nb) * 40;  // 32 code bytes + scale + sum per block
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_generic<TYPE>), int(smem));
@@ -444,6 +490,8 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
 
 cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *y, const int64_t *M,
                         const float *x, int64_t K, uint32_t *rec_ws, cudaStream_t stream) {
+  if (type == kTypeQ4_K) return launch_typed<kTypeQ4_K>(n, W, y, M, x, K, rec_ws, stream);
+  if (type == kTypeQ6_K) return launch_typed<kTypeQ6_K>(n, W, y, M, x, K, rec_ws, stream);
   if (type == kTypeQ4_1) return launch_typed<kTypeQ4_1>(n, W, y, M, x, K, rec_ws, stream);
   if (type == kTypeQ5_0) return launch_typed<kTypeQ5_0>(n, W, y, M, x, K, rec_ws, stream);
   if (type == kTypeQ5_1) return launch_typed<kTypeQ5_1>(n, W, y, M, x, K, rec_ws, stream);

@@ -73,6 +73,10 @@ struct GroupWords<kTypeQ8_0> {
   static constexpr int kWords = 68;  // 272 bytes
 };
 template <>
+struct GroupWords<kTypeQ4_K> {
+  static constexpr int kWords = 36;  // one 144-byte super-block
+};
+template <>
 struct GroupWords<kTypeQ4_1> {
   static constexpr int kWords = 40;  // 160 bytes
 };
@@ -131,12 +135,34 @@ __device__ __forceinline__ float group_terms(const uint32_t *w, const uint32_t *
   const uint4 dx1 = *reinterpret_cast<const uint4 *>(xr + 68);
   const uint32_t dxs[8] = {dx0.x, dx0.y, dx0.z, dx0.w, dx1.x, dx1.y, dx1.z, dx1.w};
   uint32_t sxs[8];
-  if (TYPE == kTypeQ4_0 || Legacy<TYPE>::kIs) {
+  if (TYPE == kTypeQ4_0 || TYPE == kTypeQ4_K || Legacy<TYPE>::kIs) {
     const uint4 s0 = *reinterpret_cast<const uint4 *>(xr + 72);
     const uint4 s1 = *reinterpret_cast<const uint4 *>(xr + 76);
     sxs[0] = s0.x; sxs[1] = s0.y; sxs[2] = s0.z; sxs[3] = s0.w;
     sxs[4] = s1.x; sxs[5] = s1.y; sxs[6] = s1.z; sxs[7] = s1.w;
   }
+  if constexpr (TYPE == kTypeQ4_K) {
+    // the group is one super-block: w[0] = d | dmin, w[1..3] the 6-bit
+    // scale/minimum stream, sub-block j's codes in w[4 + 4j .. 7 + 4j]
+    const float d = half_bits_to_float(w[0] & 0xffffu), dm = half_bits_to_float(w[0] >> 16);
+#pragma unroll
+    for (int jb = 0; jb < 8; ++jb) {
+      const uint4 xa = *reinterpret_cast<const uint4 *>(xr + 8 * jb);
+      const uint4 xb = *reinterpret_cast<const uint4 *>(xr + 8 * jb + 4);
+      const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      int su = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        su = dp4a_us(w[4 + 4 * jb + i] & 0x0f0f0f0fu, xw[i], su);
+        su = dp4a_us((w[4 + 4 * jb + i] >> 4) & 0x0f0f0f0fu, xw[4 + i], su);
+      }
+      const float dx = __uint_as_float(dxs[jb]);
+      const float S = __fmul_rn(d, float(q4k_stream(w[1], w[2], w[3], jb)));
+      const float Mn = __fmul_rn(dm, float(q4k_stream(w[1], w[2], w[3], 8 + jb)));
+      acc = __fmaf_rn(__fmul_rn(S, dx), float(su), acc);
+      acc = __fmaf_rn(__fmul_rn(Mn, dx), float(-int(sxs[jb])), acc);
+    }
+  } else {
 #pragma unroll
   for (int jb = 0; jb < 8; ++jb) {
     if constexpr (Legacy<TYPE>::kIs) {
@@ -175,6 +201,7 @@ __device__ __forceinline__ float group_terms(const uint32_t *w, const uint32_t *
       sumi = sumi_q8_q8(q, xw);
     const float s = __fmul_rn(half_bits_to_float(dbits), __uint_as_float(dxs[jb]));
     acc = __fmaf_rn(s, float(sumi), acc);
+  }
   }
   return acc;
 }

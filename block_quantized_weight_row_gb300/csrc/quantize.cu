@@ -241,6 +241,168 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// k-quants: one warp per super-block of 256 values, lane l holding values
+// 8l..8l+7; the sub-block extremes and the super-block maxima are reductions
+// (order-free), every other step the exact rule of the block format.
+template <int TYPE>
+__global__ void __launch_bounds__(256) k_quantize_kq(const float *__restrict__ src, uint8_t *__restrict__ dst,
+                                                     int64_t n_sb) {
+  constexpr int BB = Fmt<TYPE>::kBytes;
+  const int lane = threadIdx.x & 31;
+  for (int64_t sb = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; sb < n_sb;
+       sb += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + sb * kQK_K) + 2 * lane);
+    const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + sb * kQK_K) + 2 * lane + 1);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint8_t *out = dst + sb * BB;
+    if constexpr (TYPE == kTypeQ4_K) {
+      float lo = v[0], hi = v[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) {
+        lo = fminf(lo, v[i]);
+        hi = fmaxf(hi, v[i]);
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {  // the 4 lanes of a sub-block of 32
+        lo = fminf(lo, __shfl_xor_sync(kFull, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, o));
+      }
+      const float m = lo < 0.0f ? -lo : 0.0f;
+      const float sj = __fdiv_rn(__fadd_rn(hi, m), 15.0f);
+      float smax = sj, mmax = m;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, o));
+        mmax = fmaxf(mmax, __shfl_xor_sync(kFull, mmax, o));
+      }
+      const __half hd = __float2half_rn(__fdiv_rn(smax, 63.0f)), hm = __float2half_rn(__fdiv_rn(mmax, 63.0f));
+      const float d = __half2float(hd), dm = __half2float(hm);
+      const int sc = d == 0.0f ? 0 : min(max(int(rintf(__fdiv_rn(sj, d))), 0), 63);
+      const int mn = dm == 0.0f ? 0 : min(max(int(rintf(__fdiv_rn(m, dm))), 0), 63);
+      const float S = __fmul_rn(d, float(sc)), M = __fmul_rn(dm, float(mn));
+      uint32_t packed = 0;  // the lane's 8 codes, 4 bits each
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int u = S == 0.0f ? 0 : min(max(int(rintf(__fdiv_rn(__fadd_rn(v[i], M), S))), 0), 15);
+        packed |= uint32_t(u) << (4 * i);
+      }
+      // header: d, dmin and the 96-bit stream of sc[0..7], mn[0..7] (lane 4j has sub-block j's)
+      uint64_t lo64 = 0;
+      uint32_t hi32 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint64_t sv = uint64_t(__shfl_sync(kFull, sc, 4 * j)), mv = uint64_t(__shfl_sync(kFull, mn, 4 * j));
+        lo64 |= sv << (6 * j);  // bits 0..47
+        const int bm = 48 + 6 * j;
+        if (bm + 6 <= 64) lo64 |= mv << bm;
+        else if (bm >= 64) hi32 |= uint32_t(mv << (bm - 64));
+        else { lo64 |= mv << bm; hi32 |= uint32_t(mv >> (64 - bm)); }
+      }
+      const uint32_t partner = __shfl_down_sync(kFull, packed, 2);  // codes i + 16 of this lane's i
+      if (lane == 0)
+        *reinterpret_cast<uint4 *>(out) = make_uint4(uint32_t(__half_as_ushort(hd)) | (uint32_t(__half_as_ushort(hm)) << 16),
+                                                     uint32_t(lo64), uint32_t(lo64 >> 32), hi32);
+      if ((lane & 3) < 2) {
+        uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w0 |= (((packed >> (4 * i)) & 15u) | (((partner >> (4 * i)) & 15u) << 4)) << (8 * i);
+          w1 |= (((packed >> (4 * i + 16)) & 15u) | (((partner >> (4 * i + 16)) & 15u) << 4)) << (8 * i);
+        }
+        *reinterpret_cast<uint2 *>(out + 16 + 16 * (lane >> 2) + 8 * (lane & 3)) = make_uint2(w0, w1);
+      }
+    } else {  // Q6_K
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));  // the 2 lanes of a sub-block of 16
+      const float sk = __fdiv_rn(amax, 31.0f);
+      float smax = sk;
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, o));
+      const __half hd = __float2half_rn(__fdiv_rn(smax, 127.0f));
+      const float d = __half2float(hd);
+      const int sc = d == 0.0f ? 0 : min(max(int(rintf(__fdiv_rn(sk, d))), -128), 127);
+      const float S = __fmul_rn(d, float(sc));
+      uint32_t lo4 = 0, hi2 = 0;  // the lane's 8 codes: low 4 bits, top 2 bits
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int u = (S == 0.0f ? 0 : min(max(int(rintf(__fdiv_rn(v[i], S))), -32), 31)) + 32;
+        lo4 |= uint32_t(u & 15) << (4 * i);
+        hi2 |= uint32_t(u >> 4) << (2 * i);
+      }
+      uint16_t *o16 = reinterpret_cast<uint16_t *>(out);  // 2-byte aligned
+      const uint32_t lo_up = __shfl_down_sync(kFull, lo4, 16);  // codes i + 128
+      if (lane < 16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t b0 = ((lo4 >> (8 * k)) & 15u) | (((lo_up >> (8 * k)) & 15u) << 4);
+          const uint32_t b1 = ((lo4 >> (8 * k + 4)) & 15u) | (((lo_up >> (8 * k + 4)) & 15u) << 4);
+          o16[4 * lane + k] = uint16_t(b0 | (b1 << 8));
+        }
+      }
+      const uint32_t h1 = __shfl_down_sync(kFull, hi2, 8), h2 = __shfl_down_sync(kFull, hi2, 16),
+                     h3 = __shfl_down_sync(kFull, hi2, 24);  // codes i + 64, i + 128, i + 192
+      if (lane < 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t bb[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 2 * k + e;
+            bb[e] = ((hi2 >> (2 * i)) & 3u) | (((h1 >> (2 * i)) & 3u) << 2) | (((h2 >> (2 * i)) & 3u) << 4) |
+                    (((h3 >> (2 * i)) & 3u) << 6);
+          }
+          o16[64 + 4 * lane + k] = uint16_t(bb[0] | (bb[1] << 8));
+        }
+      }
+      if ((lane & 1) == 0) out[192 + (lane >> 1)] = uint8_t(int8_t(sc));
+      if (lane == 0) o16[104] = __half_as_ushort(hd);
+    }
+  }
+}
+
+template <int TYPE>
+__global__ void __launch_bounds__(256) k_dequantize_kq(const uint8_t *__restrict__ blocks, float *__restrict__ dst,
+                                                       int64_t n_sb) {
+  constexpr int BB = Fmt<TYPE>::kBytes;
+  const int lane = threadIdx.x & 31;
+  for (int64_t sb = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; sb < n_sb;
+       sb += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+    const uint8_t *blk = blocks + sb * BB;
+    float r[8];
+    if constexpr (TYPE == kTypeQ4_K) {
+      const uint4 h = *reinterpret_cast<const uint4 *>(blk);
+      const int j = lane >> 2;
+      const float d = half_bits_to_float(h.x & 0xffffu), dm = half_bits_to_float(h.x >> 16);
+      const float S = __fmul_rn(d, float(q4k_stream(h.y, h.z, h.w, j)));
+      const float M = __fmul_rn(dm, float(q4k_stream(h.y, h.z, h.w, 8 + j)));
+      const uint2 c = *reinterpret_cast<const uint2 *>(blk + 16 + 16 * j + 8 * (lane & 1));
+      const uint32_t sh = (lane & 2) ? 4u : 0u;  // lanes 4j+2, 4j+3: the high nibbles
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t u = (((i < 4 ? c.x : c.y) >> (8 * (i & 3))) >> sh) & 15u;
+        r[i] = __fsub_rn(__fmul_rn(S, float(u)), M);
+      }
+    } else {
+      const uint16_t *b16 = reinterpret_cast<const uint16_t *>(blk);
+      const float d = half_bits_to_float(b16[104]);
+      const float S = __fmul_rn(d, float(int8_t(blk[192 + (lane >> 1)])));
+      const int lo_off = (8 * lane) & 127, hi_off = (8 * lane) & 63;
+      const uint32_t lsh = lane < 16 ? 0u : 4u, hsh = 2u * uint32_t(lane >> 3);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t ql = blk[lo_off + i], qh = blk[128 + hi_off + i];
+        const int u = int(((ql >> lsh) & 15u) | (((qh >> hsh) & 3u) << 4));
+        r[i] = __fmul_rn(S, float(u - 32));
+      }
+    }
+    float4 *o = reinterpret_cast<float4 *>(dst + sb * kQK_K) + 2 * lane;
+    o[0] = make_float4(r[0], r[1], r[2], r[3]);
+    o[1] = make_float4(r[4], r[5], r[6], r[7]);
+  }
+}
+
 template <int TYPE, bool BIAS, bool ROT>
 cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
                      cudaStream_t stream) {
@@ -332,6 +494,17 @@ cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64
                                  int64_t /*blocks_per_row*/, const float *bias, int64_t bias_period,
                                  cudaStream_t stream, bool rotate) {
   if (n_blocks == 0) return cudaSuccess;
+  if (type == kTypeQ4_K || type == kTypeQ6_K) {  // n_blocks counts super-blocks here
+    cudaError_t err;
+    const DeviceInfo *di = device_info(&err);
+    if (!di) return err;
+    const unsigned grid = unsigned(min((n_blocks + 7) / 8, int64_t(di->sm_count) * 8));
+    if (type == kTypeQ4_K)
+      k_quantize_kq<kTypeQ4_K><<<grid, 256, 0, stream>>>(src, dst, n_blocks);
+    else
+      k_quantize_kq<kTypeQ6_K><<<grid, 256, 0, stream>>>(src, dst, n_blocks);
+    return cudaGetLastError();
+  }
   return rotate ? launch_q_typed<true>(type, src, dst, n_blocks, bias, bias_period, stream)
                 : launch_q_typed<false>(type, src, dst, n_blocks, bias, bias_period, stream);
 }
@@ -354,6 +527,14 @@ cudaError_t launch_dequantize_rows(int type, const uint8_t *blocks, float *dst, 
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
+  if (type == kTypeQ4_K || type == kTypeQ6_K) {  // n_blocks counts super-blocks here
+    const unsigned grid = unsigned(min((n_blocks + 7) / 8, int64_t(di->sm_count) * 8));
+    if (type == kTypeQ4_K)
+      k_dequantize_kq<kTypeQ4_K><<<grid, 256, 0, stream>>>(blocks, dst, n_blocks);
+    else
+      k_dequantize_kq<kTypeQ6_K><<<grid, 256, 0, stream>>>(blocks, dst, n_blocks);
+    return cudaGetLastError();
+  }
   const int64_t grid = min((n_blocks * 8 + 255) / 256, int64_t(di->sm_count) * 8);
   switch (type) {
     case kTypeQ4_0: k_dequantize_rows<kTypeQ4_0><<<unsigned(grid), 256, 0, stream>>>(blocks, dst, n_blocks); break;

@@ -18,7 +18,7 @@ Workloads (shapes and distributions of the pages' models):
              mu[h][c] ~ U(-2, 2) per layer, V ~ N(0, 1); a separate 4096-token
              calibration draw of K gives the bias; 28 layers
   legacy     W 11008 x 4096 ~ N(0, 0.02) (8 draws), x ~ N(0, 1): the GEMV in
-             Q4_1, Q5_0, Q5_1 (and Q4_0 for comparison)
+             Q4_1, Q5_0, Q5_1, Q4_K, Q6_K (and Q4_0 for comparison)
 Seeds: workload index * 1000 + layer * 10 + matrix index.
 """
 from dataclasses import dataclass

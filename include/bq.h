@@ -68,6 +68,29 @@ extern "C" {
 #define BQ_TYPE_Q4_1 3
 #define BQ_TYPE_Q5_0 6
 #define BQ_TYPE_Q5_1 7
+/* k-quants: super-blocks of 256 weights with 8 sub-blocks of 32 whose scales
+ * are themselves quantized to 6 bits ("05. llama.cpp…", §量化类型). The pages
+ * give no bit layout or quantization search; this library's reading
+ * (little endian):
+ *   Q4_K, 144 bytes per 256: fp16 d, fp16 dmin, 12 bytes = 6-bit sub-block
+ *     scales sc[0..7] then minimums mn[0..7] as one 96-bit stream (value k
+ *     at bits 6k..6k+5), 128 bytes: sub-block j's codes in bytes 16j.., low
+ *     nibble code i, high nibble code i + 16; value fp32(d sc_j) u -
+ *     fp32(dmin mn_j). Quantizer: m_j = max(0, -min), s_j = (max + m_j)/15,
+ *     d = max s_j / 63, dmin = max m_j / 63 (fp16), sc/mn = rn(s_j / d),
+ *     rn(m_j / dmin) in 0..63, u = clamp(rn((x + M_j) / S_j), 0, 15).
+ *   Q6_K, 210 bytes per 256 (the size the pages' Llama-3-8B file sizes
+ *     imply): 128 bytes ql (byte i: low 4 bits of code i, then code i + 128),
+ *     64 bytes qh (byte i: top 2 bits of codes i, i+64, i+128, i+192), 16 int8
+ *     scales of the sub-blocks of 16, fp16 d; value fp32(d sc_k) (u - 32).
+ *     Quantizer: s_k = amax / 31, d = max s_k / 127, sc_k = rn(s_k / d),
+ *     u = clamp(rn(x / S_k), -32, 31) + 32.
+ * Rows hold a multiple of 256 values (else BQ_ERR_SHAPE). Taken by
+ * bq_quantize_rows, bq_dequantize_rows and bq_gemv / bq_gemv_multi; every
+ * other entry point answers BQ_ERR_UNSUPPORTED. bq_block_bytes gives the
+ * bytes of one super-block, bq_block_values 256. */
+#define BQ_TYPE_Q4_K 12
+#define BQ_TYPE_Q6_K 14
 
 #define BQ_OK 0
 #define BQ_ERR_INVALID_ARG (-1) /* null pointer, negative size, aliasing */
@@ -293,8 +316,12 @@ size_t bq_gemv_workspace_size(int type, int64_t K);
 /* Thread-local message of the last failure (never NULL). */
 const char *bq_last_error(void);
 
-/* Bytes per block: 18 (Q4_0), 34 (Q8_0), 0 otherwise. */
+/* Bytes per block: 18 (Q4_0), 34 (Q8_0), 20 (Q4_1), 22 (Q5_0), 24 (Q5_1),
+ * 144 (Q4_K) and 210 (Q6_K) per super-block; 0 for an unknown type. */
 int bq_block_bytes(int type);
+/* Values per block: 32, or 256 for the k-quant super-blocks; 0 for an
+ * unknown type. */
+int bq_block_values(int type);
 
 /* Synchronize the calling thread's stream, then read and clear the device
  * error word: BQ_OK, BQ_ERR_TIMEOUT if a bounded wait ran out, BQ_ERR_CUDA if

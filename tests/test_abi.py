@@ -274,3 +274,19 @@ def test_rotated_kv_and_bias_validation(L):
     assert L.bq_attn_decode_basis(2, 8, 1, q, K, V, o, 100, 16, 8, 128, f) == -7  # valid, no workspace
     assert L.bq_attn_decode_basis(2, 8, 1, q, K, V, o, 100, 8, 8, 96, f) == -2    # rotated, head_dim 96
     assert L.bq_attn_decode_basis(2, 8, 3, q, K, V, o, 100, 16, 8, 128, f) == -3  # unknown basis
+
+
+def test_kquants_where_they_are_taken(L):
+    """Q4_K (12) and Q6_K (14): super-blocks of 256 values; rows must hold
+    whole super-blocks; only the row quantizer, dequantizer and GEMV take them."""
+    p = ctypes.c_void_p
+    assert [L.bq_block_bytes(t) for t in (12, 14)] == [144, 210]
+    assert [L.bq_block_values(t) for t in (12, 14, 2, 3)] == [256, 256, 32, 32]
+    assert L.bq_block_values(99) == 0
+    for t in (12, 14):
+        assert L.bq_quantize_rows(t, p(FAKE), p(FAKE + (1 << 20)), 2, 96) == SHAPE
+        assert L.bq_dequantize_rows(t, p(FAKE), p(FAKE + (1 << 20)), 2, 288) == SHAPE
+        assert L.bq_gemv(t, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 4128) == SHAPE
+        assert L.bq_kv_quantize(t, p(FAKE), None, p(FAKE + (2 << 20)), 2, 2, 256) == UNSUPPORTED
+        assert L.bq_block_dots(t, p(FAKE), p(FAKE), p(FAKE), 1, 256) == UNSUPPORTED
+        assert L.bq_gemm(t, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 4, 256) == UNSUPPORTED

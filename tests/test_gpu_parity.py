@@ -822,3 +822,33 @@ def test_legacy_kv_write_bit_exact(bq, orc, dev, t):
     K = (rng.normal(size=(T, NKV, D)) + rng.uniform(-2, 2, size=(NKV, D))).astype(np.float32)
     got = _np(bq.kv_quantize(t, torch.from_numpy(K).to(dev), None))
     assert np.array_equal(got, orc.kv_quantize(t, K, None, T, NKV, D))
+
+
+# ------------------------------------------------------ k-quants Q4_K, Q6_K --
+
+KQUANTS = [12, 14]
+
+
+@pytest.mark.parametrize("t", KQUANTS)
+def test_kquant_quantize_and_dequantize_bit_exact(bq, orc, dev, t):
+    rng = np.random.default_rng(70 + t)
+    x = np.concatenate([rng.normal(size=(100, 512)), rng.standard_t(2, size=(100, 512)) * 10,
+                        rng.uniform(0.5, 3.0, size=(100, 512)), rng.normal(size=(100, 512)) * 1e-3 + 40.0,
+                        np.zeros((4, 512)), np.full((4, 512), -2.5)]).astype(np.float32)
+    got = _np(bq.quantize_rows(t, torch.from_numpy(x).to(dev)))
+    ref = orc.quantize_rows(t, x)
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} bytes differ"
+    deq = _np(bq.dequantize_rows(t, torch.from_numpy(ref).to(dev), 512))
+    assert np.array_equal(deq.view(np.uint32), orc.dequantize_rows(t, ref, 512).view(np.uint32))
+
+
+@pytest.mark.parametrize("t", KQUANTS)
+@pytest.mark.parametrize("M,K", [(1, 256), (37, 768), (4096, 4096), (11008, 4096), (300, 11008)])
+def test_kquant_gemv_matches_oracle(bq, orc, dev, t, M, K):
+    rng = np.random.default_rng(M + K + t)
+    W = (rng.normal(size=(M, K)) * 0.02).astype(np.float32)
+    x = rng.normal(size=K).astype(np.float32)
+    wb = orc.quantize_rows(t, W)
+    y = _np(bq.gemv(t, torch.from_numpy(wb).to(dev), torch.from_numpy(x).to(dev), M, K))
+    y_ref, mag = orc.gemv(t, wb, x, M, K, with_mag=True)
+    _check_float(y, y_ref, mag, f"type {t}")
