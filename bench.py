@@ -616,7 +616,7 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
         del mats, gl
     out["gemv_legacy_types"] = {"metric": "decode GEMV GB/s of weights per type (11008 x 4096, back to back)",
                                 "value": leg["Q5_0"]["GB/s"], "unit": "GB/s", "per_type": leg,
-                                "kernel": "k_gemv_tma (+ k_gemv_prep) for every type but Q6_K (k_gemv_generic); "
+                                "kernel": "k_gemv_tma (+ k_gemv_prep) for every type (Q6_K: K % 2048 == 0); "
                                           "Q4_0 for comparison",
                                 "l2": "8 distinct matrices per type, 203-370 MB: beyond L2"}
     torch.cuda.empty_cache()

@@ -39,6 +39,7 @@ using gemv::kXRecWords;
 using gemv::group_terms;
 using gemv::quantize_x_records;
 using gemv::GroupWords;
+using gemv::q6k_group_terms;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kMaxMats = BQ_GEMV_MAX_MATS;
@@ -178,6 +179,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
         if (row < nrows) {
           const uint8_t *rowp = stage + size_t(row) * a.row_bytes;
           for (int g = gl; g < a.groups; g += L) {
+            if constexpr (TYPE == kTypeQ6_K) {
+              // 210-byte super-blocks: 2-byte aligned in the stage
+              acc = q6k_group_terms(rowp + size_t(g) * Fmt<kTypeQ6_K>::kBytes, xrec + g * kXRecWords, acc);
+            } else {
             uint32_t w[GW];
             const uint4 *src = reinterpret_cast<const uint4 *>(rowp + size_t(g) * GW * 4);
 #pragma unroll
@@ -189,6 +194,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
               w[4 * k + 3] = u.w;
             }
             acc = group_terms<TYPE>(w, xrec + g * kXRecWords, acc);
+            }
           }
         }
         for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
@@ -372,8 +378,8 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
   for (int i = 0; i < n; ++i) M_total += M[i];
   if (M_total == 0) return cudaSuccess;
 
-  if constexpr (TYPE != kTypeQ6_K) {  // Q6_K: 210-byte super-blocks, generic kernel only
-  if (K % 256 == 0) {
+  // Q6_K's 210-byte super-blocks keep rows 16-byte aligned only for K % 2048 == 0
+  if (K % 256 == 0 && (TYPE != kTypeQ6_K || K % 2048 == 0)) {
     GemvArgs a{};
     int acc_rows = 0;
     a.n_mats = 0;
@@ -470,7 +476,6 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
       cfg.numAttrs = pdl ? 1 : 0;
       return cudaLaunchKernelEx(&cfg, k_gemv_tma<TYPE>, a);
     }
-  }
   }
   // any K % 32 == 0 (or rows too long for two stages): one plain launch per matrix
   const size_t smem = size_t(nb) * 40;  // 32 code bytes + scale + sum per block

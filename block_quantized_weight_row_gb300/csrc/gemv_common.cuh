@@ -77,6 +77,10 @@ struct GroupWords<kTypeQ4_K> {
   static constexpr int kWords = 36;  // one 144-byte super-block
 };
 template <>
+struct GroupWords<kTypeQ6_K> {
+  static constexpr int kWords = 4;  // unused: Q6_K groups are read by q6k_group_terms
+};
+template <>
 struct GroupWords<kTypeQ4_1> {
   static constexpr int kWords = 40;  // 160 bytes
 };
@@ -123,6 +127,51 @@ __device__ __forceinline__ float legacy_group_block(const uint32_t *w, int w0, b
   if (!L::kAffine) sumi -= 16 * xsum;
   acc = __fmaf_rn(__fmul_rn(half_bits_to_float(dbits), dx), float(sumi), acc);
   if (L::kAffine) acc = __fmaf_rn(__fmul_rn(half_bits_to_float(mbits), dx), float(xsum), acc);
+  return acc;
+}
+
+// 8 words of a shared-memory byte range starting at an even address.
+__device__ __forceinline__ void lds_8words_even(const uint8_t *p, uint32_t (&w)[8]) {
+  const uint32_t *a = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(3));
+  const uint32_t sh = (reinterpret_cast<uintptr_t>(p) & 2) * 8;
+  uint32_t r[9];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) r[i] = a[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = __funnelshift_rc(r[i], r[i + 1], sh);
+}
+
+// One Q6_K super-block (2-byte aligned in shared memory) against its 8 x
+// blocks: x block j holds codes 32j..32j+31 = sub-blocks 2j, 2j+1. The low
+// bits of codes 32j' .. (j' < 4) and 128 + 32j' .. share ql bytes 32j'..;
+// their top bits sit in qh bytes 32 (j' & 1).. at bit pairs j >> 1.
+__device__ __forceinline__ float q6k_group_terms(const uint8_t *sb, const uint32_t *xr, float acc) {
+  const float d = half_bits_to_float(uint32_t(*reinterpret_cast<const uint16_t *>(sb + 208)));
+#pragma unroll
+  for (int jp = 0; jp < 4; ++jp) {
+    uint32_t ql[8], qh[8];
+    lds_8words_even(sb + 32 * jp, ql);
+    lds_8words_even(sb + 128 + 32 * (jp & 1), qh);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int j = jp + 4 * half;
+      const uint32_t *xw = xr + 8 * j;
+      const float dx = __uint_as_float(xr[64 + j]);
+      const uint32_t lsh = 4u * uint32_t(half), hsh = 2u * uint32_t(j >> 1);
+      int su[2] = {0, 0}, sx[2] = {0, 0};
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const uint32_t u = ((ql[w] >> lsh) & 0x0f0f0f0fu) | (((qh[w] >> hsh) & 0x03030303u) << 4);
+        su[w >> 2] = dp4a_us(u, xw[w], su[w >> 2]);
+        sx[w >> 2] = dp4a_ss(0x01010101u, xw[w], sx[w >> 2]);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float S = __fmul_rn(d, float(int8_t(sb[192 + 2 * j + h])));
+        acc = __fmaf_rn(__fmul_rn(S, dx), float(su[h] - 32 * sx[h]), acc);
+      }
+    }
+  }
   return acc;
 }
 
