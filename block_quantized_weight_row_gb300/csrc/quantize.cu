@@ -46,22 +46,42 @@ __device__ __forceinline__ int swz(int b, int c) { return b * 128 + ((c ^ (b & 7
 
 // 32 values of one block (elements 32 * (lane & 1) + i of a 64-group) ->
 // H64 x / 8: butterflies (a, b) -> (a + b, a - b) of span 1, 2, 4, 8, 16 in
-// the lane, span 32 with lane ^ 1, then * 0.125. Every lane of the warp takes part.
+// the lane, span 32 with lane ^ 1, then * 0.125. Every lane of the warp takes
+// part. Spans 2-32 run on fp32 pairs (v[2k], v[2k+1]); a - b is the fused
+// -1 * b + a, which rounds once like the subtraction, and the cross-lane
+// step is s * v + p with s = +1 or -1.
 __device__ __forceinline__ void hadamard64_lane_pair(float (&v)[32], int lane) {
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1)
+  for (int i = 0; i < 32; i += 2) {
+    const float a = v[i], b = v[i + 1];
+    v[i] = __fadd_rn(a, b);
+    v[i + 1] = __fsub_rn(a, b);
+  }
+  uint64_t P[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = __fadd_rn(a, b);
-        v[i + h] = __fsub_rn(a, b);
+  for (int k = 0; k < 16; ++k) P[k] = pack2(__float_as_uint(v[2 * k]), __float_as_uint(v[2 * k + 1]));
+  const uint64_t m1 = pack2(__float_as_uint(-1.0f), __float_as_uint(-1.0f));
+#pragma unroll
+  for (int hp = 1; hp < 16; hp <<= 1)  // span 2 * hp, in pairs
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      if ((k & hp) == 0) {
+        const uint64_t t = P[k];
+        P[k] = fadd2(t, P[k + hp]);
+        P[k + hp] = ffma2(m1, P[k + hp], t);
       }
-  const bool lo = (lane & 1) == 0;
+  const float sg = (lane & 1) ? -1.0f : 1.0f;
+  const uint64_t s2 = pack2(__float_as_uint(sg), __float_as_uint(sg));
+  const uint64_t e2 = pack2(__float_as_uint(0.125f), __float_as_uint(0.125f));
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float p = __shfl_xor_sync(kFull, v[i], 1);
-    v[i] = __fmul_rn(lo ? __fadd_rn(v[i], p) : __fsub_rn(p, v[i]), 0.125f);
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t plo = __shfl_xor_sync(kFull, uint32_t(P[k]), 1), phi = __shfl_xor_sync(kFull, uint32_t(P[k] >> 32), 1);
+    P[k] = fmul2(ffma2(s2, P[k], pack2(plo, phi)), e2);
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    v[2 * k] = __uint_as_float(uint32_t(P[k]));
+    v[2 * k + 1] = __uint_as_float(uint32_t(P[k] >> 32));
   }
 }
 
