@@ -211,15 +211,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
 // ------------------------------------------------------------ prep kernel --
 
 // Runs before k_gemv_tma in the same stream when a workspace is available:
-//   1. asks L2 to fetch every weight byte of the launch (no dependency on
-//      earlier kernels, so with programmatic dependent launch this overlaps
-//      the previous kernel and keeps HBM busy through the launch boundary);
+//   1. with programmatic dependent launch, and weights of at most 64 MB,
+//      asks L2 to fetch every weight byte of the launch (no dependency on
+//      earlier kernels, so this overlaps the previous kernel and keeps HBM
+//      busy through the launch boundary);
 //   2. after the previous kernel completed, quantizes x once into records in
 //      global memory (16 blocks per CTA, 8 lanes per block), which every GEMV
 //      CTA then copies instead of quantizing x itself.
 constexpr int kPrepThreads = 128;
 constexpr int kPrepBlocksPerCta = kPrepThreads / 8;
 constexpr uint32_t kPrepChunk = 64 * 1024;
+constexpr int64_t kPrefetchMaxBytes = int64_t(64) << 20;  // about half of L2
 
 struct PrepArgs {
   const uint8_t *W[kMaxMats];
@@ -446,10 +448,16 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
         PrepArgs p{};
         p.n_mats = a.n_mats;
         p.chunk_start[0] = 0;
+        // The L2 prefetch pays only when it overlaps the previous kernel
+        // (programmatic dependent launch) and the weights fit L2 beside the
+        // stream of that kernel; otherwise it only competes with this
+        // launch's own weight stream (measured: 14% slower decode steps
+        // without dependent launch, 30% slower 200 MB launches).
+        const bool l2_prefetch = pdl && int64_t(a.M) * row_bytes <= kPrefetchMaxBytes;
         for (int i = 0; i < a.n_mats; ++i) {
           p.W[i] = a.W[i];
           p.bytes[i] = int64_t(a.row_start[i + 1] - a.row_start[i]) * row_bytes;
-          p.chunk_start[i + 1] = p.chunk_start[i] + (p.bytes[i] + kPrepChunk - 1) / kPrepChunk;
+          p.chunk_start[i + 1] = p.chunk_start[i] + (l2_prefetch ? (p.bytes[i] + kPrepChunk - 1) / kPrepChunk : 0);
         }
         for (int i = a.n_mats; i < kMaxMats; ++i) p.chunk_start[i + 1] = p.chunk_start[i];
         p.x = x;

@@ -306,7 +306,8 @@ size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K);
 /* Workspace bytes that let bq_gemv / bq_gemv_multi quantize x once per call
  * (0 when K % 256 != 0, where x is always quantized inside the GEMV kernel).
  * With a workspace of at least this size set by bq_set_workspace, a call
- * launches a small prep kernel, which first asks L2 to fetch the call's
+ * launches a small prep kernel, which (with weight prefetch enabled and at
+ * most 64 MB of weights in the call) first asks L2 to fetch the call's
  * weights and then writes x's Q8_0 codes, scales and code sums to the
  * workspace, and then the GEMV kernel, which copies them. Without one, every
  * GEMV CTA quantizes x itself. Both give bit-identical results. The
