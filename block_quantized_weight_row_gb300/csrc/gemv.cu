@@ -411,13 +411,18 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
     const int reserve = 1024;  // per-CTA system reservation
     const int half_sm = min(di->smem_per_sm / 2 - reserve, di->max_smem_optin);
     const int whole_sm = min(di->smem_per_sm - reserve, di->max_smem_optin);
-    const int forced_rows = tuning_value("BQ_GEMV_STAGE_ROWS");
+    // tuning overrides, read from the environment once per process (a
+    // lookup per call costs host time that a decode step of direct calls
+    // cannot spare)
+    static const int forced_rows = tuning_value("BQ_GEMV_STAGE_ROWS");
+    static const int forced_stages = tuning_value("BQ_GEMV_STAGES");
+    static const int forced_ctas = tuning_value("BQ_GEMV_CTAS_PER_SM");
     int stage_rows = forced_rows > 0 ? forced_rows : kConsumerWarps * a.rows_per_warp;
     stage_rows = min(stage_rows, max(1, kMaxStageBytes / row_bytes));
     stage_rows = int(std::min<int64_t>(stage_rows, a.M));
     a.stage_rows = stage_rows;
     a.stage_bytes = stage_rows * row_bytes;
-    const int max_stages = tuning_value("BQ_GEMV_STAGES") > 0 ? tuning_value("BQ_GEMV_STAGES") : 4;
+    const int max_stages = forced_stages > 0 ? forced_stages : 4;
     auto ring = [&](int budget) {
       return min(max_stages, (budget - a.xrec_bytes - 16 * max_stages) / a.stage_bytes);
     };
@@ -430,7 +435,7 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
       ctas_per_sm = 1;
       stages = ring(whole_sm);
     }
-    if (const int forced = tuning_value("BQ_GEMV_CTAS_PER_SM")) ctas_per_sm = forced;
+    if (forced_ctas) ctas_per_sm = forced_ctas;
     if (stages >= 2) {
       a.stages = stages;
       const size_t smem = size_t(a.xrec_bytes) + size_t(stages) * a.stage_bytes + 2 * 8 * size_t(stages);

@@ -346,7 +346,8 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   per_sm = std::min(per_sm, 2);
-  if (const int forced = tuning_value("BQ_GEMV_SEQ_CTAS_PER_SM")) per_sm = std::min(per_sm, forced);
+  static const int forced = tuning_value("BQ_GEMV_SEQ_CTAS_PER_SM");  // read once per process
+  if (forced) per_sm = std::min(per_sm, forced);
   if ((e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), stream)) != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
