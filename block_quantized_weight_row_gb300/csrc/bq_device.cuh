@@ -460,6 +460,38 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
 }
 
 
+// quantize_block_lane_fast on fp32 pairs: per value the same IEEE operations
+// (the product by the reciprocal, the rounding add of the magic number, the
+// subtraction back, and the distance r - (t - M) as the fused -1 * d + r,
+// which rounds once like the subtraction), two values per instruction. The
+// codes and the exact-path decision are bit-identical.
+template <int TYPE>
+__device__ __forceinline__ bool quantize_block_lane_fast_pairs(const float (&v)[32], uint16_t &scale,
+                                                               uint32_t *words) {
+  float ds;
+  block_scale<TYPE>(block_amax<TYPE>(v), scale, ds);
+  const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
+  constexpr float kMagic = 12582912.0f + float(TYPE == kTypeQ4_0 ? 8 : 0);
+  const uint64_t inv2 = pack2(__float_as_uint(inv), __float_as_uint(inv));
+  const uint64_t mg2 = pack2(__float_as_uint(kMagic), __float_as_uint(kMagic));
+  const uint64_t nmg2 = pack2(__float_as_uint(-kMagic), __float_as_uint(-kMagic));
+  const uint64_t m1 = pack2(__float_as_uint(-1.0f), __float_as_uint(-1.0f));
+  uint32_t tb[32];
+  float dmax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint64_t r = fmul2(pack2(__float_as_uint(v[2 * k]), __float_as_uint(v[2 * k + 1])), inv2);
+    const uint64_t t = fadd2(r, mg2);
+    const uint64_t e = ffma2(m1, fadd2(t, nmg2), r);
+    tb[2 * k] = uint32_t(t);
+    tb[2 * k + 1] = uint32_t(t >> 32);
+    dmax = fmaxf(dmax, fmaxf(fabsf(__uint_as_float(uint32_t(e))), fabsf(__uint_as_float(uint32_t(e >> 32)))));
+  }
+  if (dmax > 0.4999f || (ds > 0.0f && ds < 6.103515625e-05f)) return false;
+  pack_code_words<TYPE>(tb, words);
+  return true;
+}
+
 // ------------------------------------------------------------------ memory --
 
 __device__ __forceinline__ float4 ld_stream_f4(const float *p) {

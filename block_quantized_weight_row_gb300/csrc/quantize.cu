@@ -85,50 +85,112 @@ __device__ __forceinline__ void hadamard64_lane_pair(float (&v)[32], int lane) {
   }
 }
 
+// 16-byte asynchronous copy global -> shared, zero-filled when !valid (src
+// must then still be a mapped address).
+__device__ __forceinline__ void cp_async16_zf(void *dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+// The fast path of quantize_block_lane on fp32 pairs, the code words built
+// as the values are rounded (no per-value staging): per value the same IEEE
+// operations (product by the reciprocal, rounding add of the magic number,
+// subtraction back, and the distance r - (t - M) as the fused -1 * d + r,
+// which rounds once like the subtraction). False when the block needs the
+// exact path; the words and scale are then not final.
+template <int TYPE>
+__device__ __forceinline__ bool quantize_block_words_fast(const float (&v)[32], uint16_t &scale,
+                                                          uint32_t (&w)[TYPE == kTypeQ4_0 ? 4 : 8]) {
+  float ds;
+  block_scale<TYPE>(block_amax<TYPE>(v), scale, ds);
+  const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
+  constexpr float kMagic = 12582912.0f + float(TYPE == kTypeQ4_0 ? 8 : 0);
+  const uint64_t inv2 = pack2(__float_as_uint(inv), __float_as_uint(inv));
+  const uint64_t mg2 = pack2(__float_as_uint(kMagic), __float_as_uint(kMagic));
+  const uint64_t nmg2 = pack2(__float_as_uint(-kMagic), __float_as_uint(-kMagic));
+  const uint64_t m1 = pack2(__float_as_uint(-1.0f), __float_as_uint(-1.0f));
+  float dmax = 0.0f;
+  // the code bytes of values j0 .. j0+3 (low byte of each t) as one word
+  auto word4 = [&](int j0) {
+    uint32_t t[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint64_t r = fmul2(pack2(__float_as_uint(v[j0 + 2 * h]), __float_as_uint(v[j0 + 2 * h + 1])), inv2);
+      const uint64_t tt = fadd2(r, mg2);
+      const uint64_t e = ffma2(m1, fadd2(tt, nmg2), r);
+      t[2 * h] = uint32_t(tt);
+      t[2 * h + 1] = uint32_t(tt >> 32);
+      dmax = fmaxf(dmax, fmaxf(fabsf(__uint_as_float(uint32_t(e))), fabsf(__uint_as_float(uint32_t(e >> 32)))));
+    }
+    return pack_bytes(t[0], t[1], t[2], t[3]);
+  };
+  if constexpr (TYPE == kTypeQ4_0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = word4(4 * i), hi = word4(16 + 4 * i);
+      w[i] = lo + (hi << 4);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = word4(4 * i);
+  }
+  return !(dmax > 0.4999f || (ds > 0.0f && ds < 6.103515625e-05f));
+}
+
+// Shared memory of k_quantize_rows: per warp two 4 KB input tiles (the next
+// tile's asynchronous copies land in one while the other is quantized; the
+// output blocks are written back into the consumed tile), the legacy types'
+// output tiles, then the bias blocks when they fit.
+template <int TYPE>
+constexpr int quant_out_bytes() {
+  return Legacy<TYPE>::kIs ? kQuantWarps * 32 * Fmt<TYPE>::kBytes : 0;
+}
+template <int TYPE>
+size_t quant_smem_bytes(int64_t bias_smem_blocks) {
+  return size_t(kQuantWarps) * 2 * 32 * 128 + size_t(quant_out_bytes<TYPE>()) + size_t(bias_smem_blocks) * 128;
+}
+
 template <int TYPE, bool BIAS, bool ROT>
-__global__ void __launch_bounds__(kQuantThreads, 2)
+__global__ void __launch_bounds__(kQuantThreads, 3)
     k_quantize_rows(const float *__restrict__ src, uint8_t *__restrict__ dst, int64_t n_blocks,
-                    const float *__restrict__ bias, int64_t bias_period) {
+                    const float *__restrict__ bias, int64_t bias_period, int bias_smem_blocks) {
   constexpr int BB = Fmt<TYPE>::kBytes;
   constexpr int NW = TYPE == kTypeQ4_0 ? 4 : 8;  // code words per block (Q4_0 / Q8_0)
-  __shared__ __align__(16) uint8_t in_tile[kQuantWarps][32 * 128];
-  __shared__ __align__(16) uint8_t out_tile[kQuantWarps][32 * BB];
-  __shared__ __align__(16) uint8_t bias_tile[BIAS ? kMaxSmemBiasBlocks * 128 : 16];
+  constexpr int kTile = 32 * 128;
+  extern __shared__ __align__(128) uint8_t qsm[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  uint8_t *it = in_tile[warp];
-  uint8_t *ot = out_tile[warp];
-  const bool bias_in_smem = BIAS && bias_period <= kMaxSmemBiasBlocks;
+  uint8_t *tiles = qsm + warp * 2 * kTile;
+  uint8_t *ot = qsm + kQuantWarps * 2 * kTile + warp * 32 * BB;  // legacy types only
+  uint8_t *bias_tile = qsm + kQuantWarps * 2 * kTile + quant_out_bytes<TYPE>();
+  const bool bias_in_smem = BIAS && bias_smem_blocks > 0;
   if (bias_in_smem) {
-    for (int i = threadIdx.x; i < int(bias_period) * 8; i += kQuantThreads)
+    for (int i = threadIdx.x; i < bias_smem_blocks * 8; i += kQuantThreads)
       *reinterpret_cast<float4 *>(bias_tile + swz(i >> 3, i & 7)) = __ldg(reinterpret_cast<const float4 *>(bias) + i);
     __syncthreads();
   }
+  const bool bias_pow2 = (bias_period & (bias_period - 1)) == 0;
   const int64_t total_warps = int64_t(gridDim.x) * kQuantWarps;
-  // coalesced: vector i = lane + 32c of a tile is chunk (i & 7) of block (i >> 3).
-  // The loads of a warp's next tile are in flight while it quantizes the
-  // current one, so that every warp keeps 4 KB of reads outstanding.
-  auto load_tile = [&](int64_t t, float4 (&ld)[8]) {
+  // coalesced: vector i = lane + 32c of a tile is chunk (i & 7) of block (i >> 3)
+  auto issue_tile = [&](int64_t t, uint8_t *buf) {
     const int64_t nb = t * 32 < n_blocks ? min(int64_t(32), n_blocks - t * 32) : 0;
-    const float4 *gsrc = reinterpret_cast<const float4 *>(src + t * 32 * kQK);
+    const float *g = src + t * 32 * kQK;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int i = lane + 32 * c;
-      ld[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if ((i >> 3) < nb) ld[c] = __ldcs(gsrc + i);
+      const bool in = (i >> 3) < nb;
+      cp_async16_zf(buf + swz(i >> 3, i & 7), in ? static_cast<const void *>(g + 4 * i) : src, in);
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  float4 ld[8];
-  load_tile(int64_t(blockIdx.x) * kQuantWarps + warp, ld);
-  for (int64_t tile = int64_t(blockIdx.x) * kQuantWarps + warp; tile * 32 < n_blocks; tile += total_warps) {
-    const int nblk = int(min(int64_t(32), n_blocks - tile * 32));
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int i = lane + 32 * c;
-      *reinterpret_cast<float4 *>(it + swz(i >> 3, i & 7)) = ld[c];
-    }
+  int64_t tile = int64_t(blockIdx.x) * kQuantWarps + warp;
+  issue_tile(tile, tiles);
+  for (int k = 0; tile * 32 < n_blocks; tile += total_warps, k ^= 1) {
+    uint8_t *it = tiles + k * kTile;
+    issue_tile(tile + total_warps, tiles + (k ^ 1) * kTile);  // in flight while this tile is quantized
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncwarp();
-    load_tile(tile + total_warps, ld);
+    const int nblk = int(min(int64_t(32), n_blocks - tile * 32));
     float v[32];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -146,70 +208,71 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
         *reinterpret_cast<float4 *>(it + swz(lane, c)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     }
     const int64_t b = tile * 32 + lane;
-    if (BIAS && b < n_blocks) {
-      // block b of row (token, head) uses bias block b mod (heads * blocks per row)
-      const int64_t bb = b % bias_period;
+    // block b of row (token, head) uses bias block b mod (heads * blocks per row)
+    const int64_t bb = BIAS ? (bias_pow2 ? (b & (bias_period - 1)) : b % bias_period) : 0;
+    auto sub_bias = [&](float (&x)[32]) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const float4 f = bias_in_smem ? *reinterpret_cast<const float4 *>(bias_tile + swz(int(bb), c))
                                       : __ldg(reinterpret_cast<const float4 *>(bias + bb * kQK) + c);
-        v[4 * c] = __fsub_rn(v[4 * c], f.x);
-        v[4 * c + 1] = __fsub_rn(v[4 * c + 1], f.y);
-        v[4 * c + 2] = __fsub_rn(v[4 * c + 2], f.z);
-        v[4 * c + 3] = __fsub_rn(v[4 * c + 3], f.w);
+        x[4 * c] = __fsub_rn(x[4 * c], f.x);
+        x[4 * c + 1] = __fsub_rn(x[4 * c + 1], f.y);
+        x[4 * c + 2] = __fsub_rn(x[4 * c + 2], f.z);
+        x[4 * c + 3] = __fsub_rn(x[4 * c + 3], f.w);
       }
-    }
+    };
+    if (BIAS && b < n_blocks) sub_bias(v);
+    const uint8_t *out_src;
     if constexpr (Legacy<TYPE>::kIs) {
       // legacy types: the exact rule for every block
       legacy_quantize_block<TYPE>(v, reinterpret_cast<uint16_t *>(ot + lane * BB));
+      out_src = ot;
     } else {
-    uint16_t scale;
-    uint32_t w[NW];
-    if (!quantize_block_lane_fast<TYPE>(v, scale, w)) {
-      // rare (a value near a tie, or a subnormal scale): the block again from
-      // the tile, through the exact path
-      float e[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 f = *reinterpret_cast<const float4 *>(it + swz(lane, c));
-        e[4 * c] = f.x;
-        e[4 * c + 1] = f.y;
-        e[4 * c + 2] = f.z;
-        e[4 * c + 3] = f.w;
-      }
-      if (BIAS && b < n_blocks) {
-        const int64_t bb = b % bias_period;
+      uint16_t scale;
+      uint32_t w[NW];
+      if (!quantize_block_words_fast<TYPE>(v, scale, w)) {
+        // rare (a value near a tie, or a subnormal scale): the block again
+        // from the tile, through the exact path
+        float e[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const float4 f = bias_in_smem ? *reinterpret_cast<const float4 *>(bias_tile + swz(int(bb), c))
-                                        : __ldg(reinterpret_cast<const float4 *>(bias + bb * kQK) + c);
-          e[4 * c] = __fsub_rn(e[4 * c], f.x);
-          e[4 * c + 1] = __fsub_rn(e[4 * c + 1], f.y);
-          e[4 * c + 2] = __fsub_rn(e[4 * c + 2], f.z);
-          e[4 * c + 3] = __fsub_rn(e[4 * c + 3], f.w);
+          const float4 f = *reinterpret_cast<const float4 *>(it + swz(lane, c));
+          e[4 * c] = f.x;
+          e[4 * c + 1] = f.y;
+          e[4 * c + 2] = f.z;
+          e[4 * c + 3] = f.w;
         }
+        if (BIAS && b < n_blocks) sub_bias(e);
+        quantize_block_lane_exact<TYPE>(e, scale, w);
       }
-      quantize_block_lane_exact<TYPE>(e, scale, w);
-    }
-    // block `lane` of the tile at byte lane*BB (2-byte aligned)
-    uint16_t *o = reinterpret_cast<uint16_t *>(ot + lane * BB);
-    o[0] = scale;
+      __syncwarp();  // every lane has read its block before outputs land in the tile
+      // block `lane` at byte lane*BB of the consumed tile (BB = 2 mod 4: even
+      // lanes start on a word, odd lanes half a word later)
+      uint8_t *ob = it + lane * BB;
+      if (lane & 1) {
+        *reinterpret_cast<uint16_t *>(ob) = scale;
 #pragma unroll
-    for (int i = 0; i < NW; ++i) {
-      o[1 + 2 * i] = uint16_t(w[i] & 0xffffu);
-      o[2 + 2 * i] = uint16_t(w[i] >> 16);
-    }
+        for (int i = 0; i < NW; ++i) reinterpret_cast<uint32_t *>(ob + 2)[i] = w[i];
+      } else {
+        uint32_t *o32 = reinterpret_cast<uint32_t *>(ob);
+        o32[0] = uint32_t(scale) | (w[0] << 16);
+#pragma unroll
+        for (int i = 1; i < NW; ++i) o32[i] = __funnelshift_r(w[i - 1], w[i], 16);
+        *reinterpret_cast<uint16_t *>(ob + 4 * NW) = uint16_t(w[NW - 1] >> 16);
+      }
+      out_src = it;
     }
     __syncwarp();
     const int nbytes = nblk * BB;
     uint8_t *out = dst + tile * 32 * BB;  // 16-byte aligned: 32 * BB is a multiple of 16
     const int n16 = nbytes / 16;
     for (int i = lane; i < n16; i += 32)
-      reinterpret_cast<uint4 *>(out)[i] = reinterpret_cast<const uint4 *>(ot)[i];
+      reinterpret_cast<uint4 *>(out)[i] = reinterpret_cast<const uint4 *>(out_src)[i];
     for (int i = n16 * 8 + lane; i < nbytes / 2; i += 32)
-      reinterpret_cast<uint16_t *>(out)[i] = reinterpret_cast<const uint16_t *>(ot)[i];
-    __syncwarp();
+      reinterpret_cast<uint16_t *>(out)[i] = reinterpret_cast<const uint16_t *>(out_src)[i];
+    __syncwarp();  // the tile is refilled by the next-but-one iteration's copies
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
 }
 
 // x_hat = scale * q, exact in fp32. One thread per 4 outputs.
@@ -431,9 +494,13 @@ cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const flo
   if (!di) return err;
   const int64_t tiles = (n_blocks + 31) / 32;
   const int64_t ctas = (tiles + kQuantWarps - 1) / kQuantWarps;
-  const int64_t grid = min(ctas, int64_t(di->sm_count) * 2);  // persistent: 2 resident CTAs per SM
-  k_quantize_rows<TYPE, BIAS, ROT><<<unsigned(grid), kQuantThreads, 0, stream>>>(src, dst, n_blocks, bias,
-                                                                                bias_period);
+  const int64_t grid = min(ctas, int64_t(di->sm_count) * 3);  // persistent: 3 resident CTAs per SM
+  const int bias_smem_blocks = (BIAS && bias_period <= kMaxSmemBiasBlocks) ? int(bias_period) : 0;
+  const size_t smem = quant_smem_bytes<TYPE>(bias_smem_blocks);
+  err = ensure_smem(reinterpret_cast<const void *>(k_quantize_rows<TYPE, BIAS, ROT>), int(smem));
+  if (err != cudaSuccess) return err;
+  k_quantize_rows<TYPE, BIAS, ROT><<<unsigned(grid), kQuantThreads, smem, stream>>>(src, dst, n_blocks, bias,
+                                                                                  bias_period, bias_smem_blocks);
   return cudaGetLastError();
 }
 
