@@ -38,6 +38,7 @@ using gemv::kXRecBytes;
 using gemv::kXRecWords;
 using gemv::group_terms;
 using gemv::quantize_x_records;
+using gemv::quantize_x_records_2lane;
 using gemv::GroupWords;
 using gemv::q6k_group_terms;
 
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
         reinterpret_cast<uint4 *>(xrec)[k] = __ldcg(reinterpret_cast<const uint4 *>(a.rec) + k);
       }
     } else {
-      quantize_x_records(a.x, a.K / kQK, xrec, threadIdx.x, kConsumerWarps * 32, int(blockIdx.x) * 8);
+      quantize_x_records_2lane(a.x, a.K / kQK, xrec, threadIdx.x, kConsumerWarps * 32);
     }
     named_bar_sync(1, kConsumerWarps * 32);
 
@@ -446,6 +447,7 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
       const int64_t grid = std::min((int64_t(a.M) + half_stage - 1) / half_stage,
                                     int64_t(di->sm_count) * ctas_per_sm);
       const bool pdl = weight_prefetch();
+      a.rec = rec_ws;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -477,6 +477,41 @@ def test_gemv_both_activation_paths(bq, orc, dev, t, with_ws, Ms, K):
         _check_float(_np(outs[i]), y_ref, mag, f"matrix {i}, workspace={with_ws}")
 
 
+@pytest.mark.parametrize("K", [256, 2304, 11008])
+def test_gemv_activation_paths_bit_identical(bq, dev, K):
+    """x's records built in every GEMV CTA (two lanes per block) and by the
+    prep kernel (eight lanes per block) are the same, so y is bit-identical,
+    on plain, scaled, sparse, exact-tie and subnormal-scale activations."""
+    import ctypes
+    from block_quantized_weight_row_gb300 import binding, inputs
+    L = binding.lib()
+    M = 300
+    w = bq.quantize_rows(Q4, inputs.weight(M, K, seed=K + 17).to(dev))
+    base = inputs.activation(K, seed=K + 19)
+    ties = base.clone()
+    ties[0::32] = 127.0                                   # scale exactly 1.0 in every block ...
+    ties[1::32] = torch.arange(1, K // 32 + 1) % 100 + 0.5  # ... and a value on a tie
+    tiny = base * 1e-6                                    # scales below binary16's normal range
+    cases = {"plain": base, "small": base * 1e-3, "large": base * 300.0, "ties": ties, "tiny": tiny}
+    sparse = base.clone()
+    sparse[::3] = 0.0
+    cases["sparse"] = sparse
+    ws = torch.empty(max(256, int(L.bq_gemv_workspace_size(Q4, K))), dtype=torch.uint8, device=dev)
+    assert L.bq_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+    for name, x in cases.items():
+        xd = x.to(dev)
+        y_ws = torch.empty(M, device=dev)
+        y_cta = torch.empty(M, device=dev)
+        assert L.bq_set_workspace(ctypes.c_void_p(ws.data_ptr()), ws.numel()) == 0
+        assert L.bq_gemv(Q4, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(xd.data_ptr()),
+                         ctypes.c_void_p(y_ws.data_ptr()), M, K) == 0
+        assert L.bq_set_workspace(None, 0) == 0
+        assert L.bq_gemv(Q4, ctypes.c_void_p(w.data_ptr()), ctypes.c_void_p(xd.data_ptr()),
+                         ctypes.c_void_p(y_cta.data_ptr()), M, K) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(y_ws, y_cta), name
+
+
 # ------------------------------------------------ GEMV sequence (one launch) --
 
 def _seq_case(t, seed, shapes):
