@@ -5,9 +5,13 @@
 // 本地推理服务", §性能直觉：带宽决定 Decode，算力决定 Prefill). The kernel is
 // therefore built to stream W from HBM at full rate:
 //
-//   - x (fp32) is quantized to Q8_0 by each CTA into shared memory (same block
-//     rule as the row quantizer, so the codes are bit-identical), while the
-//     weight stream is already in flight. No workspace, no extra launch.
+//   - x (fp32) is quantized to Q8_0 (same block rule as the row quantizer, so
+//     the codes are bit-identical) either once per launch by a small prep
+//     kernel into the caller's workspace, whose records every GEMV CTA copies
+//     (with programmatic dependent launch the prep kernel also asks L2 for
+//     the launch's weights while the previous kernel runs), or, without a
+//     workspace, by every CTA itself (two lanes per block) while its weight
+//     stream is already in flight. The two paths give bit-identical records.
 //   - One producer warp streams the CTA's rows with 1-D bulk async copies
 //     (cp.async.bulk) into a ring of shared-memory stages, completing on
 //     mbarriers; 8 consumer warps wait on those barriers and release stages

@@ -11,18 +11,21 @@
 // quantization arithmetic must stay well under the SMs' issue rate at that
 // byte rate, so one lane owns one whole block: no shuffles, one division per
 // block, full-rate rounding, one tie test per block):
-//   - warp tile = 32 consecutive blocks (4 KB): read with fully coalesced
-//     128-bit loads (512 contiguous bytes per instruction), the next tile's
-//     loads issued before the current tile is quantized (a persistent grid of
-//     two CTAs per SM, so every warp keeps 4 KB of reads in flight), then moved through
-//     a warp-private shared-memory tile so that lane i holds block i. The tile
-//     is XOR-swizzled (16-byte chunk c of block b sits at chunk c ^ (b & 7)),
+//   - warp tile = 32 consecutive blocks (4 KB), copied with fully coalesced
+//     16-byte asynchronous copies (cp.async; 512 contiguous bytes per
+//     instruction) into one of two warp-private shared-memory tiles while the
+//     warp quantizes the other, so every warp keeps 4 KB of reads in flight
+//     without holding them in registers (80 registers: a persistent grid of
+//     three CTAs per SM); lane i then reads block i. The tiles are
+//     XOR-swizzled (16-byte chunk c of block b sits at chunk c ^ (b & 7)),
 //     which keeps both the coalesced writes and the per-block reads free of
 //     bank conflicts;
+//   - the per-value rounding runs on fp32 pairs, and the code words are
+//     built as the values are rounded;
 //   - a mean-centering bias (one block per (kv-head, 32 channels), a few KB)
 //     is staged once per CTA in the same swizzled layout;
-//   - the tile's output (576 B Q4_0 / 1088 B Q8_0) is assembled in shared
-//     memory and leaves as 16-byte stores.
+//   - the tile's output (576 B Q4_0 / 1088 B Q8_0) is written back into the
+//     consumed input tile with word stores and leaves as 16-byte stores.
 // Hadamard-rotated K (lpnh.cn KV-cache article, §三步上手, third step: a
 // quantized K cache with head_dim a multiple of 64 is rotated, and the bias
 // must be measured in the same basis): every 64 channels of a head become
