@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
       reinterpret_cast<uint4 *>(out)[i] = reinterpret_cast<const uint4 *>(out_src)[i];
     for (int i = n16 * 8 + lane; i < nbytes / 2; i += 32)
       reinterpret_cast<uint16_t *>(out)[i] = reinterpret_cast<const uint16_t *>(out_src)[i];
-    __syncwarp();  // the tile is refilled by the next-but-one iteration's copies
+    __syncwarp();  // the next iteration refills this buffer
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
 }
