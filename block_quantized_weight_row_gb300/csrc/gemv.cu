@@ -241,6 +241,13 @@ struct PrepArgs {
 
 __global__ void __launch_bounds__(kPrepThreads) k_gemv_prep(const PrepArgs p) {
   if (threadIdx.x == 0) {
+    // this CTA's part of x into L2 first: its load after the wait below is
+    // then an L2 hit. A prefetch reads nothing into the SM, and L2 is where
+    // the previous kernel's stores to x land, so it cannot expose stale data.
+    if (int(blockIdx.x) < p.quant_ctas) {
+      const int b0 = int(blockIdx.x) * kPrepBlocksPerCta;
+      prefetch_l2(p.x + int64_t(b0) * kQK, uint32_t(min(kPrepBlocksPerCta, p.nb - b0)) * kQK * 4u);
+    }
     for (int64_t c = blockIdx.x; c < p.chunk_start[p.n_mats]; c += gridDim.x) {
       int m = 0;
       while (c >= p.chunk_start[m + 1]) ++m;
