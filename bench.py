@@ -381,7 +381,11 @@ def main():
         clocks.close()
     ms_max = max_over_ranks(ms, dist)
     value = aggregate_rate(step["weight_bytes"], world, ms_max * 1e-3) / 1e9
-    launches = (len(step["groups"]) if batched else len(step["mats"])) * args.steps
+    # our kernels per timed step: every call whose K takes a GEMV workspace
+    # launches the prep kernel and the GEMV kernel, other calls the GEMV only
+    Lb = binding.lib()
+    calls = [(g["K"]) for g in step["groups"]] if batched else [m[4] for m in step["mats"]]
+    launches = sum(2 if Lb.bq_gemv_workspace_size(bq.Q4_0, K) > 0 else 1 for K in calls) * args.steps
 
     # ---- roofline: the dominant kernel alone on distinct 11008 x 4096 matrices
     gate_up = [m for m, e in zip(step["mats"], step["plan"]) if e.name in ("gate", "up")]
