@@ -116,6 +116,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
+      // without records, every CTA loads x after the wait: ask L2 for it now
+      // (no data comes to the SM; the previous kernel's stores to x land in
+      // L2, so the later loads cannot see stale values)
+      if (!a.rec) prefetch_l2(a.x, uint32_t(a.K) * 4u);
       int issued = 0;
       const uint64_t stream_policy = l2_evict_first_policy();  // W is read once
       StageCursor cur{r0};
