@@ -451,6 +451,20 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
       ctas_per_sm = 1;
       stages = ring(whole_sm);
     }
+    // Launches beyond kPrefetchMaxBytes (no L2 prefetch; the ring alone keeps
+    // HBM busy) stream faster with a third, slightly smaller stage where two
+    // full ones leave the room (4-5% on a 203 MB launch at K = 4096; launches
+    // of a decode chain, which wait on their predecessor, measured slower).
+    if (forced_rows <= 0 && forced_stages <= 0 && ctas_per_sm == 2 && stages == 2 &&
+        int64_t(a.M) * row_bytes > kPrefetchMaxBytes) {
+      const int r3 = (half_sm - a.xrec_bytes - 16 * max_stages) / (3 * row_bytes);
+      if (r3 >= 1 && r3 >= stage_rows - 2) {
+        stage_rows = min(stage_rows - 1, r3);
+        a.stage_rows = stage_rows;
+        a.stage_bytes = stage_rows * row_bytes;
+        stages = 3;
+      }
+    }
     if (forced_ctas) ctas_per_sm = forced_ctas;
     if (stages >= 2) {
       a.stages = stages;

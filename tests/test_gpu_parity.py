@@ -477,6 +477,26 @@ def test_gemv_both_activation_paths(bq, orc, dev, t, with_ws, Ms, K):
         _check_float(_np(outs[i]), y_ref, mag, f"matrix {i}, workspace={with_ws}")
 
 
+def test_gemv_large_launch_three_stage_ring(bq, orc, dev):
+    """A launch of more than 64 MB of weights (three 11008 x 4096 Q4_0
+    matrices, 76 MB) runs with a three-stage ring: it matches the oracle and
+    is bit-identical to the same matrices launched one per call (two-stage
+    ring; each row is computed the same way whatever the stage size)."""
+    from block_quantized_weight_row_gb300 import inputs
+    M, K = 11008, 4096
+    x = inputs.activation(K, seed=77)
+    wq = [orc.quantize_rows(Q4, inputs.weight(M, K, seed=7700 + i).numpy()) for i in range(3)]
+    w_dev = [torch.from_numpy(w).to(dev) for w in wq]
+    xd = x.to(dev)
+    ys = bq.gemv_multi(Q4, w_dev, xd, [M] * 3, K)
+    singles = [bq.gemv(Q4, w, xd, M, K) for w in w_dev]
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(ys[i], singles[i]), f"matrix {i}"
+    y_ref, mag = orc.gemv(Q4, wq[0], x.numpy(), M, K, with_mag=True)
+    _check_float(_np(ys[0]), y_ref, mag, "matrix 0 of the large launch")
+
+
 @pytest.mark.parametrize("K", [256, 2304, 11008])
 def test_gemv_activation_paths_bit_identical(bq, dev, K):
     """x's records built in every GEMV CTA (two lanes per block) and by the
