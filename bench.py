@@ -124,31 +124,98 @@ def kernel_traffic(key: str):
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms or finer) kept only inside [t0, t1]."""
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, its maximum, power and the clock-event reasons, sampled every
+    ~2 ms through NVML (read-only queries of libnvidia-ml via ctypes) by a
+    background thread and kept only inside [t0, t1], so that even a timed
+    region of a few milliseconds carries samples. Falls back to nvidia-smi at
+    its finest period when NVML cannot be loaded."""
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
+    SMI_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
-        self.rows = []
-        self.proc = None
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.rows = []  # (time, sm_mhz, max_mhz, power_w, set of reasons)
         self.t0 = self.t1 = None
+        self.source = None
+        self.stop_evt = threading.Event()
+        self.proc = None
+        self.th = None
+        nv = self._nvml(device_index)
+        if nv is not None:
+            self.source = "nvml"
+            self.th = threading.Thread(target=self._poll_nvml, args=(nv, period_s), daemon=True)
+            self.th.start()
+            return
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.SMI_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
-        self.first = threading.Event()
-        self.th = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi"
+        first = threading.Event()
+        self.th = threading.Thread(target=self._read_smi, args=(first,), daemon=True)
         self.th.start()
-        self.first.wait(timeout=10)
+        first.wait(timeout=10)
 
-    def _read(self):
+    @staticmethod
+    def _nvml(device_index):
+        """(library, handle) of this process's GPU, or None."""
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            ok = False
+            try:
+                import torch
+                uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+                ok = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+            if not ok:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(h)) == 0
+            if not ok:
+                return None
+            reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            return nv, h, reasons
+        except (OSError, AttributeError):
+            return None
+
+    def _poll_nvml(self, nvh, period_s):
+        nv, h, reasons = nvh
+        sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_evt.is_set():
+            t = time.time()
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and \
+                    nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                power = pw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                bits = rs.value if reasons(h, ctypes.byref(rs)) == 0 else 0
+                names = {n for n, b in self.REASON_BITS.items() if bits & b}
+                self.rows.append((t, float(sm.value), float(mx.value), power, names))
+            time.sleep(period_s)
+
+    def _read_smi(self, first):
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.proc.stdout:
-            self.rows.append((time.time(), line.strip()))
-            self.first.set()
+            parts = [p.strip() for p in line.split(",")]
+            first.set()
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            try:
+                power = float(parts[3])
+            except ValueError:
+                power = None
+            self.rows.append((time.time(), sm, mx, power,
+                              {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
 
     def start(self):
         self.t0 = time.time()
@@ -157,62 +224,62 @@ class ClockSampler:
         self.t1 = time.time()
 
     def close(self):
+        self.stop_evt.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.th:
+            self.th.join(timeout=5)
 
     def summary(self):
         if self.t0 is None or self.t1 is None:
-            return {"samples": 0}
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for t, line in self.rows:
-            if not (self.t0 <= t <= self.t1 + 0.05):
-                continue
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            return {"samples": 0, "source": self.source}
+        rows = [r for r in list(self.rows) if self.t0 <= r[0] <= self.t1]
+        if not rows:
+            return {"samples": 0, "source": self.source}
+        reasons = set()
+        for r in rows:
+            reasons |= r[4]
+        powers = [r[3] for r in rows if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "source": self.source,
+                "power_w_max": round(max(powers), 1) if powers else None,
+                "window_s": round(self.t1 - self.t0, 4)}
 
 
 # -------------------------------------------------------------- workloads --
 
-def build_decode_step(workload, dev, bq, inputs, pool_x=True):
+def build_decode_step(workload, dev, bq, inputs, chain=False):
     """Resident Q4_0 weights of every matrix of the step, one fp32 input per
     distinct activation (in one contiguous buffer) and one output per matrix
-    (in one contiguous buffer)."""
+    (in one contiguous buffer). Matrices reading the same activation (q/k/v,
+    gate/up) form one batch.
+
+    chain: every batch after the first reads an output of the batch before it
+    (o reads q's output, gate/up read o's, down reads gate's, the next layer's
+    q/k/v read down's), so each batch depends on the previous one through
+    memory; the weights are then ~N(0, 1/K) so that the values stay in range
+    along the chain, and x_all holds only the first batch's input."""
     import torch
     plan = inputs.decode_plan(workload)
     keys = []
     for e in plan:
         if e.x_key not in keys:
             keys.append(e.x_key)
+    if chain:
+        keys = keys[:1]
     x_len = {e.x_key: e.K for e in plan}
     x_off, off = {}, 0
     for k in keys:
         x_off[k] = off
         off += (x_len[k] + 3) // 4 * 4  # keep every x 16-byte aligned
     x_all = torch.empty(off, dtype=torch.float32, device=dev)
-    filled = set()
-    for e in plan:
-        if e.x_key not in filled:
-            o = x_off[e.x_key]
-            x_all[o:o + e.K].copy_(inputs.activation(e.K, e.x_seed, device=dev))
-            filled.add(e.x_key)
+    for k in keys:
+        e = next(e for e in plan if e.x_key == k)
+        x_all[x_off[k]:x_off[k] + e.K].copy_(inputs.activation(e.K, e.x_seed, device=dev))
     y_off, off = [], 0
     for e in plan:
         y_off.append(off)
@@ -220,30 +287,42 @@ def build_decode_step(workload, dev, bq, inputs, pool_x=True):
     y_all = torch.empty(off, dtype=torch.float32, device=dev)
     mats = []
     for i, e in enumerate(plan):
-        W = inputs.weight(e.M, e.K, e.w_seed, device=dev)
+        W = inputs.chain_weight(e.M, e.K, e.w_seed + 100000, device=dev) if chain else \
+            inputs.weight(e.M, e.K, e.w_seed, device=dev)
         wq = bq.quantize_rows(bq.Q4_0, W)
         del W
-        o = x_off[e.x_key]
-        mats.append((wq, x_all[o:o + e.K], y_all[y_off[i]:y_off[i] + e.M], e.M, e.K))
-    # matrices that read the same activation (q/k/v, gate/up) form one launch
+        mats.append([wq, None, y_all[y_off[i]:y_off[i] + e.M], e.M, e.K])
     groups = []
-    for (wq, x, y, M, K), e in zip(mats, plan):
+    for m, e in zip(mats, plan):
         if groups and groups[-1]["key"] == e.x_key:
             g = groups[-1]
         else:
-            g = {"key": e.x_key, "x": x, "K": K, "w": [], "y": [], "M": []}
+            if chain and groups:
+                x = groups[-1]["y"][0][:e.K]
+                assert x.numel() == e.K, "chain: an output of the previous batch is this batch's input"
+            else:
+                x = x_all[x_off[e.x_key]:x_off[e.x_key] + e.K]
+            g = {"key": e.x_key, "x": x, "K": e.K, "w": [], "y": [], "M": []}
             groups.append(g)
-        g["w"].append(wq)
-        g["y"].append(y)
-        g["M"].append(M)
+        m[1] = g["x"]
+        g["w"].append(m[0])
+        g["y"].append(m[2])
+        g["M"].append(m[3])
     torch.cuda.synchronize(dev)
     wbytes = sum(e.M * (e.K // 32) * 18 for e in plan)
-    return {"plan": plan, "mats": mats, "groups": groups, "x_all": x_all, "y_all": y_all, "weight_bytes": wbytes}
+    return {"plan": plan, "mats": [tuple(m) for m in mats], "groups": groups, "x_all": x_all, "y_all": y_all,
+            "weight_bytes": wbytes, "chain": chain}
+
+
+def seq_groups(step):
+    """The step's batches in the form bq_gemv_sequence takes."""
+    return [(g["w"], g["x"], g["M"], g["K"], g["y"]) for g in step["groups"]]
 
 
 def run_step(step, bq, batched=True):
-    """One decode token: every matrix once, in layer order. batched: one
-    launch per group of matrices sharing an input; else one per matrix."""
+    """One decode token, one launch per batch: every matrix once, in layer
+    order. batched: one launch per group of matrices sharing an input; else
+    one per matrix."""
     if batched:
         for g in step["groups"]:
             bq.gemv_multi(bq.Q4_0, g["w"], g["x"], g["M"], g["K"], outs=g["y"])
@@ -264,13 +343,30 @@ def capture(fn, stream):
     return g
 
 
+def capture_or_direct(fn, stream):
+    """(callable replaying one step, how): a CUDA graph of fn when its launches
+    can be captured, else fn itself issued on `stream` each step."""
+    import torch
+    try:
+        g = capture(fn, stream)
+        return g.replay, "cuda graph"
+    except Exception as e:  # a launch kind the capture does not take
+        torch.cuda.synchronize()
+        return fn, f"direct calls ({type(e).__name__} in capture)"
+
+
 def time_graph(g, stream, steps, warmup, dist=None, clocks=None, between=None):
+    """Per-step device time (ms) of graph replays (see time_steps)."""
+    return time_steps(g.replay, stream, steps, warmup, dist, clocks, between)
+
+
+def time_steps(run, stream, steps, warmup, dist=None, clocks=None, between=None):
     """Per-step device time (ms): events on the launching stream around each
-    replay; `between` (e.g. an L2 flush) runs outside the timed spans."""
+    step run(); `between` (e.g. an L2 flush) runs outside the timed spans."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            g.replay()
+            run()
             if between:
                 between()
     torch.cuda.synchronize()
@@ -283,7 +379,7 @@ def time_graph(g, stream, steps, warmup, dist=None, clocks=None, between=None):
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(steps):
-                g.replay()
+                run()
             e1.record(stream)
         e1.synchronize()
         total = e0.elapsed_time(e1)
@@ -293,7 +389,7 @@ def time_graph(g, stream, steps, warmup, dist=None, clocks=None, between=None):
         with torch.cuda.stream(stream):
             for a, b in evs:
                 a.record(stream)
-                g.replay()
+                run()
                 b.record(stream)
                 between()
         torch.cuda.synchronize()
@@ -307,9 +403,8 @@ def time_graph(g, stream, steps, warmup, dist=None, clocks=None, between=None):
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def oracle_decode_sample(seconds: float, workload="7b-decode"):
-    """The oracle GEMV over layer 0 of the decode step, repeated until at
-    least `seconds` of oracle time; returns (GB/s, description)."""
+def oracle_layer0(workload="7b-decode"):
+    """Layer 0 of the decode step for the oracle: (Q4_0 blocks, x, M, K) per matrix."""
     import oracle
     from block_quantized_weight_row_gb300 import inputs
     plan = [e for e in inputs.decode_plan(workload) if e.layer == 0]
@@ -318,6 +413,13 @@ def oracle_decode_sample(seconds: float, workload="7b-decode"):
         W = inputs.weight(e.M, e.K, e.w_seed).numpy()
         mats.append((oracle.quantize_rows(oracle.Q4_0, W), inputs.activation(e.K, e.x_seed).numpy(), e.M, e.K))
         del W
+    return mats
+
+
+def oracle_decode_sample(seconds: float, mats, label="single thread", workload="7b-decode"):
+    """The oracle GEMV over layer 0 of the decode step, repeated until at
+    least `seconds` of oracle time; returns (GB/s, description)."""
+    import oracle
     done_bytes, spent, passes = 0, 0.0, 0
     while spent < seconds:
         for wq, x, M, K in mats:
@@ -327,8 +429,8 @@ def oracle_decode_sample(seconds: float, workload="7b-decode"):
             done_bytes += wq.nbytes
         passes += 1
     mb = sum(m[0].nbytes for m in mats) / 1e6
-    return done_bytes / spent / 1e9, (f"oracle GEMV (single thread) over layer 0 of the {workload} step "
-                                      f"(7 matrices, {mb:.1f} MB Q4_0), {passes} passes, {spent:.1f} s")
+    return done_bytes / spent / 1e9, (f"oracle GEMV ({label}) over layer 0 of the {workload} step "
+                                      f"({len(mats)} matrices, {mb:.1f} MB Q4_0), {passes} passes, {spent:.1f} s")
 
 
 # ------------------------------------------------------------------ main ---
@@ -339,13 +441,15 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--path", choices=("sequence", "per-launch"), default="sequence",
+                    help="the whole step in one persistent launch, or one launch per batch")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true",
-                    help="launch each GEMV only after the previous kernel completed")
+                    help="per-launch path: launch each GEMV only after the previous kernel completed")
     ap.add_argument("--no-batch", action="store_true",
-                    help="one launch per matrix instead of one per group of matrices sharing an input")
+                    help="per-launch path: one launch per matrix instead of one per batch sharing an input")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "gemm", "kv", "attn"), default=None,
+    ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "seq", "gemm", "kv", "attn"), default=None,
                     help="run one kernel case a few times and exit (for profiler captures)")
     ap.add_argument("--case-launches", type=int, default=16)
     args = ap.parse_args()
@@ -367,49 +471,63 @@ def main():
     dist = init_dist(world, "nccl")
     peaks = load_peaks()
     stream = torch.cuda.Stream(dev)
+    clocks = ClockSampler(local) if rank == 0 else None
 
-    # ---- headline: 7B decode step. Model weights are written once, before
-    # the step, so every GEMV may stream its weights while the previous
-    # kernel on the stream finishes (programmatic dependent launch).
+    # ---- headline: 7B decode step, every weight read once per token
     step = build_decode_step("7b-decode", dev, bq, inputs)
     binding.set_weight_prefetch(not args.no_prefetch)
-    batched = not args.no_batch
-    g = capture(lambda: run_step(step, bq, batched), stream)
-    clocks = ClockSampler(local) if rank == 0 else None
-    ms = time_graph(g, stream, args.steps, args.warmup, dist, clocks)
-    if clocks:
-        clocks.close()
+    Lb = binding.lib()
+    if args.path == "sequence":
+        sargs = binding.gemv_sequence_args(seq_groups(step))
+        run, how = capture_or_direct(lambda: binding.gemv_sequence_call(bq.Q4_0, sargs, dev), stream)
+        launches_per_step = 1
+        kernel = "k_gemv_seq<Q4_0>"
+    else:
+        batched = not args.no_batch
+        run, how = capture_or_direct(lambda: run_step(step, bq, batched), stream)
+        calls = [g["K"] for g in step["groups"]] if batched else [m[4] for m in step["mats"]]
+        launches_per_step = sum(2 if Lb.bq_gemv_workspace_size(bq.Q4_0, K) > 0 else 1 for K in calls)
+        kernel = "k_gemv_tma<Q4_0> (+ k_gemv_prep)"
+    ms = time_steps(run, stream, args.steps, args.warmup, dist, clocks)
     ms_max = max_over_ranks(ms, dist)
     value = aggregate_rate(step["weight_bytes"], world, ms_max * 1e-3) / 1e9
-    # our kernels per timed step: every call whose K takes a GEMV workspace
-    # launches the prep kernel and the GEMV kernel, other calls the GEMV only
-    Lb = binding.lib()
-    calls = [(g["K"]) for g in step["groups"]] if batched else [m[4] for m in step["mats"]]
-    launches = sum(2 if Lb.bq_gemv_workspace_size(bq.Q4_0, K) > 0 else 1 for K in calls) * args.steps
+    launches = launches_per_step * args.steps
 
-    # ---- roofline: the dominant kernel alone on distinct 11008 x 4096 matrices
-    gate_up = [m for m, e in zip(step["mats"], step["plan"]) if e.name in ("gate", "up")]
-    rg = capture(lambda: [bq.gemv(bq.Q4_0, wq, x, M, K, out=y) for wq, x, y, M, K in gate_up], stream)
-    r_ms = time_graph(rg, stream, 20, 3) / len(gate_up)
-    M_, K_ = 11008, 4096
-    alg_bytes = M_ * (K_ // 32) * 18 + K_ * 4 + M_ * 4
-    achieved = alg_bytes / (r_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_gemv_tma<Q4_0> 11008x4096", "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": kernel_traffic("gemv_q4_0_11008x4096"), "peak_source": peaks["source"],
-                "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_us": round(r_ms * 1e3, 3)}
+    # ---- roofline of the dominant kernel
+    if args.path == "sequence":
+        # one launch is the whole step: weights, every x once, every y once
+        x_bytes = sum(4 * g["K"] for g in step["groups"])
+        y_bytes = sum(4 * M for g in step["groups"] for M in g["M"])
+        alg_bytes = step["weight_bytes"] + x_bytes + y_bytes
+        launch_ms = ms
+        roofline = {"bound": "hbm", "kernel": "k_gemv_seq<Q4_0>, the whole 7B decode step in one launch",
+                    "traffic": kernel_traffic("gemv_seq_q4_0_7b_step"),
+                    "duration_note": "launch duration = step time on its stream (the step is this one "
+                                     "launch after a counter reset of 1 KB)"}
+    else:
+        # the 11008 x 4096 launch alone, back to back on distinct matrices
+        gate_up = [m for m, e in zip(step["mats"], step["plan"]) if e.name in ("gate", "up")]
+        rg = capture(lambda: [bq.gemv(bq.Q4_0, wq, x, M, K, out=y) for wq, x, y, M, K in gate_up], stream)
+        launch_ms = time_graph(rg, stream, 20, 3) / len(gate_up)
+        M_, K_ = 11008, 4096
+        alg_bytes = M_ * (K_ // 32) * 18 + K_ * 4 + M_ * 4
+        roofline = {"bound": "hbm", "kernel": "k_gemv_tma<Q4_0> 11008x4096",
+                    "traffic": kernel_traffic("gemv_q4_0_11008x4096")}
+    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+    roofline.update({"achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+                     "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_us": round(launch_ms * 1e3, 3)})
 
     # ---- e2e: direct C-ABI calls, host buffers, copies inside the timed region
     e2e = e2e_decode(step, stream, dev, args, dist, world)
 
     secondary = {}
     if not args.no_secondary:
-        secondary = secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world)
+        secondary = secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, args)
 
     cpu = None
     if rank == 0 and world == 1:
-        v, desc = oracle_decode_sample(args.cpu_seconds)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline(args.cpu_seconds)
 
     if rank == 0:
         out = {
@@ -421,11 +539,11 @@ def main():
                                    "down 4096x11008}, batch 1, Q4_0 weights, 224 GEMVs per step",
                        "weight_bytes_per_step": step["weight_bytes"],
                        "l2": "inputs larger than L2 (3.64 GB of weights per step)",
-                       "parallelism": f"replicas x{world}", "graph": "one CUDA graph per step",
-                       "weight_prefetch": not args.no_prefetch,
-                       "launches_per_step": len(step["groups"]) if batched else len(step["mats"]),
-                       "batching": "q/k/v and gate/up share one launch each (one x)" if batched
-                                   else "one launch per matrix"},
+                       "parallelism": f"replicas x{world}", "issue": how, "path": args.path,
+                       "kernel": kernel, "launches_per_step": launches_per_step,
+                       "inputs": "one fp32 x per distinct activation (q/k/v share one, gate/up share one); no "
+                                 "batch reads another's output, so no batch waits (secondary.decode_chain "
+                                 "times the step with every batch reading the previous batch's output)"},
             "hbm_frac_of_measured": round(value / world / peaks["hbm_gbs"], 4),
             "tokens_per_s_equiv": round(1e3 / ms_max, 1),
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
@@ -433,55 +551,66 @@ def main():
             "cpu_baseline": cpu, "secondary": secondary,
         }
         print(json.dumps(out))
+    if clocks:
+        clocks.close()
     if dist is not None:
         dist.destroy_process_group()
 
 
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return None
+
+
+def cpu_baseline(seconds):
+    """The oracle's GEMV on this host: single-threaded, and the same source
+    built with OpenMP over rows on every core this process may use."""
+    mats = oracle_layer0()
+    v1, desc1 = oracle_decode_sample(seconds, mats)
+    cores = len(os.sched_getaffinity(0))
+    out = {"value": round(v1, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc1,
+           "cpu_model": cpu_model()}
+    try:
+        import oracle
+        from oracle import build as obuild
+        os.environ["OMP_NUM_THREADS"] = str(cores)
+        with oracle.use_library(obuild.build_omp()):
+            vn, descn = oracle_decode_sample(seconds, mats, f"OpenMP over rows, {cores} threads")
+        out["all_cores"] = {"value": round(vn, 4), "unit": "GB/s", "cores": cores, "kind": "oracle (OpenMP rows)",
+                            "sample": descn}
+    except Exception as e:  # no OpenMP runtime on this host
+        out["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"}
+    return out
+
+
 def e2e_decode(step, stream, dev, args, dist, world):
-    """Per step: pinned host -> device copy of every activation, the 224
-    GEMVs as direct C-ABI calls, device -> pinned host copy of every output,
-    and a host wait. The outputs are read back in four parts, each on a side
-    stream as soon as its layers are done, so only the last part's copy
-    follows the last GEMV. No GEMV workspace is set: without one each call is
-    a single launch (x quantized in every CTA), which direct calls favour
-    (1.29 vs 1.41 ms per step measured), while graph replays favour the prep
-    kernel; the results are bit-identical."""
+    """Per step: pinned host -> device copy of every activation, the whole step
+    as one bq_gemv_sequence C-ABI call (argument arrays built once), device ->
+    pinned host copy of every output, and a host wait."""
     import torch
     from block_quantized_weight_row_gb300 import binding
     L = binding.lib()
     x_host = step["x_all"].cpu().pin_memory()
     y_host = torch.empty(step["y_all"].numel(), dtype=torch.float32).pin_memory()
-    calls = [(*binding.gemv_multi_args(g["w"], g["y"], g["M"]), ctypes.c_void_p(g["x"].data_ptr()), g["K"])
-             for g in step["groups"]]
-    f = L.bq_gemv_multi
-    # the groups after which a part of the outputs is complete: y_all holds
-    # the outputs in plan (layer) order
-    y0 = step["y_all"].data_ptr()
-    ends = [(g["y"][-1].data_ptr() - y0) // 4 + g["M"][-1] for g in step["groups"]]
-    n_parts = 4
-    cut = [len(calls) * (k + 1) // n_parts - 1 for k in range(n_parts)]
-    side = torch.cuda.Stream(device=dev)
-    evs = [torch.cuda.Event() for _ in range(n_parts)]
+    sargs = binding.gemv_sequence_args(seq_groups(step))
+    binding._workspace(dev, int(L.bq_gemv_sequence_workspace_size()))
+    f = L.bq_gemv_sequence
 
     def one():
         step["x_all"].copy_(x_host, non_blocking=True)
-        part, lo = 0, 0
-        for gi, (n_, W_, Y_, M_, x_, K_) in enumerate(calls):
-            rc = f(2, n_, W_, Y_, M_, x_, K_)
-            if rc:
-                raise binding.BQError(rc, L.bq_last_error().decode())
-            if gi == cut[part]:
-                hi = ends[gi] if part < n_parts - 1 else y_host.numel()
-                evs[part].record(stream)
-                side.wait_event(evs[part])
-                with torch.cuda.stream(side):
-                    y_host[lo:hi].copy_(step["y_all"][lo:hi], non_blocking=True)
-                part, lo = part + 1, hi
+        rc = f(2, *sargs)
+        if rc:
+            raise binding.BQError(rc, L.bq_last_error().decode())
+        y_host.copy_(step["y_all"], non_blocking=True)
         stream.synchronize()
-        side.synchronize()
 
     n = max(3, min(args.steps, 200))
-    assert L.bq_set_workspace(None, 0) == 0
     with torch.cuda.stream(stream):
         assert L.bq_set_stream(ctypes.c_void_p(stream.cuda_stream)) == 0
         for _ in range(args.warmup):
@@ -495,13 +624,63 @@ def e2e_decode(step, stream, dev, args, dist, world):
         e1.record(stream)
         e1.synchronize()
     torch.cuda.synchronize()
-    assert torch.equal(y_host, step["y_all"].cpu()), "the read-back parts must cover every output"
+    assert torch.equal(y_host, step["y_all"].cpu()), "the read-back must cover every output"
     ms = max_over_ranks(e0.elapsed_time(e1) / n, dist)
     return {"value": round(aggregate_rate(step["weight_bytes"], world, ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": int(step["x_all"].numel() * 4), "d2h_bytes_per_step": int(y_host.numel() * 4),
             "ms_per_step": round(ms, 4), "steps": n,
-            "path": "direct bq_gemv_multi C-ABI calls (no graph, no GEMV workspace: one launch per call); "
-                    "outputs read back in four parts on a side stream as their layers finish"}
+            "path": "per step: pinned H2D copy of the inputs, one bq_gemv_sequence C-ABI call, pinned D2H copy "
+                    "of every output, host wait"}
+
+
+def tensor_rates(dev):
+    """Measured int8 (and, beside it, f16) tensor-op rates this GPU offers,
+    the denominators of the prefill GEMM's fractions: mma.sync throughput from
+    the probe library (register operands, 8 independent chains per warp, 4
+    CTAs of 8 warps per SM, best of 3) and torch._int_mm (cuBLAS int8 GEMM,
+    8192^3, best of 5 after 2 warm-ups). No clock or other setting is changed."""
+    import torch
+    from block_quantized_weight_row_gb300 import build as bbuild
+    out = {}
+    try:
+        P = ctypes.CDLL(bbuild.PROBE_LIB)
+        P.bq_probe_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+        P.bq_probe_mma_rate.restype = ctypes.c_int
+        for kind, name in ((0, "mma_sync_s8_tops"), (1, "mma_sync_f16_tflops")):
+            best = 0.0
+            for _ in range(3):
+                v = ctypes.c_double()
+                if P.bq_probe_mma_rate(kind, 16384, 4, ctypes.byref(v)) == 0:
+                    best = max(best, v.value)
+            out[name] = round(best, 1)
+    except OSError as e:
+        out["probe"] = f"unavailable: {e}"
+    try:
+        n = 8192
+        A = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+        B = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+        for _ in range(2):
+            torch._int_mm(A, B)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._int_mm(A, B)
+            e1.record()
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        out["torch_int_mm_tops"] = round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1)
+        del A, B
+    except Exception as e:  # no int8 GEMM in this torch build for this GPU
+        out["torch_int_mm"] = f"unavailable: {type(e).__name__}: {str(e)[:120]}"
+    i8 = [v for k, v in out.items() if k in ("mma_sync_s8_tops", "torch_int_mm_tops") and v]
+    out["int8_tops_measured"] = max(i8) if i8 else None
+    out["note"] = ("sm_103a has no int8 tcgen05.mma; the int8 tensor path is mma.sync s8 (and whatever cuBLAS "
+                   "runs for torch._int_mm); int8_tops_measured is the larger of the two")
+    torch.cuda.empty_cache()
+    return out
 
 
 def l2_flusher(dev):
@@ -513,12 +692,44 @@ def l2_flusher(dev):
     return flush
 
 
-def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
+def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, args):
     import torch
     out = {}
     flush = l2_flusher(dev)
 
+    # the 7B step issued one launch per batch (the previous path), and the
+    # step as a dependency chain on both paths
+    def rate(st, ms_):
+        return round(aggregate_rate(st["weight_bytes"], world, ms_ * 1e-3) / 1e9, 1)
+
+    if args.path == "sequence":
+        g = capture(lambda: run_step(step, bq, True), stream)
+        ms = max_over_ranks(time_graph(g, stream, 50, 5), dist)
+        out["decode_per_launch"] = {"metric": "Q4_0 decode GEMV weight GB/s, 7B step, one launch per batch "
+                                              "(prep + GEMV kernel pairs with dependent launch, one CUDA graph)",
+                                    "value": rate(step, ms), "unit": "GB/s", "ms_per_step": round(ms, 4),
+                                    "launches_per_step": 2 * len(step["groups"])}
+        del g
+    chain = build_decode_step("7b-decode", dev, bq, inputs, chain=True)
+    sargs = binding.gemv_sequence_args(seq_groups(chain))
+    run, how = capture_or_direct(lambda: binding.gemv_sequence_call(bq.Q4_0, sargs, dev), stream)
+    ms_seq = max_over_ranks(time_steps(run, stream, 50, 5), dist)
+    g = capture(lambda: run_step(chain, bq, True), stream)
+    ms_pl = max_over_ranks(time_graph(g, stream, 50, 5), dist)
+    out["decode_chain"] = {"metric": "Q4_0 decode GEMV weight GB/s, 7B step as a chain: every batch reads the "
+                                     "previous batch's output (o <- q, gate/up <- o, down <- gate, next q/k/v <- "
+                                     "down), weights ~N(0, 1/K)",
+                           "value": rate(chain, ms_seq), "unit": "GB/s", "ms_per_step": round(ms_seq, 4),
+                           "issue": how, "waits_per_step": len(chain["groups"]) - 1,
+                           "per_launch": {"value": rate(chain, ms_pl), "ms_per_step": round(ms_pl, 4)},
+                           "hbm_frac_of_measured": round(chain["weight_bytes"] / (ms_seq * 1e-3) / 1e9 /
+                                                         peaks["hbm_gbs"], 4)}
+    del chain, g, run
+    torch.cuda.empty_cache()
+
     # prefill GEMM, 512 tokens, Q8_0 weights
+    rates = tensor_rates(dev)
+    out["tensor_rates"] = rates
     cfg = inputs.WORKLOADS["prefill-q8_0"]
     N = cfg["tokens"]
     rows = []
@@ -539,6 +750,9 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
     out["prefill_gemm"] = {"metric": "prefill GEMM int8-equivalent TOPS (2*N*M*K per GEMM, X quantize included)",
                            "value": round(tops, 1), "unit": "TOPS", "shapes": rows,
                            "tensor_frac_of_measured": round(tops / peaks["bf16_tflops"], 4),
+                           "tensor_frac_of_int8_peak": (round(tops / rates["int8_tops_measured"], 4)
+                                                        if rates.get("int8_tops_measured") else None),
+                           "int8_peak_tops": rates.get("int8_tops_measured"),
                            "tensor_peak_note": "integer codes run as binary16 operands, so the peak is the measured "
                                                "dense bf16/f16 rate",
                            "kernel": "k_gemm_q8_tc (tcgen05.mma kind::f16, exact integer codes) + k_quantize_x_tc",
@@ -653,12 +867,22 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world):
 
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps
     q = build_decode_step("qwen3-0.6b-decode", dev, bq, inputs)
+    qargs = binding.gemv_sequence_args(seq_groups(q))
+    run, how = capture_or_direct(lambda: binding.gemv_sequence_call(bq.Q4_0, qargs, dev), stream)
+    ms = max_over_ranks(time_steps(run, stream, 50, 5, between=flush), dist)
     g = capture(lambda: run_step(q, bq, True), stream)
-    ms = max_over_ranks(time_graph(g, stream, 50, 5, between=flush), dist)
+    ms_pl = max_over_ranks(time_graph(g, stream, 50, 5, between=flush), dist)
     out["qwen3_0_6b_decode"] = {"metric": "Q4_0 decode GEMV weight GB/s", "unit": "GB/s",
                                 "value": round(aggregate_rate(q["weight_bytes"], world, ms * 1e-3) / 1e9, 1),
                                 "ms_per_step": round(ms, 4), "weight_bytes_per_step": q["weight_bytes"],
-                                "gemvs_per_step": len(q["mats"]), "launches_per_step": len(q["groups"]),
+                                "gemvs_per_step": len(q["mats"]), "launches_per_step": 1, "issue": how,
+                                "path": "bq_gemv_sequence (one persistent launch)",
+                                "per_launch": {"value": round(aggregate_rate(q["weight_bytes"], world,
+                                                                             ms_pl * 1e-3) / 1e9, 1),
+                                               "ms_per_step": round(ms_pl, 4),
+                                               "launches_per_step": 2 * len(q["groups"])},
+                                "hbm_frac_of_measured": round(q["weight_bytes"] / (ms * 1e-3) / 1e9 /
+                                                              peaks["hbm_gbs"], 4),
                                 "l2": "flushed between steps"}
     return out
 
@@ -682,6 +906,24 @@ def kernel_case(name, launches):
         y = torch.empty(M, device=dev)
         for i in range(launches):
             bq.gemv(t, mats[i % len(mats)], x, M, K, out=y)
+    elif name == "seq":
+        from block_quantized_weight_row_gb300 import binding
+        # the first 4 layers of the 7B step (455 MB of weights: beyond L2) in
+        # one bq_gemv_sequence launch, on two copies of the weights in turn
+        plan = [e for e in inputs.decode_plan("7b-decode") if e.layer < 4]
+        steps = []
+        for c in range(2):
+            groups, cur = [], None
+            for e in plan:
+                if cur is None or cur[5] != e.x_key:
+                    cur = ([], inputs.activation(e.K, e.x_seed + c, device=dev), [], e.K, [], e.x_key)
+                    groups.append(cur)
+                cur[0].append(bq.quantize_rows(bq.Q4_0, inputs.weight(e.M, e.K, e.w_seed + 7 * c, device=dev)))
+                cur[2].append(e.M)
+                cur[4].append(torch.empty(e.M, device=dev))
+            steps.append(binding.gemv_sequence_args([g[:5] for g in groups]))
+        for i in range(launches):
+            binding.gemv_sequence_call(bq.Q4_0, steps[i % 2], dev)
     elif name == "gemm":
         M, N, K = 4096, 512, 4096
         wq = bq.quantize_rows(bq.Q8_0, inputs.weight(M, K, 7200, device=dev))

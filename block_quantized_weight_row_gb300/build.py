@@ -15,6 +15,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(CSRC, "_build")
 LIB = os.path.join(HERE, "libbq.so")
+# measurement probe (tensor-op rates for the roofline denominators); not part of the libbq ABI
+PROBE_SRC = "probe_mma.cu"
+PROBE_LIB = os.path.join(HERE, "libbq_probe.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["bq_api.cu", "quantize.cu", "gemv.cu", "gemv_seq.cu", "gemm.cu", "gemm_tc.cu", "gemm_noalloc.cu", "attn.cu"]
@@ -61,11 +64,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             raise RuntimeError(f"nvcc failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
         return r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    probe_src = os.path.join(CSRC, PROBE_SRC)
+    probe_tmp = PROBE_LIB + f".tmp{os.getpid()}"
+    build_probe = force or _stale(PROBE_LIB, [probe_src, __file__])
+    if build_probe:
+        jobs.append([cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-shared", probe_src, "-o", probe_tmp])
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + 1) as ex:
         for out in ex.map(run, jobs):
             if verbose and out:
                 print(out, file=sys.stderr)
-    if force or jobs or _stale(LIB, objs):
+    if build_probe:
+        os.replace(probe_tmp, PROBE_LIB)
+    if force or any("-c" in j for j in jobs) or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
         run([cc, *ARCH, "-shared", "-o", tmp, *objs])
         os.replace(tmp, LIB)

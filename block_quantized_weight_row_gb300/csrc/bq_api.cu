@@ -317,7 +317,7 @@ int bq_gemv(int type, const void *W, const float *x, float *y, int64_t M, int64_
   return bq_gemv_multi(type, 1, &W, &y, &M, x, K);
 }
 
-size_t bq_gemv_sequence_workspace_size(void) { return 256; }
+size_t bq_gemv_sequence_workspace_size(void) { return (gemv_seq_sync_bytes() + 255) / 256 * 256; }
 
 int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *const *W, float *const *y,
                      const int64_t *M, const float *const *x, const int64_t *K) {

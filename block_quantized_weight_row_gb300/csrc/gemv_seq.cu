@@ -1,27 +1,43 @@
-// gemv_seq.cu — a sequence of decode GEMV batches in one persistent launch.
+// gemv_seq.cu — a decode step's GEMV batches in one persistent launch.
 //
-// A decode step is a chain of weight-matrix products, each bounded by the
+// A decode step is a run of weight-matrix products, each bounded by the
 // weight bytes it reads ("05. llama.cpp：从 GGUF 文件到本地推理服务",
-// §性能直觉：带宽决定 Decode，算力决定 Prefill). Launched one batch at a time, the
-// weight stream stops at every launch boundary: the next kernel's copies
-// begin only after the previous one has drained and the new one has started
-// and quantized its input. Here one launch covers the whole sequence and the
-// stream does not stop:
+// §性能直觉：带宽决定 Decode，算力决定 Prefill: decode reads every weight once per
+// token, so tokens/s is about bandwidth / weight bytes). Launched one batch at
+// a time, the weight stream stops at every launch boundary (the next kernel
+// starts, waits for the previous one, quantizes its input, refills its
+// pipeline). Here one launch covers the whole run and the stream never stops:
 //
-//   - batch g has the semantics of one bq_gemv_multi call issued after the
-//     calls of batches 0..g-1: its x is read only once every output of the
-//     earlier batches has been written (x may be such an output). A
-//     grid-wide barrier (a counter in global memory, bounded waits) separates
-//     the batches for the consumer warps;
-//   - the producer warp of every CTA has no such dependency (weights are
-//     never written by the sequence) and keeps streaming the next batches'
-//     rows into its shared-memory ring while the consumers wait at a barrier
-//     and quantize the new x; the ring absorbs that pause;
-//   - the consumer code (x's Q8_0 records, the group dot product) is the one
-//     of the per-batch kernel, so the results are those of bq_gemv_multi.
-// The launch is cooperative, so that every CTA of the grid is resident and
-// the barrier cannot wait for a CTA that has not started. Every CTA takes a
-// contiguous, balanced range of each batch's rows.
+//   - one CTA per SM, three roles:
+//       producer warp   streams this CTA's rows of every batch, in batch
+//                       order, with 1-D bulk copies into a ring of shared-
+//                       memory stages (mbarrier-completed); it depends on
+//                       nothing but free stages, since the run never writes
+//                       a weight;
+//       x warps         quantize the input of the CTA's next batch into the
+//                       second of two record buffers (Q8_0 codes, scales,
+//                       code sums, the layout of the per-launch GEMV) while
+//                       the consumers use the first;
+//       consumer warps  dot every row of a stage with the records, reduce the
+//                       row's lanes and write y;
+//   - batch g has the result of one bq_gemv_multi call issued after the calls
+//     of batches 0..g-1. Only memory explains an order between them: when x[g]
+//     overlaps an output of an earlier batch, or an output of batch g overlaps
+//     the input of an earlier batch, batch g waits until every CTA has
+//     finished the latest such batch (a per-batch counter in global memory,
+//     incremented once per CTA with release semantics, polled with acquire
+//     loads, all waits bounded). The host derives these waits from the
+//     pointers; batches that share no memory never wait;
+//   - every CTA takes a contiguous, balanced range of each batch's rows, the
+//     ranges rotating over the CTAs from batch to batch so that the CTAs'
+//     total bytes stay level;
+//   - consumer warps take the row slots of the stage sequence round robin, so
+//     every warp gets an equal share whatever the stage sizes;
+//   - per row the arithmetic (records, group order, lanes per row, shuffle
+//     tree) is that of the per-launch kernel, so the outputs are bit-identical
+//     to bq_gemv_multi.
+// The launch is cooperative (every CTA resident), so a wait on other CTAs
+// cannot wait for a CTA that has not started.
 #include <algorithm>
 #include <memory>
 #include <vector>
@@ -37,25 +53,27 @@ using gemv::GroupWords;
 using gemv::group_terms;
 using gemv::kXRecBytes;
 using gemv::kXRecWords;
-using gemv::quantize_x_records;
+using gemv::quantize_x_records_2lane;
 
-constexpr int kSeqConsumers = 8;  // consumer warps per CTA
-constexpr int kSeqThreads = (kSeqConsumers + 1) * 32;
-constexpr int kSeqMaxGroups = 256;  // per launch; longer sequences take several launches
+constexpr int kSqConsumers = 16;  // consumer warps per CTA
+constexpr int kSqXWarps = 3;      // warps quantizing x (20 warps: 96 registers a thread)
+constexpr int kSqXThreads = kSqXWarps * 32;
+constexpr int kSqProducer = kSqConsumers + kSqXWarps;  // warp index of the producer
+constexpr int kSqThreads = (kSqConsumers + kSqXWarps + 1) * 32;
+constexpr int kSeqMaxGroups = 256;  // per launch; longer runs take several launches
 constexpr int kSeqMaxMats = 512;
 constexpr uint32_t kSeqDrainLimit = 1u << 26;
+constexpr int kRowRotation = 37;  // CTA range rotation per batch
+constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
 
 struct SeqGroup {
   const float *x;
-  int K;              // a multiple of 256
-  int first_mat;      // matrices first_mat .. first_mat + n_mats - 1 of SeqArgs::m
+  int K;          // a multiple of 256
+  int first_mat;  // matrices first_mat .. first_mat + n_mats - 1 of SeqArgs::m
   int n_mats;
-  int rows;           // rows of all the batch's matrices
-  int groups8;        // K / 256: groups of 8 blocks per row
-  int lanes_per_row;  // power of two <= 32
-  int rows_per_warp;  // 32 / lanes_per_row
-  int row_bytes;
-  int stage_rows;     // rows per stage (stage_rows * row_bytes <= slot_bytes)
+  int rows;       // rows of all the batch's matrices
+  int wait_on;    // batch (of this launch) every CTA must have finished first, or -1
+  int signal;     // nonzero: a later batch waits for this one
 };
 
 struct SeqMat {
@@ -70,116 +88,142 @@ struct SeqArgs {
   SeqMat m[kSeqMaxMats];
   int n_groups;
   int stages;
-  int slot_bytes;
-  int xrec_bytes;       // records of the largest K of the sequence
-  unsigned *sync;       // [0]: CTAs done with a batch (counts up), [1]: abort; zeroed before the launch
+  int slot_bytes;  // bytes of one ring stage
+  int xrec_bytes;  // bytes of one record buffer (the largest K of the launch)
+  unsigned *sync;  // [0]: abort flag, [1 + g]: CTAs done with batch g; zeroed before the launch
   unsigned *err;
   uint32_t spin_limit;
 };
 
-// Stage sequence of one CTA over every batch: rows [r0, r1) of batch g in
-// stages that never straddle two matrices. Producer and consumers walk it in
-// the same order.
-struct SeqCursor {
-  int g, row, r1;
-  __device__ __forceinline__ void start(const SeqArgs &a, int gg) {
-    g = gg;
-    for (; g < a.n_groups; ++g) {
-      const int rows = a.g[g].rows;
-      row = int(int64_t(rows) * blockIdx.x / gridDim.x);
-      r1 = int(int64_t(rows) * (blockIdx.x + 1) / gridDim.x);
-      if (row < r1) return;
-    }
-  }
-  // matrix and row count of the stage at the cursor
-  __device__ __forceinline__ void stage(const SeqArgs &a, int &mat, int &nrows) const {
-    const SeqGroup &G = a.g[g];
-    mat = G.first_mat;
-    while (mat + 1 < G.first_mat + G.n_mats && row >= a.m[mat + 1].row_start) ++mat;
-    const int mat_end = (mat + 1 < G.first_mat + G.n_mats) ? a.m[mat + 1].row_start : G.rows;
-    nrows = min(min(G.stage_rows, r1 - row), mat_end - row);
-  }
-  __device__ __forceinline__ void advance(const SeqArgs &a, int nrows) {
-    row += nrows;
-    if (row >= r1) start(a, g + 1);
+// Per-batch shape, derived from K the same way on every side.
+template <int TYPE>
+struct BatchShape {
+  int groups8;    // K / 256 groups of 8 blocks per row
+  int L;          // lanes per row: a power of two <= 32
+  int rpw;        // rows per warp pass = 32 / L
+  int row_bytes;
+  int stage_rows;
+  __device__ __forceinline__ BatchShape(int K, int slot_bytes) {
+    groups8 = K >> 8;
+    L = groups8 <= 1 ? 1 : min(32, 1 << (32 - __clz(groups8 - 1)));
+    rpw = 32 / L;
+    row_bytes = (K / kQK) * Fmt<TYPE>::kBytes;
+    stage_rows = max(1, slot_bytes / row_bytes);
   }
 };
 
-__device__ __forceinline__ bool seq_aborted(const SeqArgs &a, volatile int *cta_abort) {
-  return *cta_abort || *reinterpret_cast<volatile unsigned *>(a.sync + 1);
+// Rows [r0, r1) of batch g taken by this CTA.
+__device__ __forceinline__ void cta_rows(int rows, int g, int &r0, int &r1) {
+  const int G = int(gridDim.x);
+  const int p = int((blockIdx.x + unsigned(g) * kRowRotation) % unsigned(G));
+  r0 = int(int64_t(rows) * p / G);
+  r1 = int(int64_t(rows) * (p + 1) / G);
+}
+
+// Matrix of the batch holding batch row `row`, and the rows of the stage that
+// starts there (at most stage_rows, never past r1 or the matrix's end).
+__device__ __forceinline__ void stage_at(const SeqArgs &a, const SeqGroup &G, int row, int r1, int stage_rows,
+                                         int &mat, int &nrows) {
+  mat = G.first_mat;
+  const int last = G.first_mat + G.n_mats - 1;
+  while (mat < last && row >= a.m[mat + 1].row_start) ++mat;
+  const int mat_end = mat < last ? a.m[mat + 1].row_start : G.rows;
+  nrows = min(min(stage_rows, r1 - row), mat_end - row);
+}
+
+__device__ __forceinline__ bool grid_aborted(const SeqArgs &a) {
+  return *reinterpret_cast<volatile unsigned *>(a.sync) != 0u;
 }
 
 __device__ __forceinline__ void seq_abort(const SeqArgs &a, volatile int *cta_abort) {
   *cta_abort = 1;
-  atomicExch(a.sync + 1, 1u);
+  atomicExch(a.sync, 1u);
   atomicOr(a.err, kErrTimeout);
 }
 
-// Bounded mbarrier wait that gives up early once the CTA or the grid aborted.
+// Bounded mbarrier wait that also gives up once the CTA or the grid aborted.
+// Each poll may sleep up to kSleepNs (the warp wakes when the phase
+// completes), so waiting warps take almost no issue slots from working ones.
+constexpr uint32_t kSleepNs = 1000;
 __device__ __forceinline__ bool seq_wait(const SeqArgs &a, uint64_t *bar, uint32_t parity, volatile int *cta_abort) {
   for (uint32_t i = 0; i < a.spin_limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15) == 15 && seq_aborted(a, cta_abort)) return false;
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    if ((i & 3) == 3 && (*cta_abort || grid_aborted(a))) return false;
   }
   seq_abort(a, cta_abort);
   return false;
 }
 
-// Until `target` CTAs have arrived at the grid counter (acquire), bounded.
-__device__ __forceinline__ bool seq_grid_wait(const SeqArgs &a, unsigned target, volatile int *cta_abort) {
+// Until every CTA has counted itself done with batch `g` (acquire), bounded.
+__device__ __forceinline__ bool seq_batch_wait(const SeqArgs &a, int g, volatile int *cta_abort) {
+  const unsigned target = gridDim.x;
+  const unsigned *cnt = a.sync + 1 + g;
   for (uint32_t i = 0; i < a.spin_limit; ++i) {
     unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.sync) : "memory");
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
     if (v >= target) return true;
-    if (seq_aborted(a, cta_abort)) return false;
-    __nanosleep(32);
+    if (*cta_abort || grid_aborted(a)) return false;
+    __nanosleep(20);
   }
   seq_abort(a, cta_abort);
   return false;
 }
 
 template <int TYPE>
-__global__ void __launch_bounds__(kSeqThreads, 2) k_gemv_seq(const __grid_constant__ SeqArgs a) {
+__global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constant__ SeqArgs a) {
   constexpr int GW = GroupWords<TYPE>::kWords;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_go;
-  uint32_t *xrec = reinterpret_cast<uint32_t *>(smem);
-  uint8_t *ring = smem + a.xrec_bytes;
+  // record buffer b at smem + b * xrec_bytes
+  uint8_t *ring = smem + 2 * size_t(a.xrec_bytes);
   uint64_t *full = reinterpret_cast<uint64_t *>(ring + size_t(a.stages) * a.slot_bytes);
   uint64_t *empty = full + a.stages;
-  volatile int *cta_abort = reinterpret_cast<volatile int *>(empty + a.stages);
+  uint64_t *rfull = empty + a.stages;  // [2]: records of buffer b written
+  uint64_t *rempty = rfull + 2;        // [2]: records of buffer b no longer read
+  volatile int *cta_abort = reinterpret_cast<volatile int *>(rempty + 2);
+  __shared__ int s_go;  // dependency wait result, broadcast to the consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kSeqConsumers);  // every consumer warp releases every stage
+      mbar_init(&empty[s], kSqConsumers);  // every consumer warp releases every stage
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&rfull[b], kSqXThreads);  // every x thread, after its record stores
+      mbar_init(&rempty[b], kSqConsumers);
     }
     *cta_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kSeqConsumers) {
+  if (warp == kSqProducer) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       int issued = 0;
       const uint64_t policy = l2_evict_first_policy();  // every weight is read once
-      SeqCursor cur;
-      cur.start(a, 0);
-      for (int j = 0; cur.g < a.n_groups; ++j) {
-        const int s = j % S;
-        if (j >= S && !seq_wait(a, &empty[s], uint32_t((j / S - 1) & 1), cta_abort)) break;
-        int mat, nrows;
-        cur.stage(a, mat, nrows);
-        const int row_bytes = a.g[cur.g].row_bytes;
-        const uint32_t bytes = uint32_t(nrows) * uint32_t(row_bytes);
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s_hint(ring + size_t(s) * a.slot_bytes,
-                      a.m[mat].W + int64_t(cur.row - a.m[mat].row_start) * row_bytes, bytes, &full[s], policy);
-        cur.advance(a, nrows);
-        issued = j + 1;
+      bool stop = false;
+      for (int g = 0, j = 0; g < a.n_groups && !stop; ++g) {
+        const SeqGroup &G = a.g[g];
+        const BatchShape<TYPE> sh(G.K, a.slot_bytes);
+        int row, r1;
+        cta_rows(G.rows, g, row, r1);
+        while (row < r1) {
+          const int s = j % S;
+          if (j >= S && !seq_wait(a, &empty[s], uint32_t((j / S - 1) & 1), cta_abort)) {
+            stop = true;
+            break;
+          }
+          int mat, nrows;
+          stage_at(a, G, row, r1, sh.stage_rows, mat, nrows);
+          const uint32_t bytes = uint32_t(nrows) * uint32_t(sh.row_bytes);
+          mbar_arrive_expect_tx(&full[s], bytes);
+          bulk_g2s_hint(ring + size_t(s) * a.slot_bytes,
+                        a.m[mat].W + int64_t(row - a.m[mat].row_start) * sh.row_bytes, bytes, &full[s], policy);
+          row += nrows;
+          issued = ++j;
+        }
       }
       // never leave with a copy in flight: wait for the last use of each slot
       for (int s = 0; s < min(S, issued); ++s) {
@@ -187,83 +231,112 @@ __global__ void __launch_bounds__(kSeqThreads, 2) k_gemv_seq(const __grid_consta
         if (!mbar_wait_bounded(&full[s], uint32_t((last / S) & 1), kSeqDrainLimit)) atomicOr(a.err, kErrTimeout);
       }
     }
+  } else if (warp >= kSqConsumers) {
+    // ------------------------------------------------------------ x warps --
+    // The records of every batch that waits for nothing, one batch ahead of
+    // the consumers. A batch that waits for an earlier one is quantized by
+    // the consumers themselves once the wait is over (they are idle then).
+    const int xt = threadIdx.x - kSqConsumers * 32;
+    for (int g = 0, k = 0; g < a.n_groups; ++g) {
+      const SeqGroup &G = a.g[g];
+      int r0, r1;
+      cta_rows(G.rows, g, r0, r1);
+      if (r0 >= r1) continue;  // no rows here: nothing read, nothing written
+      const int b = k++ & 1;
+      if (G.wait_on >= 0) continue;
+      // the buffer's previous batch is done once its consumers released it
+      if (k > 2 && !seq_wait(a, &rempty[b], uint32_t((((k - 1) >> 1) - 1) & 1), cta_abort)) break;
+      quantize_x_records_2lane(G.x, G.K / kQK, reinterpret_cast<uint32_t *>(smem + b * a.xrec_bytes), xt,
+                               kSqXThreads);
+      mbar_arrive(&rfull[b]);
+    }
   } else {
     // --------------------------------------------------------- consumers --
-    const int tid = threadIdx.x;
-    SeqCursor cur;
-    cur.start(a, 0);
-    int j = 0;  // stage index, the producer's numbering
-    bool skip = false;
-    for (int g = 0; g < a.n_groups; ++g) {
-      if (g > 0) {
-        // every CTA has finished batch g-1, so its outputs (which this
-        // batch's x may be) are written and visible
-        if (tid == 0) {
-          const bool ok = !skip && seq_grid_wait(a, unsigned(g) * gridDim.x, cta_abort);
-          if (ok) __threadfence();
-          s_go = ok ? 1 : 0;
-        }
-        named_bar_sync(1, kSeqConsumers * 32);
-        if (!s_go) break;  // uniform: written before the barrier, rewritten only after the next one
-      }
+    bool skip = false;  // a wait ran out: walk on without waiting or computing
+    int j = 0;          // stage index, the producer's numbering
+    int slot_base = 0;  // row slots of all earlier stages (round robin over the warps)
+    uint32_t nq = 0;    // bit b: parity of the x warps' uses of buffer b so far (phases of rfull)
+    for (int g = 0, k = 0; g < a.n_groups; ++g) {
       const SeqGroup &G = a.g[g];
-      const bool mine = cur.g == g;  // this CTA has rows of batch g
-      if (mine) {
-        quantize_x_records(G.x, G.K / kQK, xrec, tid, kSeqConsumers * 32, int(blockIdx.x) * 8);
-        named_bar_sync(1, kSeqConsumers * 32);
-      }
-      const int L = G.lanes_per_row;
-      const int rr = lane / L;  // row (within the warp's pass) handled by this lane
-      const int gl = lane % L;  // first group of that row handled by this lane
-      while (cur.g == g) {
-        const int s = j % S;
-        if (!skip) {
+      const BatchShape<TYPE> sh(G.K, a.slot_bytes);
+      int row, r1;
+      cta_rows(G.rows, g, row, r1);
+      if (row < r1) {
+        const int b = k & 1;
+        if (G.wait_on >= 0) {
+          // batch wait_on's outputs are (or overlap) this batch's x, or this
+          // batch's outputs overwrite its x: once every CTA has finished it,
+          // all consumer threads quantize x into the buffer (its last batch,
+          // k - 2, is done: the consumers run the batches in order)
+          if (threadIdx.x == 0) s_go = (!skip && seq_batch_wait(a, G.wait_on, cta_abort)) ? 1 : 0;
+          named_bar_sync(kBarConsumers, kSqConsumers * 32);
+          if (!s_go) skip = true;
+          if (!skip)  // read past L1: x was written by other CTAs during this launch
+            quantize_x_records_2lane(G.x, G.K / kQK, reinterpret_cast<uint32_t *>(smem + b * a.xrec_bytes),
+                                     threadIdx.x, kSqConsumers * 32);
+          // the records are written, and s_go is read before it is rewritten
+          named_bar_sync(kBarConsumers, kSqConsumers * 32);
+        } else {
+          if (!skip) skip = !seq_wait(a, &rfull[b], (nq >> b) & 1u, cta_abort);
+          nq ^= 1u << b;
+        }
+        const uint32_t *xr = reinterpret_cast<const uint32_t *>(smem + b * a.xrec_bytes);
+        const int rr = lane / sh.L;  // row of the slot handled by this lane
+        const int gl = lane % sh.L;  // first group of that row handled by this lane
+        while (row < r1) {
+          const int s = j % S;
           // every warp consumes every stage in order, so a parity wait is
-          // never more than one phase ahead of the barrier; lane 0 waits
-          int ok = 1;
-          if (lane == 0) ok = seq_wait(a, &full[s], uint32_t((j / S) & 1), cta_abort);
-          ok = __shfl_sync(kFull, ok, 0);
-          __syncwarp();
-          skip = !ok;
-        }
-        int mat, nrows;
-        cur.stage(a, mat, nrows);
-        if (!skip) {
-          float *yp = a.m[mat].y + (cur.row - a.m[mat].row_start);
-          const uint8_t *stage = ring + size_t(s) * a.slot_bytes;
-          for (int pr = warp * G.rows_per_warp; pr < nrows; pr += kSeqConsumers * G.rows_per_warp) {
-            const int row = pr + rr;
-            float acc = 0.0f;
-            if (row < nrows) {
-              const uint8_t *rowp = stage + size_t(row) * G.row_bytes;
-              for (int q = gl; q < G.groups8; q += L) {
-                uint32_t w[GW];
-                const uint4 *src = reinterpret_cast<const uint4 *>(rowp + size_t(q) * GW * 4);
+          // never more than one phase ahead of the barrier
+          if (!skip) skip = !seq_wait(a, &full[s], uint32_t((j / S) & 1), cta_abort);
+          int mat, nrows;
+          stage_at(a, G, row, r1, sh.stage_rows, mat, nrows);
+          const int nslots = (nrows + sh.rpw - 1) / sh.rpw;
+          if (!skip) {
+            float *yp = a.m[mat].y + (row - a.m[mat].row_start);
+            const uint8_t *stage = ring + size_t(s) * a.slot_bytes;
+            for (int t = (warp - slot_base % kSqConsumers + kSqConsumers) % kSqConsumers; t < nslots;
+                 t += kSqConsumers) {
+              const int r = t * sh.rpw + rr;
+              float acc = 0.0f;
+              if (r < nrows) {
+                const uint8_t *rowp = stage + size_t(r) * sh.row_bytes;
+                for (int q = gl; q < sh.groups8; q += sh.L) {
+                  uint32_t w[GW];
+                  const uint4 *src = reinterpret_cast<const uint4 *>(rowp + size_t(q) * GW * 4);
 #pragma unroll
-                for (int k = 0; k < GW / 4; ++k) {
-                  const uint4 u = src[k];
-                  w[4 * k] = u.x;
-                  w[4 * k + 1] = u.y;
-                  w[4 * k + 2] = u.z;
-                  w[4 * k + 3] = u.w;
+                  for (int c = 0; c < GW / 4; ++c) {
+                    const uint4 u = src[c];
+                    w[4 * c] = u.x;
+                    w[4 * c + 1] = u.y;
+                    w[4 * c + 2] = u.z;
+                    w[4 * c + 3] = u.w;
+                  }
+                  acc = group_terms<TYPE>(w, xr + q * kXRecWords, acc);
                 }
-                acc = group_terms<TYPE>(w, xrec + q * kXRecWords, acc);
               }
+              for (int off = sh.L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+              if (gl == 0 && r < nrows) yp[r] = acc;
             }
-            for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-            if (gl == 0 && row < nrows) yp[row] = acc;
           }
+          slot_base += nslots;
+          row += nrows;
+          __syncwarp();
+          if (!skip && lane == 0) mbar_arrive(&empty[s]);
+          ++j;
         }
-        cur.advance(a, nrows);
         __syncwarp();
-        if (!skip && lane == 0) mbar_arrive(&empty[s]);
-        ++j;
+        if (!skip && lane == 0) mbar_arrive(&rempty[b]);
+        ++k;
       }
-      // every row of batch g this CTA owns is written, and x's records are free
-      named_bar_sync(1, kSeqConsumers * 32);
-      if (tid == 0 && g + 1 < a.n_groups && !skip) {
-        __threadfence();
-        atomicAdd(a.sync, 1u);
+      if (G.signal) {
+        // every row of batch g (and of every earlier batch) this CTA owns is
+        // written: count the CTA done with batch g, after a fence that makes
+        // the consumers' stores visible to the whole GPU
+        named_bar_sync(kBarConsumers, kSqConsumers * 32);
+        if (threadIdx.x == 0 && !skip) {
+          __threadfence();
+          atomicAdd(a.sync + 1 + g, 1u);
+        }
       }
     }
   }
@@ -274,38 +347,57 @@ __global__ void __launch_bounds__(kSeqThreads, 2) k_gemv_seq(const __grid_consta
 
 namespace {
 
-int pow2_at_least(int v) {
-  int p = 1;
-  while (p < v) p <<= 1;
-  return p;
-}
+bool spans_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
-// One launch over batches [g0, g1) (all with K % 256 == 0 and rows > 0).
+// One launch over the batches `groups` (each with K % 256 == 0 and rows > 0).
 template <int TYPE>
 cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<int> &mat0, const int *n_mats,
                              const uint8_t *const *W, float *const *y, const int64_t *M, const float *const *x,
                              const int64_t *K, unsigned *sync, const DeviceInfo *di, cudaStream_t stream) {
   constexpr int BB = Fmt<TYPE>::kBytes;
   std::unique_ptr<SeqArgs> a(new SeqArgs{});
-  int xrec_bytes = 0, max_row = 0, max_pass = 0;
-  for (size_t i = 0; i < groups.size(); ++i) {
+  const int n = int(groups.size());
+  int xrec_bytes = 0, max_row = 0;
+  // bytes per distinct row length, to choose the stage size
+  std::vector<std::pair<int, int64_t>> by_row;
+  for (int i = 0; i < n; ++i) {
     const int gi = groups[i];
-    const int groups8 = int(K[gi] / 256);
     const int row_bytes = int(K[gi] / kQK) * BB;
-    const int L = std::min(32, pow2_at_least(groups8));
-    xrec_bytes = std::max(xrec_bytes, groups8 * kXRecBytes);
+    xrec_bytes = std::max(xrec_bytes, int(K[gi] / 256) * kXRecBytes);
     max_row = std::max(max_row, row_bytes);
-    max_pass = std::max(max_pass, kSeqConsumers * (32 / L) * row_bytes);
+    int64_t rows = 0;
+    for (int k = 0; k < n_mats[gi]; ++k) rows += M[mat0[gi] + k];
+    auto it = std::find_if(by_row.begin(), by_row.end(), [&](const std::pair<int, int64_t> &p) {
+      return p.first == row_bytes;
+    });
+    if (it == by_row.end())
+      by_row.push_back({row_bytes, rows * row_bytes});
+    else
+      it->second += rows * row_bytes;
   }
   xrec_bytes = (xrec_bytes + 127) / 128 * 128;
-  // Two CTAs per SM (16 consumer warps): a ring of at least 3 stages within
-  // half an SM; a stage is one pass of the consumer warps, cut to fit.
-  const int reserve = 1024 + 128;  // per-CTA system reservation and static shared memory
-  const int budget = std::min(di->smem_per_sm / 2 - reserve, di->max_smem_optin) - xrec_bytes - 256;
-  int slot = std::min(max_pass, budget / 3) / 16 * 16;
-  if (slot < max_row) return cudaErrorInvalidValue;  // the ABI layer bounds K, so this does not happen
-  const int stages = std::min(8, budget / slot);
-  a->n_groups = int(groups.size());
+  // Shared memory: two record buffers, the ring, 2 (S + 2) barriers and the
+  // abort flag. Stages of 16-40 KB (large copies: the copy cost is per copy),
+  // the size that wastes the fewest bytes on this launch's row lengths.
+  const int reserve = 1024;  // per-CTA system reservation
+  const int budget = std::min(di->smem_per_sm - reserve, di->max_smem_optin) - 2 * xrec_bytes - 1024;
+  static const int forced_slot = tuning_value("BQ_GEMV_SEQ_SLOT_BYTES");  // read once per process
+  int slot = 0;
+  double best = -1.0;
+  for (int c = std::max(16 << 10, (max_row + 15) / 16 * 16); c <= (40 << 10); c += 16) {
+    if (budget / c < 4) break;
+    double used = 0.0;
+    for (const auto &p : by_row) used += double(p.second) * double((c / p.first) * p.first) / double(c);
+    if (used > best * (1.0 + 1e-9)) {
+      best = used;
+      slot = c;
+    }
+  }
+  if (forced_slot > 0) slot = (forced_slot + 15) / 16 * 16;
+  if (slot < max_row) slot = (max_row + 15) / 16 * 16;
+  const int stages = std::min(32, budget / slot);
+  if (stages < 2) return cudaErrorInvalidValue;  // the ABI layer bounds K, so this does not happen
+  a->n_groups = n;
   a->stages = stages;
   a->slot_bytes = slot;
   a->xrec_bytes = xrec_bytes;
@@ -313,17 +405,13 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   a->err = di->err_word;
   a->spin_limit = spin_limit();
   int nm = 0;
-  for (size_t i = 0; i < groups.size(); ++i) {
+  for (int i = 0; i < n; ++i) {
     const int gi = groups[i];
     SeqGroup &G = a->g[i];
     G.x = x[gi];
     G.K = int(K[gi]);
-    G.groups8 = G.K / 256;
-    G.lanes_per_row = std::min(32, pow2_at_least(G.groups8));
-    G.rows_per_warp = 32 / G.lanes_per_row;
-    G.row_bytes = (G.K / kQK) * BB;
-    G.stage_rows = std::max(1, std::min(kSeqConsumers * G.rows_per_warp, slot / G.row_bytes));
     G.first_mat = nm;
+    G.wait_on = -1;
     int rows = 0;
     for (int k = 0; k < n_mats[gi]; ++k) {
       const int mi = mat0[gi] + k;
@@ -337,24 +425,43 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
     G.n_mats = nm - G.first_mat;
     G.rows = rows;
   }
-  const size_t smem = size_t(xrec_bytes) + size_t(stages) * slot + 16 * size_t(stages) + 16;
+  // Orders that memory imposes: batch i waits for the latest earlier batch
+  // whose outputs its x reads, or whose x its outputs overwrite. (Outputs
+  // never overlap outputs; the ABI layer rejects that.)
+  for (int i = 1; i < n; ++i) {
+    const SeqGroup &G = a->g[i];
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(G.x), x1 = x0 + uintptr_t(G.K) * 4;
+    for (int p = i - 1; p >= 0 && a->g[i].wait_on < 0; --p) {
+      const SeqGroup &P = a->g[p];
+      const uintptr_t px0 = reinterpret_cast<uintptr_t>(P.x), px1 = px0 + uintptr_t(P.K) * 4;
+      bool dep = false;
+      for (int mp = P.first_mat; mp < P.first_mat + P.n_mats && !dep; ++mp) {
+        const uintptr_t y0 = reinterpret_cast<uintptr_t>(a->m[mp].y);
+        const int rows = (mp + 1 < P.first_mat + P.n_mats ? a->m[mp + 1].row_start : P.rows) - a->m[mp].row_start;
+        dep = spans_overlap(x0, x1, y0, y0 + uintptr_t(rows) * 4);
+      }
+      for (int mi = G.first_mat; mi < G.first_mat + G.n_mats && !dep; ++mi) {
+        const uintptr_t y0 = reinterpret_cast<uintptr_t>(a->m[mi].y);
+        const int rows = (mi + 1 < G.first_mat + G.n_mats ? a->m[mi + 1].row_start : G.rows) - a->m[mi].row_start;
+        dep = spans_overlap(px0, px1, y0, y0 + uintptr_t(rows) * 4);
+      }
+      if (dep) {
+        a->g[i].wait_on = p;
+        a->g[p].signal = 1;
+      }
+    }
+  }
+  const size_t smem = 2 * size_t(xrec_bytes) + size_t(stages) * slot + 8 * (2 * size_t(stages) + 4) + 16;
   const void *fn = reinterpret_cast<const void *>(k_gemv_seq<TYPE>);
   cudaError_t e = ensure_smem(fn, int(smem));
   if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv_seq<TYPE>, kSeqThreads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  per_sm = std::min(per_sm, 2);
-  static const int forced = tuning_value("BQ_GEMV_SEQ_CTAS_PER_SM");  // read once per process
-  if (forced) per_sm = std::min(per_sm, forced);
-  if ((e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), stream)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(sync, 0, sizeof(unsigned) * size_t(1 + n), stream)) != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(di->sm_count * per_sm));
-  cfg.blockDim = dim3(kSeqThreads);
+  cfg.gridDim = dim3(unsigned(di->sm_count));
+  cfg.blockDim = dim3(kSqThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -372,7 +479,8 @@ cudaError_t launch_seq_typed(int n_groups, const int *n_mats, const uint8_t *con
   std::vector<int> mat0(size_t(n_groups) + 1, 0);
   for (int gi = 0; gi < n_groups; ++gi) mat0[gi + 1] = mat0[gi] + n_mats[gi];
   // batches in order, cut into launches of at most kSeqMaxGroups batches and
-  // kSeqMaxMats matrices; batches without rows are left out
+  // kSeqMaxMats matrices (the stream orders the launches); batches without
+  // rows are left out
   std::vector<int> chunk;
   int chunk_mats = 0;
   for (int gi = 0; gi <= n_groups; ++gi) {
@@ -395,6 +503,8 @@ cudaError_t launch_seq_typed(int n_groups, const int *n_mats, const uint8_t *con
 }
 
 }  // namespace
+
+size_t gemv_seq_sync_bytes() { return sizeof(unsigned) * size_t(1 + kSeqMaxGroups); }
 
 cudaError_t launch_gemv_seq(int type, int n_groups, const int *n_mats, const uint8_t *const *W, float *const *y,
                             const int64_t *M, const float *const *x, const int64_t *K, unsigned *sync,

@@ -1,0 +1,98 @@
+// probe_mma.cu — measurement probe (libbq_probe.so, not part of the libbq
+// ABI): the issue rate of the legacy warp-level tensor-core instructions on
+// this GPU, the denominator the prefill GEMM's int8 target is stated against.
+// sm_103a has no int8 form of tcgen05.mma, so the int8 tensor path left is
+// mma.sync with s8 operands; its f16 form is measured beside it.
+//
+// Every warp issues long runs of independent mma.sync instructions on
+// register operands (no memory traffic); the accumulators are summed and
+// stored at the end so that no instruction is dead. Timed with CUDA events
+// on the legacy default stream.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace {
+
+constexpr int kChains = 8;  // independent accumulators per warp: covers the pipeline latency
+
+__global__ void __launch_bounds__(256) k_mma_s8(int iters, int *out) {
+  const uint32_t t = threadIdx.x + 1;
+  const uint32_t a0 = t * 0x01010101u, a1 = t * 0x02020202u, a2 = t * 0x03030303u, a3 = t * 0x05050505u;
+  const uint32_t b0 = t * 0x07070707u, b1 = t * 0x0b0b0b0bu;
+  int c[kChains][4] = {};
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int k = 0; k < kChains; ++k)
+      asm volatile(
+          "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+          "{%0,%1,%2,%3};"
+          : "+r"(c[k][0]), "+r"(c[k][1]), "+r"(c[k][2]), "+r"(c[k][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) s += c[k][0] ^ c[k][1] ^ c[k][2] ^ c[k][3];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+__global__ void __launch_bounds__(256) k_mma_f16(int iters, int *out) {
+  const uint32_t t = threadIdx.x & 7;
+  // small exact binary16 pairs (1.0 + t/8), so the sums stay finite
+  const uint32_t h = 0x3c00u + (t << 7);
+  const uint32_t a = h | (h << 16);
+  float c[kChains][4] = {};
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int k = 0; k < kChains; ++k)
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+          "{%0,%1,%2,%3};"
+          : "+f"(c[k][0]), "+f"(c[k][1]), "+f"(c[k][2]), "+f"(c[k][3])
+          : "r"(a), "r"(a), "r"(a), "r"(a), "r"(a), "r"(a));
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) s += c[k][0] + c[k][1] + c[k][2] + c[k][3];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = __float_as_int(s);
+}
+
+}  // namespace
+
+// Tensor-op rate of mma.sync on the current device in tera-ops per second
+// (2 * m * n * k per instruction): kind 0 = m16n8k32 s8 x s8 -> s32, kind 1
+// = m16n8k16 f16 x f16 -> f32. Grid: ctas_per_sm x SMs of 8 warps. Returns 0
+// on success, -1 on a bad argument, -5 when a CUDA call fails.
+extern "C" int bq_probe_mma_rate(int kind, int iters, int ctas_per_sm, double *tops) {
+  if ((kind != 0 && kind != 1) || iters < 1 || ctas_per_sm < 1 || !tops) return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -5;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -5;
+  const int grid = sms * ctas_per_sm, block = 256;
+  int *out = nullptr;
+  if (cudaMalloc(&out, size_t(grid) * block * sizeof(int)) != cudaSuccess) return -5;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  auto launch = [&](int it) {
+    if (kind == 0)
+      k_mma_s8<<<grid, block>>>(it, out);
+    else
+      k_mma_f16<<<grid, block>>>(it, out);
+  };
+  launch(iters / 8 + 1);  // warm-up
+  cudaEventRecord(e0);
+  launch(iters);
+  cudaEventRecord(e1);
+  cudaError_t err = cudaEventSynchronize(e1);
+  float ms = 0.0f;
+  if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, e0, e1);
+  if (err == cudaSuccess) err = cudaGetLastError();
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaFree(out);
+  if (err != cudaSuccess || ms <= 0.0f) return -5;
+  const double ops_per_mma = kind == 0 ? 2.0 * 16 * 8 * 32 : 2.0 * 16 * 8 * 16;
+  const double mmas = double(grid) * (block / 32) * double(iters) * kChains;
+  *tops = mmas * ops_per_mma / (double(ms) * 1e-3) / 1e12;
+  return 0;
+}

@@ -79,6 +79,13 @@ def weight(M: int, K: int, seed: int, device="cpu") -> torch.Tensor:
     return normal((M, K), WEIGHT_STD, seed, device)
 
 
+def chain_weight(M: int, K: int, seed: int, device="cpu") -> torch.Tensor:
+    """W ~ N(0, 1/K): a product y = W x then has per-element variance equal to
+    that of x, so that a chain of products (each reading the previous output)
+    stays in range however long it is."""
+    return normal((M, K), K ** -0.5, seed, device)
+
+
 def activation(K: int, seed: int, device="cpu", rows: int | None = None) -> torch.Tensor:
     shape = (K,) if rows is None else (rows, K)
     return normal(shape, 1.0, seed, device)

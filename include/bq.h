@@ -149,26 +149,30 @@ int bq_gemv_multi(int type, int n, const void *const *W_blocks, float *const *y,
 #define BQ_GEMV_SEQ_MAX_K 16384
 
 /* A sequence of decode GEMV batches in one persistent launch (a decode step's
- * matrix products, "05. llama.cpp…", §性能直觉：带宽决定 Decode). Batch g has
- * n_mats[g] matrices that read the input x[g] and the same K[g]; its
- * matrices are entries mat0 .. mat0 + n_mats[g] - 1 of the flattened arrays
- * W_blocks, y and M, mat0 being the sum of the earlier n_mats. The result is
- * that of one bq_gemv_multi call per batch, issued in order: batch g reads
- * x[g] only after every output of batches 0..g-1 has been written, so x[g]
- * may be (part of) such an output. Inside the launch a grid-wide barrier
- * (bounded waits) separates the batches while the weights of later batches
- * keep streaming into shared memory.
+ * matrix products, "05. llama.cpp…", §性能直觉：带宽决定 Decode: every weight is
+ * read once per token). Batch g has n_mats[g] matrices that read the input
+ * x[g] and the same K[g]; its matrices are entries mat0 .. mat0 + n_mats[g] - 1
+ * of the flattened arrays W_blocks, y and M, mat0 being the sum of the earlier
+ * n_mats. The result is that of one bq_gemv_multi call per batch, issued in
+ * order, bit for bit: x[g] may be (part of) an output of an earlier batch, and
+ * an output of batch g may overwrite the input of an earlier batch. Inside the
+ * launch the weights stream without a pause from batch to batch; a batch waits
+ * for other CTAs only where memory orders it after an earlier batch (its x
+ * overlaps that batch's outputs, or its outputs overlap that batch's x), and
+ * then until every CTA has finished that batch (bounded waits). Batches that
+ * share no memory run without any wait.
  * All arrays are HOST arrays; their entries are device pointers. W_blocks
  * (16-byte aligned): M rows of K/32 blocks of `type`; x[g] (16-byte aligned):
- * K[g] fp32; y (4-byte aligned): M fp32.
+ * K[g] fp32; y (4-byte aligned): M fp32. Runs of more than 256 batches or 512
+ * matrices take several launches, ordered by the stream.
  * Errors: BQ_ERR_SHAPE (K[g] not a positive multiple of 256 or above
  * BQ_GEMV_SEQ_MAX_K, a batch of 2^31 rows or more), BQ_ERR_ALIGN,
  * BQ_ERR_INVALID_ARG (null pointers, negative sizes, an output overlapping
  * another output, any weight matrix or its own batch's x), BQ_ERR_WORKSPACE
  * (no workspace of bq_gemv_sequence_workspace_size() bytes set: the launch
- * keeps its barrier counter there, so calls sharing a workspace must not run
- * concurrently). The pages have no persistent launch; llama.cpp launches one
- * kernel per matrix product. */
+ * keeps its per-batch counters there, so calls sharing a workspace must not
+ * run concurrently). The pages have no persistent launch; llama.cpp launches
+ * one kernel per matrix product. */
 int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *const *W_blocks, float *const *y,
                      const int64_t *M, const float *const *x, const int64_t *K);
 size_t bq_gemv_sequence_workspace_size(void);
@@ -277,7 +281,10 @@ int bq_block_dots(int type, const void *W_blocks, const void *xq_blocks, int32_t
  * Q8_0 activations; N * (K/32) * 34 bytes beyond the array are rejected with
  * BQ_ERR_WORKSPACE. The call makes no cudaMalloc, cudaFree or other allocating
  * call. Its first call on a device looks up the array's device address with
- * that device current; make that first call before any stream capture. All
+ * that device current and keeps it for the life of the process; make that
+ * first call before any stream capture, and make no call on a device after
+ * cudaDeviceReset on it (the reset unloads the array the kept address
+ * points to). All
  * calls share the one array (every call overwrites the part it uses before
  * reading it), so calls that overlap on the GPU race: issue them on one
  * stream, or order them. */

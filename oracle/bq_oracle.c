@@ -706,6 +706,11 @@ int oracle_gemv(int w_type, const uint8_t *w_blocks, const float *x, float *y,
     if (!xq)
         return -3;
     oracle_quantize_rows(ORACLE_TYPE_Q8_0, x, xq, 1, K); /* R5 */
+    /* rows are independent: a build with OpenMP may run them on several
+       threads (same per-row arithmetic, same results) */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t m = 0; m < M; m++)
         dot_row(w_type, w_blocks + m * row_bytes, xq, nb, y + m, mag ? mag + m : NULL);
     free(xq);

@@ -210,7 +210,7 @@ def test_gemv_sequence_validation(L):
     Y0, Y1 = base + (2 << 24), base + (3 << 24)
     X0, X1 = base + (4 << 24), base + (5 << 24)
     ok = dict(n_mats=[1, 1], W=[W0, W1], Y=[Y0, Y1], M=[64, 64], X=[X0, X1], K=[512, 512])
-    assert L.bq_gemv_sequence_workspace_size() == 256
+    assert L.bq_gemv_sequence_workspace_size() >= 4 * 257  # abort flag + one counter per batch of a launch
     assert L.bq_gemv_sequence(8, 0, None, None, None, None, None, None) == 0
     assert _seq(L, **ok) == -7                               # valid, but no workspace set
     assert _seq(L, **{**ok, "K": [512, 96]}) == -2           # K not a multiple of 256

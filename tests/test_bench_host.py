@@ -57,18 +57,31 @@ def test_single_process_needs_no_group():
     assert bench.aggregate_rate(10.0, 1, 2.0) == 5.0
 
 
-def test_clock_summary_parses_samples():
+def test_clock_summary_keeps_the_timed_window():
+    """Samples (time, SM MHz, max MHz, power W, active reasons) outside
+    [t0, t1] are dropped; the median clock, the maximum and the union of the
+    reasons inside are reported."""
     c = bench.ClockSampler.__new__(bench.ClockSampler)
-    c.rows = [(10.0, "2026/12/02 05:00:00.000, 1900, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active"),
-              (10.5, "2026/12/02 05:00:00.500, 1800, 2070, 1200.5, 0x4, Not Active, Not Active, Not Active, Active"),
-              (11.0, "2026/12/02 05:00:01.000, 1700, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active"),
-              (20.0, "2026/12/02 05:00:10.000, 300, 2070, 100.0, 0x0, Active, Not Active, Not Active, Not Active")]
+    c.source = "nvml"
+    c.rows = [(10.0, 1900.0, 2070.0, 900.1, set()),
+              (10.5, 1800.0, 2070.0, 1200.5, {"sw_power_cap"}),
+              (11.0, 1700.0, 2070.0, 1300.0, {"sw_power_cap"}),
+              (20.0, 300.0, 2070.0, 100.0, {"hw_slowdown"})]
     c.t0, c.t1 = 9.9, 11.0
     s = c.summary()
     assert s["samples"] == 3
     assert s["sm_mhz"] == 1800
     assert s["sm_max_mhz"] == 2070
     assert s["reasons"] == ["sw_power_cap"]
+    assert s["power_w_max"] == 1300.0
+    c.t0, c.t1 = 30.0, 31.0
+    assert c.summary()["samples"] == 0
+
+
+def test_clock_reason_bits():
+    """NVML clock-event reason bits of the four reasons the timing rules name."""
+    assert bench.ClockSampler.REASON_BITS == {"sw_power_cap": 0x4, "hw_slowdown": 0x8,
+                                              "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
 
 
 def test_peaks_and_traffic(tmp_path, monkeypatch):
