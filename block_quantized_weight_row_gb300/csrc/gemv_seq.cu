@@ -56,6 +56,7 @@ using gemv::kXRecWords;
 using gemv::quantize_x_records_2lane;
 
 constexpr int kSqConsumers = 16;  // consumer warps per CTA
+constexpr int kSqGroupWarps = 8;  // consumer warps per group (two groups take the stages in turn)
 constexpr int kSqXWarps = 3;      // warps quantizing x (20 warps: 96 registers a thread)
 constexpr int kSqXThreads = kSqXWarps * 32;
 constexpr int kSqProducer = kSqConsumers + kSqXWarps;  // warp index of the producer
@@ -65,15 +66,22 @@ constexpr int kSeqMaxMats = 512;
 constexpr uint32_t kSeqDrainLimit = 1u << 26;
 constexpr int kRowRotation = 37;  // CTA range rotation per batch
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
+#ifndef SEQ_POLL_NS
+#define SEQ_POLL_NS 32  // sleep between polls of a mbarrier
+#endif
 
 struct SeqGroup {
   const float *x;
-  int K;          // a multiple of 256
-  int first_mat;  // matrices first_mat .. first_mat + n_mats - 1 of SeqArgs::m
+  int K;           // a multiple of 256
+  int first_mat;   // matrices first_mat .. first_mat + n_mats - 1 of SeqArgs::m
   int n_mats;
-  int rows;       // rows of all the batch's matrices
-  int wait_on;    // batch (of this launch) every CTA must have finished first, or -1
-  int signal;     // nonzero: a later batch waits for this one
+  int rows;        // rows of all the batch's matrices
+  int wait_on;     // batch (of this launch) every CTA must have finished first, or -1
+  int signal;      // nonzero: a later batch waits for this one
+  int groups8;     // K / 256 groups of 8 blocks per row
+  int lanes;       // lanes per row: the power of two <= 32 the per-launch kernel takes
+  int row_bytes;
+  int stage_rows;  // rows per stage: one pass of a consumer group's warps, as the ring slot allows
 };
 
 struct SeqMat {
@@ -95,23 +103,6 @@ struct SeqArgs {
   uint32_t spin_limit;
 };
 
-// Per-batch shape, derived from K the same way on every side.
-template <int TYPE>
-struct BatchShape {
-  int groups8;    // K / 256 groups of 8 blocks per row
-  int L;          // lanes per row: a power of two <= 32
-  int rpw;        // rows per warp pass = 32 / L
-  int row_bytes;
-  int stage_rows;
-  __device__ __forceinline__ BatchShape(int K, int slot_bytes) {
-    groups8 = K >> 8;
-    L = groups8 <= 1 ? 1 : min(32, 1 << (32 - __clz(groups8 - 1)));
-    rpw = 32 / L;
-    row_bytes = (K / kQK) * Fmt<TYPE>::kBytes;
-    stage_rows = max(1, slot_bytes / row_bytes);
-  }
-};
-
 // Rows [r0, r1) of batch g taken by this CTA.
 __device__ __forceinline__ void cta_rows(int rows, int g, int &r0, int &r1) {
   const int G = int(gridDim.x);
@@ -120,16 +111,28 @@ __device__ __forceinline__ void cta_rows(int rows, int g, int &r0, int &r1) {
   r1 = int(int64_t(rows) * (p + 1) / G);
 }
 
-// Matrix of the batch holding batch row `row`, and the rows of the stage that
-// starts there (at most stage_rows, never past r1 or the matrix's end).
-__device__ __forceinline__ void stage_at(const SeqArgs &a, const SeqGroup &G, int row, int r1, int stage_rows,
-                                         int &mat, int &nrows) {
-  mat = G.first_mat;
-  const int last = G.first_mat + G.n_mats - 1;
-  while (mat < last && row >= a.m[mat + 1].row_start) ++mat;
-  const int mat_end = mat < last ? a.m[mat + 1].row_start : G.rows;
-  nrows = min(min(stage_rows, r1 - row), mat_end - row);
-}
+// Stages of one batch's row range in order: each at most stage_rows rows,
+// never past the range or a matrix's end. Producer and consumers walk the
+// same sequence (incrementally: no division per stage).
+struct StageWalk {
+  int row, r1, mat, mat_end, last;
+  __device__ __forceinline__ void begin(const SeqArgs &a, const SeqGroup &G, int r0, int r1_) {
+    row = r0;
+    r1 = r1_;
+    mat = G.first_mat;
+    last = G.first_mat + G.n_mats - 1;
+    while (mat < last && row >= a.m[mat + 1].row_start) ++mat;
+    mat_end = mat < last ? a.m[mat + 1].row_start : G.rows;
+  }
+  // rows of the stage that starts at `row` (row < r1)
+  __device__ __forceinline__ int next(const SeqArgs &a, const SeqGroup &G) {
+    if (row >= mat_end) {
+      ++mat;
+      mat_end = mat < last ? a.m[mat + 1].row_start : G.rows;
+    }
+    return min(min(G.stage_rows, r1 - row), mat_end - row);
+  }
+};
 
 __device__ __forceinline__ bool grid_aborted(const SeqArgs &a) {
   return *reinterpret_cast<volatile unsigned *>(a.sync) != 0u;
@@ -141,14 +144,19 @@ __device__ __forceinline__ void seq_abort(const SeqArgs &a, volatile int *cta_ab
   atomicOr(a.err, kErrTimeout);
 }
 
-// Bounded mbarrier wait that also gives up once the CTA or the grid aborted.
-// Each poll may sleep up to kSleepNs (the warp wakes when the phase
-// completes), so waiting warps take almost no issue slots from working ones.
-constexpr uint32_t kSleepNs = 1000;
+// Bounded wait on one of this CTA's mbarriers that also gives up once
+// another role of the CTA gave up. Polls never suspend in the barrier unit
+// (whose wake-up comes long after the phase completes: with a handoff per
+// stage that latency, not the work, set the pace); between polls the warp
+// sleeps briefly so that waiting warps leave the issue slots to working ones.
+// Only the CTA's own flag (shared memory) is read here: these barriers depend
+// on this CTA's roles alone, which all end; the grid-wide flag is read where a
+// CTA waits for other CTAs.
 __device__ __forceinline__ bool seq_wait(const SeqArgs &a, uint64_t *bar, uint32_t parity, volatile int *cta_abort) {
   for (uint32_t i = 0; i < a.spin_limit; ++i) {
-    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
-    if ((i & 3) == 3 && (*cta_abort || grid_aborted(a))) return false;
+    if (mbar_test_wait(bar, parity)) return true;
+    if (SEQ_POLL_NS > 0) __nanosleep(SEQ_POLL_NS);
+    if ((i & 63) == 63 && *cta_abort) return false;
   }
   seq_abort(a, cta_abort);
   return false;
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kSqConsumers);  // every consumer warp releases every stage
+      mbar_init(&empty[s], kSqGroupWarps);  // every warp of the stage's consumer group releases it
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&rfull[b], kSqXThreads);  // every x thread, after its record stores
@@ -204,25 +212,33 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
       int issued = 0;
       const uint64_t policy = l2_evict_first_policy();  // every weight is read once
       bool stop = false;
-      for (int g = 0, j = 0; g < a.n_groups && !stop; ++g) {
+      int j = 0, s = 0;  // stage index, its ring slot
+      uint32_t ph = 0;   // (j / S) & 1
+      for (int g = 0; g < a.n_groups && !stop; ++g) {
         const SeqGroup &G = a.g[g];
-        const BatchShape<TYPE> sh(G.K, a.slot_bytes);
-        int row, r1;
-        cta_rows(G.rows, g, row, r1);
-        while (row < r1) {
-          const int s = j % S;
-          if (j >= S && !seq_wait(a, &empty[s], uint32_t((j / S - 1) & 1), cta_abort)) {
+        int r0, r1;
+        cta_rows(G.rows, g, r0, r1);
+        if (r0 >= r1) continue;
+        StageWalk wk;
+        wk.begin(a, G, r0, r1);
+        while (wk.row < r1) {
+          // the slot's previous use (stage j - S) must have been released
+          if (j >= S && !seq_wait(a, &empty[s], ph ^ 1u, cta_abort)) {
             stop = true;
             break;
           }
-          int mat, nrows;
-          stage_at(a, G, row, r1, sh.stage_rows, mat, nrows);
-          const uint32_t bytes = uint32_t(nrows) * uint32_t(sh.row_bytes);
+          const int nrows = wk.next(a, G);
+          const uint32_t bytes = uint32_t(nrows) * uint32_t(G.row_bytes);
           mbar_arrive_expect_tx(&full[s], bytes);
           bulk_g2s_hint(ring + size_t(s) * a.slot_bytes,
-                        a.m[mat].W + int64_t(row - a.m[mat].row_start) * sh.row_bytes, bytes, &full[s], policy);
-          row += nrows;
+                        a.m[wk.mat].W + int64_t(wk.row - a.m[wk.mat].row_start) * G.row_bytes, bytes, &full[s],
+                        policy);
+          wk.row += nrows;
           issued = ++j;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
       // never leave with a copy in flight: wait for the last use of each slot
@@ -252,16 +268,21 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
     }
   } else {
     // --------------------------------------------------------- consumers --
+    // Two groups of kSqGroupWarps warps take the stages in turn (stage j:
+    // group j & 1); within a stage every warp of the group takes its rows,
+    // as in the per-launch kernel, so that a stage is consumed by its whole
+    // group at once and released once.
+    const int cg = warp / kSqGroupWarps;  // consumer group
+    const int cw = warp % kSqGroupWarps;  // warp within the group
     bool skip = false;  // a wait ran out: walk on without waiting or computing
-    int j = 0;          // stage index, the producer's numbering
-    int slot_base = 0;  // row slots of all earlier stages (round robin over the warps)
+    int j = 0, s = 0;   // stage index (the producer's numbering), its ring slot
+    uint32_t ph = 0;    // (j / S) & 1
     uint32_t nq = 0;    // bit b: parity of the x warps' uses of buffer b so far (phases of rfull)
     for (int g = 0, k = 0; g < a.n_groups; ++g) {
       const SeqGroup &G = a.g[g];
-      const BatchShape<TYPE> sh(G.K, a.slot_bytes);
-      int row, r1;
-      cta_rows(G.rows, g, row, r1);
-      if (row < r1) {
+      int r0, r1;
+      cta_rows(G.rows, g, r0, r1);
+      if (r0 < r1) {
         const int b = k & 1;
         if (G.wait_on >= 0) {
           // batch wait_on's outputs are (or overlap) this batch's x, or this
@@ -281,48 +302,52 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
           nq ^= 1u << b;
         }
         const uint32_t *xr = reinterpret_cast<const uint32_t *>(smem + b * a.xrec_bytes);
-        const int rr = lane / sh.L;  // row of the slot handled by this lane
-        const int gl = lane % sh.L;  // first group of that row handled by this lane
-        while (row < r1) {
-          const int s = j % S;
-          // every warp consumes every stage in order, so a parity wait is
-          // never more than one phase ahead of the barrier
-          if (!skip) skip = !seq_wait(a, &full[s], uint32_t((j / S) & 1), cta_abort);
-          int mat, nrows;
-          stage_at(a, G, row, r1, sh.stage_rows, mat, nrows);
-          const int nslots = (nrows + sh.rpw - 1) / sh.rpw;
-          if (!skip) {
-            float *yp = a.m[mat].y + (row - a.m[mat].row_start);
-            const uint8_t *stage = ring + size_t(s) * a.slot_bytes;
-            for (int t = (warp - slot_base % kSqConsumers + kSqConsumers) % kSqConsumers; t < nslots;
-                 t += kSqConsumers) {
-              const int r = t * sh.rpw + rr;
-              float acc = 0.0f;
-              if (r < nrows) {
-                const uint8_t *rowp = stage + size_t(r) * sh.row_bytes;
-                for (int q = gl; q < sh.groups8; q += sh.L) {
-                  uint32_t w[GW];
-                  const uint4 *src = reinterpret_cast<const uint4 *>(rowp + size_t(q) * GW * 4);
+        const int L = G.lanes, rpw = 32 / L;
+        const int rr = lane / L;  // row (within the warp's pass) handled by this lane
+        const int gl = lane % L;  // first group of that row handled by this lane
+        StageWalk wk;
+        wk.begin(a, G, r0, r1);
+        while (wk.row < r1) {
+          const int nrows = wk.next(a, G);
+          if ((j & 1) == cg) {
+            // every warp of the group consumes every stage of the group in
+            // order, so a parity wait is never more than one phase ahead
+            if (!skip) skip = !seq_wait(a, &full[s], ph, cta_abort);
+            if (!skip) {
+              float *yp = a.m[wk.mat].y + (wk.row - a.m[wk.mat].row_start);
+              const uint8_t *stage = ring + size_t(s) * a.slot_bytes;
+              for (int pr = cw * rpw; pr < nrows; pr += kSqGroupWarps * rpw) {
+                const int r = pr + rr;
+                float acc = 0.0f;
+                if (r < nrows) {
+                  const uint8_t *rowp = stage + size_t(r) * G.row_bytes;
+                  for (int q = gl; q < G.groups8; q += L) {
+                    uint32_t w[GW];
+                    const uint4 *src = reinterpret_cast<const uint4 *>(rowp + size_t(q) * GW * 4);
 #pragma unroll
-                  for (int c = 0; c < GW / 4; ++c) {
-                    const uint4 u = src[c];
-                    w[4 * c] = u.x;
-                    w[4 * c + 1] = u.y;
-                    w[4 * c + 2] = u.z;
-                    w[4 * c + 3] = u.w;
+                    for (int c = 0; c < GW / 4; ++c) {
+                      const uint4 u = src[c];
+                      w[4 * c] = u.x;
+                      w[4 * c + 1] = u.y;
+                      w[4 * c + 2] = u.z;
+                      w[4 * c + 3] = u.w;
+                    }
+                    acc = group_terms<TYPE>(w, xr + q * kXRecWords, acc);
                   }
-                  acc = group_terms<TYPE>(w, xr + q * kXRecWords, acc);
                 }
+                for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+                if (gl == 0 && r < nrows) yp[r] = acc;
               }
-              for (int off = sh.L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-              if (gl == 0 && r < nrows) yp[r] = acc;
             }
+            __syncwarp();
+            if (!skip && lane == 0) mbar_arrive(&empty[s]);
           }
-          slot_base += nslots;
-          row += nrows;
-          __syncwarp();
-          if (!skip && lane == 0) mbar_arrive(&empty[s]);
+          wk.row += nrows;
           ++j;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         __syncwarp();
         if (!skip && lane == 0) mbar_arrive(&rempty[b]);
@@ -357,42 +382,32 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   constexpr int BB = Fmt<TYPE>::kBytes;
   std::unique_ptr<SeqArgs> a(new SeqArgs{});
   const int n = int(groups.size());
-  int xrec_bytes = 0, max_row = 0;
-  // bytes per distinct row length, to choose the stage size
-  std::vector<std::pair<int, int64_t>> by_row;
+  // Per batch: the per-launch kernel's lanes per row (so that every row's
+  // arithmetic is the same), and the bytes of one pass of a consumer group
+  // (kSqGroupWarps warps, 32 / lanes rows each).
+  std::vector<int> lanes(n), row_bytes(n), pass_rows(n);
+  int xrec_bytes = 0, max_row = 0, max_pass = 0;
   for (int i = 0; i < n; ++i) {
     const int gi = groups[i];
-    const int row_bytes = int(K[gi] / kQK) * BB;
-    xrec_bytes = std::max(xrec_bytes, int(K[gi] / 256) * kXRecBytes);
-    max_row = std::max(max_row, row_bytes);
-    int64_t rows = 0;
-    for (int k = 0; k < n_mats[gi]; ++k) rows += M[mat0[gi] + k];
-    auto it = std::find_if(by_row.begin(), by_row.end(), [&](const std::pair<int, int64_t> &p) {
-      return p.first == row_bytes;
-    });
-    if (it == by_row.end())
-      by_row.push_back({row_bytes, rows * row_bytes});
-    else
-      it->second += rows * row_bytes;
+    const int groups8 = int(K[gi] / 256);
+    int L = 1;
+    while (L < groups8 && L < 32) L <<= 1;
+    lanes[i] = L;
+    row_bytes[i] = int(K[gi] / kQK) * BB;
+    pass_rows[i] = kSqGroupWarps * (32 / L);
+    xrec_bytes = std::max(xrec_bytes, groups8 * kXRecBytes);
+    max_row = std::max(max_row, row_bytes[i]);
+    max_pass = std::max(max_pass, pass_rows[i] * row_bytes[i]);
   }
   xrec_bytes = (xrec_bytes + 127) / 128 * 128;
   // Shared memory: two record buffers, the ring, 2 (S + 2) barriers and the
-  // abort flag. Stages of 16-40 KB (large copies: the copy cost is per copy),
-  // the size that wastes the fewest bytes on this launch's row lengths.
+  // abort flag. A ring slot holds one pass of a consumer group (a single large
+  // copy: the copy cost is per copy), capped so that the ring keeps at least
+  // four stages; a batch whose pass does not fit takes the rows that do.
   const int reserve = 1024;  // per-CTA system reservation
   const int budget = std::min(di->smem_per_sm - reserve, di->max_smem_optin) - 2 * xrec_bytes - 1024;
   static const int forced_slot = tuning_value("BQ_GEMV_SEQ_SLOT_BYTES");  // read once per process
-  int slot = 0;
-  double best = -1.0;
-  for (int c = std::max(16 << 10, (max_row + 15) / 16 * 16); c <= (40 << 10); c += 16) {
-    if (budget / c < 4) break;
-    double used = 0.0;
-    for (const auto &p : by_row) used += double(p.second) * double((c / p.first) * p.first) / double(c);
-    if (used > best * (1.0 + 1e-9)) {
-      best = used;
-      slot = c;
-    }
-  }
+  int slot = std::min(max_pass, budget / 4) / 16 * 16;
   if (forced_slot > 0) slot = (forced_slot + 15) / 16 * 16;
   if (slot < max_row) slot = (max_row + 15) / 16 * 16;
   const int stages = std::min(32, budget / slot);
@@ -412,6 +427,11 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
     G.K = int(K[gi]);
     G.first_mat = nm;
     G.wait_on = -1;
+    G.groups8 = G.K / 256;
+    G.lanes = lanes[i];
+    G.row_bytes = row_bytes[i];
+    const int pass_bytes = pass_rows[i] * row_bytes[i];
+    G.stage_rows = pass_bytes <= slot ? pass_rows[i] * (slot / pass_bytes) : slot / row_bytes[i];
     int rows = 0;
     for (int k = 0; k < n_mats[gi]; ++k) {
       const int mi = mat0[gi] + k;

@@ -56,7 +56,63 @@ __global__ void __launch_bounds__(256) k_mma_f16(int iters, int *out) {
   out[blockIdx.x * blockDim.x + threadIdx.x] = __float_as_int(s);
 }
 
+// Integer dot-product issue rate: every thread runs kChains independent
+// dp4a.u32.s32 chains (kind 2) or, for comparison, 32-bit integer
+// multiply-add chains (kind 3).
+__global__ void __launch_bounds__(256) k_dp4a(int iters, int kind, int *out) {
+  const uint32_t t = threadIdx.x * 0x01010101u + 0x03050709u;
+  int c[kChains];
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) c[k] = int(t) + k;
+  if (kind == 2) {
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+      for (int k = 0; k < kChains; ++k)
+        asm volatile("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(c[k]) : "r"(t + uint32_t(k)), "r"(t ^ 0x5a5a5a5au));
+    }
+  } else {
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+      for (int k = 0; k < kChains; ++k)
+        asm volatile("mad.lo.s32 %0, %1, %2, %0;" : "+r"(c[k]) : "r"(int(t) + k), "r"(int(t ^ 0x5a5a5a5au)));
+    }
+  }
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) s ^= c[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 }  // namespace
+
+// Thread-instruction rate (tera-instructions per second) of kind 2 = dp4a,
+// kind 3 = 32-bit integer multiply-add, each as independent chains.
+extern "C" int bq_probe_int_rate(int kind, int iters, int ctas_per_sm, double *tinst) {
+  if ((kind != 2 && kind != 3) || iters < 1 || ctas_per_sm < 1 || !tinst) return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -5;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -5;
+  const int grid = sms * ctas_per_sm, block = 256;
+  int *out = nullptr;
+  if (cudaMalloc(&out, size_t(grid) * block * sizeof(int)) != cudaSuccess) return -5;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  k_dp4a<<<grid, block>>>(iters / 8 + 1, kind, out);
+  cudaEventRecord(e0);
+  k_dp4a<<<grid, block>>>(iters, kind, out);
+  cudaEventRecord(e1);
+  cudaError_t err = cudaEventSynchronize(e1);
+  float ms = 0.0f;
+  if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, e0, e1);
+  if (err == cudaSuccess) err = cudaGetLastError();
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaFree(out);
+  if (err != cudaSuccess || ms <= 0.0f) return -5;
+  *tinst = double(grid) * block * double(iters) * kChains / (double(ms) * 1e-3) / 1e12;
+  return 0;
+}
 
 // Tensor-op rate of mma.sync on the current device in tera-ops per second
 // (2 * m * n * k per instruction): kind 0 = m16n8k32 s8 x s8 -> s32, kind 1
