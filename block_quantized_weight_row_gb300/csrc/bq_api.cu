@@ -317,7 +317,7 @@ int bq_gemv(int type, const void *W, const float *x, float *y, int64_t M, int64_
   return bq_gemv_multi(type, 1, &W, &y, &M, x, K);
 }
 
-size_t bq_gemv_sequence_workspace_size(void) { return (gemv_seq_sync_bytes() + 255) / 256 * 256; }
+size_t bq_gemv_sequence_workspace_size(void) { return (gemv_seq_workspace_bytes() + 255) / 256 * 256; }
 
 int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *const *W, float *const *y,
                      const int64_t *M, const float *const *x, const int64_t *K) {
@@ -394,8 +394,18 @@ int bq_gemv_sequence(int type, int n_groups, const int *n_mats, const void *cons
   const size_t need = bq_gemv_sequence_workspace_size();
   if (!t_ws || t_ws_bytes < need)
     return fail(BQ_ERR_WORKSPACE, "bq_gemv_sequence: needs %zu workspace bytes, %zu set", need, t_ws_bytes);
-  if (hits(reinterpret_cast<uintptr_t>(t_ws), reinterpret_cast<uintptr_t>(t_ws) + need, -1))
-    return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: the workspace overlaps an output");
+  const uintptr_t ws0 = reinterpret_cast<uintptr_t>(t_ws), ws1 = ws0 + need;
+  if (hits(ws0, ws1, -1)) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: the workspace overlaps an output");
+  mi = 0;
+  for (int g = 0; g < n_groups; ++g) {  // the launch writes the workspace while it reads x and W
+    const uintptr_t xl = reinterpret_cast<uintptr_t>(x[g]);
+    bool bad = x[g] && xl < ws1 && ws0 < xl + uintptr_t(K[g]) * 4;
+    for (int k = 0; k < n_mats[g]; ++k, ++mi) {
+      const uintptr_t wl = reinterpret_cast<uintptr_t>(W[mi]);
+      bad = bad || (M[mi] > 0 && wl < ws1 && ws0 < wl + uintptr_t(M[mi]) * uintptr_t(K[g] / kQK) * uintptr_t(bb));
+    }
+    if (bad) return fail(BQ_ERR_INVALID_ARG, "bq_gemv_sequence: the workspace overlaps an input of batch %d", g);
+  }
   cudaError_t e = launch_gemv_seq(type, n_groups, n_mats, reinterpret_cast<const uint8_t *const *>(W), y, M, x, K,
                                   static_cast<unsigned *>(t_ws), t_stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_gemv_sequence launch");

@@ -65,8 +65,9 @@ size_t gemv_workspace_bytes(int64_t K);
 // A sequence of GEMV batches in one launch per at most 256 batches: batch g
 // (n_mats[g] matrices from the flattened W / y / M arrays, input x[g], K[g] a
 // multiple of 256) behaves as a launch_gemv issued after those of batches
-// 0..g-1. sync: gemv_seq_sync_bytes() of scratch (zeroed before each launch).
-size_t gemv_seq_sync_bytes();
+// 0..g-1. ws: gemv_seq_workspace_bytes() of scratch (counters, zeroed before
+// each launch, then x's quantized records).
+size_t gemv_seq_workspace_bytes();
 cudaError_t launch_gemv_seq(int type, int n_groups, const int *n_mats, const uint8_t *const *W, float *const *y,
                             const int64_t *M, const float *const *x, const int64_t *K, unsigned *sync,
                             cudaStream_t stream);

@@ -62,14 +62,61 @@ __device__ __forceinline__ void quantize_x_records(const float *__restrict__ x, 
   }
 }
 
+// One block of x quantized by a lane pair: the lane with h = 0 holds values
+// 0-15, the lane with h = 1 values 16-31 (f). Both lanes of every pair of the
+// warp must call it (it exchanges with the pair's other lane); `store` says
+// whether this pair writes its block: codes to words 8 jb .. 8 jb + 7 of the
+// group record rg, the scale (fp32) to word 64 + jb, the code sum to 72 + jb.
+// Each lane decides the exact path for its own 16 values (the rule is exact
+// per value), so the record is bit-identical to quantize_x_records'.
+__device__ __forceinline__ void quantize_block_pair(const float (&f)[16], int h, uint32_t *rg, int jb, bool store) {
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+  uint16_t scale;
+  float ds;
+  block_scale<kTypeQ8_0>(m, scale, ds);
+  const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
+  constexpr float kMagic = 12582912.0f;
+  uint32_t t[16];
+  float dmax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float r = __fmul_rn(f[j], inv);
+    const float tt = __fadd_rn(r, kMagic);
+    t[j] = __float_as_uint(tt);
+    dmax = fmaxf(dmax, fabsf(__fsub_rn(r, __fsub_rn(tt, kMagic))));
+  }
+  if (dmax > 0.4999f || (ds > 0.0f && ds < 6.103515625e-05f)) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = 0x4B400000u + uint32_t(code_of<kTypeQ8_0>(f[j], ds, inv));
+  }
+  uint32_t w[4];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w[i] = pack_bytes(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sum += int(t[4 * i + k] - 0x4B400000u);
+  }
+  sum += __shfl_xor_sync(kFull, sum, 1);
+  if (store) {
+    *reinterpret_cast<uint4 *>(rg + 8 * jb + 4 * h) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (h == 0) {
+      rg[64 + jb] = __float_as_uint(half_bits_to_float(scale));
+      rg[72 + jb] = uint32_t(sum);
+    }
+  }
+}
+
 // The same records, two lanes per block (the lanes of a pair hold values
 // 0-15 and 16-31 of one block), nthreads / 2 blocks per pass and the loads of
 // two passes issued before any arithmetic: one pass for K = 4096 and three
 // for K = 11008 with 256 threads, against 4 and 11 dependent 8-lane passes.
 // x is quantized after the previous kernel completes, on the critical path of
 // every launch without a workspace (measured 1.28 -> 1.19 ms per 7B decode
-// step). Each lane decides the exact path for its own 16 values (the rule is
-// exact per value), so the records are bit-identical to quantize_x_records.
+// step). Bit-identical to quantize_x_records.
 __device__ __forceinline__ void quantize_x_records_2lane(const float *__restrict__ x, int nb, uint32_t *rec, int tid,
                                                          int nthreads) {
   const int h = tid & 1;
@@ -97,46 +144,7 @@ __device__ __forceinline__ void quantize_x_records_2lane(const float *__restrict
         f[4 * c + 2] = v[p][c].z;
         f[4 * c + 3] = v[p][c].w;
       }
-      float m = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(f[j]));
-      m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
-      uint16_t scale;
-      float ds;
-      block_scale<kTypeQ8_0>(m, scale, ds);
-      const float inv = ds > 0.0f ? rcp_approx(ds) : 0.0f;
-      constexpr float kMagic = 12582912.0f;
-      uint32_t t[16];
-      float dmax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float r = __fmul_rn(f[j], inv);
-        const float tt = __fadd_rn(r, kMagic);
-        t[j] = __float_as_uint(tt);
-        dmax = fmaxf(dmax, fabsf(__fsub_rn(r, __fsub_rn(tt, kMagic))));
-      }
-      if (dmax > 0.4999f || (ds > 0.0f && ds < 6.103515625e-05f)) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] = 0x4B400000u + uint32_t(code_of<kTypeQ8_0>(f[j], ds, inv));
-      }
-      uint32_t w[4];
-      int sum = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        w[i] = pack_bytes(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) sum += int(t[4 * i + k] - 0x4B400000u);
-      }
-      sum += __shfl_xor_sync(kFull, sum, 1);
-      if (b < nb) {
-        uint32_t *r = rec + (b >> 3) * kXRecWords;
-        const int jb = b & 7;
-        *reinterpret_cast<uint4 *>(r + 8 * jb + 4 * h) = make_uint4(w[0], w[1], w[2], w[3]);
-        if (h == 0) {
-          r[64 + jb] = __float_as_uint(half_bits_to_float(scale));
-          r[72 + jb] = uint32_t(sum);
-        }
-      }
+      quantize_block_pair(f, h, rec + (b >> 3) * kXRecWords, b & 7, b < nb);
     }
   }
 }

@@ -6,38 +6,39 @@
 // token, so tokens/s is about bandwidth / weight bytes). Launched one batch at
 // a time, the weight stream stops at every launch boundary (the next kernel
 // starts, waits for the previous one, quantizes its input, refills its
-// pipeline). Here one launch covers the whole run and the stream never stops:
+// pipeline). Here one launch covers the whole run and the stream never stops.
 //
-//   - one CTA per SM, three roles:
-//       producer warp   streams this CTA's rows of every batch, in batch
-//                       order, with 1-D bulk copies into a ring of shared-
-//                       memory stages (mbarrier-completed); it depends on
-//                       nothing but free stages, since the run never writes
-//                       a weight;
-//       x warps         quantize the input of the CTA's next batch into the
-//                       second of two record buffers (Q8_0 codes, scales,
-//                       code sums, the layout of the per-launch GEMV) while
-//                       the consumers use the first;
-//       consumer warps  dot every row of a stage with the records, reduce the
-//                       row's lanes and write y;
-//   - batch g has the result of one bq_gemv_multi call issued after the calls
-//     of batches 0..g-1. Only memory explains an order between them: when x[g]
-//     overlaps an output of an earlier batch, or an output of batch g overlaps
-//     the input of an earlier batch, batch g waits until every CTA has
-//     finished the latest such batch (a per-batch counter in global memory,
-//     incremented once per CTA with release semantics, polled with acquire
-//     loads, all waits bounded). The host derives these waits from the
-//     pointers; batches that share no memory never wait;
-//   - every CTA takes a contiguous, balanced range of each batch's rows, the
-//     ranges rotating over the CTAs from batch to batch so that the CTAs'
-//     total bytes stay level;
-//   - consumer warps take the row slots of the stage sequence round robin, so
-//     every warp gets an equal share whatever the stage sizes;
-//   - per row the arithmetic (records, group order, lanes per row, shuffle
-//     tree) is that of the per-launch kernel, so the outputs are bit-identical
-//     to bq_gemv_multi.
-// The launch is cooperative (every CTA resident), so a wait on other CTAs
-// cannot wait for a CTA that has not started.
+// One CTA per SM:
+//   producer warp    streams this CTA's rows of every batch, in batch order,
+//                    with 1-D bulk copies into a ring of shared-memory stages
+//                    (mbarrier-completed). It depends on nothing but free
+//                    stages: the run never writes a weight.
+//   consumer warps   two groups of 8 take the stages in turn; a stage is one
+//                    pass of a group (each warp 32 / lanes rows, as in the
+//                    per-launch kernel), so a stage is consumed by its whole
+//                    group at once and released once. Every row is dotted
+//                    with x's Q8_0 records, its lanes reduced, y written.
+//   x warps          at the start, with the consumers, quantize x of every
+//                    batch that waits for nothing (see below) into records in
+//                    the workspace, each CTA a slice, and count the CTA done;
+//                    then one lane copies each batch's records into a ring of
+//                    record buffers (bulk copies), batches ahead of the
+//                    consumers.
+// Batch g has the result of one bq_gemv_multi call issued after the calls of
+// batches 0..g-1. Only memory orders them: when x[g] overlaps an output of an
+// earlier batch, or an output of batch g overlaps the input of an earlier
+// batch, batch g waits until every CTA has finished the latest such batch (a
+// per-batch counter in global memory, incremented once per CTA after a fence,
+// polled with acquire loads), and then the consumers quantize x[g]
+// themselves. The host derives these waits from the pointers; batches that
+// share no memory never wait. All waits are bounded.
+// Every CTA takes a contiguous, balanced range of each batch's rows, the
+// ranges rotating over the CTAs from batch to batch so that the CTAs' total
+// bytes stay level. Per row the arithmetic (records, group order, lanes per
+// row, shuffle tree) is that of the per-launch kernel, so the outputs are
+// bit-identical to bq_gemv_multi. The launch is cooperative (every CTA
+// resident), so a wait on other CTAs cannot wait for a CTA that has not
+// started.
 #include <algorithm>
 #include <memory>
 #include <vector>
@@ -57,8 +58,7 @@ using gemv::quantize_x_records_2lane;
 
 constexpr int kSqConsumers = 16;  // consumer warps per CTA
 constexpr int kSqGroupWarps = 8;  // consumer warps per group (two groups take the stages in turn)
-constexpr int kSqXWarps = 3;      // warps quantizing x (20 warps: 96 registers a thread)
-constexpr int kSqXThreads = kSqXWarps * 32;
+constexpr int kSqXWarps = 3;      // quantize x at the start; then one lane copies records (20 warps: 96 registers)
 constexpr int kSqProducer = kSqConsumers + kSqXWarps;  // warp index of the producer
 constexpr int kSqThreads = (kSqConsumers + kSqXWarps + 1) * 32;
 constexpr int kSeqMaxGroups = 256;  // per launch; longer runs take several launches
@@ -66,6 +66,12 @@ constexpr int kSeqMaxMats = 512;
 constexpr uint32_t kSeqDrainLimit = 1u << 26;
 constexpr int kRowRotation = 37;  // CTA range rotation per batch
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
+constexpr int kBarPre = 2;        // named barrier of the warps that quantize x before the stream
+constexpr int kPreThreads = (kSqConsumers + kSqXWarps) * 32;
+constexpr int kMaxRecBufs = 8;    // record buffers in shared memory
+constexpr int kSyncWords = 2 + kSeqMaxGroups;  // abort flag, CTAs done quantizing, CTAs done per batch
+constexpr size_t kSyncBytes = (kSyncWords * 4 + 255) / 256 * 256;
+constexpr size_t kRecBytesMax = size_t(kSeqMaxGroups) * (BQ_GEMV_SEQ_MAX_K / 256) * kXRecBytes;
 #ifndef SEQ_POLL_NS
 #define SEQ_POLL_NS 32  // sleep between polls of a mbarrier
 #endif
@@ -82,6 +88,8 @@ struct SeqGroup {
   int lanes;       // lanes per row: the power of two <= 32 the per-launch kernel takes
   int row_bytes;
   int stage_rows;  // rows per stage: one pass of a consumer group's warps, as the ring slot allows
+  int rec_off;     // words: x's records in SeqArgs::rec (batches that wait for nothing), else -1
+  int blk0;        // first block of x in the launch's quantization order (rec_off >= 0)
 };
 
 struct SeqMat {
@@ -98,7 +106,10 @@ struct SeqArgs {
   int stages;
   int slot_bytes;  // bytes of one ring stage
   int xrec_bytes;  // bytes of one record buffer (the largest K of the launch)
-  unsigned *sync;  // [0]: abort flag, [1 + g]: CTAs done with batch g; zeroed before the launch
+  int nrec;        // record buffers in shared memory: a power of two, 2..kMaxRecBufs
+  int pre_blocks;  // blocks of x quantized at the start (every batch with rec_off >= 0)
+  uint32_t *rec;   // x's records of those batches (global memory)
+  unsigned *sync;  // [0]: abort flag, [1]: CTAs done quantizing, [2 + g]: CTAs done with batch g; zeroed
   unsigned *err;
   uint32_t spin_limit;
 };
@@ -162,10 +173,10 @@ __device__ __forceinline__ bool seq_wait(const SeqArgs &a, uint64_t *bar, uint32
   return false;
 }
 
-// Until every CTA has counted itself done with batch `g` (acquire), bounded.
-__device__ __forceinline__ bool seq_batch_wait(const SeqArgs &a, int g, volatile int *cta_abort) {
+// Until the counter `cnt` (global memory, counts CTAs) reaches every CTA of
+// the grid (acquire), bounded; also gives up once the grid aborted.
+__device__ __forceinline__ bool seq_count_wait(const SeqArgs &a, const unsigned *cnt, volatile int *cta_abort) {
   const unsigned target = gridDim.x;
-  const unsigned *cnt = a.sync + 1 + g;
   for (uint32_t i = 0; i < a.spin_limit; ++i) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
@@ -177,17 +188,60 @@ __device__ __forceinline__ bool seq_batch_wait(const SeqArgs &a, int g, volatile
   return false;
 }
 
+// Until every CTA has counted itself done with batch `g`.
+__device__ __forceinline__ bool seq_batch_wait(const SeqArgs &a, int g, volatile int *cta_abort) {
+  return seq_count_wait(a, a.sync + 2 + g, cta_abort);
+}
+
+// Quantize this CTA's share of x's blocks of every batch that waits for
+// nothing (the launch's blocks in batch order, cut evenly over the CTAs) into
+// the global records: two threads per block (quantize_block_pair), so the
+// records are those of the per-launch kernels. tid < kPreThreads.
+__device__ __forceinline__ void seq_prequantize(const SeqArgs &a, int tid) {
+  const int G = int(gridDim.x);
+  const int lo = int(int64_t(a.pre_blocks) * blockIdx.x / G);
+  const int hi = int(int64_t(a.pre_blocks) * (blockIdx.x + 1) / G);
+  const int h = tid & 1;
+  int g = 0;  // batch of block i (i only grows)
+  for (int base = lo; base < hi; base += kPreThreads / 2) {  // uniform: every lane runs every round
+    const int i = base + (tid >> 1);
+    const bool valid = i < hi;
+    float f[16];
+    uint32_t *rg = a.rec;
+    int jb = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = 0.0f;
+    if (valid) {
+      while (a.g[g].rec_off < 0 || i >= a.g[g].blk0 + a.g[g].K / kQK) ++g;
+      const int bl = i - a.g[g].blk0;
+      const float4 *src = reinterpret_cast<const float4 *>(a.g[g].x + int64_t(bl) * kQK + 16 * h);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 v = __ldcg(src + c);
+        f[4 * c] = v.x;
+        f[4 * c + 1] = v.y;
+        f[4 * c + 2] = v.z;
+        f[4 * c + 3] = v.w;
+      }
+      rg = a.rec + a.g[g].rec_off + (bl >> 3) * kXRecWords;
+      jb = bl & 7;
+    }
+    gemv::quantize_block_pair(f, h, rg, jb, valid);
+  }
+}
+
 template <int TYPE>
 __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constant__ SeqArgs a) {
   constexpr int GW = GroupWords<TYPE>::kWords;
   extern __shared__ __align__(128) uint8_t smem[];
-  // record buffer b at smem + b * xrec_bytes
-  uint8_t *ring = smem + 2 * size_t(a.xrec_bytes);
+  // record buffer b at smem + b * xrec_bytes, b < nrec
+  uint8_t *ring = smem + size_t(a.nrec) * a.xrec_bytes;
   uint64_t *full = reinterpret_cast<uint64_t *>(ring + size_t(a.stages) * a.slot_bytes);
   uint64_t *empty = full + a.stages;
-  uint64_t *rfull = empty + a.stages;  // [2]: records of buffer b written
-  uint64_t *rempty = rfull + 2;        // [2]: records of buffer b no longer read
-  volatile int *cta_abort = reinterpret_cast<volatile int *>(rempty + 2);
+  uint64_t *rfull = empty + a.stages;  // [nrec]: records of buffer b in place
+  uint64_t *rempty = rfull + a.nrec;   // [nrec]: records of buffer b no longer read
+  volatile int *cta_abort = reinterpret_cast<volatile int *>(rempty + a.nrec);
+  const uint32_t rmask = uint32_t(a.nrec - 1);
   __shared__ int s_go;  // dependency wait result, broadcast to the consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
@@ -197,14 +251,26 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSqGroupWarps);  // every warp of the stage's consumer group releases it
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&rfull[b], kSqXThreads);  // every x thread, after its record stores
+    for (int b = 0; b < a.nrec; ++b) {
+      mbar_init(&rfull[b], 1);  // the record copier (bytes on the transaction count)
       mbar_init(&rempty[b], kSqConsumers);
     }
     *cta_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
+
+  if (warp != kSqProducer && a.pre_blocks > 0) {
+    // x of every batch that waits for nothing, quantized once for the whole
+    // grid while the producer already streams weights; then this CTA counts
+    // itself done (release: the records are visible to the whole GPU)
+    seq_prequantize(a, threadIdx.x);
+    named_bar_sync(kBarPre, kPreThreads);
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(a.sync + 1, 1u);
+    }
+  }
 
   if (warp == kSqProducer) {
     // ---------------------------------------------------------- producer --
@@ -248,23 +314,39 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
       }
     }
   } else if (warp >= kSqConsumers) {
-    // ------------------------------------------------------------ x warps --
-    // The records of every batch that waits for nothing, one batch ahead of
-    // the consumers. A batch that waits for an earlier one is quantized by
-    // the consumers themselves once the wait is over (they are idle then).
-    const int xt = threadIdx.x - kSqConsumers * 32;
-    for (int g = 0, k = 0; g < a.n_groups; ++g) {
-      const SeqGroup &G = a.g[g];
-      int r0, r1;
-      cta_rows(G.rows, g, r0, r1);
-      if (r0 >= r1) continue;  // no rows here: nothing read, nothing written
-      const int b = k++ & 1;
-      if (G.wait_on >= 0) continue;
-      // the buffer's previous batch is done once its consumers released it
-      if (k > 2 && !seq_wait(a, &rempty[b], uint32_t((((k - 1) >> 1) - 1) & 1), cta_abort)) break;
-      quantize_x_records_2lane(G.x, G.K / kQK, reinterpret_cast<uint32_t *>(smem + b * a.xrec_bytes), xt,
-                               kSqXThreads);
-      mbar_arrive(&rfull[b]);
+    // ------------------------------------------------------- record copier --
+    // One lane copies the records of every batch that waits for nothing from
+    // global memory into the record buffers, up to nrec - 1 batches ahead of
+    // the consumers (1-D bulk copies completing on rfull). A batch that waits
+    // for an earlier one is quantized by the consumers themselves once the
+    // wait is over (they are idle then).
+    if (warp == kSqConsumers && lane == 0) {
+      bool ok = a.pre_blocks == 0 || seq_count_wait(a, a.sync + 1, cta_abort);
+      // the records were written by other threads' ordinary stores; the
+      // copies read them through the asynchronous proxy
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      uint32_t used = 0, par = 0;  // buffers copied into; parity of each one's last copy
+      for (int g = 0, k = 0; g < a.n_groups && ok; ++g) {
+        const SeqGroup &G = a.g[g];
+        int r0, r1;
+        cta_rows(G.rows, g, r0, r1);
+        if (r0 >= r1) continue;  // no rows here: nothing read, nothing written
+        const int b = int(uint32_t(k) & rmask);
+        const int use = k / a.nrec;
+        ++k;
+        if (G.rec_off < 0) continue;
+        // the buffer's previous batch is done once its consumers released it
+        if (use > 0 && !seq_wait(a, &rempty[b], uint32_t((use - 1) & 1), cta_abort)) break;
+        const uint32_t bytes = uint32_t(G.K / 256) * kXRecBytes;
+        mbar_arrive_expect_tx(&rfull[b], bytes);
+        bulk_g2s(smem + size_t(b) * a.xrec_bytes, a.rec + G.rec_off, bytes, &rfull[b]);
+        used |= 1u << b;
+        par = (par & ~(1u << b)) | (uint32_t(use & 1) << b);
+      }
+      // never leave with a copy in flight
+      for (int b = 0; b < a.nrec; ++b)
+        if (((used >> b) & 1u) && !mbar_wait_bounded(&rfull[b], (par >> b) & 1u, kSeqDrainLimit))
+          atomicOr(a.err, kErrTimeout);
     }
   } else {
     // --------------------------------------------------------- consumers --
@@ -277,13 +359,13 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
     bool skip = false;  // a wait ran out: walk on without waiting or computing
     int j = 0, s = 0;   // stage index (the producer's numbering), its ring slot
     uint32_t ph = 0;    // (j / S) & 1
-    uint32_t nq = 0;    // bit b: parity of the x warps' uses of buffer b so far (phases of rfull)
+    uint32_t nq = 0;    // bit b: parity of the copies into buffer b so far (phases of rfull)
     for (int g = 0, k = 0; g < a.n_groups; ++g) {
       const SeqGroup &G = a.g[g];
       int r0, r1;
       cta_rows(G.rows, g, r0, r1);
       if (r0 < r1) {
-        const int b = k & 1;
+        const int b = int(uint32_t(k) & rmask);
         if (G.wait_on >= 0) {
           // batch wait_on's outputs are (or overlap) this batch's x, or this
           // batch's outputs overwrite its x: once every CTA has finished it,
@@ -360,7 +442,7 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
         named_bar_sync(kBarConsumers, kSqConsumers * 32);
         if (threadIdx.x == 0 && !skip) {
           __threadfence();
-          atomicAdd(a.sync + 1 + g, 1u);
+          atomicAdd(a.sync + 2 + g, 1u);
         }
       }
     }
@@ -400,12 +482,16 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
     max_pass = std::max(max_pass, pass_rows[i] * row_bytes[i]);
   }
   xrec_bytes = (xrec_bytes + 127) / 128 * 128;
-  // Shared memory: two record buffers, the ring, 2 (S + 2) barriers and the
-  // abort flag. A ring slot holds one pass of a consumer group (a single large
-  // copy: the copy cost is per copy), capped so that the ring keeps at least
-  // four stages; a batch whose pass does not fit takes the rows that do.
+  // Record buffers: as many (2 .. kMaxRecBufs, a power of two) as fit in
+  // 32 KB, so that short batches' records arrive several batches ahead.
+  int nrec = 2;
+  while (nrec < kMaxRecBufs && 2 * nrec * xrec_bytes <= (32 << 10)) nrec *= 2;
+  // Shared memory: the record buffers, the ring, 2 (S + nrec) barriers and
+  // the abort flag. A ring slot holds one pass of a consumer group (a single
+  // large copy: the copy cost is per copy), capped so that the ring keeps at
+  // least four stages; a batch whose pass does not fit takes the rows that do.
   const int reserve = 1024;  // per-CTA system reservation
-  const int budget = std::min(di->smem_per_sm - reserve, di->max_smem_optin) - 2 * xrec_bytes - 1024;
+  const int budget = std::min(di->smem_per_sm - reserve, di->max_smem_optin) - nrec * xrec_bytes - 1024;
   static const int forced_slot = tuning_value("BQ_GEMV_SEQ_SLOT_BYTES");  // read once per process
   int slot = std::min(max_pass, budget / 4) / 16 * 16;
   if (forced_slot > 0) slot = (forced_slot + 15) / 16 * 16;
@@ -416,7 +502,9 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   a->stages = stages;
   a->slot_bytes = slot;
   a->xrec_bytes = xrec_bytes;
+  a->nrec = nrec;
   a->sync = sync;
+  a->rec = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(sync) + kSyncBytes);
   a->err = di->err_word;
   a->spin_limit = spin_limit();
   int nm = 0;
@@ -471,11 +559,25 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
       }
     }
   }
-  const size_t smem = 2 * size_t(xrec_bytes) + size_t(stages) * slot + 8 * (2 * size_t(stages) + 4) + 16;
+  // x of every batch that waits for nothing is quantized once at the start
+  // of the launch, in batch order, into the records area of the workspace
+  int rec_words = 0, blocks = 0;
+  for (int i = 0; i < n; ++i) {
+    SeqGroup &G = a->g[i];
+    G.rec_off = -1;
+    G.blk0 = blocks;
+    if (G.wait_on >= 0) continue;
+    G.rec_off = rec_words;
+    rec_words += G.groups8 * kXRecWords;
+    blocks += G.K / kQK;
+  }
+  a->pre_blocks = blocks;
+  const size_t smem =
+      size_t(nrec) * xrec_bytes + size_t(stages) * slot + 8 * (2 * size_t(stages) + 2 * size_t(nrec)) + 16;
   const void *fn = reinterpret_cast<const void *>(k_gemv_seq<TYPE>);
   cudaError_t e = ensure_smem(fn, int(smem));
   if (e != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(sync, 0, sizeof(unsigned) * size_t(1 + n), stream)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(sync, 0, sizeof(unsigned) * size_t(2 + n), stream)) != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
@@ -524,7 +626,7 @@ cudaError_t launch_seq_typed(int n_groups, const int *n_mats, const uint8_t *con
 
 }  // namespace
 
-size_t gemv_seq_sync_bytes() { return sizeof(unsigned) * size_t(1 + kSeqMaxGroups); }
+size_t gemv_seq_workspace_bytes() { return kSyncBytes + kRecBytesMax; }
 
 cudaError_t launch_gemv_seq(int type, int n_groups, const int *n_mats, const uint8_t *const *W, float *const *y,
                             const int64_t *M, const float *const *x, const int64_t *K, unsigned *sync,
