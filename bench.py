@@ -684,11 +684,16 @@ def tensor_rates(dev):
 
 
 def l2_flusher(dev):
+    """Evict every line of L2 between timed steps: write a buffer twice the
+    size of L2, then read another one (so that the write-backs of the flush's
+    own dirty lines happen inside the flush, not inside the next timed step)."""
     import torch
-    buf = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    wbuf = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(64 * 2**20, dtype=torch.float32, device=dev)
 
     def flush():
-        buf.fill_(1)
+        wbuf.fill_(1)
+        rbuf.sum()
     return flush
 
 

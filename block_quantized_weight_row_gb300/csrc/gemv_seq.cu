@@ -57,91 +57,115 @@ using gemv::kXRecWords;
 using gemv::quantize_x_records_2lane;
 
 constexpr int kSqConsumers = 16;  // consumer warps per CTA
-constexpr int kSqGroupWarps = 8;  // consumer warps per group (two groups take the stages in turn)
 constexpr int kSqXWarps = 3;      // quantize x at the start; then one lane copies records (20 warps: 96 registers)
 constexpr int kSqProducer = kSqConsumers + kSqXWarps;  // warp index of the producer
-constexpr int kSqThreads = (kSqConsumers + kSqXWarps + 1) * 32;
+constexpr int kSqWarps = kSqConsumers + kSqXWarps + 1;
+constexpr int kSqThreads = kSqWarps * 32;
 constexpr int kSeqMaxGroups = 256;  // per launch; longer runs take several launches
 constexpr int kSeqMaxMats = 512;
 constexpr uint32_t kSeqDrainLimit = 1u << 26;
 constexpr int kRowRotation = 37;  // CTA range rotation per batch
 constexpr int kBarConsumers = 1;  // named barrier of the consumer warps
-constexpr int kBarPre = 2;        // named barrier of the warps that quantize x before the stream
+constexpr int kBarPre = 2;        // named barrier of the warps that quantize x at the start
 constexpr int kPreThreads = (kSqConsumers + kSqXWarps) * 32;
 constexpr int kMaxRecBufs = 8;    // record buffers in shared memory
+constexpr int kCopyWarps = 2;     // x warps that copy records (nrec is a multiple of it)
 constexpr int kSyncWords = 2 + kSeqMaxGroups;  // abort flag, CTAs done quantizing, CTAs done per batch
 constexpr size_t kSyncBytes = (kSyncWords * 4 + 255) / 256 * 256;
 constexpr size_t kRecBytesMax = size_t(kSeqMaxGroups) * (BQ_GEMV_SEQ_MAX_K / 256) * kXRecBytes;
-#ifndef SEQ_POLL_NS
-#define SEQ_POLL_NS 32  // sleep between polls of a mbarrier
-#endif
 
-struct SeqGroup {
+// One batch, as every CTA keeps it in shared memory during the launch (32
+// bytes; read there, not from the kernel parameters, whose dynamically
+// indexed reads miss the constant cache).
+struct BatchDesc {
   const float *x;
-  int K;           // a multiple of 256
-  int first_mat;   // matrices first_mat .. first_mat + n_mats - 1 of SeqArgs::m
-  int n_mats;
-  int rows;        // rows of all the batch's matrices
-  int wait_on;     // batch (of this launch) every CTA must have finished first, or -1
-  int signal;      // nonzero: a later batch waits for this one
-  int groups8;     // K / 256 groups of 8 blocks per row
-  int lanes;       // lanes per row: the power of two <= 32 the per-launch kernel takes
-  int row_bytes;
-  int stage_rows;  // rows per stage: one pass of a consumer group's warps, as the ring slot allows
-  int rec_off;     // words: x's records in SeqArgs::rec (batches that wait for nothing), else -1
-  int blk0;        // first block of x in the launch's quantization order (rec_off >= 0)
+  int rows;            // rows of all the batch's matrices
+  int rec_off;         // words: x's records in SeqArgs::rec, or -1: quantized in every CTA
+  int blk0;            // first block of x in the start-of-launch quantization (rec_off >= 0)
+  uint16_t K;          // a multiple of 256, at most BQ_GEMV_SEQ_MAX_K
+  uint16_t first_mat;  // matrices first_mat .. first_mat + n_mats - 1
+  uint16_t stage_rows; // rows per stage: one pass of a consumer group, as the ring slot allows
+  int16_t wait_on;     // batch (of this launch) every CTA must have finished first, or -1
+  uint8_t n_mats;
+  uint8_t lanes;       // lanes per row: the power of two <= 32 the per-launch kernel takes
+  uint8_t signal;      // nonzero: a later batch waits for this one
+  uint8_t lanes_log2;
 };
+static_assert(sizeof(BatchDesc) == 32, "batch descriptor");
 
-struct SeqMat {
+struct MatDesc {
   const uint8_t *W;
   float *y;
   int row_start;  // first row of this matrix within its batch
   int pad;
 };
+static_assert(sizeof(MatDesc) == 24, "matrix descriptor");
 
 struct SeqArgs {
-  SeqGroup g[kSeqMaxGroups];
-  SeqMat m[kSeqMaxMats];
+  BatchDesc g[kSeqMaxGroups];
+  MatDesc m[kSeqMaxMats];
   int n_groups;
+  int n_mats;
   int stages;
   int slot_bytes;  // bytes of one ring stage
   int xrec_bytes;  // bytes of one record buffer (the largest K of the launch)
   int nrec;        // record buffers in shared memory: a power of two, 2..kMaxRecBufs
+  int nrec_log2;
+  int ngroups;     // consumer groups: 2 or 4 (kSqConsumers / ngroups warps each)
   int pre_blocks;  // blocks of x quantized at the start (every batch with rec_off >= 0)
+  int n_local;     // the first n_local batches are quantized by every CTA itself
+  int desc_bytes;  // shared-memory bytes of the descriptor tables (16-byte multiple)
   uint32_t *rec;   // x's records of those batches (global memory)
   unsigned *sync;  // [0]: abort flag, [1]: CTAs done quantizing, [2 + g]: CTAs done with batch g; zeroed
   unsigned *err;
   uint32_t spin_limit;
+  uint32_t poll_ns;  // sleep between polls of a mbarrier
 };
 
-// Rows [r0, r1) of batch g taken by this CTA.
-__device__ __forceinline__ void cta_rows(int rows, int g, int &r0, int &r1) {
+// A batch's fields in registers.
+template <int TYPE>
+struct Batch {
+  const float *x;
+  int rows, rec_off, blk0, K, first_mat, n_mats, stage_rows, wait_on, lanes, lanes_log2, signal, groups8, row_bytes;
+  __device__ __forceinline__ explicit Batch(const BatchDesc &d)
+      : x(d.x), rows(d.rows), rec_off(d.rec_off), blk0(d.blk0), K(d.K), first_mat(d.first_mat), n_mats(d.n_mats),
+        stage_rows(d.stage_rows), wait_on(d.wait_on), lanes(d.lanes), lanes_log2(d.lanes_log2), signal(d.signal),
+        groups8(d.K >> 8), row_bytes((d.K >> 5) * Fmt<TYPE>::kBytes) {}
+};
+
+// Rows [r0, r1) of a batch of `rows` rows taken by this CTA (the batch's
+// part p, the parts rotating over the CTAs from batch to batch). Computed
+// once per batch at the start of the launch into a shared-memory table: the
+// 64-bit divisions cost hundreds of cycles.
+__device__ __forceinline__ int2 cta_rows(int rows, int g) {
   const int G = int(gridDim.x);
   const int p = int((blockIdx.x + unsigned(g) * kRowRotation) % unsigned(G));
-  r0 = int(int64_t(rows) * p / G);
-  r1 = int(int64_t(rows) * (p + 1) / G);
+  return make_int2(int(int64_t(rows) * p / G), int(int64_t(rows) * (p + 1) / G));
 }
 
 // Stages of one batch's row range in order: each at most stage_rows rows,
 // never past the range or a matrix's end. Producer and consumers walk the
 // same sequence (incrementally: no division per stage).
 struct StageWalk {
-  int row, r1, mat, mat_end, last;
-  __device__ __forceinline__ void begin(const SeqArgs &a, const SeqGroup &G, int r0, int r1_) {
+  int row, r1, mat, mat_end, last, rows, stage_rows;
+  template <int TYPE>
+  __device__ __forceinline__ void begin(const MatDesc *md, const Batch<TYPE> &B, int r0, int r1_) {
     row = r0;
     r1 = r1_;
-    mat = G.first_mat;
-    last = G.first_mat + G.n_mats - 1;
-    while (mat < last && row >= a.m[mat + 1].row_start) ++mat;
-    mat_end = mat < last ? a.m[mat + 1].row_start : G.rows;
+    rows = B.rows;
+    stage_rows = B.stage_rows;
+    mat = B.first_mat;
+    last = B.first_mat + B.n_mats - 1;
+    while (mat < last && row >= md[mat + 1].row_start) ++mat;
+    mat_end = mat < last ? md[mat + 1].row_start : rows;
   }
   // rows of the stage that starts at `row` (row < r1)
-  __device__ __forceinline__ int next(const SeqArgs &a, const SeqGroup &G) {
+  __device__ __forceinline__ int next(const MatDesc *md) {
     if (row >= mat_end) {
       ++mat;
-      mat_end = mat < last ? a.m[mat + 1].row_start : G.rows;
+      mat_end = mat < last ? md[mat + 1].row_start : rows;
     }
-    return min(min(G.stage_rows, r1 - row), mat_end - row);
+    return min(min(stage_rows, r1 - row), mat_end - row);
   }
 };
 
@@ -166,7 +190,7 @@ __device__ __forceinline__ void seq_abort(const SeqArgs &a, volatile int *cta_ab
 __device__ __forceinline__ bool seq_wait(const SeqArgs &a, uint64_t *bar, uint32_t parity, volatile int *cta_abort) {
   for (uint32_t i = 0; i < a.spin_limit; ++i) {
     if (mbar_test_wait(bar, parity)) return true;
-    if (SEQ_POLL_NS > 0) __nanosleep(SEQ_POLL_NS);
+    __nanosleep(a.poll_ns);
     if ((i & 63) == 63 && *cta_abort) return false;
   }
   seq_abort(a, cta_abort);
@@ -193,14 +217,20 @@ __device__ __forceinline__ bool seq_batch_wait(const SeqArgs &a, int g, volatile
   return seq_count_wait(a, a.sync + 2 + g, cta_abort);
 }
 
-// Quantize this CTA's share of x's blocks of every batch that waits for
-// nothing (the launch's blocks in batch order, cut evenly over the CTAs) into
-// the global records: two threads per block (quantize_block_pair), so the
-// records are those of the per-launch kernels. tid < kPreThreads.
-__device__ __forceinline__ void seq_prequantize(const SeqArgs &a, int tid) {
+// Blocks [lo, hi) of the start-of-launch quantization taken by this CTA.
+__device__ __forceinline__ void pre_range(const SeqArgs &a, int &lo, int &hi) {
   const int G = int(gridDim.x);
-  const int lo = int(int64_t(a.pre_blocks) * blockIdx.x / G);
-  const int hi = int(int64_t(a.pre_blocks) * (blockIdx.x + 1) / G);
+  lo = int(int64_t(a.pre_blocks) * blockIdx.x / G);
+  hi = int(int64_t(a.pre_blocks) * (blockIdx.x + 1) / G);
+}
+
+// Quantize this CTA's share of x's blocks of every batch whose records come
+// from the workspace (the launch's blocks in batch order, cut evenly over the
+// CTAs) into those records: two threads per block (quantize_block_pair), so
+// the records are those of the per-launch kernels. tid < kPreThreads.
+__device__ __forceinline__ void seq_prequantize(const SeqArgs &a, const BatchDesc *bd, int tid) {
+  int lo, hi;
+  pre_range(a, lo, hi);
   const int h = tid & 1;
   int g = 0;  // batch of block i (i only grows)
   for (int base = lo; base < hi; base += kPreThreads / 2) {  // uniform: every lane runs every round
@@ -212,9 +242,9 @@ __device__ __forceinline__ void seq_prequantize(const SeqArgs &a, int tid) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) f[j] = 0.0f;
     if (valid) {
-      while (a.g[g].rec_off < 0 || i >= a.g[g].blk0 + a.g[g].K / kQK) ++g;
-      const int bl = i - a.g[g].blk0;
-      const float4 *src = reinterpret_cast<const float4 *>(a.g[g].x + int64_t(bl) * kQK + 16 * h);
+      while (bd[g].rec_off < 0 || i >= bd[g].blk0 + bd[g].K / kQK) ++g;
+      const int bl = i - bd[g].blk0;
+      const float4 *src = reinterpret_cast<const float4 *>(bd[g].x + int64_t(bl) * kQK + 16 * h);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float4 v = __ldcg(src + c);
@@ -223,10 +253,28 @@ __device__ __forceinline__ void seq_prequantize(const SeqArgs &a, int tid) {
         f[4 * c + 2] = v.z;
         f[4 * c + 3] = v.w;
       }
-      rg = a.rec + a.g[g].rec_off + (bl >> 3) * kXRecWords;
+      rg = a.rec + bd[g].rec_off + (bl >> 3) * kXRecWords;
       jb = bl & 7;
     }
     gemv::quantize_block_pair(f, h, rg, jb, valid);
+  }
+}
+
+// L2 prefetch of this CTA's slice of the start-of-launch quantization (the
+// x ranges seq_prequantize reads here) and of x of the first batches, which
+// every CTA quantizes itself.
+__device__ __forceinline__ void seq_prefetch_x(const SeqArgs &a, const BatchDesc *bd) {
+  int lo, hi;
+  pre_range(a, lo, hi);
+  for (int g = 0; g < a.n_groups; ++g) {
+    const BatchDesc &d = bd[g];
+    if (d.rec_off < 0) {
+      if (d.wait_on < 0 && g < a.n_local) prefetch_l2(d.x, uint32_t(d.K) * 4u);
+      continue;
+    }
+    if (d.blk0 >= hi) break;
+    const int b0 = max(lo, d.blk0), b1 = min(hi, d.blk0 + d.K / kQK);
+    if (b0 < b1) prefetch_l2(d.x + int64_t(b0 - d.blk0) * kQK, uint32_t(b1 - b0) * kQK * 4u);
   }
 }
 
@@ -234,25 +282,39 @@ template <int TYPE>
 __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constant__ SeqArgs a) {
   constexpr int GW = GroupWords<TYPE>::kWords;
   extern __shared__ __align__(128) uint8_t smem[];
-  // record buffer b at smem + b * xrec_bytes, b < nrec
+  // record buffer b at smem + b * xrec_bytes, b < nrec; then the ring, the
+  // descriptor tables, the barriers
   uint8_t *ring = smem + size_t(a.nrec) * a.xrec_bytes;
-  uint64_t *full = reinterpret_cast<uint64_t *>(ring + size_t(a.stages) * a.slot_bytes);
+  BatchDesc *bd = reinterpret_cast<BatchDesc *>(ring + size_t(a.stages) * a.slot_bytes);
+  MatDesc *md = reinterpret_cast<MatDesc *>(bd + a.n_groups);
+  int2 *rr = reinterpret_cast<int2 *>(md + a.n_mats);  // this CTA's rows of batch g
+  uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(bd) + a.desc_bytes);
   uint64_t *empty = full + a.stages;
   uint64_t *rfull = empty + a.stages;  // [nrec]: records of buffer b in place
   uint64_t *rempty = rfull + a.nrec;   // [nrec]: records of buffer b no longer read
   volatile int *cta_abort = reinterpret_cast<volatile int *>(rempty + a.nrec);
-  const uint32_t rmask = uint32_t(a.nrec - 1);
   __shared__ int s_go;  // dependency wait result, broadcast to the consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.stages;
+  const uint32_t rmask = uint32_t(a.nrec - 1);
 
+  {
+    // descriptor tables into shared memory (the words of g[] and m[] in use)
+    const uint32_t *pg = reinterpret_cast<const uint32_t *>(a.g);
+    const uint32_t *pm = reinterpret_cast<const uint32_t *>(a.m);
+    uint32_t *sg = reinterpret_cast<uint32_t *>(bd), *sm_ = reinterpret_cast<uint32_t *>(md);
+    const int ng = a.n_groups * int(sizeof(BatchDesc) / 4), nm = a.n_mats * int(sizeof(MatDesc) / 4);
+    for (int i = threadIdx.x; i < ng; i += kSqThreads) sg[i] = pg[i];
+    for (int i = threadIdx.x; i < nm; i += kSqThreads) sm_[i] = pm[i];
+    for (int g = threadIdx.x; g < a.n_groups; g += kSqThreads) rr[g] = cta_rows(a.g[g].rows, g);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kSqGroupWarps);  // every warp of the stage's consumer group releases it
+      mbar_init(&empty[s], kSqConsumers / a.ngroups);  // every warp of the stage's consumer group releases it
     }
     for (int b = 0; b < a.nrec; ++b) {
-      mbar_init(&rfull[b], 1);  // the record copier (bytes on the transaction count)
+      mbar_init(&rfull[b], 32);  // every lane of the copying x warp, after its record stores
       mbar_init(&rempty[b], kSqConsumers);
     }
     *cta_abort = 0;
@@ -261,10 +323,10 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
   __syncthreads();
 
   if (warp != kSqProducer && a.pre_blocks > 0) {
-    // x of every batch that waits for nothing, quantized once for the whole
-    // grid while the producer already streams weights; then this CTA counts
-    // itself done (release: the records are visible to the whole GPU)
-    seq_prequantize(a, threadIdx.x);
+    // x of the batches whose records come from the workspace, quantized once
+    // for the whole grid (this CTA's slice); then this CTA counts itself done
+    // (release: the records are visible to the whole GPU)
+    seq_prequantize(a, bd, threadIdx.x);
     named_bar_sync(kBarPre, kPreThreads);
     if (threadIdx.x == 0) {
       __threadfence();
@@ -275,29 +337,33 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
   if (warp == kSqProducer) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
+      // Before the weight stream, ask L2 for the x this CTA reads first (its
+      // slice of the start-of-launch quantization, and x of the first batch,
+      // which every CTA quantizes itself): these loads then do not queue
+      // behind the whole GPU's weight stream.
+      seq_prefetch_x(a, bd);
       int issued = 0;
       const uint64_t policy = l2_evict_first_policy();  // every weight is read once
       bool stop = false;
       int j = 0, s = 0;  // stage index, its ring slot
       uint32_t ph = 0;   // (j / S) & 1
       for (int g = 0; g < a.n_groups && !stop; ++g) {
-        const SeqGroup &G = a.g[g];
-        int r0, r1;
-        cta_rows(G.rows, g, r0, r1);
+        const Batch<TYPE> B(bd[g]);
+        const int r0 = rr[g].x, r1 = rr[g].y;
         if (r0 >= r1) continue;
-        StageWalk wk;
-        wk.begin(a, G, r0, r1);
+        StageWalk wk{};
+        wk.begin(md, B, r0, r1);
         while (wk.row < r1) {
           // the slot's previous use (stage j - S) must have been released
           if (j >= S && !seq_wait(a, &empty[s], ph ^ 1u, cta_abort)) {
             stop = true;
             break;
           }
-          const int nrows = wk.next(a, G);
-          const uint32_t bytes = uint32_t(nrows) * uint32_t(G.row_bytes);
+          const int nrows = wk.next(md);
+          const uint32_t bytes = uint32_t(nrows) * uint32_t(B.row_bytes);
           mbar_arrive_expect_tx(&full[s], bytes);
           bulk_g2s_hint(ring + size_t(s) * a.slot_bytes,
-                        a.m[wk.mat].W + int64_t(wk.row - a.m[wk.mat].row_start) * G.row_bytes, bytes, &full[s],
+                        md[wk.mat].W + int64_t(wk.row - md[wk.mat].row_start) * B.row_bytes, bytes, &full[s],
                         policy);
           wk.row += nrows;
           issued = ++j;
@@ -315,67 +381,84 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
     }
   } else if (warp >= kSqConsumers) {
     // ------------------------------------------------------- record copier --
-    // One lane copies the records of every batch that waits for nothing from
-    // global memory into the record buffers, up to nrec - 1 batches ahead of
-    // the consumers (1-D bulk copies completing on rfull). A batch that waits
-    // for an earlier one is quantized by the consumers themselves once the
-    // wait is over (they are idle then).
-    if (warp == kSqConsumers && lane == 0) {
-      bool ok = a.pre_blocks == 0 || seq_count_wait(a, a.sync + 1, cta_abort);
-      // the records were written by other threads' ordinary stores; the
-      // copies read them through the asynchronous proxy
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      uint32_t used = 0, par = 0;  // buffers copied into; parity of each one's last copy
-      for (int g = 0, k = 0; g < a.n_groups && ok; ++g) {
-        const SeqGroup &G = a.g[g];
-        int r0, r1;
-        cta_rows(G.rows, g, r0, r1);
-        if (r0 >= r1) continue;  // no rows here: nothing read, nothing written
-        const int b = int(uint32_t(k) & rmask);
-        const int use = k / a.nrec;
-        ++k;
-        if (G.rec_off < 0) continue;
-        // the buffer's previous batch is done once its consumers released it
-        if (use > 0 && !seq_wait(a, &rempty[b], uint32_t((use - 1) & 1), cta_abort)) break;
-        const uint32_t bytes = uint32_t(G.K / 256) * kXRecBytes;
-        mbar_arrive_expect_tx(&rfull[b], bytes);
-        bulk_g2s(smem + size_t(b) * a.xrec_bytes, a.rec + G.rec_off, bytes, &rfull[b]);
-        used |= 1u << b;
-        par = (par & ~(1u << b)) | (uint32_t(use & 1) << b);
+    // The x warps copy the records of every batch whose records come from
+    // the workspace into the record buffers, up to nrec - 1 batches ahead of
+    // the consumers, with 16-byte loads through L2 (not bulk copies: the
+    // SM's bulk-copy unit, which streams the weights, takes a fixed time per
+    // copy, and short batches would double its copies). Copier warp w
+    // copies the CTA's batches k with k mod kCopyWarps == w, so that the
+    // copies of several batches are in flight at once; as nrec is a multiple
+    // of kCopyWarps, every record buffer is filled by one warp only, in the
+    // order of its uses, so that a parity wait on its release is never more
+    // than one phase ahead. The other batches are quantized by the consumers
+    // themselves.
+    const int xw = warp - kSqConsumers;
+    bool ok = a.pre_blocks == 0;
+    if (!ok) {
+      int w = 1;
+      if (lane == 0) w = seq_count_wait(a, a.sync + 1, cta_abort);
+      ok = __shfl_sync(kFull, w, 0) != 0;
+      __syncwarp();  // the other lanes' loads follow lane 0's acquire
+    }
+    for (int g = 0, k = 0; g < a.n_groups && ok && xw < kCopyWarps; ++g) {
+      const BatchDesc &d = bd[g];
+      const int r0 = rr[g].x, r1 = rr[g].y;
+      if (r0 >= r1) continue;  // no rows here: nothing read, nothing written
+      const int b = int(uint32_t(k) & rmask);
+      const int use = k >> a.nrec_log2;
+      const bool mine = k % kCopyWarps == xw;
+      ++k;
+      if (d.rec_off < 0 || !mine) continue;
+      // the buffer's previous batch is done once its consumers released it
+      if (use > 0 && !seq_wait(a, &rempty[b], uint32_t((use - 1) & 1), cta_abort)) break;
+      const int n16 = (d.K / 256) * (kXRecBytes / 16);
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.rec + d.rec_off);
+      uint4 *dst = reinterpret_cast<uint4 *>(smem + size_t(b) * a.xrec_bytes);
+      int i = lane;
+      for (; i + 3 * 32 < n16; i += 4 * 32) {  // four loads in flight per lane
+        const uint4 v0 = __ldcg(src + i), v1 = __ldcg(src + i + 32), v2 = __ldcg(src + i + 64),
+                    v3 = __ldcg(src + i + 96);
+        dst[i] = v0;
+        dst[i + 32] = v1;
+        dst[i + 64] = v2;
+        dst[i + 96] = v3;
       }
-      // never leave with a copy in flight
-      for (int b = 0; b < a.nrec; ++b)
-        if (((used >> b) & 1u) && !mbar_wait_bounded(&rfull[b], (par >> b) & 1u, kSeqDrainLimit))
-          atomicOr(a.err, kErrTimeout);
+      for (; i < n16; i += 32) dst[i] = __ldcg(src + i);
+      mbar_arrive(&rfull[b]);  // release: this lane's stores before the consumers' wait
     }
   } else {
     // --------------------------------------------------------- consumers --
-    // Two groups of kSqGroupWarps warps take the stages in turn (stage j:
-    // group j & 1); within a stage every warp of the group takes its rows,
+    // ngroups groups of gw warps take the stages in turn (stage j: group
+    // j mod ngroups); within a stage every warp of the group takes its rows,
     // as in the per-launch kernel, so that a stage is consumed by its whole
     // group at once and released once.
-    const int cg = warp / kSqGroupWarps;  // consumer group
-    const int cw = warp % kSqGroupWarps;  // warp within the group
+    const int gw = kSqConsumers / a.ngroups;
+    const int cg = warp / gw;  // consumer group
+    const int cw = warp % gw;  // warp within the group
+    const int gmask = a.ngroups - 1;
     bool skip = false;  // a wait ran out: walk on without waiting or computing
     int j = 0, s = 0;   // stage index (the producer's numbering), its ring slot
     uint32_t ph = 0;    // (j / S) & 1
     uint32_t nq = 0;    // bit b: parity of the copies into buffer b so far (phases of rfull)
     for (int g = 0, k = 0; g < a.n_groups; ++g) {
-      const SeqGroup &G = a.g[g];
-      int r0, r1;
-      cta_rows(G.rows, g, r0, r1);
+      const Batch<TYPE> B(bd[g]);
+      const int r0 = rr[g].x, r1 = rr[g].y;
       if (r0 < r1) {
         const int b = int(uint32_t(k) & rmask);
-        if (G.wait_on >= 0) {
-          // batch wait_on's outputs are (or overlap) this batch's x, or this
-          // batch's outputs overwrite its x: once every CTA has finished it,
-          // all consumer threads quantize x into the buffer (its last batch,
-          // k - 2, is done: the consumers run the batches in order)
-          if (threadIdx.x == 0) s_go = (!skip && seq_batch_wait(a, G.wait_on, cta_abort)) ? 1 : 0;
+        if (B.rec_off < 0) {
+          // x quantized here by all consumer threads: a batch that waits for
+          // an earlier one (batch wait_on's outputs are, or overlap, its x, or
+          // its outputs overwrite wait_on's x), once every CTA has finished
+          // that batch; or one of the launch's first batches, whose records
+          // the start-of-launch quantization has not produced yet. The
+          // buffer's last batch (k - nrec) is done: the consumers run the
+          // batches in order.
+          if (threadIdx.x == 0)
+            s_go = (!skip && (B.wait_on < 0 || seq_batch_wait(a, B.wait_on, cta_abort))) ? 1 : 0;
           named_bar_sync(kBarConsumers, kSqConsumers * 32);
           if (!s_go) skip = true;
-          if (!skip)  // read past L1: x was written by other CTAs during this launch
-            quantize_x_records_2lane(G.x, G.K / kQK, reinterpret_cast<uint32_t *>(smem + b * a.xrec_bytes),
+          if (!skip)  // read past L1: x may have been written by other CTAs during this launch
+            quantize_x_records_2lane(B.x, B.K / kQK, reinterpret_cast<uint32_t *>(smem + b * a.xrec_bytes),
                                      threadIdx.x, kSqConsumers * 32);
           // the records are written, and s_go is read before it is rewritten
           named_bar_sync(kBarConsumers, kSqConsumers * 32);
@@ -384,26 +467,26 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
           nq ^= 1u << b;
         }
         const uint32_t *xr = reinterpret_cast<const uint32_t *>(smem + b * a.xrec_bytes);
-        const int L = G.lanes, rpw = 32 / L;
-        const int rr = lane / L;  // row (within the warp's pass) handled by this lane
-        const int gl = lane % L;  // first group of that row handled by this lane
-        StageWalk wk;
-        wk.begin(a, G, r0, r1);
+        const int L = B.lanes, rpw = 32 >> B.lanes_log2;
+        const int lr = lane >> B.lanes_log2;  // row (within the warp's pass) handled by this lane
+        const int gl = lane & (L - 1);        // first group of that row handled by this lane
+        StageWalk wk{};
+        wk.begin(md, B, r0, r1);
         while (wk.row < r1) {
-          const int nrows = wk.next(a, G);
-          if ((j & 1) == cg) {
+          const int nrows = wk.next(md);
+          if ((j & gmask) == cg) {
             // every warp of the group consumes every stage of the group in
             // order, so a parity wait is never more than one phase ahead
             if (!skip) skip = !seq_wait(a, &full[s], ph, cta_abort);
             if (!skip) {
-              float *yp = a.m[wk.mat].y + (wk.row - a.m[wk.mat].row_start);
+              float *yp = md[wk.mat].y + (wk.row - md[wk.mat].row_start);
               const uint8_t *stage = ring + size_t(s) * a.slot_bytes;
-              for (int pr = cw * rpw; pr < nrows; pr += kSqGroupWarps * rpw) {
-                const int r = pr + rr;
+              for (int pr = cw * rpw; pr < nrows; pr += gw * rpw) {
+                const int r = pr + lr;
                 float acc = 0.0f;
                 if (r < nrows) {
-                  const uint8_t *rowp = stage + size_t(r) * G.row_bytes;
-                  for (int q = gl; q < G.groups8; q += L) {
+                  const uint8_t *rowp = stage + size_t(r) * B.row_bytes;
+                  for (int q = gl; q < B.groups8; q += L) {
                     uint32_t w[GW];
                     const uint4 *src = reinterpret_cast<const uint4 *>(rowp + size_t(q) * GW * 4);
 #pragma unroll
@@ -435,7 +518,7 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
         if (!skip && lane == 0) mbar_arrive(&rempty[b]);
         ++k;
       }
-      if (G.signal) {
+      if (B.signal) {
         // every row of batch g (and of every earlier batch) this CTA owns is
         // written: count the CTA done with batch g, after a fence that makes
         // the consumers' stores visible to the whole GPU
@@ -456,7 +539,6 @@ namespace {
 
 bool spans_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
-// One launch over the batches `groups` (each with K % 256 == 0 and rows > 0).
 template <int TYPE>
 cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<int> &mat0, const int *n_mats,
                              const uint8_t *const *W, float *const *y, const int64_t *M, const float *const *x,
@@ -464,9 +546,19 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   constexpr int BB = Fmt<TYPE>::kBytes;
   std::unique_ptr<SeqArgs> a(new SeqArgs{});
   const int n = int(groups.size());
+  // Consumer groups: two of 8 warps, or four of 4 where the CTAs' share of a
+  // batch is short (a stage then holds a few rows, and four stages in
+  // progress instead of two hide their latency).
+  int64_t wbytes = 0;
+  for (int i = 0; i < n; ++i)
+    for (int k = 0; k < n_mats[groups[i]]; ++k) wbytes += M[mat0[groups[i]] + k] * (K[groups[i]] / kQK) * BB;
+  static const int forced_groups = tuning_value("BQ_GEMV_SEQ_GROUPS");  // read once per process
+  int ngroups = wbytes < int64_t(n) * di->sm_count * (64 << 10) ? 4 : 2;
+  if (forced_groups == 2 || forced_groups == 4) ngroups = forced_groups;
+  const int gw = kSqConsumers / ngroups;
   // Per batch: the per-launch kernel's lanes per row (so that every row's
   // arithmetic is the same), and the bytes of one pass of a consumer group
-  // (kSqGroupWarps warps, 32 / lanes rows each).
+  // (gw warps, 32 / lanes rows each).
   std::vector<int> lanes(n), row_bytes(n), pass_rows(n);
   int xrec_bytes = 0, max_row = 0, max_pass = 0;
   for (int i = 0; i < n; ++i) {
@@ -476,7 +568,7 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
     while (L < groups8 && L < 32) L <<= 1;
     lanes[i] = L;
     row_bytes[i] = int(K[gi] / kQK) * BB;
-    pass_rows[i] = kSqGroupWarps * (32 / L);
+    pass_rows[i] = gw * (32 / L);
     xrec_bytes = std::max(xrec_bytes, groups8 * kXRecBytes);
     max_row = std::max(max_row, row_bytes[i]);
     max_pass = std::max(max_pass, pass_rows[i] * row_bytes[i]);
@@ -491,35 +583,50 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   // large copy: the copy cost is per copy), capped so that the ring keeps at
   // least four stages; a batch whose pass does not fit takes the rows that do.
   const int reserve = 1024;  // per-CTA system reservation
-  const int budget = std::min(di->smem_per_sm - reserve, di->max_smem_optin) - nrec * xrec_bytes - 1024;
+  // descriptor tables of this launch (nm: matrices with rows)
+  int nm_total = 0;
+  for (int i = 0; i < n; ++i)
+    for (int k = 0; k < n_mats[groups[i]]; ++k) nm_total += M[mat0[groups[i]] + k] > 0 ? 1 : 0;
+  const int desc_bytes =
+      (n * int(sizeof(BatchDesc)) + nm_total * int(sizeof(MatDesc)) + n * int(sizeof(int2)) + 15) / 16 * 16;
+  const int budget =
+      std::min(di->smem_per_sm - reserve, di->max_smem_optin) - nrec * xrec_bytes - desc_bytes - 1024;
   static const int forced_slot = tuning_value("BQ_GEMV_SEQ_SLOT_BYTES");  // read once per process
   int slot = std::min(max_pass, budget / 4) / 16 * 16;
   if (forced_slot > 0) slot = (forced_slot + 15) / 16 * 16;
   if (slot < max_row) slot = (max_row + 15) / 16 * 16;
-  const int stages = std::min(32, budget / slot);
-  if (stages < 2) return cudaErrorInvalidValue;  // the ABI layer bounds K, so this does not happen
+  // A multiple of ngroups: a ring slot then always serves the same consumer
+  // group, which waits on it only for stages after the slot's previous one
+  // (of the same group, so already consumed): parity waits stay one phase
+  // ahead at most.
+  const int stages = std::min(32, budget / slot) / ngroups * ngroups;
+  if (stages < ngroups) return cudaErrorInvalidValue;  // slot <= budget / 4: does not happen
   a->n_groups = n;
   a->stages = stages;
   a->slot_bytes = slot;
   a->xrec_bytes = xrec_bytes;
+  a->desc_bytes = desc_bytes;
   a->nrec = nrec;
+  a->nrec_log2 = nrec == 2 ? 1 : nrec == 4 ? 2 : 3;
+  a->ngroups = ngroups;
   a->sync = sync;
   a->rec = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(sync) + kSyncBytes);
   a->err = di->err_word;
   a->spin_limit = spin_limit();
+  static const int forced_poll = tuning_value("BQ_GEMV_SEQ_POLL_NS");  // read once per process
+  a->poll_ns = forced_poll > 0 ? uint32_t(forced_poll) : 32u;
   int nm = 0;
   for (int i = 0; i < n; ++i) {
     const int gi = groups[i];
-    SeqGroup &G = a->g[i];
+    BatchDesc &G = a->g[i];
     G.x = x[gi];
-    G.K = int(K[gi]);
-    G.first_mat = nm;
+    G.K = uint16_t(K[gi]);
+    G.first_mat = uint16_t(nm);
     G.wait_on = -1;
-    G.groups8 = G.K / 256;
-    G.lanes = lanes[i];
-    G.row_bytes = row_bytes[i];
+    G.lanes = uint8_t(lanes[i]);
+    G.lanes_log2 = uint8_t(__builtin_ctz(unsigned(lanes[i])));
     const int pass_bytes = pass_rows[i] * row_bytes[i];
-    G.stage_rows = pass_bytes <= slot ? pass_rows[i] * (slot / pass_bytes) : slot / row_bytes[i];
+    G.stage_rows = uint16_t(pass_bytes <= slot ? pass_rows[i] * (slot / pass_bytes) : slot / row_bytes[i]);
     int rows = 0;
     for (int k = 0; k < n_mats[gi]; ++k) {
       const int mi = mat0[gi] + k;
@@ -530,50 +637,56 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
       rows += int(M[mi]);
       ++nm;
     }
-    G.n_mats = nm - G.first_mat;
+    G.n_mats = uint8_t(nm - G.first_mat);
     G.rows = rows;
   }
+  a->n_mats = nm;
   // Orders that memory imposes: batch i waits for the latest earlier batch
   // whose outputs its x reads, or whose x its outputs overwrite. (Outputs
   // never overlap outputs; the ABI layer rejects that.)
+  auto mat_rows = [&](const BatchDesc &B, int mi) {
+    return (mi + 1 < B.first_mat + B.n_mats ? a->m[mi + 1].row_start : B.rows) - a->m[mi].row_start;
+  };
   for (int i = 1; i < n; ++i) {
-    const SeqGroup &G = a->g[i];
+    const BatchDesc &G = a->g[i];
     const uintptr_t x0 = reinterpret_cast<uintptr_t>(G.x), x1 = x0 + uintptr_t(G.K) * 4;
     for (int p = i - 1; p >= 0 && a->g[i].wait_on < 0; --p) {
-      const SeqGroup &P = a->g[p];
+      const BatchDesc &P = a->g[p];
       const uintptr_t px0 = reinterpret_cast<uintptr_t>(P.x), px1 = px0 + uintptr_t(P.K) * 4;
       bool dep = false;
       for (int mp = P.first_mat; mp < P.first_mat + P.n_mats && !dep; ++mp) {
         const uintptr_t y0 = reinterpret_cast<uintptr_t>(a->m[mp].y);
-        const int rows = (mp + 1 < P.first_mat + P.n_mats ? a->m[mp + 1].row_start : P.rows) - a->m[mp].row_start;
-        dep = spans_overlap(x0, x1, y0, y0 + uintptr_t(rows) * 4);
+        dep = spans_overlap(x0, x1, y0, y0 + uintptr_t(mat_rows(P, mp)) * 4);
       }
       for (int mi = G.first_mat; mi < G.first_mat + G.n_mats && !dep; ++mi) {
         const uintptr_t y0 = reinterpret_cast<uintptr_t>(a->m[mi].y);
-        const int rows = (mi + 1 < G.first_mat + G.n_mats ? a->m[mi + 1].row_start : G.rows) - a->m[mi].row_start;
-        dep = spans_overlap(px0, px1, y0, y0 + uintptr_t(rows) * 4);
+        dep = spans_overlap(px0, px1, y0, y0 + uintptr_t(mat_rows(G, mi)) * 4);
       }
       if (dep) {
-        a->g[i].wait_on = p;
+        a->g[i].wait_on = int16_t(p);
         a->g[p].signal = 1;
       }
     }
   }
   // x of every batch that waits for nothing is quantized once at the start
   // of the launch, in batch order, into the records area of the workspace
+  // (but the first batch, which every CTA quantizes itself while the grid
+  // quantizes the rest)
+  const int n_local = std::min(n, 1);
   int rec_words = 0, blocks = 0;
   for (int i = 0; i < n; ++i) {
-    SeqGroup &G = a->g[i];
+    BatchDesc &G = a->g[i];
     G.rec_off = -1;
     G.blk0 = blocks;
-    if (G.wait_on >= 0) continue;
+    if (G.wait_on >= 0 || i < n_local) continue;
     G.rec_off = rec_words;
-    rec_words += G.groups8 * kXRecWords;
+    rec_words += (G.K / 256) * kXRecWords;
     blocks += G.K / kQK;
   }
   a->pre_blocks = blocks;
-  const size_t smem =
-      size_t(nrec) * xrec_bytes + size_t(stages) * slot + 8 * (2 * size_t(stages) + 2 * size_t(nrec)) + 16;
+  a->n_local = n_local;
+  const size_t smem = size_t(nrec) * xrec_bytes + size_t(stages) * slot + size_t(desc_bytes) +
+                     8 * (2 * size_t(stages) + 2 * size_t(nrec)) + 16;
   const void *fn = reinterpret_cast<const void *>(k_gemv_seq<TYPE>);
   cudaError_t e = ensure_smem(fn, int(smem));
   if (e != cudaSuccess) return e;

@@ -566,6 +566,8 @@ def test_gemv_sequence_matches_oracle(bq, orc, dev, t):
         groups.append(([torch.from_numpy(w).to(dev) for w in mats], x.to(dev), Ms, K, outs))
     bq.gemv_sequence(t, groups)
     torch.cuda.synchronize()
+    from block_quantized_weight_row_gb300 import binding
+    assert binding.device_status() == 0, "a bounded wait ran out"
     for (K, Ms, x, mats), g in zip(batches, groups):
         for M, w, y in zip(Ms, mats, g[4]):
             if M == 0:
@@ -595,6 +597,46 @@ def test_gemv_sequence_chain_reads_previous_outputs(bq, orc, dev):
         assert torch.equal(ys[g], ref[g]), f"batch {g}"
     y_ref, mag = orc.gemv(Q4, _np(ws[0]), x0.cpu().numpy(), K, K, with_mag=True)
     _check_float(_np(ys[0]), y_ref, mag, "chain batch 0")
+
+
+def test_gemv_sequence_mixed_waits_match_per_launch(bq, orc, dev):
+    """20 batches, some reading the previous batch's output (RAW), one whose
+    output overwrites an earlier batch's input (WAR), the rest independent:
+    the record buffers rotate through every kind of batch. Identical bits to
+    one bq_gemv_multi call per batch, no bounded wait runs out, and the first
+    and last products match the oracle."""
+    from block_quantized_weight_row_gb300 import binding, inputs
+    K = 1024
+    G = 20
+    ws = [bq.quantize_rows(Q4, inputs.weight(K, K, seed=800 + g, device=dev)) for g in range(G)]
+    xs = [inputs.activation(K, seed=850 + g, device=dev) for g in range(G)]
+    spare = inputs.activation(K, seed=899, device=dev)
+    reads_prev = {3, 4, 9, 14, 15, 16}
+    def build(outs, x_war):
+        groups = []
+        for g in range(G):
+            x = outs[g - 1] if g in reads_prev else (x_war if g == 7 else xs[g])
+            out = x_war if g == 11 else outs[g]  # batch 11 overwrites batch 7's input
+            groups.append(([ws[g]], x, [K], K, [out]))
+        return groups
+    outs = [torch.full((K,), float("nan"), device=dev) for _ in range(G)]
+    x_war = spare.clone()
+    assert binding.device_status() == 0
+    bq.gemv_sequence(Q4, build(outs, x_war))
+    assert binding.device_status() == 0
+    ref = [torch.full((K,), float("nan"), device=dev) for _ in range(G)]
+    x_war_ref = spare.clone()
+    for w_list, x, M_list, K_, y_list in build(ref, x_war_ref):
+        bq.gemv_multi(Q4, w_list, x, M_list, K_, outs=y_list)
+    torch.cuda.synchronize()
+    for g in range(G):
+        if g != 11:
+            assert torch.equal(outs[g], ref[g]), f"batch {g}"
+    assert torch.equal(x_war, x_war_ref), "batch 11's output (over batch 7's input)"
+    for g in (0, G - 1):
+        y_ref, mag = orc.gemv(Q4, _np(ws[g]), xs[g].cpu().numpy() if g not in reads_prev else _np(ref[g - 1]),
+                              K, K, with_mag=True)
+        _check_float(_np(outs[g]), y_ref, mag, f"batch {g}")
 
 
 def test_gemv_sequence_longer_than_one_launch(bq, orc, dev):
@@ -634,6 +676,8 @@ def test_gemv_sequence_full_decode_step_matches_per_launch(bq, orc, dev):
     bq.gemv_sequence(Q4, groups)
     bench.run_step(step, bq, True)
     torch.cuda.synchronize()
+    from block_quantized_weight_row_gb300 import binding
+    assert binding.device_status() == 0, "a bounded wait ran out"
     for g, outs in zip(step["groups"], seq_out):
         for y_ref, y in zip(g["y"], outs):
             assert torch.equal(y, y_ref)
