@@ -237,7 +237,14 @@ class ClockSampler:
     def summary(self):
         if self.t0 is None or self.t1 is None:
             return {"samples": 0, "source": self.source}
-        rows = [r for r in list(self.rows) if self.t0 <= r[0] <= self.t1]
+        allrows = list(self.rows)
+        rows = [r for r in allrows if self.t0 <= r[0] <= self.t1]
+        window = "timed region"
+        if not rows:  # a region shorter than the sampling period: the samples just around it
+            before = [r for r in allrows if r[0] < self.t0][-1:]
+            after = [r for r in allrows if r[0] > self.t1][:1]
+            rows = before + after
+            window = "samples just before and after the timed region (shorter than the period)"
         if not rows:
             return {"samples": 0, "source": self.source}
         reasons = set()
@@ -247,7 +254,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows), "source": self.source,
                 "power_w_max": round(max(powers), 1) if powers else None,
-                "window_s": round(self.t1 - self.t0, 4)}
+                "window_s": round(self.t1 - self.t0, 4), "window": window}
 
 
 # -------------------------------------------------------------- workloads --
@@ -452,9 +459,14 @@ def main():
     ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "seq", "gemm", "kv", "attn"), default=None,
                     help="run one kernel case a few times and exit (for profiler captures)")
     ap.add_argument("--case-launches", type=int, default=16)
+    ap.add_argument("--probe", choices=("bulk", "rates"), default=None,
+                    help="print a hardware probe's numbers and exit: bulk-copy read rate by copy size, or the "
+                         "tensor-op and dp4a rates")
     args = ap.parse_args()
     if args.kernel_case:
         return kernel_case(args.kernel_case, args.case_launches)
+    if args.probe:
+        return hardware_probe(args.probe)
     if args.warmup < 3:
         args.warmup = 3
 
@@ -892,6 +904,37 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, a
     return out
 
 
+def hardware_probe(name):
+    """Probe numbers behind design choices (libbq_probe.so), one JSON line."""
+    import torch
+    from block_quantized_weight_row_gb300 import build as bbuild
+    torch.cuda.set_device(0)
+    torch.zeros(1, device="cuda")
+    P = ctypes.CDLL(bbuild.PROBE_LIB)
+    dbl = ctypes.POINTER(ctypes.c_double)
+    out = {"probe": name}
+    if name == "bulk":
+        P.bq_probe_bulk_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_size_t, dbl]
+        rates = {}
+        for sz in (4096, 8192, 12288, 16384, 24576, 32768, 49152, 98304):
+            for depth in (1, 2, 4, 8):
+                if sz * depth > 200 * 1024:
+                    continue
+                v = ctypes.c_double()
+                rc = P.bq_probe_bulk_rate(sz, depth, 4 << 30, ctypes.byref(v))
+                rates[f"{sz}x{depth}"] = round(v.value, 1) if rc == 0 else f"rc {rc}"
+        out.update({"unit": "GB/s read", "key": "copy bytes x copies in flight per SM", "rates": rates})
+    else:
+        P.bq_probe_int_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dbl]
+        P.bq_probe_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dbl]
+        for kind, key, f in ((2, "dp4a_tera_lane_ops", P.bq_probe_int_rate), (3, "imad_tera_lane_ops", P.bq_probe_int_rate),
+                             (0, "mma_sync_s8_tops", P.bq_probe_mma_rate), (1, "mma_sync_f16_tflops", P.bq_probe_mma_rate)):
+            v = ctypes.c_double()
+            rc = f(kind, 16384 if kind < 2 else 20000, 4, ctypes.byref(v))
+            out[key] = round(v.value, 2) if rc == 0 else f"rc {rc}"
+    print(json.dumps(out))
+
+
 def kernel_case(name, launches):
     """A small, self-contained case of one kernel for profiler captures:
     inputs larger than L2 (rotated over distinct buffers) but well under a
@@ -916,7 +959,7 @@ def kernel_case(name, launches):
         # the first 4 layers of the 7B step (455 MB of weights: beyond L2) in
         # one bq_gemv_sequence launch, on two copies of the weights in turn
         plan = [e for e in inputs.decode_plan("7b-decode") if e.layer < 4]
-        steps = []
+        steps, keep = [], []  # keep: the tensors the argument arrays point to
         for c in range(2):
             groups, cur = [], None
             for e in plan:
@@ -926,6 +969,7 @@ def kernel_case(name, launches):
                 cur[0].append(bq.quantize_rows(bq.Q4_0, inputs.weight(e.M, e.K, e.w_seed + 7 * c, device=dev)))
                 cur[2].append(e.M)
                 cur[4].append(torch.empty(e.M, device=dev))
+            keep.append(groups)
             steps.append(binding.gemv_sequence_args([g[:5] for g in groups]))
         for i in range(launches):
             binding.gemv_sequence_call(bq.Q4_0, steps[i % 2], dev)

@@ -66,7 +66,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     probe_src = os.path.join(CSRC, PROBE_SRC)
     probe_tmp = PROBE_LIB + f".tmp{os.getpid()}"
-    build_probe = force or _stale(PROBE_LIB, [probe_src, __file__])
+    build_probe = force or _stale(PROBE_LIB, [probe_src, __file__] + deps)
     if build_probe:
         jobs.append([cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-shared", probe_src, "-o", probe_tmp])
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + 1) as ex:

@@ -188,10 +188,17 @@ __device__ __forceinline__ void seq_abort(const SeqArgs &a, volatile int *cta_ab
 // on this CTA's roles alone, which all end; the grid-wide flag is read where a
 // CTA waits for other CTAs.
 __device__ __forceinline__ bool seq_wait(const SeqArgs &a, uint64_t *bar, uint32_t parity, volatile int *cta_abort) {
-  for (uint32_t i = 0; i < a.spin_limit; ++i) {
-    if (mbar_test_wait(bar, parity)) return true;
-    __nanosleep(a.poll_ns);
-    if ((i & 63) == 63 && *cta_abort) return false;
+  if (a.poll_ns == 0) {  // suspend in the barrier unit between polls
+    for (uint32_t i = 0; i < a.spin_limit; ++i) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((i & 15) == 15 && *cta_abort) return false;
+    }
+  } else {
+    for (uint32_t i = 0; i < a.spin_limit; ++i) {
+      if (mbar_test_wait(bar, parity)) return true;
+      __nanosleep(a.poll_ns);
+      if ((i & 63) == 63 && *cta_abort) return false;
+    }
   }
   seq_abort(a, cta_abort);
   return false;
@@ -614,7 +621,7 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   a->err = di->err_word;
   a->spin_limit = spin_limit();
   static const int forced_poll = tuning_value("BQ_GEMV_SEQ_POLL_NS");  // read once per process
-  a->poll_ns = forced_poll > 0 ? uint32_t(forced_poll) : 32u;
+  a->poll_ns = forced_poll > 0 ? uint32_t(forced_poll) : 0u;  // 0: suspend in the barrier unit
   int nm = 0;
   for (int i = 0; i < n; ++i) {
     const int gi = groups[i];

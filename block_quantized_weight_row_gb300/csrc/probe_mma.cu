@@ -1,8 +1,10 @@
-// probe_mma.cu — measurement probe (libbq_probe.so, not part of the libbq
+// probe_mma.cu — measurement probes (libbq_probe.so, not part of the libbq
 // ABI): the issue rate of the legacy warp-level tensor-core instructions on
-// this GPU, the denominator the prefill GEMM's int8 target is stated against.
-// sm_103a has no int8 form of tcgen05.mma, so the int8 tensor path left is
-// mma.sync with s8 operands; its f16 form is measured beside it.
+// this GPU, the denominator the prefill GEMM's int8 target is stated against
+// (sm_103a has no int8 form of tcgen05.mma, so the int8 tensor path left is
+// mma.sync with s8 operands; its f16 form is measured beside it); the issue
+// rate of dp4a; and the read rate of 1-D bulk copies by copy size, which
+// sets the GEMV's stage size.
 //
 // Every warp issues long runs of independent mma.sync instructions on
 // register operands (no memory traffic); the accumulators are summed and
@@ -10,6 +12,8 @@
 // on the legacy default stream.
 #include <cstdint>
 #include <cuda_runtime.h>
+
+#include "bq_device.cuh"
 
 namespace {
 
@@ -83,7 +87,87 @@ __global__ void __launch_bounds__(256) k_dp4a(int iters, int kind, int *out) {
   out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// One CTA per SM, one thread streams the CTA's contiguous range of `src`
+// with 1-D bulk copies of `sz` bytes into a ring of `depth` shared-memory
+// slots (one mbarrier each), issuing a slot's next copy as soon as its
+// previous one landed. Waits are bounded; `err` gets 1 if one ran out.
+__global__ void __launch_bounds__(32, 1) k_bulk_stream(const uint8_t *src, size_t per_cta, int sz, int depth,
+                                                      unsigned *err) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + size_t(depth) * sz);
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < depth; ++s) bq::mbar_init(&bar[s], 1);
+  bq::fence_mbar_init();
+  const uint8_t *base = src + per_cta * blockIdx.x;
+  const int64_t n = int64_t(per_cta / sz);
+  const uint64_t pol = bq::l2_evict_first_policy();
+  int64_t issued = 0;
+  for (int64_t j = 0; j < n; ++j) {
+    const int s = int(j % depth);
+    if (j >= depth && !bq::mbar_wait_bounded(&bar[s], uint32_t(((j / depth) - 1) & 1), 1u << 24)) {
+      atomicOr(err, 1u);
+      break;
+    }
+    bq::mbar_arrive_expect_tx(&bar[s], uint32_t(sz));
+    bq::bulk_g2s_hint(sm + size_t(s) * sz, base + j * sz, uint32_t(sz), &bar[s], pol);
+    issued = j + 1;
+  }
+  for (int s = 0; s < depth && s < issued; ++s) {
+    const int64_t last = s + depth * ((issued - 1 - s) / depth);
+    if (!bq::mbar_wait_bounded(&bar[s], uint32_t((last / depth) & 1), 1u << 24)) atomicOr(err, 1u);
+  }
+}
+
 }  // namespace
+
+// Read rate (GB/s) of 1-D bulk copies of `copy_bytes` (a multiple of 16,
+// depth * copy_bytes <= 200 KB) over `total_bytes` of device memory
+// allocated here, one CTA per SM and `depth` copies in flight per SM; best of
+// three runs. Returns 0, -1 on a bad argument, -5 when a CUDA call fails or a
+// wait ran out.
+extern "C" int bq_probe_bulk_rate(int copy_bytes, int depth, size_t total_bytes, double *gbs) {
+  if (copy_bytes < 16 || copy_bytes % 16 || depth < 1 || size_t(depth) * copy_bytes > (200u << 10) || !gbs)
+    return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -5;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -5;
+  const size_t per_cta = total_bytes / size_t(sms) / size_t(copy_bytes) * size_t(copy_bytes);
+  if (per_cta == 0) return -1;
+  uint8_t *buf = nullptr;
+  unsigned *err = nullptr;
+  if (cudaMalloc(&buf, per_cta * sms) != cudaSuccess) return -5;
+  if (cudaMalloc(&err, sizeof(unsigned)) != cudaSuccess) {
+    cudaFree(buf);
+    return -5;
+  }
+  cudaMemset(buf, 1, per_cta * sms);
+  cudaMemset(err, 0, sizeof(unsigned));
+  const int smem = depth * copy_bytes + 8 * depth;
+  cudaError_t e = cudaFuncSetAttribute(k_bulk_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  float best = 0.0f;
+  for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) {
+    cudaEventRecord(e0);
+    k_bulk_stream<<<sms, 32, smem>>>(buf, per_cta, copy_bytes, depth, err);
+    cudaEventRecord(e1);
+    e = cudaEventSynchronize(e1);
+    float ms = 0.0f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess && (best == 0.0f || ms < best)) best = ms;
+  }
+  unsigned herr = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&herr, err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  cudaFree(buf);
+  cudaFree(err);
+  if (e != cudaSuccess || herr || best <= 0.0f) return -5;
+  *gbs = double(per_cta) * sms / (double(best) * 1e-3) / 1e9;
+  return 0;
+}
 
 // Thread-instruction rate (tera-instructions per second) of kind 2 = dp4a,
 // kind 3 = 32-bit integer multiply-add, each as independent chains.

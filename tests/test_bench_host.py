@@ -74,7 +74,11 @@ def test_clock_summary_keeps_the_timed_window():
     assert s["sm_max_mhz"] == 2070
     assert s["reasons"] == ["sw_power_cap"]
     assert s["power_w_max"] == 1300.0
-    c.t0, c.t1 = 30.0, 31.0
+    # a region between two samples: the samples just before and after it
+    c.t0, c.t1 = 10.6, 10.9
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 1750 and "before and after" in s["window"]
+    c.rows = []
     assert c.summary()["samples"] == 0
 
 
