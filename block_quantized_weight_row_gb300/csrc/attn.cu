@@ -423,6 +423,7 @@ struct AttnWArgs {
   int k_rot;         // K cache Hadamard-rotated: rotate q alike
   unsigned *err;
   uint32_t spin_limit;
+  uint32_t poll_ns;  // 0: stage waits may suspend in the barrier unit; else poll, sleeping poll_ns between polls
 };
 
 // CPL codes of one V block from channel o (o % CPL == 0), as CPL/2 exact fp32
@@ -466,14 +467,22 @@ __device__ __forceinline__ void v_pairs(const uint8_t *vb, int o, uint64_t (&v)[
   for (int k = 0; k < CPL / 2; ++k) v[k] = fadd2(pack2(bits[2 * k], bits[2 * k + 1]), b2);
 }
 
-template <int KT, int VT, int G>
+// NBT > 0: the head size (NBT blocks of 32) and the warp tile (kFixedTW
+// tokens) are compile-time constants, so that the lane roles, the butterflies
+// and the tile loops unroll; NBT = 0 takes them from the arguments.
+constexpr int kFixedTW = 16;
+
+constexpr int pow2_at_least(int n) { return n <= 1 ? 1 : 2 * pow2_at_least((n + 1) / 2); }
+
+template <int KT, int VT, int G, int NBT>
 __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWArgs a) {
   constexpr int CPL = 32 / G;  // channels per lane in the value step
   constexpr int NP = CPL / 2;
   constexpr int BBk = Fmt<KT>::kBytes, BBv = Fmt<VT>::kBytes;
+  constexpr bool kFix = NBT > 0;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nb = a.nb, H = a.n_heads, n_kv = a.n_kv, D = a.D;
+  const int nb = kFix ? NBT : a.nb, H = a.n_heads, n_kv = a.n_kv, D = kFix ? NBT * kQK : a.D;
   // ring | q records [H][nb][12] | scores [8 warps][32][G] | (m, l) [8][G][2] |
   // control words (abort flag, tiles issued, release count per stage) | barriers
   uint8_t *ring = smem;
@@ -574,7 +583,7 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
 
   const int j = warp % n_kv, ws = warp / n_kv;
   // score step: lane = (token tt1, block b1)
-  const int LB = a.lb, b1 = lane % LB, tt1 = lane / LB, tpp1 = 32 / LB;
+  const int LB = kFix ? pow2_at_least(NBT) : a.lb, b1 = lane % LB, tt1 = lane / LB, tpp1 = 32 / LB;
   const bool b1ok = b1 < nb;
   // the lane's q records (block b1 of its G heads): in registers for G <= 4,
   // else read from shared memory where they are used
@@ -617,14 +626,28 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
     const int st = i % NS;
     // the decision to go on is the same for every lane of the warp (the
     // shuffles below need all 32 lanes)
-    bool ok = false;
-    for (uint32_t k = 0; k < a.spin_limit; ++k) {
-      if (mbar_test_wait(&full[st], uint32_t((i / NS) & 1))) {
-        ok = true;
-        break;
+    const uint32_t par = uint32_t((i / NS) & 1);
+    // a tile that has already landed answers the non-blocking test at once
+    // (a limit of 0 polls gives up without looking)
+    bool ok = a.spin_limit > 0 && mbar_test_wait(&full[st], par);
+    if (ok) {
+    } else if (a.poll_ns == 0) {
+      for (uint32_t k = 0; k < a.spin_limit; ++k) {
+        if (mbar_try_wait(&full[st], par)) {
+          ok = true;
+          break;
+        }
+        if ((k & 15) == 15 && *abort_flag) break;
       }
-      if ((k & 63) == 63 && *abort_flag) break;
-      __nanosleep(k < 64 ? 20 : 200);
+    } else {
+      for (uint32_t k = 0; k < a.spin_limit; ++k) {
+        if (mbar_test_wait(&full[st], par)) {
+          ok = true;
+          break;
+        }
+        if ((k & 63) == 63 && *abort_flag) break;
+        __nanosleep(k < 64 ? 20 : a.poll_ns);
+      }
     }
     if (!__all_sync(kFull, ok)) {
       if (lane == 0) {
@@ -640,7 +663,8 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
       // ---- scores s = scale * sum_b dk * dq * sumi ----
       const uint8_t *krow = Ks + size_t(w0 + tt1) * a.k_tok + kb_off;  // the lane's block of its token
       const size_t kstep = size_t(tpp1) * a.k_tok;
-      for (int tb = 0; tb < wn; tb += tpp1, krow += kstep) {
+#pragma unroll
+      for (int tb = 0; tb < (kFix ? kFixedTW : wn); tb += tpp1, krow += kstep) {
         const int t = tb + tt1;
         float part[G];
 #pragma unroll
@@ -716,8 +740,9 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
         const uint8_t *vb = Vs + size_t(w0 + tt2) * a.v_tok + vb_off;  // the lane's block of its token
         const size_t vstep = size_t(tpp2) * a.v_tok;
         const float *pw = Pw + tt2 * G;
-#pragma unroll 2
-        for (int t = tt2; t < wn; t += tpp2, vb += vstep, pw += tpp2 * G) {
+#pragma unroll
+        for (int tb = 0; tb < (kFix ? kFixedTW : wn); tb += tpp2, vb += vstep, pw += tpp2 * G) {
+          if (tb + tt2 >= wn) break;  // tokens past the tile's end (the chunk's last tile)
           const float dv = half_bits_to_float(*reinterpret_cast<const uint16_t *>(vb));
           uint64_t vals[NP];
           v_pairs<VT, CPL>(vb, o2, vals);
@@ -958,16 +983,23 @@ AttnWPlan attn_wplan(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t
   return p;
 }
 
-template <int KT, int VT>
-cudaError_t launch_attn_warp(int G, const AttnWArgs &a, int chunks, size_t smem, cudaStream_t stream) {
-  const void *fn = nullptr;
+template <int KT, int VT, int NBT>
+const void *attn_warp_fn(int G) {
   switch (G) {
-    case 1: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 1>); break;
-    case 2: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 2>); break;
-    case 4: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 4>); break;
-    case 8: fn = reinterpret_cast<const void *>(k_attn_warp<KT, VT, 8>); break;
-    default: return cudaErrorInvalidValue;
+    case 1: return reinterpret_cast<const void *>(k_attn_warp<KT, VT, 1, NBT>);
+    case 2: return reinterpret_cast<const void *>(k_attn_warp<KT, VT, 2, NBT>);
+    case 4: return reinterpret_cast<const void *>(k_attn_warp<KT, VT, 4, NBT>);
+    case 8: return reinterpret_cast<const void *>(k_attn_warp<KT, VT, 8, NBT>);
+    default: return nullptr;
   }
+}
+
+// head_dim 128 with full 16-token warp tiles (the common decode shapes) takes
+// the compile-time-shaped kernel
+template <int KT, int VT>
+cudaError_t launch_attn_warp(int G, bool fixed128, const AttnWArgs &a, int chunks, size_t smem, cudaStream_t stream) {
+  const void *fn = fixed128 ? attn_warp_fn<KT, VT, 4>(G) : attn_warp_fn<KT, VT, 0>(G);
+  if (!fn) return cudaErrorInvalidValue;
   cudaError_t e = ensure_smem(fn, int(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -980,12 +1012,8 @@ cudaError_t launch_attn_warp(int G, const AttnWArgs &a, int chunks, size_t smem,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  switch (G) {
-    case 1: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 1>, a);
-    case 2: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 2>, a);
-    case 4: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 4>, a);
-    default: return cudaLaunchKernelEx(&cfg, k_attn_warp<KT, VT, 8>, a);
-  }
+  void *args[] = {const_cast<AttnWArgs *>(&a)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 template <int KT, int VT>
@@ -1065,12 +1093,16 @@ cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K,
     a.k_rot = k_rot ? 1 : 0;
     a.err = di->err_word;
     a.spin_limit = spin_limit();
+    static const int forced_poll = tuning_value("BQ_ATTN_POLL_NS");  // read once per process
+    a.poll_ns = forced_poll > 0 ? uint32_t(forced_poll) : 0u;
+    static const int no_fixed = tuning_value("BQ_ATTN_GENERIC");
+    const bool fixed128 = D == 4 * kQK && w.tw == kFixedTW && no_fixed <= 0;
     if (kt == kTypeQ4_0)
-      e = vt == kTypeQ4_0 ? launch_attn_warp<kTypeQ4_0, kTypeQ4_0>(G, a, chunks, w.smem, stream)
-                          : launch_attn_warp<kTypeQ4_0, kTypeQ8_0>(G, a, chunks, w.smem, stream);
+      e = vt == kTypeQ4_0 ? launch_attn_warp<kTypeQ4_0, kTypeQ4_0>(G, fixed128, a, chunks, w.smem, stream)
+                          : launch_attn_warp<kTypeQ4_0, kTypeQ8_0>(G, fixed128, a, chunks, w.smem, stream);
     else
-      e = vt == kTypeQ4_0 ? launch_attn_warp<kTypeQ8_0, kTypeQ4_0>(G, a, chunks, w.smem, stream)
-                          : launch_attn_warp<kTypeQ8_0, kTypeQ8_0>(G, a, chunks, w.smem, stream);
+      e = vt == kTypeQ4_0 ? launch_attn_warp<kTypeQ8_0, kTypeQ4_0>(G, fixed128, a, chunks, w.smem, stream)
+                          : launch_attn_warp<kTypeQ8_0, kTypeQ8_0>(G, fixed128, a, chunks, w.smem, stream);
   } else {
     const AttnPlan p = attn_plan(kt, vt, T, H, n_kv, D);
     AttnArgs a{};

@@ -180,14 +180,18 @@ __device__ __forceinline__ void seq_abort(const SeqArgs &a, volatile int *cta_ab
 }
 
 // Bounded wait on one of this CTA's mbarriers that also gives up once
-// another role of the CTA gave up. Polls never suspend in the barrier unit
-// (whose wake-up comes long after the phase completes: with a handoff per
-// stage that latency, not the work, set the pace); between polls the warp
-// sleeps briefly so that waiting warps leave the issue slots to working ones.
+// another role of the CTA gave up. By default each poll may suspend the
+// thread in the barrier unit until the phase completes (a waiting warp then
+// issues almost nothing); with poll_ns set, polls never suspend and the warp
+// sleeps poll_ns between them.
 // Only the CTA's own flag (shared memory) is read here: these barriers depend
 // on this CTA's roles alone, which all end; the grid-wide flag is read where a
 // CTA waits for other CTAs.
 __device__ __forceinline__ bool seq_wait(const SeqArgs &a, uint64_t *bar, uint32_t parity, volatile int *cta_abort) {
+  // a phase that has already completed: the non-blocking test answers at
+  // once (a suspending wait takes a few hundred cycles even then); a limit
+  // of 0 polls gives up without looking
+  if (a.spin_limit > 0 && mbar_test_wait(bar, parity)) return true;
   if (a.poll_ns == 0) {  // suspend in the barrier unit between polls
     for (uint32_t i = 0; i < a.spin_limit; ++i) {
       if (mbar_try_wait(bar, parity)) return true;
