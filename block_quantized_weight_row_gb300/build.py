@@ -20,7 +20,8 @@ PROBE_SRC = "probe_mma.cu"
 PROBE_LIB = os.path.join(HERE, "libbq_probe.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["bq_api.cu", "quantize.cu", "gemv.cu", "gemv_seq.cu", "gemm.cu", "gemm_tc.cu", "gemm_noalloc.cu", "attn.cu"]
+SOURCES = ["bq_api.cu", "quantize.cu", "gemv.cu", "gemv_seq.cu", "gemm.cu", "gemm_tc.cu", "gemm_noalloc.cu", "attn.cu",
+           "attn_fixed_q4k.cu", "attn_fixed_q8k.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]

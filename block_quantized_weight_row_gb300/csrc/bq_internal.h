@@ -76,6 +76,11 @@ cudaError_t launch_gemv_seq(int type, int n_groups, const int *n_mats, const uin
 // attn_workspace_bytes(...) bytes of partial results.
 size_t attn_workspace_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D);
 size_t attn_smem_bytes(int kt, int vt, int64_t T, int64_t H, int64_t n_kv, int64_t D);
+// The compile-time-shaped decode-attention warp kernel (head_dim 128) for a
+// Q4_0 / Q8_0 K cache, V type vt, G query heads per kv head and n_kv kv heads;
+// nullptr where none is built.
+const void *attn_warp_fixed_fn_q4k(int vt, int G, int n_kv);
+const void *attn_warp_fixed_fn_q8k(int vt, int G, int n_kv);
 cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K, const uint8_t *V, float *o,
                                int64_t T, int64_t H, int64_t n_kv, int64_t D, float scale, void *ws,
                                cudaStream_t stream, bool k_rot = false);
