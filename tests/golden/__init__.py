@@ -34,3 +34,22 @@ def sizes():
             k, v, _src = (p.strip() for p in line.split("|"))
             out[k] = float(v)
     return out
+
+
+def kquant_worked():
+    """-> list of (name, type_name, {index: value}, {field: value or list})."""
+    cases = []
+    with open(os.path.join(HERE, "kquant_worked.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, t, inputs, fields = (p.strip() for p in line.split("|"))
+            vals = {int(k): float(v) for k, v in (kv.split("=") for kv in inputs.split(","))}
+            exp = {}
+            for kv in fields.split(";"):
+                k, v = kv.split("=")
+                nums = [float(x) for x in v.split(",")]
+                exp[k] = nums if len(nums) > 1 else nums[0]
+            cases.append((name, t, vals, exp))
+    return cases

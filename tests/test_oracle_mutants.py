@@ -50,6 +50,19 @@ MUTANTS = [
      "dst[i] = (d * (float)(int8_t)blk[192 + i / 16]) * (float)(u[i] - 31);"),
     ("q6k_high_bits_order", "int hi = (blk[128 + (i & 63)] >> (2 * (i >> 6))) & 3;",
      "int hi = (blk[128 + (i >> 2)] >> (2 * (i & 3))) & 3;"),
+    ("q4k_superscale_64", "smax / 63.0f", "smax / 64.0f"),
+    ("q4k_supermin_64", "mmax / 63.0f", "mmax / 64.0f"),
+    ("q4k_min_unclamped", "m[j] = lo < 0.0f ? -lo : 0.0f;", "m[j] = -lo;"),
+    ("q4k_range_16", "s[j] = (hi + m[j]) / 15.0f;", "s[j] = (hi + m[j]) / 16.0f;"),
+    ("q4k_code_clamp_14", "clampi((int)oracle_round_half_even((x[32 * j + i] + M) / S), 0, 15)",
+     "clampi((int)oracle_round_half_even((x[32 * j + i] + M) / S), 0, 14)"),
+    ("q4k_codes_from_unrounded_factors", "float S = d * (float)sc[j], M = dm * (float)mn[j];", "float S = s[j], M = m[j];"),
+    ("q6k_sub_32", "s[k] = amax / 31.0f;", "s[k] = amax / 32.0f;"),
+    ("q6k_super_128", "uint16_t d16 = oracle_f32_to_f16(smax / 127.0f);",
+     "uint16_t d16 = oracle_f32_to_f16(smax / 128.0f);"),
+    ("q6k_clamp_31", "clampi((int)oracle_round_half_even(x[16 * k + i] / S), -32, 31)) + 32",
+     "clampi((int)oracle_round_half_even(x[16 * k + i] / S), -31, 31)) + 32"),
+    ("q6k_codes_from_unrounded_factor", "float S = d * (float)sc;", "float S = s[k];"),
     ("kquant_gemv_min_term_dropped", "double t1 = dx * (double)S[j] * (double)su, t2 = -dx * (double)M[j] * (double)sx;",
      "double t1 = dx * (double)S[j] * (double)su, t2 = 0.0 * (double)M[j] * (double)sx;"),
     ("kquant_row_stride", "int64_t nb = K / QK, row_bytes = K / bv * bw;\n    uint8_t *xq = (uint8_t *)malloc((size_t)(nb * oracle_block_bytes(ORACLE_TYPE_Q8_0)) + 1);",

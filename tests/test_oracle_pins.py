@@ -787,6 +787,62 @@ def test_kquant_values_from_an_independent_parse(orc, t):
     assert np.array_equal(deq.view(np.uint32), ref.astype(np.float32).view(np.uint32))
 
 
+@pytest.mark.parametrize("case", golden.kquant_worked(), ids=lambda c: c[0])
+def test_kquant_hand_worked_factors(orc, case):
+    """Super-scales and sub-block factors of hand-worked super-blocks
+    (tests/golden/kquant_worked.txt): the super-scale maps the largest
+    sub-block factor to the top of its 6-bit (Q4_K) or signed 8-bit (Q6_K)
+    range, every other factor rounds half to even, and a code below the
+    range's floor clamps to it."""
+    name, tname, vals, exp = case
+    t = {"Q4_K": Q4_K, "Q6_K": Q6_K}[tname]
+    x = np.zeros((1, 256), np.float32)
+    for i, v in vals.items():
+        x[0, i] = v
+    q = orc.quantize_rows(t, x)
+    if t == Q4_K:
+        d, dm, sc, mn, u = _parse_q4k(q)
+        assert d[0] == exp["d"] and dm[0] == exp["dmin"]
+        assert sc[0].tolist() == exp["sc"] and mn[0].tolist() == exp["mn"]
+    else:
+        d, sc, u = _parse_q6k(q)
+        assert d[0] == exp["d"]
+        if "sc" in exp:
+            assert sc[0].tolist() == exp["sc"]
+        if "sc0" in exp:
+            assert sc[0][0] == exp["sc0"] and sc[0][15] == exp["sc15"]
+            assert u[0][0] == exp["u0"] and u[0][240] == exp["u240"]
+
+
+@pytest.mark.parametrize("t", [Q4_K, Q6_K])
+def test_kquant_codes_are_nearest_under_the_stored_factors(orc, t):
+    """Each code is the nearest one to its value under the factors the
+    super-block stores (d * sc, dmin * mn), as a block quantizer's code is the
+    rounded quotient by the stored scale: the quotient lies within half a step
+    of the code, or beyond the end of the range the code clamps to."""
+    rng = np.random.default_rng(70 + t)
+    x = np.concatenate([rng.normal(size=(30, 256)), rng.standard_t(3, size=(30, 256)) * 3,
+                        rng.uniform(0.2, 4.0, size=(30, 256))]).astype(np.float32)
+    q = orc.quantize_rows(t, x)
+    slop = 1e-5
+    if t == Q4_K:
+        d, dm, sc, mn, u = _parse_q4k(q)
+        S = np.repeat((d[:, None] * sc.astype(np.float32)).astype(np.float32), 32, axis=1).astype(np.float64)
+        M = np.repeat((dm[:, None] * mn.astype(np.float32)).astype(np.float32), 32, axis=1).astype(np.float64)
+        live = S > 0
+        r = np.where(live, (x + M) / np.where(live, S, 1.0), 0.0)
+        c, lo, hi = u.astype(np.float64), 0, 15
+    else:
+        d, sc, u = _parse_q6k(q)
+        S = np.repeat((d[:, None] * sc.astype(np.float32)).astype(np.float32), 16, axis=1).astype(np.float64)
+        live = S != 0
+        r = np.where(live, x / np.where(live, S, 1.0), 0.0)
+        c, lo, hi = (u - 32).astype(np.float64), -32, 31
+    inner = (c > lo) & (c < hi)
+    assert np.all(np.abs(r - c)[inner] <= 0.5 + slop)
+    assert np.all(r[c == lo] <= lo + 0.5 + slop) and np.all(r[c == hi] >= hi - 0.5 - slop)
+
+
 @pytest.mark.parametrize("t", [Q4_K, Q6_K])
 def test_kquant_round_trip_bound(orc, t):
     """Half a sub-block step, plus what quantizing the sub-block factors to
