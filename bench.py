@@ -882,6 +882,35 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, a
                                 "l2": "8 distinct matrices per type, 203-370 MB: beyond L2"}
     torch.cuda.empty_cache()
 
+    # shapes whose rows are not whole multiples of 16 bytes: Q6_K down-projection
+    # rows (K = 11008: bulk copies of whole 8-row quanta) and Q4_0 / Q8_0 with
+    # K = 4128, not a multiple of 256 (the generic kernel, x quantized once
+    # into the workspace)
+    gen = {}
+    for name, t, M_, K_ in (("Q6_K_4096x11008", bq.Q6_K, 4096, 11008), ("Q4_0_11008x4128", bq.Q4_0, 11008, 4128),
+                            ("Q8_0_11008x4128", bq.Q8_0, 11008, 4128)):
+        x_ = inputs.activation(K_, inputs.seed_of("generic-gemv", 0, 0), device=dev)
+        y_ = torch.empty(M_, dtype=torch.float32, device=dev)
+        mats = [bq.quantize_rows(t, inputs.weight(M_, K_, inputs.seed_of("generic-gemv", 1, i), device=dev))
+                for i in range(8)]
+
+        def gen_step():
+            for w in mats:
+                bq.gemv(t, w, x_, M_, K_, out=y_)
+        gg = capture(gen_step, stream)
+        msg = max_over_ranks(time_graph(gg, stream, 20, 3), dist)
+        byts = 8 * mats[0].numel()
+        gen[name] = {"GB/s": round(aggregate_rate(byts, world, msg * 1e-3) / 1e9, 1),
+                     "us_per_launch": round(msg * 1e3 / 8, 2),
+                     "hbm_frac_of_measured": round(byts / (msg * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        del mats, gg
+    out["gemv_unaligned_rows"] = {"metric": "decode GEMV GB/s of weights, rows not multiples of 16 bytes (back to back)",
+                                "value": gen["Q6_K_4096x11008"]["GB/s"], "unit": "GB/s", "per_shape": gen,
+                                "kernel": "Q6_K: k_gemv_tma in 8-row quanta (+ k_gemv_prep); K % 256 != 0: "
+                                          "k_gemv_generic_prep + k_gemv_generic",
+                                "l2": "8 distinct matrices per shape, 232-384 MB: beyond L2"}
+    torch.cuda.empty_cache()
+
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps
     q = build_decode_step("qwen3-0.6b-decode", dev, bq, inputs)
     qargs = binding.gemv_sequence_args(seq_groups(q))

@@ -30,6 +30,7 @@
 //   - Rows with K % 256 != 0 (row bytes not a multiple of 16) take a plain
 //     warp-per-row kernel with 2-byte loads.
 #include <algorithm>
+#include <numeric>
 
 #include "bq_device.cuh"
 #include "bq_internal.h"
@@ -68,6 +69,7 @@ struct GemvArgs {
   int stage_rows;      // at most this many rows per stage (one bulk copy)
   int stages;
   int stage_bytes;     // stage_rows * row_bytes
+  int row_quantum;     // rows whose bytes are a multiple of 16: CTA ranges and stages are multiples of it
   int xrec_bytes;      // groups * kXRecBytes rounded up to 128
   const uint32_t *rec;  // x's records written by k_gemv_prep, or null: quantize x here
   unsigned *err;
@@ -96,9 +98,11 @@ __global__ void __launch_bounds__(kGemvThreads, 2) k_gemv_tma(const GemvArgs a) 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // contiguous, balanced row range of this CTA, streamed in stages
-  const int r0 = int(int64_t(a.M) * blockIdx.x / gridDim.x);
-  const int r1 = int(int64_t(a.M) * (blockIdx.x + 1) / gridDim.x);
+  // contiguous, balanced row range of this CTA (in whole row quanta, so that
+  // every bulk copy starts on a 16-byte boundary), streamed in stages
+  const int nq = a.M / a.row_quantum;
+  const int r0 = int(int64_t(nq) * blockIdx.x / gridDim.x) * a.row_quantum;
+  const int r1 = int(int64_t(nq) * (blockIdx.x + 1) / gridDim.x) * a.row_quantum;
   const int S = a.stages;
 
   if (threadIdx.x == 0) {
@@ -271,26 +275,42 @@ __global__ void __launch_bounds__(kPrepThreads) k_gemv_prep(const PrepArgs p) {
 
 // ------------------------------------------------------ generic fallback --
 
+// x quantized to Q8_0 once, for the generic kernel: words [8b + i], the
+// scale (fp32) at [8nb + b], the code sum at [9nb + b]. One lane per block.
+__device__ __forceinline__ void quantize_x_generic(const float *__restrict__ x, uint32_t *xs, int nb, int b) {
+  float v[32];
+  load_block<false>(x + b * kQK, v);
+  uint16_t scale;
+  uint32_t w[8];
+  int sum;
+  quantize_block_lane<kTypeQ8_0, true>(v, scale, w, sum);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) xs[8 * b + i] = w[i];
+  xs[8 * nb + b] = __float_as_uint(half_bits_to_float(scale));
+  xs[9 * nb + b] = uint32_t(sum);
+}
+
+__global__ void __launch_bounds__(256) k_gemv_generic_prep(const float *__restrict__ x, uint32_t *__restrict__ xg,
+                                                           int nb) {
+  const int b = int(blockIdx.x) * 256 + int(threadIdx.x);
+  if (b < nb) quantize_x_generic(x, xg, nb, b);
+}
+
 // Any K % 32 == 0: warp per row, lane per block, 2-byte loads. x's codes are
-// stored unpadded: word [8b + i], scales at [8nb + b], sums at [9nb + b].
+// stored unpadded (as quantize_x_generic writes them), in shared memory:
+// quantized by the CTA itself, or copied from xg where a prep launch wrote
+// them once for the whole grid.
 template <int TYPE>
 __global__ void __launch_bounds__(256)
-    k_gemv_generic(const uint8_t *__restrict__ W, const float *__restrict__ x,
+    k_gemv_generic(const uint8_t *__restrict__ W, const float *__restrict__ x, const uint32_t *__restrict__ xg,
                    float *__restrict__ y, int M, int K) {
   constexpr int BB = Fmt<TYPE>::kBytes;
   extern __shared__ __align__(16) uint32_t xs[];
   const int nb = K / kQK;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-    float v[32];
-    load_block<false>(x + b * kQK, v);
-    uint16_t scale;
-    uint32_t w[8];
-    int sum;
-    quantize_block_lane<kTypeQ8_0, true>(v, scale, w, sum);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xs[8 * b + i] = w[i];
-    xs[8 * nb + b] = __float_as_uint(half_bits_to_float(scale));
-    xs[9 * nb + b] = uint32_t(sum);
+  if (xg) {
+    for (int i = threadIdx.x; i < 10 * nb; i += blockDim.x) xs[i] = __ldg(xg + i);
+  } else {
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) quantize_x_generic(x, xs, nb, b);
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -396,8 +416,15 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
   for (int i = 0; i < n; ++i) M_total += M[i];
   if (M_total == 0) return cudaSuccess;
 
-  // Q6_K's 210-byte super-blocks keep rows 16-byte aligned only for K % 2048 == 0
-  if (K % 256 == 0 && (TYPE != kTypeQ6_K || K % 2048 == 0)) {
+  // Bulk copies need 16-byte aligned offsets and sizes: rows of every type are
+  // whole multiples of 16 bytes for K % 256 == 0 except Q6_K's (210-byte
+  // super-blocks, read 2-byte aligned by the consumers), whose stages then
+  // hold whole quanta of rows (16 / gcd(row bytes, 16) rows), which every
+  // matrix of the call must divide into.
+  const int quantum = 16 / std::gcd(row_bytes, 16);
+  bool quanta_ok = true;
+  for (int i = 0; i < n; ++i) quanta_ok = quanta_ok && M[i] % quantum == 0;
+  if (K % 256 == 0 && (quantum == 1 || (TYPE == kTypeQ6_K && quanta_ok))) {
     GemvArgs a{};
     int acc_rows = 0;
     a.n_mats = 0;
@@ -416,6 +443,7 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
     a.lanes_per_row = min(32, next_pow2(a.groups));
     a.rows_per_warp = 32 / a.lanes_per_row;
     a.row_bytes = row_bytes;
+    a.row_quantum = quantum;
     a.xrec_bytes = (a.groups * kXRecBytes + 127) / 128 * 128;
     a.err = di->err_word;
     a.spin_limit = spin_limit();
@@ -436,6 +464,7 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
     int stage_rows = forced_rows > 0 ? forced_rows : kConsumerWarps * a.rows_per_warp;
     stage_rows = min(stage_rows, max(1, kMaxStageBytes / row_bytes));
     stage_rows = int(std::min<int64_t>(stage_rows, a.M));
+    stage_rows = std::max(quantum, stage_rows / quantum * quantum);
     a.stage_rows = stage_rows;
     a.stage_bytes = stage_rows * row_bytes;
     const int max_stages = forced_stages > 0 ? forced_stages : 4;
@@ -457,9 +486,9 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
     // of a decode chain, which wait on their predecessor, measured slower).
     if (forced_rows <= 0 && forced_stages <= 0 && ctas_per_sm == 2 && stages == 2 &&
         int64_t(a.M) * row_bytes > kPrefetchMaxBytes) {
-      const int r3 = (half_sm - a.xrec_bytes - 16 * max_stages) / (3 * row_bytes);
-      if (r3 >= 1 && r3 >= stage_rows - 2) {
-        stage_rows = min(stage_rows - 1, r3);
+      const int r3 = (half_sm - a.xrec_bytes - 16 * max_stages) / (3 * row_bytes) / quantum * quantum;
+      if (r3 >= quantum && r3 >= stage_rows - 2 * quantum) {
+        stage_rows = min(stage_rows - quantum, r3);
         a.stage_rows = stage_rows;
         a.stage_bytes = stage_rows * row_bytes;
         stages = 3;
@@ -521,14 +550,21 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
       return cudaLaunchKernelEx(&cfg, k_gemv_tma<TYPE>, a);
     }
   }
-  // any K % 32 == 0 (or rows too long for two stages): one plain launch per matrix
+  // any K % 32 == 0 (or rows too long for two stages): one plain launch per
+  // matrix; with a workspace, x is quantized once by a prep launch
   const size_t smem = size_t(nb) * 40;  // 32 code bytes + scale + sum per block
   cudaError_t e = ensure_smem(reinterpret_cast<const void *>(k_gemv_generic<TYPE>), int(smem));
   if (e != cudaSuccess) return e;
+  const uint32_t *xg = nullptr;
+  if (rec_ws) {
+    k_gemv_generic_prep<<<unsigned((nb + 255) / 256), 256, 0, stream>>>(x, rec_ws, nb);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    xg = rec_ws;
+  }
   for (int i = 0; i < n; ++i) {
     if (M[i] == 0) continue;
     const int64_t grid = std::min((M[i] + 7) / 8, int64_t(di->sm_count) * 4);
-    k_gemv_generic<TYPE><<<unsigned(grid), 256, smem, stream>>>(W[i], x, y[i], int(M[i]), int(K));
+    k_gemv_generic<TYPE><<<unsigned(grid), 256, smem, stream>>>(W[i], x, xg, y[i], int(M[i]), int(K));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -549,8 +585,11 @@ cudaError_t launch_gemv(int type, int n, const uint8_t *const *W, float *const *
 }
 
 size_t gemv_workspace_bytes(int64_t K) {
-  if (K <= 0 || K % 256) return 0;
-  return (size_t(K / 256) * kXRecBytes + 255) / 256 * 256;
+  if (K <= 0 || K % kQK) return 0;
+  // the records of the bulk-copy kernel (K % 256 == 0), which also hold the
+  // generic kernel's 40 bytes per block; else the generic layout alone
+  const size_t bytes = K % 256 == 0 ? size_t(K / 256) * kXRecBytes : size_t(K / kQK) * 40;
+  return (bytes + 255) / 256 * 256;
 }
 
 // ------------------------------------------------------------ block dots --

@@ -311,14 +311,16 @@ int bq_set_workspace(void *dev_ptr, size_t bytes);
 size_t bq_workspace_size(int type, int64_t M, int64_t N, int64_t K);
 
 /* Workspace bytes that let bq_gemv / bq_gemv_multi quantize x once per call
- * (0 when K % 256 != 0, where x is always quantized inside the GEMV kernel).
- * With a workspace of at least this size set by bq_set_workspace, a call
- * launches a small prep kernel, which (with weight prefetch enabled and at
- * most 64 MB of weights in the call) first asks L2 to fetch the call's
- * weights and then writes x's Q8_0 codes, scales and code sums to the
- * workspace, and then the GEMV kernel, which copies them. Without one, every
- * GEMV CTA quantizes x itself. Both give bit-identical results. The
- * workspace must not be in use by another call that may run concurrently. */
+ * (0 when K is not a positive multiple of 32). With a workspace of at least
+ * this size set by bq_set_workspace, a call launches a small prep kernel,
+ * which (on the bulk-copy path, with weight prefetch enabled and at most
+ * 64 MB of weights in the call) first asks L2 to fetch the call's weights and
+ * then writes x's Q8_0 codes, scales and code sums to the workspace, and then
+ * the GEMV kernel, which copies them; shapes off the bulk-copy path (K % 256
+ * != 0, Q6_K with K % 2048 != 0) take a generic kernel that reads the same
+ * codes from the workspace. Without one, every GEMV CTA quantizes x itself.
+ * Both give bit-identical results. The workspace must not be in use by
+ * another call that may run concurrently. */
 size_t bq_gemv_workspace_size(int type, int64_t K);
 
 /* Thread-local message of the last failure (never NULL). */

@@ -81,6 +81,9 @@ def test_legacy_types_where_they_are_not_taken(L):
         assert L.bq_block_dots(t, p(FAKE), p(FAKE), p(FAKE), 1, 32) == UNSUPPORTED
         assert L.bq_gemm(t, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 4, 4, 64) == UNSUPPORTED
         assert L.bq_gemv_workspace_size(t, 4096) == L.bq_gemv_workspace_size(2, 4096) > 0  # x records, as Q4_0
+        # K % 256 != 0 (generic kernel): 32 code bytes, scale and code sum per block of x
+        assert L.bq_gemv_workspace_size(t, 4128) == (129 * 40 + 255) // 256 * 256
+        assert L.bq_gemv_workspace_size(t, 4100) == 0
         assert L.bq_kv_quantize(t, p(FAKE), p(FAKE + (1 << 20)), p(FAKE + (2 << 20)), 2, 2, 64) == UNSUPPORTED  # bias
         assert L.bq_kv_quantize_basis(t, p(FAKE), None, 1, 1, p(FAKE + (2 << 20)), 2, 2, 64) == UNSUPPORTED  # rotation
         assert L.bq_attn_decode(t, 8, p(FAKE), p(FAKE), p(FAKE), p(FAKE + (1 << 24)), 10, 8, 8, 64,

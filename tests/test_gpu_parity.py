@@ -449,7 +449,8 @@ def test_gemv_multi_rejects_bad_batches(bq, dev):
 
 @pytest.mark.parametrize("t", [Q4, Q8])
 @pytest.mark.parametrize("with_ws", [True, False])
-@pytest.mark.parametrize("Ms,K", [([4096, 1024], 4096), ([3, 700], 11008), ([257], 2304)])
+@pytest.mark.parametrize("Ms,K", [([4096, 1024], 4096), ([3, 700], 11008), ([257], 2304),
+                                  ([33, 500], 4128), ([5], 96)])  # K % 256 != 0: the generic kernel
 def test_gemv_both_activation_paths(bq, orc, dev, t, with_ws, Ms, K):
     """x quantized once by the prep kernel into the workspace, or by every
     GEMV CTA: both must match the oracle (and hence each other)."""
@@ -942,7 +943,10 @@ def test_kquant_quantize_and_dequantize_bit_exact(bq, orc, dev, t):
 
 
 @pytest.mark.parametrize("t", KQUANTS)
-@pytest.mark.parametrize("M,K", [(1, 256), (37, 768), (4096, 4096), (11008, 4096), (300, 11008)])
+@pytest.mark.parametrize("M,K", [(1, 256), (37, 768), (4096, 4096), (11008, 4096), (300, 11008),
+                                 # Q6_K rows not a multiple of 16 bytes: bulk copies of whole
+                                 # quanta of 8 (K = 768, 11008) or 4 (K = 2560) rows
+                                 (96, 768), (4096, 11008), (52, 2560)])
 def test_kquant_gemv_matches_oracle(bq, orc, dev, t, M, K):
     rng = np.random.default_rng(M + K + t)
     W = (rng.normal(size=(M, K)) * 0.02).astype(np.float32)
