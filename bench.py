@@ -889,9 +889,9 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, a
     gen = {}
     for name, t, M_, K_ in (("Q6_K_4096x11008", bq.Q6_K, 4096, 11008), ("Q4_0_11008x4128", bq.Q4_0, 11008, 4128),
                             ("Q8_0_11008x4128", bq.Q8_0, 11008, 4128)):
-        x_ = inputs.activation(K_, inputs.seed_of("generic-gemv", 0, 0), device=dev)
+        x_ = inputs.activation(K_, inputs.seed_of("legacy-gemv", 2, 0), device=dev)
         y_ = torch.empty(M_, dtype=torch.float32, device=dev)
-        mats = [bq.quantize_rows(t, inputs.weight(M_, K_, inputs.seed_of("generic-gemv", 1, i), device=dev))
+        mats = [bq.quantize_rows(t, inputs.weight(M_, K_, inputs.seed_of("legacy-gemv", 3, i), device=dev))
                 for i in range(8)]
 
         def gen_step():
