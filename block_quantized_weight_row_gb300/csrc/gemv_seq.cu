@@ -289,7 +289,24 @@ __device__ __forceinline__ void seq_prefetch_x(const SeqArgs &a, const BatchDesc
   }
 }
 
-template <int TYPE>
+// Consumer group cg takes stages j with j mod ngroups == cg: does it take
+// one of the batch's stages here (first stage js.x, js.y stages)?
+__device__ __forceinline__ bool seq_group_owns(const SeqArgs &a, int2 js, int cg) {
+  return js.y >= a.ngroups || ((cg - js.x) & (a.ngroups - 1)) < js.y;
+}
+// Can the consumer groups with no stage of this batch here step over it? Only
+// where its records come from the workspace and no other batch waits for it
+// (else every group takes part: the consumers' own quantization of x and the
+// signal to the grid need them all), and where some group has no stage.
+__device__ __forceinline__ bool seq_batch_skippable(const SeqArgs &a, const BatchDesc &d, int2 js) {
+  return d.rec_off >= 0 && !d.signal && js.y < a.ngroups;
+}
+
+// SKIP: the consumer groups step over the batches in which they own no
+// stage (instantiated for launches of four groups, where a CTA's share of a
+// batch is often a stage or two; with two groups the stage table and the
+// extra branch cost more than they save).
+template <int TYPE, bool SKIP>
 __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constant__ SeqArgs a) {
   constexpr int GW = GroupWords<TYPE>::kWords;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -299,6 +316,7 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
   BatchDesc *bd = reinterpret_cast<BatchDesc *>(ring + size_t(a.stages) * a.slot_bytes);
   MatDesc *md = reinterpret_cast<MatDesc *>(bd + a.n_groups);
   int2 *rr = reinterpret_cast<int2 *>(md + a.n_mats);  // this CTA's rows of batch g
+  int2 *js = rr + a.n_groups;  // this CTA's first stage of batch g and its number of stages
   uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(bd) + a.desc_bytes);
   uint64_t *empty = full + a.stages;
   uint64_t *rfull = empty + a.stages;  // [nrec]: records of buffer b in place
@@ -318,6 +336,41 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
     for (int i = threadIdx.x; i < ng; i += kSqThreads) sg[i] = pg[i];
     for (int i = threadIdx.x; i < nm; i += kSqThreads) sm_[i] = pm[i];
     for (int g = threadIdx.x; g < a.n_groups; g += kSqThreads) rr[g] = cta_rows(a.g[g].rows, g);
+  }
+  if constexpr (SKIP) {
+    __syncthreads();
+    // stages of every batch in this CTA (the walk the producer and the
+    // consumers make), then their first stage indices by a prefix sum over the
+    // batches (warp 0, 32 batches per step)
+    for (int g = threadIdx.x; g < a.n_groups; g += kSqThreads) {
+      const Batch<TYPE> B(bd[g]);
+      int n = 0;
+      if (rr[g].x < rr[g].y) {
+        StageWalk wk{};
+        wk.begin(md, B, rr[g].x, rr[g].y);
+        while (wk.row < wk.r1) {
+          wk.row += wk.next(md);
+          ++n;
+        }
+      }
+      js[g].y = n;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int base = 0;
+      for (int g0 = 0; g0 < a.n_groups; g0 += 32) {
+        const int g = g0 + lane;
+        const int v = g < a.n_groups ? js[g].y : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int t = __shfl_up_sync(kFull, incl, off);
+          if (lane >= off) incl += t;
+        }
+        if (g < a.n_groups) js[g].x = base + incl - v;
+        base += __shfl_sync(kFull, incl, 31);
+      }
+    }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -419,9 +472,12 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
       const int use = k >> a.nrec_log2;
       const bool mine = k % kCopyWarps == xw;
       ++k;
-      if (d.rec_off < 0 || !mine) continue;
-      // the buffer's previous batch is done once its consumers released it
+      if (!mine) continue;
+      // the buffer's previous batch is done once its consumers released it;
+      // waited for also before a batch the consumers fill themselves, so that
+      // this warp is never two phases ahead of the buffer's release barrier
       if (use > 0 && !seq_wait(a, &rempty[b], uint32_t((use - 1) & 1), cta_abort)) break;
+      if (d.rec_off < 0) continue;
       const int n16 = (d.K / 256) * (kXRecBytes / 16);
       const uint4 *src = reinterpret_cast<const uint4 *>(a.rec + d.rec_off);
       uint4 *dst = reinterpret_cast<uint4 *>(smem + size_t(b) * a.xrec_bytes);
@@ -456,6 +512,21 @@ __global__ void __launch_bounds__(kSqThreads, 1) k_gemv_seq(const __grid_constan
       const int r0 = rr[g].x, r1 = rr[g].y;
       if (r0 < r1) {
         const int b = int(uint32_t(k) & rmask);
+        if (SKIP && seq_batch_skippable(a, bd[g], js[g]) && !seq_group_owns(a, js[g], cg)) {
+          // no stage of this batch for this group: step over its stages. The
+          // group still waits for the batch's records and releases the buffer
+          // like every other batch, so that the record copies never run more
+          // than one use of a buffer ahead of any group (a later parity wait
+          // on the buffer then cannot alias).
+          if (!skip) skip = !seq_wait(a, &rfull[b], (nq >> b) & 1u, cta_abort);
+          nq ^= 1u << b;
+          j += js[g].y;
+          for (s += js[g].y; s >= S; s -= S) ph ^= 1u;
+          __syncwarp();
+          if (!skip && lane == 0) mbar_arrive(&rempty[b]);
+          ++k;
+          continue;
+        }
         if (B.rec_off < 0) {
           // x quantized here by all consumer threads: a batch that waits for
           // an earlier one (batch wait_on's outputs are, or overlap, its x, or
@@ -567,6 +638,7 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   int ngroups = wbytes < int64_t(n) * di->sm_count * (64 << 10) ? 4 : 2;
   if (forced_groups == 2 || forced_groups == 4) ngroups = forced_groups;
   const int gw = kSqConsumers / ngroups;
+  const bool skip_idle = ngroups == 4;  // the kernel with the per-batch stage table
   // Per batch: the per-launch kernel's lanes per row (so that every row's
   // arithmetic is the same), and the bytes of one pass of a consumer group
   // (gw warps, 32 / lanes rows each).
@@ -599,7 +671,8 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   for (int i = 0; i < n; ++i)
     for (int k = 0; k < n_mats[groups[i]]; ++k) nm_total += M[mat0[groups[i]] + k] > 0 ? 1 : 0;
   const int desc_bytes =
-      (n * int(sizeof(BatchDesc)) + nm_total * int(sizeof(MatDesc)) + n * int(sizeof(int2)) + 15) / 16 * 16;
+      (n * int(sizeof(BatchDesc)) + nm_total * int(sizeof(MatDesc)) + (skip_idle ? 2 : 1) * n * int(sizeof(int2)) +
+       15) / 16 * 16;
   const int budget =
       std::min(di->smem_per_sm - reserve, di->max_smem_optin) - nrec * xrec_bytes - desc_bytes - 1024;
   static const int forced_slot = tuning_value("BQ_GEMV_SEQ_SLOT_BYTES");  // read once per process
@@ -698,7 +771,8 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   a->n_local = n_local;
   const size_t smem = size_t(nrec) * xrec_bytes + size_t(stages) * slot + size_t(desc_bytes) +
                      8 * (2 * size_t(stages) + 2 * size_t(nrec)) + 16;
-  const void *fn = reinterpret_cast<const void *>(k_gemv_seq<TYPE>);
+  const void *fn = skip_idle ? reinterpret_cast<const void *>(k_gemv_seq<TYPE, true>)
+                             : reinterpret_cast<const void *>(k_gemv_seq<TYPE, false>);
   cudaError_t e = ensure_smem(fn, int(smem));
   if (e != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(sync, 0, sizeof(unsigned) * size_t(2 + n), stream)) != cudaSuccess) return e;
@@ -712,7 +786,8 @@ cudaError_t launch_seq_chunk(const std::vector<int> &groups, const std::vector<i
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemv_seq<TYPE>, *a);
+  return skip_idle ? cudaLaunchKernelEx(&cfg, k_gemv_seq<TYPE, true>, *a)
+                   : cudaLaunchKernelEx(&cfg, k_gemv_seq<TYPE, false>, *a);
 }
 
 template <int TYPE>

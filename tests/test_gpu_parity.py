@@ -687,6 +687,37 @@ def test_gemv_sequence_full_decode_step_matches_per_launch(bq, orc, dev):
     _check_float(_np(seq_out[-1][0]), y_ref, mag, "last batch")
 
 
+def test_gemv_sequence_two_group_launch_matches_per_launch(bq, orc, dev):
+    """Batches of 4096 x 4096 Q8_0 (17.8 MB each, more than 64 KB per CTA):
+    the launch takes two consumer groups of eight warps (the 7B decode step's
+    configuration, without the per-batch stage table). Batches 2 and 3 read
+    the previous output, the rest are independent: identical bits to one
+    bq_gemv_multi call per batch, no bounded wait runs out, and batch 0 and
+    batch 3 match the oracle."""
+    from block_quantized_weight_row_gb300 import binding, inputs
+    K = 4096
+    G = 6
+    ws = [bq.quantize_rows(Q8, inputs.weight(K, K, seed=870 + g, device=dev)) for g in range(G)]
+    xs = [inputs.activation(K, seed=880 + g, device=dev) for g in range(G)]
+    reads_prev = {2, 3}
+    def build(outs):
+        return [([ws[g]], outs[g - 1] if g in reads_prev else xs[g], [K], K, [outs[g]]) for g in range(G)]
+    outs = [torch.full((K,), float("nan"), device=dev) for _ in range(G)]
+    assert binding.device_status() == 0
+    bq.gemv_sequence(Q8, build(outs))
+    ref = [torch.full((K,), float("nan"), device=dev) for _ in range(G)]
+    for w_list, x, M_list, K_, y_list in build(ref):
+        bq.gemv_multi(Q8, w_list, x, M_list, K_, outs=y_list)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0, "a bounded wait ran out"
+    for g in range(G):
+        assert torch.equal(outs[g], ref[g]), f"batch {g}"
+    for g in (0, 3):
+        x = xs[g] if g not in reads_prev else ref[g - 1]
+        y_ref, mag = orc.gemv(Q8, _np(ws[g]), _np(x), K, K, with_mag=True)
+        _check_float(_np(outs[g]), y_ref, mag, f"batch {g}")
+
+
 def test_gemv_sequence_timeout_path_returns_error(bq, orc, dev):
     """Poll budget 0: every wait gives up at once, the grid-wide abort flag
     stops the other CTAs, copies in flight are drained, the status reports
