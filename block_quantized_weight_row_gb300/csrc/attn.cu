@@ -20,7 +20,8 @@
 //     head with its own online softmax, no block-wide barrier per tile;
 //   k_attn_chunk (every other shape): the block takes all heads together,
 //     scores for the chunk, one softmax per head, then the values.
-// Each chunk writes (m, l, o) per head; k_attn_combine merges the chunks:
+// Each chunk writes (m, l, o) per head, laid out per head and 32-channel slice;
+// k_attn_combine merges the chunks:
 // o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c (fp32).
 #include "attn_kernels.cuh"
 
@@ -262,8 +263,11 @@ cudaError_t launch_attn_decode(int kt, int vt, const float *q, const uint8_t *K,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(H), unsigned((D + 31) / 32));
+  const int csmem = combine_smem_bytes(chunks);
+  if ((e = ensure_smem(reinterpret_cast<const void *>(k_attn_combine), csmem)) != cudaSuccess) return e;
+  cfg.gridDim = dim3(unsigned(H), unsigned(D / 32));
   cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = size_t(csmem);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;

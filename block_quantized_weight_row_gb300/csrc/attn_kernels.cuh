@@ -16,6 +16,14 @@ namespace {
 
 constexpr int kAttnThreads = 256;
 
+// Partial results of chunk c (= blockIdx.x of the chunk kernels, gridDim.x
+// chunks): o_part[h][d / 32][c][d % 32] and ml[h][c] = (m, l). The chunks of
+// one head and 32-channel slice are contiguous (chunks x 128 bytes), so that
+// the combine moves them into shared memory with plain 16-byte async copies.
+__device__ __forceinline__ size_t part_offset(int h, int d, int D) {
+  return ((size_t(h) * (D / 32) + d / 32) * gridDim.x + blockIdx.x) * 32 + d % 32;
+}
+
 // q in the basis of a Hadamard-rotated K cache (lpnh.cn KV-cache article,
 // §三步上手, third step): every 64 channels of a head become H64 q / 8, so
 // (Hq).(Hk) = q.k. Lanes hold 4 channels each, 8 lanes per block of 32, two
@@ -353,15 +361,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_attn_chunk(const AttnArgs a
     for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int k = 0; k < DPU / 2; ++k) {
-        float *dst = a.o_part + (size_t(blockIdx.x) * H + kvh * G + g) * a.D + d0 + 2 * k;
+        float *dst = a.o_part + part_offset(kvh * G + g, d0 + 2 * k, a.D);
         dst[0] = __uint_as_float(uint32_t(acc[g][k]));
         dst[1] = __uint_as_float(uint32_t(acc[g][k] >> 32));
       }
   }
-  for (int h = tid; h < H; h += kAttnThreads) {
-    a.ml[(size_t(blockIdx.x) * H + h) * 2] = ML[2 * h];
-    a.ml[(size_t(blockIdx.x) * H + h) * 2 + 1] = ML[2 * h + 1];
-  }
+  for (int h = tid; h < H; h += kAttnThreads)
+    *reinterpret_cast<float2 *>(a.ml + (size_t(h) * gridDim.x + blockIdx.x) * 2) = make_float2(ML[2 * h], ML[2 * h + 1]);
 }
 
 // ---------------------------------------------------------------------------
@@ -534,13 +540,14 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
   const int vpart = kFix ? kSub * kKTok : a.sub * a.k_tok;  // offset of the V rows in a stage (a multiple of 16)
 
   // Launched as a programmatic dependent of the previous kernel on the
-  // stream: the K and V rows of the chunk's first prefetch_tokens tokens are
-  // asked into L2 at once (always safe: L2 is where writes become visible, so
-  // a line the previous kernel writes later is updated there), everything
-  // else waits until that kernel has completed. The combine may then be
+  // stream: q and the K and V rows of the chunk's first prefetch_tokens
+  // tokens are asked into L2 at once (always safe: L2 is where writes become
+  // visible, so a line the previous kernel writes later is updated there),
+  // everything else waits until that kernel has completed. The combine may then be
   // scheduled.
   if (tid == 0) {
     const uint32_t n = uint32_t(min(tn, a.prefetch_tokens));
+    prefetch_l2(a.q, uint32_t(H * D) * 4u);  // every CTA reads all of q first
     prefetch_l2(a.K + int64_t(t0) * a.k_tok, (n * uint32_t(a.k_tok)) & ~15u);
     prefetch_l2(a.V + int64_t(t0) * a.v_tok, (n * uint32_t(a.v_tok)) & ~15u);
   }
@@ -912,7 +919,7 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
     if (tt2 == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float *dst = a.o_part + (size_t(blockIdx.x) * H + j * G + g) * D + c0;
+        float *dst = a.o_part + part_offset(j * G + g, c0, D);  // c0 .. c0 + CPL - 1: one 32-channel slice
 #pragma unroll
         for (int k = 0; k + 1 < NP; k += 2)
           *reinterpret_cast<float4 *>(dst + 2 * k) =
@@ -926,7 +933,7 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
     if (lane == 0)
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        *reinterpret_cast<float2 *>(a.ml + (size_t(blockIdx.x) * H + j * G + g) * 2) = make_float2(m_run[g], l_run[g]);
+        *reinterpret_cast<float2 *>(a.ml + (size_t(j * G + g) * gridDim.x + blockIdx.x) * 2) = make_float2(m_run[g], l_run[g]);
     return;
   }
   // ---- merge: warps of a kv head and lanes of a channel group ----
@@ -974,79 +981,123 @@ __global__ void __launch_bounds__(kWarpAttnThreads, 2) k_attn_warp(const AttnWAr
         for (int q2 = 0; q2 < tpp2; ++q2) Ow = __fadd_rn(Ow, src[q2 * RS]);
         O = __fmaf_rn(f, Ow, O);
       }
-      a.o_part[(size_t(blockIdx.x) * H + h) * D + d] = O;
+      a.o_part[part_offset(h, d, D)] = O;
     }
-    if (lane == 0) {
-      a.ml[(size_t(blockIdx.x) * H + h) * 2] = M;
-      a.ml[(size_t(blockIdx.x) * H + h) * 2 + 1] = L;
-    }
+    if (lane == 0) *reinterpret_cast<float2 *>(a.ml + (size_t(h) * gridDim.x + blockIdx.x) * 2) = make_float2(M, L);
   }
 }
 
 // o[h][d] = sum_c e^(m_c - M) o_c[h][d] / sum_c e^(m_c - M) l_c[h]. One CTA
-// per head and 32 channels, 32 slices of the chunks per channel. A thread
-// loads every (o_c, m_c, l_c) of its slice at once (one round trip per 16
-// chunks) and keeps a running maximum with its own sums rescaled as in the
-// chunks; the slices are then merged the same way. fp32 throughout. Launched
-// as a programmatic dependent of the chunk kernel: it lets the next kernel
-// start at once and waits for the chunk kernel's writes before reading them.
+// per head and 32-channel slice: its chunks' partials (contiguous, chunks x
+// 128 bytes, and the head's (m, l) pairs) come into shared memory by 16- and
+// 8-byte async copies, every thread's copies in flight at once, up to
+// kCombineCap chunks per round. Per round: the block's maximum M of the m_c
+// (a running maximum over rounds, the sums so far rescaled by 2^(M_old - M)),
+// each chunk's weight w_c = 2^(m_c - M) computed once, then 32 slices of the
+// chunks add w_c o_c (one lane per channel) and w_c l_c; the slices' sums are
+// added at the end. fp32 throughout. Launched as a programmatic dependent of
+// the chunk kernel: it lets the next kernel start at once and waits for the
+// chunk kernel's writes before reading them.
 constexpr int kCombineThreads = 1024;
-constexpr int kCombineSlices = kCombineThreads / 32;
-constexpr int kCombinePer = 16;  // chunks per thread and round
+constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kCombineCap = 1024;  // chunks per round: 136 KB of shared memory
+
+__host__ __device__ constexpr int combine_smem_bytes(int chunks) {
+  return (chunks < kCombineCap ? chunks : kCombineCap) * (32 * 4 + 8);
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kCombineThreads) k_attn_combine(const float *__restrict__ o_part,
                                                                   const float *__restrict__ ml,
                                                                   float *__restrict__ o, int chunks, int H, int D) {
-  __shared__ float sO[kCombineSlices][33];
-  __shared__ float sM[kCombineSlices], sL[kCombineSlices];
-  const int h = blockIdx.x, lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
-  const int d = blockIdx.y * 32 + lane;
-  const bool dv = d < D;
+  extern __shared__ __align__(16) uint8_t csm[];
+  const int cap = chunks < kCombineCap ? chunks : kCombineCap;
+  float *sP = reinterpret_cast<float *>(csm);                         // [cap][32]: o_c of the slice
+  float2 *sW = reinterpret_cast<float2 *>(csm + size_t(cap) * 128);  // [cap]: (m_c, l_c), then (w_c, w_c l_c)
+  __shared__ float sO[kCombineWarps][33];
+  __shared__ float sRed[kCombineWarps], sL[kCombineWarps];
+  const int h = blockIdx.x, db = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float4 *src = reinterpret_cast<const float4 *>(o_part + (size_t(h) * (D / 32) + db) * size_t(chunks) * 32);
+  const float2 *msrc = reinterpret_cast<const float2 *>(ml) + size_t(h) * chunks;
   pdl_launch_dependents();
   pdl_wait();
-  float m = -INFINITY, l = 0.0f, O = 0.0f;
-  for (int base = 0; base < chunks; base += kCombineSlices * kCombinePer) {
-    float v[kCombinePer];
-    float2 p[kCombinePer];
+  float M = -INFINITY;  // block-uniform running maximum
+  float O = 0.0f, L = 0.0f;  // this warp's sums (channel lane; L in every lane)
+  for (int base = 0; base < chunks; base += cap) {
+    const int n = min(cap, chunks - base);
+    for (int i = threadIdx.x; i < n * 8; i += kCombineThreads)
+      cp_async16(reinterpret_cast<float4 *>(sP) + i, src + size_t(base) * 8 + i);
+    for (int i = threadIdx.x; i < n; i += kCombineThreads) cp_async8(sW + i, msrc + base + i);
+    cp_async_wait_all();
+    __syncthreads();
+    // the round's maximum
+    float mx = -INFINITY;
+    for (int c = threadIdx.x; c < n; c += kCombineThreads) mx = fmaxf(mx, sW[c].x);
 #pragma unroll
-    for (int k = 0; k < kCombinePer; ++k) {
-      const int c = base + slice + kCombineSlices * k;
-      const bool in = c < chunks;
-      v[k] = (in && dv) ? __ldg(o_part + (size_t(c) * H + h) * D + d) : 0.0f;
-      p[k] = in ? __ldg(reinterpret_cast<const float2 *>(ml) + size_t(c) * H + h) : make_float2(-INFINITY, 0.0f);
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) sRed[warp] = mx;
+    __syncthreads();
+    mx = sRed[lane];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float Mn = fmaxf(M, mx);
+    if (Mn != -INFINITY) {  // else no chunk so far saw a token: nothing to add
+      if (M != Mn && M != -INFINITY) {  // an earlier round's sums, rescaled
+        const float f = ex2(__fsub_rn(M, Mn));
+        O = __fmul_rn(O, f);
+        L = __fmul_rn(L, f);
+      }
+      M = Mn;
+      // chunk weights, each computed once (read after the barrier below)
+      for (int c = threadIdx.x; c < n; c += kCombineThreads) {
+        const float2 p = sW[c];
+        const float w = ex2(__fsub_rn(p.x, M));  // 0 for a chunk that saw no token
+        sW[c] = make_float2(w, __fmul_rn(w, p.y));
+      }
     }
-    float mr = m;
-#pragma unroll
-    for (int k = 0; k < kCombinePer; ++k) mr = fmaxf(mr, p[k].x);
-    if (mr == -INFINITY) continue;  // this slice has no chunk in the round
-    const float f = ex2(__fsub_rn(m, mr));  // 0 while m = -inf
-    l = __fmul_rn(l, f);
-    O = __fmul_rn(O, f);
-#pragma unroll
-    for (int k = 0; k < kCombinePer; ++k) {
-      const float e = ex2(__fsub_rn(p[k].x, mr));  // 0 past the last chunk
-      l = __fmaf_rn(e, p[k].y, l);
-      O = __fmaf_rn(e, v[k], O);
+    __syncthreads();
+    if (M != -INFINITY) {
+      int c = warp;
+      for (; c + 3 * kCombineWarps < n; c += 4 * kCombineWarps) {
+        const float2 w0 = sW[c], w1 = sW[c + kCombineWarps], w2 = sW[c + 2 * kCombineWarps],
+                     w3 = sW[c + 3 * kCombineWarps];
+        const float p0 = sP[c * 32 + lane], p1 = sP[(c + kCombineWarps) * 32 + lane],
+                    p2 = sP[(c + 2 * kCombineWarps) * 32 + lane], p3 = sP[(c + 3 * kCombineWarps) * 32 + lane];
+        O = __fmaf_rn(w0.x, p0, O);
+        L = __fadd_rn(L, w0.y);
+        O = __fmaf_rn(w1.x, p1, O);
+        L = __fadd_rn(L, w1.y);
+        O = __fmaf_rn(w2.x, p2, O);
+        L = __fadd_rn(L, w2.y);
+        O = __fmaf_rn(w3.x, p3, O);
+        L = __fadd_rn(L, w3.y);
+      }
+      for (; c < n; c += kCombineWarps) {
+        const float2 w = sW[c];
+        O = __fmaf_rn(w.x, sP[c * 32 + lane], O);
+        L = __fadd_rn(L, w.y);
+      }
     }
-    m = mr;
+    __syncthreads();  // the round's shared memory is read before the next round's copies
   }
-  sO[slice][lane] = O;
-  if (lane == 0) {
-    sM[slice] = m;
-    sL[slice] = l;
-  }
+  sO[warp][lane] = O;
+  if (lane == 0) sL[warp] = L;
   __syncthreads();
-  if (slice == 0 && dv) {
-    float M = -INFINITY;
+  if (warp == 0) {
+    float sum = 0.0f, Lt = 0.0f;
 #pragma unroll 8
-    for (int k = 0; k < kCombineSlices; ++k) M = fmaxf(M, sM[k]);
-    float sum = 0.0f, L = 0.0f;
-#pragma unroll 8
-    for (int k = 0; k < kCombineSlices; ++k) {
-      const float f = ex2(__fsub_rn(sM[k], M));  // 0 for a slice with no chunk
-      sum = __fmaf_rn(f, sO[k][lane], sum);
-      L = __fmaf_rn(f, sL[k], L);
+    for (int k = 0; k < kCombineWarps; ++k) {
+      sum = __fadd_rn(sum, sO[k][lane]);
+      Lt = __fadd_rn(Lt, sL[k]);
     }
-    o[size_t(h) * D + d] = __fdiv_rn(sum, L);
+    o[size_t(h) * D + db * 32 + lane] = __fdiv_rn(sum, Lt);
   }
 }
 
