@@ -66,6 +66,7 @@ def lib():
         "bq_attn_workspace_size": ([i, i, i64, i64, i64, i64], sz),
         "bq_gemm": ([i, vp, vp, vp, i64, i64, i64], i),
         "bq_kv_quantize": ([i, vp, vp, vp, i64, i64, i64], i),
+        "bq_kv_write": ([i, vp, vp, i, i, vp, i, vp, vp, i64, i64, i64], i),
         "bq_block_dots": ([i, vp, vp, vp, i64, i64], i),
         "bq_set_stream": ([vp], i),
         "bq_get_stream": ([], vp),
@@ -287,6 +288,29 @@ def kv_quantize(t: int, rows: torch.Tensor, bias: torch.Tensor | None,
     _check(L.bq_kv_quantize_basis(t, _ptr(rows), _ptr(bias), basis if bias_basis is None else bias_basis, basis,
                                   _ptr(out), T, H, D), "bq_kv_quantize_basis")
     return out
+
+
+def kv_write(k_type: int, k_rows: torch.Tensor, bias: torch.Tensor | None, v_type: int, v_rows: torch.Tensor,
+             out_k: torch.Tensor | None = None, out_v: torch.Tensor | None = None, basis: int = BASIS_PLAIN,
+             bias_basis: int | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """One layer's K and V cache write in one launch (bq_kv_write): k_rows and
+    v_rows (n_tokens, n_kv_heads, head_dim) fp32; bias (n_kv_heads, head_dim)
+    or None; basis: the K cache's basis. Returns (K blocks, V blocks)."""
+    _cuda(k_rows, "k_rows")
+    _cuda(v_rows, "v_rows")
+    if bias is not None:
+        _cuda(bias, "bias")
+    T, H, D = k_rows.shape
+    if tuple(v_rows.shape) != (T, H, D):
+        raise ValueError("k_rows and v_rows must have the same shape")
+    if out_k is None:
+        out_k = torch.empty((T, H, (D // QK) * max(block_bytes(k_type), 1)), dtype=torch.uint8, device=k_rows.device)
+    if out_v is None:
+        out_v = torch.empty((T, H, (D // QK) * max(block_bytes(v_type), 1)), dtype=torch.uint8, device=v_rows.device)
+    L = _prep(k_rows.device)
+    _check(L.bq_kv_write(k_type, _ptr(k_rows), _ptr(bias), basis if bias_basis is None else bias_basis, basis,
+                         _ptr(out_k), v_type, _ptr(v_rows), _ptr(out_v), T, H, D), "bq_kv_write")
+    return out_k, out_v
 
 
 def kv_bias(rows: torch.Tensor, basis: int = BASIS_PLAIN, out: torch.Tensor | None = None) -> torch.Tensor:

@@ -533,6 +533,41 @@ int bq_kv_quantize_basis(int type, const float *rows, const float *bias, int bia
   return e == cudaSuccess ? ok() : cuda_fail(e, "bq_kv_quantize launch");
 }
 
+int bq_kv_write(int k_type, const float *K_rows, const float *bias, int bias_basis, int k_basis, void *K_dst,
+                int v_type, const float *V_rows, void *V_dst, int64_t n_tokens, int64_t n_kv_heads,
+                int64_t head_dim) {
+  if (!core_type(k_type) || !core_type(v_type))
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_write: K and V types must be Q4_0 or Q8_0 (got %d, %d)", k_type, v_type);
+  if (k_basis != BQ_BASIS_PLAIN && k_basis != BQ_BASIS_HADAMARD64)
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_write: unknown basis %d", k_basis);
+  if (bias && k_type != BQ_TYPE_Q4_0)
+    return fail(BQ_ERR_UNSUPPORTED, "bq_kv_write: a mean-centering bias requires a Q4_0 K cache");
+  if (bias && bias_basis != k_basis)
+    return fail(BQ_ERR_BASIS, "bq_kv_write: the bias was calibrated in basis %d, the K cache is in basis %d",
+                bias_basis, k_basis);
+  if (!sizes_ok(n_tokens, n_kv_heads) || !sizes_ok(n_tokens * n_kv_heads, head_dim))
+    return fail(BQ_ERR_INVALID_ARG, "bq_kv_write: bad sizes");
+  if (head_dim % kQK) return fail(BQ_ERR_SHAPE, "bq_kv_write: head_dim %lld is not a multiple of 32", (long long)head_dim);
+  if (k_basis == BQ_BASIS_HADAMARD64 && head_dim % 64)
+    return fail(BQ_ERR_SHAPE, "bq_kv_write: the rotated basis needs head_dim %% 64 == 0, got %lld", (long long)head_dim);
+  const int64_t n_blocks = n_tokens * n_kv_heads * (head_dim / kQK);
+  if (n_blocks == 0) return ok();
+  if (!K_rows || !K_dst || !V_rows || !V_dst) return fail(BQ_ERR_INVALID_ARG, "bq_kv_write: null pointer");
+  if (!aligned(K_rows, 16) || !aligned(K_dst, 16) || !aligned(V_rows, 16) || !aligned(V_dst, 16) ||
+      (bias && !aligned(bias, 16)))
+    return fail(BQ_ERR_ALIGN, "bq_kv_write: rows, bias and outputs must be 16-byte aligned");
+  const size_t in_bytes = size_t(n_blocks) * 128, bias_bytes = size_t(n_kv_heads * head_dim) * 4;
+  const size_t kb = size_t(n_blocks) * size_t(block_bytes(k_type)), vb = size_t(n_blocks) * size_t(block_bytes(v_type));
+  if (overlap(K_dst, kb, K_rows, in_bytes) || overlap(K_dst, kb, V_rows, in_bytes) || overlap(K_dst, kb, bias, bias_bytes) ||
+      overlap(V_dst, vb, K_rows, in_bytes) || overlap(V_dst, vb, V_rows, in_bytes) || overlap(V_dst, vb, bias, bias_bytes) ||
+      overlap(K_dst, kb, V_dst, vb))
+    return fail(BQ_ERR_INVALID_ARG, "bq_kv_write: an output overlaps an input or the other output");
+  cudaError_t e = launch_kv_write(k_type, v_type, k_basis == BQ_BASIS_HADAMARD64, K_rows, static_cast<uint8_t *>(K_dst),
+                                  V_rows, static_cast<uint8_t *>(V_dst), n_blocks, bias, n_kv_heads * (head_dim / kQK),
+                                  t_stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "bq_kv_write launch");
+}
+
 int bq_kv_bias(const float *rows, int basis, float *bias, int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim) {
   if (basis != BQ_BASIS_PLAIN && basis != BQ_BASIS_HADAMARD64)
     return fail(BQ_ERR_UNSUPPORTED, "bq_kv_bias: unknown basis %d", basis);

@@ -173,6 +173,10 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     __syncthreads();
   }
   const bool bias_pow2 = (bias_period & (bias_period - 1)) == 0;
+  // a launch that follows as a programmatic dependent (the V half of a
+  // one-layer KV write) may be scheduled at once: it touches none of this
+  // launch's memory, and its CTAs take the SMs this grid's CTAs leave
+  pdl_launch_dependents();
   const int64_t total_warps = int64_t(gridDim.x) * kQuantWarps;
   // coalesced: vector i = lane + 32c of a tile is chunk (i & 7) of block (i >> 3)
   auto issue_tile = [&](int64_t t, uint8_t *buf) {
@@ -489,9 +493,13 @@ __global__ void __launch_bounds__(256) k_dequantize_kq(const uint8_t *__restrict
   }
 }
 
+// early: launched as a programmatic dependent of the previous launch on the
+// stream, without waiting for it (only for a launch whose memory is disjoint
+// from that launch's, the previous launch having itself waited for all
+// earlier work).
 template <int TYPE, bool BIAS, bool ROT>
 cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, bool early = false) {
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
@@ -502,9 +510,18 @@ cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const flo
   const size_t smem = quant_smem_bytes<TYPE>(bias_smem_blocks);
   err = ensure_smem(reinterpret_cast<const void *>(k_quantize_rows<TYPE, BIAS, ROT>), int(smem));
   if (err != cudaSuccess) return err;
-  k_quantize_rows<TYPE, BIAS, ROT><<<unsigned(grid), kQuantThreads, smem, stream>>>(src, dst, n_blocks, bias,
-                                                                                  bias_period, bias_smem_blocks);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kQuantThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = early ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_quantize_rows<TYPE, BIAS, ROT>, src, dst, n_blocks, bias, bias_period,
+                            bias_smem_blocks);
 }
 
 template <bool ROT>
@@ -519,6 +536,31 @@ cudaError_t launch_q_typed(int type, const float *src, uint8_t *dst, int64_t n_b
                 : launch_q<kTypeQ4_0, false, ROT>(src, dst, n_blocks, nullptr, 1, stream);
   // a bias with Q8_0 is rejected by the ABI layer
   return launch_q<kTypeQ8_0, false, ROT>(src, dst, n_blocks, nullptr, 1, stream);
+}
+
+// One layer's KV write (lpnh.cn KV-cache article, §解法 and §三步上手): K, then
+// V as a programmatic dependent that does not wait for K. K and V share no
+// memory, so V's CTAs may fill the SMs that K's persistent CTAs leave as they
+// finish (K's arithmetic-heavy tail then overlaps V's memory-bound start);
+// V cannot start before K has, and K starts after every earlier launch.
+cudaError_t launch_kv_write_pair(int k_type, int v_type, bool k_rot, const float *k_src, uint8_t *k_dst,
+                                 const float *v_src, uint8_t *v_dst, int64_t n_blocks, const float *bias,
+                                 int64_t bias_period, cudaStream_t stream) {
+  cudaError_t e;
+  if (k_type == kTypeQ4_0) {
+    if (bias)
+      e = k_rot ? launch_q<kTypeQ4_0, true, true>(k_src, k_dst, n_blocks, bias, bias_period, stream)
+                : launch_q<kTypeQ4_0, true, false>(k_src, k_dst, n_blocks, bias, bias_period, stream);
+    else
+      e = k_rot ? launch_q<kTypeQ4_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream)
+                : launch_q<kTypeQ4_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream);
+  } else {
+    e = k_rot ? launch_q<kTypeQ8_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream)
+              : launch_q<kTypeQ8_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream);
+  }
+  if (e != cudaSuccess) return e;
+  return v_type == kTypeQ4_0 ? launch_q<kTypeQ4_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, true)
+                             : launch_q<kTypeQ8_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, true);
 }
 
 // bias[h][c] = fp32(sum_t r_t[h][c] / n_tokens), the sum in fp64 in token
@@ -597,6 +639,13 @@ cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64
   }
   return rotate ? launch_q_typed<true>(type, src, dst, n_blocks, bias, bias_period, stream)
                 : launch_q_typed<false>(type, src, dst, n_blocks, bias, bias_period, stream);
+}
+
+cudaError_t launch_kv_write(int k_type, int v_type, bool k_rot, const float *k_src, uint8_t *k_dst,
+                            const float *v_src, uint8_t *v_dst, int64_t n_blocks, const float *bias,
+                            int64_t bias_period, cudaStream_t stream) {
+  if (n_blocks == 0) return cudaSuccess;
+  return launch_kv_write_pair(k_type, v_type, k_rot, k_src, k_dst, v_src, v_dst, n_blocks, bias, bias_period, stream);
 }
 
 cudaError_t launch_kv_bias(const float *rows, float *bias, int64_t n_tokens, int64_t row_len, bool rotate,

@@ -248,6 +248,24 @@ int bq_kv_quantize(int type, const float *K_rows, const float *bias, void *dst, 
 int bq_kv_quantize_basis(int type, const float *K_rows, const float *bias, int bias_basis, int basis, void *dst,
                          int64_t n_tokens, int64_t n_kv_heads, int64_t head_dim);
 
+/* KV-cache write of one layer in one call: K_rows to k_type in k_basis
+ * (rotation and bias as bq_kv_quantize_basis: the bias NULL or with a Q4_0 K
+ * only, calibrated in bias_basis == k_basis) and V_rows to v_type (plain
+ * basis, no bias), both n_tokens x n_kv_heads x head_dim fp32 (16-byte
+ * aligned); K_dst / V_dst: n_tokens x n_kv_heads x head_dim/32 blocks
+ * (16-byte aligned). The bytes written are those of bq_kv_quantize_basis on K
+ * and bq_kv_quantize on V. As the two tensors share no memory, V's launch
+ * follows K's as a programmatic dependent that does not wait for it: V's
+ * blocks start on the SMs that K's finishing blocks leave, instead of after
+ * K's last one (the pages write the cache one tensor per kernel; this is a
+ * schedule, not a different result). Ordered after all earlier work on the
+ * stream; later work is ordered after both. Types: Q4_0 or Q8_0 for each
+ * (else BQ_ERR_UNSUPPORTED). Errors as bq_kv_quantize_basis, and
+ * BQ_ERR_INVALID_ARG when an output overlaps an input or the other output. */
+int bq_kv_write(int k_type, const float *K_rows, const float *bias, int bias_basis, int k_basis, void *K_dst,
+                int v_type, const float *V_rows, void *V_dst, int64_t n_tokens, int64_t n_kv_heads,
+                int64_t head_dim);
+
 /* Mean-centering bias calibration (lpnh.cn KV-cache article, §三步上手: the
  * channel mean of K over a calibration run): bias[h][c] = fp32(sum_t
  * r_t[h][c] / n_tokens), the sum in fp64 in token order, r_t the token's row

@@ -279,6 +279,31 @@ def test_rotated_kv_and_bias_validation(L):
     assert L.bq_attn_decode_basis(2, 8, 3, q, K, V, o, 100, 16, 8, 128, f) == -3  # unknown basis
 
 
+def test_layer_kv_write_validation(L):
+    """bq_kv_write checks both tensors' types, the K basis and bias, sizes,
+    alignment and every overlap on the host, before anything runs."""
+    base = 1 << 32
+    K, V, bias = base, base + (1 << 26), base + (2 << 26)
+    kd, vd = base + (3 << 26), base + (4 << 26)
+    n = (10, 2, 128)
+    assert L.bq_kv_write(2, K, bias, 1, 0, kd, 8, V, vd, *n) == -8     # bias basis differs from the cache's
+    assert L.bq_kv_write(8, K, bias, 0, 0, kd, 8, V, vd, *n) == -3     # bias with a Q8_0 K
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 3, V, vd, *n) == -3     # legacy V type
+    assert L.bq_kv_write(12, K, None, 0, 0, kd, 8, V, vd, *n) == -3    # k-quant K type
+    assert L.bq_kv_write(2, K, None, 0, 2, kd, 8, V, vd, *n) == -3     # unknown basis
+    assert L.bq_kv_write(2, K, None, 0, 1, kd, 8, V, vd, 10, 2, 96) == -2   # rotation needs head_dim % 64
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V, vd, 10, 2, 48) == -2   # head_dim % 32
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V, vd, -1, 2, 128) == -1
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, None, vd, *n) == -1
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V + 4, vd, *n) == -4
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V, vd + 8, *n) == -4
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V, V + 1024, *n) == -1       # V output inside V's rows
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V, K + 4096, *n) == -1       # V output inside K's rows
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V, kd + 16, *n) == -1        # the outputs overlap
+    assert L.bq_kv_write(2, K, bias, 0, 0, bias - 16, 8, V, vd, *n) == -1      # K output over the bias
+    assert L.bq_kv_write(2, K, None, 0, 0, kd, 8, V, vd, 0, 2, 128) == 0       # empty: a no-op
+
+
 def test_kquants_where_they_are_taken(L):
     """Q4_K (12) and Q6_K (14): super-blocks of 256 values; rows must hold
     whole super-blocks; only the row quantizer, dequantizer and GEMV take them."""

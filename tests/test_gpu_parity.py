@@ -342,6 +342,82 @@ def test_kv_write_full_layer(bq, orc, dev):
     assert np.array_equal(vq, orc.kv_quantize(Q8, _np(L.V), None, T, H, D))
 
 
+@pytest.mark.parametrize("T,NKV,D,kt,vt,basis,with_bias", [
+    (1, 1, 32, Q4, Q8, 0, True), (37, 8, 128, Q4, Q8, 0, True), (1000, 8, 128, Q4, Q8, 1, True),
+    (33, 3, 64, Q4, Q4, 1, False), (130, 3, 96, Q8, Q8, 0, False), (7, 2, 256, Q8, Q4, 1, False),
+    (4099, 5, 64, Q4, Q8, 0, True)])
+def test_kv_write_layer_matches_oracle(bq, orc, dev, T, NKV, D, kt, vt, basis, with_bias):
+    """bq_kv_write (K and V of a layer in one call, V's launch not waiting for
+    K's): K and V bytes equal to the oracle's and to one bq_kv_quantize call
+    per tensor, for block counts
+    that leave a ragged last tile (1 block; 21 x 3 x 2; 4099 x 5 x 2), both
+    bases, with and without the bias, every type pair."""
+    rng = np.random.default_rng(T + 3 * NKV + D + basis)
+    K = _outlier_rows(rng, T, NKV, D)
+    V = rng.normal(size=(T, NKV, D)).astype(np.float32)
+    bias = orc.kv_bias(_outlier_rows(rng, 64, NKV, D), basis, 64, NKV, D) if with_bias else None
+    Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
+    bd = torch.from_numpy(bias).to(dev) if with_bias else None
+    kq, vq = bq.kv_write(kt, Kd, bd, vt, Vd, basis=basis)
+    assert np.array_equal(_np(kq), orc.kv_quantize(kt, K, bias, T, NKV, D, basis=basis))
+    assert np.array_equal(_np(vq), orc.kv_quantize(vt, V, None, T, NKV, D))
+    assert torch.equal(kq, bq.kv_quantize(kt, Kd, bd, basis=basis))
+    assert torch.equal(vq, bq.kv_quantize(vt, Vd, None))
+
+
+def test_kv_write_layer_full_size(bq, orc, dev):
+    """One full layer of the KV-write workload through bq_kv_write (K
+    mean-centered to Q4_0, V to Q8_0): the oracle's bytes in either basis.
+    Calls follow each other on the stream without a sync, the second writing
+    the same outputs (its V launch must not overtake the first call's): the
+    later call's bytes remain."""
+    from block_quantized_weight_row_gb300 import inputs
+    cfg = inputs.WORKLOADS["kv-write"]
+    L = inputs.kv_layer(1, cfg["tokens"], cfg["kv_heads"], cfg["head_dim"], cfg["calib_tokens"], device=dev)
+    T, H, D = L.K.shape
+    Kn, Vn = _np(L.K), _np(L.V)
+    v_ref = orc.kv_quantize(Q8, Vn, None, T, H, D)
+    biases = [bq.kv_bias(L.K_calib, basis) for basis in (0, 1)]
+    zeros_v = torch.zeros_like(L.V)
+    kq = torch.empty((T, H, D // 32 * 18), dtype=torch.uint8, device=dev)
+    vq = torch.empty((T, H, D // 32 * 34), dtype=torch.uint8, device=dev)
+    for last in (0, 1):
+        first = 1 - last
+        bq.kv_write(Q4, L.K, biases[first], Q8, zeros_v, out_k=kq, out_v=vq, basis=first)
+        bq.kv_write(Q4, L.K, biases[last], Q8, L.V, out_k=kq, out_v=vq, basis=last)
+        assert np.array_equal(_np(kq), orc.kv_quantize(Q4, Kn, _np(biases[last]), T, H, D, basis=last))
+        assert np.array_equal(_np(vq), v_ref)
+
+
+def test_kv_write_layer_rejects_before_writing(bq, dev):
+    """A bias with a Q8_0 K, a bias from another basis, an unknown V type or
+    outputs that overlap: an error status and nothing written."""
+    from block_quantized_weight_row_gb300 import binding
+    K = torch.ones(4, 2, 64, device=dev)
+    V = torch.ones(4, 2, 64, device=dev)
+    ok_k = torch.full((4, 2, 36), 7, dtype=torch.uint8, device=dev)
+    ok_v = torch.full((4, 2, 68), 7, dtype=torch.uint8, device=dev)
+    shared = torch.full((1024,), 7, dtype=torch.uint8, device=dev)  # two outputs that overlap
+    q8_k = torch.full((4, 2, 68), 7, dtype=torch.uint8, device=dev)
+    cases = [
+        (dict(k_type=Q8, bias=torch.zeros(2, 64, device=dev), v_type=Q8, out_k=q8_k), -3),
+        (dict(k_type=Q4, bias=torch.zeros(2, 64, device=dev), v_type=Q8, basis=1, bias_basis=0), -8),
+        (dict(k_type=Q4, bias=None, v_type=bq.Q4_1), -3),
+        (dict(k_type=Q4, bias=None, v_type=Q8, out_k=shared[:288].view(4, 2, 36),
+              out_v=shared[256:256 + 544].view(4, 2, 68)), -1),
+    ]
+    for kw, status in cases:
+        kt, b, vt = kw.pop("k_type"), kw.pop("bias"), kw.pop("v_type")
+        kw.setdefault("out_k", ok_k)
+        kw.setdefault("out_v", ok_v)
+        with pytest.raises(binding.BQError) as e:
+            bq.kv_write(kt, K, b, vt, V, **kw)
+        assert e.value.status == status
+    torch.cuda.synchronize()
+    for t in (ok_k, ok_v, shared, q8_k):
+        assert bool((t == 7).all())  # nothing was written
+
+
 def test_kv_mean_centering_keeps_softmax_and_helps(bq, dev):
     """GPU-written cache: adding the bias back after dequantization recovers K
     within half a scale step, and centering lowers the attention KL against
