@@ -51,8 +51,8 @@ cudaError_t launch_quantize_rows(int type, const float *src, uint8_t *dst, int64
                                  cudaStream_t stream, bool rotate = false);
 // K (k_type, rotated when k_rot, the bias subtracted when given) and V
 // (v_type, plain), n_blocks blocks each: the same launches as
-// launch_quantize_rows on each tensor, V a programmatic dependent of K that
-// does not wait for it (the tensors share no memory).
+// launch_quantize_rows on each tensor, the second a programmatic dependent
+// of the first that does not wait for it (the tensors share no memory).
 cudaError_t launch_kv_write(int k_type, int v_type, bool k_rot, const float *k_src, uint8_t *k_dst,
                             const float *v_src, uint8_t *v_dst, int64_t n_blocks, const float *bias,
                             int64_t bias_period, cudaStream_t stream);

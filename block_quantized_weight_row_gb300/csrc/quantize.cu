@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     __syncthreads();
   }
   const bool bias_pow2 = (bias_period & (bias_period - 1)) == 0;
-  // a launch that follows as a programmatic dependent (the V half of a
+  // a launch that follows as a programmatic dependent (the other half of a
   // one-layer KV write) may be scheduled at once: it touches none of this
   // launch's memory, and its CTAs take the SMs this grid's CTAs leave
   pdl_launch_dependents();
@@ -538,29 +538,35 @@ cudaError_t launch_q_typed(int type, const float *src, uint8_t *dst, int64_t n_b
   return launch_q<kTypeQ8_0, false, ROT>(src, dst, n_blocks, nullptr, 1, stream);
 }
 
-// One layer's KV write (lpnh.cn KV-cache article, §解法 and §三步上手): K, then
-// V as a programmatic dependent that does not wait for K. K and V share no
-// memory, so V's CTAs may fill the SMs that K's persistent CTAs leave as they
-// finish (K's arithmetic-heavy tail then overlaps V's memory-bound start);
-// V cannot start before K has, and K starts after every earlier launch.
+// One layer's KV write (lpnh.cn KV-cache article, §解法 and §三步上手): the two
+// tensors' row-quantize launches, the second a programmatic dependent of the
+// first that does not wait for it. K and V share no memory, so the second
+// launch's CTAs may fill the SMs that the first launch's persistent CTAs
+// leave as they finish; the second cannot start before the first has, and
+// the first starts after every earlier launch. Order (measured): K first for
+// a plain K (V's memory-bound start then overlaps K's arithmetic-heavy
+// tail), V first for a rotated K (the longer K half then fills V's tail).
 cudaError_t launch_kv_write_pair(int k_type, int v_type, bool k_rot, const float *k_src, uint8_t *k_dst,
                                  const float *v_src, uint8_t *v_dst, int64_t n_blocks, const float *bias,
                                  int64_t bias_period, cudaStream_t stream) {
-  cudaError_t e;
-  if (k_type == kTypeQ4_0) {
-    if (bias)
-      e = k_rot ? launch_q<kTypeQ4_0, true, true>(k_src, k_dst, n_blocks, bias, bias_period, stream)
-                : launch_q<kTypeQ4_0, true, false>(k_src, k_dst, n_blocks, bias, bias_period, stream);
-    else
-      e = k_rot ? launch_q<kTypeQ4_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream)
-                : launch_q<kTypeQ4_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream);
-  } else {
-    e = k_rot ? launch_q<kTypeQ8_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream)
-              : launch_q<kTypeQ8_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream);
-  }
+  auto launch_k = [&](bool early) {
+    if (k_type == kTypeQ4_0) {
+      if (bias)
+        return k_rot ? launch_q<kTypeQ4_0, true, true>(k_src, k_dst, n_blocks, bias, bias_period, stream, early)
+                     : launch_q<kTypeQ4_0, true, false>(k_src, k_dst, n_blocks, bias, bias_period, stream, early);
+      return k_rot ? launch_q<kTypeQ4_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream, early)
+                   : launch_q<kTypeQ4_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream, early);
+    }
+    return k_rot ? launch_q<kTypeQ8_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream, early)
+                 : launch_q<kTypeQ8_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream, early);
+  };
+  auto launch_v = [&](bool early) {
+    return v_type == kTypeQ4_0 ? launch_q<kTypeQ4_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, early)
+                               : launch_q<kTypeQ8_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, early);
+  };
+  cudaError_t e = k_rot ? launch_v(false) : launch_k(false);
   if (e != cudaSuccess) return e;
-  return v_type == kTypeQ4_0 ? launch_q<kTypeQ4_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, true)
-                             : launch_q<kTypeQ8_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, true);
+  return k_rot ? launch_k(true) : launch_v(true);
 }
 
 // bias[h][c] = fp32(sum_t r_t[h][c] / n_tokens), the sum in fp64 in token

@@ -254,11 +254,12 @@ int bq_kv_quantize_basis(int type, const float *K_rows, const float *bias, int b
  * basis, no bias), both n_tokens x n_kv_heads x head_dim fp32 (16-byte
  * aligned); K_dst / V_dst: n_tokens x n_kv_heads x head_dim/32 blocks
  * (16-byte aligned). The bytes written are those of bq_kv_quantize_basis on K
- * and bq_kv_quantize on V. As the two tensors share no memory, V's launch
- * follows K's as a programmatic dependent that does not wait for it: V's
- * blocks start on the SMs that K's finishing blocks leave, instead of after
- * K's last one (the pages write the cache one tensor per kernel; this is a
- * schedule, not a different result). Ordered after all earlier work on the
+ * and bq_kv_quantize on V. As the two tensors share no memory, the second
+ * tensor's launch follows the first's as a programmatic dependent that does
+ * not wait for it: its blocks start on the SMs that the first launch's
+ * finishing blocks leave, instead of after its last one (K first for a plain
+ * K, V first for a rotated one; the pages write the cache one tensor per
+ * kernel; this is a schedule, not a different result). Ordered after all earlier work on the
  * stream; later work is ordered after both. Types: Q4_0 or Q8_0 for each
  * (else BQ_ERR_UNSUPPORTED). Errors as bq_kv_quantize_basis, and
  * BQ_ERR_INVALID_ARG when an output overlaps an input or the other output. */
