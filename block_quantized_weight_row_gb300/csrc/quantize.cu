@@ -153,7 +153,14 @@ size_t quant_smem_bytes(int64_t bias_smem_blocks) {
   return size_t(kQuantWarps) * 2 * 32 * 128 + size_t(quant_out_bytes<TYPE>()) + size_t(bias_smem_blocks) * 128;
 }
 
-template <int TYPE, bool BIAS, bool ROT>
+// BMODE: where the bias lives. 0: decided at run time (staged in shared
+// memory when it fits, else read from global memory); 1: staged negated in
+// shared memory and added as fp32 pairs (x - b and x + (-b) are the same IEEE
+// sum), with a branch-free block store; 2: global memory. The rotated writes
+// with a bias take 1 or 2 (fewer instructions where the rotation already
+// makes the kernel issue-bound); the others 0 (the specialised forms cost the
+// plain kernel registers: at 80 registers a stack frame).
+template <int TYPE, bool BIAS, bool ROT, int BMODE = 0>
 __global__ void __launch_bounds__(kQuantThreads, 3)
     k_quantize_rows(const float *__restrict__ src, uint8_t *__restrict__ dst, int64_t n_blocks,
                     const float *__restrict__ bias, int64_t bias_period, int bias_smem_blocks) {
@@ -166,10 +173,13 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
   uint8_t *tiles = qsm + warp * 2 * kTile;
   uint8_t *ot = qsm + kQuantWarps * 2 * kTile + warp * 32 * BB;  // legacy types only
   uint8_t *bias_tile = qsm + kQuantWarps * 2 * kTile + quant_out_bytes<TYPE>();
-  const bool bias_in_smem = BIAS && bias_smem_blocks > 0;
+  const bool bias_in_smem = BMODE == 1 || (BMODE == 0 && BIAS && bias_smem_blocks > 0);
   if (bias_in_smem) {
-    for (int i = threadIdx.x; i < bias_smem_blocks * 8; i += kQuantThreads)
-      *reinterpret_cast<float4 *>(bias_tile + swz(i >> 3, i & 7)) = __ldg(reinterpret_cast<const float4 *>(bias) + i);
+    for (int i = threadIdx.x; i < bias_smem_blocks * 8; i += kQuantThreads) {
+      float4 f = __ldg(reinterpret_cast<const float4 *>(bias) + i);
+      if (BMODE == 1) f = make_float4(-f.x, -f.y, -f.z, -f.w);  // x - b is the identical sum x + (-b)
+      *reinterpret_cast<float4 *>(bias_tile + swz(i >> 3, i & 7)) = f;
+    }
     __syncthreads();
   }
   const bool bias_pow2 = (bias_period & (bias_period - 1)) == 0;
@@ -220,12 +230,24 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     auto sub_bias = [&](float (&x)[32]) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 f = bias_in_smem ? *reinterpret_cast<const float4 *>(bias_tile + swz(int(bb), c))
-                                      : __ldg(reinterpret_cast<const float4 *>(bias + bb * kQK) + c);
-        x[4 * c] = __fsub_rn(x[4 * c], f.x);
-        x[4 * c + 1] = __fsub_rn(x[4 * c + 1], f.y);
-        x[4 * c + 2] = __fsub_rn(x[4 * c + 2], f.z);
-        x[4 * c + 3] = __fsub_rn(x[4 * c + 3], f.w);
+        if constexpr (BMODE == 1) {
+          const float4 f = *reinterpret_cast<const float4 *>(bias_tile + swz(int(bb), c));  // -bias
+          const uint64_t a = fadd2(pack2(__float_as_uint(x[4 * c]), __float_as_uint(x[4 * c + 1])),
+                                   pack2(__float_as_uint(f.x), __float_as_uint(f.y)));
+          const uint64_t d = fadd2(pack2(__float_as_uint(x[4 * c + 2]), __float_as_uint(x[4 * c + 3])),
+                                   pack2(__float_as_uint(f.z), __float_as_uint(f.w)));
+          x[4 * c] = __uint_as_float(uint32_t(a));
+          x[4 * c + 1] = __uint_as_float(uint32_t(a >> 32));
+          x[4 * c + 2] = __uint_as_float(uint32_t(d));
+          x[4 * c + 3] = __uint_as_float(uint32_t(d >> 32));
+        } else {
+          const float4 f = (BMODE == 0 && bias_in_smem) ? *reinterpret_cast<const float4 *>(bias_tile + swz(int(bb), c))
+                                                        : __ldg(reinterpret_cast<const float4 *>(bias + bb * kQK) + c);
+          x[4 * c] = __fsub_rn(x[4 * c], f.x);
+          x[4 * c + 1] = __fsub_rn(x[4 * c + 1], f.y);
+          x[4 * c + 2] = __fsub_rn(x[4 * c + 2], f.z);
+          x[4 * c + 3] = __fsub_rn(x[4 * c + 3], f.w);
+        }
       }
     };
     if (BIAS && b < n_blocks) sub_bias(v);
@@ -256,7 +278,19 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
       // block `lane` at byte lane*BB of the consumed tile (BB = 2 mod 4: even
       // lanes start on a word, odd lanes half a word later)
       uint8_t *ob = it + lane * BB;
-      if (lane & 1) {
+      if constexpr (BMODE != 0) {
+        // branch-free: odd lanes start half a word later
+        const bool odd = lane & 1;
+        uint32_t *o32 = reinterpret_cast<uint32_t *>(ob + (odd ? 2 : 0));
+        const uint32_t sh = odd ? 32u : 16u;
+        uint32_t prev = uint32_t(scale) << 16;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+          o32[i] = __funnelshift_rc(prev, w[i], sh);
+          prev = w[i];
+        }
+        *reinterpret_cast<uint16_t *>(ob + (odd ? 0 : 4 * NW)) = odd ? scale : uint16_t(w[NW - 1] >> 16);
+      } else if (lane & 1) {
         *reinterpret_cast<uint16_t *>(ob) = scale;
 #pragma unroll
         for (int i = 0; i < NW; ++i) reinterpret_cast<uint32_t *>(ob + 2)[i] = w[i];
@@ -497,18 +531,18 @@ __global__ void __launch_bounds__(256) k_dequantize_kq(const uint8_t *__restrict
 // stream, without waiting for it (only for a launch whose memory is disjoint
 // from that launch's, the previous launch having itself waited for all
 // earlier work).
-template <int TYPE, bool BIAS, bool ROT>
-cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
-                     cudaStream_t stream, bool early = false) {
+template <int TYPE, bool BIAS, bool ROT, int BMODE = 0>
+cudaError_t launch_q_mode(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
+                          cudaStream_t stream, bool early) {
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
   const int64_t tiles = (n_blocks + 31) / 32;
   const int64_t ctas = (tiles + kQuantWarps - 1) / kQuantWarps;
   const int64_t grid = min(ctas, int64_t(di->sm_count) * 3);  // persistent: 3 resident CTAs per SM
-  const int bias_smem_blocks = (BIAS && bias_period <= kMaxSmemBiasBlocks) ? int(bias_period) : 0;
+  const int bias_smem_blocks = (BIAS && BMODE != 2 && bias_period <= kMaxSmemBiasBlocks) ? int(bias_period) : 0;
   const size_t smem = quant_smem_bytes<TYPE>(bias_smem_blocks);
-  err = ensure_smem(reinterpret_cast<const void *>(k_quantize_rows<TYPE, BIAS, ROT>), int(smem));
+  err = ensure_smem(reinterpret_cast<const void *>(k_quantize_rows<TYPE, BIAS, ROT, BMODE>), int(smem));
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -520,8 +554,23 @@ cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const flo
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = early ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_quantize_rows<TYPE, BIAS, ROT>, src, dst, n_blocks, bias, bias_period,
+  return cudaLaunchKernelEx(&cfg, k_quantize_rows<TYPE, BIAS, ROT, BMODE>, src, dst, n_blocks, bias, bias_period,
                             bias_smem_blocks);
+}
+
+// The rotated writes with a bias take instantiations specialised on where
+// the bias lives (staged negated in shared memory, added as fp32 pairs; or
+// read from global memory), the plain writes one that decides at run time.
+template <int TYPE, bool BIAS, bool ROT>
+cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
+                     cudaStream_t stream, bool early = false) {
+  if constexpr (ROT && BIAS) {
+    if (bias_period <= kMaxSmemBiasBlocks)
+      return launch_q_mode<TYPE, true, true, 1>(src, dst, n_blocks, bias, bias_period, stream, early);
+    return launch_q_mode<TYPE, true, true, 2>(src, dst, n_blocks, bias, bias_period, stream, early);
+  } else {
+    return launch_q_mode<TYPE, BIAS, ROT, 0>(src, dst, n_blocks, bias, bias_period, stream, early);
+  }
 }
 
 template <bool ROT>

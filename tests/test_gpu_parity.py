@@ -345,7 +345,9 @@ def test_kv_write_full_layer(bq, orc, dev):
 @pytest.mark.parametrize("T,NKV,D,kt,vt,basis,with_bias", [
     (1, 1, 32, Q4, Q8, 0, True), (37, 8, 128, Q4, Q8, 0, True), (1000, 8, 128, Q4, Q8, 1, True),
     (33, 3, 64, Q4, Q4, 1, False), (130, 3, 96, Q8, Q8, 0, False), (7, 2, 256, Q8, Q4, 1, False),
-    (4099, 5, 64, Q4, Q8, 0, True)])
+    (4099, 5, 64, Q4, Q8, 0, True),
+    # a bias of 160 blocks: read from global memory, in both bases
+    (9, 5, 1024, Q4, Q8, 0, True), (9, 5, 1024, Q4, Q8, 1, True)])
 def test_kv_write_layer_matches_oracle(bq, orc, dev, T, NKV, D, kt, vt, basis, with_bias):
     """bq_kv_write (K and V of a layer in one call, V's launch not waiting for
     K's): K and V bytes equal to the oracle's and to one bq_kv_quantize call
@@ -903,7 +905,9 @@ def _outlier_rows(rng, T, NKV, D):
     return K.astype(np.float32)
 
 
-@pytest.mark.parametrize("T,NKV,D", [(1, 1, 64), (33, 2, 64), (1000, 8, 128), (7, 1, 256), (130, 3, 192)])
+# (9, 5, 1024): a bias of 160 blocks, beyond the 128 staged in shared memory
+@pytest.mark.parametrize("T,NKV,D", [(1, 1, 64), (33, 2, 64), (1000, 8, 128), (7, 1, 256), (130, 3, 192),
+                                     (9, 5, 1024)])
 def test_kv_write_rotated_bit_exact(bq, orc, dev, T, NKV, D):
     rng = np.random.default_rng(T * 7 + D)
     K = _outlier_rows(rng, T, NKV, D)
