@@ -217,13 +217,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
       v[4 * c + 2] = f.z;
       v[4 * c + 3] = f.w;
     }
-    if (ROT) {
-      // rotate, and keep the rotated block in the tile for the exact path
-      hadamard64_lane_pair(v, lane);
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<float4 *>(it + swz(lane, c)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-    }
+    if (ROT) hadamard64_lane_pair(v, lane);
     const int64_t b = tile * 32 + lane;
     // block b of row (token, head) uses bias block b mod (heads * blocks per row)
     const int64_t bb = BIAS ? (bias_pow2 ? (b & (bias_period - 1)) : b % bias_period) : 0;
@@ -261,7 +255,11 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
       uint32_t w[NW];
       if (!quantize_block_words_fast<TYPE>(v, scale, w)) {
         // rare (a value near a tie, or a subnormal scale): the block again
-        // from the tile, through the exact path
+        // through the exact path (rotated: from the registers, which still
+        // hold the rotated, centred values)
+        if constexpr (ROT) {
+          quantize_block_lane_exact<TYPE>(v, scale, w);
+        } else {
         float e[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -273,6 +271,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
         }
         if (BIAS && b < n_blocks) sub_bias(e);
         quantize_block_lane_exact<TYPE>(e, scale, w);
+        }
       }
       __syncwarp();  // every lane has read its block before outputs land in the tile
       // block `lane` at byte lane*BB of the consumed tile (BB = 2 mod 4: even
