@@ -918,7 +918,8 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, a
     out["gemv_unaligned_rows"] = {"metric": "decode GEMV GB/s of weights, rows not multiples of 16 bytes (back to back)",
                                 "value": gen["Q6_K_4096x11008"]["GB/s"], "unit": "GB/s", "per_shape": gen,
                                 "kernel": "Q6_K: k_gemv_tma in 8-row quanta (+ k_gemv_prep); K % 256 != 0: "
-                                          "k_gemv_generic_prep + k_gemv_generic",
+                                          "k_gemv_generic_prep + k_gemv_staged (rows staged in shared memory by "
+                                          "async copies, a dependent launch of the prep)",
                                 "l2": "8 distinct matrices per shape, 232-384 MB: beyond L2"}
     torch.cuda.empty_cache()
 

@@ -290,13 +290,33 @@ __device__ __forceinline__ void quantize_x_generic(const float *__restrict__ x, 
   xs[9 * nb + b] = uint32_t(sum);
 }
 
+// x's records for k_gemv_generic / k_gemv_staged, 8 lanes per block (the
+// same codes, scales and sums as quantize_x_generic: one block rule), 32
+// blocks per CTA.
 __global__ void __launch_bounds__(256) k_gemv_generic_prep(const float *__restrict__ x, uint32_t *__restrict__ xg,
                                                            int nb) {
-  const int b = int(blockIdx.x) * 256 + int(threadIdx.x);
-  if (b < nb) quantize_x_generic(x, xg, nb, b);
+  // k_gemv_staged, launched as a programmatic dependent, may start streaming
+  // its rows now (it reads the records only after this launch completed)
+  pdl_launch_dependents();
+  const int b = int(blockIdx.x) * 32 + int(threadIdx.x >> 3), j = int(threadIdx.x & 7);
+  if (int(blockIdx.x) * 32 >= nb) return;  // whole CTA: the shuffles below stay converged
+  const float4 v = b < nb ? __ldg(reinterpret_cast<const float4 *>(x + int64_t(b) * kQK) + j)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+  uint16_t sc;
+  uint32_t word;
+  int sum;
+  quantize_block_8lanes(v, sc, word, sum);
+  if (b < nb) {
+    xg[8 * b + j] = word;
+    if (j == 0) {
+      xg[8 * nb + b] = __float_as_uint(half_bits_to_float(sc));
+      xg[9 * nb + b] = uint32_t(sum);
+    }
+  }
 }
 
-// Any K % 32 == 0: warp per row, lane per block, 2-byte loads. x's codes are
+// Any K % 32 == 0: warp per row, lane per block (Q4_0 / Q8_0: aligned 32-bit
+// loads, four blocks per lane in flight; the other types 2-byte loads). x's codes are
 // stored unpadded (as quantize_x_generic writes them), in shared memory:
 // quantized by the CTA itself, or copied from xg where a prep launch wrote
 // them once for the whole grid.
@@ -318,6 +338,7 @@ __global__ void __launch_bounds__(256)
   const int64_t row_bytes = IsKQuant<TYPE>::kV ? int64_t(nb / 8) * BB : int64_t(nb) * BB;
   for (int64_t m = int64_t(blockIdx.x) * 8 + warp; m < M; m += int64_t(gridDim.x) * 8) {
     float acc = 0.0f;
+    if constexpr (TYPE != kTypeQ4_0 && TYPE != kTypeQ8_0)
     for (int b = lane; b < nb; b += 32) {
       if constexpr (IsKQuant<TYPE>::kV) {
         // x block b meets sub-block(s) of super-block b / 8
@@ -376,25 +397,150 @@ __global__ void __launch_bounds__(256)
         const float dx = __uint_as_float(xs[8 * nb + b]);
         acc = __fmaf_rn(__fmul_rn(half_bits_to_float(blk[0]), dx), float(sumi), acc);
         if (L::kAffine) acc = __fmaf_rn(__fmul_rn(half_bits_to_float(blk[1]), dx), float(xsum), acc);
-        continue;
       }
+    }
+    if constexpr (TYPE == kTypeQ4_0 || TYPE == kTypeQ8_0) {
+      // A block starts 2-byte aligned (BB = 2 mod 4): it is read as the
+      // aligned 32-bit words that cover it, kQW + 1 of them, and realigned
+      // with one clamped funnel shift per word. A block that starts on a
+      // word ends half a word into its last one, which is then read with a
+      // 16-bit load (nothing past the block is read). The lane's blocks are
+      // taken kU at a time, all their loads issued before any is used.
       constexpr int kQW = (TYPE == kTypeQ4_0) ? 4 : 8;
+      constexpr int kU = 4;
+      const uint8_t *row = W + m * row_bytes;
+      for (int b0 = lane; b0 < nb; b0 += 32 * kU) {
+        uint32_t raw[kU][kQW + 1];
+        uint32_t half[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int b = b0 + 32 * u;
+          const uintptr_t a = reinterpret_cast<uintptr_t>(row + int64_t(b < nb ? b : 0) * BB);
+          const uint32_t *wp = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
+          half[u] = uint32_t(a & 2);
+#pragma unroll
+          for (int i = 0; i < kQW; ++i) raw[u][i] = b < nb ? __ldg(wp + i) : 0u;
+          raw[u][kQW] = b >= nb ? 0u
+                        : half[u] ? __ldg(wp + kQW)
+                                  : uint32_t(__ldg(reinterpret_cast<const uint16_t *>(wp + kQW)));
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int b = b0 + 32 * u;
+          if (b >= nb) break;
+          // scale: bytes 0-1 of the block; codes: from byte 2
+          const uint32_t sh = half[u] ? 32u : 16u;
+          uint32_t q[kQW];
+#pragma unroll
+          for (int i = 0; i < kQW; ++i) q[i] = __funnelshift_rc(raw[u][i], raw[u][i + 1], sh);
+          const uint32_t sbits = (half[u] ? (raw[u][0] >> 16) : raw[u][0]) & 0xffffu;
+          const uint32_t *xw = xs + 8 * b;
+          int sumi;
+          if (TYPE == kTypeQ4_0)
+            sumi = sumi_q4_q8(q, xw, int(xs[9 * nb + b]));
+          else
+            sumi = sumi_q8_q8(q, xw);
+          const float s = __fmul_rn(half_bits_to_float(uint16_t(sbits)), __uint_as_float(xs[8 * nb + b]));
+          acc = __fmaf_rn(s, float(sumi), acc);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+    if (lane == 0) y[m] = acc;
+  }
+}
+
+// Q4_0 / Q8_0 rows that are not multiples of 16 bytes (K % 256 != 0): warp
+// per row, the row staged in shared memory by 16-byte asynchronous copies of
+// the aligned chunks that cover it, two row buffers per warp (the next row's
+// copies in flight, holding no registers, while the current row's dot
+// products run: lane per block, each block read as the aligned 32-bit words
+// that cover it and realigned with one clamped funnel shift per word). The
+// matrix's last chunk copies only the matrix's bytes. x's records (as
+// quantize_x_generic writes them) come from the workspace, where a prep
+// launch wrote them once: quantizing x in the CTA would cost the row loop
+// registers (64 here, four CTAs per SM).
+__device__ __forceinline__ void cp_async16_n(void *dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// shared-memory bytes of one row buffer: the covering chunks and one word of
+// slack (a lane's last word may reach 2 bytes past its block)
+__host__ __device__ constexpr int staged_row_buf(int64_t row_bytes) { return int((row_bytes + 15 + 15) / 16 * 16 + 16); }
+__host__ __device__ constexpr int staged_xs_bytes(int nb) { return (40 * nb + 15) / 16 * 16; }
+
+template <int TYPE>
+__global__ void __launch_bounds__(256, 4)
+    k_gemv_staged(const uint8_t *__restrict__ W, const uint32_t *__restrict__ xg, float *__restrict__ y, int M,
+                  int K) {
+  constexpr int BB = Fmt<TYPE>::kBytes;
+  constexpr int kQW = (TYPE == kTypeQ4_0) ? 4 : 8;
+  extern __shared__ __align__(16) uint32_t xs[];
+  const int nb = K / kQK;
+  const int64_t row_bytes = int64_t(nb) * BB;
+  const int row_buf = staged_row_buf(row_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *buf0 = reinterpret_cast<uint8_t *>(xs) + staged_xs_bytes(nb) + size_t(warp) * 2 * row_buf;
+  uint8_t *buf1 = buf0 + row_buf;
+  const uint8_t *end = W + int64_t(M) * row_bytes;
+  const int64_t stride = int64_t(gridDim.x) * 8;
+  // row m's covering chunks into buf (one commit group, empty past the last row)
+  auto issue = [&](int64_t m, uint8_t *buf) {
+    if (m < M) {
+      const uint8_t *a = W + m * row_bytes;
+      const uint8_t *a16 = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(15));
+      const int n16 = int((a + row_bytes - a16 + 15) / 16);
+      for (int i = lane; i < n16; i += 32) {
+        const uint8_t *src = a16 + 16 * i;
+        const int64_t left = end - src;
+        cp_async16_n(buf + 16 * i, src, left >= 16 ? 16 : int(left));
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  int64_t m = int64_t(blockIdx.x) * 8 + warp;
+  // the first two rows' copies go out while the prep launch (a normal launch,
+  // after all earlier work; it writes only the records) may still run
+  issue(m, buf0);
+  pdl_wait();
+  for (int i = threadIdx.x; i < 10 * nb; i += blockDim.x) xs[i] = __ldcg(xg + i);
+  __syncthreads();
+  for (int k = 0; m < M; m += stride, k ^= 1) {
+    const uint8_t *cur = k ? buf1 : buf0;
+    issue(m + stride, k ? buf0 : buf1);
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncwarp();
+    const int s16 = int(reinterpret_cast<uintptr_t>(W + m * row_bytes) & 15);
+    float acc = 0.0f;
+#pragma unroll 1
+    for (int b = lane; b < nb; b += 32) {
+      const int o = s16 + b * BB;  // 2-byte aligned
+      const uint32_t *wp = reinterpret_cast<const uint32_t *>(cur + (o & ~3));
+      const uint32_t sh = (o & 2) ? 32u : 16u;
+      uint32_t raw[kQW + 1];
+#pragma unroll
+      for (int i = 0; i <= kQW; ++i) raw[i] = wp[i];
       uint32_t q[kQW];
 #pragma unroll
-      for (int i = 0; i < kQW; ++i) q[i] = uint32_t(blk[1 + 2 * i]) | (uint32_t(blk[2 + 2 * i]) << 16);
+      for (int i = 0; i < kQW; ++i) q[i] = __funnelshift_rc(raw[i], raw[i + 1], sh);
+      const uint32_t sbits = ((o & 2) ? (raw[0] >> 16) : raw[0]) & 0xffffu;
       const uint32_t *xw = xs + 8 * b;
       int sumi;
       if (TYPE == kTypeQ4_0)
         sumi = sumi_q4_q8(q, xw, int(xs[9 * nb + b]));
       else
         sumi = sumi_q8_q8(q, xw);
-      const float s = __fmul_rn(half_bits_to_float(blk[0]), __uint_as_float(xs[8 * nb + b]));
-      acc = __fmaf_rn(s, float(sumi), acc);
+      const float sc = __fmul_rn(half_bits_to_float(uint16_t(sbits)), __uint_as_float(xs[8 * nb + b]));
+      acc = __fmaf_rn(sc, float(sumi), acc);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
     if (lane == 0) y[m] = acc;
+    __syncwarp();  // every lane has read the buffer before the copies after next refill it
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
 }
 
 int next_pow2(int v) {
@@ -557,13 +703,46 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
   if (e != cudaSuccess) return e;
   const uint32_t *xg = nullptr;
   if (rec_ws) {
-    k_gemv_generic_prep<<<unsigned((nb + 255) / 256), 256, 0, stream>>>(x, rec_ws, nb);
+    k_gemv_generic_prep<<<unsigned((nb + 31) / 32), 256, 0, stream>>>(x, rec_ws, nb);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     xg = rec_ws;
   }
+  // Q4_0 / Q8_0 with x's records in the workspace: rows staged in shared
+  // memory when two row buffers per warp fit
+  const size_t staged_smem = size_t(staged_xs_bytes(int(nb))) + size_t(16) * staged_row_buf(nb * BB);
+  constexpr bool kStagedType = TYPE == kTypeQ4_0 || TYPE == kTypeQ8_0;
+  const bool staged = kStagedType && xg && staged_smem <= size_t(di->max_smem_optin);
+  const void *fn = reinterpret_cast<const void *>(k_gemv_generic<TYPE>);
+  if constexpr (kStagedType)
+    if (staged) fn = reinterpret_cast<const void *>(k_gemv_staged<TYPE>);
+  const size_t fsmem = staged ? staged_smem : smem;
+  if (staged && (e = ensure_smem(fn, int(fsmem))) != cudaSuccess) return e;
+  // one wave of CTAs (8 rows each in flight), as many per SM as are resident
+  int per_sm = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256, fsmem)) != cudaSuccess) return e;
+  per_sm = std::max(per_sm, 1);
   for (int i = 0; i < n; ++i) {
     if (M[i] == 0) continue;
-    const int64_t grid = std::min((M[i] + 7) / 8, int64_t(di->sm_count) * 4);
+    const int64_t grid = std::min((M[i] + 7) / 8, int64_t(di->sm_count) * per_sm);
+    if constexpr (kStagedType)
+      if (staged) {
+        // a programmatic dependent of the prep launch (for i > 0, of the
+        // previous matrix's launch, whose completion implies the prep's)
+        cudaLaunchAttribute sattr[1];
+        sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        sattr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t sc = {};
+        sc.gridDim = dim3(unsigned(grid));
+        sc.blockDim = dim3(256);
+        sc.dynamicSmemBytes = fsmem;
+        sc.stream = stream;
+        sc.attrs = sattr;
+        sc.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&sc, k_gemv_staged<TYPE>, static_cast<const uint8_t *>(W[i]),
+                                    static_cast<const uint32_t *>(xg), y[i], int(M[i]), int(K))) != cudaSuccess)
+          return e;
+        continue;
+      }
     k_gemv_generic<TYPE><<<unsigned(grid), 256, smem, stream>>>(W[i], x, xg, y[i], int(M[i]), int(K));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

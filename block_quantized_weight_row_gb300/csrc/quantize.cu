@@ -163,7 +163,7 @@ size_t quant_smem_bytes(int64_t bias_smem_blocks) {
 template <int TYPE, bool BIAS, bool ROT, int BMODE = 0>
 __global__ void __launch_bounds__(kQuantThreads, 3)
     k_quantize_rows(const float *__restrict__ src, uint8_t *__restrict__ dst, int64_t n_blocks,
-                    const float *__restrict__ bias, int64_t bias_period, int bias_smem_blocks) {
+                    const float *__restrict__ bias, int64_t bias_period, int bias_smem_blocks, int pair) {
   constexpr int BB = Fmt<TYPE>::kBytes;
   constexpr int NW = TYPE == kTypeQ4_0 ? 4 : 8;  // code words per block (Q4_0 / Q8_0)
   constexpr int kTile = 32 * 128;
@@ -183,10 +183,12 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     __syncthreads();
   }
   const bool bias_pow2 = (bias_period & (bias_period - 1)) == 0;
-  // a launch that follows as a programmatic dependent (the other half of a
-  // one-layer KV write) may be scheduled at once: it touches none of this
-  // launch's memory, and its CTAs take the SMs this grid's CTAs leave
-  pdl_launch_dependents();
+  // the first launch of a one-layer KV write lets the second (the other
+  // tensor) be scheduled at once: it touches none of this launch's memory,
+  // and its CTAs take the SMs this grid's CTAs leave. No other launch does:
+  // a dependent GEMV streams its weights before its dependency wait, and
+  // these may be the rows this launch writes.
+  if (pair == 1) pdl_launch_dependents();
   const int64_t total_warps = int64_t(gridDim.x) * kQuantWarps;
   // coalesced: vector i = lane + 32c of a tile is chunk (i & 7) of block (i >> 3)
   auto issue_tile = [&](int64_t t, uint8_t *buf) {
@@ -313,6 +315,9 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
     __syncwarp();  // the next iteration refills this buffer
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy in flight at exit
+  // the second launch of the pair ends only after the first has completed,
+  // so that whatever follows on the stream is ordered after both
+  if (pair == 2) pdl_wait();
 }
 
 // x_hat = scale * q, exact in fp32. One thread per 4 outputs.
@@ -526,13 +531,14 @@ __global__ void __launch_bounds__(256) k_dequantize_kq(const uint8_t *__restrict
   }
 }
 
-// early: launched as a programmatic dependent of the previous launch on the
-// stream, without waiting for it (only for a launch whose memory is disjoint
-// from that launch's, the previous launch having itself waited for all
-// earlier work).
+// pair: 0 a launch of its own; 1 the first launch of a one-layer KV write
+// (lets the second start at once); 2 the second: launched as a programmatic
+// dependent of the first without waiting for it to start work (their memory
+// is disjoint, and the first waited for all earlier work), and waiting for
+// it to complete before ending.
 template <int TYPE, bool BIAS, bool ROT, int BMODE = 0>
 cudaError_t launch_q_mode(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
-                          cudaStream_t stream, bool early) {
+                          cudaStream_t stream, int pair) {
   cudaError_t err;
   const DeviceInfo *di = device_info(&err);
   if (!di) return err;
@@ -552,9 +558,9 @@ cudaError_t launch_q_mode(const float *src, uint8_t *dst, int64_t n_blocks, cons
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = early ? 1 : 0;
+  cfg.numAttrs = pair == 2 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, k_quantize_rows<TYPE, BIAS, ROT, BMODE>, src, dst, n_blocks, bias, bias_period,
-                            bias_smem_blocks);
+                            bias_smem_blocks, pair);
 }
 
 // The rotated writes with a bias take instantiations specialised on where
@@ -562,13 +568,13 @@ cudaError_t launch_q_mode(const float *src, uint8_t *dst, int64_t n_blocks, cons
 // read from global memory), the plain writes one that decides at run time.
 template <int TYPE, bool BIAS, bool ROT>
 cudaError_t launch_q(const float *src, uint8_t *dst, int64_t n_blocks, const float *bias, int64_t bias_period,
-                     cudaStream_t stream, bool early = false) {
+                     cudaStream_t stream, int pair = 0) {
   if constexpr (ROT && BIAS) {
     if (bias_period <= kMaxSmemBiasBlocks)
-      return launch_q_mode<TYPE, true, true, 1>(src, dst, n_blocks, bias, bias_period, stream, early);
-    return launch_q_mode<TYPE, true, true, 2>(src, dst, n_blocks, bias, bias_period, stream, early);
+      return launch_q_mode<TYPE, true, true, 1>(src, dst, n_blocks, bias, bias_period, stream, pair);
+    return launch_q_mode<TYPE, true, true, 2>(src, dst, n_blocks, bias, bias_period, stream, pair);
   } else {
-    return launch_q_mode<TYPE, BIAS, ROT, 0>(src, dst, n_blocks, bias, bias_period, stream, early);
+    return launch_q_mode<TYPE, BIAS, ROT, 0>(src, dst, n_blocks, bias, bias_period, stream, pair);
   }
 }
 
@@ -597,24 +603,24 @@ cudaError_t launch_q_typed(int type, const float *src, uint8_t *dst, int64_t n_b
 cudaError_t launch_kv_write_pair(int k_type, int v_type, bool k_rot, const float *k_src, uint8_t *k_dst,
                                  const float *v_src, uint8_t *v_dst, int64_t n_blocks, const float *bias,
                                  int64_t bias_period, cudaStream_t stream) {
-  auto launch_k = [&](bool early) {
+  auto launch_k = [&](int pair) {
     if (k_type == kTypeQ4_0) {
       if (bias)
-        return k_rot ? launch_q<kTypeQ4_0, true, true>(k_src, k_dst, n_blocks, bias, bias_period, stream, early)
-                     : launch_q<kTypeQ4_0, true, false>(k_src, k_dst, n_blocks, bias, bias_period, stream, early);
-      return k_rot ? launch_q<kTypeQ4_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream, early)
-                   : launch_q<kTypeQ4_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream, early);
+        return k_rot ? launch_q<kTypeQ4_0, true, true>(k_src, k_dst, n_blocks, bias, bias_period, stream, pair)
+                     : launch_q<kTypeQ4_0, true, false>(k_src, k_dst, n_blocks, bias, bias_period, stream, pair);
+      return k_rot ? launch_q<kTypeQ4_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream, pair)
+                   : launch_q<kTypeQ4_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream, pair);
     }
-    return k_rot ? launch_q<kTypeQ8_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream, early)
-                 : launch_q<kTypeQ8_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream, early);
+    return k_rot ? launch_q<kTypeQ8_0, false, true>(k_src, k_dst, n_blocks, nullptr, 1, stream, pair)
+                 : launch_q<kTypeQ8_0, false, false>(k_src, k_dst, n_blocks, nullptr, 1, stream, pair);
   };
-  auto launch_v = [&](bool early) {
-    return v_type == kTypeQ4_0 ? launch_q<kTypeQ4_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, early)
-                               : launch_q<kTypeQ8_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, early);
+  auto launch_v = [&](int pair) {
+    return v_type == kTypeQ4_0 ? launch_q<kTypeQ4_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, pair)
+                               : launch_q<kTypeQ8_0, false, false>(v_src, v_dst, n_blocks, nullptr, 1, stream, pair);
   };
-  cudaError_t e = k_rot ? launch_v(false) : launch_k(false);
+  cudaError_t e = k_rot ? launch_v(1) : launch_k(1);
   if (e != cudaSuccess) return e;
-  return k_rot ? launch_k(true) : launch_v(true);
+  return k_rot ? launch_k(2) : launch_v(2);
 }
 
 // bias[h][c] = fp32(sum_t r_t[h][c] / n_tokens), the sum in fp64 in token

@@ -556,6 +556,37 @@ def test_gemv_both_activation_paths(bq, orc, dev, t, with_ws, Ms, K):
         _check_float(_np(outs[i]), y_ref, mag, f"matrix {i}, workspace={with_ws}")
 
 
+@pytest.mark.parametrize("t", [Q4, Q8])
+@pytest.mark.parametrize("Ms,K", [([33, 500], 4128), ([5], 96), ([4096], 4128), ([3, 1], 32)])
+def test_gemv_unaligned_rows_both_paths_bit_identical(bq, orc, dev, t, Ms, K):
+    """Rows that are not multiples of 16 bytes (K % 256 != 0): with a
+    workspace, x's records come from the 8-lane prep launch and the rows are
+    staged in shared memory; without, every CTA quantizes x one block per
+    thread and reads the rows from global memory. The same records and the
+    same order of terms: identical bits."""
+    import ctypes
+    from block_quantized_weight_row_gb300 import binding, inputs
+    L = binding.lib()
+    x = inputs.activation(K, seed=K + 11).to(dev)
+    w_dev = [bq.quantize_rows(t, inputs.weight(m, K, seed=3000 + 7 * i + m, device=dev)) for i, m in enumerate(Ms)]
+    ws = torch.empty(max(256, int(L.bq_gemv_workspace_size(t, K))), dtype=torch.uint8, device=dev)
+    res = []
+    for with_ws in (True, False):
+        outs = [torch.full((m,), float("nan"), device=dev) for m in Ms]
+        torch.cuda.synchronize()
+        assert L.bq_set_stream(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+        assert L.bq_set_workspace(ctypes.c_void_p(ws.data_ptr()) if with_ws else None, ws.numel() if with_ws else 0) == 0
+        n, W, Y, M = binding.gemv_multi_args(w_dev, outs, Ms)
+        assert L.bq_gemv_multi(t, n, W, Y, M, ctypes.c_void_p(x.data_ptr()), K) == 0, L.bq_last_error()
+        torch.cuda.synchronize()
+        res.append(outs)
+    L.bq_set_workspace(None, 0)
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+    y_ref, mag = orc.gemv(t, _np(w_dev[0]), _np(x), Ms[0], K, with_mag=True)
+    _check_float(_np(res[0][0]), y_ref, mag, "with the workspace")
+
+
 def test_gemv_large_launch_three_stage_ring(bq, orc, dev):
     """A launch of more than 64 MB of weights (three 11008 x 4096 Q4_0
     matrices, 76 MB) runs with a three-stage ring: it matches the oracle and
