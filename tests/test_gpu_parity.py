@@ -587,6 +587,35 @@ def test_gemv_unaligned_rows_both_paths_bit_identical(bq, orc, dev, t, Ms, K):
     _check_float(_np(res[0][0]), y_ref, mag, "with the workspace")
 
 
+def test_gemv_with_weight_prefetch_right_after_quantizing_its_weights(bq, orc, dev):
+    """With weight prefetch on, a GEMV may stream its weights before the
+    previous launch has completed; a row quantization of those weights just
+    before it must still have finished first (it lets no dependent start
+    early). Four rounds quantize new weights into the same buffer and run the
+    GEMV at once, without a sync: each output matches the oracle for its
+    round's weights."""
+    from block_quantized_weight_row_gb300 import binding, inputs
+    M, K = 4096, 4096
+    x = inputs.activation(K, seed=91, device=dev)
+    wq = torch.empty((M, K // 32 * 18), dtype=torch.uint8, device=dev)
+    ws = [inputs.weight(M, K, seed=900 + i, device=dev) for i in range(4)]
+    ys = [torch.full((M,), float("nan"), device=dev) for _ in ws]
+    torch.cuda.synchronize()
+    binding.set_weight_prefetch(True)
+    try:
+        for W, y in zip(ws, ys):
+            bq.quantize_rows(Q4, W, out=wq)
+            bq.gemv(Q4, wq, x, M, K, out=y)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_weight_prefetch(False)
+    xn = _np(x)
+    for i, (W, y) in enumerate(zip(ws, ys)):
+        w_ref = orc.quantize_rows(Q4, _np(W))
+        y_ref, mag = orc.gemv(Q4, w_ref, xn, M, K, with_mag=True)
+        _check_float(_np(y), y_ref, mag, f"round {i}")
+
+
 def test_gemv_large_launch_three_stage_ring(bq, orc, dev):
     """A launch of more than 64 MB of weights (three 11008 x 4096 Q4_0
     matrices, 76 MB) runs with a three-stage ring: it matches the oracle and
