@@ -894,12 +894,13 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, a
     torch.cuda.empty_cache()
 
     # shapes whose rows are not whole multiples of 16 bytes: Q6_K down-projection
-    # rows (K = 11008: bulk copies of whole 8-row quanta) and Q4_0 / Q8_0 with
-    # K = 4128, not a multiple of 256 (the generic kernel, x quantized once
-    # into the workspace)
+    # rows (K = 11008: bulk copies of whole 8-row quanta) and Q4_0 / Q8_0 and
+    # the legacy types with K = 4128, not a multiple of 256 (rows staged in
+    # shared memory, x quantized once into the workspace)
     gen = {}
     for name, t, M_, K_ in (("Q6_K_4096x11008", bq.Q6_K, 4096, 11008), ("Q4_0_11008x4128", bq.Q4_0, 11008, 4128),
-                            ("Q8_0_11008x4128", bq.Q8_0, 11008, 4128)):
+                            ("Q8_0_11008x4128", bq.Q8_0, 11008, 4128), ("Q4_1_11008x4128", bq.Q4_1, 11008, 4128),
+                            ("Q5_0_11008x4128", bq.Q5_0, 11008, 4128), ("Q5_1_11008x4128", bq.Q5_1, 11008, 4128)):
         x_ = inputs.activation(K_, inputs.seed_of("legacy-gemv", 2, 0), device=dev)
         y_ = torch.empty(M_, dtype=torch.float32, device=dev)
         mats = [bq.quantize_rows(t, inputs.weight(M_, K_, inputs.seed_of("legacy-gemv", 3, i), device=dev))
@@ -920,7 +921,7 @@ def secondary_rows(bq, binding, inputs, dev, stream, peaks, dist, world, step, a
                                 "kernel": "Q6_K: k_gemv_tma in 8-row quanta (+ k_gemv_prep); K % 256 != 0: "
                                           "k_gemv_generic_prep + k_gemv_staged (rows staged in shared memory by "
                                           "async copies, a dependent launch of the prep)",
-                                "l2": "8 distinct matrices per shape, 232-384 MB: beyond L2"}
+                                "l2": "8 distinct matrices per shape, 204-384 MB: beyond L2"}
     torch.cuda.empty_cache()
 
     # Qwen3-0.6B-shaped decode step (247.7 MB of Q4_0), L2 flushed between steps

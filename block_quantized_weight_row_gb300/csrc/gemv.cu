@@ -451,12 +451,13 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Q4_0 / Q8_0 rows that are not multiples of 16 bytes (K % 256 != 0): warp
-// per row, the row staged in shared memory by 16-byte asynchronous copies of
+// Rows that are not multiples of 16 bytes (K % 256 != 0) of Q4_0, Q8_0 and
+// the legacy types: warp per row, the row staged in shared memory by 16-byte asynchronous copies of
 // the aligned chunks that cover it, two row buffers per warp (the next row's
 // copies in flight, holding no registers, while the current row's dot
-// products run: lane per block, each block read as the aligned 32-bit words
-// that cover it and realigned with one clamped funnel shift per word). The
+// products run: lane per block; a Q4_0 / Q8_0 block read as the aligned
+// 32-bit words that cover it and realigned with one clamped funnel shift per
+// word, a legacy block by 16-bit shared loads). The
 // matrix's last chunk copies only the matrix's bytes. x's records (as
 // quantize_x_generic writes them) come from the workspace, where a prep
 // launch wrote them once: quantizing x in the CTA would cost the row loop
@@ -476,7 +477,7 @@ __global__ void __launch_bounds__(256, 4)
     k_gemv_staged(const uint8_t *__restrict__ W, const uint32_t *__restrict__ xg, float *__restrict__ y, int M,
                   int K) {
   constexpr int BB = Fmt<TYPE>::kBytes;
-  constexpr int kQW = (TYPE == kTypeQ4_0) ? 4 : 8;
+  constexpr int kQW = (TYPE == kTypeQ4_0) ? 4 : 8;  // Q4_0 / Q8_0 code words (the legacy types: below)
   extern __shared__ __align__(16) uint32_t xs[];
   const int nb = K / kQK;
   const int64_t row_bytes = int64_t(nb) * BB;
@@ -517,6 +518,23 @@ __global__ void __launch_bounds__(256, 4)
 #pragma unroll 1
     for (int b = lane; b < nb; b += 32) {
       const int o = s16 + b * BB;  // 2-byte aligned
+      if constexpr (Legacy<TYPE>::kIs) {
+        // the legacy types' blocks by 16-bit shared loads (the same terms as
+        // k_gemv_generic)
+        using L = Legacy<TYPE>;
+        const uint16_t *blk = reinterpret_cast<const uint16_t *>(cur + o);
+        uint32_t qs[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qs[i] = uint32_t(blk[L::kQs / 2 + 2 * i]) | (uint32_t(blk[L::kQs / 2 + 2 * i + 1]) << 16);
+        const uint32_t qh = L::kQh >= 0 ? (uint32_t(blk[L::kQh / 2]) | (uint32_t(blk[L::kQh / 2 + 1]) << 16)) : 0u;
+        const int xsum = int(xs[9 * nb + b]);
+        int sumi = legacy_sumu<TYPE>(qs, qh, xs + 8 * b);
+        if (!L::kAffine) sumi -= 16 * xsum;
+        const float dx = __uint_as_float(xs[8 * nb + b]);
+        acc = __fmaf_rn(__fmul_rn(half_bits_to_float(blk[0]), dx), float(sumi), acc);
+        if (L::kAffine) acc = __fmaf_rn(__fmul_rn(half_bits_to_float(blk[1]), dx), float(xsum), acc);
+        continue;
+      }
       const uint32_t *wp = reinterpret_cast<const uint32_t *>(cur + (o & ~3));
       const uint32_t sh = (o & 2) ? 32u : 16u;
       uint32_t raw[kQW + 1];
@@ -707,10 +725,10 @@ cudaError_t launch_typed(int n, const uint8_t *const *W, float *const *y, const 
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     xg = rec_ws;
   }
-  // Q4_0 / Q8_0 with x's records in the workspace: rows staged in shared
-  // memory when two row buffers per warp fit
+  // Q4_0, Q8_0 and the legacy types with x's records in the workspace: rows
+  // staged in shared memory when two row buffers per warp fit
   const size_t staged_smem = size_t(staged_xs_bytes(int(nb))) + size_t(16) * staged_row_buf(nb * BB);
-  constexpr bool kStagedType = TYPE == kTypeQ4_0 || TYPE == kTypeQ8_0;
+  constexpr bool kStagedType = !IsKQuant<TYPE>::kV;
   const bool staged = kStagedType && xg && staged_smem <= size_t(di->max_smem_optin);
   const void *fn = reinterpret_cast<const void *>(k_gemv_generic<TYPE>);
   if constexpr (kStagedType)

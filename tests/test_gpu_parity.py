@@ -556,7 +556,7 @@ def test_gemv_both_activation_paths(bq, orc, dev, t, with_ws, Ms, K):
         _check_float(_np(outs[i]), y_ref, mag, f"matrix {i}, workspace={with_ws}")
 
 
-@pytest.mark.parametrize("t", [Q4, Q8])
+@pytest.mark.parametrize("t", [Q4, Q8, 3, 6, 7])
 @pytest.mark.parametrize("Ms,K", [([33, 500], 4128), ([5], 96), ([4096], 4128), ([3, 1], 32)])
 def test_gemv_unaligned_rows_both_paths_bit_identical(bq, orc, dev, t, Ms, K):
     """Rows that are not multiples of 16 bytes (K % 256 != 0): with a
