@@ -456,7 +456,8 @@ def main():
     ap.add_argument("--no-batch", action="store_true",
                     help="per-launch path: one launch per matrix instead of one per batch sharing an input")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "seq", "gemm", "kv", "attn"), default=None,
+    ap.add_argument("--kernel-case", choices=("gemv", "gemv-q8", "gemv-unaligned", "seq", "gemm", "kv", "attn"),
+                    default=None,
                     help="run one kernel case a few times and exit (for profiler captures)")
     ap.add_argument("--case-launches", type=int, default=16)
     ap.add_argument("--probe", choices=("bulk", "rates"), default=None,
@@ -986,9 +987,9 @@ def kernel_case(name, launches):
     from block_quantized_weight_row_gb300 import inputs
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if name in ("gemv", "gemv-q8"):
-        t = bq.Q4_0 if name == "gemv" else bq.Q8_0
-        M, K = 11008, 4096
+    if name in ("gemv", "gemv-q8", "gemv-unaligned"):
+        t = bq.Q8_0 if name == "gemv-q8" else bq.Q4_0
+        M, K = 11008, 4128 if name == "gemv-unaligned" else 4096
         mats = []
         for i in range(8):  # 8 x 25.4 MB (Q4_0) or 48 MB (Q8_0): beyond L2
             mats.append(bq.quantize_rows(t, inputs.weight(M, K, 7000 + i, device=dev)))
