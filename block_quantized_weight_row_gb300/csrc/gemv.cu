@@ -506,7 +506,10 @@ __global__ void __launch_bounds__(256, 4)
   // after all earlier work; it writes only the records) may still run
   issue(m, buf0);
   pdl_wait();
-  for (int i = threadIdx.x; i < 10 * nb; i += blockDim.x) xs[i] = __ldcg(xg + i);
+  // x's records, the code words transposed to [word][block] so that the
+  // lanes' loads of consecutive blocks hit consecutive banks
+  for (int i = threadIdx.x; i < 8 * nb; i += blockDim.x) xs[(i & 7) * nb + (i >> 3)] = __ldcg(xg + i);
+  for (int i = 8 * nb + threadIdx.x; i < 10 * nb; i += blockDim.x) xs[i] = __ldcg(xg + i);
   __syncthreads();
   for (int k = 0; m < M; m += stride, k ^= 1) {
     const uint8_t *cur = k ? buf1 : buf0;
@@ -527,8 +530,11 @@ __global__ void __launch_bounds__(256, 4)
 #pragma unroll
         for (int i = 0; i < 4; ++i) qs[i] = uint32_t(blk[L::kQs / 2 + 2 * i]) | (uint32_t(blk[L::kQs / 2 + 2 * i + 1]) << 16);
         const uint32_t qh = L::kQh >= 0 ? (uint32_t(blk[L::kQh / 2]) | (uint32_t(blk[L::kQh / 2 + 1]) << 16)) : 0u;
+        uint32_t xv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xv[i] = xs[i * nb + b];
         const int xsum = int(xs[9 * nb + b]);
-        int sumi = legacy_sumu<TYPE>(qs, qh, xs + 8 * b);
+        int sumi = legacy_sumu<TYPE>(qs, qh, xv);
         if (!L::kAffine) sumi -= 16 * xsum;
         const float dx = __uint_as_float(xs[8 * nb + b]);
         acc = __fmaf_rn(__fmul_rn(half_bits_to_float(blk[0]), dx), float(sumi), acc);
@@ -544,7 +550,9 @@ __global__ void __launch_bounds__(256, 4)
 #pragma unroll
       for (int i = 0; i < kQW; ++i) q[i] = __funnelshift_rc(raw[i], raw[i + 1], sh);
       const uint32_t sbits = ((o & 2) ? (raw[0] >> 16) : raw[0]) & 0xffffu;
-      const uint32_t *xw = xs + 8 * b;
+      uint32_t xw[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xw[i] = xs[i * nb + b];
       int sumi;
       if (TYPE == kTypeQ4_0)
         sumi = sumi_q4_q8(q, xw, int(xs[9 * nb + b]));
