@@ -262,17 +262,17 @@ __global__ void __launch_bounds__(kQuantThreads, 3)
         if constexpr (ROT) {
           quantize_block_lane_exact<TYPE>(v, scale, w);
         } else {
-        float e[32];
+          float e[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 f = *reinterpret_cast<const float4 *>(it + swz(lane, c));
-          e[4 * c] = f.x;
-          e[4 * c + 1] = f.y;
-          e[4 * c + 2] = f.z;
-          e[4 * c + 3] = f.w;
-        }
-        if (BIAS && b < n_blocks) sub_bias(e);
-        quantize_block_lane_exact<TYPE>(e, scale, w);
+          for (int c = 0; c < 8; ++c) {
+            const float4 f = *reinterpret_cast<const float4 *>(it + swz(lane, c));
+            e[4 * c] = f.x;
+            e[4 * c + 1] = f.y;
+            e[4 * c + 2] = f.z;
+            e[4 * c + 3] = f.w;
+          }
+          if (BIAS && b < n_blocks) sub_bias(e);
+          quantize_block_lane_exact<TYPE>(e, scale, w);
         }
       }
       __syncwarp();  // every lane has read its block before outputs land in the tile
