@@ -452,16 +452,17 @@ __global__ void __launch_bounds__(256)
 }
 
 // Rows that are not multiples of 16 bytes (K % 256 != 0) of Q4_0, Q8_0 and
-// the legacy types: warp per row, the row staged in shared memory by 16-byte asynchronous copies of
-// the aligned chunks that cover it, two row buffers per warp (the next row's
-// copies in flight, holding no registers, while the current row's dot
-// products run: lane per block; a Q4_0 / Q8_0 block read as the aligned
+// the legacy types: warp per row, the row staged in shared memory by 16-byte
+// asynchronous copies of the aligned chunks that cover it (the matrix's last
+// chunk copies only the matrix's bytes), two row buffers per warp: the next
+// row's copies are in flight, holding no registers, while the current row's
+// dot products run, lane per block (a Q4_0 / Q8_0 block read as the aligned
 // 32-bit words that cover it and realigned with one clamped funnel shift per
-// word, a legacy block by 16-bit shared loads). The
-// matrix's last chunk copies only the matrix's bytes. x's records (as
+// word, a legacy block by 16-bit shared loads). x's records (as
 // quantize_x_generic writes them) come from the workspace, where a prep
-// launch wrote them once: quantizing x in the CTA would cost the row loop
-// registers (64 here, four CTAs per SM).
+// launch wrote them once: quantizing x in every CTA measured slower, and the
+// one-lane-per-block quantizer would cost the row loop registers (at most 64
+// here, for four or more CTAs per SM).
 __device__ __forceinline__ void cp_async16_n(void *dst, const void *src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                : "memory");
@@ -502,7 +503,7 @@ __global__ void __launch_bounds__(256, 4)
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
   int64_t m = int64_t(blockIdx.x) * 8 + warp;
-  // the first two rows' copies go out while the prep launch (a normal launch,
+  // the first row's copies go out while the prep launch (a normal launch,
   // after all earlier work; it writes only the records) may still run
   issue(m, buf0);
   pdl_wait();
