@@ -908,8 +908,10 @@ def _attn_case(orc, T, H, NKV, D, kt, vt, seed, centered=False):
     # of two, and eight heads per kv head at head_dim 256, take the
     # block-wide kernel
     (333, 4, 4, 96, Q4, Q8), (517, 6, 3, 64, Q4, Q8), (300, 16, 2, 256, Q8, Q4),
-    # over 1024 chunks: the combine takes its chunks in two rounds
-    (600000, 2, 1, 32, Q4, Q8)])
+    # over 1024 chunks: the combine takes its chunks in two rounds; exactly
+    # 1024 chunks (one full round) and 1025 (a second round of one chunk
+    # holding one token)
+    (600000, 2, 1, 32, Q4, Q8), (524288, 2, 1, 32, Q4, Q8), (524289, 2, 1, 32, Q8, Q4)])
 def test_attn_decode_matches_oracle(bq, orc, dev, T, H, NKV, D, kt, vt):
     q, K, V = _attn_case(orc, T, H, NKV, D, kt, vt, seed=T + 31 * H + D)
     scale = 1.0 / math.sqrt(D)
